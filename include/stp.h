@@ -1,0 +1,233 @@
+/*
+ * stp.h -- C ABI of the prefix-tree packing + tree-attention library (libstp.so).
+ *
+ * The library packs tokenized sequences as one radix tree per training row
+ * (a host packer) and runs causal tree attention over the packed rows on a
+ * GB300 (sm_103a): tile classification, forward (O, LSE) and backward
+ * (dQ, dK, dV).  Sources, by page and section:
+ *
+ *   [P1] "Prefix tree packing" (furtherai.github.io/blog/posts/prefix-tree-packing):
+ *        tree-build section (the recursive walk, minimum shared-segment length,
+ *        trainable tokens never shared, the join-token copy); global-tree
+ *        section; bin-packing section (tree-aware best-fit-decreasing);
+ *        attention section (ancestor-only visibility, DFS enter/exit interval
+ *        check, empty blocks skipped); materialization section.
+ *   [P2] "How to Configure Sequence Packing ..." (AReaL how-to), "Monitoring
+ *        Packing Efficiency": the tree_token_ratio statistic.
+ *   [P3] "ART-Optimized Megatron" (CoreWeave), "How do we implement shared
+ *        prefix?": attention over the tree layout with a mask that lets tokens
+ *        see the shared prefix and isolates sibling branches.
+ *
+ * Conventions
+ *   - Every call returns an stp_status; no exception crosses the ABI.  On a
+ *     non-zero status a thread-local message is available from stp_last_error().
+ *   - Host buffers are caller-owned unless stated.  The opaque stp_plan is
+ *     owned by the library (free it with stp_plan_free); it is immutable after
+ *     stp_pack, so concurrent reads from several threads are safe.
+ *   - Device buffers and workspaces are caller-owned; the library never
+ *     allocates device memory.  Device calls are asynchronous on the given
+ *     stream (a cudaStream_t passed as void*; NULL = the legacy default
+ *     stream).  Their status covers host-side validation and launch errors;
+ *     device-side checks set an error word in the workspace that
+ *     stp_device_status() reads.
+ *   - Tensors are contiguous row-major: Q, O, dO, dQ [R, T, Hq, D];
+ *     K, V, dK, dV [R, T, Hkv, D]; LSE float32 [R, Hq, T] (natural log);
+ *     subtree_end int32 [R, T].
+ */
+#ifndef STP_H_
+#define STP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t stp_status;
+enum {
+  STP_OK = 0,
+  STP_EINVAL = 1,       /* bad argument: NULL pointer, size, alignment, shape     */
+  STP_ETOOLONG = 2,     /* a sequence is longer than a row                        */
+  STP_ENOMEM = 3,       /* host allocation failed                                 */
+  STP_ECUDA = 4,        /* a CUDA launch or stream error                          */
+  STP_EUNSUPPORTED = 5, /* dtype / head_dim / head ratio / row length not handled */
+  STP_EDEVICE = 6       /* a device-side check tripped (see stp_device_status)    */
+};
+
+/* ------------------------------------------------------------------------ */
+/* Host packer                                                              */
+/* ------------------------------------------------------------------------ */
+
+enum {
+  STP_GLOBAL = 0u,        /* one global tree over every sequence ([P1] global-tree section) */
+  STP_PER_FAMILY = 1u,    /* one tree per family, then the same placement (comparison arm)  */
+  STP_IN_ORDER = 2u       /* fill rows in input order, moving on when a leaf does not fit
+                             ([P1] "fill in the bins as you go"; comparison arm)             */
+};
+
+typedef struct stp_plan stp_plan;
+
+typedef struct {
+  int32_t n_rows;          /* R: rows (bins) in creation order                        */
+  int32_t row_len;         /* T                                                       */
+  int64_t input_tokens;    /* sum of sequence lengths                                 */
+  int64_t packed_tokens;   /* real (non-pad) tokens over all rows                     */
+  int64_t n_segments;      /* segments emitted by the walk, empty leaf segments too   */
+  int64_t n_leaves;        /* = number of sequences                                   */
+  int64_t useful_pairs;    /* visible (query, key) pairs over real tokens =
+                              sum over real tokens of (position id + 1)               */
+  double tree_token_ratio; /* input_tokens / packed_tokens ([P2] Monitoring)          */
+} stp_plan_info_t;
+
+/*
+ * stp_pack -- build the global prefix tree and place its leaves into rows.
+ *
+ * [P1] tree-build section: the longest run every active sequence agrees on is
+ * emitted once and the rest is split by next token.  A run shorter than
+ * `min_shared` is not shared (it is repeated inside each sub-branch); runs stop
+ * at trainable tokens; where a member's next token is trainable the shared run
+ * gives up its last token and every branch below carries its own copy of it.
+ * [P1] bin-packing section: leaves (one per sequence, cost = its length) are
+ * placed best-fit-decreasing on their insertion delta (path segments the row
+ * does not hold yet), families ordered by their largest leaf (stable), leaves
+ * of a family in input order, the earliest row on ties.
+ *
+ *   tokens     int32 [offsets[n_seqs]]  token ids, sequences back to back (host)
+ *   offsets    int64 [n_seqs + 1]       offsets[0] = 0, non-decreasing; every
+ *                                       sequence must be non-empty (host)
+ *   n_seqs     >= 0
+ *   trainable  uint8 [offsets[n_seqs]] or NULL (= no trainable token)
+ *   family     int32 [n_seqs] or NULL (= every sequence its own family)
+ *   row_len    T > 0
+ *   min_shared >= 1 (the pages' default is 64)
+ *   flags      STP_GLOBAL, STP_PER_FAMILY or STP_IN_ORDER (may be OR-ed)
+ *   out        receives the plan; *out is NULL on error
+ * Errors: STP_EINVAL (bad pointer/offsets/arguments), STP_ETOOLONG (a sequence
+ * longer than row_len), STP_ENOMEM.
+ */
+stp_status stp_pack(const int32_t* tokens, const int64_t* offsets, int32_t n_seqs,
+                    const uint8_t* trainable, const int32_t* family, int32_t row_len,
+                    int32_t min_shared, uint32_t flags, stp_plan** out);
+
+/* Statistics of a plan (host). */
+stp_status stp_plan_info(const stp_plan* plan, stp_plan_info_t* info);
+
+/*
+ * stp_plan_write -- materialize the plan into caller-owned host buffers
+ * ([P1] materialization section: one pass slices the tokens into rows).
+ * Rows hold the DFS pre-order of their segments, so a token's row index is its
+ * DFS enter index and subtree_end[x] is the row index of the last token of the
+ * subtree below x's segment (the exit index; [P1] attention section): key j is
+ * visible to query i iff j <= i && subtree_end[j] >= i.  Pads fill each row
+ * after its last real token with token 0, position 0, subtree_end = own index,
+ * loss 0.
+ *   token_ids, position_ids, subtree_end  int32 [R * T]
+ *   loss_mask     uint8 [R * T]: 1 where the next token of the sequence is trainable
+ *   gather_index  int64 [offsets[n_seqs]]: row-major flat index (r * T + x) of
+ *                 every input token, sequences in input order
+ * Any output pointer may be NULL (not written).
+ */
+stp_status stp_plan_write(const stp_plan* plan, int32_t* token_ids, int32_t* position_ids,
+                          int32_t* subtree_end, uint8_t* loss_mask, int64_t* gather_index);
+
+/* Row index (bin) of every sequence, int32 [n_seqs] (host). */
+stp_status stp_plan_rows_of(const stp_plan* plan, int32_t* row_of_seq);
+
+void stp_plan_free(stp_plan* plan);
+
+/* ------------------------------------------------------------------------ */
+/* Tree attention on the GPU                                                */
+/* ------------------------------------------------------------------------ */
+
+enum { STP_BF16 = 0, STP_FP32 = 1 };
+
+typedef struct {
+  int32_t n_rows;      /* R                                                        */
+  int32_t row_len;     /* T, a multiple of 128, at most 131072                     */
+  int32_t n_q_heads;   /* Hq                                                       */
+  int32_t n_kv_heads;  /* Hkv; Hq % Hkv == 0; query head h reads kv head h/(Hq/Hkv) */
+  int32_t head_dim;    /* D: 128 (bf16 or fp32) or 64 (fp32)                       */
+  int32_t dtype;       /* STP_BF16 or STP_FP32, for Q, K, V, O, dO, dQ, dK, dV     */
+  float scale;         /* softmax scale, usually 1/sqrt(D)                         */
+  int32_t block_m;     /* must be 128 (or 0 = 128)                                 */
+  int32_t block_n;     /* must be 128 (or 0 = 128)                                 */
+} stp_attn_desc;
+
+/*
+ * Byte sizes of the caller-owned device buffers for a descriptor:
+ *   tile_meta  -- tile classes and work lists written by stp_classify
+ *   fwd_ws     -- workspace of stp_attn_fwd (error word)
+ *   bwd_ws     -- workspace of stp_attn_bwd (error word, per-query
+ *                 Delta = dO . O, float32 dQ accumulator)
+ * Any pointer may be NULL.  Buffers must be 256-byte aligned.
+ */
+stp_status stp_workspace_size(const stp_attn_desc* desc, size_t* tile_meta_bytes,
+                              size_t* fwd_ws_bytes, size_t* bwd_ws_bytes);
+
+/*
+ * stp_classify -- mark every (query tile, key tile) pair of each row EMPTY (0),
+ * PARTIAL (1) or FULL (2) from subtree_end, and build the per-query-tile list
+ * of non-empty key tiles and the per-key-tile list of non-empty query tiles
+ * ([P1] attention section: most blocks of a packed row are empty and are
+ * skipped; the rest are fully visible ancestor blocks or partial blocks).
+ *   d_subtree_end  device int32 [R, T] as written by stp_plan_write
+ *   d_tile_meta    device, tile_meta_bytes
+ * Relies on subtree_end[j] >= j (true for any packed row).
+ */
+stp_status stp_classify(const stp_attn_desc* desc, const int32_t* d_subtree_end,
+                        void* d_tile_meta, void* stream);
+
+/* Copy the class matrix int8 [R, T/128, T/128] out of tile_meta (device to device). */
+stp_status stp_read_tile_classes(const stp_attn_desc* desc, const void* d_tile_meta,
+                                 int8_t* d_cls_out, void* stream);
+
+/*
+ * stp_attn_fwd -- tree attention forward ([P1] attention section; [P3]).
+ * For query i of head h (kv head g = h / (Hq/Hkv)) over the visible keys
+ * V(i) = { j : j <= i && subtree_end[j] >= i }:
+ *   s_ij = scale * q_i . k_j,  LSE_i = ln sum_j exp(s_ij),
+ *   O_i = sum_j exp(s_ij - LSE_i) v_j.
+ * Empty tiles are skipped; the predicate is evaluated on partial tiles only.
+ *   q, k, v   device, dtype of desc, layouts above, 16-byte aligned
+ *   o         device [R, T, Hq, D], same dtype;  lse device float32 [R, Hq, T]
+ *   d_ws      device, fwd_ws_bytes
+ * d_tile_meta must come from stp_classify on the same subtree_end.
+ */
+stp_status stp_attn_fwd(const stp_attn_desc* desc, const void* q, const void* k, const void* v,
+                        const int32_t* d_subtree_end, const void* d_tile_meta, void* o,
+                        float* lse, void* d_ws, void* stream);
+
+/*
+ * stp_attn_bwd -- analytic backward of the forward above for L = sum dO . O:
+ *   dP_ij = dO_i . v_j,  Delta_i = dO_i . O_i,  dS_ij = p_ij (dP_ij - Delta_i),
+ *   dQ_i = scale sum_j dS_ij k_j,
+ *   dK_j = scale sum_{i, h in group} dS_ij q_i,  dV_j = sum_{i, h in group} p_ij dO_i.
+ *   o, lse     the forward's outputs;  d_o device [R, T, Hq, D]
+ *   dq, dk, dv device outputs (overwritten), dtype of desc
+ *   d_ws       device, bwd_ws_bytes
+ */
+stp_status stp_attn_bwd(const stp_attn_desc* desc, const void* q, const void* k, const void* v,
+                        const void* o, const float* lse, const void* d_o,
+                        const int32_t* d_subtree_end, const void* d_tile_meta, void* dq,
+                        void* dk, void* dv, void* d_ws, void* stream);
+
+/*
+ * Read the device error word of a workspace (fwd_ws or bwd_ws): synchronizes
+ * the stream, then *out = STP_OK or STP_EDEVICE (a device check tripped or a
+ * bounded wait ran out; the kernel returned early and its outputs are invalid).
+ * The word is cleared by the next call that uses the workspace.
+ */
+stp_status stp_device_status(const void* d_ws, void* stream, stp_status* out);
+
+/* Thread-local text of the last error (empty string if none). */
+const char* stp_last_error(void);
+
+/* Library version string. */
+const char* stp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STP_H_ */

@@ -1,0 +1,17 @@
+// Internal helpers shared by the translation units of libstp.so.
+#pragma once
+
+#include <cstdarg>
+#include <cstdint>
+
+#include "../../include/stp.h"
+
+namespace stp {
+
+// Records a printf-style message as the thread's last error and returns `code`.
+stp_status fail(stp_status code, const char* fmt, ...);
+
+// Clears the thread's last error.
+void clear_error();
+
+}  // namespace stp

@@ -1,0 +1,36 @@
+// Arguments shared by the tree-attention launchers of libstp.so.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace stp {
+
+struct AttnArgs {
+  int R, T, Hq, Hkv, D;
+  float scale;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o_in;      // forward output (backward only)
+  const void* dout;      // dO (backward only)
+  void* o;               // forward output
+  float* lse;            // [R, Hq, T]
+  void* dq;
+  void* dk;
+  void* dv;
+  const int32_t* se;     // subtree_end [R, T]
+  const int32_t* csr_cnt;
+  const int32_t* csr;
+  const int32_t* csc_cnt;
+  const int32_t* csc;
+  float* delta;          // [R, Hq, T] (backward)
+  float* dq_acc;         // [R, T, Hq, D] float32 (backward, bf16 path)
+  uint32_t* err;         // device error word of the workspace
+};
+
+cudaError_t simt_fwd(const AttnArgs& a, bool bf16, cudaStream_t s);
+cudaError_t simt_bwd(const AttnArgs& a, bool bf16, cudaStream_t s);
+
+}  // namespace stp

@@ -1,0 +1,265 @@
+"""Python binding of libstp.so (include/stp.h): the same entry points, with
+argument marshalling only.  Every step of the path runs in the library: the
+host packer in C++, classification and attention in CUDA kernels.  There is
+no fallback: if the library is missing or a call fails, an exception says so.
+
+Device tensors are torch CUDA tensors (PyTorch only provides device memory and
+streams); host arrays are numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libstp.so")
+
+STP_OK, STP_EINVAL, STP_ETOOLONG, STP_ENOMEM, STP_ECUDA, STP_EUNSUPPORTED, STP_EDEVICE = range(7)
+STATUS_NAMES = {0: "STP_OK", 1: "STP_EINVAL", 2: "STP_ETOOLONG", 3: "STP_ENOMEM", 4: "STP_ECUDA",
+                5: "STP_EUNSUPPORTED", 6: "STP_EDEVICE"}
+STP_GLOBAL, STP_PER_FAMILY, STP_IN_ORDER = 0, 1, 2
+STP_BF16, STP_FP32 = 0, 1
+
+EXPORTED = ["stp_pack", "stp_plan_info", "stp_plan_write", "stp_plan_rows_of", "stp_plan_free",
+            "stp_workspace_size", "stp_classify", "stp_read_tile_classes", "stp_attn_fwd",
+            "stp_attn_bwd", "stp_device_status", "stp_last_error", "stp_version"]
+
+
+class StpError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int32), ("row_len", ctypes.c_int32),
+                ("input_tokens", ctypes.c_int64), ("packed_tokens", ctypes.c_int64),
+                ("n_segments", ctypes.c_int64), ("n_leaves", ctypes.c_int64),
+                ("useful_pairs", ctypes.c_int64), ("tree_token_ratio", ctypes.c_double)]
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int32), ("row_len", ctypes.c_int32),
+                ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("block_m", ctypes.c_int32), ("block_n", ctypes.c_int32)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_I64P = ctypes.POINTER(ctypes.c_int64)
+_U8P = ctypes.POINTER(ctypes.c_uint8)
+_SZ = ctypes.POINTER(ctypes.c_size_t)
+
+
+def lib():
+    """Loads libstp.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with sft_trie_build_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        st = ctypes.c_int32
+        L.stp_pack.argtypes = [_I32P, _I64P, ctypes.c_int32, _U8P, _I32P, ctypes.c_int32,
+                               ctypes.c_int32, ctypes.c_uint32, ctypes.POINTER(_P)]
+        L.stp_pack.restype = st
+        L.stp_plan_info.argtypes = [_P, ctypes.POINTER(PlanInfo)]
+        L.stp_plan_info.restype = st
+        L.stp_plan_write.argtypes = [_P, _I32P, _I32P, _I32P, _U8P, _I64P]
+        L.stp_plan_write.restype = st
+        L.stp_plan_rows_of.argtypes = [_P, _I32P]
+        L.stp_plan_rows_of.restype = st
+        L.stp_plan_free.argtypes = [_P]
+        L.stp_plan_free.restype = None
+        L.stp_workspace_size.argtypes = [ctypes.POINTER(AttnDesc), _SZ, _SZ, _SZ]
+        L.stp_workspace_size.restype = st
+        L.stp_classify.argtypes = [ctypes.POINTER(AttnDesc), _P, _P, _P]
+        L.stp_classify.restype = st
+        L.stp_read_tile_classes.argtypes = [ctypes.POINTER(AttnDesc), _P, _P, _P]
+        L.stp_read_tile_classes.restype = st
+        L.stp_attn_fwd.argtypes = [ctypes.POINTER(AttnDesc), _P, _P, _P, _P, _P, _P, _P, _P, _P]
+        L.stp_attn_fwd.restype = st
+        L.stp_attn_bwd.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 13
+        L.stp_attn_bwd.restype = st
+        L.stp_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
+        L.stp_device_status.restype = st
+        L.stp_last_error.argtypes = []
+        L.stp_last_error.restype = ctypes.c_char_p
+        L.stp_version.argtypes = []
+        L.stp_version.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(status, where):
+    if status != STP_OK:
+        raise StpError(status, where, lib().stp_last_error().decode())
+
+
+def _ptr(a, ctype):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _dptr(t):
+    """Device pointer of a torch tensor (or an int address)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return ctypes.c_void_p(t)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ---------------------------------------------------------------------------
+# Host packer
+# ---------------------------------------------------------------------------
+
+class Plan:
+    """Owns an stp_plan handle (freed with stp_plan_free)."""
+
+    def __init__(self, handle, n_seqs, n_tokens):
+        self.handle = handle
+        self.n_seqs = n_seqs
+        self.n_tokens = n_tokens
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h and _lib is not None:
+            _lib.stp_plan_free(h)
+            self.handle = None
+
+
+def stp_pack(tokens: np.ndarray, offsets: np.ndarray, trainable=None, family=None, *,
+             row_len: int, min_shared: int = 64, flags: int = STP_GLOBAL) -> Plan:
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    offsets = np.ascontiguousarray(offsets, dtype=np.int64)
+    n = len(offsets) - 1
+    tr = None if trainable is None else np.ascontiguousarray(trainable, dtype=np.uint8)
+    fam = None if family is None else np.ascontiguousarray(family, dtype=np.int32)
+    h = _P()
+    _check(lib().stp_pack(_ptr(tokens, ctypes.c_int32), _ptr(offsets, ctypes.c_int64), n,
+                          _ptr(tr, ctypes.c_uint8), _ptr(fam, ctypes.c_int32), int(row_len),
+                          int(min_shared), int(flags), ctypes.byref(h)), "stp_pack")
+    return Plan(h, n, int(offsets[-1]) if n > 0 else 0)
+
+
+def stp_plan_info(plan: Plan) -> dict:
+    info = PlanInfo()
+    _check(lib().stp_plan_info(plan.handle, ctypes.byref(info)), "stp_plan_info")
+    return {f: getattr(info, f) for f, _ in PlanInfo._fields_}
+
+
+def stp_plan_write(plan: Plan, out=None) -> dict:
+    """Materializes the plan into host arrays (allocated here when ``out`` is
+    None; pass a dict of preallocated, e.g. pinned, arrays to reuse them)."""
+    info = stp_plan_info(plan)
+    R, T = info["n_rows"], info["row_len"]
+    if out is None:
+        out = {"token_ids": np.empty((R, T), np.int32), "position_ids": np.empty((R, T), np.int32),
+               "subtree_end": np.empty((R, T), np.int32), "loss_mask": np.empty((R, T), np.uint8),
+               "gather_index": np.empty(plan.n_tokens, np.int64)}
+    _check(lib().stp_plan_write(plan.handle, _ptr(out.get("token_ids"), ctypes.c_int32),
+                                _ptr(out.get("position_ids"), ctypes.c_int32),
+                                _ptr(out.get("subtree_end"), ctypes.c_int32),
+                                _ptr(out.get("loss_mask"), ctypes.c_uint8),
+                                _ptr(out.get("gather_index"), ctypes.c_int64)), "stp_plan_write")
+    return out
+
+
+def stp_plan_rows_of(plan: Plan) -> np.ndarray:
+    out = np.empty(plan.n_seqs, np.int32)
+    _check(lib().stp_plan_rows_of(plan.handle, _ptr(out, ctypes.c_int32)), "stp_plan_rows_of")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Device calls
+# ---------------------------------------------------------------------------
+
+@dataclass
+class Desc:
+    n_rows: int
+    row_len: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    dtype: int = STP_BF16
+    scale: float = 0.0
+
+    def c(self) -> AttnDesc:
+        sc = self.scale if self.scale > 0 else self.head_dim ** -0.5
+        return AttnDesc(self.n_rows, self.row_len, self.n_q_heads, self.n_kv_heads, self.head_dim,
+                        self.dtype, sc, 128, 128)
+
+
+def stp_workspace_size(desc: Desc):
+    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    d = desc.c()
+    _check(lib().stp_workspace_size(ctypes.byref(d), ctypes.byref(a), ctypes.byref(b),
+                                    ctypes.byref(c)), "stp_workspace_size")
+    return a.value, b.value, c.value
+
+
+def stp_classify(desc: Desc, subtree_end, tile_meta, stream=None):
+    d = desc.c()
+    _check(lib().stp_classify(ctypes.byref(d), _dptr(subtree_end), _dptr(tile_meta), _stream(stream)),
+           "stp_classify")
+
+
+def stp_read_tile_classes(desc: Desc, tile_meta, cls_out, stream=None):
+    d = desc.c()
+    _check(lib().stp_read_tile_classes(ctypes.byref(d), _dptr(tile_meta), _dptr(cls_out),
+                                       _stream(stream)), "stp_read_tile_classes")
+
+
+def stp_attn_fwd(desc: Desc, q, k, v, subtree_end, tile_meta, o, lse, ws, stream=None):
+    d = desc.c()
+    _check(lib().stp_attn_fwd(ctypes.byref(d), _dptr(q), _dptr(k), _dptr(v), _dptr(subtree_end),
+                              _dptr(tile_meta), _dptr(o), _dptr(lse), _dptr(ws), _stream(stream)),
+           "stp_attn_fwd")
+
+
+def stp_attn_bwd(desc: Desc, q, k, v, o, lse, d_o, subtree_end, tile_meta, dq, dk, dv, ws,
+                 stream=None):
+    d = desc.c()
+    _check(lib().stp_attn_bwd(ctypes.byref(d), _dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse),
+                              _dptr(d_o), _dptr(subtree_end), _dptr(tile_meta), _dptr(dq),
+                              _dptr(dk), _dptr(dv), _dptr(ws), _stream(stream)), "stp_attn_bwd")
+
+
+def stp_device_status(ws, stream=None) -> int:
+    out = ctypes.c_int32()
+    _check(lib().stp_device_status(_dptr(ws), _stream(stream), ctypes.byref(out)),
+           "stp_device_status")
+    return out.value
+
+
+def stp_version() -> str:
+    return lib().stp_version().decode()
+
+
+# ---------------------------------------------------------------------------
+# Convenience: buffers for one descriptor
+# ---------------------------------------------------------------------------
+
+class Buffers:
+    """Caller-owned device buffers (torch) for one attention descriptor."""
+
+    def __init__(self, desc: Desc, device="cuda"):
+        import torch
+        meta, fwd, bwd = stp_workspace_size(desc)
+        self.tile_meta = torch.empty(max(meta, 256), dtype=torch.uint8, device=device)
+        self.fwd_ws = torch.empty(max(fwd, 256), dtype=torch.uint8, device=device)
+        self.bwd_ws = torch.empty(max(bwd, 256), dtype=torch.uint8, device=device)

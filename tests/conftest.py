@@ -33,3 +33,15 @@ def golden(name):
     import json
     with open(os.path.join(GOLDEN, name)) as f:
         return json.load(f)
+
+
+@pytest.fixture(scope="session")
+def stp_lib():
+    """libstp.so, built in-tree if it is missing or older than its sources."""
+    from sft_trie_build_gb300 import build, stp
+    srcs = [os.path.join(build.CSRC, f) for f in os.listdir(build.CSRC)]
+    srcs.append(os.path.join(ROOT, "include", "stp.h"))
+    if (not os.path.exists(build.LIB)
+            or os.path.getmtime(build.LIB) < max(os.path.getmtime(s) for s in srcs)):
+        build.build()
+    return stp.lib()
