@@ -1,9 +1,821 @@
-// bf16 tree attention launchers.
+// Tree attention on the tcgen05 tensor cores (bf16 in, f32 accumulate,
+// head_dim 128), driven by the tile lists of stp_classify.
+//
+// Forward ("Prefix tree packing", attention section; masked causal attention
+// with FlashAttention-style online softmax).  One CTA per (row, kv head,
+// query tile, pair of query heads of the kv head's group): both heads read
+// the same key/value tiles, so one TMA load of K and V feeds two query tiles.
+//   warp 8      TMA producer: Q tiles once, then K / V tiles of the query
+//               tile's list through a 2-stage ring;
+//   warp 9      MMA issuer: S_h = Q_h K^T (M=N=128, K=128) into TMEM, then
+//               O_h += P V (P from shared memory, V as an MN-major operand);
+//               owns the TMEM allocation (512 columns: S_0, S_1, O_0, O_1);
+//   warps 0-3   softmax for head slot 0, warps 4-7 for head slot 1: one thread
+//               per query row (= TMEM lane); the predicate
+//               j <= i && subtree_end[j] >= i is applied on PARTIAL tiles only;
+//               online softmax in base 2; O is rescaled in TMEM only when the
+//               running max grows by more than 2^8 (exact: numerator and
+//               denominator keep the same reference max).
+// The two softmax groups share one P buffer: head 0 writes P(e) after PV_1(e-1)
+// has read it, head 1 after PV_0(e); the MMA warp issues PV_0(e), S_0(e+1),
+// PV_1(e), S_1(e+1) so the tensor core works on one head while the other's
+// softmax runs.
+// Every mbarrier wait is bounded; a wait that runs out sets the workspace
+// error word, the CTA drains its outstanding copies and MMAs, frees TMEM and
+// returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "layout.h"
 #include "tc.h"
+#include "tc_ptx.cuh"
+
+namespace stp {
+namespace {
+
+using namespace tc;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+constexpr int kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile
+constexpr int kHalfTile = kTileBytes / 2;  // one 128-row x 64-column swizzled block
+constexpr int kSmallBytes = 256;           // barriers, TMEM slot, abort flag
+constexpr int kFwdBigBytes = 7 * kTileBytes;  // Q0 Q1 K0 K1 V0 V1 P
+constexpr int kSmemLimit = 232448;
+
+// ------------------------------------------------------------------------
+// Host: tensor maps
+// ------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [rows, H, 128] bf16 viewed as a 3-D tensor (d, head, row); boxes of
+// 64 d x 1 head x 128 rows land as 128 rows of 128 bytes, 128-byte swizzled.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------------
+// Device helpers
+// ------------------------------------------------------------------------
+
+// K-major operand of a 128-row x 128-column bf16 tile (two 64-column swizzled
+// halves): descriptor for the 16-column slice kk (0..7).
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+  return smem_desc_sw128(tile + (kk >> 2) * kHalfTile + (kk & 3) * 32, 16, 1024);
+}
+
+// MN-major operand: a [128 K-rows][128 N-columns] tile stored as two
+// 64-column halves; slice kk covers K-rows 16 kk .. 16 kk + 15.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
+  return smem_desc_sw128(tile + kk * 16 * 128, kHalfTile, 1024);
+}
+
+// Writes 8 consecutive bf16 values (columns 8c .. 8c+7 of row `row`) into a
+// K-major swizzled 128 x 128 tile.
+__device__ __forceinline__ void st_swizzled8(uint8_t* tile, int row, int c, uint4 v) {
+  uint8_t* half = tile + (c >> 3) * kHalfTile;
+  const int chunk = (c & 7) ^ (row & 7);
+  *reinterpret_cast<uint4*>(half + row * 128 + chunk * 16) = v;
+}
+
+struct FwdParams {
+  int R, T, Hq, Hkv, NT, G, npairs;
+  float scale_log2;
+  const int32_t* se;
+  const int32_t* csr_cnt;
+  const int32_t* csr;
+  __nv_bfloat16* o;
+  float* lse;
+  uint32_t* err;
+};
+
+enum {
+  B_Q = 0, B_KF = 1, B_VF = 3, B_KE = 5, B_VE = 7, B_SF = 9, B_PF = 11, B_OD = 13, B_DRAIN = 15,
+  B_COUNT = 16
+};
+
+__global__ void __launch_bounds__(320, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t raw = smem_u32(smem_raw) + kSmallBytes;
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t* big = smem_raw + kSmallBytes + pad;
+  const uint32_t big_s = raw + pad;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_qt = p.R * p.Hkv * p.npairs;
+  const int qt = p.NT - 1 - (int)(blockIdx.x / per_qt);
+  int rem = blockIdx.x % per_qt;
+  const int r = rem / (p.Hkv * p.npairs);
+  rem %= p.Hkv * p.npairs;
+  const int g = rem / p.npairs, pair = rem % p.npairs;
+  const int h0 = g * p.G + 2 * pair;
+  const int nh = min(2, p.G - 2 * pair);
+  const int cnt = p.csr_cnt[(size_t)r * p.NT + qt];
+  const int32_t* list = p.csr + ((size_t)r * p.NT + qt) * p.NT;
+  const int row0 = r * p.T;  // first row of this packed row in the [R*T] views
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[B_Q], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars[B_KF + s], 1);
+      mbar_init(&bars[B_VF + s], 1);
+      mbar_init(&bars[B_KE + s], 1);
+      mbar_init(&bars[B_VE + s], 1);
+      mbar_init(&bars[B_SF + s], 1);
+      mbar_init(&bars[B_PF + s], 128);
+      mbar_init(&bars[B_OD + s], 1);
+    }
+    mbar_init(&bars[B_DRAIN], 1);
+    *abort_flag = 0;
+    if (pad + kSmallBytes + kFwdBigBytes > kSmemLimit || cnt <= 0 || cnt > p.NT) {
+      *abort_flag = 1;
+      atomicOr(p.err, cnt <= 0 || cnt > p.NT ? kErrBadList : kErrTmem);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const bool run = !*abort_flag;
+
+  uint32_t q_s[2] = {big_s, big_s + kTileBytes};
+  uint32_t k_s[2] = {big_s + 2 * kTileBytes, big_s + 3 * kTileBytes};
+  uint32_t v_s[2] = {big_s + 4 * kTileBytes, big_s + 5 * kTileBytes};
+  const uint32_t p_s = big_s + 6 * kTileBytes;
+  uint8_t* p_tile = big + 6 * kTileBytes;
+
+  int issued_k[2] = {-1, -1};  // producer: last issued use of each stage
+  int issued_v[2] = {-1, -1};
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && run) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      mbar_expect_tx(&bars[B_Q], nh * kTileBytes);
+      for (int hs = 0; hs < nh; ++hs)
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(big + hs * kTileBytes + hf * kHalfTile, &tq, &bars[B_Q], hf * 64, h0 + hs,
+                      row0 + qt * 128);
+      for (int e = 0; e < cnt; ++e) {
+        const int st = e & 1, n = e >> 1;
+        const int kt = list[e] >> 1;
+        if (kt < 0 || kt > qt) {
+          *abort_flag = 1;
+          atomicOr(p.err, kErrBadList);
+          break;
+        }
+        if (e >= 2 && !mbar_wait(&bars[B_KE + st], (n - 1) & 1, abort_flag, p.err)) break;
+        mbar_expect_tx(&bars[B_KF + st], kTileBytes);
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(big + (2 + st) * kTileBytes + hf * kHalfTile, &tk, &bars[B_KF + st],
+                      hf * 64, g, row0 + kt * 128);
+        issued_k[st] = n;
+        if (e >= 2 && !mbar_wait(&bars[B_VE + st], (n - 1) & 1, abort_flag, p.err)) break;
+        mbar_expect_tx(&bars[B_VF + st], kTileBytes);
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(big + (4 + st) * kTileBytes + hf * kHalfTile, &tv, &bars[B_VF + st],
+                      hf * 64, g, row0 + kt * 128);
+        issued_v[st] = n;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && run) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
+      constexpr uint32_t idesc_o = idesc_bf16(128, 128, 0, 1);
+      bool ok = mbar_wait(&bars[B_Q], 0, abort_flag, p.err) &&
+                mbar_wait(&bars[B_KF], 0, abort_flag, p.err);
+      if (ok) {
+        fence_after_sync();
+        for (int hs = 0; hs < nh; ++hs) {
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + hs * 128, kmajor_desc(q_s[hs], kk), kmajor_desc(k_s[0], kk), idesc_s,
+                   kk > 0);
+          mma_commit(&bars[B_SF + hs]);
+        }
+        mma_commit(&bars[B_KE]);
+      }
+      for (int e = 0; ok && e < cnt; ++e) {
+        const int st = e & 1, n = e >> 1;
+        const int st1 = (e + 1) & 1, n1 = (e + 1) >> 1;
+        if (!mbar_wait(&bars[B_VF + st], n & 1, abort_flag, p.err)) break;
+        for (int hs = 0; hs < nh && ok; ++hs) {
+          if (!mbar_wait(&bars[B_PF + hs], e & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          fence_after_sync();
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + 256 + hs * 128, kmajor_desc(p_s, kk), mnmajor_desc(v_s[st], kk), idesc_o,
+                   (e > 0 || kk > 0));
+          mma_commit(&bars[B_OD + hs]);
+          if (e + 1 < cnt) {
+            if (hs == 0 && !mbar_wait(&bars[B_KF + st1], n1 & 1, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            fence_after_sync();
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem + hs * 128, kmajor_desc(q_s[hs], kk), kmajor_desc(k_s[st1], kk),
+                     idesc_s, kk > 0);
+            mma_commit(&bars[B_SF + hs]);
+            if (hs == nh - 1) mma_commit(&bars[B_KE + st1]);
+          }
+        }
+        if (ok) mma_commit(&bars[B_VE + st]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int hs = warp >> 2;
+    const int row = threadIdx.x & 127;
+    const int i = qt * 128 + row;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + hs * 128;
+    const uint32_t o_addr = tmem + lane_base + 256 + hs * 128;
+    const int32_t* se_row = p.se + (size_t)row0;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = run && hs < nh;
+    for (int e = 0; ok && e < cnt; ++e) {
+      const int ent = list[e], kt = ent >> 1, part = ent & 1, k0 = kt * 128;
+      if (!mbar_wait(&bars[B_SF + hs], e & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      // pass 1: row max of the (masked) scores, in log2 units
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(s_addr + c * 32, u);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          float x = __uint_as_float(u[k]) * p.scale_log2;
+          if (part) {
+            const int j = k0 + c * 32 + k;
+            x = ((j <= i) && (__ldg(se_row + j) >= i)) ? x : -INFINITY;
+          }
+          mx = fmaxf(mx, x);
+        }
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const float m_use = (m_new > m_run + kRescaleThreshold) ? m_new : m_run;
+      const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
+      const float alpha = exp2f(m_run - m_sub);
+      // pass 2: probabilities, kept packed as bf16 pairs until P is free
+      float rs = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(s_addr + c * 32, u);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          float x0 = __uint_as_float(u[k]) * p.scale_log2;
+          float x1 = __uint_as_float(u[k + 1]) * p.scale_log2;
+          if (part) {
+            const int j = k0 + c * 32 + k;
+            x0 = ((j <= i) && (__ldg(se_row + j) >= i)) ? x0 : -INFINITY;
+            x1 = ((j + 1 <= i) && (__ldg(se_row + j + 1) >= i)) ? x1 : -INFINITY;
+          }
+          const float p0 = exp2f(x0 - m_sub), p1 = exp2f(x1 - m_sub);
+          rs += p0 + p1;
+          pk[c * 16 + (k >> 1)] = pack_bf16x2(p0, p1);
+        }
+      }
+      // the P buffer is free and O_hs stable once the previous reader of P is done
+      if (nh == 2) {
+        if (hs == 0) {
+          if (e > 0 && !mbar_wait(&bars[B_OD + 1], (e - 1) & 1, abort_flag, p.err)) ok = false;
+        } else {
+          if (!mbar_wait(&bars[B_OD + 0], e & 1, abort_flag, p.err)) ok = false;
+        }
+      } else if (e > 0 && !mbar_wait(&bars[B_OD + 0], (e - 1) & 1, abort_flag, p.err)) {
+        ok = false;
+      }
+      if (!ok) break;
+      fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        st_swizzled8(p_tile, row, c, make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+      fence_proxy_async_smem();
+      if (e > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        uint32_t u[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(o_addr + c * 32, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) u[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
+          tmem_st32(o_addr + c * 32, u);
+        }
+        tmem_st_wait();
+      }
+      l_run = l_run * alpha + rs;
+      m_run = m_use;
+      fence_before_sync();
+      mbar_arrive(&bars[B_PF + hs]);
+    }
+    if (ok && mbar_wait(&bars[B_OD + hs], (cnt - 1) & 1, abort_flag, p.err)) {
+      fence_after_sync();
+      const int h = h0 + hs;
+      __nv_bfloat16* orow = p.o + (((size_t)row0 + i) * p.Hq + h) * 128;
+      const float inv = 1.f / l_run;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(o_addr + c * 32, u);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(u[8 * k + 0]) * inv, __uint_as_float(u[8 * k + 1]) * inv);
+          v.y = pack_bf16x2(__uint_as_float(u[8 * k + 2]) * inv, __uint_as_float(u[8 * k + 3]) * inv);
+          v.z = pack_bf16x2(__uint_as_float(u[8 * k + 4]) * inv, __uint_as_float(u[8 * k + 5]) * inv);
+          v.w = pack_bf16x2(__uint_as_float(u[8 * k + 6]) * inv, __uint_as_float(u[8 * k + 7]) * inv);
+          *reinterpret_cast<uint4*>(orow + c * 32 + 8 * k) = v;
+        }
+      }
+      p.lse[((size_t)r * p.Hq + h) * p.T + i] = (m_run + log2f(l_run)) * kLn2;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  if (warp == 8 && lane == 0 && run) {
+    mbar_wait_drain(&bars[B_Q], 0);
+    for (int st = 0; st < 2; ++st) {
+      if (issued_k[st] >= 0) mbar_wait_drain(&bars[B_KF + st], issued_k[st] & 1);
+      if (issued_v[st] >= 0) mbar_wait_drain(&bars[B_VF + st], issued_v[st] & 1);
+    }
+  }
+  if (warp == 9 && lane == 0 && run) {
+    mma_commit(&bars[B_DRAIN]);
+    mbar_wait_drain(&bars[B_DRAIN], 0);
+  }
+  __syncwarp();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
+
+// ------------------------------------------------------------------------
+// Backward
+// ------------------------------------------------------------------------
+//
+// Per CTA: (row r, kv head g, key tile kt).  The key tile's list of
+// non-empty query tiles, times the G query heads of the group, gives the
+// iterations j = (query tile, head).  Per iteration:
+//   MMA      S^T = K Q^T and dP^T = V dO^T (keys on TMEM lanes), then, once
+//            P^T and dS^T are in shared memory, dV += P^T dO, dK += dS^T Q
+//            (accumulated in TMEM over all iterations) and dQ_j = dS K into
+//            the S^T columns;
+//   warps 0-3  one thread per key j: p = exp2(s * scale log2e - LSE_i log2e)
+//            (masked on PARTIAL tiles with the thread's own subtree_end[j]),
+//            dS = p (dP - Delta_i); writes P^T and dS^T as bf16;
+//   warps 4-7  one thread per query: reads dQ_j from TMEM and adds it into the
+//            float32 accumulator with vector atomics;
+//   warp 8   TMA: K, V once; Q and dO of each iteration;
+//   warp 9   MMA issue, TMEM owner.
+// dK (times scale) and dV leave TMEM once at the end.
+
+struct BwdParams {
+  int R, T, Hq, Hkv, NT, G;
+  float scale_log2;
+  const int32_t* se;
+  const int32_t* csc_cnt;
+  const int32_t* csc;
+  const float* lse;
+  const float* delta;
+  float* dq_acc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float scale;
+  uint32_t* err;
+};
+
+enum {
+  C_KV = 0, C_QF = 1, C_QE = 2, C_SF = 3, C_DR = 4, C_QD = 5, C_SFREE = 6, C_PSF = 7,
+  C_DONE = 8, C_DRAIN = 9, C_COUNT = 10
+};
+constexpr int kBwdBigBytes = 6 * kTileBytes;  // K V Q dO P^T dS^T
+constexpr int kBwdVecBytes = 2 * 128 * 4;  // LSE and Delta of the current query tile
+
+__global__ void __launch_bounds__(320, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* vec = reinterpret_cast<float*>(smem_raw + kSmallBytes);  // [LSE 128 | Delta 128]
+  const uint32_t raw = smem_u32(smem_raw) + kSmallBytes + kBwdVecBytes;
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t* big = smem_raw + kSmallBytes + kBwdVecBytes + pad;
+  const uint32_t big_s = raw + pad;
+  const uint32_t k_s = big_s, v_s = big_s + kTileBytes, q_s = big_s + 2 * kTileBytes,
+                 do_s = big_s + 3 * kTileBytes, pt_s = big_s + 4 * kTileBytes,
+                 dst_s = big_s + 5 * kTileBytes;
+  uint8_t* pt_tile = big + 4 * kTileBytes;
+  uint8_t* dst_tile = big + 5 * kTileBytes;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_kt = p.R * p.Hkv;
+  const int kt = (int)(blockIdx.x / per_kt);
+  const int r = (blockIdx.x % per_kt) / p.Hkv;
+  const int g = blockIdx.x % p.Hkv;
+  const int cnt = p.csc_cnt[(size_t)r * p.NT + kt];
+  const int32_t* list = p.csc + ((size_t)r * p.NT + kt) * p.NT;
+  const int n_it = cnt * p.G;
+  const int row0 = r * p.T;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < C_COUNT; ++b) mbar_init(&bars[b], (b == C_DR || b == C_SFREE) ? 128 : 1);
+    *abort_flag = 0;
+    if (pad + kSmallBytes + kBwdVecBytes + kBwdBigBytes > kSmemLimit || cnt <= 0 || cnt > p.NT) {
+      *abort_flag = 1;
+      atomicOr(p.err, cnt <= 0 || cnt > p.NT ? kErrBadList : kErrTmem);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const bool run = !*abort_flag;
+  // TMEM columns: S^T / dQ 0..127, dP^T 128..255, dV 256..383, dK 384..511
+  int issued_kv = -1, issued_q = -1;
+
+  if (warp == 8) {
+    if (lane == 0 && run) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&tdo);
+      mbar_expect_tx(&bars[C_KV], 2 * kTileBytes);
+      for (int hf = 0; hf < 2; ++hf) {
+        tma_load_3d(big + hf * kHalfTile, &tk, &bars[C_KV], hf * 64, g, row0 + kt * 128);
+        tma_load_3d(big + kTileBytes + hf * kHalfTile, &tv, &bars[C_KV], hf * 64, g, row0 + kt * 128);
+      }
+      issued_kv = 0;
+      for (int j = 0; j < n_it; ++j) {
+        const int qt = list[j / p.G] >> 1, h = g * p.G + j % p.G;
+        if (qt < kt || qt >= p.NT) {
+          *abort_flag = 1;
+          atomicOr(p.err, kErrBadList);
+          break;
+        }
+        if (j > 0 && !mbar_wait(&bars[C_QE], (j - 1) & 1, abort_flag, p.err)) break;
+        mbar_expect_tx(&bars[C_QF], 2 * kTileBytes + 2 * 128 * 4);
+        bulk_load(vec, p.lse + ((size_t)r * p.Hq + h) * p.T + qt * 128, 512, &bars[C_QF]);
+        bulk_load(vec + 128, p.delta + ((size_t)r * p.Hq + h) * p.T + qt * 128, 512, &bars[C_QF]);
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_load_3d(big + 2 * kTileBytes + hf * kHalfTile, &tq, &bars[C_QF], hf * 64, h, row0 + qt * 128);
+          tma_load_3d(big + 3 * kTileBytes + hf * kHalfTile, &tdo, &bars[C_QF], hf * 64, h, row0 + qt * 128);
+        }
+        issued_q = j;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    if (lane == 0 && run) {
+      constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
+      constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // dV, dK
+      constexpr uint32_t id_nn = idesc_bf16(128, 128, 1, 1);  // dQ
+      bool ok = mbar_wait(&bars[C_KV], 0, abort_flag, p.err);
+      for (int j = 0; ok && j < n_it; ++j) {
+        if (!mbar_wait(&bars[C_QF], j & 1, abort_flag, p.err)) break;
+        if (j > 0 && !mbar_wait(&bars[C_SFREE], (j - 1) & 1, abort_flag, p.err)) break;
+        fence_after_sync();
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem, kmajor_desc(k_s, kk), kmajor_desc(q_s, kk), id_kk, kk > 0);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 128, kmajor_desc(v_s, kk), kmajor_desc(do_s, kk), id_kk, kk > 0);
+        mma_commit(&bars[C_SF]);
+        if (!mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err)) break;
+        fence_after_sync();
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 256, kmajor_desc(pt_s, kk), mnmajor_desc(do_s, kk), id_kn, (j > 0 || kk > 0));
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + 384, kmajor_desc(dst_s, kk), mnmajor_desc(q_s, kk), id_kn, (j > 0 || kk > 0));
+        mma_commit(&bars[C_QE]);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem, mnmajor_desc(dst_s, kk), mnmajor_desc(k_s, kk), id_nn, kk > 0);
+        mma_commit(&bars[C_QD]);
+        mma_commit(&bars[C_PSF]);
+      }
+      if (ok) mma_commit(&bars[C_DONE]);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------ per-key elementwise
+    const int t = threadIdx.x;          // key row = TMEM lane
+    const int jk = kt * 128 + t;        // key index in the row
+    const int se_j = p.se[(size_t)row0 + jk];
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    bool ok = run;
+    for (int j = 0; ok && j < n_it; ++j) {
+      const int ent = list[j / p.G], qt = ent >> 1, part = ent & 1;
+      const int h = g * p.G + j % p.G;
+      const int q0 = qt * 128;
+      (void)h;
+      const float* lse_s = vec;
+      const float* dlt_s = vec + 128;
+      // LSE / Delta of this query tile arrive with its Q / dO tiles
+      if (!mbar_wait(&bars[C_QF], j & 1, abort_flag, p.err) ||
+          !mbar_wait(&bars[C_SF], j & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      uint32_t pp[64], dd[64];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t us[32], ud[32];
+        tmem_ld32(tmem + lane_base + c * 32, us);
+        tmem_ld32(tmem + lane_base + 128 + c * 32, ud);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          float pr[2], ds[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = c * 32 + k + u;
+            const int i = q0 + col;
+            const bool vis = !part || (jk <= i && se_j >= i);
+            const float pv = vis ? exp2f(__uint_as_float(us[k + u]) * p.scale_log2 - lse_s[col] * kLog2e) : 0.f;
+            pr[u] = pv;
+            ds[u] = pv * (__uint_as_float(ud[k + u]) - dlt_s[col]);
+          }
+          pp[c * 16 + (k >> 1)] = pack_bf16x2(pr[0], pr[1]);
+          dd[c * 16 + (k >> 1)] = pack_bf16x2(ds[0], ds[1]);
+        }
+      }
+      if (j > 0 && !mbar_wait(&bars[C_PSF], (j - 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        st_swizzled8(pt_tile, t, c, make_uint4(pp[4 * c], pp[4 * c + 1], pp[4 * c + 2], pp[4 * c + 3]));
+        st_swizzled8(dst_tile, t, c, make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]));
+      }
+      fence_proxy_async_smem();
+      fence_before_sync();
+      mbar_arrive(&bars[C_DR]);
+    }
+    if (ok && mbar_wait(&bars[C_DONE], 0, abort_flag, p.err)) {
+      fence_after_sync();
+      __nv_bfloat16* dvr = p.dv + (((size_t)row0 + jk) * p.Hkv + g) * 128;
+      __nv_bfloat16* dkr = p.dk + (((size_t)row0 + jk) * p.Hkv + g) * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t uv[32], uk[32];
+        tmem_ld32(tmem + lane_base + 256 + c * 32, uv);
+        tmem_ld32(tmem + lane_base + 384 + c * 32, uk);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 a, b;
+          a.x = pack_bf16x2(__uint_as_float(uv[8 * k + 0]), __uint_as_float(uv[8 * k + 1]));
+          a.y = pack_bf16x2(__uint_as_float(uv[8 * k + 2]), __uint_as_float(uv[8 * k + 3]));
+          a.z = pack_bf16x2(__uint_as_float(uv[8 * k + 4]), __uint_as_float(uv[8 * k + 5]));
+          a.w = pack_bf16x2(__uint_as_float(uv[8 * k + 6]), __uint_as_float(uv[8 * k + 7]));
+          b.x = pack_bf16x2(__uint_as_float(uk[8 * k + 0]) * p.scale, __uint_as_float(uk[8 * k + 1]) * p.scale);
+          b.y = pack_bf16x2(__uint_as_float(uk[8 * k + 2]) * p.scale, __uint_as_float(uk[8 * k + 3]) * p.scale);
+          b.z = pack_bf16x2(__uint_as_float(uk[8 * k + 4]) * p.scale, __uint_as_float(uk[8 * k + 5]) * p.scale);
+          b.w = pack_bf16x2(__uint_as_float(uk[8 * k + 6]) * p.scale, __uint_as_float(uk[8 * k + 7]) * p.scale);
+          *reinterpret_cast<uint4*>(dvr + c * 32 + 8 * k) = a;
+          *reinterpret_cast<uint4*>(dkr + c * 32 + 8 * k) = b;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------ dQ drain (per query)
+    const int t = threadIdx.x - 128;    // query row = TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = run;
+    for (int j = 0; ok && j < n_it; ++j) {
+      const int qt = list[j / p.G] >> 1;
+      const int h = g * p.G + j % p.G;
+      if (!mbar_wait(&bars[C_QD], j & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      float4* dst = reinterpret_cast<float4*>(p.dq_acc + (((size_t)row0 + qt * 128 + t) * p.Hq + h) * 128);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_base + c * 32, u);
+        tmem_ld_wait();
+        if (c == 3) {
+          fence_before_sync();
+          mbar_arrive(&bars[C_SFREE]);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          atomicAdd(dst + c * 8 + k, make_float4(__uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1]),
+                                                 __uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3])));
+      }
+    }
+  }
+
+  if (warp == 8 && lane == 0 && run) {
+    if (issued_kv >= 0) mbar_wait_drain(&bars[C_KV], 0);
+    if (issued_q >= 0) mbar_wait_drain(&bars[C_QF], issued_q & 1);
+  }
+  if (warp == 9 && lane == 0 && run) {
+    mma_commit(&bars[C_DRAIN]);
+    mbar_wait_drain(&bars[C_DRAIN], 0);
+  }
+  __syncwarp();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
+// Delta[r,h,i] = sum_d dO . O (bf16 in, f32 out); one warp per (row, token, head).
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        float* __restrict__ delta, int R, int T,
+                                                        int Hq) {
+  const int lane = threadIdx.x & 31;
+  const size_t rows = (size_t)R * T * Hq;
+  for (size_t w = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < rows; w += (size_t)gridDim.x * 8) {
+    const uint2 a = reinterpret_cast<const uint2*>(o + w * 128)[lane];
+    const uint2 b = reinterpret_cast<const uint2*>(dout + w * 128)[lane];
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float2 x = __bfloat1622float2(a2[k]), y = __bfloat1622float2(b2[k]);
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (lane == 0) {
+      const int h = (int)(w % Hq);
+      const size_t ri = w / Hq;
+      const size_t rr = ri / T, i = ri - rr * T;
+      delta[(rr * Hq + h) * T + i] = acc;
+    }
+  }
+}
+
+// dQ = bf16(scale * dQ_acc), 8 elements per thread.
+__global__ void __launch_bounds__(256) bwd_dq_finalize_kernel(const float* __restrict__ acc,
+                                                              __nv_bfloat16* __restrict__ dq,
+                                                              size_t n8, float scale) {
+  for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n8; k += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * k];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * k + 1];
+    uint4 v;
+    v.x = pack_bf16x2(a.x * scale, a.y * scale);
+    v.y = pack_bf16x2(a.z * scale, a.w * scale);
+    v.z = pack_bf16x2(b.x * scale, b.y * scale);
+    v.w = pack_bf16x2(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4*>(dq)[k] = v;
+  }
+}
+
+}  // namespace
+
+cudaError_t tc_fwd(const AttnArgs& a, cudaStream_t s) {
+  CUtensorMap mq, mk, mv;
+  const int64_t rows = (int64_t)a.R * a.T;
+  if (!make_map(&mq, a.q, rows, a.Hq) || !make_map(&mk, a.k, rows, a.Hkv) ||
+      !make_map(&mv, a.v, rows, a.Hkv))
+    return cudaErrorInvalidValue;
+  FwdParams p;
+  p.R = a.R;
+  p.T = a.T;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.NT = a.T / 128;
+  p.G = a.Hq / a.Hkv;
+  p.npairs = (p.G + 1) / 2;
+  p.scale_log2 = a.scale * kLog2e;
+  p.se = a.se;
+  p.csr_cnt = a.csr_cnt;
+  p.csr = a.csr;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.err = a.err;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemLimit);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const unsigned grid = (unsigned)(p.NT * p.R * p.Hkv * p.npairs);
+  fwd_tc_kernel<<<grid, 320, kSmemLimit, s>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+
+}  // namespace stp
 
 namespace stp {
 
-cudaError_t tc_fwd(const AttnArgs& a, cudaStream_t s) { return simt_fwd(a, true, s); }
-cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) { return simt_bwd(a, true, s); }
+cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
+  CUtensorMap mq, mk, mv, mdo;
+  const int64_t rows = (int64_t)a.R * a.T;
+  if (!make_map(&mq, a.q, rows, a.Hq) || !make_map(&mk, a.k, rows, a.Hkv) ||
+      !make_map(&mv, a.v, rows, a.Hkv) || !make_map(&mdo, a.dout, rows, a.Hq))
+    return cudaErrorInvalidValue;
+  const size_t n = (size_t)a.R * a.T * a.Hq * 128;
+  cudaError_t e = cudaMemsetAsync(a.dq_acc, 0, n * sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  bwd_delta_kernel<<<2048, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.o_in),
+                                        static_cast<const __nv_bfloat16*>(a.dout), a.delta, a.R, a.T,
+                                        a.Hq);
+  BwdParams p;
+  p.R = a.R;
+  p.T = a.T;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.NT = a.T / 128;
+  p.G = a.Hq / a.Hkv;
+  p.scale_log2 = a.scale * kLog2e;
+  p.scale = a.scale;
+  p.se = a.se;
+  p.csc_cnt = a.csc_cnt;
+  p.csc = a.csc;
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.dq_acc = a.dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.err = a.err;
+  static bool attr = false;
+  if (!attr) {
+    e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  bwd_tc_kernel<<<(unsigned)(p.NT * p.R * p.Hkv), 320, kSmemLimit, s>>>(mq, mk, mv, mdo, p);
+  bwd_dq_finalize_kernel<<<2048, 256, 0, s>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n / 8,
+                                              a.scale);
+  return cudaGetLastError();
+}
 
 }  // namespace stp
