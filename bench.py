@@ -1,0 +1,355 @@
+"""Benchmark of the prefix-tree tree-attention path on GB300.
+
+One step = the whole path over one batch: host packing (trie walk, tree-aware
+best-fit-decreasing, materialization) -> copy of the row metadata to the GPU
+-> tile classification -> forward (O, LSE) -> backward (dQ, dK, dV).
+Q, K, V and dO are resident in HBM when the timed region starts; L2 is
+flushed (a 512 MiB write, untimed) before every timed step.
+
+Metric: useful tree-attention fwd+bwd TFLOP/s, where useful work counts each
+visible (query, key) pair once per query head: 4 * D flops forward and
+10 * D backward (the FlashAttention convention, recomputation of S included);
+masked or skipped work is not counted.  Trajectories/s = sequences per step
+/ step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun: every rank packs and processes its own batch
+(weak scaling, no collective on the data path); the step time is the maximum
+over ranks.  --impl reference times the CPU oracle (float64 NumPy) on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sft_trie_build_gb300 import workloads as W  # noqa: E402
+
+WORKLOAD = "grpo"
+WORKLOAD_DESC = ("one GRPO group: 5000-token non-trainable system prefix + 16 trainable rollouts "
+                 "U[100,1000], packed into one 16384-token row; bf16 attention, 32 query heads, "
+                 "8 kv heads, head_dim 128, scale 1/sqrt(128)")
+METRIC = "tree-attn fwd+bwd useful TFLOP/s (% of BF16 peak) and trajectories/s on 1 GB300"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["bf16_tflops"]), float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 6800.0, "fallback"
+
+
+def _batch(seed_offset=0):
+    return W.grpo(W.CONFIG_SEEDS[WORKLOAD] + seed_offset)
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sms, mx, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sms.append(float(f[0]))
+                mx = float(f[1])
+                power.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms),
+                "power_w_max": max(power) if power else None}
+
+
+def _gpu_id(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+def oracle_sample(plan_o, q, k, v, do, scale, heads=1):
+    """Float64 oracle fwd+bwd on the first `heads` query heads (and the kv
+    heads they read); returns (seconds, useful flops of the sample)."""
+    from oracle import attn as OA
+    G = q.shape[2] // k.shape[2]
+    nkv = -(-heads // G)
+    qs, ks, vs, dos = q[:, :, :heads], k[:, :, :nkv], v[:, :, :nkv], do[:, :, :heads]
+    pairs = OA.useful_pairs(plan_o)
+    t0 = time.perf_counter()
+    OA.attn_bwd(plan_o, qs, ks, vs, dos, scale)
+    dt = time.perf_counter() - t0
+    return dt, 14.0 * q.shape[-1] * heads * pairs
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle timed on this host's cores, a bounded sample per step."""
+    if rank != 0:
+        return
+    from oracle import pack as OP
+    b = _batch()
+    plan_o = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared, b.family)
+    shape = W.attn_shape(WORKLOAD, plan_o.n_rows, b.row_len)
+    q, k, v, do = W.attn_tensors(shape, 0)
+    heads = 1
+    for _ in range(args.warmup):
+        oracle_sample(plan_o, q, k, v, do, shape.scale, heads)
+    times = []
+    flops = 0.0
+    for _ in range(args.steps):
+        dt, flops = oracle_sample(plan_o, q, k, v, do, shape.scale, heads)
+        times.append(dt)
+    tot = sum(times)
+    val = flops * args.steps / tot / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"float64 NumPy oracle, fwd+bwd of {heads} of {shape.n_q_heads} query heads "
+              f"(its kv head) over the whole packed row, per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD_DESC, "sample_heads": heads},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "trajectories_per_s": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    from sft_trie_build_gb300 import stp
+
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    b = _batch(seed_offset=1000 * rank)
+    tokens, offsets, train = b.flat()
+    plan0 = stp.stp_pack(tokens, offsets, train, b.family, row_len=b.row_len, min_shared=b.min_shared)
+    info = stp.stp_plan_info(plan0)
+    R, T = info["n_rows"], info["row_len"]
+    shape = W.attn_shape(WORKLOAD, R, T)
+    Hq, Hkv, D = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+    q_h, k_h, v_h, do_h = W.attn_tensors(shape, 17 + rank)
+    pin = lambda t: t.contiguous().pin_memory()  # noqa: E731
+    q_h, k_h, v_h, do_h = (pin(x) for x in (q_h, k_h, v_h, do_h))
+    q, k, v, do = (x.to(dev) for x in (q_h, k_h, v_h, do_h))
+    desc = stp.Desc(R, T, Hq, Hkv, D, stp.STP_BF16, shape.scale)
+    buf = stp.Buffers(desc, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(R, Hq, T, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    meta_h = {n: torch.empty(R, T, dtype=torch.int32).pin_memory() for n in
+              ("token_ids", "position_ids", "subtree_end")}
+    meta_np = {n: t.numpy() for n, t in meta_h.items()}
+    meta_np["loss_mask"] = torch.empty(R, T, dtype=torch.uint8).pin_memory().numpy()
+    meta_np["gather_index"] = np.empty(int(offsets[-1]), np.int64)
+    meta_d = {n: torch.empty(R, T, dtype=torch.int32, device=dev) for n in meta_h}
+    se = meta_d["subtree_end"]
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    useful = float(info["useful_pairs"])
+    fwd_flops = 4.0 * D * Hq * useful
+    bwd_flops = 10.0 * D * Hq * useful
+    step_flops = fwd_flops + bwd_flops
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def pack_and_upload():
+        plan = stp.stp_pack(tokens, offsets, train, b.family, row_len=b.row_len,
+                            min_shared=b.min_shared)
+        stp.stp_plan_write(plan, meta_np)
+        for n in meta_h:
+            meta_d[n].copy_(meta_h[n], non_blocking=True)
+        return plan
+
+    def attention(marks=None):
+        stp.stp_classify(desc, se, buf.tile_meta)
+        if marks:
+            marks[0].record()
+        stp.stp_attn_fwd(desc, q, k, v, se, buf.tile_meta, o, lse, buf.fwd_ws)
+        if marks:
+            marks[1].record()
+        stp.stp_attn_bwd(desc, q, k, v, o, lse, do, se, buf.tile_meta, dq, dk, dv, buf.bwd_ws)
+        if marks:
+            marks[2].record()
+
+    # ---- device leg: inputs resident in HBM
+    for _ in range(args.warmup):
+        pack_and_upload()
+        attention()
+    torch.cuda.synchronize()
+    for ws in (buf.tile_meta, buf.fwd_ws, buf.bwd_ws):
+        assert stp.stp_device_status(ws) == stp.STP_OK
+    sampler = ClockSampler(_gpu_id(torch, local))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    steps = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()  # the GPU idles while the host packs: the pack is timed
+        s0, f0, f1, b1, s1 = ev(), ev(), ev(), ev(), ev()
+        s0.record()
+        plan = pack_and_upload()
+        attention((f0, f1, b1))
+        s1.record()
+        steps.append((s0, f0, f1, b1, s1, plan))
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    step_ms = [a.elapsed_time(e) for a, _, _, _, e, _ in steps]
+    fwd_ms = [f0.elapsed_time(f1) for _, f0, f1, _, _, _ in steps]
+    bwd_ms = [f1.elapsed_time(b1) for _, _, f1, b1, _, _ in steps]
+    head_ms = [a.elapsed_time(f0) for a, f0, _, _, _, _ in steps]  # pack + upload + classify
+    tot_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([tot_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    ms_per_step = tot_ms / args.steps
+    value = world * step_flops * args.steps / (tot_ms / 1e3) / 1e12
+    assert stp.stp_device_status(buf.bwd_ws) == stp.STP_OK
+
+    # ---- end-to-end leg: host buffers in, gradients and O back to host
+    o_h = torch.empty_like(q_h).pin_memory()
+    dq_h, dk_h, dv_h = (torch.empty_like(x).pin_memory() for x in (q_h, k_h, v_h))
+    h2d = sum(x.numel() * x.element_size() for x in (q_h, k_h, v_h, do_h)) + \
+        sum(x.numel() * x.element_size() for x in meta_h.values())
+    d2h = sum(x.numel() * x.element_size() for x in (o_h, dq_h, dk_h, dv_h))
+
+    def e2e_step():
+        for src, dst in ((q_h, q), (k_h, k), (v_h, v), (do_h, do)):
+            dst.copy_(src, non_blocking=True)
+        pack_and_upload()
+        attention()
+        for src, dst in ((o, o_h), (dq, dq_h), (dk, dk_h), (dv, dv_h)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        a, e = ev(), ev()
+        a.record()
+        e2e_step()
+        e.record()
+        e_ms.append((a, e))
+    torch.cuda.synchronize()
+    e_tot = sum(a.elapsed_time(e) for a, e in e_ms)
+    if world > 1:
+        t = torch.tensor([e_tot], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_tot = float(t.item())
+    e2e_value = world * step_flops * args.steps / (e_tot / 1e3) / 1e12
+
+    peak, hbm, peak_kind = _peaks()
+    bwd_avg = statistics.mean(bwd_ms)
+    achieved = bwd_flops / (bwd_avg / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "rows": R, "row_len": T, "sequences": b.n_seqs,
+                   "useful_pairs_per_head": int(useful), "useful_tflop_per_step": step_flops / 1e12,
+                   "packed_tokens": info["packed_tokens"], "input_tokens": info["input_tokens"],
+                   "l2": "flushed (512 MiB write) before every timed step", "parallelism": f"replicas x{world}"},
+        "pct_of_bf16_peak": 100.0 * value / world / peak,
+        "trajectories_per_s": world * b.n_seqs * args.steps / (tot_ms / 1e3),
+        "breakdown_ms": {"pack_upload_classify": statistics.mean(head_ms), "fwd": statistics.mean(fwd_ms),
+                         "bwd": bwd_avg, "fwd_tflops": fwd_flops / (statistics.mean(fwd_ms) / 1e3) / 1e12,
+                         "bwd_tflops": achieved},
+        "roofline": {"bound": "tensor", "kernel": "stp_attn_bwd (delta + dK/dV/dQ tcgen05 kernel + dQ finalize)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} bf16 burst", "traffic": None},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e_tot / args.steps},
+        "gpu_launches": 6 * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import pack as OP
+        plan_o = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared, b.family)
+        nh = 8
+        dt, fl = oracle_sample(plan_o, q_h.float(), k_h.float(), v_h.float(), do_h.float(), shape.scale, nh)
+        line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
+                                "kind": "oracle",
+                                "sample": f"float64 NumPy oracle fwd+bwd of {nh} of {Hq} query heads "
+                                          f"(their kv heads) over the whole packed row ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
