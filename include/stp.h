@@ -24,8 +24,9 @@
  *   - Host buffers are caller-owned unless stated.  The opaque stp_plan is
  *     owned by the library (free it with stp_plan_free); it is immutable after
  *     stp_pack, so concurrent reads from several threads are safe.
- *   - Device buffers and workspaces are caller-owned; the library never
- *     allocates device memory.  Device calls are asynchronous on the given
+ *   - Device buffers and workspaces are caller-owned; no call allocates
+ *     device memory (stp_classify_noalloc uses a fixed array the library
+ *     holds instead of caller scratch).  Device calls are asynchronous on the given
  *     stream (a cudaStream_t passed as void*; NULL = the legacy default
  *     stream).  Their status covers host-side validation and launch errors;
  *     device-side checks set an error word in the workspace that
@@ -177,6 +178,28 @@ stp_status stp_workspace_size(const stp_attn_desc* desc, size_t* tile_meta_bytes
  */
 stp_status stp_classify(const stp_attn_desc* desc, const int32_t* d_subtree_end,
                         void* d_tile_meta, void* stream);
+
+/*
+ * stp_classify_noalloc -- stp_classify for callers that cannot allocate device
+ * memory (for instance code being recorded into a CUDA graph, where cudaMalloc
+ * is not allowed, or a plug-in host that only passes the buffers of its inputs
+ * and outputs).  The paper has no counterpart; this is a library convenience.
+ * Same arguments, outputs and checks as stp_classify, but the kernel's scratch
+ * (per-key-tile min / max of subtree_end) lives in a fixed device array inside
+ * the library, 1 MiB, held by every GPU that loads the library until the
+ * process exits; no allocation is made by this call.
+ *   - at most n_rows * (row_len / 128) <= 131072 tiles; larger sizes return
+ *     STP_EINVAL with a message (use stp_classify);
+ *   - the first call on a device looks up the array's device address with that
+ *     device current (cudaGetSymbolAddress); make that first call before any
+ *     stream capture;
+ *   - all calls share the one array: calls that overlap on the GPU (different
+ *     streams, or different host threads without ordering) race and may
+ *     corrupt each other's result.  The array keeps the last call's contents;
+ *     every entry is rewritten before it is read, so nothing needs clearing.
+ */
+stp_status stp_classify_noalloc(const stp_attn_desc* desc, const int32_t* d_subtree_end,
+                                void* d_tile_meta, void* stream);
 
 /* Copy the class matrix int8 [R, T/128, T/128] out of tile_meta (device to device). */
 stp_status stp_read_tile_classes(const stp_attn_desc* desc, const void* d_tile_meta,

@@ -18,6 +18,8 @@
 // (ascending) and the list of non-empty query tiles of key tile b.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "layout.h"
 
@@ -198,5 +200,86 @@ extern "C" stp_status stp_device_status(const void* d_ws, void* stream, stp_stat
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_device_status: %s", cudaGetErrorString(e));
   *out = word ? STP_EDEVICE : STP_OK;
   if (word) fail(STP_EDEVICE, "device error word 0x%x", word);
+  return STP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Classification for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc (or any allocator) at the point where
+// they classify: code recording a CUDA graph, a plug-in host that only hands
+// over the buffers of its inputs and outputs, or a latency-critical loop that
+// forbids allocation.  This variant keeps its only scratch -- the per-key-tile
+// min / max of subtree_end -- in a fixed array owned by the library instead
+// of in the caller's buffer.  The array is a file-scope device variable: every
+// GPU that loads the library holds it (1 MiB) until the process exits.
+// ---------------------------------------------------------------------------
+
+constexpr int64_t kNoAllocMaxTiles = 131072;  // rows x (row_len / 128), at most
+static __device__ __align__(256) int32_t g_classify_scratch[2 * kNoAllocMaxTiles];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_classify_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device, with that device current, and cached.
+stp_status classify_scratch(int32_t** out) {
+  static std::mutex mu;
+  static int32_t* addr[kMaxDevices] = {};
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(STP_ECUDA, "stp_classify_noalloc: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(STP_EUNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_classify_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(STP_ECUDA, "stp_classify_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = addr[dev];
+  return STP_OK;
+}
+
+}  // namespace
+
+extern "C" stp_status stp_classify_noalloc(const stp_attn_desc* desc, const int32_t* d_subtree_end,
+                                           void* d_tile_meta, void* stream) {
+  clear_error();
+  stp_status st = check_desc(desc);
+  if (st) return st;
+  if (!d_subtree_end || !d_tile_meta)
+    return fail(STP_EINVAL, "stp_classify_noalloc: NULL device pointer");
+  if ((reinterpret_cast<uintptr_t>(d_tile_meta) & 255) || (reinterpret_cast<uintptr_t>(d_subtree_end) & 15))
+    return fail(STP_EINVAL, "stp_classify_noalloc: tile_meta must be 256-byte and subtree_end 16-byte aligned");
+  const int64_t NT = desc->row_len / kTile;
+  if ((int64_t)desc->n_rows * NT > kNoAllocMaxTiles)
+    return fail(STP_EINVAL,
+                "stp_classify_noalloc: %d rows x %lld tiles exceed the fixed scratch of %lld tiles "
+                "(use stp_classify)",
+                desc->n_rows, (long long)NT, (long long)kNoAllocMaxTiles);
+  if (desc->n_rows == 0) return STP_OK;
+  int32_t* scratch = nullptr;
+  st = classify_scratch(&scratch);
+  if (st) return st;
+  const TileMeta m = tile_meta_layout(desc->n_rows, NT);
+  char* base = static_cast<char*>(d_tile_meta);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* err = reinterpret_cast<uint32_t*>(base + m.err);
+  cudaMemsetAsync(err, 0, 4, s);
+  // every min / max entry is written before it is read: nothing to clear
+  int32_t* kmin = scratch;
+  int32_t* kmax = scratch + kNoAllocMaxTiles;
+  dim3 grid((unsigned)NT, desc->n_rows);
+  tile_minmax_kernel<<<grid, 128, 0, s>>>(d_subtree_end, desc->row_len, (int)NT, kmin, kmax, err);
+  tile_lists_kernel<<<grid, 128, 0, s>>>(
+      (int)NT, kmin, kmax, reinterpret_cast<int8_t*>(base + m.cls),
+      reinterpret_cast<int32_t*>(base + m.csr_cnt), reinterpret_cast<int32_t*>(base + m.csr),
+      reinterpret_cast<int32_t*>(base + m.csc_cnt), reinterpret_cast<int32_t*>(base + m.csc));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(STP_ECUDA, "stp_classify_noalloc: %s", cudaGetErrorString(e));
   return STP_OK;
 }

@@ -24,7 +24,8 @@ STP_GLOBAL, STP_PER_FAMILY, STP_IN_ORDER = 0, 1, 2
 STP_BF16, STP_FP32 = 0, 1
 
 EXPORTED = ["stp_pack", "stp_plan_info", "stp_plan_write", "stp_plan_rows_of", "stp_plan_free",
-            "stp_workspace_size", "stp_classify", "stp_read_tile_classes", "stp_attn_fwd",
+            "stp_workspace_size", "stp_classify", "stp_classify_noalloc", "stp_read_tile_classes",
+            "stp_attn_fwd",
             "stp_attn_bwd", "stp_device_status", "stp_last_error", "stp_version"]
 
 
@@ -79,6 +80,8 @@ def lib():
         L.stp_workspace_size.restype = st
         L.stp_classify.argtypes = [ctypes.POINTER(AttnDesc), _P, _P, _P]
         L.stp_classify.restype = st
+        L.stp_classify_noalloc.argtypes = [ctypes.POINTER(AttnDesc), _P, _P, _P]
+        L.stp_classify_noalloc.restype = st
         L.stp_read_tile_classes.argtypes = [ctypes.POINTER(AttnDesc), _P, _P, _P]
         L.stp_read_tile_classes.restype = st
         L.stp_attn_fwd.argtypes = [ctypes.POINTER(AttnDesc), _P, _P, _P, _P, _P, _P, _P, _P, _P]
@@ -216,6 +219,15 @@ def stp_classify(desc: Desc, subtree_end, tile_meta, stream=None):
     d = desc.c()
     _check(lib().stp_classify(ctypes.byref(d), _dptr(subtree_end), _dptr(tile_meta), _stream(stream)),
            "stp_classify")
+
+
+def stp_classify_noalloc(desc: Desc, subtree_end, tile_meta, stream=None):
+    """stp_classify without device allocation: scratch lives in the library's
+    fixed 1 MiB device array (at most 131072 tiles; calls overlapping on the
+    GPU race).  Make the first call on a device before any stream capture."""
+    d = desc.c()
+    _check(lib().stp_classify_noalloc(ctypes.byref(d), _dptr(subtree_end), _dptr(tile_meta),
+                                      _stream(stream)), "stp_classify_noalloc")
 
 
 def stp_read_tile_classes(desc: Desc, tile_meta, cls_out, stream=None):
