@@ -122,6 +122,7 @@ extern "C" stp_status stp_attn_bwd(const stp_attn_desc* desc, const void* q, con
   char* ws = static_cast<char*>(d_ws);
   a.err = reinterpret_cast<uint32_t*>(ws + w.err);
   a.delta = reinterpret_cast<float*>(ws + w.delta);
+  a.nlse2 = desc->dtype == STP_BF16 ? reinterpret_cast<float*>(ws + w.nlse2) : nullptr;
   a.dq_acc = desc->dtype == STP_BF16 ? reinterpret_cast<float*>(ws + w.dq_acc) : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaMemsetAsync(a.err, 0, 4, s);

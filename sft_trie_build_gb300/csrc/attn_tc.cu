@@ -126,7 +126,18 @@ enum {
   B_COUNT = 16
 };
 
-__global__ void __launch_bounds__(320, 1)
+// 12 warps = three full warpgroups; registers move from the control
+// warpgroup (TMA + MMA issue) to the math warpgroups with setmaxnreg, at the
+// head of each role's branch.  Forward: 384 x 168 at launch =
+// 256 x 216 (two softmax groups) + 128 x 72.  Backward: 128 x 240
+// (elementwise) + 128 x 168 (dQ drain, unchanged) + 128 x 72 <= 384 x 168.
+// Per SM sub-partition (warps w, w+4, w+8): 216+216+72 and 240+168+72 <= 512.
+constexpr int kThreads = 384;
+constexpr int kRegsAtLaunch = 168, kRegsMath = 216, kRegsCtl = 72, kRegsBwdMath = 240;
+static_assert(kThreads * kRegsAtLaunch >= 256 * kRegsMath + 128 * kRegsCtl, "register split");
+static_assert(kThreads * kRegsAtLaunch >= 128 * (kRegsBwdMath + kRegsAtLaunch + kRegsCtl), "register split");
+
+__global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -189,6 +200,9 @@ __global__ void __launch_bounds__(320, 1)
   int issued_k[2] = {-1, -1};  // producer: last issued use of each stage
   int issued_v[2] = {-1, -1};
 
+  if (warp >= 8) {
+    regs_dec<kRegsCtl>();
+  }
   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && run) {
@@ -220,6 +234,12 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_3d(big + (4 + st) * kTileBytes + hf * kHalfTile, &tv, &bars[B_VF + st],
                       hf * 64, g, row0 + kt * 128);
         issued_v[st] = n;
+      }
+      // wait (bounded) for every copy this warp started
+      mbar_wait_drain(&bars[B_Q], 0);
+      for (int st = 0; st < 2; ++st) {
+        if (issued_k[st] >= 0) mbar_wait_drain(&bars[B_KF + st], issued_k[st] & 1);
+        if (issued_v[st] >= 0) mbar_wait_drain(&bars[B_VF + st], issued_v[st] & 1);
       }
     }
     __syncwarp();
@@ -270,9 +290,15 @@ __global__ void __launch_bounds__(320, 1)
         if (ok) mma_commit(&bars[B_VE + st]);
       }
     }
+    if (lane == 0 && run) {
+      // wait (bounded) for every MMA this thread issued
+      mma_commit(&bars[B_DRAIN]);
+      mbar_wait_drain(&bars[B_DRAIN], 0);
+    }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
+    regs_inc<kRegsMath>();
     const int hs = warp >> 2;
     const int row = threadIdx.x & 127;
     const int i = qt * 128 + row;
@@ -289,49 +315,47 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       fence_after_sync();
-      // pass 1: row max of the (masked) scores, in log2 units
+      // the whole score row: 128 TMEM columns of this thread's lane
+      uint32_t u[128];
+      tmem_ld32(s_addr + 0, u);
+      tmem_ld32(s_addr + 32, u + 32);
+      tmem_ld32(s_addr + 64, u + 64);
+      tmem_ld32(s_addr + 96, u + 96);
+      tmem_ld_wait();
+      if (part) {
+        // visible iff j <= i && subtree_end[j] >= i; the others become -inf
+        const int4* se4 = reinterpret_cast<const int4*>(se_row + k0);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int4 v = __ldg(se4 + c);
+          const int j = k0 + 4 * c;
+          if (!(j + 0 <= i && v.x >= i)) u[4 * c + 0] = 0xff800000u;
+          if (!(j + 1 <= i && v.y >= i)) u[4 * c + 1] = 0xff800000u;
+          if (!(j + 2 <= i && v.z >= i)) u[4 * c + 2] = 0xff800000u;
+          if (!(j + 3 <= i && v.w >= i)) u[4 * c + 3] = 0xff800000u;
+        }
+      }
+      // row max on the raw scores (the scale is positive)
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        tmem_ld32(s_addr + c * 32, u);
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          float x = __uint_as_float(u[k]) * p.scale_log2;
-          if (part) {
-            const int j = k0 + c * 32 + k;
-            x = ((j <= i) && (__ldg(se_row + j) >= i)) ? x : -INFINITY;
-          }
-          mx = fmaxf(mx, x);
-        }
-      }
-      const float m_new = fmaxf(m_run, mx);
+      for (int c = 0; c < 128; c += 2) mx = max3(mx, __uint_as_float(u[c]), __uint_as_float(u[c + 1]));
+      const float m_new = fmaxf(m_run, mx * p.scale_log2);
       const float m_use = (m_new > m_run + kRescaleThreshold) ? m_new : m_run;
       const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
-      const float alpha = exp2f(m_run - m_sub);
-      // pass 2: probabilities, kept packed as bf16 pairs until P is free
-      float rs = 0.f;
+      const float alpha = ex2(m_run - m_sub);
+      // p = 2^(s * scale log2e - m), two columns per packed FFMA
+      const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 nm2 = make_float2(-m_sub, -m_sub);
+      float2 acc2 = make_float2(0.f, 0.f);
       uint32_t pk[64];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        tmem_ld32(s_addr + c * 32, u);
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          float x0 = __uint_as_float(u[k]) * p.scale_log2;
-          float x1 = __uint_as_float(u[k + 1]) * p.scale_log2;
-          if (part) {
-            const int j = k0 + c * 32 + k;
-            x0 = ((j <= i) && (__ldg(se_row + j) >= i)) ? x0 : -INFINITY;
-            x1 = ((j + 1 <= i) && (__ldg(se_row + j + 1) >= i)) ? x1 : -INFINITY;
-          }
-          const float p0 = exp2f(x0 - m_sub), p1 = exp2f(x1 - m_sub);
-          rs += p0 + p1;
-          pk[c * 16 + (k >> 1)] = pack_bf16x2(p0, p1);
-        }
+      for (int c = 0; c < 64; ++c) {
+        const float2 y = __ffma2_rn(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2, nm2);
+        const float2 pr = make_float2(ex2(y.x), ex2(y.y));
+        acc2 = __fadd2_rn(acc2, pr);
+        pk[c] = pack_bf16x2(pr.x, pr.y);
       }
+      const float rs = acc2.x + acc2.y;
       // the P buffer is free and O_hs stable once the previous reader of P is done
       if (nh == 2) {
         if (hs == 0) {
@@ -390,17 +414,6 @@ __global__ void __launch_bounds__(320, 1)
   }
 
   // ---------------------------------------------------------------- teardown
-  if (warp == 8 && lane == 0 && run) {
-    mbar_wait_drain(&bars[B_Q], 0);
-    for (int st = 0; st < 2; ++st) {
-      if (issued_k[st] >= 0) mbar_wait_drain(&bars[B_KF + st], issued_k[st] & 1);
-      if (issued_v[st] >= 0) mbar_wait_drain(&bars[B_VF + st], issued_v[st] & 1);
-    }
-  }
-  if (warp == 9 && lane == 0 && run) {
-    mma_commit(&bars[B_DRAIN]);
-    mbar_wait_drain(&bars[B_DRAIN], 0);
-  }
   __syncwarp();
   fence_before_sync();
   __syncthreads();
@@ -435,8 +448,8 @@ struct BwdParams {
   const int32_t* se;
   const int32_t* csc_cnt;
   const int32_t* csc;
-  const float* lse;
-  const float* delta;
+  const float* nlse2;   // -LSE * log2 e
+  const float* ndelta;  // -Delta
   float* dq_acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -451,7 +464,7 @@ enum {
 constexpr int kBwdBigBytes = 6 * kTileBytes;  // K V Q dO P^T dS^T
 constexpr int kBwdVecBytes = 2 * 128 * 4;  // LSE and Delta of the current query tile
 
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const BwdParams p) {
@@ -501,6 +514,9 @@ __global__ void __launch_bounds__(320, 1)
   // TMEM columns: S^T / dQ 0..127, dP^T 128..255, dV 256..383, dK 384..511
   int issued_kv = -1, issued_q = -1;
 
+  if (warp >= 8) {
+    regs_dec<kRegsCtl>();
+  }
   if (warp == 8) {
     if (lane == 0 && run) {
       tma_prefetch_desc(&tq);
@@ -522,14 +538,16 @@ __global__ void __launch_bounds__(320, 1)
         }
         if (j > 0 && !mbar_wait(&bars[C_QE], (j - 1) & 1, abort_flag, p.err)) break;
         mbar_expect_tx(&bars[C_QF], 2 * kTileBytes + 2 * 128 * 4);
-        bulk_load(vec, p.lse + ((size_t)r * p.Hq + h) * p.T + qt * 128, 512, &bars[C_QF]);
-        bulk_load(vec + 128, p.delta + ((size_t)r * p.Hq + h) * p.T + qt * 128, 512, &bars[C_QF]);
+        bulk_load(vec, p.nlse2 + ((size_t)r * p.Hq + h) * p.T + qt * 128, 512, &bars[C_QF]);
+        bulk_load(vec + 128, p.ndelta + ((size_t)r * p.Hq + h) * p.T + qt * 128, 512, &bars[C_QF]);
         for (int hf = 0; hf < 2; ++hf) {
           tma_load_3d(big + 2 * kTileBytes + hf * kHalfTile, &tq, &bars[C_QF], hf * 64, h, row0 + qt * 128);
           tma_load_3d(big + 3 * kTileBytes + hf * kHalfTile, &tdo, &bars[C_QF], hf * 64, h, row0 + qt * 128);
         }
         issued_q = j;
       }
+      if (issued_kv >= 0) mbar_wait_drain(&bars[C_KV], 0);
+      if (issued_q >= 0) mbar_wait_drain(&bars[C_QF], issued_q & 1);
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -561,9 +579,14 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (ok) mma_commit(&bars[C_DONE]);
     }
+    if (lane == 0 && run) {
+      mma_commit(&bars[C_DRAIN]);
+      mbar_wait_drain(&bars[C_DRAIN], 0);
+    }
     __syncwarp();
   } else if (warp < 4) {
     // ------------------------------------------------ per-key elementwise
+    regs_inc<kRegsBwdMath>();
     const int t = threadIdx.x;          // key row = TMEM lane
     const int jk = kt * 128 + t;        // key index in the row
     const int se_j = p.se[(size_t)row0 + jk];
@@ -574,8 +597,8 @@ __global__ void __launch_bounds__(320, 1)
       const int h = g * p.G + j % p.G;
       const int q0 = qt * 128;
       (void)h;
-      const float* lse_s = vec;
-      const float* dlt_s = vec + 128;
+      const float* nl_s = vec;         // -LSE log2 e per query column
+      const float* nd_s = vec + 128;   // -Delta per query column
       // LSE / Delta of this query tile arrive with its Q / dO tiles
       if (!mbar_wait(&bars[C_QF], j & 1, abort_flag, p.err) ||
           !mbar_wait(&bars[C_SF], j & 1, abort_flag, p.err)) {
@@ -584,6 +607,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       fence_after_sync();
       uint32_t pp[64], dd[64];
+      const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t us[32], ud[32];
@@ -592,18 +616,19 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
-          float pr[2], ds[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = c * 32 + k + u;
+          const int col = c * 32 + k;
+          const float2 nl2 = *reinterpret_cast<const float2*>(nl_s + col);
+          const float2 nd2 = *reinterpret_cast<const float2*>(nd_s + col);
+          float2 y = __ffma2_rn(make_float2(__uint_as_float(us[k]), __uint_as_float(us[k + 1])), sl2, nl2);
+          if (part) {
             const int i = q0 + col;
-            const bool vis = !part || (jk <= i && se_j >= i);
-            const float pv = vis ? exp2f(__uint_as_float(us[k + u]) * p.scale_log2 - lse_s[col] * kLog2e) : 0.f;
-            pr[u] = pv;
-            ds[u] = pv * (__uint_as_float(ud[k + u]) - dlt_s[col]);
+            if (!(jk <= i && se_j >= i)) y.x = -INFINITY;
+            if (!(jk <= i + 1 && se_j >= i + 1)) y.y = -INFINITY;
           }
-          pp[c * 16 + (k >> 1)] = pack_bf16x2(pr[0], pr[1]);
-          dd[c * 16 + (k >> 1)] = pack_bf16x2(ds[0], ds[1]);
+          const float2 pr = make_float2(ex2(y.x), ex2(y.y));
+          const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(ud[k]), __uint_as_float(ud[k + 1])), nd2));
+          pp[c * 16 + (k >> 1)] = pack_bf16x2(pr.x, pr.y);
+          dd[c * 16 + (k >> 1)] = pack_bf16x2(ds.x, ds.y);
         }
       }
       if (j > 0 && !mbar_wait(&bars[C_PSF], (j - 1) & 1, abort_flag, p.err)) {
@@ -645,7 +670,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
     }
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------ dQ drain (per query)
     const int t = threadIdx.x - 128;    // query row = TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -658,7 +683,7 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       fence_after_sync();
-      float4* dst = reinterpret_cast<float4*>(p.dq_acc + (((size_t)row0 + qt * 128 + t) * p.Hq + h) * 128);
+      float* dst = p.dq_acc + (((size_t)row0 + qt * 128 + t) * p.Hq + h) * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t u[32];
@@ -670,20 +695,12 @@ __global__ void __launch_bounds__(320, 1)
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          atomicAdd(dst + c * 8 + k, make_float4(__uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1]),
-                                                 __uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3])));
+          red_add_v4(dst + c * 32 + 4 * k, __uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1]),
+                     __uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3]));
       }
     }
   }
 
-  if (warp == 8 && lane == 0 && run) {
-    if (issued_kv >= 0) mbar_wait_drain(&bars[C_KV], 0);
-    if (issued_q >= 0) mbar_wait_drain(&bars[C_QF], issued_q & 1);
-  }
-  if (warp == 9 && lane == 0 && run) {
-    mma_commit(&bars[C_DRAIN]);
-    mbar_wait_drain(&bars[C_DRAIN], 0);
-  }
   __syncwarp();
   fence_before_sync();
   __syncthreads();
@@ -694,7 +711,9 @@ __global__ void __launch_bounds__(320, 1)
 // Delta[r,h,i] = sum_d dO . O (bf16 in, f32 out); one warp per (row, token, head).
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
                                                         const __nv_bfloat16* __restrict__ dout,
-                                                        float* __restrict__ delta, int R, int T,
+                                                        const float* __restrict__ lse,
+                                                        float* __restrict__ ndelta,
+                                                        float* __restrict__ nlse2, int R, int T,
                                                         int Hq) {
   const int lane = threadIdx.x & 31;
   const size_t rows = (size_t)R * T * Hq;
@@ -715,7 +734,9 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
       const int h = (int)(w % Hq);
       const size_t ri = w / Hq;
       const size_t rr = ri / T, i = ri - rr * T;
-      delta[(rr * Hq + h) * T + i] = acc;
+      const size_t at = (rr * Hq + h) * T + i;
+      ndelta[at] = -acc;
+      nlse2[at] = -lse[at] * kLog2e;
     }
   }
 }
@@ -767,7 +788,7 @@ cudaError_t tc_fwd(const AttnArgs& a, cudaStream_t s) {
     attr = true;
   }
   const unsigned grid = (unsigned)(p.NT * p.R * p.Hkv * p.npairs);
-  fwd_tc_kernel<<<grid, 320, kSmemLimit, s>>>(mq, mk, mv, p);
+  fwd_tc_kernel<<<grid, kThreads, kSmemLimit, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -786,8 +807,8 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(a.dq_acc, 0, n * sizeof(float), s);
   if (e != cudaSuccess) return e;
   bwd_delta_kernel<<<2048, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.o_in),
-                                        static_cast<const __nv_bfloat16*>(a.dout), a.delta, a.R, a.T,
-                                        a.Hq);
+                                        static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.delta,
+                                        a.nlse2, a.R, a.T, a.Hq);
   BwdParams p;
   p.R = a.R;
   p.T = a.T;
@@ -800,8 +821,8 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
   p.se = a.se;
   p.csc_cnt = a.csc_cnt;
   p.csc = a.csc;
-  p.lse = a.lse;
-  p.delta = a.delta;
+  p.nlse2 = a.nlse2;
+  p.ndelta = a.delta;
   p.dq_acc = a.dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
@@ -812,7 +833,7 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  bwd_tc_kernel<<<(unsigned)(p.NT * p.R * p.Hkv), 320, kSmemLimit, s>>>(mq, mk, mv, mdo, p);
+  bwd_tc_kernel<<<(unsigned)(p.NT * p.R * p.Hkv), kThreads, kSmemLimit, s>>>(mq, mk, mv, mdo, p);
   bwd_dq_finalize_kernel<<<2048, 256, 0, s>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n / 8,
                                               a.scale);
   return cudaGetLastError();

@@ -11,8 +11,9 @@
 //   kmin, kmax int32 [R][NT]          min / max subtree_end over each key tile
 //
 // fwd workspace: err (uint32) only.
-// bwd workspace: err, delta float32 [R][Hq][T], dq_acc float32 [R][T][Hq][D]
-// (the float32 accumulator exists for the bf16 path only).
+// bwd workspace: err, delta float32 [R][Hq][T] (Delta on the float32 path,
+// -Delta on the bf16 path), and for the bf16 path nlse2 float32 [R][Hq][T]
+// (-LSE * log2 e) and dq_acc float32 [R][T][Hq][D].
 #pragma once
 
 #include <cstddef>
@@ -47,7 +48,7 @@ inline TileMeta tile_meta_layout(int64_t R, int64_t NT) {
 }
 
 struct BwdWs {
-  size_t err, delta, dq_acc, total;
+  size_t err, delta, nlse2, dq_acc, total;
 };
 
 inline BwdWs bwd_ws_layout(int64_t R, int64_t T, int64_t Hq, int64_t D, bool need_acc) {
@@ -55,6 +56,7 @@ inline BwdWs bwd_ws_layout(int64_t R, int64_t T, int64_t Hq, int64_t D, bool nee
   size_t o = 0;
   w.err = o;    o += 256;
   w.delta = o;  o += align256(size_t(R * Hq * T) * 4);
+  w.nlse2 = o;  o += need_acc ? align256(size_t(R * Hq * T) * 4) : 0;
   w.dq_acc = o; o += need_acc ? align256(size_t(R * T * Hq * D) * 4) : 0;
   w.total = o;
   return w;

@@ -25,7 +25,8 @@ struct AttnArgs {
   const int32_t* csr;
   const int32_t* csc_cnt;
   const int32_t* csc;
-  float* delta;          // [R, Hq, T] (backward)
+  float* delta;          // [R, Hq, T] (backward): Delta (fp32 path) or -Delta (bf16 path)
+  float* nlse2;          // [R, Hq, T] (backward, bf16 path): -LSE * log2 e
   float* dq_acc;         // [R, T, Hq, D] float32 (backward, bf16 path)
   uint32_t* err;         // device error word of the workspace
 };
