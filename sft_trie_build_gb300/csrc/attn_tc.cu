@@ -133,9 +133,9 @@ enum {
 // (elementwise) + 128 x 168 (dQ drain, unchanged) + 128 x 72 <= 384 x 168.
 // Per SM sub-partition (warps w, w+4, w+8): 216+216+72 and 240+168+72 <= 512.
 constexpr int kThreads = 384;
-constexpr int kRegsAtLaunch = 168, kRegsMath = 216, kRegsCtl = 72, kRegsBwdMath = 240;
+constexpr int kRegsAtLaunch = 168, kRegsMath = 216, kRegsCtl = 72, kRegsBwdMath = 208, kRegsBwdCtl = 128;
 static_assert(kThreads * kRegsAtLaunch >= 256 * kRegsMath + 128 * kRegsCtl, "register split");
-static_assert(kThreads * kRegsAtLaunch >= 128 * (kRegsBwdMath + kRegsAtLaunch + kRegsCtl), "register split");
+static_assert(kThreads * kRegsAtLaunch >= 128 * (kRegsBwdMath + kRegsAtLaunch + kRegsBwdCtl), "register split");
 
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -429,16 +429,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Per CTA: (row r, kv head g, key tile kt).  The key tile's list of
 // non-empty query tiles, times the G query heads of the group, gives the
 // iterations j = (query tile, head).  Per iteration:
-//   MMA      S^T = K Q^T and dP^T = V dO^T (keys on TMEM lanes), then, once
-//            P^T and dS^T are in shared memory, dV += P^T dO, dK += dS^T Q
-//            (accumulated in TMEM over all iterations) and dQ_j = dS K into
-//            the S^T columns;
-//   warps 0-3  one thread per key j: p = exp2(s * scale log2e - LSE_i log2e)
+//   MMA      S^T = K Q^T into TMEM columns 0..127 and dP^T = V dO^T into
+//            128..255 (keys on TMEM lanes); once P^T is in TMEM (over S^T) and
+//            dS^T in shared memory: dV += P^T dO (A from TMEM), dK += dS^T Q
+//            (both accumulated in TMEM over all iterations), then dQ_j = dS K
+//            into columns 128..255; S^T of the next iteration follows at once;
+//   warps 0-3  one thread per key j: p = 2^(s scale log2e - LSE_i log2e)
 //            (masked on PARTIAL tiles with the thread's own subtree_end[j]),
-//            dS = p (dP - Delta_i); writes P^T and dS^T as bf16;
+//            dS = p (dP - Delta_i); P^T goes back to TMEM as packed bf16 pairs,
+//            dS^T to shared memory;
 //   warps 4-7  one thread per query: reads dQ_j from TMEM and adds it into the
-//            float32 accumulator with vector atomics;
-//   warp 8   TMA: K, V once; Q and dO of each iteration;
+//            float32 accumulator with vector reductions;
+//   warp 8   TMA: K, V once; Q, dO, -LSE log2e and -Delta of each iteration
+//            through a two-stage ring;
 //   warp 9   MMA issue, TMEM owner.
 // dK (times scale) and dV leave TMEM once at the end.
 
@@ -458,30 +461,29 @@ struct BwdParams {
 };
 
 enum {
-  C_KV = 0, C_QF = 1, C_QE = 2, C_SF = 3, C_DR = 4, C_QD = 5, C_SFREE = 6, C_PSF = 7,
-  C_DONE = 8, C_DRAIN = 9, C_COUNT = 10
+  C_KV = 0, C_QF = 1, C_QE = 3, C_SF = 5, C_DR = 6, C_QD = 7, C_SFREE = 8, C_PSF = 9,
+  C_DONE = 10, C_DRAIN = 11, C_COUNT = 12
 };
-constexpr int kBwdBigBytes = 6 * kTileBytes;  // K V Q dO P^T dS^T
-constexpr int kBwdVecBytes = 2 * 128 * 4;  // LSE and Delta of the current query tile
+// shared memory: [K | V | Q0 | Q1 | dO0 | dO1 | dS^T] (1024-aligned, at the
+// start of dynamic shared memory) [vec0 | vec1] [barriers ...]
+constexpr int kBwdBigBytes = 7 * kTileBytes;
+constexpr int kBwdVecBytes = 2 * 2 * 128 * 4;  // per stage: -LSE log2e and -Delta, 128 each
+constexpr int kBwdSmem = kBwdBigBytes + kBwdVecBytes + kSmallBytes;
+static_assert(kBwdSmem <= kSmemLimit, "backward shared memory");
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const BwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* big = smem_raw;
+  const uint32_t big_s = smem_u32(smem_raw);
+  float* vec = reinterpret_cast<float*>(smem_raw + kBwdBigBytes);  // [stage][-LSE log2e 128 | -Delta 128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + kBwdBigBytes + kBwdVecBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* vec = reinterpret_cast<float*>(smem_raw + kSmallBytes);  // [LSE 128 | Delta 128]
-  const uint32_t raw = smem_u32(smem_raw) + kSmallBytes + kBwdVecBytes;
-  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-  uint8_t* big = smem_raw + kSmallBytes + kBwdVecBytes + pad;
-  const uint32_t big_s = raw + pad;
-  const uint32_t k_s = big_s, v_s = big_s + kTileBytes, q_s = big_s + 2 * kTileBytes,
-                 do_s = big_s + 3 * kTileBytes, pt_s = big_s + 4 * kTileBytes,
-                 dst_s = big_s + 5 * kTileBytes;
-  uint8_t* pt_tile = big + 4 * kTileBytes;
-  uint8_t* dst_tile = big + 5 * kTileBytes;
+  const uint32_t k_s = big_s, v_s = big_s + kTileBytes, dst_s = big_s + 6 * kTileBytes;
+  uint8_t* dst_tile = big + 6 * kTileBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per_kt = p.R * p.Hkv;
@@ -496,9 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int b = 0; b < C_COUNT; ++b) mbar_init(&bars[b], (b == C_DR || b == C_SFREE) ? 128 : 1);
     *abort_flag = 0;
-    if (pad + kSmallBytes + kBwdVecBytes + kBwdBigBytes > kSmemLimit || cnt <= 0 || cnt > p.NT) {
+    if ((big_s & 1023u) != 0 || cnt <= 0 || cnt > p.NT) {
       *abort_flag = 1;
-      atomicOr(p.err, cnt <= 0 || cnt > p.NT ? kErrBadList : kErrTmem);
+      atomicOr(p.err, (big_s & 1023u) != 0 ? kErrTmem : kErrBadList);
     }
     fence_mbar_init();
   }
@@ -511,14 +513,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const bool run = !*abort_flag;
-  // TMEM columns: S^T / dQ 0..127, dP^T 128..255, dV 256..383, dK 384..511
-  int issued_kv = -1, issued_q = -1;
+  // TMEM columns: S^T / P^T 0..127, dP^T / dQ 128..255, dV 256..383, dK 384..511
 
   if (warp >= 8) {
-    regs_dec<kRegsCtl>();
+    regs_dec<kRegsBwdCtl>();
   }
   if (warp == 8) {
     if (lane == 0 && run) {
+      int issued_q[2] = {-1, -1};
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
@@ -528,54 +530,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(big + hf * kHalfTile, &tk, &bars[C_KV], hf * 64, g, row0 + kt * 128);
         tma_load_3d(big + kTileBytes + hf * kHalfTile, &tv, &bars[C_KV], hf * 64, g, row0 + kt * 128);
       }
-      issued_kv = 0;
+      int ent = list[0];
       for (int j = 0; j < n_it; ++j) {
-        const int qt = list[j / p.G] >> 1, h = g * p.G + j % p.G;
+        const int st = j & 1, n = j >> 1;
+        const int qt = ent >> 1, h = g * p.G + j % p.G;
+        if (j + 1 < n_it) ent = list[(j + 1) / p.G];
         if (qt < kt || qt >= p.NT) {
           *abort_flag = 1;
           atomicOr(p.err, kErrBadList);
           break;
         }
-        if (j > 0 && !mbar_wait(&bars[C_QE], (j - 1) & 1, abort_flag, p.err)) break;
-        mbar_expect_tx(&bars[C_QF], 2 * kTileBytes + 2 * 128 * 4);
-        bulk_load(vec, p.nlse2 + ((size_t)r * p.Hq + h) * p.T + qt * 128, 512, &bars[C_QF]);
-        bulk_load(vec + 128, p.ndelta + ((size_t)r * p.Hq + h) * p.T + qt * 128, 512, &bars[C_QF]);
+        if (j >= 2 && !mbar_wait(&bars[C_QE + st], (n - 1) & 1, abort_flag, p.err)) break;
+        mbar_expect_tx(&bars[C_QF + st], 2 * kTileBytes + 2 * 128 * 4);
+        float* vs = vec + st * 256;
+        const size_t at = ((size_t)r * p.Hq + h) * p.T + qt * 128;
+        bulk_load(vs, p.nlse2 + at, 512, &bars[C_QF + st]);
+        bulk_load(vs + 128, p.ndelta + at, 512, &bars[C_QF + st]);
         for (int hf = 0; hf < 2; ++hf) {
-          tma_load_3d(big + 2 * kTileBytes + hf * kHalfTile, &tq, &bars[C_QF], hf * 64, h, row0 + qt * 128);
-          tma_load_3d(big + 3 * kTileBytes + hf * kHalfTile, &tdo, &bars[C_QF], hf * 64, h, row0 + qt * 128);
+          tma_load_3d(big + (2 + st) * kTileBytes + hf * kHalfTile, &tq, &bars[C_QF + st], hf * 64, h,
+                      row0 + qt * 128);
+          tma_load_3d(big + (4 + st) * kTileBytes + hf * kHalfTile, &tdo, &bars[C_QF + st], hf * 64, h,
+                      row0 + qt * 128);
         }
-        issued_q = j;
+        issued_q[st] = n;
       }
-      if (issued_kv >= 0) mbar_wait_drain(&bars[C_KV], 0);
-      if (issued_q >= 0) mbar_wait_drain(&bars[C_QF], issued_q & 1);
+      mbar_wait_drain(&bars[C_KV], 0);
+      for (int st = 0; st < 2; ++st)
+        if (issued_q[st] >= 0) mbar_wait_drain(&bars[C_QF + st], issued_q[st] & 1);
     }
     __syncwarp();
   } else if (warp == 9) {
     if (lane == 0 && run) {
       constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
-      constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // dV, dK
+      constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // dV (A in TMEM), dK
       constexpr uint32_t id_nn = idesc_bf16(128, 128, 1, 1);  // dQ
       bool ok = mbar_wait(&bars[C_KV], 0, abort_flag, p.err);
+      // S^T of the first iteration
+      if (ok && n_it > 0) {
+        ok = mbar_wait(&bars[C_QF], 0, abort_flag, p.err);
+        if (ok) {
+          fence_after_sync();
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem, kmajor_desc(k_s, kk), kmajor_desc(big_s + 2 * kTileBytes, kk), id_kk, kk > 0);
+        }
+      }
       for (int j = 0; ok && j < n_it; ++j) {
-        if (!mbar_wait(&bars[C_QF], j & 1, abort_flag, p.err)) break;
+        const int st = j & 1;
+        const uint32_t q_s = big_s + (2 + st) * kTileBytes, do_s = big_s + (4 + st) * kTileBytes;
+        // dP^T into columns 128..255 once dQ_{j-1} has been read out of them
         if (j > 0 && !mbar_wait(&bars[C_SFREE], (j - 1) & 1, abort_flag, p.err)) break;
         fence_after_sync();
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem, kmajor_desc(k_s, kk), kmajor_desc(q_s, kk), id_kk, kk > 0);
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tmem + 128, kmajor_desc(v_s, kk), kmajor_desc(do_s, kk), id_kk, kk > 0);
         mma_commit(&bars[C_SF]);
         if (!mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err)) break;
         fence_after_sync();
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + 256, kmajor_desc(pt_s, kk), mnmajor_desc(do_s, kk), id_kn, (j > 0 || kk > 0));
+          mma_ts(tmem + 256, tmem + kk * 8, mnmajor_desc(do_s, kk), id_kn, (j > 0 || kk > 0));
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tmem + 384, kmajor_desc(dst_s, kk), mnmajor_desc(q_s, kk), id_kn, (j > 0 || kk > 0));
-        mma_commit(&bars[C_QE]);
+        mma_commit(&bars[C_QE + st]);
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem, mnmajor_desc(dst_s, kk), mnmajor_desc(k_s, kk), id_nn, kk > 0);
+          mma_ss(tmem + 128, mnmajor_desc(dst_s, kk), mnmajor_desc(k_s, kk), id_nn, kk > 0);
         mma_commit(&bars[C_QD]);
         mma_commit(&bars[C_PSF]);
+        // S^T of the next iteration (P^T_j in columns 0..127 is consumed by dV above)
+        if (j + 1 < n_it) {
+          const int st1 = (j + 1) & 1;
+          if (!mbar_wait(&bars[C_QF + st1], ((j + 1) >> 1) & 1, abort_flag, p.err)) break;
+          fence_after_sync();
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem, kmajor_desc(k_s, kk), kmajor_desc(big_s + (2 + st1) * kTileBytes, kk), id_kk, kk > 0);
+        }
       }
       if (ok) mma_commit(&bars[C_DONE]);
     }
@@ -591,34 +617,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int jk = kt * 128 + t;        // key index in the row
     const int se_j = p.se[(size_t)row0 + jk];
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
     bool ok = run;
+    int ent = run ? list[0] : 0;
     for (int j = 0; ok && j < n_it; ++j) {
-      const int ent = list[j / p.G], qt = ent >> 1, part = ent & 1;
-      const int h = g * p.G + j % p.G;
+      const int st = j & 1;
+      const int qt = ent >> 1, part = ent & 1;
+      if (j + 1 < n_it) ent = list[(j + 1) / p.G];
       const int q0 = qt * 128;
-      (void)h;
-      const float* nl_s = vec;         // -LSE log2 e per query column
-      const float* nd_s = vec + 128;   // -Delta per query column
-      // LSE / Delta of this query tile arrive with its Q / dO tiles
-      if (!mbar_wait(&bars[C_QF], j & 1, abort_flag, p.err) ||
-          !mbar_wait(&bars[C_SF], j & 1, abort_flag, p.err)) {
+      const float* nl_s = vec + st * 256;   // -LSE log2 e per query column
+      const float* nd_s = nl_s + 128;       // -Delta per query column
+      if (!mbar_wait(&bars[C_QF + st], (j >> 1) & 1, abort_flag, p.err) ||
+          !mbar_wait(&bars[C_SF], j & 1, abort_flag, p.err) ||
+          (j > 0 && !mbar_wait(&bars[C_PSF], (j - 1) & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
       fence_after_sync();
-      uint32_t pp[64], dd[64];
-      const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t us[32], ud[32];
+        uint32_t us[32], ud[32], pp[16], dd[16];
         tmem_ld32(tmem + lane_base + c * 32, us);
         tmem_ld32(tmem + lane_base + 128 + c * 32, ud);
         tmem_ld_wait();
+        float4 nl4 = make_float4(0.f, 0.f, 0.f, 0.f), nd4 = nl4;
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
           const int col = c * 32 + k;
-          const float2 nl2 = *reinterpret_cast<const float2*>(nl_s + col);
-          const float2 nd2 = *reinterpret_cast<const float2*>(nd_s + col);
+          if ((k & 3) == 0) {
+            nl4 = *reinterpret_cast<const float4*>(nl_s + col);
+            nd4 = *reinterpret_cast<const float4*>(nd_s + col);
+          }
+          const float2 nl2 = (k & 3) ? make_float2(nl4.z, nl4.w) : make_float2(nl4.x, nl4.y);
+          const float2 nd2 = (k & 3) ? make_float2(nd4.z, nd4.w) : make_float2(nd4.x, nd4.y);
           float2 y = __ffma2_rn(make_float2(__uint_as_float(us[k]), __uint_as_float(us[k + 1])), sl2, nl2);
           if (part) {
             const int i = q0 + col;
@@ -627,19 +658,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float2 pr = make_float2(ex2(y.x), ex2(y.y));
           const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(ud[k]), __uint_as_float(ud[k + 1])), nd2));
-          pp[c * 16 + (k >> 1)] = pack_bf16x2(pr.x, pr.y);
-          dd[c * 16 + (k >> 1)] = pack_bf16x2(ds.x, ds.y);
+          pp[k >> 1] = pack_bf16x2(pr.x, pr.y);
+          dd[k >> 1] = pack_bf16x2(ds.x, ds.y);
         }
+        // P^T columns 16c..16c+15 lie in score columns this thread has read
+        tmem_st16(tmem + lane_base + c * 16, pp);
+        st_swizzled8(dst_tile, t, 4 * c + 0, make_uint4(dd[0], dd[1], dd[2], dd[3]));
+        st_swizzled8(dst_tile, t, 4 * c + 1, make_uint4(dd[4], dd[5], dd[6], dd[7]));
+        st_swizzled8(dst_tile, t, 4 * c + 2, make_uint4(dd[8], dd[9], dd[10], dd[11]));
+        st_swizzled8(dst_tile, t, 4 * c + 3, make_uint4(dd[12], dd[13], dd[14], dd[15]));
       }
-      if (j > 0 && !mbar_wait(&bars[C_PSF], (j - 1) & 1, abort_flag, p.err)) {
-        ok = false;
-        break;
-      }
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        st_swizzled8(pt_tile, t, c, make_uint4(pp[4 * c], pp[4 * c + 1], pp[4 * c + 2], pp[4 * c + 3]));
-        st_swizzled8(dst_tile, t, c, make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]));
-      }
+      tmem_st_wait();
       fence_proxy_async_smem();
       fence_before_sync();
       mbar_arrive(&bars[C_DR]);
@@ -675,29 +704,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = threadIdx.x - 128;    // query row = TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = run;
+    int ent = run ? list[0] : 0;
     for (int j = 0; ok && j < n_it; ++j) {
-      const int qt = list[j / p.G] >> 1;
+      const int qt = ent >> 1;
+      if (j + 1 < n_it) ent = list[(j + 1) / p.G];
       const int h = g * p.G + j % p.G;
       if (!mbar_wait(&bars[C_QD], j & 1, abort_flag, p.err)) {
         ok = false;
         break;
       }
       fence_after_sync();
-      float* dst = p.dq_acc + (((size_t)row0 + qt * 128 + t) * p.Hq + h) * 128;
+      // accumulator tile (r, h, qt) is stored [32 column quads][128 rows][4], so
+      // the 32 threads of a warp reduce into 512 contiguous bytes
+      float* dst = p.dq_acc + (((size_t)r * p.Hq + h) * p.NT + qt) * 16384 + 4 * t;
+      uint32_t u[128];
+      tmem_ld32(tmem + lane_base + 128, u);
+      tmem_ld32(tmem + lane_base + 160, u + 32);
+      tmem_ld32(tmem + lane_base + 192, u + 64);
+      tmem_ld32(tmem + lane_base + 224, u + 96);
+      tmem_ld_wait();
+      fence_before_sync();
+      mbar_arrive(&bars[C_SFREE]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_base + c * 32, u);
-        tmem_ld_wait();
-        if (c == 3) {
-          fence_before_sync();
-          mbar_arrive(&bars[C_SFREE]);
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          red_add_v4(dst + c * 32 + 4 * k, __uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1]),
-                     __uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3]));
-      }
+      for (int k = 0; k < 32; ++k)
+        red_add_v4(dst + 512 * k, __uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1]),
+                   __uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3]));
     }
   }
 
@@ -741,19 +772,25 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
   }
 }
 
-// dQ = bf16(scale * dQ_acc), 8 elements per thread.
-__global__ void __launch_bounds__(256) bwd_dq_finalize_kernel(const float* __restrict__ acc,
+// dQ = bf16(scale * dQ_acc).  One block per accumulator tile (row, head,
+// query tile), one thread per query row: 32 coalesced float4 reads, one
+// 256-byte row written.
+__global__ void __launch_bounds__(128) bwd_dq_finalize_kernel(const float* __restrict__ acc,
                                                               __nv_bfloat16* __restrict__ dq,
-                                                              size_t n8, float scale) {
-  for (size_t k = (size_t)blockIdx.x * blockDim.x + threadIdx.x; k < n8; k += (size_t)gridDim.x * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * k];
-    const float4 b = reinterpret_cast<const float4*>(acc)[2 * k + 1];
+                                                              int T, int Hq, int NT, float scale) {
+  const int tile = blockIdx.x, t = threadIdx.x;
+  const int qt = tile % NT, h = (tile / NT) % Hq, r = tile / (NT * Hq);
+  const float4* src = reinterpret_cast<const float4*>(acc + (size_t)tile * 16384) + t;
+  uint4* out = reinterpret_cast<uint4*>(dq + (((size_t)r * T + qt * 128 + t) * Hq + h) * 128);
+#pragma unroll
+  for (int k = 0; k < 32; k += 2) {
+    const float4 a = src[128 * k], b = src[128 * (k + 1)];
     uint4 v;
     v.x = pack_bf16x2(a.x * scale, a.y * scale);
     v.y = pack_bf16x2(a.z * scale, a.w * scale);
     v.z = pack_bf16x2(b.x * scale, b.y * scale);
     v.w = pack_bf16x2(b.z * scale, b.w * scale);
-    reinterpret_cast<uint4*>(dq)[k] = v;
+    out[k >> 1] = v;
   }
 }
 
@@ -829,13 +866,13 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
   p.err = a.err;
   static bool attr = false;
   if (!attr) {
-    e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  bwd_tc_kernel<<<(unsigned)(p.NT * p.R * p.Hkv), kThreads, kSmemLimit, s>>>(mq, mk, mv, mdo, p);
-  bwd_dq_finalize_kernel<<<2048, 256, 0, s>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n / 8,
-                                              a.scale);
+  bwd_tc_kernel<<<(unsigned)(p.NT * p.R * p.Hkv), kThreads, kBwdSmem, s>>>(mq, mk, mv, mdo, p);
+  bwd_dq_finalize_kernel<<<(unsigned)(a.R * a.Hq * p.NT), 128, 0, s>>>(
+      a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.T, a.Hq, p.NT, a.scale);
   return cudaGetLastError();
 }
 

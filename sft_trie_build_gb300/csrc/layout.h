@@ -13,7 +13,8 @@
 // fwd workspace: err (uint32) only.
 // bwd workspace: err, delta float32 [R][Hq][T] (Delta on the float32 path,
 // -Delta on the bf16 path), and for the bf16 path nlse2 float32 [R][Hq][T]
-// (-LSE * log2 e) and dq_acc float32 [R][T][Hq][D].
+// (-LSE * log2 e) and dq_acc float32, one 128 x 128 tile per (row, query
+// head, query tile), each tile stored [32 column quads][128 rows][4].
 #pragma once
 
 #include <cstddef>
