@@ -126,16 +126,13 @@ enum {
   B_COUNT = 16
 };
 
-// 12 warps = three full warpgroups; registers move from the control
-// warpgroup (TMA + MMA issue) to the math warpgroups with setmaxnreg, at the
-// head of each role's branch.  Forward: 384 x 168 at launch =
-// 256 x 216 (two softmax groups) + 128 x 72.  Backward: 128 x 240
-// (elementwise) + 128 x 168 (dQ drain, unchanged) + 128 x 72 <= 384 x 168.
-// Per SM sub-partition (warps w, w+4, w+8): 216+216+72 and 240+168+72 <= 512.
+// Forward: 12 warps = three full warpgroups; registers move from the control
+// warpgroup (TMA + MMA issue) to the two softmax warpgroups with setmaxnreg,
+// at the head of each role's branch: 384 x 168 at launch = 256 x 216 + 128 x 72,
+// and per SM sub-partition (warps w, w+4, w+8) 216 + 216 + 72 <= 512.
 constexpr int kThreads = 384;
-constexpr int kRegsAtLaunch = 168, kRegsMath = 216, kRegsCtl = 72, kRegsBwdMath = 208, kRegsBwdCtl = 128;
+constexpr int kRegsAtLaunch = 168, kRegsMath = 216, kRegsCtl = 72;
 static_assert(kThreads * kRegsAtLaunch >= 256 * kRegsMath + 128 * kRegsCtl, "register split");
-static_assert(kThreads * kRegsAtLaunch >= 128 * (kRegsBwdMath + kRegsAtLaunch + kRegsBwdCtl), "register split");
 
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -428,21 +425,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 //
 // Per CTA: (row r, kv head g, key tile kt).  The key tile's list of
 // non-empty query tiles, times the G query heads of the group, gives the
-// iterations j = (query tile, head).  Per iteration:
-//   MMA      S^T = K Q^T into TMEM columns 0..127 and dP^T = V dO^T into
-//            128..255 (keys on TMEM lanes); once P^T is in TMEM (over S^T) and
-//            dS^T in shared memory: dV += P^T dO (A from TMEM), dK += dS^T Q
-//            (both accumulated in TMEM over all iterations), then dQ_j = dS K
-//            into columns 128..255; S^T of the next iteration follows at once;
-//   warps 0-3  one thread per key j: p = 2^(s scale log2e - LSE_i log2e)
-//            (masked on PARTIAL tiles with the thread's own subtree_end[j]),
-//            dS = p (dP - Delta_i); P^T goes back to TMEM as packed bf16 pairs,
-//            dS^T to shared memory;
-//   warps 4-7  one thread per query: reads dQ_j from TMEM and adds it into the
-//            float32 accumulator with vector reductions;
-//   warp 8   TMA: K, V once; Q, dO, -LSE log2e and -Delta of each iteration
-//            through a two-stage ring;
-//   warp 9   MMA issue, TMEM owner.
+// iterations j = (query tile, head).  16 warps:
+//   warps 0-7   elementwise, one thread per key (= TMEM lane); warps 0-3 take
+//               query columns 0..63, warps 4-7 columns 64..127:
+//               p = 2^(s scale log2e - LSE_i log2e) (masked on PARTIAL tiles
+//               with the thread's own subtree_end[j]), dS = p (dP - Delta_i);
+//               P^T goes back to TMEM as packed bf16 pairs over the consumed
+//               score columns, dS^T to shared memory;
+//   warps 8-11  dQ drain, one thread per query: reads dQ_j from TMEM and adds
+//               it into the float32 accumulator with vector reductions;
+//   warp 12     TMA: K, V once; Q, dO, -LSE log2e and -Delta of each
+//               iteration through a two-stage ring;
+//   warp 13     MMA issue and TMEM owner: S^T = K Q^T (columns 0..127) and
+//               dP^T = V dO^T (128..255); after the elementwise pass
+//               dV += P^T dO (A from TMEM) and dK += dS^T Q (accumulated over
+//               all iterations in 256..383 and 384..511), then dQ_j = dS K into
+//               128..255; S^T of the next iteration follows at once.
 // dK (times scale) and dV leave TMEM once at the end.
 
 struct BwdParams {
@@ -470,8 +468,14 @@ constexpr int kBwdBigBytes = 7 * kTileBytes;
 constexpr int kBwdVecBytes = 2 * 2 * 128 * 4;  // per stage: -LSE log2e and -Delta, 128 each
 constexpr int kBwdSmem = kBwdBigBytes + kBwdVecBytes + kSmallBytes;
 static_assert(kBwdSmem <= kSmemLimit, "backward shared memory");
+// 16 warps x 128 registers at launch; the control warpgroup gives 64 of its
+// registers per thread to the two elementwise warpgroups (+32 each):
+// 128 x (160 + 160 + 128 + 64) = 65536, and per sub-partition 512.
+constexpr int kBwdThreads = 512;
+constexpr int kBwdRegsMath = 160, kBwdRegsCtl = 64;
+static_assert(128 * (2 * kBwdRegsMath + 128 + kBwdRegsCtl) <= kBwdThreads * 128, "register split");
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const BwdParams p) {
@@ -496,7 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int row0 = r * p.T;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < C_COUNT; ++b) mbar_init(&bars[b], (b == C_DR || b == C_SFREE) ? 128 : 1);
+    for (int b = 0; b < C_COUNT; ++b)
+      mbar_init(&bars[b], b == C_DR ? 256 : (b == C_SFREE ? 128 : 1));
     *abort_flag = 0;
     if ((big_s & 1023u) != 0 || cnt <= 0 || cnt > p.NT) {
       *abort_flag = 1;
@@ -504,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -513,13 +518,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const bool run = !*abort_flag;
-  // TMEM columns: S^T / P^T 0..127, dP^T / dQ 128..255, dV 256..383, dK 384..511
 
-  if (warp >= 8) {
-    regs_dec<kRegsBwdCtl>();
-  }
-  if (warp == 8) {
-    if (lane == 0 && run) {
+  if (warp >= 12) {
+    regs_dec<kBwdRegsCtl>();
+    if (warp == 12 && lane == 0 && run) {
+      // ---------------------------------------------------------- producer
       int issued_q[2] = {-1, -1};
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
@@ -531,6 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(big + kTileBytes + hf * kHalfTile, &tv, &bars[C_KV], hf * 64, g, row0 + kt * 128);
       }
       int ent = list[0];
+#pragma unroll 1
       for (int j = 0; j < n_it; ++j) {
         const int st = j & 1, n = j >> 1;
         const int qt = ent >> 1, h = g * p.G + j % p.G;
@@ -546,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t at = ((size_t)r * p.Hq + h) * p.T + qt * 128;
         bulk_load(vs, p.nlse2 + at, 512, &bars[C_QF + st]);
         bulk_load(vs + 128, p.ndelta + at, 512, &bars[C_QF + st]);
+#pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
           tma_load_3d(big + (2 + st) * kTileBytes + hf * kHalfTile, &tq, &bars[C_QF + st], hf * 64, h,
                       row0 + qt * 128);
@@ -557,66 +562,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(&bars[C_KV], 0);
       for (int st = 0; st < 2; ++st)
         if (issued_q[st] >= 0) mbar_wait_drain(&bars[C_QF + st], issued_q[st] & 1);
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    if (lane == 0 && run) {
+    } else if (warp == 13 && lane == 0 && run) {
+      // ---------------------------------------------------------- MMA issue
       constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
       constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // dV (A in TMEM), dK
       constexpr uint32_t id_nn = idesc_bf16(128, 128, 1, 1);  // dQ
       bool ok = mbar_wait(&bars[C_KV], 0, abort_flag, p.err);
-      // S^T of the first iteration
       if (ok && n_it > 0) {
         ok = mbar_wait(&bars[C_QF], 0, abort_flag, p.err);
         if (ok) {
           fence_after_sync();
+#pragma unroll 1
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem, kmajor_desc(k_s, kk), kmajor_desc(big_s + 2 * kTileBytes, kk), id_kk, kk > 0);
         }
       }
+#pragma unroll 1
       for (int j = 0; ok && j < n_it; ++j) {
         const int st = j & 1;
         const uint32_t q_s = big_s + (2 + st) * kTileBytes, do_s = big_s + (4 + st) * kTileBytes;
-        // dP^T into columns 128..255 once dQ_{j-1} has been read out of them
         if (j > 0 && !mbar_wait(&bars[C_SFREE], (j - 1) & 1, abort_flag, p.err)) break;
         fence_after_sync();
+#pragma unroll 1
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tmem + 128, kmajor_desc(v_s, kk), kmajor_desc(do_s, kk), id_kk, kk > 0);
         mma_commit(&bars[C_SF]);
         if (!mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err)) break;
         fence_after_sync();
+        // P^T of query columns 16 kk..16 kk+15: packed columns 8 kk (first
+        // half) or 64 + 8 (kk - 4) (second half)
+#pragma unroll 1
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + 256, tmem + kk * 8, mnmajor_desc(do_s, kk), id_kn, (j > 0 || kk > 0));
+          mma_ts(tmem + 256, tmem + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmajor_desc(do_s, kk), id_kn,
+                 (j > 0 || kk > 0));
+#pragma unroll 1
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tmem + 384, kmajor_desc(dst_s, kk), mnmajor_desc(q_s, kk), id_kn, (j > 0 || kk > 0));
         mma_commit(&bars[C_QE + st]);
+#pragma unroll 1
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tmem + 128, mnmajor_desc(dst_s, kk), mnmajor_desc(k_s, kk), id_nn, kk > 0);
         mma_commit(&bars[C_QD]);
         mma_commit(&bars[C_PSF]);
-        // S^T of the next iteration (P^T_j in columns 0..127 is consumed by dV above)
         if (j + 1 < n_it) {
           const int st1 = (j + 1) & 1;
           if (!mbar_wait(&bars[C_QF + st1], ((j + 1) >> 1) & 1, abort_flag, p.err)) break;
           fence_after_sync();
+#pragma unroll 1
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem, kmajor_desc(k_s, kk), kmajor_desc(big_s + (2 + st1) * kTileBytes, kk), id_kk, kk > 0);
         }
       }
       if (ok) mma_commit(&bars[C_DONE]);
-    }
-    if (lane == 0 && run) {
       mma_commit(&bars[C_DRAIN]);
       mbar_wait_drain(&bars[C_DRAIN], 0);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------ per-key elementwise
-    regs_inc<kRegsBwdMath>();
-    const int t = threadIdx.x;          // key row = TMEM lane
-    const int jk = kt * 128 + t;        // key index in the row
+    regs_inc<kBwdRegsMath>();
+    const int half = warp >> 2;          // query columns 64 half .. 64 half + 63
+    const int t = threadIdx.x & 127;     // key row = TMEM lane
+    const int jk = kt * 128 + t;         // key index in the row
     const int se_j = p.se[(size_t)row0 + jk];
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_col = lane_base + half * 64, dp_col = lane_base + 128 + half * 64;
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
     bool ok = run;
     int ent = run ? list[0] : 0;
@@ -624,9 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = j & 1;
       const int qt = ent >> 1, part = ent & 1;
       if (j + 1 < n_it) ent = list[(j + 1) / p.G];
-      const int q0 = qt * 128;
-      const float* nl_s = vec + st * 256;   // -LSE log2 e per query column
-      const float* nd_s = nl_s + 128;       // -Delta per query column
+      const int q0 = qt * 128 + half * 64;
+      const float* nl_s = vec + st * 256 + half * 64;   // -LSE log2 e per query column
+      const float* nd_s = nl_s + 128;                   // -Delta per query column
       if (!mbar_wait(&bars[C_QF + st], (j >> 1) & 1, abort_flag, p.err) ||
           !mbar_wait(&bars[C_SF], j & 1, abort_flag, p.err) ||
           (j > 0 && !mbar_wait(&bars[C_PSF], (j - 1) & 1, abort_flag, p.err))) {
@@ -635,10 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_after_sync();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t us[32], ud[32], pp[16], dd[16];
-        tmem_ld32(tmem + lane_base + c * 32, us);
-        tmem_ld32(tmem + lane_base + 128 + c * 32, ud);
+        tmem_ld32(tmem + s_col + c * 32, us);
+        tmem_ld32(tmem + dp_col + c * 32, ud);
         tmem_ld_wait();
         float4 nl4 = make_float4(0.f, 0.f, 0.f, 0.f), nd4 = nl4;
 #pragma unroll
@@ -661,12 +671,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           pp[k >> 1] = pack_bf16x2(pr.x, pr.y);
           dd[k >> 1] = pack_bf16x2(ds.x, ds.y);
         }
-        // P^T columns 16c..16c+15 lie in score columns this thread has read
-        tmem_st16(tmem + lane_base + c * 16, pp);
-        st_swizzled8(dst_tile, t, 4 * c + 0, make_uint4(dd[0], dd[1], dd[2], dd[3]));
-        st_swizzled8(dst_tile, t, 4 * c + 1, make_uint4(dd[4], dd[5], dd[6], dd[7]));
-        st_swizzled8(dst_tile, t, 4 * c + 2, make_uint4(dd[8], dd[9], dd[10], dd[11]));
-        st_swizzled8(dst_tile, t, 4 * c + 3, make_uint4(dd[12], dd[13], dd[14], dd[15]));
+        // packed P^T columns 16c..16c+15 of this half lie in score columns
+        // this warp has already read
+        tmem_st16(tmem + s_col + c * 16, pp);
+        const int cb = half * 8 + 4 * c;   // 16-byte chunk index of dS^T row t
+        st_swizzled8(dst_tile, t, cb + 0, make_uint4(dd[0], dd[1], dd[2], dd[3]));
+        st_swizzled8(dst_tile, t, cb + 1, make_uint4(dd[4], dd[5], dd[6], dd[7]));
+        st_swizzled8(dst_tile, t, cb + 2, make_uint4(dd[8], dd[9], dd[10], dd[11]));
+        st_swizzled8(dst_tile, t, cb + 3, make_uint4(dd[12], dd[13], dd[14], dd[15]));
       }
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -675,33 +687,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && mbar_wait(&bars[C_DONE], 0, abort_flag, p.err)) {
       fence_after_sync();
-      __nv_bfloat16* dvr = p.dv + (((size_t)row0 + jk) * p.Hkv + g) * 128;
-      __nv_bfloat16* dkr = p.dk + (((size_t)row0 + jk) * p.Hkv + g) * 128;
+      // warps 0-3 write dV, warps 4-7 dK (times scale)
+      const bool is_dv = half == 0;
+      __nv_bfloat16* dst = (is_dv ? p.dv : p.dk) + (((size_t)row0 + jk) * p.Hkv + g) * 128;
+      const float sc = is_dv ? 1.f : p.scale;
+      const uint32_t col0 = lane_base + (is_dv ? 256 : 384);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t uv[32], uk[32];
-        tmem_ld32(tmem + lane_base + 256 + c * 32, uv);
-        tmem_ld32(tmem + lane_base + 384 + c * 32, uk);
+        uint32_t u[32];
+        tmem_ld32(tmem + col0 + c * 32, u);
         tmem_ld_wait();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          uint4 a, b;
-          a.x = pack_bf16x2(__uint_as_float(uv[8 * k + 0]), __uint_as_float(uv[8 * k + 1]));
-          a.y = pack_bf16x2(__uint_as_float(uv[8 * k + 2]), __uint_as_float(uv[8 * k + 3]));
-          a.z = pack_bf16x2(__uint_as_float(uv[8 * k + 4]), __uint_as_float(uv[8 * k + 5]));
-          a.w = pack_bf16x2(__uint_as_float(uv[8 * k + 6]), __uint_as_float(uv[8 * k + 7]));
-          b.x = pack_bf16x2(__uint_as_float(uk[8 * k + 0]) * p.scale, __uint_as_float(uk[8 * k + 1]) * p.scale);
-          b.y = pack_bf16x2(__uint_as_float(uk[8 * k + 2]) * p.scale, __uint_as_float(uk[8 * k + 3]) * p.scale);
-          b.z = pack_bf16x2(__uint_as_float(uk[8 * k + 4]) * p.scale, __uint_as_float(uk[8 * k + 5]) * p.scale);
-          b.w = pack_bf16x2(__uint_as_float(uk[8 * k + 6]) * p.scale, __uint_as_float(uk[8 * k + 7]) * p.scale);
-          *reinterpret_cast<uint4*>(dvr + c * 32 + 8 * k) = a;
-          *reinterpret_cast<uint4*>(dkr + c * 32 + 8 * k) = b;
+          uint4 a;
+          a.x = pack_bf16x2(__uint_as_float(u[8 * k + 0]) * sc, __uint_as_float(u[8 * k + 1]) * sc);
+          a.y = pack_bf16x2(__uint_as_float(u[8 * k + 2]) * sc, __uint_as_float(u[8 * k + 3]) * sc);
+          a.z = pack_bf16x2(__uint_as_float(u[8 * k + 4]) * sc, __uint_as_float(u[8 * k + 5]) * sc);
+          a.w = pack_bf16x2(__uint_as_float(u[8 * k + 6]) * sc, __uint_as_float(u[8 * k + 7]) * sc);
+          *reinterpret_cast<uint4*>(dst + c * 32 + 8 * k) = a;
         }
       }
     }
-  } else if (warp < 8) {
+  } else {
     // ------------------------------------------------ dQ drain (per query)
-    const int t = threadIdx.x - 128;    // query row = TMEM lane
+    const int t = threadIdx.x & 127;    // query row = TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = run;
     int ent = run ? list[0] : 0;
@@ -717,18 +726,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // accumulator tile (r, h, qt) is stored [32 column quads][128 rows][4], so
       // the 32 threads of a warp reduce into 512 contiguous bytes
       float* dst = p.dq_acc + (((size_t)r * p.Hq + h) * p.NT + qt) * 16384 + 4 * t;
-      uint32_t u[128];
+      uint32_t u[64], w[64];
       tmem_ld32(tmem + lane_base + 128, u);
       tmem_ld32(tmem + lane_base + 160, u + 32);
-      tmem_ld32(tmem + lane_base + 192, u + 64);
-      tmem_ld32(tmem + lane_base + 224, u + 96);
+      tmem_ld32(tmem + lane_base + 192, w);
+      tmem_ld32(tmem + lane_base + 224, w + 32);
       tmem_ld_wait();
       fence_before_sync();
       mbar_arrive(&bars[C_SFREE]);
 #pragma unroll
-      for (int k = 0; k < 32; ++k)
+      for (int k = 0; k < 16; ++k)
         red_add_v4(dst + 512 * k, __uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1]),
                    __uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3]));
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        red_add_v4(dst + 512 * (16 + k), __uint_as_float(w[4 * k]), __uint_as_float(w[4 * k + 1]),
+                   __uint_as_float(w[4 * k + 2]), __uint_as_float(w[4 * k + 3]));
     }
   }
 
@@ -736,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 9) tmem_dealloc(tmem, 512);
+  if (warp == 13) tmem_dealloc(tmem, 512);
 }
 
 // Delta[r,h,i] = sum_d dO . O (bf16 in, f32 out); one warp per (row, token, head).
@@ -870,7 +883,7 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  bwd_tc_kernel<<<(unsigned)(p.NT * p.R * p.Hkv), kThreads, kBwdSmem, s>>>(mq, mk, mv, mdo, p);
+  bwd_tc_kernel<<<(unsigned)(p.NT * p.R * p.Hkv), kBwdThreads, kBwdSmem, s>>>(mq, mk, mv, mdo, p);
   bwd_dq_finalize_kernel<<<(unsigned)(a.R * a.Hq * p.NT), 128, 0, s>>>(
       a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.T, a.Hq, p.NT, a.scale);
   return cudaGetLastError();

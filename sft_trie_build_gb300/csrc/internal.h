@@ -4,7 +4,7 @@
 #include <cstdarg>
 #include <cstdint>
 
-#include "../../include/stp.h"
+#include "stp.h"
 
 namespace stp {
 
