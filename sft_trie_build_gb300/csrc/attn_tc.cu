@@ -468,12 +468,12 @@ constexpr int kBwdBigBytes = 7 * kTileBytes;
 constexpr int kBwdVecBytes = 2 * 2 * 128 * 4;  // per stage: -LSE log2e and -Delta, 128 each
 constexpr int kBwdSmem = kBwdBigBytes + kBwdVecBytes + kSmallBytes;
 static_assert(kBwdSmem <= kSmemLimit, "backward shared memory");
-// 16 warps x 128 registers at launch; the control warpgroup gives 64 of its
-// registers per thread to the two elementwise warpgroups (+32 each):
-// 128 x (160 + 160 + 128 + 64) = 65536, and per sub-partition 512.
+// 16 warps x 128 registers at launch, rebalanced with setmaxnreg:
+// 128 x (152 + 152 (elementwise) + 136 (dQ drain) + 72 (control)) = 65536,
+// and per SM sub-partition (warps w, w+4, w+8, w+12) 512.
 constexpr int kBwdThreads = 512;
-constexpr int kBwdRegsMath = 160, kBwdRegsCtl = 64;
-static_assert(128 * (2 * kBwdRegsMath + 128 + kBwdRegsCtl) <= kBwdThreads * 128, "register split");
+constexpr int kBwdRegsMath = 152, kBwdRegsDrain = 136, kBwdRegsCtl = 72;
+static_assert(128 * (2 * kBwdRegsMath + kBwdRegsDrain + kBwdRegsCtl) <= kBwdThreads * 128, "register split");
 
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -567,50 +567,52 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
       constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // dV (A in TMEM), dK
       constexpr uint32_t id_nn = idesc_bf16(128, 128, 1, 1);  // dQ
+      // descriptor low words; slice kk adds a constant to the start-address field
+      const uint32_t k_km = desc_lo_kmajor(k_s), v_km = desc_lo_kmajor(v_s), k_mn = desc_lo_mnmajor(k_s);
+      const uint32_t ds_km = desc_lo_kmajor(dst_s), ds_mn = desc_lo_mnmajor(dst_s);
+      const uint32_t q_km0 = desc_lo_kmajor(big_s + 2 * kTileBytes), do_km0 = desc_lo_kmajor(big_s + 4 * kTileBytes);
+      const uint32_t q_mn0 = desc_lo_mnmajor(big_s + 2 * kTileBytes), do_mn0 = desc_lo_mnmajor(big_s + 4 * kTileBytes);
+      constexpr uint32_t kStage = kTileBytes >> 4;  // one tile further in the ring
+      auto km = [](int kk) { return (uint32_t)((kk >> 2) * (kHalfTile >> 4) + (kk & 3) * 2); };
+      auto mn = [](int kk) { return (uint32_t)(kk * 128); };
       bool ok = mbar_wait(&bars[C_KV], 0, abort_flag, p.err);
       if (ok && n_it > 0) {
         ok = mbar_wait(&bars[C_QF], 0, abort_flag, p.err);
         if (ok) {
           fence_after_sync();
-#pragma unroll 1
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem, kmajor_desc(k_s, kk), kmajor_desc(big_s + 2 * kTileBytes, kk), id_kk, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, k_km + km(kk), q_km0 + km(kk), id_kk, kk > 0);
         }
       }
 #pragma unroll 1
       for (int j = 0; ok && j < n_it; ++j) {
-        const int st = j & 1;
-        const uint32_t q_s = big_s + (2 + st) * kTileBytes, do_s = big_s + (4 + st) * kTileBytes;
+        const uint32_t so = (j & 1) ? kStage : 0;
+        const uint32_t do_km = do_km0 + so, q_mn = q_mn0 + so, do_mn = do_mn0 + so;
         if (j > 0 && !mbar_wait(&bars[C_SFREE], (j - 1) & 1, abort_flag, p.err)) break;
         fence_after_sync();
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + 128, kmajor_desc(v_s, kk), kmajor_desc(do_s, kk), id_kk, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km + km(kk), id_kk, kk > 0);
         mma_commit(&bars[C_SF]);
         if (!mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err)) break;
         fence_after_sync();
         // P^T of query columns 16 kk..16 kk+15: packed columns 8 kk (first
         // half) or 64 + 8 (kk - 4) (second half)
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + 256, tmem + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmajor_desc(do_s, kk), id_kn,
-                 (j > 0 || kk > 0));
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + 384, kmajor_desc(dst_s, kk), mnmajor_desc(q_s, kk), id_kn, (j > 0 || kk > 0));
-        mma_commit(&bars[C_QE + st]);
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + 128, mnmajor_desc(dst_s, kk), mnmajor_desc(k_s, kk), id_nn, kk > 0);
+          mma_ts_lo(tmem + 256, tmem + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), do_mn + mn(kk), id_kn, (j > 0 || kk > 0));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 384, ds_km + km(kk), q_mn + mn(kk), id_kn, (j > 0 || kk > 0));
+        mma_commit(&bars[C_QE + (j & 1)]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, ds_mn + mn(kk), k_mn + mn(kk), id_nn, kk > 0);
         mma_commit(&bars[C_QD]);
         mma_commit(&bars[C_PSF]);
         if (j + 1 < n_it) {
-          const int st1 = (j + 1) & 1;
-          if (!mbar_wait(&bars[C_QF + st1], ((j + 1) >> 1) & 1, abort_flag, p.err)) break;
+          if (!mbar_wait(&bars[C_QF + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, p.err)) break;
           fence_after_sync();
-#pragma unroll 1
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem, kmajor_desc(k_s, kk), kmajor_desc(big_s + (2 + st1) * kTileBytes, kk), id_kk, kk > 0);
+          const uint32_t q_next = q_km0 + ((j & 1) ? 0 : kStage);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, k_km + km(kk), q_next + km(kk), id_kk, kk > 0);
         }
       }
       if (ok) mma_commit(&bars[C_DONE]);
@@ -644,41 +646,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       fence_after_sync();
+      // all 64 score and 64 dP columns of this half with one TMEM wait
+      uint32_t us[64], ud[64];
+      tmem_ld32(tmem + s_col, us);
+      tmem_ld32(tmem + s_col + 32, us + 32);
+      tmem_ld32(tmem + dp_col, ud);
+      tmem_ld32(tmem + dp_col + 32, ud + 32);
+      tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t us[32], ud[32], pp[16], dd[16];
-        tmem_ld32(tmem + s_col + c * 32, us);
-        tmem_ld32(tmem + dp_col + c * 32, ud);
-        tmem_ld_wait();
-        float4 nl4 = make_float4(0.f, 0.f, 0.f, 0.f), nd4 = nl4;
+      for (int c = 0; c < 4; ++c) {       // 16 query columns at a time
+        uint32_t pp[8], dd[8];
 #pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const int col = c * 32 + k;
-          if ((k & 3) == 0) {
-            nl4 = *reinterpret_cast<const float4*>(nl_s + col);
-            nd4 = *reinterpret_cast<const float4*>(nd_s + col);
+        for (int k = 0; k < 16; k += 4) {
+          const int col = c * 16 + k;
+          const float4 nl4 = *reinterpret_cast<const float4*>(nl_s + col);
+          const float4 nd4 = *reinterpret_cast<const float4*>(nd_s + col);
+#pragma unroll
+          for (int u2 = 0; u2 < 2; ++u2) {
+            const int cc = col + 2 * u2;
+            const float2 nl2 = u2 ? make_float2(nl4.z, nl4.w) : make_float2(nl4.x, nl4.y);
+            const float2 nd2 = u2 ? make_float2(nd4.z, nd4.w) : make_float2(nd4.x, nd4.y);
+            float2 y = __ffma2_rn(make_float2(__uint_as_float(us[cc]), __uint_as_float(us[cc + 1])), sl2, nl2);
+            if (part) {
+              const int i = q0 + cc;
+              if (!(jk <= i && se_j >= i)) y.x = -INFINITY;
+              if (!(jk <= i + 1 && se_j >= i + 1)) y.y = -INFINITY;
+            }
+            const float2 pr = make_float2(ex2(y.x), ex2(y.y));
+            const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(ud[cc]), __uint_as_float(ud[cc + 1])), nd2));
+            pp[(k >> 1) + u2] = pack_bf16x2(pr.x, pr.y);
+            dd[(k >> 1) + u2] = pack_bf16x2(ds.x, ds.y);
           }
-          const float2 nl2 = (k & 3) ? make_float2(nl4.z, nl4.w) : make_float2(nl4.x, nl4.y);
-          const float2 nd2 = (k & 3) ? make_float2(nd4.z, nd4.w) : make_float2(nd4.x, nd4.y);
-          float2 y = __ffma2_rn(make_float2(__uint_as_float(us[k]), __uint_as_float(us[k + 1])), sl2, nl2);
-          if (part) {
-            const int i = q0 + col;
-            if (!(jk <= i && se_j >= i)) y.x = -INFINITY;
-            if (!(jk <= i + 1 && se_j >= i + 1)) y.y = -INFINITY;
-          }
-          const float2 pr = make_float2(ex2(y.x), ex2(y.y));
-          const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(ud[k]), __uint_as_float(ud[k + 1])), nd2));
-          pp[k >> 1] = pack_bf16x2(pr.x, pr.y);
-          dd[k >> 1] = pack_bf16x2(ds.x, ds.y);
         }
-        // packed P^T columns 16c..16c+15 of this half lie in score columns
-        // this warp has already read
-        tmem_st16(tmem + s_col + c * 16, pp);
-        const int cb = half * 8 + 4 * c;   // 16-byte chunk index of dS^T row t
+        // packed P^T columns 8c..8c+7 of this half lie in score columns
+        // already read
+        tmem_st8(tmem + s_col + c * 8, pp);
+        const int cb = half * 8 + 2 * c;   // 16-byte chunk index of dS^T row t
         st_swizzled8(dst_tile, t, cb + 0, make_uint4(dd[0], dd[1], dd[2], dd[3]));
         st_swizzled8(dst_tile, t, cb + 1, make_uint4(dd[4], dd[5], dd[6], dd[7]));
-        st_swizzled8(dst_tile, t, cb + 2, make_uint4(dd[8], dd[9], dd[10], dd[11]));
-        st_swizzled8(dst_tile, t, cb + 3, make_uint4(dd[12], dd[13], dd[14], dd[15]));
       }
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -710,6 +715,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------------ dQ drain (per query)
+    if (kBwdRegsDrain > 128) regs_inc<kBwdRegsDrain>();
+    if (kBwdRegsDrain < 128) regs_dec<kBwdRegsDrain>();
     const int t = threadIdx.x & 127;    // query row = TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = run;
