@@ -150,6 +150,7 @@ struct Walker {
       for (size_t k = 1; k < S.size() && A > 0; ++k) {
         const int32_t* o = tok + off[S[k]] + w.start;
         int64_t a = 0;
+        while (a + 16 <= A && std::memcmp(o + a, ref + a, 16 * sizeof(int32_t)) == 0) a += 16;
         while (a < A && o[a] == ref[a]) ++a;
         A = a;
       }
@@ -176,6 +177,18 @@ struct Walker {
     }
   }
 };
+
+// Number of leading zero bytes of [p, p + n), eight bytes at a time.
+int64_t leading_zero_bytes(const uint8_t* p, int64_t n) {
+  int64_t k = 0;
+  for (; k + 8 <= n; k += 8) {
+    uint64_t w;
+    std::memcpy(&w, p + k, 8);
+    if (w) break;
+  }
+  while (k < n && !p[k]) ++k;
+  return k;
+}
 
 }  // namespace
 
@@ -280,13 +293,7 @@ stp_status stp_pack(const int32_t* tokens, const int64_t* offsets, int32_t n_seq
     w.leaf_of.assign(n_seqs, -1);
     for (int32_t s = 0; s < n_seqs; ++s) {
       w.len[s] = offsets[s + 1] - offsets[s];
-      int64_t k = 0;
-      if (w.tr) {
-        while (k < w.len[s] && !w.tr[offsets[s] + k]) ++k;
-      } else {
-        k = w.len[s];
-      }
-      w.ntr[s] = k;
+      w.ntr[s] = w.tr ? leading_zero_bytes(w.tr + offsets[s], w.len[s]) : w.len[s];
     }
     if (n_seqs > 0) {
       if (flags & STP_PER_FAMILY) {
@@ -395,6 +402,8 @@ stp_status stp_plan_write(const stp_plan* P, int32_t* token_ids, int32_t* positi
   const int64_t T = P->T;
   const size_t nseg = P->segs.size();
   std::vector<int64_t> start(nseg, -1), last(nseg, -1);
+  std::vector<uint8_t> is_leaf(nseg, 0);
+  for (int32_t x : P->leaf_of) is_leaf[x] = 1;
   const uint8_t* tr = P->trainable.empty() ? nullptr : P->trainable.data();
   for (size_t r = 0; r < P->bins.size(); ++r) {
     const Bin& b = P->bins[r];
@@ -405,12 +414,10 @@ stp_status stp_plan_write(const stp_plan* P, int32_t* token_ids, int32_t* positi
       const int64_t n = sg.hi - sg.lo;
       start[x] = cur;
       last[x] = n > 0 ? cur + n - 1 : -1;
-      const int32_t* src = P->tokens.data() + P->offsets[sg.rep] + sg.lo;
-      for (int64_t k = 0; k < n; ++k) {
-        if (token_ids) token_ids[base + cur + k] = src[k];
-        if (position_ids) position_ids[base + cur + k] = (int32_t)(sg.lo + k);
-        if (loss_mask) loss_mask[base + cur + k] = 0;
-      }
+      if (token_ids && n > 0)
+        std::memcpy(token_ids + base + cur, P->tokens.data() + P->offsets[sg.rep] + sg.lo, n * sizeof(int32_t));
+      if (position_ids)
+        for (int64_t k = 0; k < n; ++k) position_ids[base + cur + k] = (int32_t)(sg.lo + k);
       cur += n;
     }
     // exit index: children follow their parent in pre-order, so one reverse
@@ -423,23 +430,27 @@ stp_status stp_plan_write(const stp_plan* P, int32_t* token_ids, int32_t* positi
     if (subtree_end) {
       for (int32_t x : b.segs) {
         const int64_t n = P->segs[x].hi - P->segs[x].lo;
-        for (int64_t k = 0; k < n; ++k) subtree_end[base + start[x] + k] = (int32_t)last[x];
+        std::fill(subtree_end + base + start[x], subtree_end + base + start[x] + n, (int32_t)last[x]);
       }
       for (int64_t j = cur; j < T; ++j) subtree_end[base + j] = (int32_t)j;
     }
-    for (int64_t j = cur; j < T; ++j) {
-      if (token_ids) token_ids[base + j] = 0;
-      if (position_ids) position_ids[base + j] = 0;
-      if (loss_mask) loss_mask[base + j] = 0;
-    }
+    if (token_ids) std::fill(token_ids + base + cur, token_ids + base + T, 0);
+    if (position_ids) std::fill(position_ids + base + cur, position_ids + base + T, 0);
+    if (loss_mask) std::memset(loss_mask + base, 0, (size_t)T);
     for (int32_t s : b.leaves) {
       const int64_t o = P->offsets[s], L = P->offsets[s + 1] - o;
       for (int32_t x = P->leaf_of[s]; x >= 0; x = P->segs[x].parent) {
         const Segment& sg = P->segs[x];
-        for (int64_t p = sg.lo; p < sg.hi; ++p) {
-          const int64_t flat = base + start[x] + (p - sg.lo);
-          if (gather_index) gather_index[o + p] = flat;
-          if (loss_mask && tr && p + 1 < L && tr[o + p + 1]) loss_mask[flat] = 1;
+        const int64_t flat0 = base + start[x] - sg.lo;  // row-major index of position p is flat0 + p
+        if (gather_index)
+          for (int64_t p = sg.lo; p < sg.hi; ++p) gather_index[o + p] = flat0 + p;
+        // a loss position is one whose next token is trainable; the walk ends
+        // every shared segment before a trainable token, so only the leaf's
+        // own segment can hold one
+        if (loss_mask && tr && is_leaf[x]) {
+          const int64_t hi = std::min<int64_t>(sg.hi, L - 1);
+          for (int64_t p = sg.lo; p < hi; ++p)
+            if (tr[o + p + 1]) loss_mask[flat0 + p] = 1;
         }
       }
     }
