@@ -8,7 +8,7 @@
 //   warp 8      TMA producer: Q tiles once, then K / V tiles of the query
 //               tile's list through a 2-stage ring;
 //   warp 9      MMA issuer: S_h = Q_h K^T (M=N=128, K=128) into TMEM, then
-//               O_h += P V (P from shared memory, V as an MN-major operand);
+//               O_h += P_h V (P_h read from TMEM, V an MN-major operand);
 //               owns the TMEM allocation (512 columns: S_0, S_1, O_0, O_1);
 //   warps 0-3   softmax for head slot 0, warps 4-7 for head slot 1: one thread
 //               per query row (= TMEM lane); the predicate
@@ -16,10 +16,10 @@
 //               online softmax in base 2; O is rescaled in TMEM only when the
 //               running max grows by more than 2^8 (exact: numerator and
 //               denominator keep the same reference max).
-// The two softmax groups share one P buffer: head 0 writes P(e) after PV_1(e-1)
-// has read it, head 1 after PV_0(e); the MMA warp issues PV_0(e), S_0(e+1),
-// PV_1(e), S_1(e+1) so the tensor core works on one head while the other's
-// softmax runs.
+// Each softmax group writes its P as packed bf16 pairs over the first 64
+// columns of its own S; the MMA warp issues PV_0(e), S_0(e+1), PV_1(e),
+// S_1(e+1), so the tensor core works on one head while the other's softmax
+// runs.
 // Every mbarrier wait is bounded; a wait that runs out sets the workspace
 // error word, the CTA drains its outstanding copies and MMAs, frees TMEM and
 // returns.
@@ -46,7 +46,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile
 constexpr int kHalfTile = kTileBytes / 2;  // one 128-row x 64-column swizzled block
 constexpr int kSmallBytes = 256;           // barriers, TMEM slot, abort flag
-constexpr int kFwdBigBytes = 7 * kTileBytes;  // Q0 Q1 K0 K1 V0 V1 P
+constexpr int kFwdBigBytes = 6 * kTileBytes;  // Q0 Q1 K0 K1 V0 V1
 constexpr int kSmemLimit = 232448;
 
 // ------------------------------------------------------------------------
@@ -191,8 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t q_s[2] = {big_s, big_s + kTileBytes};
   uint32_t k_s[2] = {big_s + 2 * kTileBytes, big_s + 3 * kTileBytes};
   uint32_t v_s[2] = {big_s + 4 * kTileBytes, big_s + 5 * kTileBytes};
-  const uint32_t p_s = big_s + 6 * kTileBytes;
-  uint8_t* p_tile = big + 6 * kTileBytes;
 
   int issued_k[2] = {-1, -1};  // producer: last issued use of each stage
   int issued_v[2] = {-1, -1};
@@ -245,41 +243,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && run) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16(128, 128, 0, 1);
+      // descriptor low words; slice kk adds a constant to the start-address field
+      const uint32_t q_km0 = desc_lo_kmajor(q_s[0]), q_km1 = desc_lo_kmajor(q_s[1]);
+      const uint32_t k_km0 = desc_lo_kmajor(k_s[0]), v_mn0 = desc_lo_mnmajor(v_s[0]);
+      constexpr uint32_t kStage = kTileBytes >> 4;
+      auto km = [](int kk) { return (uint32_t)((kk >> 2) * (kHalfTile >> 4) + (kk & 3) * 2); };
+      auto mn = [](int kk) { return (uint32_t)(kk * 128); };
       bool ok = mbar_wait(&bars[B_Q], 0, abort_flag, p.err) &&
                 mbar_wait(&bars[B_KF], 0, abort_flag, p.err);
       if (ok) {
         fence_after_sync();
-        for (int hs = 0; hs < nh; ++hs) {
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + hs * 128, kmajor_desc(q_s[hs], kk), kmajor_desc(k_s[0], kk), idesc_s,
-                   kk > 0);
-          mma_commit(&bars[B_SF + hs]);
+#pragma unroll
+        for (int hs = 0; hs < 2; ++hs) {
+          if (hs < nh) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss_lo(tmem + hs * 128, (hs ? q_km1 : q_km0) + km(kk), k_km0 + km(kk), idesc_s, kk > 0);
+            mma_commit(&bars[B_SF + hs]);
+          }
         }
         mma_commit(&bars[B_KE]);
       }
+#pragma unroll 1
       for (int e = 0; ok && e < cnt; ++e) {
         const int st = e & 1, n = e >> 1;
         const int st1 = (e + 1) & 1, n1 = (e + 1) >> 1;
+        const uint32_t v_mn = v_mn0 + (st ? kStage : 0);
+        const uint32_t k_next = k_km0 + (st1 ? kStage : 0);
         if (!mbar_wait(&bars[B_VF + st], n & 1, abort_flag, p.err)) break;
-        for (int hs = 0; hs < nh && ok; ++hs) {
+#pragma unroll
+        for (int hs = 0; hs < 2; ++hs) {
+          if (hs >= nh || !ok) continue;
           if (!mbar_wait(&bars[B_PF + hs], e & 1, abort_flag, p.err)) {
             ok = false;
-            break;
+            continue;
           }
           fence_after_sync();
+          // O_hs += P_hs V: P_hs is packed bf16 in TMEM over the first 64
+          // columns of S_hs
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tmem + 256 + hs * 128, kmajor_desc(p_s, kk), mnmajor_desc(v_s[st], kk), idesc_o,
-                   (e > 0 || kk > 0));
+            mma_ts_lo(tmem + 256 + hs * 128, tmem + hs * 128 + kk * 8, v_mn + mn(kk), idesc_o, (e > 0 || kk > 0));
           mma_commit(&bars[B_OD + hs]);
           if (e + 1 < cnt) {
             if (hs == 0 && !mbar_wait(&bars[B_KF + st1], n1 & 1, abort_flag, p.err)) {
               ok = false;
-              break;
+              continue;
             }
             fence_after_sync();
+#pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tmem + hs * 128, kmajor_desc(q_s[hs], kk), kmajor_desc(k_s[st1], kk),
-                     idesc_s, kk > 0);
+              mma_ss_lo(tmem + hs * 128, (hs ? q_km1 : q_km0) + km(kk), k_next + km(kk), idesc_s, kk > 0);
             mma_commit(&bars[B_SF + hs]);
             if (hs == nh - 1) mma_commit(&bars[B_KE + st1]);
           }
@@ -353,22 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[c] = pack_bf16x2(pr.x, pr.y);
       }
       const float rs = acc2.x + acc2.y;
-      // the P buffer is free and O_hs stable once the previous reader of P is done
-      if (nh == 2) {
-        if (hs == 0) {
-          if (e > 0 && !mbar_wait(&bars[B_OD + 1], (e - 1) & 1, abort_flag, p.err)) ok = false;
-        } else {
-          if (!mbar_wait(&bars[B_OD + 0], e & 1, abort_flag, p.err)) ok = false;
-        }
-      } else if (e > 0 && !mbar_wait(&bars[B_OD + 0], (e - 1) & 1, abort_flag, p.err)) {
-        ok = false;
-      }
-      if (!ok) break;
-      fence_after_sync();
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_swizzled8(p_tile, row, c, make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-      fence_proxy_async_smem();
+      // P goes back over the first 64 score columns (already read).  PV of the
+      // previous tile, which read the old P and wrote O, completed before this
+      // tile's S (issued after it), so both may be overwritten now.
+      tmem_st32(s_addr, pk);
+      tmem_st32(s_addr + 32, pk + 32);
       if (e > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         uint32_t u[32];
 #pragma unroll
@@ -379,8 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 32; ++k) u[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
           tmem_st32(o_addr + c * 32, u);
         }
-        tmem_st_wait();
       }
+      tmem_st_wait();
       l_run = l_run * alpha + rs;
       m_run = m_use;
       fence_before_sync();
