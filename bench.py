@@ -35,6 +35,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from sft_trie_build_gb300 import workloads as W  # noqa: E402
+from sft_trie_build_gb300.shard import max_over_ranks, rank_seed  # noqa: E402
 
 WORKLOAD = "grpo"
 WORKLOAD_DESC = ("one GRPO group: 5000-token non-trainable system prefix + 16 trainable rollouts "
@@ -52,8 +53,8 @@ def _peaks():
         return 1900.0, 6800.0, "fallback"
 
 
-def _batch(seed_offset=0):
-    return W.grpo(W.CONFIG_SEEDS[WORKLOAD] + seed_offset)
+def _batch(rank=0):
+    return W.grpo(rank_seed(W.CONFIG_SEEDS[WORKLOAD], rank))
 
 
 class ClockSampler:
@@ -187,7 +188,7 @@ def main():
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
 
-    b = _batch(seed_offset=1000 * rank)
+    b = _batch(rank)
     tokens, offsets, train = b.flat()
     plan0 = stp.stp_pack(tokens, offsets, train, b.family, row_len=b.row_len, min_shared=b.min_shared)
     info = stp.stp_plan_info(plan0)
@@ -268,11 +269,7 @@ def main():
     fwd_ms = [f0.elapsed_time(f1) for _, f0, f1, _, _, _ in steps]
     bwd_ms = [f1.elapsed_time(b1) for _, _, f1, b1, _, _ in steps]
     head_ms = [a.elapsed_time(f0) for a, f0, _, _, _, _ in steps]  # pack + upload + classify
-    tot_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([tot_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = tot_ms / args.steps
     value = world * step_flops * args.steps / (tot_ms / 1e3) / 1e12
     assert stp.stp_device_status(buf.bwd_ws) == stp.STP_OK
@@ -305,11 +302,7 @@ def main():
         e.record()
         e_ms.append((a, e))
     torch.cuda.synchronize()
-    e_tot = sum(a.elapsed_time(e) for a, e in e_ms)
-    if world > 1:
-        t = torch.tensor([e_tot], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_tot = float(t.item())
+    e_tot = max_over_ranks(sum(a.elapsed_time(e) for a, e in e_ms), dev)
     e2e_value = world * step_flops * args.steps / (e_tot / 1e3) / 1e12
 
     peak, hbm, peak_kind = _peaks()
