@@ -443,7 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 //               dP^T = V dO^T (128..255); after the elementwise pass
 //               dV += P^T dO (A from TMEM) and dK += dS^T Q (accumulated over
 //               all iterations in 256..383 and 384..511), then dQ_j = dS K into
-//               128..255; S^T of the next iteration follows at once.
+//               0..127; dP^T of the next iteration follows at once and its
+//               S^T as soon as the drain has read dQ_j, so the drain works
+//               while the tensor core computes dP^T.
 // dK (times scale) and dV leave TMEM once at the end.
 
 struct BwdParams {
@@ -584,18 +586,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok) {
           fence_after_sync();
 #pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km0 + km(kk), id_kk, kk > 0);
+#pragma unroll
           for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, k_km + km(kk), q_km0 + km(kk), id_kk, kk > 0);
+          mma_commit(&bars[C_SF]);
         }
       }
 #pragma unroll 1
       for (int j = 0; ok && j < n_it; ++j) {
         const uint32_t so = (j & 1) ? kStage : 0;
-        const uint32_t do_km = do_km0 + so, q_mn = q_mn0 + so, do_mn = do_mn0 + so;
-        if (j > 0 && !mbar_wait(&bars[C_SFREE], (j - 1) & 1, abort_flag, p.err)) break;
-        fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km + km(kk), id_kk, kk > 0);
-        mma_commit(&bars[C_SF]);
+        const uint32_t q_mn = q_mn0 + so, do_mn = do_mn0 + so;
         if (!mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err)) break;
         fence_after_sync();
         // P^T of query columns 16 kk..16 kk+15: packed columns 8 kk (first
@@ -606,16 +606,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 384, ds_km + km(kk), q_mn + mn(kk), id_kn, (j > 0 || kk > 0));
         mma_commit(&bars[C_QE + (j & 1)]);
+        // dQ_j = dS K into columns 0..127 (P^T_j there is consumed by dV above)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, ds_mn + mn(kk), k_mn + mn(kk), id_nn, kk > 0);
+        for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, ds_mn + mn(kk), k_mn + mn(kk), id_nn, kk > 0);
         mma_commit(&bars[C_QD]);
         mma_commit(&bars[C_PSF]);
         if (j + 1 < n_it) {
+          // dP^T of the next iteration needs nothing but its dO tile; S^T waits
+          // until the drain has read dQ_j out of columns 0..127
+          const uint32_t so1 = (j & 1) ? 0 : kStage;
           if (!mbar_wait(&bars[C_QF + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, p.err)) break;
           fence_after_sync();
-          const uint32_t q_next = q_km0 + ((j & 1) ? 0 : kStage);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, k_km + km(kk), q_next + km(kk), id_kk, kk > 0);
+          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km0 + so1 + km(kk), id_kk, kk > 0);
+          if (!mbar_wait(&bars[C_SFREE], j & 1, abort_flag, p.err)) break;
+          fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, k_km + km(kk), q_km0 + so1 + km(kk), id_kk, kk > 0);
+          mma_commit(&bars[C_SF]);
         }
       }
       if (ok) mma_commit(&bars[C_DONE]);
@@ -737,10 +745,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // the 32 threads of a warp reduce into 512 contiguous bytes
       float* dst = p.dq_acc + (((size_t)r * p.Hq + h) * p.NT + qt) * 16384 + 4 * t;
       uint32_t u[64], w[64];
-      tmem_ld32(tmem + lane_base + 128, u);
-      tmem_ld32(tmem + lane_base + 160, u + 32);
-      tmem_ld32(tmem + lane_base + 192, w);
-      tmem_ld32(tmem + lane_base + 224, w + 32);
+      tmem_ld32(tmem + lane_base + 0, u);
+      tmem_ld32(tmem + lane_base + 32, u + 32);
+      tmem_ld32(tmem + lane_base + 64, w);
+      tmem_ld32(tmem + lane_base + 96, w + 32);
       tmem_ld_wait();
       fence_before_sync();
       mbar_arrive(&bars[C_SFREE]);
