@@ -321,6 +321,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = run && hs < nh;
     for (int e = 0; ok && e < cnt; ++e) {
       const int ent = list[e], kt = ent >> 1, part = ent & 1, k0 = kt * 128;
+      // visibility bits of a partial tile (j <= i && subtree_end[j] >= i),
+      // computed before the scores are ready so the loads stay off the
+      // critical path
+      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+      if (part) {
+        const int4* se4 = reinterpret_cast<const int4*>(se_row + k0);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t bits = 0;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int4 v = __ldg(se4 + 8 * w + c);
+            const int j = k0 + 32 * w + 4 * c;
+            bits |= (uint32_t)(j + 0 <= i && v.x >= i) << (4 * c + 0);
+            bits |= (uint32_t)(j + 1 <= i && v.y >= i) << (4 * c + 1);
+            bits |= (uint32_t)(j + 2 <= i && v.z >= i) << (4 * c + 2);
+            bits |= (uint32_t)(j + 3 <= i && v.w >= i) << (4 * c + 3);
+          }
+          vis[w] = bits;
+        }
+      }
       if (!mbar_wait(&bars[B_SF + hs], e & 1, abort_flag, p.err)) {
         ok = false;
         break;
@@ -334,22 +355,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(s_addr + 96, u + 96);
       tmem_ld_wait();
       if (part) {
-        // visible iff j <= i && subtree_end[j] >= i; the others become -inf
-        const int4* se4 = reinterpret_cast<const int4*>(se_row + k0);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int4 v = __ldg(se4 + c);
-          const int j = k0 + 4 * c;
-          if (!(j + 0 <= i && v.x >= i)) u[4 * c + 0] = 0xff800000u;
-          if (!(j + 1 <= i && v.y >= i)) u[4 * c + 1] = 0xff800000u;
-          if (!(j + 2 <= i && v.z >= i)) u[4 * c + 2] = 0xff800000u;
-          if (!(j + 3 <= i && v.w >= i)) u[4 * c + 3] = 0xff800000u;
-        }
+        for (int c = 0; c < 128; ++c)
+          if (!((vis[c >> 5] >> (c & 31)) & 1u)) u[c] = 0xff800000u;
       }
-      // row max on the raw scores (the scale is positive)
-      float mx = -INFINITY;
+      // row max on the raw scores (the scale is positive); four independent
+      // chains keep the dependent-latency path short
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) mx = max3(mx, __uint_as_float(u[c]), __uint_as_float(u[c + 1]));
+      for (int c = 0; c < 128; c += 8)
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          mx4[t] = max3(mx4[t], __uint_as_float(u[c + 2 * t]), __uint_as_float(u[c + 2 * t + 1]));
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float m_new = fmaxf(m_run, mx * p.scale_log2);
       const float m_use = (m_new > m_run + kRescaleThreshold) ? m_new : m_run;
       const float m_sub = (m_use == -INFINITY) ? 0.f : m_use;
@@ -358,20 +376,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
       const float2 nm2 = make_float2(-m_sub, -m_sub);
       float2 acc2 = make_float2(0.f, 0.f);
-      uint32_t pk[64];
+      // P goes back over the first 64 score columns (already read), half a
+      // row at a time.  PV of the previous tile, which read the old P and
+      // wrote O, completed before this tile's S (issued after it), so both
+      // may be overwritten now.
+      float2 acc2b = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float2 y = __ffma2_rn(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), sl2, nm2);
-        const float2 pr = make_float2(ex2(y.x), ex2(y.y));
-        acc2 = __fadd2_rn(acc2, pr);
-        pk[c] = pack_bf16x2(pr.x, pr.y);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const int c0 = 64 * hf + 2 * c;
+          const float2 y0 = __ffma2_rn(make_float2(__uint_as_float(u[c0]), __uint_as_float(u[c0 + 1])), sl2, nm2);
+          const float2 y1 = __ffma2_rn(make_float2(__uint_as_float(u[c0 + 2]), __uint_as_float(u[c0 + 3])), sl2, nm2);
+          const float2 p0 = make_float2(ex2(y0.x), ex2(y0.y));
+          const float2 p1 = make_float2(ex2(y1.x), ex2(y1.y));
+          acc2 = __fadd2_rn(acc2, p0);
+          acc2b = __fadd2_rn(acc2b, p1);
+          pk[c] = pack_bf16x2(p0.x, p0.y);
+          pk[c + 1] = pack_bf16x2(p1.x, p1.y);
+        }
+        tmem_st32(s_addr + 32 * hf, pk);
       }
-      const float rs = acc2.x + acc2.y;
-      // P goes back over the first 64 score columns (already read).  PV of the
-      // previous tile, which read the old P and wrote O, completed before this
-      // tile's S (issued after it), so both may be overwritten now.
-      tmem_st32(s_addr, pk);
-      tmem_st32(s_addr + 32, pk + 32);
+      const float rs = (acc2.x + acc2b.x) + (acc2.y + acc2b.y);
       if (e > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
         uint32_t u[32];
 #pragma unroll
