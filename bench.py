@@ -167,6 +167,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chunks", type=int, default=4, help="kv-head groups of the host-buffer step")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -281,33 +282,18 @@ def main():
         sum(x.numel() * x.element_size() for x in meta_h.values())
     d2h = sum(x.numel() * x.element_size() for x in (o_h, dq_h, dk_h, dv_h))
 
-    # Copies overlap compute on two side streams: dO (read only by the
-    # backward) goes up while the host packs and the forward runs, and O comes
-    # back while the backward runs.  The step ends on the compute stream once
-    # both side streams are done.
-    copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in, ev_do, ev_fwd = (torch.cuda.Event() for _ in range(3))
+    # The host-buffer step of the library: uploads, kernels and downloads
+    # pipelined over groups of kv heads on the library's own streams.
+    n_chunks = args.chunks
+    scratch = torch.empty(stp.stp_step_scratch_size(desc, n_chunks), dtype=torch.uint8, device=dev)
+    lse_h = torch.empty(R, Hq, T, dtype=torch.float32).pin_memory()
+    d2h += lse_h.numel() * lse_h.element_size()
 
     def e2e_step():
-        for src, dst in ((q_h, q), (k_h, k), (v_h, v)):
-            dst.copy_(src, non_blocking=True)
-        ev_in.record(stream)
-        copy_in.wait_event(ev_in)  # also orders this dO upload after the last backward
-        with torch.cuda.stream(copy_in):
-            do.copy_(do_h, non_blocking=True)
-        ev_do.record(copy_in)
         pack_and_upload()
         stp.stp_classify(desc, se, buf.tile_meta)
-        stp.stp_attn_fwd(desc, q, k, v, se, buf.tile_meta, o, lse, buf.fwd_ws)
-        ev_fwd.record(stream)
-        copy_out.wait_event(ev_fwd)
-        with torch.cuda.stream(copy_out):
-            o_h.copy_(o, non_blocking=True)
-        stream.wait_event(ev_do)
-        stp.stp_attn_bwd(desc, q, k, v, o, lse, do, se, buf.tile_meta, dq, dk, dv, buf.bwd_ws)
-        for src, dst in ((dq, dq_h), (dk, dk_h), (dv, dv_h)):
-            dst.copy_(src, non_blocking=True)
-        stream.wait_stream(copy_out)
+        stp.stp_attn_step_host(desc, n_chunks, q_h, k_h, v_h, do_h, se, buf.tile_meta,
+                               o_h, lse_h, dq_h, dk_h, dv_h, scratch)
 
     for _ in range(args.warmup):
         e2e_step()
@@ -323,7 +309,8 @@ def main():
         e_ms.append((a, e))
     torch.cuda.synchronize()
     e_tot = max_over_ranks(sum(a.elapsed_time(e) for a, e in e_ms), dev)
-    assert torch.equal(o_h, o.cpu()), "O read back through the side stream differs"
+    assert stp.stp_device_status(scratch) == stp.STP_OK
+    assert torch.equal(o_h, o.cpu()) and torch.equal(lse_h, lse.cpu()), "host-buffer step differs"
     e2e_value = world * step_flops * args.steps / (e_tot / 1e3) / 1e12
 
     peak, hbm, peak_kind = _peaks()
@@ -347,7 +334,7 @@ def main():
                      "peak_kind": f"{peak_kind} bf16 burst", "traffic": None},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e_tot / args.steps},
+                "ms_per_step": e_tot / args.steps, "call": "stp_attn_step_host", "kv_head_groups": n_chunks},
         "gpu_launches": 6 * args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -236,6 +236,44 @@ stp_status stp_attn_bwd(const stp_attn_desc* desc, const void* q, const void* k,
                         void* dk, void* dv, void* d_ws, void* stream);
 
 /*
+ * stp_attn_step_host -- stp_attn_fwd followed by stp_attn_bwd on HOST buffers:
+ * uploads Q, K, V, dO, runs both passes and writes O, LSE, dQ, dK, dV back to
+ * host memory.  The paper computes the same two passes on device tensors; the
+ * host-buffer pipeline is a library convenience.  The heads split into
+ * n_chunks groups of whole kv heads (n_kv_heads % n_chunks == 0, at most 16);
+ * group c holds kv heads [c Hkv/n, (c+1) Hkv/n) and their query heads.  Groups
+ * are independent problems, so the copies of one group run while the kernels
+ * of another do (library-owned streams, created on the first call on a
+ * device and kept).  Results equal those of stp_attn_fwd / stp_attn_bwd on the
+ * whole problem: O, LSE, dK, dV bit for bit, dQ up to the order of its float
+ * reductions.
+ *   q, k, v, d_o       host, layouts of stp_attn_fwd / stp_attn_bwd; page-locked
+ *                      memory lets the copies run asynchronously
+ *   d_subtree_end,
+ *   d_tile_meta        device, as for stp_attn_fwd (stp_classify already
+ *                      enqueued on `stream`)
+ *   o, lse, dq, dk, dv host outputs, layouts of stp_attn_fwd / stp_attn_bwd
+ *   d_scratch          device, 256-byte aligned, scratch_bytes >=
+ *                      stp_step_scratch_size(desc, n_chunks); its first 4
+ *                      bytes receive the step's device error word (read it
+ *                      with stp_device_status(d_scratch, stream, &st))
+ * Ordering: the step starts where `stream` stands at the call and `stream`
+ * waits for all of it, so outputs are valid once `stream` is synchronized.
+ * Host buffers must stay alive and untouched until then.  Calls made from
+ * several host threads on one device are serialized by the library; steps
+ * that share a scratch must be ordered on one stream.
+ * Errors: STP_EINVAL (NULL pointer, bad n_chunks, short or unaligned
+ * scratch), the checks of stp_attn_fwd / stp_attn_bwd, STP_ECUDA.
+ */
+stp_status stp_step_scratch_size(const stp_attn_desc* desc, int32_t n_chunks,
+                                 size_t* scratch_bytes);
+stp_status stp_attn_step_host(const stp_attn_desc* desc, int32_t n_chunks, const void* q,
+                              const void* k, const void* v, const void* d_o,
+                              const int32_t* d_subtree_end, const void* d_tile_meta, void* o,
+                              float* lse, void* dq, void* dk, void* dv, void* d_scratch,
+                              size_t scratch_bytes, void* stream);
+
+/*
  * Read the device error word of a workspace (fwd_ws or bwd_ws): synchronizes
  * the stream, then *out = STP_OK or STP_EDEVICE (a device check tripped or a
  * bounded wait ran out; the kernel returned early and its outputs are invalid).

@@ -126,9 +126,6 @@ __global__ void __launch_bounds__(128) tile_lists_kernel(int NT, const int32_t* 
 
 using namespace stp;
 
-namespace stp {
-stp_status check_desc(const stp_attn_desc* d);
-}
 
 extern "C" stp_status stp_workspace_size(const stp_attn_desc* desc, size_t* tile_meta_bytes,
                                          size_t* fwd_ws_bytes, size_t* bwd_ws_bytes) {

@@ -14,4 +14,7 @@ stp_status fail(stp_status code, const char* fmt, ...);
 // Clears the thread's last error.
 void clear_error();
 
+// Validates an attention descriptor (records the reason and returns its code).
+stp_status check_desc(const stp_attn_desc* d);
+
 }  // namespace stp

@@ -25,8 +25,8 @@ STP_BF16, STP_FP32 = 0, 1
 
 EXPORTED = ["stp_pack", "stp_plan_info", "stp_plan_write", "stp_plan_rows_of", "stp_plan_free",
             "stp_workspace_size", "stp_classify", "stp_classify_noalloc", "stp_read_tile_classes",
-            "stp_attn_fwd",
-            "stp_attn_bwd", "stp_device_status", "stp_last_error", "stp_version"]
+            "stp_attn_fwd", "stp_attn_bwd", "stp_step_scratch_size", "stp_attn_step_host",
+            "stp_device_status", "stp_last_error", "stp_version"]
 
 
 class StpError(RuntimeError):
@@ -88,6 +88,11 @@ def lib():
         L.stp_attn_fwd.restype = st
         L.stp_attn_bwd.argtypes = [ctypes.POINTER(AttnDesc)] + [_P] * 13
         L.stp_attn_bwd.restype = st
+        L.stp_step_scratch_size.argtypes = [ctypes.POINTER(AttnDesc), ctypes.c_int32, _SZ]
+        L.stp_step_scratch_size.restype = st
+        L.stp_attn_step_host.argtypes = [ctypes.POINTER(AttnDesc), ctypes.c_int32] + [_P] * 12 + \
+            [ctypes.c_size_t, _P]
+        L.stp_attn_step_host.restype = st
         L.stp_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
         L.stp_device_status.restype = st
         L.stp_last_error.argtypes = []
@@ -249,6 +254,30 @@ def stp_attn_bwd(desc: Desc, q, k, v, o, lse, d_o, subtree_end, tile_meta, dq, d
     _check(lib().stp_attn_bwd(ctypes.byref(d), _dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse),
                               _dptr(d_o), _dptr(subtree_end), _dptr(tile_meta), _dptr(dq),
                               _dptr(dk), _dptr(dv), _dptr(ws), _stream(stream)), "stp_attn_bwd")
+
+
+def stp_step_scratch_size(desc: Desc, n_chunks: int) -> int:
+    out = ctypes.c_size_t()
+    d = desc.c()
+    _check(lib().stp_step_scratch_size(ctypes.byref(d), n_chunks, ctypes.byref(out)),
+           "stp_step_scratch_size")
+    return out.value
+
+
+def stp_attn_step_host(desc: Desc, n_chunks: int, q, k, v, d_o, subtree_end, tile_meta,
+                       o, lse, dq, dk, dv, scratch, stream=None):
+    """Forward + backward on host tensors (torch CPU tensors, ideally pinned):
+    q, k, v, d_o in; o, lse, dq, dk, dv out.  subtree_end, tile_meta and
+    scratch are device tensors.  Outputs are valid once `stream` is synced."""
+    for t in (q, k, v, d_o, o, lse, dq, dk, dv):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("stp_attn_step_host takes contiguous host tensors")
+    d = desc.c()
+    _check(lib().stp_attn_step_host(ctypes.byref(d), n_chunks, _dptr(q), _dptr(k), _dptr(v), _dptr(d_o),
+                                    _dptr(subtree_end), _dptr(tile_meta), _dptr(o), _dptr(lse),
+                                    _dptr(dq), _dptr(dk), _dptr(dv), _dptr(scratch),
+                                    scratch.numel() * scratch.element_size(), _stream(stream)),
+           "stp_attn_step_host")
 
 
 def stp_device_status(ws, stream=None) -> int:
