@@ -200,7 +200,8 @@ def main():
     pin = lambda t: t.contiguous().pin_memory()  # noqa: E731
     q_h, k_h, v_h, do_h = (pin(x) for x in (q_h, k_h, v_h, do_h))
     q, k, v, do = (x.to(dev) for x in (q_h, k_h, v_h, do_h))
-    desc = stp.Desc(R, T, Hq, Hkv, D, stp.STP_BF16, shape.scale)
+    se0 = stp.stp_plan_write(plan0)["subtree_end"]
+    desc = stp.Desc(R, T, Hq, Hkv, D, stp.STP_BF16, shape.scale, stp.stp_count_tile_pairs(se0))
     buf = stp.Buffers(desc, dev)
     o = torch.empty_like(q)
     lse = torch.empty(R, Hq, T, dtype=torch.float32, device=dev)

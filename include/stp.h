@@ -153,14 +153,31 @@ typedef struct {
   float scale;         /* softmax scale, usually 1/sqrt(D)                         */
   int32_t block_m;     /* must be 128 (or 0 = 128)                                 */
   int32_t block_n;     /* must be 128 (or 0 = 128)                                 */
+  int32_t max_tile_pairs; /* bound on the non-empty (query tile, key tile) pairs
+                             over all rows (stp_count_tile_pairs gives the exact
+                             count); sizes the bf16 backward's dS workspace.
+                             0 = every pair with key tile <= query tile,
+                             R * NT * (NT + 1) / 2 with NT = T / 128            */
 } stp_attn_desc;
+
+/*
+ * Exact number of non-empty (query tile, key tile) pairs of 128-token tiles
+ * over all rows of a host subtree_end array int32 [n_rows, row_len]:
+ * key tile kt pairs with query tiles kt .. max_{j in kt} subtree_end[j] / 128
+ * (the predicate j <= i && subtree_end[j] >= i).  Errors: STP_EINVAL (NULL,
+ * row_len not a positive multiple of 128, subtree_end[j] outside [j, row_len)).
+ */
+stp_status stp_count_tile_pairs(const int32_t* subtree_end, int32_t n_rows, int32_t row_len,
+                                int64_t* n_pairs);
 
 /*
  * Byte sizes of the caller-owned device buffers for a descriptor:
  *   tile_meta  -- tile classes and work lists written by stp_classify
  *   fwd_ws     -- workspace of stp_attn_fwd (error word)
  *   bwd_ws     -- workspace of stp_attn_bwd (error word, per-query
- *                 Delta = dO . O, float32 dQ accumulator)
+ *                 Delta = dO . O and -LSE log2 e, and on the bf16 path one
+ *                 32 KiB dS tile per (non-empty tile pair, query head), so
+ *                 max_tile_pairs * Hq * 32 KiB)
  * Any pointer may be NULL.  Buffers must be 256-byte aligned.
  */
 stp_status stp_workspace_size(const stp_attn_desc* desc, size_t* tile_meta_bytes,

@@ -28,6 +28,7 @@ stp_status check_desc(const stp_attn_desc* d) {
   if (d->dtype == STP_FP32 && d->head_dim != 64 && d->head_dim != 128)
     return fail(STP_EUNSUPPORTED, "fp32 needs head_dim 64 or 128 (got %d)", d->head_dim);
   if (!(d->scale > 0.f) || d->scale > 1e4f) return fail(STP_EINVAL, "scale must be positive");
+  if (d->max_tile_pairs < 0) return fail(STP_EINVAL, "max_tile_pairs must be >= 0");
   if ((int64_t)d->n_rows * d->row_len * d->n_q_heads * d->head_dim > (int64_t)1 << 40)
     return fail(STP_EUNSUPPORTED, "problem too large");
   return STP_OK;
@@ -50,6 +51,9 @@ static stp_status fill_common(const stp_attn_desc* d, const int32_t* se, const v
   a.csr = reinterpret_cast<const int32_t*>(base + m.csr);
   a.csc_cnt = reinterpret_cast<const int32_t*>(base + m.csc_cnt);
   a.csc = reinterpret_cast<const int32_t*>(base + m.csc);
+  a.csr_off = reinterpret_cast<const int32_t*>(base + m.csr_off);
+  a.row_base = reinterpret_cast<const int32_t*>(base + m.row_base);
+  a.csc_pair = reinterpret_cast<const int32_t*>(base + m.csc_pair);
   return STP_OK;
 }
 
@@ -117,13 +121,14 @@ extern "C" stp_status stp_attn_bwd(const stp_attn_desc* desc, const void* q, con
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  const BwdWs w = bwd_ws_layout(desc->n_rows, desc->row_len, desc->n_q_heads, desc->head_dim,
-                                desc->dtype == STP_BF16);
+  const int64_t cap = pair_capacity(desc->n_rows, desc->row_len / kTile, desc->max_tile_pairs);
+  const BwdWs w = bwd_ws_layout(desc->n_rows, desc->row_len, desc->n_q_heads, desc->dtype == STP_BF16, cap);
   char* ws = static_cast<char*>(d_ws);
   a.err = reinterpret_cast<uint32_t*>(ws + w.err);
   a.delta = reinterpret_cast<float*>(ws + w.delta);
   a.nlse2 = desc->dtype == STP_BF16 ? reinterpret_cast<float*>(ws + w.nlse2) : nullptr;
-  a.dq_acc = desc->dtype == STP_BF16 ? reinterpret_cast<float*>(ws + w.dq_acc) : nullptr;
+  a.ds = desc->dtype == STP_BF16 ? ws + w.ds : nullptr;
+  a.ds_cap = cap;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaMemsetAsync(a.err, 0, 4, s);
   cudaError_t e;

@@ -90,18 +90,6 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H) {
 // Device helpers
 // ------------------------------------------------------------------------
 
-// K-major operand of a 128-row x 128-column bf16 tile (two 64-column swizzled
-// halves): descriptor for the 16-column slice kk (0..7).
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
-  return smem_desc_sw128(tile + (kk >> 2) * kHalfTile + (kk & 3) * 32, 16, 1024);
-}
-
-// MN-major operand: a [128 K-rows][128 N-columns] tile stored as two
-// 64-column halves; slice kk covers K-rows 16 kk .. 16 kk + 15.
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
-  return smem_desc_sw128(tile + kk * 16 * 128, kHalfTile, 1024);
-}
-
 // Writes 8 consecutive bf16 values (columns 8c .. 8c+7 of row `row`) into a
 // K-major swizzled 128 x 128 tile.
 __device__ __forceinline__ void st_swizzled8(uint8_t* tile, int row, int c, uint4 v) {
@@ -453,47 +441,59 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Backward
 // ------------------------------------------------------------------------
 //
-// Per CTA: (row r, kv head g, key tile kt).  The key tile's list of
-// non-empty query tiles, times the G query heads of the group, gives the
-// iterations j = (query tile, head).  16 warps:
+// Two kernels after the Delta pass.
+//
+// bwd_tc_kernel, one CTA per (row r, kv head g, key tile kt): the key tile's
+// list of non-empty query tiles, times the G query heads of the group, gives
+// the iterations j = (query tile, head).  dK and dV accumulate in TMEM over
+// all iterations; each iteration's dS^T tile (bf16, the shared-memory operand
+// of the dK MMA) is also copied out to the workspace slot of its (pair, head).
+// 16 warps:
 //   warps 0-7   elementwise, one thread per key (= TMEM lane); warps 0-3 take
 //               query columns 0..63, warps 4-7 columns 64..127:
 //               p = 2^(s scale log2e - LSE_i log2e) (masked on PARTIAL tiles
 //               with the thread's own subtree_end[j]), dS = p (dP - Delta_i);
 //               P^T goes back to TMEM as packed bf16 pairs over the consumed
-//               score columns, dS^T to shared memory;
-//   warps 8-11  dQ drain, one thread per query: reads dQ_j from TMEM and adds
-//               it into the float32 accumulator with vector reductions;
+//               score columns, dS^T to shared memory once the previous tile
+//               there has been consumed;
+//   warp 8      dS^T store: one 32 KiB bulk copy per iteration, shared memory
+//               to the pair's slot; the tile is free again once the copy has
+//               read it and the dK MMA has finished with it;
+//   warps 9-11  no role (their registers go to the elementwise warps);
 //   warp 12     TMA: K, V once; Q, dO, -LSE log2e and -Delta of each
 //               iteration through a two-stage ring;
-//   warp 13     MMA issue and TMEM owner: S^T = K Q^T (columns 0..127) and
-//               dP^T = V dO^T (128..255); after the elementwise pass
-//               dV += P^T dO (A from TMEM) and dK += dS^T Q (accumulated over
-//               all iterations in 256..383 and 384..511), then dQ_j = dS K into
-//               0..127; dP^T of the next iteration follows at once and its
-//               S^T as soon as the drain has read dQ_j, so the drain works
-//               while the tensor core computes dP^T.
+//   warp 13     MMA issue and TMEM owner: S^T = K Q^T (columns 0..127),
+//               dP^T = V dO^T (128..255), dV += P^T dO (A from TMEM, 256..383),
+//               dK += dS^T Q (384..511).  After the elementwise pass of j it
+//               issues dP^T(j+1), dV(j), S^T(j+1) (over P^T(j), which dV(j)
+//               read before), dK(j): the elementwise pass of j+1 overlaps
+//               dK(j).
 // dK (times scale) and dV leave TMEM once at the end.
+//
+// dq_tc_kernel, one CTA per (row, kv head, query tile, up to four query heads
+// of the group): dQ_h = scale sum over the query tile's key tiles of dS K, the
+// dS tiles read back from the workspace and K by TMA, accumulated in TMEM
+// (128 columns per head).  Every dQ element is summed in one fixed order, and
+// no atomics are involved.
 
 struct BwdParams {
   int R, T, Hq, Hkv, NT, G;
   float scale_log2;
+  int64_t cap;          // dS slots (pairs) in the workspace
   const int32_t* se;
   const int32_t* csc_cnt;
   const int32_t* csc;
+  const int32_t* csc_pair;
   const float* nlse2;   // -LSE * log2 e
   const float* ndelta;  // -Delta
-  float* dq_acc;
+  uint8_t* ds;          // [pair][Hq] dS^T tiles
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   float scale;
   uint32_t* err;
 };
 
-enum {
-  C_KV = 0, C_QF = 1, C_QE = 3, C_SF = 5, C_DR = 6, C_QD = 7, C_SFREE = 8, C_PSF = 9,
-  C_DONE = 10, C_DRAIN = 11, C_COUNT = 12
-};
+enum { C_KV = 0, C_QF = 1, C_QE = 3, C_SF = 5, C_DR = 6, C_PSF = 7, C_DONE = 8, C_DRAIN = 9, C_COUNT = 10 };
 // shared memory: [K | V | Q0 | Q1 | dO0 | dO1 | dS^T] (1024-aligned, at the
 // start of dynamic shared memory) [vec0 | vec1] [barriers ...]
 constexpr int kBwdBigBytes = 7 * kTileBytes;
@@ -501,11 +501,11 @@ constexpr int kBwdVecBytes = 2 * 2 * 128 * 4;  // per stage: -LSE log2e and -Del
 constexpr int kBwdSmem = kBwdBigBytes + kBwdVecBytes + kSmallBytes;
 static_assert(kBwdSmem <= kSmemLimit, "backward shared memory");
 // 16 warps x 128 registers at launch, rebalanced with setmaxnreg:
-// 128 x (152 + 152 (elementwise) + 136 (dQ drain) + 72 (control)) = 65536,
+// 128 x (184 + 184 (elementwise) + 72 (store group) + 72 (control)) = 65536,
 // and per SM sub-partition (warps w, w+4, w+8, w+12) 512.
 constexpr int kBwdThreads = 512;
-constexpr int kBwdRegsMath = 152, kBwdRegsDrain = 136, kBwdRegsCtl = 72;
-static_assert(128 * (2 * kBwdRegsMath + kBwdRegsDrain + kBwdRegsCtl) <= kBwdThreads * 128, "register split");
+constexpr int kBwdRegsMath = 184, kBwdRegsCtl = 72;
+static_assert(128 * (2 * kBwdRegsMath + 2 * kBwdRegsCtl) <= kBwdThreads * 128, "register split");
 
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < C_COUNT; ++b)
-      mbar_init(&bars[b], b == C_DR ? 256 : (b == C_SFREE ? 128 : 1));
+      mbar_init(&bars[b], b == C_DR ? 256 : (b == C_PSF ? 2 : 1));
     *abort_flag = 0;
     if ((big_s & 1023u) != 0 || cnt <= 0 || cnt > p.NT) {
       *abort_flag = 1;
@@ -598,10 +598,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // ---------------------------------------------------------- MMA issue
       constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
       constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // dV (A in TMEM), dK
-      constexpr uint32_t id_nn = idesc_bf16(128, 128, 1, 1);  // dQ
       // descriptor low words; slice kk adds a constant to the start-address field
-      const uint32_t k_km = desc_lo_kmajor(k_s), v_km = desc_lo_kmajor(v_s), k_mn = desc_lo_mnmajor(k_s);
-      const uint32_t ds_km = desc_lo_kmajor(dst_s), ds_mn = desc_lo_mnmajor(dst_s);
+      const uint32_t k_km = desc_lo_kmajor(k_s), v_km = desc_lo_kmajor(v_s);
+      const uint32_t ds_km = desc_lo_kmajor(dst_s);
       const uint32_t q_km0 = desc_lo_kmajor(big_s + 2 * kTileBytes), do_km0 = desc_lo_kmajor(big_s + 4 * kTileBytes);
       const uint32_t q_mn0 = desc_lo_mnmajor(big_s + 2 * kTileBytes), do_mn0 = desc_lo_mnmajor(big_s + 4 * kTileBytes);
       constexpr uint32_t kStage = kTileBytes >> 4;  // one tile further in the ring
@@ -621,37 +620,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
 #pragma unroll 1
       for (int j = 0; ok && j < n_it; ++j) {
-        const uint32_t so = (j & 1) ? kStage : 0;
-        const uint32_t q_mn = q_mn0 + so, do_mn = do_mn0 + so;
+        const uint32_t so = (j & 1) ? kStage : 0, so1 = (j & 1) ? 0 : kStage;
+        const bool next = j + 1 < n_it;
         if (!mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err)) break;
         fence_after_sync();
-        // P^T of query columns 16 kk..16 kk+15: packed columns 8 kk (first
-        // half) or 64 + 8 (kk - 4) (second half)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts_lo(tmem + 256, tmem + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), do_mn + mn(kk), id_kn, (j > 0 || kk > 0));
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 384, ds_km + km(kk), q_mn + mn(kk), id_kn, (j > 0 || kk > 0));
-        mma_commit(&bars[C_QE + (j & 1)]);
-        // dQ_j = dS K into columns 0..127 (P^T_j there is consumed by dV above)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, ds_mn + mn(kk), k_mn + mn(kk), id_nn, kk > 0);
-        mma_commit(&bars[C_QD]);
-        mma_commit(&bars[C_PSF]);
-        if (j + 1 < n_it) {
-          // dP^T of the next iteration needs nothing but its dO tile; S^T waits
-          // until the drain has read dQ_j out of columns 0..127
-          const uint32_t so1 = (j & 1) ? 0 : kStage;
+        // dP^T(j+1): the elementwise pass of j has read dP^T(j)
+        if (next) {
           if (!mbar_wait(&bars[C_QF + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, p.err)) break;
           fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km0 + so1 + km(kk), id_kk, kk > 0);
-          if (!mbar_wait(&bars[C_SFREE], j & 1, abort_flag, p.err)) break;
-          fence_after_sync();
+        }
+        // dV += P^T dO: P^T of query columns 16 kk..16 kk+15 sits in packed
+        // columns 8 kk (first half) or 64 + 8 (kk - 4) (second half)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts_lo(tmem + 256, tmem + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), do_mn0 + so + mn(kk), id_kn,
+                    (j > 0 || kk > 0));
+        // S^T(j+1) over columns 0..127, after dV has read P^T(j) there
+        if (next) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, k_km + km(kk), q_km0 + so1 + km(kk), id_kk, kk > 0);
           mma_commit(&bars[C_SF]);
         }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 384, ds_km + km(kk), q_mn0 + so + mn(kk), id_kn, (j > 0 || kk > 0));
+        mma_commit(&bars[C_QE + (j & 1)]);
+        mma_commit(&bars[C_PSF]);
       }
       if (ok) mma_commit(&bars[C_DONE]);
       mma_commit(&bars[C_DRAIN]);
@@ -678,8 +673,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* nl_s = vec + st * 256 + half * 64;   // -LSE log2 e per query column
       const float* nd_s = nl_s + 128;                   // -Delta per query column
       if (!mbar_wait(&bars[C_QF + st], (j >> 1) & 1, abort_flag, p.err) ||
-          !mbar_wait(&bars[C_SF], j & 1, abort_flag, p.err) ||
-          (j > 0 && !mbar_wait(&bars[C_PSF], (j - 1) & 1, abort_flag, p.err))) {
+          !mbar_wait(&bars[C_SF], j & 1, abort_flag, p.err)) {
         ok = false;
         break;
       }
@@ -691,9 +685,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld32(tmem + dp_col, ud);
       tmem_ld32(tmem + dp_col + 32, ud + 32);
       tmem_ld_wait();
+      uint32_t dd[32];                    // dS of the 64 columns, packed bf16 pairs
 #pragma unroll
       for (int c = 0; c < 4; ++c) {       // 16 query columns at a time
-        uint32_t pp[8], dd[8];
+        uint32_t pp[8];
 #pragma unroll
         for (int k = 0; k < 16; k += 4) {
           const int col = c * 16 + k;
@@ -713,16 +708,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const float2 pr = make_float2(ex2(y.x), ex2(y.y));
             const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(ud[cc]), __uint_as_float(ud[cc + 1])), nd2));
             pp[(k >> 1) + u2] = pack_bf16x2(pr.x, pr.y);
-            dd[(k >> 1) + u2] = pack_bf16x2(ds.x, ds.y);
+            dd[c * 8 + (k >> 1) + u2] = pack_bf16x2(ds.x, ds.y);
           }
         }
         // packed P^T columns 8c..8c+7 of this half lie in score columns
         // already read
         tmem_st8(tmem + s_col + c * 8, pp);
-        const int cb = half * 8 + 2 * c;   // 16-byte chunk index of dS^T row t
-        st_swizzled8(dst_tile, t, cb + 0, make_uint4(dd[0], dd[1], dd[2], dd[3]));
-        st_swizzled8(dst_tile, t, cb + 1, make_uint4(dd[4], dd[5], dd[6], dd[7]));
       }
+      // dS^T(j-1) must have been read by its dK MMA and its store
+      if (j > 0 && !mbar_wait(&bars[C_PSF], (j - 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c)          // 16-byte chunk index of dS^T row t
+        st_swizzled8(dst_tile, t, half * 8 + c, make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]));
       tmem_st_wait();
       fence_proxy_async_smem();
       fence_before_sync();
@@ -752,42 +752,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------ dQ drain (per query)
-    if (kBwdRegsDrain > 128) regs_inc<kBwdRegsDrain>();
-    if (kBwdRegsDrain < 128) regs_dec<kBwdRegsDrain>();
-    const int t = threadIdx.x & 127;    // query row = TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    bool ok = run;
-    int ent = run ? list[0] : 0;
-    for (int j = 0; ok && j < n_it; ++j) {
-      const int qt = ent >> 1;
-      if (j + 1 < n_it) ent = list[(j + 1) / p.G];
-      const int h = g * p.G + j % p.G;
-      if (!mbar_wait(&bars[C_QD], j & 1, abort_flag, p.err)) {
-        ok = false;
-        break;
+    // ------------------------------------------------ dS^T store (warp 8)
+    regs_dec<kBwdRegsCtl>();
+    if (warp == 8 && lane == 0 && run) {
+      const int32_t* pairs = p.csc_pair + ((size_t)r * p.NT + kt) * p.NT;
+      for (int j = 0; j < n_it; ++j) {
+        if (!mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err)) break;
+        const int pair = pairs[j / p.G], h = g * p.G + j % p.G;
+        if (pair < 0 || pair >= p.cap) {
+          atomicOr(p.err, kErrCapacity);
+        } else {
+          bulk_store(p.ds + ((size_t)pair * p.Hq + h) * kDsTileBytes, dst_tile, (uint32_t)kDsTileBytes);
+          bulk_commit();
+        }
+        bulk_wait_read0();
+        mbar_arrive(&bars[C_PSF]);
       }
-      fence_after_sync();
-      // accumulator tile (r, h, qt) is stored [32 column quads][128 rows][4], so
-      // the 32 threads of a warp reduce into 512 contiguous bytes
-      float* dst = p.dq_acc + (((size_t)r * p.Hq + h) * p.NT + qt) * 16384 + 4 * t;
-      uint32_t u[64], w[64];
-      tmem_ld32(tmem + lane_base + 0, u);
-      tmem_ld32(tmem + lane_base + 32, u + 32);
-      tmem_ld32(tmem + lane_base + 64, w);
-      tmem_ld32(tmem + lane_base + 96, w + 32);
-      tmem_ld_wait();
-      fence_before_sync();
-      mbar_arrive(&bars[C_SFREE]);
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        red_add_v4(dst + 512 * k, __uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1]),
-                   __uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3]));
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        red_add_v4(dst + 512 * (16 + k), __uint_as_float(w[4 * k]), __uint_as_float(w[4 * k + 1]),
-                   __uint_as_float(w[4 * k + 2]), __uint_as_float(w[4 * k + 3]));
+      bulk_wait_all0();
     }
+    __syncwarp();
   }
 
   __syncwarp();
@@ -795,6 +778,170 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   fence_after_sync();
   if (warp == 13) tmem_dealloc(tmem, 512);
+}
+
+struct DqParams {
+  int R, T, Hq, Hkv, NT, G, nquad;
+  int64_t cap;
+  const int32_t* csr_cnt;
+  const int32_t* csr;
+  const int32_t* csr_off;
+  const int32_t* row_base;
+  const uint8_t* ds;
+  __nv_bfloat16* dq;
+  float scale;
+  uint32_t* err;
+};
+
+enum { Q_KF = 0, Q_KE = 2, Q_DF = 4, Q_DE = 8, Q_DONE = 12, Q_DRAIN = 13, Q_COUNT = 14 };
+// shared memory: [K0 | K1 | dS0 .. dS3] (1024-aligned) [barriers ...]
+constexpr int kDqBigBytes = 6 * kTileBytes;
+constexpr int kDqSmem = kDqBigBytes + kSmallBytes;
+static_assert(kDqSmem <= kSmemLimit, "dQ shared memory");
+constexpr int kDqThreads = 256;  // warp 0 loads, warp 1 MMA, warps 4-7 write dQ
+
+__global__ void __launch_bounds__(kDqThreads, 1)
+    dq_tc_kernel(const __grid_constant__ CUtensorMap tk, const DqParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* big = smem_raw;
+  const uint32_t big_s = smem_u32(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + kDqBigBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Q_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // longest lists (highest query tiles) first
+  const int per_qt = p.R * p.Hkv * p.nquad;
+  const int qt = p.NT - 1 - (int)(blockIdx.x / per_qt);
+  int rem = blockIdx.x % per_qt;
+  const int r = rem / (p.Hkv * p.nquad);
+  rem %= p.Hkv * p.nquad;
+  const int g = rem / p.nquad, quad = rem % p.nquad;
+  const int h0 = g * p.G + 4 * quad;
+  const int nh = min(4, p.G - 4 * quad);
+  const int cnt = p.csr_cnt[(size_t)r * p.NT + qt];
+  const int32_t* list = p.csr + ((size_t)r * p.NT + qt) * p.NT;
+  const int64_t pbase = (int64_t)p.row_base[r] + p.csr_off[(size_t)r * p.NT + qt];
+  const int row0 = r * p.T;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < Q_COUNT; ++b) mbar_init(&bars[b], 1);
+    *abort_flag = 0;
+    if ((big_s & 1023u) != 0 || cnt <= 0 || cnt > p.NT) {
+      *abort_flag = 1;
+      atomicOr(p.err, (big_s & 1023u) != 0 ? kErrTmem : kErrBadList);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const bool run = !*abort_flag;
+
+  if (warp == 0 && lane == 0 && run) {
+    // ------------------------------------------------------------ loads
+    tma_prefetch_desc(&tk);
+    int issued_k[2] = {-1, -1}, issued_d[4] = {-1, -1, -1, -1};
+    int d = 0;
+    for (int e = 0; e < cnt; ++e) {
+      const int kt = list[e] >> 1, sk = e & 1;
+      const int64_t pair = pbase + e;
+      if (kt > qt || pair >= p.cap) {
+        *abort_flag = 1;
+        atomicOr(p.err, kt > qt ? kErrBadList : kErrCapacity);
+        break;
+      }
+      if (e >= 2 && !mbar_wait(&bars[Q_KE + sk], ((e >> 1) - 1) & 1, abort_flag, p.err)) break;
+      mbar_expect_tx(&bars[Q_KF + sk], kTileBytes);
+      for (int hf = 0; hf < 2; ++hf)
+        tma_load_3d(big + sk * kTileBytes + hf * kHalfTile, &tk, &bars[Q_KF + sk], hf * 64, g, row0 + kt * 128);
+      issued_k[sk] = e >> 1;
+      bool ok = true;
+      for (int hh = 0; hh < nh; ++hh, ++d) {
+        const int sd = d & 3;
+        if (d >= 4 && !mbar_wait(&bars[Q_DE + sd], ((d >> 2) - 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(&bars[Q_DF + sd], (uint32_t)kDsTileBytes);
+        bulk_load(big + (2 + sd) * kTileBytes, p.ds + ((size_t)pair * p.Hq + h0 + hh) * kDsTileBytes,
+                  (uint32_t)kDsTileBytes, &bars[Q_DF + sd]);
+        issued_d[sd] = d >> 2;
+      }
+      if (!ok) break;
+    }
+    for (int s = 0; s < 2; ++s)
+      if (issued_k[s] >= 0) mbar_wait_drain(&bars[Q_KF + s], issued_k[s] & 1);
+    for (int s = 0; s < 4; ++s)
+      if (issued_d[s] >= 0) mbar_wait_drain(&bars[Q_DF + s], issued_d[s] & 1);
+  } else if (warp == 1 && lane == 0 && run) {
+    // ------------------------------------------------------------ MMA
+    constexpr uint32_t id_nn = idesc_bf16(128, 128, 1, 1);  // A = dS (queries contiguous), B = K
+    auto mn = [](int kk) { return (uint32_t)(kk * 128); };
+    bool ok = true;
+    int d = 0;
+    for (int e = 0; ok && e < cnt; ++e) {
+      const int sk = e & 1;
+      if (!mbar_wait(&bars[Q_KF + sk], (e >> 1) & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      const uint32_t k_mn = desc_lo_mnmajor(big_s + sk * kTileBytes);
+      for (int hh = 0; hh < nh; ++hh, ++d) {
+        const int sd = d & 3;
+        if (!mbar_wait(&bars[Q_DF + sd], (d >> 2) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const uint32_t ds_mn = desc_lo_mnmajor(big_s + (2 + sd) * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss_lo(tmem + hh * 128, ds_mn + mn(kk), k_mn + mn(kk), id_nn, (e > 0 || kk > 0));
+        mma_commit(&bars[Q_DE + sd]);
+      }
+      if (ok) mma_commit(&bars[Q_KE + sk]);
+    }
+    if (ok) mma_commit(&bars[Q_DONE]);
+    mma_commit(&bars[Q_DRAIN]);
+    mbar_wait_drain(&bars[Q_DRAIN], 0);
+  } else if (warp >= 4 && run) {
+    // ------------------------------------------------------------ dQ out
+    const int t = threadIdx.x - 128;   // query row = TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    if (mbar_wait(&bars[Q_DONE], 0, abort_flag, p.err)) {
+      fence_after_sync();
+      for (int hh = 0; hh < nh; ++hh) {
+        __nv_bfloat16* out = p.dq + (((size_t)row0 + qt * 128 + t) * p.Hq + h0 + hh) * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_base + hh * 128 + c * 32, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 a;
+            a.x = pack_bf16x2(__uint_as_float(u[8 * k + 0]) * p.scale, __uint_as_float(u[8 * k + 1]) * p.scale);
+            a.y = pack_bf16x2(__uint_as_float(u[8 * k + 2]) * p.scale, __uint_as_float(u[8 * k + 3]) * p.scale);
+            a.z = pack_bf16x2(__uint_as_float(u[8 * k + 4]) * p.scale, __uint_as_float(u[8 * k + 5]) * p.scale);
+            a.w = pack_bf16x2(__uint_as_float(u[8 * k + 6]) * p.scale, __uint_as_float(u[8 * k + 7]) * p.scale);
+            *reinterpret_cast<uint4*>(out + c * 32 + 8 * k) = a;
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 // Delta[r,h,i] = sum_d dO . O (bf16 in, f32 out); one warp per (row, token, head).
@@ -827,28 +974,6 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
       ndelta[at] = -acc;
       nlse2[at] = -lse[at] * kLog2e;
     }
-  }
-}
-
-// dQ = bf16(scale * dQ_acc).  One block per accumulator tile (row, head,
-// query tile), one thread per query row: 32 coalesced float4 reads, one
-// 256-byte row written.
-__global__ void __launch_bounds__(128) bwd_dq_finalize_kernel(const float* __restrict__ acc,
-                                                              __nv_bfloat16* __restrict__ dq,
-                                                              int T, int Hq, int NT, float scale) {
-  const int tile = blockIdx.x, t = threadIdx.x;
-  const int qt = tile % NT, h = (tile / NT) % Hq, r = tile / (NT * Hq);
-  const float4* src = reinterpret_cast<const float4*>(acc + (size_t)tile * 16384) + t;
-  uint4* out = reinterpret_cast<uint4*>(dq + (((size_t)r * T + qt * 128 + t) * Hq + h) * 128);
-#pragma unroll
-  for (int k = 0; k < 32; k += 2) {
-    const float4 a = src[128 * k], b = src[128 * (k + 1)];
-    uint4 v;
-    v.x = pack_bf16x2(a.x * scale, a.y * scale);
-    v.y = pack_bf16x2(a.z * scale, a.w * scale);
-    v.z = pack_bf16x2(b.x * scale, b.y * scale);
-    v.w = pack_bf16x2(b.z * scale, b.w * scale);
-    out[k >> 1] = v;
   }
 }
 
@@ -898,9 +1023,6 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
   if (!make_map(&mq, a.q, rows, a.Hq) || !make_map(&mk, a.k, rows, a.Hkv) ||
       !make_map(&mv, a.v, rows, a.Hkv) || !make_map(&mdo, a.dout, rows, a.Hq))
     return cudaErrorInvalidValue;
-  const size_t n = (size_t)a.R * a.T * a.Hq * 128;
-  cudaError_t e = cudaMemsetAsync(a.dq_acc, 0, n * sizeof(float), s);
-  if (e != cudaSuccess) return e;
   bwd_delta_kernel<<<2048, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.o_in),
                                         static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.delta,
                                         a.nlse2, a.R, a.T, a.Hq);
@@ -913,24 +1035,44 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
   p.G = a.Hq / a.Hkv;
   p.scale_log2 = a.scale * kLog2e;
   p.scale = a.scale;
+  p.cap = a.ds_cap;
   p.se = a.se;
   p.csc_cnt = a.csc_cnt;
   p.csc = a.csc;
+  p.csc_pair = a.csc_pair;
   p.nlse2 = a.nlse2;
   p.ndelta = a.delta;
-  p.dq_acc = a.dq_acc;
+  p.ds = static_cast<uint8_t*>(a.ds);
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.err = a.err;
+  DqParams q;
+  q.R = a.R;
+  q.T = a.T;
+  q.Hq = a.Hq;
+  q.Hkv = a.Hkv;
+  q.NT = p.NT;
+  q.G = p.G;
+  q.nquad = (p.G + 3) / 4;
+  q.cap = a.ds_cap;
+  q.csr_cnt = a.csr_cnt;
+  q.csr = a.csr;
+  q.csr_off = a.csr_off;
+  q.row_base = a.row_base;
+  q.ds = static_cast<const uint8_t*>(a.ds);
+  q.dq = static_cast<__nv_bfloat16*>(a.dq);
+  q.scale = a.scale;
+  q.err = a.err;
   static bool attr = false;
   if (!attr) {
-    e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem);
+    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   bwd_tc_kernel<<<(unsigned)(p.NT * p.R * p.Hkv), kBwdThreads, kBwdSmem, s>>>(mq, mk, mv, mdo, p);
-  bwd_dq_finalize_kernel<<<(unsigned)(a.R * a.Hq * p.NT), 128, 0, s>>>(
-      a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.T, a.Hq, p.NT, a.scale);
+  dq_tc_kernel<<<(unsigned)(p.NT * p.R * p.Hkv * q.nquad), kDqThreads, kDqSmem, s>>>(mk, q);
   return cudaGetLastError();
 }
 

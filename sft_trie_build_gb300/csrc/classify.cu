@@ -12,10 +12,13 @@
 // (i = j is always visible, j = k1-1 > q0 is not), kt < qt decided by the
 // key tile's min and max of se.
 //
-// Two launches: one block per (row, key tile) reduces se to min/max (reads
+// Three launches: one block per (row, key tile) reduces se to min/max (reads
 // 4*T bytes per row); one block per (row, tile index b) writes row b of the
 // class matrix, the compacted list of non-empty key tiles of query tile b
-// (ascending) and the list of non-empty query tiles of key tile b.
+// (ascending, with each key tile's rank in it) and the list of non-empty query
+// tiles of key tile b; one block per row numbers the row's non-empty pairs
+// (query-tile major) and gives every key-tile list entry its pair index, which
+// addresses the backward's per-pair dS tiles.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -81,7 +84,8 @@ __global__ void __launch_bounds__(128) tile_lists_kernel(int NT, const int32_t* 
                                                          int32_t* __restrict__ csr_cnt,
                                                          int32_t* __restrict__ csr,
                                                          int32_t* __restrict__ csc_cnt,
-                                                         int32_t* __restrict__ csc) {
+                                                         int32_t* __restrict__ csc,
+                                                         int32_t* __restrict__ crank) {
   __shared__ int s_warp[4];
   const int b = blockIdx.x, r = blockIdx.y, t = threadIdx.x;
   const int32_t* mn = kmin + (size_t)r * NT;
@@ -90,6 +94,7 @@ __global__ void __launch_bounds__(128) tile_lists_kernel(int NT, const int32_t* 
   {
     int8_t* crow = cls + ((size_t)r * NT + b) * NT;
     int32_t* list = csr + ((size_t)r * NT + b) * NT;
+    int32_t* rank = crank + ((size_t)r * NT + b) * NT;
     int base = 0;
     for (int k0 = 0; k0 < NT; k0 += 128) {
       const int kt = k0 + t;
@@ -100,7 +105,10 @@ __global__ void __launch_bounds__(128) tile_lists_kernel(int NT, const int32_t* 
       }
       int tot;
       const int pos = block_scan128(c != kEmpty, s_warp, &tot);
-      if (c != kEmpty) list[base + pos] = (kt << 1) | (c == kPartial ? 1 : 0);
+      if (c != kEmpty) {
+        list[base + pos] = (kt << 1) | (c == kPartial ? 1 : 0);
+        rank[kt] = base + pos;
+      }
       base += tot;
     }
     if (t == 0) csr_cnt[(size_t)r * NT + b] = base;
@@ -122,9 +130,113 @@ __global__ void __launch_bounds__(128) tile_lists_kernel(int NT, const int32_t* 
   }
 }
 
+// One block (1024 threads) per row: exclusive scan of the row's csr counts
+// (NT <= 1024), a contiguous range of pair indices for the row taken from a
+// global counter (rows in any order), and the pair index of every csc entry.
+__global__ void __launch_bounds__(1024) tile_pairs_kernel(int NT, int64_t cap,
+                                                          const int32_t* __restrict__ csr_cnt,
+                                                          const int32_t* __restrict__ csc_cnt,
+                                                          const int32_t* __restrict__ csc,
+                                                          const int32_t* __restrict__ crank,
+                                                          int32_t* __restrict__ csr_off,
+                                                          int32_t* __restrict__ row_base,
+                                                          int32_t* __restrict__ csc_pair,
+                                                          int32_t* __restrict__ pair_count,
+                                                          uint32_t* __restrict__ err) {
+  __shared__ int s_off[1024];
+  __shared__ int s_warp[32];
+  __shared__ int s_base;
+  const int r = blockIdx.x, t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int c = t < NT ? csr_cnt[(size_t)r * NT + t] : 0;
+  int x = c;  // inclusive scan: within the warp, then over warp totals
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int v = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    s_warp[lane] = v;
+  }
+  __syncthreads();
+  const int incl = x + (w > 0 ? s_warp[w - 1] : 0);
+  s_off[t] = incl - c;
+  if (t == 1023) {
+    const int total = incl;
+    const int base = atomicAdd(pair_count, total);
+    if ((int64_t)base + total > cap) atomicOr(err, kErrCapacity);
+    s_base = base;
+    row_base[r] = base;
+  }
+  __syncthreads();
+  if (t < NT) csr_off[(size_t)r * NT + t] = s_off[t];
+  const int base = s_base;
+  for (int idx = t; idx < NT * NT; idx += 1024) {
+    const int kt = idx / NT, e = idx - kt * NT;
+    if (e < csc_cnt[(size_t)r * NT + kt]) {
+      const int qt = csc[((size_t)r * NT + kt) * NT + e] >> 1;
+      csc_pair[((size_t)r * NT + kt) * NT + e] = base + s_off[qt] + crank[((size_t)r * NT + qt) * NT + kt];
+    }
+  }
+}
+
+// The launches after min / max: lists, ranks, pair numbering.
+cudaError_t launch_lists(const stp_attn_desc* d, const int32_t* kmin, const int32_t* kmax,
+                         char* base, const TileMeta& m, uint32_t* err, cudaStream_t s) {
+  const int NT = d->row_len / kTile;
+  dim3 grid(NT, d->n_rows);
+  int32_t* pair_count = reinterpret_cast<int32_t*>(base + m.pair_count);
+  cudaError_t e = cudaMemsetAsync(pair_count, 0, 4, s);
+  if (e != cudaSuccess) return e;
+  tile_lists_kernel<<<grid, 128, 0, s>>>(
+      NT, kmin, kmax, reinterpret_cast<int8_t*>(base + m.cls),
+      reinterpret_cast<int32_t*>(base + m.csr_cnt), reinterpret_cast<int32_t*>(base + m.csr),
+      reinterpret_cast<int32_t*>(base + m.csc_cnt), reinterpret_cast<int32_t*>(base + m.csc),
+      reinterpret_cast<int32_t*>(base + m.crank));
+  tile_pairs_kernel<<<d->n_rows, 1024, 0, s>>>(
+      NT, pair_capacity(d->n_rows, NT, d->max_tile_pairs),
+      reinterpret_cast<const int32_t*>(base + m.csr_cnt),
+      reinterpret_cast<const int32_t*>(base + m.csc_cnt),
+      reinterpret_cast<const int32_t*>(base + m.csc), reinterpret_cast<const int32_t*>(base + m.crank),
+      reinterpret_cast<int32_t*>(base + m.csr_off), reinterpret_cast<int32_t*>(base + m.row_base),
+      reinterpret_cast<int32_t*>(base + m.csc_pair), pair_count, err);
+  return cudaGetLastError();
+}
+
 }  // namespace stp
 
 using namespace stp;
+
+extern "C" stp_status stp_count_tile_pairs(const int32_t* subtree_end, int32_t n_rows,
+                                           int32_t row_len, int64_t* n_pairs) {
+  clear_error();
+  if (!n_pairs || (!subtree_end && n_rows > 0)) return fail(STP_EINVAL, "stp_count_tile_pairs: NULL pointer");
+  if (n_rows < 0 || row_len <= 0 || row_len % kTile)
+    return fail(STP_EINVAL, "stp_count_tile_pairs: need n_rows >= 0 and row_len a positive multiple of 128");
+  int64_t total = 0;
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const int32_t* se = subtree_end + r * row_len;
+    for (int32_t k0 = 0; k0 < row_len; k0 += kTile) {
+      int32_t mx = -1;
+      for (int32_t j = k0; j < k0 + kTile; ++j) {
+        if (se[j] < j || se[j] >= row_len)
+          return fail(STP_EINVAL, "stp_count_tile_pairs: subtree_end[%lld][%d] = %d outside [j, row_len)",
+                      (long long)r, j, se[j]);
+        mx = se[j] > mx ? se[j] : mx;
+      }
+      total += mx / kTile - k0 / kTile + 1;
+    }
+  }
+  *n_pairs = total;
+  return STP_OK;
+}
 
 
 extern "C" stp_status stp_workspace_size(const stp_attn_desc* desc, size_t* tile_meta_bytes,
@@ -136,8 +248,8 @@ extern "C" stp_status stp_workspace_size(const stp_attn_desc* desc, size_t* tile
   if (tile_meta_bytes) *tile_meta_bytes = tile_meta_layout(desc->n_rows, NT).total;
   if (fwd_ws_bytes) *fwd_ws_bytes = 256;
   if (bwd_ws_bytes)
-    *bwd_ws_bytes = bwd_ws_layout(desc->n_rows, desc->row_len, desc->n_q_heads, desc->head_dim,
-                                  desc->dtype == STP_BF16)
+    *bwd_ws_bytes = bwd_ws_layout(desc->n_rows, desc->row_len, desc->n_q_heads, desc->dtype == STP_BF16,
+                                  pair_capacity(desc->n_rows, NT, desc->max_tile_pairs))
                         .total;
   return STP_OK;
 }
@@ -161,12 +273,8 @@ extern "C" stp_status stp_classify(const stp_attn_desc* desc, const int32_t* d_s
   tile_minmax_kernel<<<grid, 128, 0, s>>>(d_subtree_end, desc->row_len, NT,
                                           reinterpret_cast<int32_t*>(base + m.kmin),
                                           reinterpret_cast<int32_t*>(base + m.kmax), err);
-  tile_lists_kernel<<<grid, 128, 0, s>>>(
-      NT, reinterpret_cast<const int32_t*>(base + m.kmin),
-      reinterpret_cast<const int32_t*>(base + m.kmax), reinterpret_cast<int8_t*>(base + m.cls),
-      reinterpret_cast<int32_t*>(base + m.csr_cnt), reinterpret_cast<int32_t*>(base + m.csr),
-      reinterpret_cast<int32_t*>(base + m.csc_cnt), reinterpret_cast<int32_t*>(base + m.csc));
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_lists(desc, reinterpret_cast<const int32_t*>(base + m.kmin),
+                               reinterpret_cast<const int32_t*>(base + m.kmax), base, m, err, s);
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_classify: %s", cudaGetErrorString(e));
   return STP_OK;
 }
@@ -272,11 +380,7 @@ extern "C" stp_status stp_classify_noalloc(const stp_attn_desc* desc, const int3
   int32_t* kmax = scratch + kNoAllocMaxTiles;
   dim3 grid((unsigned)NT, desc->n_rows);
   tile_minmax_kernel<<<grid, 128, 0, s>>>(d_subtree_end, desc->row_len, (int)NT, kmin, kmax, err);
-  tile_lists_kernel<<<grid, 128, 0, s>>>(
-      (int)NT, kmin, kmax, reinterpret_cast<int8_t*>(base + m.cls),
-      reinterpret_cast<int32_t*>(base + m.csr_cnt), reinterpret_cast<int32_t*>(base + m.csr),
-      reinterpret_cast<int32_t*>(base + m.csc_cnt), reinterpret_cast<int32_t*>(base + m.csc));
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_lists(desc, kmin, kmax, base, m, err, s);
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_classify_noalloc: %s", cudaGetErrorString(e));
   return STP_OK;
 }

@@ -9,12 +9,22 @@
 //   csc_cnt    int32 [R][NT]          non-empty query tiles per key tile
 //   csc        int32 [R][NT][NT]      (qt << 1) | partial, qt ascending
 //   kmin, kmax int32 [R][NT]          min / max subtree_end over each key tile
+//   crank      int32 [R][NT][NT]      crank[r][qt][kt]: position of kt in the
+//                                     csr list of qt (set for non-empty pairs)
+//   csr_off    int32 [R][NT]          non-empty pairs of the row before query tile qt
+//   row_base   int32 [R]              first pair index of the row
+//   csc_pair   int32 [R][NT][NT]      pair index of each csc entry
+//   pair_count int32                  non-empty pairs over all rows
+// A non-empty (query tile, key tile) pair has the index
+// row_base[r] + csr_off[r][qt] + (position of kt in the csr list of qt):
+// pairs are numbered query-tile major, key tiles ascending, rows in any order.
 //
 // fwd workspace: err (uint32) only.
 // bwd workspace: err, delta float32 [R][Hq][T] (Delta on the float32 path,
 // -Delta on the bf16 path), and for the bf16 path nlse2 float32 [R][Hq][T]
-// (-LSE * log2 e) and dq_acc float32, one 128 x 128 tile per (row, query
-// head, query tile), each tile stored [32 column quads][128 rows][4].
+// (-LSE * log2 e) and ds, one bf16 128 x 128 tile of dS^T per (pair, query
+// head), pair-major, each stored as the backward kernel's shared-memory image
+// (two 64-query halves of [128 keys][64 queries], 128-byte swizzled).
 #pragma once
 
 #include <cstddef>
@@ -30,7 +40,8 @@ enum : int8_t { kEmpty = 0, kPartial = 1, kFull = 2 };
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct TileMeta {
-  size_t err, cls, csr_cnt, csr, csc_cnt, csc, kmin, kmax, total;
+  size_t err, cls, csr_cnt, csr, csc_cnt, csc, kmin, kmax, crank, csr_off, row_base, csc_pair,
+      pair_count, total;
 };
 
 inline TileMeta tile_meta_layout(int64_t R, int64_t NT) {
@@ -44,21 +55,34 @@ inline TileMeta tile_meta_layout(int64_t R, int64_t NT) {
   m.csc = o;     o += align256(size_t(R * NT * NT) * 4);
   m.kmin = o;    o += align256(size_t(R * NT) * 4);
   m.kmax = o;    o += align256(size_t(R * NT) * 4);
+  m.crank = o;   o += align256(size_t(R * NT * NT) * 4);
+  m.csr_off = o; o += align256(size_t(R * NT) * 4);
+  m.row_base = o; o += align256(size_t(R) * 4);
+  m.csc_pair = o; o += align256(size_t(R * NT * NT) * 4);
+  m.pair_count = o; o += 256;
   m.total = o;
   return m;
 }
 
+constexpr size_t kDsTileBytes = 128 * 128 * 2;  // one bf16 dS^T tile
+
+// Non-empty pairs the dS workspace holds: the descriptor's max_tile_pairs, or
+// when that is 0 every pair with kt <= qt (R NT (NT+1) / 2).
+inline int64_t pair_capacity(int64_t R, int64_t NT, int64_t max_tile_pairs) {
+  return max_tile_pairs > 0 ? max_tile_pairs : R * NT * (NT + 1) / 2;
+}
+
 struct BwdWs {
-  size_t err, delta, nlse2, dq_acc, total;
+  size_t err, delta, nlse2, ds, total;
 };
 
-inline BwdWs bwd_ws_layout(int64_t R, int64_t T, int64_t Hq, int64_t D, bool need_acc) {
+inline BwdWs bwd_ws_layout(int64_t R, int64_t T, int64_t Hq, bool tensor_path, int64_t cap_pairs) {
   BwdWs w;
   size_t o = 0;
   w.err = o;    o += 256;
   w.delta = o;  o += align256(size_t(R * Hq * T) * 4);
-  w.nlse2 = o;  o += need_acc ? align256(size_t(R * Hq * T) * 4) : 0;
-  w.dq_acc = o; o += need_acc ? align256(size_t(R * T * Hq * D) * 4) : 0;
+  w.nlse2 = o;  o += tensor_path ? align256(size_t(R * Hq * T) * 4) : 0;
+  w.ds = o;     o += tensor_path ? size_t(cap_pairs) * size_t(Hq) * kDsTileBytes : 0;
   w.total = o;
   return w;
 }
@@ -68,7 +92,8 @@ enum : uint32_t {
   kErrBadSubtreeEnd = 1u << 0,  // subtree_end[j] outside [j, T)
   kErrTimeout = 1u << 1,        // a bounded wait ran out
   kErrBadList = 1u << 2,        // a tile list entry out of range
-  kErrTmem = 1u << 3            // tensor-memory allocation returned an unusable address
+  kErrTmem = 1u << 3,           // tensor-memory allocation returned an unusable address
+  kErrCapacity = 1u << 4        // more non-empty tile pairs than the dS workspace holds
 };
 
 }  // namespace stp

@@ -25,9 +25,13 @@ struct AttnArgs {
   const int32_t* csr;
   const int32_t* csc_cnt;
   const int32_t* csc;
+  const int32_t* csr_off;   // pair numbering of stp_classify (tile_meta)
+  const int32_t* row_base;
+  const int32_t* csc_pair;
   float* delta;          // [R, Hq, T] (backward): Delta (fp32 path) or -Delta (bf16 path)
   float* nlse2;          // [R, Hq, T] (backward, bf16 path): -LSE * log2 e
-  float* dq_acc;         // [R, T, Hq, D] float32 (backward, bf16 path)
+  void* ds;              // [pairs][Hq] bf16 dS^T tiles (backward, bf16 path)
+  int64_t ds_cap;        // pairs the ds buffer holds
   uint32_t* err;         // device error word of the workspace
 };
 

@@ -102,8 +102,9 @@ stp_status step_layout(const stp_attn_desc* d, int n_chunks, StepLayout& L) {
   c.dv = o;     o += kb;
   c.fwd_ws = o; o += align256(fws);
   c.bwd_ws = o; o += align256(bws);
-  c.bwd_err = c.bwd_ws + bwd_ws_layout(d->n_rows, d->row_len, L.cd.n_q_heads, d->head_dim,
-                                       d->dtype == STP_BF16).err;
+  c.bwd_err = c.bwd_ws + bwd_ws_layout(d->n_rows, d->row_len, L.cd.n_q_heads, d->dtype == STP_BF16,
+                                       pair_capacity(d->n_rows, d->row_len / kTile, d->max_tile_pairs))
+                             .err;
   c.size = o;
   L.head = 256;
   L.total = L.head + size_t(n_chunks) * c.size;

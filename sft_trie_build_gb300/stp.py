@@ -24,7 +24,7 @@ STP_GLOBAL, STP_PER_FAMILY, STP_IN_ORDER = 0, 1, 2
 STP_BF16, STP_FP32 = 0, 1
 
 EXPORTED = ["stp_pack", "stp_plan_info", "stp_plan_write", "stp_plan_rows_of", "stp_plan_free",
-            "stp_workspace_size", "stp_classify", "stp_classify_noalloc", "stp_read_tile_classes",
+            "stp_count_tile_pairs", "stp_workspace_size", "stp_classify", "stp_classify_noalloc", "stp_read_tile_classes",
             "stp_attn_fwd", "stp_attn_bwd", "stp_step_scratch_size", "stp_attn_step_host",
             "stp_device_status", "stp_last_error", "stp_version"]
 
@@ -46,7 +46,8 @@ class AttnDesc(ctypes.Structure):
     _fields_ = [("n_rows", ctypes.c_int32), ("row_len", ctypes.c_int32),
                 ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("scale", ctypes.c_float), ("block_m", ctypes.c_int32), ("block_n", ctypes.c_int32)]
+                ("scale", ctypes.c_float), ("block_m", ctypes.c_int32), ("block_n", ctypes.c_int32),
+                ("max_tile_pairs", ctypes.c_int32)]
 
 
 _lib = None
@@ -76,6 +77,8 @@ def lib():
         L.stp_plan_rows_of.restype = st
         L.stp_plan_free.argtypes = [_P]
         L.stp_plan_free.restype = None
+        L.stp_count_tile_pairs.argtypes = [_I32P, ctypes.c_int32, ctypes.c_int32, _I64P]
+        L.stp_count_tile_pairs.restype = st
         L.stp_workspace_size.argtypes = [ctypes.POINTER(AttnDesc), _SZ, _SZ, _SZ]
         L.stp_workspace_size.restype = st
         L.stp_classify.argtypes = [ctypes.POINTER(AttnDesc), _P, _P, _P]
@@ -205,11 +208,23 @@ class Desc:
     head_dim: int
     dtype: int = STP_BF16
     scale: float = 0.0
+    max_tile_pairs: int = 0   # 0 = every lower-triangular tile pair
 
     def c(self) -> AttnDesc:
         sc = self.scale if self.scale > 0 else self.head_dim ** -0.5
         return AttnDesc(self.n_rows, self.row_len, self.n_q_heads, self.n_kv_heads, self.head_dim,
-                        self.dtype, sc, 128, 128)
+                        self.dtype, sc, 128, 128, self.max_tile_pairs)
+
+
+def stp_count_tile_pairs(subtree_end: np.ndarray) -> int:
+    """Exact non-empty (query tile, key tile) pairs of a host int32 [R, T] subtree_end."""
+    se = np.ascontiguousarray(subtree_end, dtype=np.int32)
+    if se.ndim != 2:
+        raise ValueError("subtree_end must be [n_rows, row_len]")
+    out = ctypes.c_int64()
+    _check(lib().stp_count_tile_pairs(_ptr(se, ctypes.c_int32), se.shape[0], se.shape[1], ctypes.byref(out)),
+           "stp_count_tile_pairs")
+    return out.value
 
 
 def stp_workspace_size(desc: Desc):

@@ -29,7 +29,11 @@ class GpuRun:
     def __init__(self, subtree_end: np.ndarray, n_q_heads, n_kv_heads, head_dim, dtype, scale,
                  q, k, v, do=None):
         R, T = subtree_end.shape
-        self.desc = stp.Desc(R, T, n_q_heads, n_kv_heads, head_dim, dtype, scale)
+        try:  # size the backward's dS workspace exactly when subtree_end is valid
+            pairs = stp.stp_count_tile_pairs(subtree_end) if R > 0 else 0
+        except stp.StpError:
+            pairs = 0
+        self.desc = stp.Desc(R, T, n_q_heads, n_kv_heads, head_dim, dtype, scale, pairs)
         self.buf = stp.Buffers(self.desc)
         dev = "cuda"
         self.se = torch.from_numpy(np.ascontiguousarray(subtree_end)).to(dev)

@@ -167,3 +167,31 @@ def test_useful_pairs_match_oracle_visible_sets(stp_lib):
     plan, _, info = _c_pack(b)
     ref = OP.pack(b.seqs, b.trainable, b.row_len, 64)
     assert info["useful_pairs"] == OA.useful_pairs(ref)
+
+
+@pytest.mark.parametrize("name", ["tiny", "grpo", "curriculum", "deep", "bushy"])
+def test_count_tile_pairs_matches_oracle_classes(stp_lib, name):
+    """The host count of non-empty tile pairs equals the number of non-EMPTY
+    entries of the oracle's tile-class matrix."""
+    b = W.CONFIG_BATCHES[name](W.CONFIG_SEEDS[name])
+    tokens, offsets, train = b.flat()
+    plan = stp.stp_pack(tokens, offsets, train, b.family, row_len=b.row_len, min_shared=b.min_shared)
+    se = stp.stp_plan_write(plan)["subtree_end"]
+    ref = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared, b.family)
+    assert stp.stp_count_tile_pairs(se) == int((OA.tile_classes(ref) != OA.EMPTY).sum())
+
+
+def test_count_tile_pairs_edge_cases(stp_lib):
+    T = 256
+    diag = np.arange(T, dtype=np.int32)[None]          # every token sees itself only
+    assert stp.stp_count_tile_pairs(diag) == 2
+    full = np.full((1, T), T - 1, dtype=np.int32)      # causal over the whole row
+    assert stp.stp_count_tile_pairs(full) == 3
+    assert stp.stp_count_tile_pairs(np.zeros((0, T), np.int32)) == 0
+    bad = diag.copy()
+    bad[0, 10] = 5
+    with pytest.raises(stp.StpError) as e:
+        stp.stp_count_tile_pairs(bad)
+    assert e.value.status == stp.STP_EINVAL
+    with pytest.raises(stp.StpError):
+        stp.stp_count_tile_pairs(np.zeros((1, 100), np.int32))

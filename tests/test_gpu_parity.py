@@ -139,6 +139,28 @@ def test_empty_descriptor_is_noop():
     stp.stp_attn_fwd(d, x, x, x, se, buf.tile_meta, x, x.float(), buf.fwd_ws)
 
 
+def test_bwd_capacity_too_small_is_flagged():
+    """A dS workspace one pair short: classification and the backward report a
+    device error instead of writing past the workspace."""
+    b = _small_batch(2, 1024)
+    out, info, ref = pack_both(b)
+    se = out["subtree_end"]
+    R, T = se.shape
+    need = stp.stp_count_tile_pairs(se)
+    assert need == int((OA.tile_classes(ref) != OA.EMPTY).sum())
+    shape = W.AttnShape(R, T, 4, 2, 128, "bf16", 128 ** -0.5, 0.5)
+    q, k, v, do = W.attn_tensors(shape, 1)
+    g = GpuRun(se, 4, 2, 128, stp.STP_BF16, shape.scale, q, k, v, do)
+    g.desc = stp.Desc(R, T, 4, 2, 128, stp.STP_BF16, shape.scale, need - 1)
+    g.buf = stp.Buffers(g.desc)
+    g.classify()
+    g.fwd()
+    g.bwd()
+    torch.cuda.synchronize()
+    assert stp.stp_device_status(g.buf.tile_meta) == stp.STP_EDEVICE
+    assert stp.stp_device_status(g.buf.bwd_ws) == stp.STP_EDEVICE
+
+
 def test_misaligned_pointer_rejected():
     d = stp.Desc(1, 256, 2, 1, 128, stp.STP_BF16)
     buf = stp.Buffers(d)
