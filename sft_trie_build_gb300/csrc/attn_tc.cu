@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[B_KE + s], 1);
       mbar_init(&bars[B_VE + s], 1);
       mbar_init(&bars[B_SF + s], 1);
-      mbar_init(&bars[B_PF + s], 128);
+      mbar_init(&bars[B_PF + s], 4);  // one arrival per softmax warp
       mbar_init(&bars[B_OD + s], 1);
     }
     mbar_init(&bars[B_DRAIN], 1);
@@ -204,6 +204,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           *abort_flag = 1;
           atomicOr(p.err, kErrBadList);
           break;
+        }
+        // K and V of a later entry into L2 (see the backward producer)
+        if (e + 2 < cnt) {
+          const int kt2 = min(max(list[e + 2] >> 1, 0), p.NT - 1);
+          for (int hf = 0; hf < 2; ++hf) {
+            tma_prefetch_l2_3d(&tk, hf * 64, g, row0 + kt2 * 128);
+            tma_prefetch_l2_3d(&tv, hf * 64, g, row0 + kt2 * 128);
+          }
         }
         if (e >= 2 && !mbar_wait(&bars[B_KE + st], (n - 1) & 1, abort_flag, p.err)) break;
         mbar_expect_tx(&bars[B_KF + st], kTileBytes);
@@ -330,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           vis[w] = bits;
         }
       }
-      if (!mbar_wait(&bars[B_SF + hs], e & 1, abort_flag, p.err)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_SF + hs], e & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
@@ -402,7 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_run = l_run * alpha + rs;
       m_run = m_use;
       fence_before_sync();
-      mbar_arrive(&bars[B_PF + hs]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_PF + hs]);
     }
     if (ok && mbar_wait(&bars[B_OD + hs], (cnt - 1) & 1, abort_flag, p.err)) {
       fence_after_sync();
@@ -465,9 +474,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   warp 13     MMA issue and TMEM owner: S^T = K Q^T (columns 0..127),
 //               dP^T = V dO^T (128..255), dV += P^T dO (A from TMEM, 256..383),
 //               dK += dS^T Q (384..511).  After the elementwise pass of j it
-//               issues dP^T(j+1), dV(j), S^T(j+1) (over P^T(j), which dV(j)
-//               read before), dK(j): the elementwise pass of j+1 overlaps
-//               dK(j).
+//               issues dV(j), S^T(j+1) (over P^T(j), which dV(j) read
+//               before), dK(j); dP^T(j+1) goes out earlier, once the pass of
+//               j has loaded dP^T(j), so it runs during that pass, and the
+//               pass of j+1 overlaps dK(j).
 // dK (times scale) and dV leave TMEM once at the end.
 //
 // dq_tc_kernel, one CTA per (row, kv head, query tile, up to four query heads
@@ -493,7 +503,10 @@ struct BwdParams {
   uint32_t* err;
 };
 
-enum { C_KV = 0, C_QF = 1, C_QE = 3, C_SF = 5, C_DR = 6, C_PSF = 7, C_DONE = 8, C_DRAIN = 9, C_COUNT = 10 };
+enum {
+  C_KV = 0, C_QF = 1, C_QE = 3, C_SF = 5, C_DPF = 6, C_DR = 7, C_PSF = 8, C_DONE = 9, C_DRAIN = 10,
+  C_COUNT = 11
+};
 // shared memory: [K | V | Q0 | Q1 | dO0 | dO1 | dS^T] (1024-aligned, at the
 // start of dynamic shared memory) [vec0 | vec1] [barriers ...]
 constexpr int kBwdBigBytes = 7 * kTileBytes;
@@ -504,6 +517,7 @@ static_assert(kBwdSmem <= kSmemLimit, "backward shared memory");
 // 128 x (184 + 184 (elementwise) + 72 (store group) + 72 (control)) = 65536,
 // and per SM sub-partition (warps w, w+4, w+8, w+12) 512.
 constexpr int kBwdThreads = 512;
+constexpr int kBwdPrefetch = 2;  // iterations ahead for the L2 prefetch of Q, dO
 constexpr int kBwdRegsMath = 184, kBwdRegsCtl = 72;
 static_assert(128 * (2 * kBwdRegsMath + 2 * kBwdRegsCtl) <= kBwdThreads * 128, "register split");
 
@@ -533,7 +547,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < C_COUNT; ++b)
-      mbar_init(&bars[b], b == C_DR ? 256 : (b == C_PSF ? 2 : 1));
+      // C_DPF, C_DR: one arrival per elementwise warp; C_PSF: the dK commit
+      // and the dS^T store
+      mbar_init(&bars[b], (b == C_DR || b == C_DPF) ? 8 : (b == C_PSF ? 2 : 1));
     *abort_flag = 0;
     if ((big_s & 1023u) != 0 || cnt <= 0 || cnt > p.NT) {
       *abort_flag = 1;
@@ -575,6 +591,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           *abort_flag = 1;
           atomicOr(p.err, kErrBadList);
           break;
+        }
+        // Q and dO of a later iteration into L2, so that its load, issued
+        // only when a ring stage frees up, finds them there
+        if (j + kBwdPrefetch < n_it) {
+          const int e2 = list[(j + kBwdPrefetch) / p.G];
+          const int qt2 = min(max(e2 >> 1, 0), p.NT - 1), h2 = g * p.G + (j + kBwdPrefetch) % p.G;
+          for (int hf = 0; hf < 2; ++hf) {
+            tma_prefetch_l2_3d(&tq, hf * 64, h2, row0 + qt2 * 128);
+            tma_prefetch_l2_3d(&tdo, hf * 64, h2, row0 + qt2 * 128);
+          }
         }
         if (j >= 2 && !mbar_wait(&bars[C_QE + st], (n - 1) & 1, abort_flag, p.err)) break;
         mbar_expect_tx(&bars[C_QF + st], 2 * kTileBytes + 2 * 128 * 4);
@@ -622,15 +648,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int j = 0; ok && j < n_it; ++j) {
         const uint32_t so = (j & 1) ? kStage : 0, so1 = (j & 1) ? 0 : kStage;
         const bool next = j + 1 < n_it;
-        if (!mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err)) break;
-        fence_after_sync();
-        // dP^T(j+1): the elementwise pass of j has read dP^T(j)
+        // dP^T(j+1) as soon as the elementwise pass of j holds dP^T(j) in
+        // registers: the tensor core computes it during that pass
         if (next) {
-          if (!mbar_wait(&bars[C_QF + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, p.err)) break;
+          if (!mbar_wait(&bars[C_DPF], j & 1, abort_flag, p.err) ||
+              !mbar_wait(&bars[C_QF + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, p.err))
+            break;
           fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km0 + so1 + km(kk), id_kk, kk > 0);
         }
+        if (!mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err)) break;
+        fence_after_sync();
         // dV += P^T dO: P^T of query columns 16 kk..16 kk+15 sits in packed
         // columns 8 kk (first half) or 64 + 8 (kk - 4) (second half)
 #pragma unroll
@@ -672,8 +701,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int q0 = qt * 128 + half * 64;
       const float* nl_s = vec + st * 256 + half * 64;   // -LSE log2 e per query column
       const float* nd_s = nl_s + 128;                   // -Delta per query column
-      if (!mbar_wait(&bars[C_QF + st], (j >> 1) & 1, abort_flag, p.err) ||
-          !mbar_wait(&bars[C_SF], j & 1, abort_flag, p.err)) {
+      const bool ready = mbar_wait(&bars[C_QF + st], (j >> 1) & 1, abort_flag, p.err) &&
+                         mbar_wait(&bars[C_SF], j & 1, abort_flag, p.err);
+      if (!__all_sync(0xffffffffu, ready)) {
         ok = false;
         break;
       }
@@ -685,6 +715,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld32(tmem + dp_col, ud);
       tmem_ld32(tmem + dp_col + 32, ud + 32);
       tmem_ld_wait();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C_DPF]);
       uint32_t dd[32];                    // dS of the 64 columns, packed bf16 pairs
 #pragma unroll
       for (int c = 0; c < 4; ++c) {       // 16 query columns at a time
@@ -716,7 +749,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_st8(tmem + s_col + c * 8, pp);
       }
       // dS^T(j-1) must have been read by its dK MMA and its store
-      if (j > 0 && !mbar_wait(&bars[C_PSF], (j - 1) & 1, abort_flag, p.err)) {
+      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars[C_PSF], (j - 1) & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
@@ -726,7 +759,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_st_wait();
       fence_proxy_async_smem();
       fence_before_sync();
-      mbar_arrive(&bars[C_DR]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C_DR]);
     }
     if (ok && mbar_wait(&bars[C_DONE], 0, abort_flag, p.err)) {
       fence_after_sync();
