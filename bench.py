@@ -44,6 +44,12 @@ WORKLOAD_DESC = ("one GRPO group: 5000-token non-trainable system prefix + 16 tr
 METRIC = "tree-attn fwd+bwd useful TFLOP/s (% of BF16 peak) and trajectories/s on 1 GB300"
 
 
+# DRAM bytes (read + write) of one backward on the workload above, from an ncu
+# capture of bwd_tc_kernel (2.208e9 + 4.147e9) and dq_tc_kernel
+# (4.228e9 + 0.122e9); to be retaken whenever either kernel changes.
+BWD_DRAM_BYTES = 2.208184e9 + 4.147031e9 + 4.228393e9 + 0.121711e9
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -330,13 +336,17 @@ def main():
         "breakdown_ms": {"pack_upload_classify": statistics.mean(head_ms), "fwd": statistics.mean(fwd_ms),
                          "bwd": bwd_avg, "fwd_tflops": fwd_flops / (statistics.mean(fwd_ms) / 1e3) / 1e12,
                          "bwd_tflops": achieved},
-        "roofline": {"bound": "tensor", "kernel": "stp_attn_bwd (delta + dK/dV/dQ tcgen05 kernel + dQ finalize)",
+        "roofline": {"bound": "tensor",
+                     "kernel": "stp_attn_bwd call: bwd_delta_kernel + bwd_tc_kernel (dK, dV, dS tiles) + "
+                               "dq_tc_kernel (dQ from the dS tiles)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_kind": f"{peak_kind} bf16 burst", "traffic": None},
+                     "peak_kind": f"{peak_kind} bf16 burst", "traffic": BWD_DRAM_BYTES,
+                     "traffic_note": "dram read+write bytes of bwd_tc_kernel + dq_tc_kernel, one ncu launch "
+                                     "each on this workload; the dS round trip is 8.2 GB of it"},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e_tot / args.steps, "call": "stp_attn_step_host", "kv_head_groups": n_chunks},
-        "gpu_launches": 6 * args.steps,
+        "gpu_launches": 7 * args.steps,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import pack as OP
