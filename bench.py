@@ -178,7 +178,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--chunks", type=int, default=4, help="kv-head groups of the host-buffer step")
+    ap.add_argument("--chunks", type=int, default=8, help="kv-head groups of the host-buffer step")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

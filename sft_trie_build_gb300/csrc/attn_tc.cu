@@ -488,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 struct BwdParams {
   int R, T, Hq, Hkv, NT, G;
+  int g0, ng;           // kv heads [g0, g0 + ng) of this launch
   float scale_log2;
   int64_t cap;          // dS slots (pairs) in the workspace
   const int32_t* se;
@@ -536,10 +537,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* dst_tile = big + 6 * kTileBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int per_kt = p.R * p.Hkv;
+  const int per_kt = p.R * p.ng;
   const int kt = (int)(blockIdx.x / per_kt);
-  const int r = (blockIdx.x % per_kt) / p.Hkv;
-  const int g = blockIdx.x % p.Hkv;
+  const int r = (blockIdx.x % per_kt) / p.ng;
+  const int g = p.g0 + (int)(blockIdx.x % p.ng);
   const int cnt = p.csc_cnt[(size_t)r * p.NT + kt];
   const int32_t* list = p.csc + ((size_t)r * p.NT + kt) * p.NT;
   const int n_it = cnt * p.G;
@@ -816,6 +817,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 struct DqParams {
   int R, T, Hq, Hkv, NT, G, nquad;
+  int g0, ng;           // kv heads [g0, g0 + ng) of this launch
   int64_t cap;
   const int32_t* csr_cnt;
   const int32_t* csr;
@@ -845,12 +847,12 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // longest lists (highest query tiles) first
-  const int per_qt = p.R * p.Hkv * p.nquad;
+  const int per_qt = p.R * p.ng * p.nquad;
   const int qt = p.NT - 1 - (int)(blockIdx.x / per_qt);
   int rem = blockIdx.x % per_qt;
-  const int r = rem / (p.Hkv * p.nquad);
-  rem %= p.Hkv * p.nquad;
-  const int g = rem / p.nquad, quad = rem % p.nquad;
+  const int r = rem / (p.ng * p.nquad);
+  rem %= p.ng * p.nquad;
+  const int g = p.g0 + rem / p.nquad, quad = rem % p.nquad;
   const int h0 = g * p.G + 4 * quad;
   const int nh = min(4, p.G - 4 * quad);
   const int cnt = p.csr_cnt[(size_t)r * p.NT + qt];
@@ -1051,6 +1053,44 @@ cudaError_t tc_fwd(const AttnArgs& a, cudaStream_t s) {
 
 namespace stp {
 
+namespace {
+
+// Library-owned streams of the backward's kv-head groups: a pool per device,
+// created on first use, handed out round-robin so that backward calls made
+// from different caller streams do not serialize on the same ones.  Every
+// enqueue sequence that uses the pool holds g_bwd_mu.
+constexpr int kBwdGroups = 8;   // kv-head groups of one backward call, at most
+constexpr int kBwdPool = 16;
+struct BwdStreams {
+  bool ready = false;
+  int next = 0;
+  cudaStream_t s[kBwdPool] = {};
+  cudaEvent_t fork = nullptr, join[kBwdPool] = {};
+};
+std::mutex g_bwd_mu;
+BwdStreams g_bwd_streams[64];
+
+cudaError_t bwd_streams(BwdStreams** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  BwdStreams& b = g_bwd_streams[dev];
+  if (!b.ready) {
+    e = cudaEventCreateWithFlags(&b.fork, cudaEventDisableTiming);
+    for (int i = 0; i < kBwdPool && e == cudaSuccess; ++i) {
+      e = cudaStreamCreateWithFlags(&b.s[i], cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b.join[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return e;
+    b.ready = true;
+  }
+  *out = &b;
+  return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv, mdo;
   const int64_t rows = (int64_t)a.R * a.T;
@@ -1105,8 +1145,38 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  bwd_tc_kernel<<<(unsigned)(p.NT * p.R * p.Hkv), kBwdThreads, kBwdSmem, s>>>(mq, mk, mv, mdo, p);
-  dq_tc_kernel<<<(unsigned)(p.NT * p.R * p.Hkv * q.nquad), kDqThreads, kDqSmem, s>>>(mk, q);
+  // The kv heads in up to kBwdGroups groups, each on its own stream: a group's
+  // dQ pass (HBM-bound) starts as soon as that group's dK/dV kernel is done
+  // and runs while the other groups compute.
+  const int n_groups = p.Hkv < kBwdGroups ? p.Hkv : kBwdGroups;
+  std::lock_guard<std::mutex> lock(g_bwd_mu);
+  BwdStreams* bs = nullptr;
+  if (n_groups > 1) {
+    cudaError_t e = bwd_streams(&bs);
+    if (e != cudaSuccess) return e;
+    e = cudaEventRecord(bs->fork, s);
+    if (e != cudaSuccess) return e;
+  }
+  for (int gi = 0; gi < n_groups; ++gi) {
+    const int g0 = gi * p.Hkv / n_groups, g1 = (gi + 1) * p.Hkv / n_groups;
+    cudaStream_t sg = s;
+    const int slot = n_groups > 1 ? (bs->next + gi) % kBwdPool : 0;
+    if (n_groups > 1) {
+      sg = bs->s[slot];
+      cudaError_t e = cudaStreamWaitEvent(sg, bs->fork, 0);
+      if (e != cudaSuccess) return e;
+    }
+    p.g0 = q.g0 = g0;
+    p.ng = q.ng = g1 - g0;
+    bwd_tc_kernel<<<(unsigned)(p.NT * p.R * p.ng), kBwdThreads, kBwdSmem, sg>>>(mq, mk, mv, mdo, p);
+    dq_tc_kernel<<<(unsigned)(p.NT * p.R * q.ng * q.nquad), kDqThreads, kDqSmem, sg>>>(mk, q);
+    if (n_groups > 1) {
+      cudaError_t e = cudaEventRecord(bs->join[slot], sg);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, bs->join[slot], 0);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  if (n_groups > 1) bs->next = (bs->next + n_groups) % kBwdPool;
   return cudaGetLastError();
 }
 
