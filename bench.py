@@ -50,9 +50,10 @@ METRIC = "tree-attn fwd+bwd useful TFLOP/s (% of BF16 peak) and trajectories/s o
 
 
 # DRAM bytes (read + write) of one backward on the workload above, from an ncu
-# capture of bwd_tc_kernel (2.208e9 + 4.147e9) and dq_tc_kernel
-# (4.228e9 + 0.122e9); to be retaken whenever either kernel changes.
-BWD_DRAM_BYTES = None  # retaken after the last kernel change
+# capture of one kv-head group's bwd_tc_kernel (69.5e6 + 463.0e6) and
+# dq_tc_kernel (519.0e6 + 9.9e6) launches, times the 8 groups (every kv head
+# has the same tile structure); to be retaken whenever either kernel changes.
+BWD_DRAM_BYTES = 8 * (69.511936e6 + 462.977280e6 + 519.038976e6 + 9.910528e6)
 
 
 def _peaks():
@@ -401,8 +402,8 @@ def main():
                                "dq_tc_kernel (dQ from the dS tiles)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} bf16 burst", "traffic": BWD_DRAM_BYTES,
-                     "traffic_note": "dram read+write bytes of bwd_tc_kernel + dq_tc_kernel, one ncu launch "
-                                     "each on this workload; the dS round trip is 8.2 GB of it"},
+                     "traffic_note": "dram read+write bytes of bwd_tc_kernel + dq_tc_kernel for one kv-head "
+                                     "group (one ncu launch each) x 8 groups; the dS round trip is ~7.9 GB of it"},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e_tot / args.steps, "call": "stp_attn_step_host", "kv_head_groups": n_chunks,
