@@ -65,6 +65,32 @@ def _peaks():
         return 1900.0, 6800.0, "fallback"
 
 
+def _what_if(n_candidates: int = 64, groups_per_candidate: int = 8) -> dict:
+    """Host 'what if' planning: rows that candidate batches (whole groups drawn
+    from the curriculum pool) would need, global tree vs one tree per group,
+    planned in parallel without materializing anything."""
+    from sft_trie_build_gb300 import stp
+
+    b = W.curriculum(W.CONFIG_SEEDS["curriculum"])
+    tokens, offsets, train = b.flat()
+    fam = np.asarray(b.family)
+    groups = np.unique(fam)
+    rng = np.random.default_rng(11)
+    subsets = [np.flatnonzero(np.isin(fam, rng.choice(groups, groups_per_candidate, replace=False)))
+               for _ in range(n_candidates)]
+    kw = dict(row_len=b.row_len, min_shared=b.min_shared)
+    stp.stp_plan_rows_many(tokens, offsets, train, b.family, subsets[:2], **kw)  # warm-up
+    t0 = time.perf_counter()
+    rows, _ = stp.stp_plan_rows_many(tokens, offsets, train, b.family, subsets, **kw)
+    dt = time.perf_counter() - t0
+    rows_pf, _ = stp.stp_plan_rows_many(tokens, offsets, train, b.family, subsets, flags=stp.STP_PER_FAMILY, **kw)
+    return {"pool": f"curriculum config: {len(b.seqs)} sequences in {len(groups)} groups, rows of {b.row_len}",
+            "candidates": n_candidates, "groups_per_candidate": groups_per_candidate,
+            "ms_total": 1e3 * dt, "ms_per_candidate": 1e3 * dt / n_candidates,
+            "host_threads": os.cpu_count(), "rows_mean_global_tree": float(np.mean(rows)),
+            "rows_mean_tree_per_group": float(np.mean(rows_pf))}
+
+
 def _batch(rank=0):
     return W.grpo(rank_seed(W.CONFIG_SEEDS[WORKLOAD], rank))
 
@@ -410,6 +436,8 @@ def main():
                 "steps_in_flight": 2, "l2": "not flushed: every step re-uploads 336 MB of inputs (> L2)"},
         "gpu_launches": 7 * args.steps,
     }
+    if rank == 0:
+        line["what_if"] = _what_if()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import pack as OP
         plan_o = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared, b.family)

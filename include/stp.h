@@ -137,6 +137,41 @@ stp_status stp_plan_rows_of(const stp_plan* plan, int32_t* row_of_seq);
 
 void stp_plan_free(stp_plan* plan);
 
+/*
+ * stp_plan_rows -- "what if" planning ([P1] global-tree section: the pass that
+ * packs a step is also run over sampled subsets of past data, to estimate how
+ * many rows a candidate batch would need before committing to it).  Returns
+ * the number of rows and of packed (real) tokens that stp_pack would produce
+ * for the sequences subset[0..n_subset) of a pool, taken in that order, with
+ * the same row_len, min_shared and flags; no plan is kept and nothing is
+ * materialized.
+ *   tokens, offsets, n_seqs, trainable, family   the pool, as for stp_pack
+ *   subset     int32 [n_subset] indices into the pool (repeats allowed), or
+ *              NULL for the whole pool in input order
+ *   n_rows, packed_tokens   outputs
+ * Errors: those of stp_pack; STP_EINVAL for an index outside [0, n_seqs).
+ */
+stp_status stp_plan_rows(const int32_t* tokens, const int64_t* offsets, int32_t n_seqs,
+                         const uint8_t* trainable, const int32_t* family, const int32_t* subset,
+                         int32_t n_subset, int32_t row_len, int32_t min_shared, uint32_t flags,
+                         int32_t* n_rows, int64_t* packed_tokens);
+
+/*
+ * stp_plan_rows_many -- stp_plan_rows for many subsets at once, planned in
+ * parallel on host threads (n_threads <= 0: one per hardware thread).
+ * Subset i is subsets[subset_offsets[i] .. subset_offsets[i+1]);
+ * subset_offsets int64 [n_subsets + 1], subset_offsets[0] = 0, non-decreasing.
+ * n_rows int32 [n_subsets] and packed_tokens int64 [n_subsets] receive the
+ * results.  On error the status and message are those of the first failing
+ * subset (its index is in the message); the other outputs are unspecified.
+ */
+stp_status stp_plan_rows_many(const int32_t* tokens, const int64_t* offsets, int32_t n_seqs,
+                              const uint8_t* trainable, const int32_t* family,
+                              const int32_t* subsets, const int64_t* subset_offsets,
+                              int32_t n_subsets, int32_t row_len, int32_t min_shared,
+                              uint32_t flags, int32_t n_threads, int32_t* n_rows,
+                              int64_t* packed_tokens);
+
 /* ------------------------------------------------------------------------ */
 /* Tree attention on the GPU                                                */
 /* ------------------------------------------------------------------------ */

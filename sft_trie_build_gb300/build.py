@@ -18,7 +18,7 @@ LIB = os.path.join(PKG, "libstp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "--expt-relaxed-constexpr", "-Xptxas", "-v", "-I", os.path.join(ROOT, "include")]
-CXX_FLAGS = ["-O2", "-fPIC", "-std=c++17", "-Wall", "-I", os.path.join(ROOT, "include")]
+CXX_FLAGS = ["-O2", "-fPIC", "-std=c++17", "-Wall", "-pthread", "-I", os.path.join(ROOT, "include")]
 
 
 def _nvcc():

@@ -26,10 +26,14 @@
 //   * occupancy is one bitset per bin; exit indices come from one reverse
 //     pass over the bin's segments in pre-order.
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <mutex>
 #include <string>
+#include <system_error>
+#include <thread>
 #include <unordered_map>
 #include <vector>
 
@@ -459,6 +463,133 @@ stp_status stp_plan_write(const stp_plan* P, int32_t* token_ids, int32_t* positi
 }
 
 void stp_plan_free(stp_plan* P) { delete P; }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// "What if" planning: rows a candidate batch would need ("Prefix tree packing",
+// global-tree section: the same tree-and-bin-pack pass that packs a step is
+// run over sampled subsets of past data to estimate the rows of a candidate
+// batch before committing to it).  A subset is gathered into contiguous
+// arrays and planned by stp_pack itself, so the count is exactly what packing
+// that batch would give; nothing is materialized.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+stp_status plan_rows_one(const int32_t* tokens, const int64_t* offsets, int32_t n_seqs,
+                         const uint8_t* trainable, const int32_t* family, const int32_t* subset,
+                         int32_t n_subset, int32_t row_len, int32_t min_shared, uint32_t flags,
+                         int32_t* n_rows, int64_t* packed) {
+  std::vector<int32_t> t2, f2;
+  std::vector<int64_t> o2;
+  std::vector<uint8_t> tr2;
+  const int32_t *tk = tokens, *fm = family;
+  const int64_t* of = offsets;
+  const uint8_t* tr = trainable;
+  int32_t n = n_seqs;
+  if (subset) {
+    int64_t total = 0;
+    for (int32_t i = 0; i < n_subset; ++i) {
+      const int32_t s = subset[i];
+      if (s < 0 || s >= n_seqs) return fail(STP_EINVAL, "subset[%d] = %d outside [0, %d)", i, s, n_seqs);
+      total += offsets[s + 1] - offsets[s];
+    }
+    try {
+      t2.reserve(total);
+      o2.reserve(n_subset + 1);
+      o2.push_back(0);
+      if (trainable) tr2.reserve(total);
+      if (family) f2.reserve(n_subset);
+      for (int32_t i = 0; i < n_subset; ++i) {
+        const int32_t s = subset[i];
+        t2.insert(t2.end(), tokens + offsets[s], tokens + offsets[s + 1]);
+        if (trainable) tr2.insert(tr2.end(), trainable + offsets[s], trainable + offsets[s + 1]);
+        if (family) f2.push_back(family[s]);
+        o2.push_back((int64_t)t2.size());
+      }
+    } catch (const std::bad_alloc&) {
+      return fail(STP_ENOMEM, "out of host memory");
+    }
+    tk = t2.data();
+    of = o2.data();
+    tr = trainable ? tr2.data() : nullptr;
+    fm = family ? f2.data() : nullptr;
+    n = n_subset;
+  }
+  stp_plan* P = nullptr;
+  const stp_status st = stp_pack(tk, of, n, tr, fm, row_len, min_shared, flags, &P);
+  if (st) return st;
+  *n_rows = (int32_t)P->bins.size();
+  *packed = P->packed;
+  stp_plan_free(P);
+  return STP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+stp_status stp_plan_rows(const int32_t* tokens, const int64_t* offsets, int32_t n_seqs,
+                         const uint8_t* trainable, const int32_t* family, const int32_t* subset,
+                         int32_t n_subset, int32_t row_len, int32_t min_shared, uint32_t flags,
+                         int32_t* n_rows, int64_t* packed_tokens) {
+  stp::clear_error();
+  if (!n_rows || !packed_tokens) return fail(STP_EINVAL, "stp_plan_rows: NULL output");
+  if (n_seqs < 0 || n_subset < 0) return fail(STP_EINVAL, "stp_plan_rows: negative count");
+  if (n_seqs > 0 && !offsets) return fail(STP_EINVAL, "stp_plan_rows: offsets is NULL");
+  return plan_rows_one(tokens, offsets, n_seqs, trainable, family, subset, n_subset, row_len,
+                       min_shared, flags, n_rows, packed_tokens);
+}
+
+stp_status stp_plan_rows_many(const int32_t* tokens, const int64_t* offsets, int32_t n_seqs,
+                              const uint8_t* trainable, const int32_t* family,
+                              const int32_t* subsets, const int64_t* subset_offsets,
+                              int32_t n_subsets, int32_t row_len, int32_t min_shared,
+                              uint32_t flags, int32_t n_threads, int32_t* n_rows,
+                              int64_t* packed_tokens) {
+  stp::clear_error();
+  if (n_subsets < 0 || n_seqs < 0) return fail(STP_EINVAL, "stp_plan_rows_many: negative count");
+  if (n_subsets == 0) return STP_OK;
+  if (!subsets || !subset_offsets || !n_rows || !packed_tokens)
+    return fail(STP_EINVAL, "stp_plan_rows_many: NULL argument");
+  if (n_seqs > 0 && !offsets) return fail(STP_EINVAL, "stp_plan_rows_many: offsets is NULL");
+  if (subset_offsets[0] != 0) return fail(STP_EINVAL, "stp_plan_rows_many: subset_offsets[0] != 0");
+  for (int32_t i = 0; i < n_subsets; ++i)
+    if (subset_offsets[i + 1] < subset_offsets[i] || subset_offsets[i + 1] - subset_offsets[i] > INT32_MAX)
+      return fail(STP_EINVAL, "stp_plan_rows_many: subset_offsets decrease at %d", i);
+  int nt = n_threads > 0 ? n_threads : (int)std::thread::hardware_concurrency();
+  nt = std::max(1, std::min(nt, (int)n_subsets));
+  std::atomic<int32_t> next{0};
+  std::mutex mu;
+  stp_status first = STP_OK;
+  std::string msg;
+  auto work = [&]() {
+    for (int32_t i = next++; i < n_subsets; i = next++) {
+      const int64_t a = subset_offsets[i], b = subset_offsets[i + 1];
+      const stp_status st = plan_rows_one(tokens, offsets, n_seqs, trainable, family, subsets + a,
+                                          (int32_t)(b - a), row_len, min_shared, flags, n_rows + i,
+                                          packed_tokens + i);
+      if (st) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!first) {
+          first = st;
+          msg = "subset " + std::to_string(i) + ": " + stp_last_error();
+        }
+      }
+    }
+  };
+  try {
+    std::vector<std::thread> pool;
+    for (int t = 1; t < nt; ++t) pool.emplace_back(work);
+    work();
+    for (auto& th : pool) th.join();
+  } catch (const std::system_error&) {
+    return fail(STP_ENOMEM, "stp_plan_rows_many: cannot start host threads");
+  }
+  if (first) return fail(first, "stp_plan_rows_many: %s", msg.c_str());
+  return STP_OK;
+}
 
 const char* stp_last_error(void) { return stp::g_last_error.c_str(); }
 

@@ -24,6 +24,7 @@ STP_GLOBAL, STP_PER_FAMILY, STP_IN_ORDER = 0, 1, 2
 STP_BF16, STP_FP32 = 0, 1
 
 EXPORTED = ["stp_pack", "stp_plan_info", "stp_plan_write", "stp_plan_rows_of", "stp_plan_free",
+            "stp_plan_rows", "stp_plan_rows_many",
             "stp_count_tile_pairs", "stp_workspace_size", "stp_classify", "stp_classify_noalloc", "stp_read_tile_classes",
             "stp_attn_fwd", "stp_attn_bwd", "stp_step_scratch_size", "stp_attn_step_host",
             "stp_device_status", "stp_last_error", "stp_version"]
@@ -77,6 +78,13 @@ def lib():
         L.stp_plan_rows_of.restype = st
         L.stp_plan_free.argtypes = [_P]
         L.stp_plan_free.restype = None
+        L.stp_plan_rows.argtypes = [_I32P, _I64P, ctypes.c_int32, _U8P, _I32P, _I32P, ctypes.c_int32,
+                                    ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32, _I32P, _I64P]
+        L.stp_plan_rows.restype = st
+        L.stp_plan_rows_many.argtypes = [_I32P, _I64P, ctypes.c_int32, _U8P, _I32P, _I32P, _I64P,
+                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32,
+                                         ctypes.c_int32, _I32P, _I64P]
+        L.stp_plan_rows_many.restype = st
         L.stp_count_tile_pairs.argtypes = [_I32P, ctypes.c_int32, ctypes.c_int32, _I64P]
         L.stp_count_tile_pairs.restype = st
         L.stp_workspace_size.argtypes = [ctypes.POINTER(AttnDesc), _SZ, _SZ, _SZ]
@@ -214,6 +222,47 @@ class Desc:
         sc = self.scale if self.scale > 0 else self.head_dim ** -0.5
         return AttnDesc(self.n_rows, self.row_len, self.n_q_heads, self.n_kv_heads, self.head_dim,
                         self.dtype, sc, 128, 128, self.max_tile_pairs)
+
+
+def _pool(tokens, offsets, trainable, family):
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    offsets = np.ascontiguousarray(offsets, dtype=np.int64)
+    tr = None if trainable is None else np.ascontiguousarray(trainable, dtype=np.uint8)
+    fam = None if family is None else np.ascontiguousarray(family, dtype=np.int32)
+    return tokens, offsets, tr, fam
+
+
+def stp_plan_rows(tokens, offsets, trainable=None, family=None, subset=None, *, row_len: int,
+                  min_shared: int = 64, flags: int = STP_GLOBAL):
+    """(rows, packed tokens) that packing pool[subset] would give, without a plan."""
+    tokens, offsets, tr, fam = _pool(tokens, offsets, trainable, family)
+    sub = None if subset is None else np.ascontiguousarray(subset, dtype=np.int32)
+    r, pk = ctypes.c_int32(), ctypes.c_int64()
+    _check(lib().stp_plan_rows(_ptr(tokens, ctypes.c_int32), _ptr(offsets, ctypes.c_int64), len(offsets) - 1,
+                               _ptr(tr, ctypes.c_uint8), _ptr(fam, ctypes.c_int32), _ptr(sub, ctypes.c_int32),
+                               0 if sub is None else len(sub), int(row_len), int(min_shared), int(flags),
+                               ctypes.byref(r), ctypes.byref(pk)), "stp_plan_rows")
+    return r.value, pk.value
+
+
+def stp_plan_rows_many(tokens, offsets, trainable=None, family=None, subsets=(), *, row_len: int,
+                       min_shared: int = 64, flags: int = STP_GLOBAL, n_threads: int = 0):
+    """stp_plan_rows over a list of index arrays, planned in parallel on host threads."""
+    tokens, offsets, tr, fam = _pool(tokens, offsets, trainable, family)
+    subs = [np.ascontiguousarray(s, dtype=np.int32) for s in subsets]
+    so = np.zeros(len(subs) + 1, np.int64)
+    so[1:] = np.cumsum([len(s) for s in subs])
+    flat = np.concatenate(subs) if subs else np.zeros(0, np.int32)
+    rows = np.zeros(len(subs), np.int32)
+    packed = np.zeros(len(subs), np.int64)
+    if subs:
+        _check(lib().stp_plan_rows_many(_ptr(tokens, ctypes.c_int32), _ptr(offsets, ctypes.c_int64),
+                                        len(offsets) - 1, _ptr(tr, ctypes.c_uint8), _ptr(fam, ctypes.c_int32),
+                                        _ptr(flat, ctypes.c_int32), _ptr(so, ctypes.c_int64), len(subs),
+                                        int(row_len), int(min_shared), int(flags), int(n_threads),
+                                        _ptr(rows, ctypes.c_int32), _ptr(packed, ctypes.c_int64)),
+               "stp_plan_rows_many")
+    return rows, packed
 
 
 def stp_count_tile_pairs(subtree_end: np.ndarray) -> int:
