@@ -14,6 +14,8 @@ pages describe it:
 * ``oracle.attn``  -- ancestor sets taken from parent pointers, the tile
   classes by brute force, and explicit ancestor-masked softmax attention
   with its analytic backward, in float64.
+* ``oracle.index`` -- the tree-aware top-k indexer: scores over a query's
+  ancestor candidates only, top k with ties to the smaller key index.
 
 Pins (in ``tests/test_oracle_*.py``) tie every function here to something
 other than itself: the worked examples the pages print, closed forms,
