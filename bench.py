@@ -65,6 +65,33 @@ def _peaks():
         return 1900.0, 6800.0, "fallback"
 
 
+def _indexer(R, T, se, tile_meta, pairs, useful, dev, heads=8, dim=64, top_k=512, reps=10) -> dict:
+    """The tree-aware top-k indexer on the same packed row (device leg's
+    classification): scoring over ancestor candidates + top-k selection."""
+    import torch
+    from sft_trie_build_gb300 import stp
+
+    q, k, w = (x.to(dev) for x in W.index_tensors(R, T, heads, dim, seed=23))
+    idesc = stp.index_desc(R, T, heads, dim, top_k, pairs)
+    ws = torch.empty(stp.stp_index_workspace_size(idesc), dtype=torch.uint8, device=dev)
+    idx = torch.empty(R, T, top_k, dtype=torch.int32, device=dev)
+    sc = torch.empty(R, T, top_k, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        stp.stp_index_topk(idesc, q, k, w, se, tile_meta, idx, sc, ws)
+    torch.cuda.synchronize()
+    assert stp.stp_device_status(ws) == stp.STP_OK
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        stp.stp_index_topk(idesc, q, k, w, se, tile_meta, idx, sc, ws)
+    e.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(e) / reps
+    return {"heads": heads, "head_dim": dim, "top_k": top_k, "ms": ms,
+            "candidate_pairs_per_s": useful / (ms / 1e3),
+            "useful_scoring_tflops": 2.0 * heads * dim * useful / (ms / 1e3) / 1e12}
+
+
 def _what_if(n_candidates: int = 64, groups_per_candidate: int = 8) -> dict:
     """Host 'what if' planning: rows that candidate batches (whole groups drawn
     from the curriculum pool) would need, global tree vs one tree per group,
@@ -438,6 +465,7 @@ def main():
     }
     if rank == 0:
         line["what_if"] = _what_if()
+        line["indexer"] = _indexer(R, T, se, buf.tile_meta, desc.max_tile_pairs, useful, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import pack as OP
         plan_o = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared, b.family)

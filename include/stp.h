@@ -326,6 +326,44 @@ stp_status stp_attn_step_host(const stp_attn_desc* desc, int32_t n_chunks, const
                               size_t scratch_bytes, void* stream);
 
 /*
+ * Tree-aware top-k indexer ([P1] attention section, the sparse top-k indexer
+ * variants: the indexer scores candidates from a query's own ancestor chain
+ * only -- the interval check of the mask -- so keys of a sibling branch are
+ * never proposed).  For query i of a packed row:
+ *   score(i, j) = sum_h w[i, h] * max(q[i, h] . k[j], 0)  over visible j
+ * and the selection is the top_k visible keys of largest score (ties to the
+ * smaller key index), listed in ascending key order, padded with index -1 and
+ * score -inf when fewer keys are visible.  Scores are bf16 products summed in
+ * float32 on the tensor cores; the selection is exact on those float32 scores.
+ */
+typedef struct {
+  int32_t n_rows;         /* R                                                  */
+  int32_t row_len;        /* T, a multiple of 128, at most 131072               */
+  int32_t n_heads;        /* H indexer heads, H * head_dim <= 512               */
+  int32_t head_dim;       /* D: 64 or 128                                       */
+  int32_t top_k;          /* k in [1, 4096]                                     */
+  int32_t max_tile_pairs; /* as in stp_attn_desc; sizes the score workspace     */
+} stp_index_desc;
+
+/* Device workspace of stp_index_topk: 256 bytes + 64 KiB per tile pair. */
+stp_status stp_index_workspace_size(const stp_index_desc* desc, size_t* ws_bytes);
+
+/*
+ *   q           device bf16 [R, T, H, D]     k  device bf16 [R, T, D]
+ *   w           device float32 [R, T, H]     (per-query head weights)
+ *   d_subtree_end, d_tile_meta   as for stp_attn_fwd: stp_classify already run
+ *               with an stp_attn_desc of the same n_rows, row_len and
+ *               max_tile_pairs
+ *   topk_idx    device int32 [R, T, top_k]  (row-local key indices)
+ *   topk_score  device float32 [R, T, top_k]
+ *   d_ws        device, stp_index_workspace_size bytes, 256-byte aligned; its
+ *               first word is the device error word (stp_device_status)
+ */
+stp_status stp_index_topk(const stp_index_desc* desc, const void* q, const void* k, const float* w,
+                          const int32_t* d_subtree_end, const void* d_tile_meta, int32_t* topk_idx,
+                          float* topk_score, void* d_ws, void* stream);
+
+/*
  * Read the device error word of a workspace (fwd_ws or bwd_ws): synchronizes
  * the stream, then *out = STP_OK or STP_EDEVICE (a device check tripped or a
  * bounded wait ran out; the kernel returned early and its outputs are invalid).

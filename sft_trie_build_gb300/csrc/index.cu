@@ -1,0 +1,432 @@
+// Tree-aware top-k indexer ("Prefix tree packing", attention section, the
+// sparse top-k indexer variants): sparse attention gathers the key indices it
+// is handed, so the tree lives in the indexer, which scores candidates from a
+// query's own ancestor chain only (the enter/exit interval check of the mask)
+// and never proposes a sibling branch's keys.
+//
+//   score(i, j) = sum_h w[i, h] * max(q[i, h] . k[j], 0)   for visible j
+//   top-k(i)    = the k visible keys of largest score, ties to the smaller
+//                 key index, listed in ascending key order (padded with -1).
+//
+// Two kernels, both driven by the per-query-tile key-tile lists and the pair
+// numbering of stp_classify:
+//   index_scores_kernel  one CTA per (row, query tile): the tile's Q of every
+//                        indexer head once (TMA), its non-empty key tiles
+//                        through a two-stage ring; S_h = Q_h K^T on tcgen05
+//                        (four heads per pass in TMEM), and four epilogue
+//                        warps (thread = query = TMEM lane) accumulate
+//                        w * relu(S) in registers, apply the predicate on
+//                        PARTIAL tiles and write the tile's scores key-major
+//                        ([128 keys][128 queries] fp32) to the pair's slot.
+//   index_select_kernel  one thread per query: a 4-pass byte-wise radix
+//                        select over the query's candidate scores finds the
+//                        k-th largest, then one ascending pass emits the keys.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "layout.h"
+#include "tc_ptx.cuh"
+
+namespace stp {
+namespace {
+
+using namespace tc;
+
+constexpr int kIdxThreads = 192;       // warps 0-3 epilogue, warp 4 TMA, warp 5 MMA
+constexpr int kIdxSlots = 4;           // heads per TMEM pass (128 columns each)
+constexpr int kIdxQBytesMax = 131072;  // Q of all heads: H * D * 256 bytes
+constexpr int kIdxSmallBytes = 256;
+constexpr int kScoreTile = 128 * 128;  // floats per (pair) score tile
+constexpr int kSelThreads = 128;
+
+struct IdxParams {
+  int R, T, NT, H, D, top_k;
+  int64_t cap;
+  const int32_t* se;
+  const int32_t* csr_cnt;
+  const int32_t* csr;
+  const int32_t* csr_off;
+  const int32_t* row_base;
+  const float* w;       // [R*T, H]
+  float* scores;        // [cap][128 keys][128 queries]
+  int32_t* out_idx;     // [R*T, k]
+  float* out_score;     // [R*T, k]
+  uint32_t* err;
+};
+
+enum { X_Q = 0, X_KF = 1, X_KE = 3, X_SF = 5, X_SFREE = 6, X_DRAIN = 7, X_COUNT = 8 };
+
+typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                             const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                             CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// [rows, H, D] bf16 as a 3-D tensor (d, head, row); 64 d x 1 head x 128 rows
+// boxes, 128-byte swizzled.
+bool make_map_d(CUtensorMap* m, const void* base, int64_t rows, int H, int D) {
+  EncodeFn enc = encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+__global__ void __launch_bounds__(kIdxThreads, 1)
+    index_scores_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                        const IdxParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int tile_bytes = 128 * p.D * 2;          // one 128-row tile of one head
+  const int q_bytes = p.H * tile_bytes;
+  uint8_t* big = smem_raw;
+  const uint32_t big_s = smem_u32(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + q_bytes + 2 * tile_bytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + X_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = p.NT - 1 - (int)(blockIdx.x / p.R);   // longest lists first
+  const int r = (int)(blockIdx.x % p.R);
+  const int cnt = p.csr_cnt[(size_t)r * p.NT + qt];
+  const int32_t* list = p.csr + ((size_t)r * p.NT + qt) * p.NT;
+  const int64_t pbase = (int64_t)p.row_base[r] + p.csr_off[(size_t)r * p.NT + qt];
+  const int row0 = r * p.T;
+  const int n_groups = (p.H + kIdxSlots - 1) / kIdxSlots;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < X_COUNT; ++b) mbar_init(&bars[b], b == X_SFREE ? 4 : 1);
+    *abort_flag = 0;
+    if ((big_s & 1023u) != 0 || cnt <= 0 || cnt > p.NT) {
+      *abort_flag = 1;
+      atomicOr(p.err, (big_s & 1023u) != 0 ? kErrTmem : kErrBadList);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const bool run = !*abort_flag;
+
+  if (warp == 4) {
+    if (lane == 0 && run) {
+      // ------------------------------------------------------------ loads
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      mbar_expect_tx(&bars[X_Q], (uint32_t)q_bytes);
+      for (int h = 0; h < p.H; ++h)
+        for (int db = 0; db < p.D / 64; ++db)
+          tma_load_3d(big + h * tile_bytes + db * 16384, &tq, &bars[X_Q], db * 64, h, row0 + qt * 128);
+      int issued[2] = {-1, -1};
+      for (int e = 0; e < cnt; ++e) {
+        const int st = e & 1, n = e >> 1, kt = list[e] >> 1;
+        if (kt < 0 || kt > qt) {
+          *abort_flag = 1;
+          atomicOr(p.err, kErrBadList);
+          break;
+        }
+        if (e >= 2 && !mbar_wait(&bars[X_KE + st], (n - 1) & 1, abort_flag, p.err)) break;
+        mbar_expect_tx(&bars[X_KF + st], (uint32_t)tile_bytes);
+        for (int db = 0; db < p.D / 64; ++db)
+          tma_load_3d(big + q_bytes + st * tile_bytes + db * 16384, &tk, &bars[X_KF + st], db * 64, 0,
+                      row0 + kt * 128);
+        issued[st] = n;
+      }
+      mbar_wait_drain(&bars[X_Q], 0);
+      for (int st = 0; st < 2; ++st)
+        if (issued[st] >= 0) mbar_wait_drain(&bars[X_KF + st], issued[st] & 1);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0 && run) {
+      // ------------------------------------------------------------ MMA
+      constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+      auto km = [](int kk) { return (uint32_t)((kk >> 2) * (16384 >> 4) + (kk & 3) * 2); };
+      const int nk = p.D / 16;
+      bool ok = mbar_wait(&bars[X_Q], 0, abort_flag, p.err);
+      int u = 0;  // head passes issued so far
+      for (int e = 0; ok && e < cnt; ++e) {
+        const int st = e & 1;
+        if (!mbar_wait(&bars[X_KF + st], (e >> 1) & 1, abort_flag, p.err)) break;
+        const uint32_t k_km = desc_lo_kmajor(big_s + q_bytes + st * tile_bytes);
+        for (int hg = 0; ok && hg < n_groups; ++hg, ++u) {
+          if (u > 0 && !mbar_wait(&bars[X_SFREE], (u - 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          fence_after_sync();
+          for (int hs = 0; hs < kIdxSlots && kIdxSlots * hg + hs < p.H; ++hs) {
+            const uint32_t q_km = desc_lo_kmajor(big_s + (kIdxSlots * hg + hs) * tile_bytes);
+            for (int kk = 0; kk < nk; ++kk) mma_ss_lo(tmem + hs * 128, q_km + km(kk), k_km + km(kk), idesc, kk > 0);
+          }
+          mma_commit(&bars[X_SF]);
+        }
+        if (ok) mma_commit(&bars[X_KE + st]);
+      }
+      mma_commit(&bars[X_DRAIN]);
+      mbar_wait_drain(&bars[X_DRAIN], 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int il = threadIdx.x;                 // query row = TMEM lane
+    const int i = qt * 128 + il;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float* wrow = p.w + ((size_t)row0 + i) * p.H;
+    bool ok = run;
+    int u = 0;
+    for (int e = 0; ok && e < cnt; ++e) {
+      const int ent = list[e], kt = ent >> 1, part = ent & 1;
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+      for (int hg = 0; hg < n_groups; ++hg, ++u) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[X_SF], u & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        for (int hs = 0; hs < kIdxSlots && kIdxSlots * hg + hs < p.H; ++hs) {
+          const float wi = wrow[kIdxSlots * hg + hs];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t x[32];
+            tmem_ld32(tmem + lane_base + hs * 128 + c * 32, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int m = 0; m < 32; ++m) acc[c * 32 + m] = fmaf(wi, fmaxf(__uint_as_float(x[m]), 0.f), acc[c * 32 + m]);
+          }
+        }
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[X_SFREE]);
+      }
+      if (!ok) break;
+      const int64_t pair = pbase + e;
+      if (pair < 0 || pair >= p.cap) {
+        atomicOr(p.err, kErrCapacity);
+        continue;
+      }
+      float* out = p.scores + (size_t)pair * kScoreTile + il;
+      const int32_t* se_tile = p.se + (size_t)row0 + kt * 128;
+#pragma unroll
+      for (int j = 0; j < 128; ++j) {
+        const int jk = kt * 128 + j;
+        const bool vis = !part || (jk <= i && __ldg(se_tile + j) >= i);
+        out[j * 128] = vis ? acc[j] : -INFINITY;   // key-major: a warp writes 128 contiguous bytes
+      }
+    }
+  }
+
+  __syncwarp();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// float -> uint32 with the same order (larger float, larger key)
+__device__ __forceinline__ uint32_t order_key(float s) {
+  const uint32_t u = __float_as_uint(s);
+  return (u >> 31) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(kSelThreads) index_select_kernel(const IdxParams p) {
+  extern __shared__ uint32_t hist[];   // [256 bins][128 threads]
+  const int qt = p.NT - 1 - (int)(blockIdx.x / p.R);
+  const int r = (int)(blockIdx.x % p.R);
+  const int il = threadIdx.x, i = qt * 128 + il;
+  const int cnt = p.csr_cnt[(size_t)r * p.NT + qt];
+  const int32_t* list = p.csr + ((size_t)r * p.NT + qt) * p.NT;
+  const int64_t pbase = (int64_t)p.row_base[r] + p.csr_off[(size_t)r * p.NT + qt];
+  const int k = p.top_k;
+  int32_t* oi = p.out_idx + ((size_t)r * p.T + i) * k;
+  float* os = p.out_score + ((size_t)r * p.T + i) * k;
+  if (cnt <= 0 || cnt > p.NT || pbase + cnt > p.cap) {
+    if (il == 0) atomicOr(p.err, cnt <= 0 || cnt > p.NT ? kErrBadList : kErrCapacity);
+    for (int n = 0; n < k; ++n) {
+      oi[n] = -1;
+      os[n] = -INFINITY;
+    }
+    return;
+  }
+  auto tile = [&](int e) { return p.scores + (size_t)(pbase + e) * kScoreTile + il; };
+  // candidates: visible keys (finite scores)
+  int n_cand = 0;
+  for (int e = 0; e < cnt; ++e) {
+    const float* t = tile(e);
+    for (int j = 0; j < 128; ++j) n_cand += t[j * 128] != -INFINITY;
+  }
+  uint32_t thr = 0;     // key of the k-th largest candidate
+  int ties = 0;         // candidates equal to thr to keep (smallest key index first)
+  const bool all = n_cand <= k;
+  if (!all) {
+    uint32_t prefix = 0, mask = 0;
+    int remaining = k;
+    for (int b = 3; b >= 0; --b) {
+      for (int bin = 0; bin < 256; ++bin) hist[bin * kSelThreads + il] = 0;
+      for (int e = 0; e < cnt; ++e) {
+        const float* t = tile(e);
+        for (int j = 0; j < 128; ++j) {
+          const float s = t[j * 128];
+          if (s == -INFINITY) continue;
+          const uint32_t key = order_key(s);
+          if ((key & mask) == prefix) ++hist[((key >> (8 * b)) & 255u) * kSelThreads + il];
+        }
+      }
+      int cum = 0;
+      for (int bin = 255; bin >= 0; --bin) {
+        const int c = hist[bin * kSelThreads + il];
+        if (cum + c >= remaining) {
+          prefix |= (uint32_t)bin << (8 * b);
+          remaining -= cum;
+          break;
+        }
+        cum += c;
+      }
+      mask |= 255u << (8 * b);
+    }
+    thr = prefix;
+    ties = remaining;
+  }
+  int n = 0;
+  for (int e = 0; e < cnt; ++e) {
+    const float* t = tile(e);
+    const int kt = list[e] >> 1;
+    for (int j = 0; j < 128 && n < k; ++j) {
+      const float s = t[j * 128];
+      if (s == -INFINITY) continue;
+      bool take = all;
+      if (!all) {
+        const uint32_t key = order_key(s);
+        if (key > thr) {
+          take = true;
+        } else if (key == thr && ties > 0) {
+          take = true;
+          --ties;
+        }
+      }
+      if (take) {
+        oi[n] = kt * 128 + j;
+        os[n] = s;
+        ++n;
+      }
+    }
+  }
+  for (; n < k; ++n) {
+    oi[n] = -1;
+    os[n] = -INFINITY;
+  }
+}
+
+stp_status check_index_desc(const stp_index_desc* d) {
+  if (!d) return fail(STP_EINVAL, "index descriptor is NULL");
+  if (d->n_rows < 0) return fail(STP_EINVAL, "n_rows < 0");
+  if (d->row_len <= 0 || d->row_len % kTile || d->row_len > kMaxRowLen)
+    return fail(STP_EUNSUPPORTED, "row_len %d must be a positive multiple of 128 and <= %d", d->row_len, kMaxRowLen);
+  if (d->head_dim != 64 && d->head_dim != 128) return fail(STP_EUNSUPPORTED, "head_dim must be 64 or 128");
+  if (d->n_heads < 1 || (int64_t)d->n_heads * d->head_dim * 256 > kIdxQBytesMax)
+    return fail(STP_EUNSUPPORTED, "need n_heads >= 1 and n_heads * head_dim <= 512 (got %d x %d)", d->n_heads,
+                d->head_dim);
+  if (d->top_k < 1 || d->top_k > 4096) return fail(STP_EUNSUPPORTED, "top_k must lie in [1, 4096]");
+  if (d->max_tile_pairs < 0) return fail(STP_EINVAL, "max_tile_pairs must be >= 0");
+  return STP_OK;
+}
+
+}  // namespace
+}  // namespace stp
+
+using namespace stp;
+
+extern "C" stp_status stp_index_workspace_size(const stp_index_desc* desc, size_t* ws_bytes) {
+  clear_error();
+  stp_status st = check_index_desc(desc);
+  if (st) return st;
+  if (!ws_bytes) return fail(STP_EINVAL, "stp_index_workspace_size: NULL output");
+  const int64_t cap = pair_capacity(desc->n_rows, desc->row_len / kTile, desc->max_tile_pairs);
+  *ws_bytes = 256 + (size_t)cap * kScoreTile * sizeof(float);
+  return STP_OK;
+}
+
+extern "C" stp_status stp_index_topk(const stp_index_desc* desc, const void* q, const void* k,
+                                     const float* w, const int32_t* d_subtree_end,
+                                     const void* d_tile_meta, int32_t* topk_idx, float* topk_score,
+                                     void* d_ws, void* stream) {
+  clear_error();
+  stp_status st = check_index_desc(desc);
+  if (st) return st;
+  if (!q || !k || !w || !d_subtree_end || !d_tile_meta || !topk_idx || !topk_score || !d_ws)
+    return fail(STP_EINVAL, "stp_index_topk: NULL device pointer");
+  auto mis = [](const void* x, uintptr_t a) { return (reinterpret_cast<uintptr_t>(x) & (a - 1)) != 0; };
+  if (mis(q, 16) || mis(k, 16) || mis(w, 4) || mis(d_tile_meta, 256) || mis(d_ws, 256))
+    return fail(STP_EINVAL, "stp_index_topk: q, k 16-byte, tile_meta and ws 256-byte aligned");
+  if (desc->n_rows == 0) return STP_OK;
+  const int NT = desc->row_len / kTile;
+  const TileMeta m = tile_meta_layout(desc->n_rows, NT);
+  const char* tm = static_cast<const char*>(d_tile_meta);
+  IdxParams p;
+  p.R = desc->n_rows;
+  p.T = desc->row_len;
+  p.NT = NT;
+  p.H = desc->n_heads;
+  p.D = desc->head_dim;
+  p.top_k = desc->top_k;
+  p.cap = pair_capacity(desc->n_rows, NT, desc->max_tile_pairs);
+  p.se = d_subtree_end;
+  p.csr_cnt = reinterpret_cast<const int32_t*>(tm + m.csr_cnt);
+  p.csr = reinterpret_cast<const int32_t*>(tm + m.csr);
+  p.csr_off = reinterpret_cast<const int32_t*>(tm + m.csr_off);
+  p.row_base = reinterpret_cast<const int32_t*>(tm + m.row_base);
+  p.w = w;
+  p.err = static_cast<uint32_t*>(d_ws);
+  p.scores = reinterpret_cast<float*>(static_cast<char*>(d_ws) + 256);
+  p.out_idx = topk_idx;
+  p.out_score = topk_score;
+  const int64_t rows = (int64_t)desc->n_rows * desc->row_len;
+  CUtensorMap mq, mk;
+  if (!make_map_d(&mq, q, rows, p.H, p.D) || !make_map_d(&mk, k, rows, 1, p.D))
+    return fail(STP_ECUDA, "stp_index_topk: tensor map encoding failed");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(p.err, 0, 4, s);
+  const int smem = p.H * 128 * p.D * 2 + 2 * 128 * p.D * 2 + kIdxSmallBytes;
+  const int smem_sel = 256 * kSelThreads * 4;
+  static bool attr = false;
+  if (e == cudaSuccess && !attr) {
+    e = cudaFuncSetAttribute(index_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kIdxQBytesMax + 2 * 128 * 128 * 2 + kIdxSmallBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(index_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_sel);
+    attr = e == cudaSuccess;
+  }
+  if (e != cudaSuccess) return fail(STP_ECUDA, "stp_index_topk: %s", cudaGetErrorString(e));
+  const unsigned grid = (unsigned)(NT * desc->n_rows);
+  index_scores_kernel<<<grid, kIdxThreads, smem, s>>>(mq, mk, p);
+  index_select_kernel<<<grid, kSelThreads, smem_sel, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(STP_ECUDA, "stp_index_topk: %s", cudaGetErrorString(e));
+  return STP_OK;
+}

@@ -27,6 +27,7 @@ EXPORTED = ["stp_pack", "stp_plan_info", "stp_plan_write", "stp_plan_rows_of", "
             "stp_plan_rows", "stp_plan_rows_many",
             "stp_count_tile_pairs", "stp_workspace_size", "stp_classify", "stp_classify_noalloc", "stp_read_tile_classes",
             "stp_attn_fwd", "stp_attn_bwd", "stp_step_scratch_size", "stp_attn_step_host",
+            "stp_index_workspace_size", "stp_index_topk",
             "stp_device_status", "stp_last_error", "stp_version"]
 
 
@@ -41,6 +42,11 @@ class PlanInfo(ctypes.Structure):
                 ("input_tokens", ctypes.c_int64), ("packed_tokens", ctypes.c_int64),
                 ("n_segments", ctypes.c_int64), ("n_leaves", ctypes.c_int64),
                 ("useful_pairs", ctypes.c_int64), ("tree_token_ratio", ctypes.c_double)]
+
+
+class IndexDesc(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int32), ("row_len", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("top_k", ctypes.c_int32), ("max_tile_pairs", ctypes.c_int32)]
 
 
 class AttnDesc(ctypes.Structure):
@@ -104,6 +110,10 @@ def lib():
         L.stp_attn_step_host.argtypes = [ctypes.POINTER(AttnDesc), ctypes.c_int32] + [_P] * 12 + \
             [ctypes.c_size_t, _P]
         L.stp_attn_step_host.restype = st
+        L.stp_index_workspace_size.argtypes = [ctypes.POINTER(IndexDesc), _SZ]
+        L.stp_index_workspace_size.restype = st
+        L.stp_index_topk.argtypes = [ctypes.POINTER(IndexDesc)] + [_P] * 9
+        L.stp_index_topk.restype = st
         L.stp_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
         L.stp_device_status.restype = st
         L.stp_last_error.argtypes = []
@@ -342,6 +352,22 @@ def stp_attn_step_host(desc: Desc, n_chunks: int, q, k, v, d_o, subtree_end, til
                                     _dptr(dq), _dptr(dk), _dptr(dv), _dptr(scratch),
                                     scratch.numel() * scratch.element_size(), _stream(stream)),
            "stp_attn_step_host")
+
+
+def index_desc(n_rows, row_len, n_heads, head_dim, top_k, max_tile_pairs=0) -> IndexDesc:
+    return IndexDesc(n_rows, row_len, n_heads, head_dim, top_k, max_tile_pairs)
+
+
+def stp_index_workspace_size(desc: IndexDesc) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().stp_index_workspace_size(ctypes.byref(desc), ctypes.byref(out)), "stp_index_workspace_size")
+    return out.value
+
+
+def stp_index_topk(desc: IndexDesc, q, k, w, subtree_end, tile_meta, topk_idx, topk_score, ws, stream=None):
+    _check(lib().stp_index_topk(ctypes.byref(desc), _dptr(q), _dptr(k), _dptr(w), _dptr(subtree_end),
+                                _dptr(tile_meta), _dptr(topk_idx), _dptr(topk_score), _dptr(ws), _stream(stream)),
+           "stp_index_topk")
 
 
 def stp_device_status(ws, stream=None) -> int:

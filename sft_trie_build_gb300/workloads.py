@@ -361,3 +361,17 @@ def attn_tensors(shape: AttnShape, seed: int = 0, device="cpu"):
     if shape.dtype == "bf16":
         q, k, v, do = (t.to(torch.bfloat16) for t in (q, k, v, do))
     return tuple(t.to(device) for t in (q, k, v, do))
+
+
+def index_tensors(n_rows: int, row_len: int, n_heads: int, head_dim: int, seed: int = 0, device="cpu"):
+    """Indexer inputs: q [R, T, H, D] and k [R, T, D] drawn N(0, 1/D) and rounded
+    to bf16, w [R, T, H] uniform in [0, 1) float32; seeded CPU torch generator."""
+    import torch
+
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    s = float(head_dim) ** -0.5
+    q = (torch.randn(n_rows, row_len, n_heads, head_dim, generator=g) * s).to(torch.bfloat16)
+    k = (torch.randn(n_rows, row_len, head_dim, generator=g) * s).to(torch.bfloat16)
+    w = torch.rand(n_rows, row_len, n_heads, generator=g)
+    return q.to(device), k.to(device), w.to(device)
