@@ -18,9 +18,10 @@
 //                        w * relu(S) in registers, apply the predicate on
 //                        PARTIAL tiles and write the tile's scores key-major
 //                        ([128 keys][128 queries] fp32) to the pair's slot.
-//   index_select_kernel  one thread per query: a 4-pass byte-wise radix
-//                        select over the query's candidate scores finds the
-//                        k-th largest, then one ascending pass emits the keys.
+//   index_select_kernel  one CTA per (row, query tile): byte-wise radix
+//                        select of each query's k-th largest candidate score
+//                        (histograms in shared memory), then the keys above
+//                        it, and the ties it needs, emitted in ascending order.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -41,7 +42,9 @@ constexpr int kIdxSlots = 4;           // heads per TMEM pass (128 columns each)
 constexpr int kIdxQBytesMax = 131072;  // Q of all heads: H * D * 256 bytes
 constexpr int kIdxSmallBytes = 256;
 constexpr int kScoreTile = 128 * 128;  // floats per (pair) score tile
-constexpr int kSelThreads = 128;
+constexpr int kSelThreads = 1024;  // 32 warps: 2 query groups x 16 key-tile ranges
+constexpr int kSelQ = 64;          // queries per selection CTA (half a query tile)
+constexpr int kSelSplit = 32 / (kSelQ / 32);
 
 struct IdxParams {
   int R, T, NT, H, D, top_k;
@@ -255,92 +258,142 @@ __device__ __forceinline__ uint32_t order_key(float s) {
   return (u >> 31) ? ~u : (u | 0x80000000u);
 }
 
+// One CTA per (row, half a query tile), 32 warps: warp w serves queries
+// 32 (w % 2) .. +31 of the half (lane = query) over the (w / 2)-th of sixteen
+// contiguous ranges of the tile's key-tile list.  Four byte-wise radix passes build each
+// query's histogram in shared memory (atomics across the eight ranges) and
+// pin the k-th largest score; a counting pass then gives every range its
+// output offset, so the ranges emit in parallel and the keys still come out
+// in ascending order, ties to the smaller key index.
 __global__ void __launch_bounds__(kSelThreads) index_select_kernel(const IdxParams p) {
-  extern __shared__ uint32_t hist[];   // [256 bins][128 threads]
-  const int qt = p.NT - 1 - (int)(blockIdx.x / p.R);
-  const int r = (int)(blockIdx.x % p.R);
-  const int il = threadIdx.x, i = qt * 128 + il;
+  extern __shared__ uint32_t hist[];   // [256 bins][kSelQ queries]
+  __shared__ uint32_t s_prefix[kSelQ], s_mask[kSelQ];
+  __shared__ int s_rem[kSelQ], s_all[kSelQ];
+  __shared__ int s_gt[kSelSplit][kSelQ], s_eq[kSelSplit][kSelQ];
+  constexpr int kHalves = 128 / kSelQ;
+  const int qt = p.NT - 1 - (int)(blockIdx.x / (p.R * kHalves));
+  const int r = (int)(blockIdx.x / kHalves % p.R), half = (int)(blockIdx.x % kHalves);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kGroups = kSelQ / 32;
+  const int qg = warp % kGroups, ts = warp / kGroups;
+  const int ql = qg * 32 + lane;               // query within the CTA
+  const int il = half * kSelQ + ql, i = qt * 128 + il;
   const int cnt = p.csr_cnt[(size_t)r * p.NT + qt];
   const int32_t* list = p.csr + ((size_t)r * p.NT + qt) * p.NT;
   const int64_t pbase = (int64_t)p.row_base[r] + p.csr_off[(size_t)r * p.NT + qt];
   const int k = p.top_k;
   int32_t* oi = p.out_idx + ((size_t)r * p.T + i) * k;
   float* os = p.out_score + ((size_t)r * p.T + i) * k;
-  if (cnt <= 0 || cnt > p.NT || pbase + cnt > p.cap) {
-    if (il == 0) atomicOr(p.err, cnt <= 0 || cnt > p.NT ? kErrBadList : kErrCapacity);
-    for (int n = 0; n < k; ++n) {
-      oi[n] = -1;
-      os[n] = -INFINITY;
-    }
+  if (cnt <= 0 || cnt > p.NT || pbase + cnt > p.cap) {   // uniform over the CTA
+    if (threadIdx.x == 0) atomicOr(p.err, cnt <= 0 || cnt > p.NT ? kErrBadList : kErrCapacity);
+    if (ts == 0)
+      for (int n = 0; n < k; ++n) {
+        oi[n] = -1;
+        os[n] = -INFINITY;
+      }
     return;
   }
+  const int e0 = ts * cnt / kSelSplit, e1 = (ts + 1) * cnt / kSelSplit;
   auto tile = [&](int e) { return p.scores + (size_t)(pbase + e) * kScoreTile + il; };
-  // candidates: visible keys (finite scores)
-  int n_cand = 0;
-  for (int e = 0; e < cnt; ++e) {
-    const float* t = tile(e);
-    for (int j = 0; j < 128; ++j) n_cand += t[j * 128] != -INFINITY;
+  if (threadIdx.x < kSelQ) {
+    s_prefix[threadIdx.x] = 0;
+    s_mask[threadIdx.x] = 0;
+    s_rem[threadIdx.x] = k;
+    s_all[threadIdx.x] = 0;
   }
-  uint32_t thr = 0;     // key of the k-th largest candidate
-  int ties = 0;         // candidates equal to thr to keep (smallest key index first)
-  const bool all = n_cand <= k;
-  if (!all) {
-    uint32_t prefix = 0, mask = 0;
-    int remaining = k;
-    for (int b = 3; b >= 0; --b) {
-      for (int bin = 0; bin < 256; ++bin) hist[bin * kSelThreads + il] = 0;
-      for (int e = 0; e < cnt; ++e) {
+  for (int b = 3; b >= 0; --b) {
+    for (int x = threadIdx.x; x < 256 * kSelQ; x += kSelThreads) hist[x] = 0;
+    __syncthreads();
+    const uint32_t prefix = s_prefix[ql], mask = s_mask[ql];
+    if (!s_all[ql]) {
+      for (int e = e0; e < e1; ++e) {
         const float* t = tile(e);
         for (int j = 0; j < 128; ++j) {
-          const float s = t[j * 128];
-          if (s == -INFINITY) continue;
-          const uint32_t key = order_key(s);
-          if ((key & mask) == prefix) ++hist[((key >> (8 * b)) & 255u) * kSelThreads + il];
+          const float sc = t[j * 128];
+          if (sc == -INFINITY) continue;
+          const uint32_t key = order_key(sc);
+          if ((key & mask) == prefix) atomicAdd(&hist[((key >> (8 * b)) & 255u) * kSelQ + ql], 1u);
         }
       }
-      int cum = 0;
-      for (int bin = 255; bin >= 0; --bin) {
-        const int c = hist[bin * kSelThreads + il];
-        if (cum + c >= remaining) {
-          prefix |= (uint32_t)bin << (8 * b);
-          remaining -= cum;
-          break;
-        }
-        cum += c;
-      }
-      mask |= 255u << (8 * b);
     }
-    thr = prefix;
-    ties = remaining;
+    __syncthreads();
+    if (threadIdx.x < kSelQ) {
+      const int q = threadIdx.x;
+      if (b == 3) {
+        int total = 0;
+        for (int bin = 0; bin < 256; ++bin) total += (int)hist[bin * kSelQ + q];
+        if (total <= k) s_all[q] = 1;
+      }
+      if (!s_all[q]) {
+        const int remaining = s_rem[q];
+        int cum = 0;
+        for (int bin = 255; bin >= 0; --bin) {
+          const int c = (int)hist[bin * kSelQ + q];
+          if (cum + c >= remaining) {
+            s_prefix[q] |= (uint32_t)bin << (8 * b);
+            s_rem[q] = remaining - cum;
+            break;
+          }
+          cum += c;
+        }
+        s_mask[q] |= 255u << (8 * b);
+      }
+    }
+    __syncthreads();
   }
-  int n = 0;
-  for (int e = 0; e < cnt; ++e) {
+  const uint32_t thr = s_prefix[ql];
+  const int ties = s_rem[ql];
+  const bool all = s_all[ql] != 0;
+  // counting pass: keys above the threshold and keys equal to it, per range
+  int gt = 0, eq = 0;
+  for (int e = e0; e < e1; ++e) {
+    const float* t = tile(e);
+    for (int j = 0; j < 128; ++j) {
+      const float sc = t[j * 128];
+      if (sc == -INFINITY) continue;
+      if (all) {
+        ++gt;
+      } else {
+        const uint32_t key = order_key(sc);
+        gt += key > thr;
+        eq += key == thr;
+      }
+    }
+  }
+  s_gt[ts][ql] = gt;
+  s_eq[ts][ql] = eq;
+  __syncthreads();
+  int before = 0, eq_before = 0;
+  for (int t2 = 0; t2 < ts; ++t2) {
+    before += s_gt[t2][ql];
+    eq_before += s_eq[t2][ql];
+  }
+  int n = before + (all ? 0 : min(ties, eq_before));
+  int my_ties = all ? 0 : max(0, min(eq, ties - eq_before));
+  for (int e = e0; e < e1; ++e) {
     const float* t = tile(e);
     const int kt = list[e] >> 1;
-    for (int j = 0; j < 128 && n < k; ++j) {
-      const float s = t[j * 128];
-      if (s == -INFINITY) continue;
+    for (int j = 0; j < 128; ++j) {
+      const float sc = t[j * 128];
+      if (sc == -INFINITY) continue;
       bool take = all;
       if (!all) {
-        const uint32_t key = order_key(s);
-        if (key > thr) {
-          take = true;
-        } else if (key == thr && ties > 0) {
-          take = true;
-          --ties;
-        }
+        const uint32_t key = order_key(sc);
+        take = key > thr || (key == thr && my_ties > 0);
+        if (key == thr && my_ties > 0) --my_ties;
       }
       if (take) {
         oi[n] = kt * 128 + j;
-        os[n] = s;
+        os[n] = sc;
         ++n;
       }
     }
   }
-  for (; n < k; ++n) {
-    oi[n] = -1;
-    os[n] = -INFINITY;
-  }
+  if (ts == kSelSplit - 1)
+    for (; n < k; ++n) {
+      oi[n] = -1;
+      os[n] = -INFINITY;
+    }
 }
 
 stp_status check_index_desc(const stp_index_desc* d) {
@@ -413,7 +466,7 @@ extern "C" stp_status stp_index_topk(const stp_index_desc* desc, const void* q, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(p.err, 0, 4, s);
   const int smem = p.H * 128 * p.D * 2 + 2 * 128 * p.D * 2 + kIdxSmallBytes;
-  const int smem_sel = 256 * kSelThreads * 4;
+  const int smem_sel = 256 * kSelQ * 4;
   static bool attr = false;
   if (e == cudaSuccess && !attr) {
     e = cudaFuncSetAttribute(index_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -425,7 +478,7 @@ extern "C" stp_status stp_index_topk(const stp_index_desc* desc, const void* q, 
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_index_topk: %s", cudaGetErrorString(e));
   const unsigned grid = (unsigned)(NT * desc->n_rows);
   index_scores_kernel<<<grid, kIdxThreads, smem, s>>>(mq, mk, p);
-  index_select_kernel<<<grid, kSelThreads, smem_sel, s>>>(p);
+  index_select_kernel<<<grid * (128 / kSelQ), kSelThreads, smem_sel, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_index_topk: %s", cudaGetErrorString(e));
   return STP_OK;
