@@ -16,6 +16,8 @@ pages describe it:
   with its analytic backward, in float64.
 * ``oracle.index`` -- the tree-aware top-k indexer: scores over a query's
   ancestor candidates only, top k with ties to the smaller key index.
+* ``oracle.logprob`` -- next-token log-probabilities read off packed rows
+  where loss_mask is set, and the same quantity on unpacked sequences.
 
 Pins (in ``tests/test_oracle_*.py``) tie every function here to something
 other than itself: the worked examples the pages print, closed forms,
