@@ -92,6 +92,42 @@ def _indexer(R, T, se, tile_meta, pairs, useful, dev, heads=8, dim=64, top_k=512
             "useful_scoring_tflops": 2.0 * heads * dim * useful / (ms / 1e3) / 1e12}
 
 
+def _logprob(tok, mask, dev, peak, hidden=4096, vocab=151936, reps=10) -> dict:
+    """Next-token log-probabilities of the packed row's loss positions (its
+    loss mask and targets from the packer) under a synthetic vocabulary
+    projection: stp_logprob_gather (tiles list + tcgen05 logits with an online
+    log-sum-exp + split combine).  W alone (1.2 GB) exceeds L2."""
+    import torch
+    from sft_trie_build_gb300 import stp
+
+    R, T = tok.shape
+    h, w = (x.to(dev) for x in W.logprob_tensors(R * T, hidden, vocab, seed=29))
+    tok_d = torch.from_numpy(np.ascontiguousarray(tok)).to(dev)
+    mask_d = torch.from_numpy(np.ascontiguousarray(mask)).to(dev)
+    desc = stp.logprob_desc(R, T, hidden, vocab)
+    ws = torch.empty(stp.stp_logprob_workspace_size(desc), dtype=torch.uint8, device=dev)
+    out = torch.empty(R * T, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        stp.stp_logprob_gather(desc, h, w, tok_d, mask_d, out, ws)
+    torch.cuda.synchronize()
+    assert stp.stp_device_status(ws) == stp.STP_OK
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        stp.stp_logprob_gather(desc, h, w, tok_d, mask_d, out, ws)
+    e.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(e) / reps
+    m = np.asarray(mask).reshape(-1) != 0
+    n_loss = int(m.sum())
+    tiles = int(len(np.unique(np.flatnonzero(m) // 128)))
+    useful = 2.0 * n_loss * vocab * hidden / (ms / 1e3) / 1e12
+    computed = 2.0 * tiles * 128 * vocab * hidden / (ms / 1e3) / 1e12
+    return {"hidden": hidden, "vocab": vocab, "loss_positions": n_loss, "tiles_with_loss": tiles, "ms": ms,
+            "useful_tflops": useful, "computed_tflops": computed, "frac_of_bf16_peak": useful / peak,
+            "launches_per_call": 3}
+
+
 def _what_if(n_candidates: int = 64, groups_per_candidate: int = 8) -> dict:
     """Host 'what if' planning: rows that candidate batches (whole groups drawn
     from the curriculum pool) would need, global tree vs one tree per group,
@@ -265,7 +301,8 @@ def main():
     pin = lambda t: t.contiguous().pin_memory()  # noqa: E731
     q_h, k_h, v_h, do_h = (pin(x) for x in (q_h, k_h, v_h, do_h))
     q, k, v, do = (x.to(dev) for x in (q_h, k_h, v_h, do_h))
-    se0 = stp.stp_plan_write(plan0)["subtree_end"]
+    meta0 = stp.stp_plan_write(plan0)
+    se0 = meta0["subtree_end"]
     desc = stp.Desc(R, T, Hq, Hkv, D, stp.STP_BF16, shape.scale, stp.stp_count_tile_pairs(se0))
     buf = stp.Buffers(desc, dev)
     o = torch.empty_like(q)
@@ -466,6 +503,7 @@ def main():
     if rank == 0:
         line["what_if"] = _what_if()
         line["indexer"] = _indexer(R, T, se, buf.tile_meta, desc.max_tile_pairs, useful, dev)
+        line["logprob"] = _logprob(meta0["token_ids"], meta0["loss_mask"], dev, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import pack as OP
         plan_o = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared, b.family)

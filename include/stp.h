@@ -364,6 +364,45 @@ stp_status stp_index_topk(const stp_index_desc* desc, const void* q, const void*
                           float* topk_score, void* d_ws, void* stream);
 
 /*
+ * Next-token log-probabilities over packed rows ([P1] tree-build section: the
+ * join copy keeps each trainable token's predecessor right before it in the
+ * same row; materialization section: the loss mask marks those
+ * predecessors).  For every position x = r * T + t with loss_mask[x] = 1:
+ *   logprob[x] = h[x] . W[tok[x + 1]] - ln sum_v exp(h[x] . W[v])
+ * and logprob[x] = 0 elsewhere.  The [positions, vocab] logits are never
+ * stored: the products run on the tensor cores (bf16 in, float32 sums) and
+ * the log-sum-exp is kept online in float32.
+ */
+typedef struct {
+  int32_t n_rows;  /* R                                              */
+  int32_t row_len; /* T, a positive multiple of 128; R * T <= 2^28   */
+  int32_t hidden;  /* D, a multiple of 64 in [64, 16384]             */
+  int32_t vocab;   /* V in [1, 2^24]                                 */
+} stp_logprob_desc;
+
+/* Device workspace of stp_logprob_gather: 512 bytes + 8 bytes per 128-position
+ * tile + 12 * min(ceil(V / 256), 64) bytes per position (256-byte rounded). */
+stp_status stp_logprob_workspace_size(const stp_logprob_desc* desc, size_t* ws_bytes);
+
+/*
+ *   hidden       device bf16 [R * T, D], 16-byte aligned (h, one row per position)
+ *   w_vocab      device bf16 [V, D], 16-byte aligned (W, the vocabulary projection)
+ *   d_token_ids  device int32 [R * T] (tok; read at x + 1 for each loss position x)
+ *   d_loss_mask  device uint8 [R * T], nonzero = loss position
+ *   logprob      device float32 [R * T], written in full
+ *   d_ws         device, stp_logprob_workspace_size bytes, 256-byte aligned;
+ *                its first word is the device error word (stp_device_status)
+ * All buffers are the caller's; the call only enqueues work on `stream`.
+ * Errors: STP_EINVAL / STP_EUNSUPPORTED for the descriptor, NULL or unaligned
+ * pointers; STP_ECUDA.  A loss position that is the last of its row, or
+ * whose target lies outside [0, V), sets the device error word
+ * (stp_device_status then reports STP_EDEVICE) and its logprob is invalid.
+ */
+stp_status stp_logprob_gather(const stp_logprob_desc* desc, const void* hidden, const void* w_vocab,
+                              const int32_t* d_token_ids, const uint8_t* d_loss_mask, float* logprob,
+                              void* d_ws, void* stream);
+
+/*
  * Read the device error word of a workspace (fwd_ws or bwd_ws): synchronizes
  * the stream, then *out = STP_OK or STP_EDEVICE (a device check tripped or a
  * bounded wait ran out; the kernel returned early and its outputs are invalid).

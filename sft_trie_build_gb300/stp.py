@@ -28,6 +28,7 @@ EXPORTED = ["stp_pack", "stp_plan_info", "stp_plan_write", "stp_plan_rows_of", "
             "stp_count_tile_pairs", "stp_workspace_size", "stp_classify", "stp_classify_noalloc", "stp_read_tile_classes",
             "stp_attn_fwd", "stp_attn_bwd", "stp_step_scratch_size", "stp_attn_step_host",
             "stp_index_workspace_size", "stp_index_topk",
+            "stp_logprob_workspace_size", "stp_logprob_gather",
             "stp_device_status", "stp_last_error", "stp_version"]
 
 
@@ -47,6 +48,11 @@ class PlanInfo(ctypes.Structure):
 class IndexDesc(ctypes.Structure):
     _fields_ = [("n_rows", ctypes.c_int32), ("row_len", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("top_k", ctypes.c_int32), ("max_tile_pairs", ctypes.c_int32)]
+
+
+class LogprobDesc(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int32), ("row_len", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("vocab", ctypes.c_int32)]
 
 
 class AttnDesc(ctypes.Structure):
@@ -114,6 +120,10 @@ def lib():
         L.stp_index_workspace_size.restype = st
         L.stp_index_topk.argtypes = [ctypes.POINTER(IndexDesc)] + [_P] * 9
         L.stp_index_topk.restype = st
+        L.stp_logprob_workspace_size.argtypes = [ctypes.POINTER(LogprobDesc), _SZ]
+        L.stp_logprob_workspace_size.restype = st
+        L.stp_logprob_gather.argtypes = [ctypes.POINTER(LogprobDesc)] + [_P] * 7
+        L.stp_logprob_gather.restype = st
         L.stp_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
         L.stp_device_status.restype = st
         L.stp_last_error.argtypes = []
@@ -368,6 +378,22 @@ def stp_index_topk(desc: IndexDesc, q, k, w, subtree_end, tile_meta, topk_idx, t
     _check(lib().stp_index_topk(ctypes.byref(desc), _dptr(q), _dptr(k), _dptr(w), _dptr(subtree_end),
                                 _dptr(tile_meta), _dptr(topk_idx), _dptr(topk_score), _dptr(ws), _stream(stream)),
            "stp_index_topk")
+
+
+def logprob_desc(n_rows, row_len, hidden, vocab) -> LogprobDesc:
+    return LogprobDesc(n_rows, row_len, hidden, vocab)
+
+
+def stp_logprob_workspace_size(desc: LogprobDesc) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().stp_logprob_workspace_size(ctypes.byref(desc), ctypes.byref(out)), "stp_logprob_workspace_size")
+    return out.value
+
+
+def stp_logprob_gather(desc: LogprobDesc, hidden, w_vocab, token_ids, loss_mask, logprob, ws, stream=None):
+    _check(lib().stp_logprob_gather(ctypes.byref(desc), _dptr(hidden), _dptr(w_vocab), _dptr(token_ids),
+                                    _dptr(loss_mask), _dptr(logprob), _dptr(ws), _stream(stream)),
+           "stp_logprob_gather")
 
 
 def stp_device_status(ws, stream=None) -> int:

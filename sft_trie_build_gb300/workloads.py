@@ -375,3 +375,18 @@ def index_tensors(n_rows: int, row_len: int, n_heads: int, head_dim: int, seed: 
     k = (torch.randn(n_rows, row_len, head_dim, generator=g) * s).to(torch.bfloat16)
     w = torch.rand(n_rows, row_len, n_heads, generator=g)
     return q.to(device), k.to(device), w.to(device)
+
+
+def logprob_tensors(n_positions: int, hidden: int, vocab: int, seed: int = 0, logit_std: float = 2.0,
+                    device="cpu"):
+    """Inputs of the next-token log-probability gather: hidden states h [N, D]
+    drawn N(0, 1) and a vocabulary projection W [V, D] drawn N(0, logit_std^2 / D),
+    both rounded to bf16 (logits then spread about N(0, logit_std^2)); seeded
+    CPU torch generator."""
+    import torch
+
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    h = torch.randn(n_positions, hidden, generator=g).to(torch.bfloat16)
+    w = (torch.randn(vocab, hidden, generator=g) * (logit_std / float(hidden) ** 0.5)).to(torch.bfloat16)
+    return h.to(device), w.to(device)
