@@ -18,6 +18,9 @@ pages describe it:
   ancestor candidates only, top k with ties to the smaller key index.
 * ``oracle.logprob`` -- next-token log-probabilities read off packed rows
   where loss_mask is set, and the same quantity on unpacked sequences.
+* ``oracle.gdn``   -- the Gated DeltaNet layer core (short convolution along
+  each token's path, normalized heads, the gated delta rule) threaded over
+  the packed tree token by token, and the same layer on one sequence.
 
 Pins (in ``tests/test_oracle_*.py``) tie every function here to something
 other than itself: the worked examples the pages print, closed forms,

@@ -1,0 +1,148 @@
+"""Pins of the Gated DeltaNet oracle (oracle/gdn.py): closed forms of the
+gated delta rule (beta = 0, exact associations under orthonormal keys, a
+single key reduces to an unrolled moving average, pure decay), the short
+convolution against a library convolution and its tap shifts, and the
+packed tree equal to the layer run on every unpacked sequence (state forks,
+zero roots, the convolution's hand-off across segments, join copies)."""
+import numpy as np
+import pytest
+from scipy.special import expit
+
+from oracle import gdn as OG
+from oracle import pack as OP
+from sft_trie_build_gb300 import workloads as W
+
+
+def _chain(L):
+    return np.arange(L) - 1
+
+
+def test_beta_zero_keeps_the_state_empty():
+    rng = np.random.default_rng(0)
+    T, H, d = 9, 2, 4
+    q, k, v = (rng.standard_normal((T, H, d)) for _ in range(3))
+    o = OG.delta_rule(q, k, v, -rng.random((T, H)), np.zeros((T, H)), _chain(T), 0.5)
+    assert np.all(o == 0.0)
+
+
+def test_orthonormal_keys_store_exact_associations():
+    """No decay, beta = 1, keys e_0, e_1, ...: the state is sum_s k_s v_s^T, so
+    querying with k_s returns scale * v_s once s has been written, 0 before."""
+    rng = np.random.default_rng(1)
+    T, d = 6, 8
+    k = np.eye(d)[:T][:, None, :]
+    v = rng.standard_normal((T, 1, d))
+    for s in range(T):
+        q = np.repeat(np.eye(d)[s][None, None, :], T, 0)
+        o = OG.delta_rule(q, k, v, np.zeros((T, 1)), np.ones((T, 1)), _chain(T), 0.25)
+        for t in range(T):
+            want = 0.25 * v[s, 0] if t >= s else np.zeros(d)
+            np.testing.assert_allclose(o[t, 0], want, atol=1e-12)
+
+
+def test_single_key_is_an_unrolled_moving_average():
+    """One unit key for every token: the value read back under it is
+    r_t = sum_{s<=t} beta_s v_s prod_{s<u<=t} (1 - beta_u) alpha_u, a
+    closed form that keeps alpha inside the correction term."""
+    rng = np.random.default_rng(2)
+    T, d = 12, 5
+    key = rng.standard_normal(d)
+    key /= np.linalg.norm(key)
+    k = np.tile(key, (T, 1))[:, None, :]
+    v = rng.standard_normal((T, 1, d))
+    g = np.log(rng.uniform(0.5, 1.0, (T, 1)))
+    beta = rng.uniform(0.05, 0.95, (T, 1))
+    o = OG.delta_rule(k.copy(), k, v, g, beta, _chain(T), 1.0)
+    a = np.exp(g[:, 0])
+    for t in range(T):
+        want = np.zeros(d)
+        for s in range(t + 1):
+            w = beta[s, 0] * np.prod([(1 - beta[u, 0]) * a[u] for u in range(s + 1, t + 1)])
+            want += w * v[s, 0]
+        np.testing.assert_allclose(o[t, 0], want, atol=1e-12)
+
+
+def test_pure_decay():
+    """beta_1 = 1, then 0: the stored value decays by exp(sum g) and nothing else."""
+    rng = np.random.default_rng(3)
+    T, d = 7, 4
+    key = np.eye(d)[2]
+    k = np.tile(key, (T, 1))[:, None, :]
+    v = rng.standard_normal((T, 1, d))
+    g = -rng.random((T, 1))
+    beta = np.zeros((T, 1))
+    beta[0] = 1.0
+    o = OG.delta_rule(k.copy(), k, v, g, beta, _chain(T), 1.0)
+    for t in range(T):
+        np.testing.assert_allclose(o[t, 0], np.exp(g[1:t + 1, 0].sum()) * v[0, 0], atol=1e-12)
+
+
+def test_conv_taps_and_library_convolution():
+    rng = np.random.default_rng(4)
+    L, C = 10, 6
+    x = rng.standard_normal((L, C))
+    silu = lambda z: z * expit(z)  # noqa: E731
+    w = np.zeros((C, 4))
+    w[:, 3] = 1.0
+    np.testing.assert_allclose(OG.conv_path(x, w, _chain(L)), silu(x), atol=1e-12)
+    w = np.zeros((C, 4))
+    w[:, 0] = 1.0
+    shifted = np.vstack([np.zeros((3, C)), x[:-3]])
+    np.testing.assert_allclose(OG.conv_path(x, w, _chain(L)), silu(shifted), atol=1e-12)
+    w = rng.standard_normal((C, 4))
+    want = np.stack([np.convolve(x[:, c], w[c, ::-1])[:L] for c in range(C)], 1)
+    np.testing.assert_allclose(OG.conv_path(x, w, _chain(L)), silu(want), atol=1e-12)
+
+
+def test_l2norm_gives_unit_heads():
+    rng = np.random.default_rng(5)
+    y = rng.standard_normal((5, 3 * 2 * 4)) * 3
+    q, k, _ = OG.split_heads(y, 2, 4)
+    np.testing.assert_allclose(np.linalg.norm(q, axis=-1), 1.0, atol=1e-6)
+    np.testing.assert_allclose(np.linalg.norm(k, axis=-1), 1.0, atol=1e-6)
+
+
+def _token_inputs(rng, V, P, H, d):
+    """Per-(token, position) inputs, so a sequence's inputs do not depend on the packing."""
+    C = 3 * H * d
+    Ex, Px = rng.standard_normal((V, C)), 0.5 * rng.standard_normal((P, C))
+    Eg, Eb = np.log(rng.uniform(0.8, 1.0, (V, H))), rng.uniform(0.1, 0.9, (V, H))
+    Pg = np.log(rng.uniform(0.9, 1.0, (P, H)))
+    return (lambda t, p: Ex[t] + Px[p]), (lambda t, p: Eg[t] + Pg[p]), (lambda t, p: Eb[t])
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_packed_tree_equals_unpacked_sequences(seed):
+    b = W.random_forest(seed, n_roots=3, max_depth=3, max_children=3, len_lo=3, len_hi=30, row_len=256,
+                        min_shared=4, vocab=53)
+    plan = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared)
+    rng = np.random.default_rng(seed)
+    H, d, scale = 2, 4, 0.5
+    fx, fg, fb = _token_inputs(rng, 53, b.row_len, H, d)
+    conv_w = 0.5 * rng.standard_normal((3 * H * d, 4))
+    outs = []
+    for r in range(plan.n_rows):
+        tok, pos = plan.token_ids[r], plan.position_ids[r]
+        x = np.stack([fx(t, p) for t, p in zip(tok, pos)])
+        g = np.stack([fg(t, p) for t, p in zip(tok, pos)])
+        beta = np.stack([fb(t, p) for t, p in zip(tok, pos)])
+        outs.append(OG.gdn_row(plan, r, x, conv_w, g, beta, H, d, scale))
+    o = np.concatenate(outs)          # [R * T, H, d]
+    offs = np.concatenate([[0], np.cumsum([len(s) for s in b.seqs])])
+    for s, seq in enumerate(b.seqs):
+        x = np.stack([fx(t, p) for p, t in enumerate(seq)])
+        g = np.stack([fg(t, p) for p, t in enumerate(seq)])
+        beta = np.stack([fb(t, p) for p, t in enumerate(seq)])
+        want = OG.gdn_sequence(x, conv_w, g, beta, H, d, scale)
+        got = o[plan.gather_index[offs[s]: offs[s + 1]]]
+        np.testing.assert_allclose(got, want, atol=1e-12, rtol=1e-10)
+
+
+def test_pads_are_their_own_roots():
+    b = W.random_forest(9, n_roots=2, max_depth=2, len_lo=3, len_hi=20, row_len=256, min_shared=4, vocab=31)
+    plan = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared)
+    used = int(plan.used[0])
+    assert used < plan.row_len
+    prev = OG.path_prev(plan, 0)
+    assert np.all(prev[used:] == -1)
+    assert np.all(prev[:used] < np.arange(used))
