@@ -403,6 +403,69 @@ stp_status stp_logprob_gather(const stp_logprob_desc* desc, const void* hidden, 
                               void* d_ws, void* stream);
 
 /*
+ * Tree-aware Gated DeltaNet layer core, forward ([P1] GDN section; [P3] the
+ * Gated DeltaNet paragraphs).  The recurrent state is threaded along each
+ * token's own path: forked at every branch point (a child segment starts
+ * from its parent segment's final state), zero at every root; the short
+ * convolution reads the previous tokens of the same path, so the parent's
+ * last inputs are handed to each child.  Per token x of a packed row and
+ * head h, with the path x_0 .. x_t = x:
+ *   y        = SiLU(sum_{i=0..3} conv_w[:, i] * x_in[path token t-3+i])  (zero before the root)
+ *   q, k, v  = channel blocks [0, Hd), [Hd, 2Hd), [2Hd, 3Hd) of y, split into
+ *              heads of d; q, k scaled to unit norm (1 / sqrt(|.|^2 + 1e-6))
+ *   S_x      = alpha S_prev + beta k (v - alpha S_prev^T k)^T,  alpha = exp(g[x, h])
+ *   o[x, h]  = scale * S_x^T q                                  (S: [d, d], k-major)
+ * equal, token for token, to the layer run on every sequence unpacked.
+ * Computed chunk-wise (64 tokens per chunk) on the tensor cores: q, k, v and
+ * the per-chunk operands are bf16, products are summed in float32, and the
+ * state is kept in float32 between chunks.
+ */
+typedef struct {
+  int32_t n_rows;    /* R                                                        */
+  int32_t row_len;   /* T; R * T <= 2^26                                         */
+  int32_t n_heads;   /* H in [1, 64] (q, k and v heads alike)                   */
+  int32_t head_dim;  /* d; must be 128                                           */
+  float scale;       /* output scale, e.g. 1 / sqrt(d)                           */
+} stp_gdn_desc;
+
+/* Upper bound of the plan size in bytes (from R and T only). */
+stp_status stp_gdn_plan_bound(const stp_gdn_desc* desc, size_t* plan_bytes);
+
+/*
+ * Host planner: from subtree_end (host int32 [R, T], as written by
+ * stp_plan_write) and the number of real tokens of each row (host int32 [R],
+ * or NULL when no row holds pads; tokens at or past it are pads, which get
+ * o = 0), writes the plan into `plan` (host, >= stp_gdn_plan_bound bytes):
+ * the path predecessor of every token, the segments sorted by depth with
+ * their parents, and the 64-token chunks.  Its word 5 is the number of int32
+ * words used; copy at least that much to the device for stp_gdn_fwd.
+ * Errors: STP_EINVAL (NULL, short buffer, subtree_end outside [x, T) or not
+ * nested, row_used outside [0, T]).
+ */
+stp_status stp_gdn_plan(const stp_gdn_desc* desc, const int32_t* subtree_end, const int32_t* row_used,
+                        void* plan, size_t plan_bytes);
+
+/* Device workspace of stp_gdn_fwd for a given host plan. */
+stp_status stp_gdn_workspace_size(const stp_gdn_desc* desc, const void* plan, size_t* ws_bytes);
+
+/*
+ *   plan        host plan from stp_gdn_plan (launch sizes are read from it)
+ *   d_plan      device copy of the same plan, 256-byte aligned
+ *   x           device bf16 [R * T, 3 H d] (the projected q | k | v inputs), 16-byte aligned
+ *   conv_w      device float32 [3 H d, 4] (tap 3 multiplies the token itself)
+ *   g, beta     device float32 [R * T, H] (log decay <= 0, and the write strength)
+ *   o           device float32 [R * T, H, d], written in full
+ *   d_ws        device, stp_gdn_workspace_size bytes, 256-byte aligned; its
+ *               first word is the device error word (stp_device_status)
+ * The call enqueues 2 + (number of depths) kernels on `stream`.
+ * Errors: STP_EINVAL / STP_EUNSUPPORTED for the descriptor, NULL or
+ * unaligned pointers, a plan that is not one; STP_ECUDA.
+ */
+stp_status stp_gdn_fwd(const stp_gdn_desc* desc, const void* plan, const void* d_plan, const void* x,
+                       const float* conv_w, const float* g, const float* beta, float* o, void* d_ws,
+                       void* stream);
+
+/*
  * Read the device error word of a workspace (fwd_ws or bwd_ws): synchronizes
  * the stream, then *out = STP_OK or STP_EDEVICE (a device check tripped or a
  * bounded wait ran out; the kernel returned early and its outputs are invalid).

@@ -1,0 +1,699 @@
+// Tree-aware Gated DeltaNet layer core, forward ("Prefix tree packing", GDN
+// section: one pass per tree depth, every segment of that depth at once, a
+// child starting from its parent's final state; "ART-Optimized Megatron", the
+// GDN paragraphs: the convolution of a branch reads the parent's last inputs).
+//
+// Per head, with chunk-local cumulative log decay gam_t (t < L <= 64), the
+// gated delta rule over a chunk that starts from state S0 ([d_k, d_v]) is
+//   A     = strictly lower (beta_t e^{gam_t - gam_s} k_t . k_s)
+//   U^    = (I + A)^{-1} diag(beta) V,   W = (I + A)^{-1} diag(beta e^{gam}) K
+//   V'    = U^ - W S0
+//   O     = scale (diag(e^{gam}) Q S0 + (Q K^T o Gamma) V'),  Gamma_ts = e^{gam_t - gam_s}, s <= t
+//   S_L   = e^{gam_L} S0 + (diag(e^{gam_L - gam}) K)^T V'
+// (the WY form of the delta rule: substituting the recurrence into itself
+// chunk by chunk).  Three kernels:
+//   gdn_conv_kernel   one block per token: width-4 causal convolution along
+//                     the token's path (prev pointers of the plan), SiLU, unit
+//                     q and k heads; pads get o = 0.
+//   gdn_prep_kernel   one block per (chunk, head), float32 on the CUDA cores:
+//                     A by dot products, the unit-lower-triangular solve for U^
+//                     and W (one column per thread), and the chunk's operands
+//                     W | Q~ (Q~ = scale e^{gam} Q), K~ = e^{gam_L - gam} K,
+//                     P = scale (Q K^T o Gamma) in bf16, U^ transposed in
+//                     float32 and e^{gam_L}.  Nothing here depends on a state.
+//   gdn_state_kernel  one launch per depth, one CTA per (segment, head): the
+//                     state lives in TMEM (float32) for the whole segment; per
+//                     chunk the tensor core forms [W; Q~] S0, the epilogue warps
+//                     make V' = U^ - W S0, then O += P V' and S += K~^T V' (the
+//                     state pre-scaled by e^{gam_L}); the segment's final state
+//                     goes to HBM for its children.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "internal.h"
+#include "layout.h"
+#include "tc_ptx.cuh"
+
+namespace stp {
+namespace {
+
+using namespace tc;
+
+constexpr int kGd = 128;          // head dim
+constexpr int kGc = kGdnChunk;    // tokens per chunk
+constexpr int kConvThreads = 256;
+constexpr int kPrepThreads = 256;
+constexpr int kStThreads = 192;   // warps 0-3 epilogue, 4 loads, 5 MMA
+
+// gdn_prep_kernel shared memory (floats): q, k [64][129], A [64][65], gam, beta [64]; v as bf16 [64][128]
+constexpr int kPrepLd = 129;
+constexpr int kPrepSmem = (2 * kGc * kPrepLd + kGc * 65 + 2 * kGc) * 4 + kGc * kGd * 2;
+
+// gdn_state_kernel shared memory, from a 1024-byte aligned base
+constexpr int kStStage = 65536;                 // W|Q~ 32 KB, K~ 16 KB, [zeros 8 KB | P 8 KB]
+constexpr int kOffKt = 32768, kOffA2 = 49152, kOffP = 57344;
+constexpr int kOffSop = 2 * kStStage;           // S0 as a bf16 operand, 32 KB
+constexpr int kOffVop = kOffSop + 32768;        // V' as a bf16 operand, 16 KB
+constexpr int kOffUt = kOffVop + 16384;         // U^ transposed, float32, 32 KB
+constexpr int kOffBar = kOffUt + 32768;
+constexpr int kStSmem = kOffBar + 256 + 1024;
+
+struct GdnParams {
+  int N, H, C, seg0;
+  float scale;
+  const int32_t* prev;
+  const int32_t* seg_len;
+  const int32_t* seg_parent;
+  const int32_t* seg_chunk0;
+  const int32_t* chunk_start;
+  const int32_t* chunk_len;
+  const __nv_bfloat16* x;   // [N, C]
+  const float* conv_w;      // [C, 4]
+  const float* g;           // [N, H]
+  const float* beta;        // [N, H]
+  __nv_bfloat16* y;         // [N, C]
+  __nv_bfloat16* wq;        // [n_chunk H 128, 128]  rows 0-63 W, 64-127 Q~
+  __nv_bfloat16* kt;        // [n_chunk H 64, 128]
+  __nv_bfloat16* pm;        // [n_chunk H 64, 64]
+  float* ut;                // [n_chunk H, 128, 64]
+  float* decay;             // [n_chunk H]
+  float* state;             // [n_seg H, 128, 128]
+  float* o;                 // [N, H, 128]
+  uint32_t* err;
+};
+
+enum { B_F = 0, B_E = 2, B_SR = 4, B_M1 = 5, B_VR = 6, B_M2 = 7, B_UF = 8, B_UE = 9, B_DRAIN = 10, B_COUNT = 11 };
+
+typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                             const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                             CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_gdn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// [rows, cols] bf16 as a 2-D tensor; boxes of 64 columns x box_rows rows, 128-byte swizzled.
+bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, int box_rows) {
+  EncodeFn enc = encode_gdn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+__device__ __forceinline__ void tma_load_2d_g(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// MN-major 128-byte-swizzled operand whose 64-element halves lie 8 KB apart.
+__device__ __forceinline__ uint32_t desc_lo_mn8k(uint32_t addr) {
+  return ((addr & 0x3FFFFu) >> 4) | ((8192u >> 4) << 16);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 r, float* f) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Path convolution + SiLU + unit q, k heads.  Vectors of 8 channels; the 16
+// vectors of one head sit on 16 consecutive lanes.
+__global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const GdnParams p) {
+  const int x = blockIdx.x;
+  const int p1 = p.prev[x];
+  if (p1 == -2) {   // pad
+    float4* o4 = reinterpret_cast<float4*>(p.o + (size_t)x * p.H * kGd);
+    for (int i = threadIdx.x; i < p.H * kGd / 4; i += blockDim.x) o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const int p2 = p1 >= 0 ? p.prev[p1] : -1;
+  const int p3 = p2 >= 0 ? p.prev[p2] : -1;
+  const int src[4] = {p3, p2, p1, x};   // taps 0..3
+  const int nvec = p.C / 8, qk_vecs = 2 * p.H * (kGd / 8);
+  for (int base = 0; base < nvec; base += blockDim.x) {
+    const int v = base + threadIdx.x;
+    const bool valid = v < nvec;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    if (valid) {
+      const float4* w4 = reinterpret_cast<const float4*>(p.conv_w) + (size_t)v * 8;
+      float4 wv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) wv[i] = w4[i];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (src[t] < 0) continue;
+        float f[8];
+        unpack8(*reinterpret_cast<const uint4*>(p.x + (size_t)src[t] * p.C + v * 8), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float w = t == 0 ? wv[i].x : t == 1 ? wv[i].y : t == 2 ? wv[i].z : wv[i].w;
+          acc[i] = fmaf(w, f[i], acc[i]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (1.f + expf(-acc[i]));
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(acc[i], acc[i], ss);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    if (valid) {
+      if (v < qk_vecs) {
+        const float r = rsqrtf(ss + 1e-6f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] *= r;
+      }
+      uint4 out;
+      out.x = pack_bf16x2(acc[0], acc[1]);
+      out.y = pack_bf16x2(acc[2], acc[3]);
+      out.z = pack_bf16x2(acc[4], acc[5]);
+      out.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(p.y + (size_t)x * p.C + v * 8) = out;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Per (chunk, head): everything of the chunk that does not depend on a state.
+__global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const GdnParams p) {
+  extern __shared__ float psm[];
+  float* sq = psm;                         // [64][129]
+  float* sk = sq + kGc * kPrepLd;          // [64][129]
+  float* sA = sk + kGc * kPrepLd;          // [64][65]
+  float* sgam = sA + kGc * 65;             // [64]
+  float* sbeta = sgam + kGc;               // [64]
+  __nv_bfloat16* sv = reinterpret_cast<__nv_bfloat16*>(sbeta + kGc);   // [64][128]
+  const int tid = threadIdx.x;
+  const int ch = blockIdx.x / p.H, h = blockIdx.x % p.H;
+  const int x0 = p.chunk_start[ch], L = p.chunk_len[ch];
+  const int Hd = p.H * kGd;
+  const size_t row = (size_t)ch * p.H + h;
+
+  for (int i = tid; i < kGc * 16; i += kPrepThreads) {
+    const int t = i >> 4, c = (i & 15) * 8;
+    float fq[8], fk[8];
+    uint4 rv = make_uint4(0, 0, 0, 0);
+    if (t < L) {
+      const __nv_bfloat16* yr = p.y + (size_t)(x0 + t) * p.C + h * kGd + c;
+      unpack8(*reinterpret_cast<const uint4*>(yr), fq);
+      unpack8(*reinterpret_cast<const uint4*>(yr + Hd), fk);
+      rv = *reinterpret_cast<const uint4*>(yr + 2 * Hd);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) fq[j] = fk[j] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      sq[t * kPrepLd + c + j] = fq[j];
+      sk[t * kPrepLd + c + j] = fk[j];
+    }
+    *reinterpret_cast<uint4*>(sv + t * kGd + c) = rv;
+  }
+  if (tid < kGc) {
+    sgam[tid] = tid < L ? p.g[(size_t)(x0 + tid) * p.H + h] : 0.f;
+    sbeta[tid] = tid < L ? p.beta[(size_t)(x0 + tid) * p.H + h] : 0.f;
+  }
+  __syncthreads();
+  if (tid < 32) {   // inclusive prefix sum of g over the 64 rows
+    float a = sgam[tid], b = sgam[tid + 32];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float ua = __shfl_up_sync(0xffffffffu, a, off), ub = __shfl_up_sync(0xffffffffu, b, off);
+      if (tid >= off) {
+        a += ua;
+        b += ub;
+      }
+    }
+    b += __shfl_sync(0xffffffffu, a, 31);
+    sgam[tid] = a;
+    sgam[tid + 32] = b;
+  }
+  __syncthreads();
+
+  // K K^T and Q K^T: thread = (row i, 16 columns j0..j0+15)
+  {
+    const int i = tid >> 2, j0 = (tid & 3) * 16;
+    float kk[16], qk[16];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) kk[jj] = qk[jj] = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < kGd; ++c) {
+      const float ki = sk[i * kPrepLd + c], qi = sq[i * kPrepLd + c];
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) {
+        const float kj = sk[(j0 + jj) * kPrepLd + c];
+        kk[jj] = fmaf(ki, kj, kk[jj]);
+        qk[jj] = fmaf(qi, kj, qk[jj]);
+      }
+    }
+    const float gi = sgam[i], bi = sbeta[i];
+    uint32_t pw[8];
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const int j = j0 + jj;
+      const float de = j <= i ? expf(gi - sgam[j]) : 0.f;
+      sA[i * 65 + j] = j < i ? bi * de * kk[jj] : 0.f;
+      qk[jj] = (j <= i && i < L) ? p.scale * de * qk[jj] : 0.f;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) pw[jj] = pack_bf16x2(qk[2 * jj], qk[2 * jj + 1]);
+    uint4* dst = reinterpret_cast<uint4*>(p.pm + (row * kGc + i) * kGc + j0);
+    dst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+    dst[1] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+  }
+  __syncthreads();
+
+  // (I + A) X = B by forward substitution, one column per thread:
+  // columns 0-127 give U^ (B = beta V), 128-255 give W (B = beta e^gam K)
+  {
+    const int col = tid;
+    float X[kGc];
+#pragma unroll
+    for (int t = 0; t < kGc; ++t) {
+      float b = col < kGd ? sbeta[t] * __bfloat162float(sv[t * kGd + col])
+                          : sbeta[t] * expf(sgam[t]) * sk[t * kPrepLd + col - kGd];
+#pragma unroll
+      for (int s = 0; s < t; ++s) b = fmaf(-sA[t * 65 + s], X[s], b);
+      X[t] = b;
+    }
+    if (col < kGd) {
+      float4* u4 = reinterpret_cast<float4*>(p.ut + (row * kGd + col) * kGc);
+#pragma unroll
+      for (int t = 0; t < kGc; t += 4) u4[t / 4] = make_float4(X[t], X[t + 1], X[t + 2], X[t + 3]);
+    } else {
+      __nv_bfloat16* w = p.wq + row * 128 * kGd + (col - kGd);
+#pragma unroll
+      for (int t = 0; t < kGc; ++t) w[(size_t)t * kGd] = __float2bfloat16_rn(X[t]);
+    }
+  }
+  // Q~ rows (64..127 of the W|Q~ tile) and K~
+  const float gl = sgam[L - 1];
+  for (int i = tid; i < kGc * kGd; i += kPrepThreads) {
+    const int t = i / kGd, c = i % kGd;
+    const float qv = t < L ? p.scale * expf(sgam[t]) * sq[t * kPrepLd + c] : 0.f;
+    const float kv = t < L ? expf(gl - sgam[t]) * sk[t * kPrepLd + c] : 0.f;
+    p.wq[(row * 128 + kGc + t) * kGd + c] = __float2bfloat16_rn(qv);
+    p.kt[(row * kGc + t) * kGd + c] = __float2bfloat16_rn(kv);
+  }
+  if (tid == 0) p.decay[row] = expf(gl);
+}
+
+// ---------------------------------------------------------------------------
+// One CTA per (segment of this depth, head).
+__global__ void __launch_bounds__(kStThreads, 1)
+    gdn_state_kernel(const __grid_constant__ CUtensorMap mwq, const __grid_constant__ CUtensorMap mkt,
+                     const __grid_constant__ CUtensorMap mpm, const GdnParams p) {
+  extern __shared__ uint8_t gsm_dyn[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gsm_dyn) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + B_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const float* ut_s = reinterpret_cast<const float*>(sm + kOffUt);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sidx = p.seg0 + (int)(blockIdx.x / p.H), h = (int)(blockIdx.x % p.H);
+  const int c0 = p.seg_chunk0[sidx], nck = (p.seg_len[sidx] + kGc - 1) / kGc;
+  const int par = p.seg_parent[sidx];
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < B_COUNT; ++b)
+      mbar_init(&bars[b], (b == B_SR || b == B_VR) ? 4 : b == B_UE ? 2 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // the zero top halves of the [0; P] operand, both stages
+  for (int i = threadIdx.x; i < 2 * 512; i += kStThreads)
+    reinterpret_cast<uint4*>(sm + (i >> 9) * kStStage + kOffA2)[i & 511] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;   // columns 0-127: the state S; 128-255: [W S0 ; Q~ S0 + P V']
+
+  if (warp == 4) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ loads
+      tma_prefetch_desc(&mwq);
+      tma_prefetch_desc(&mkt);
+      tma_prefetch_desc(&mpm);
+      int lastf[2] = {-1, -1}, lastu = -1;
+      for (int i = 0; i < nck; ++i) {
+        const int st = i & 1;
+        if (i >= 2 && !mbar_wait(&bars[B_E + st], ((i >> 1) - 1) & 1, abort_flag, p.err)) break;
+        const int row = (c0 + i) * p.H + h;
+        uint8_t* stage = sm + st * kStStage;
+        mbar_expect_tx(&bars[B_F + st], 32768 + 16384 + 8192);
+        tma_load_2d_g(stage, &mwq, &bars[B_F + st], 0, row * 128);
+        tma_load_2d_g(stage + 16384, &mwq, &bars[B_F + st], 64, row * 128);
+        tma_load_2d_g(stage + kOffKt, &mkt, &bars[B_F + st], 0, row * kGc);
+        tma_load_2d_g(stage + kOffKt + 8192, &mkt, &bars[B_F + st], 64, row * kGc);
+        tma_load_2d_g(stage + kOffP, &mpm, &bars[B_F + st], 0, row * kGc);
+        lastf[st] = (i >> 1) & 1;
+        if (i >= 1 && !mbar_wait(&bars[B_UE], (i - 1) & 1, abort_flag, p.err)) break;
+        mbar_expect_tx(&bars[B_UF], 32768);
+        bulk_load(sm + kOffUt, p.ut + (size_t)row * kGd * kGc, 32768, &bars[B_UF]);
+        lastu = i & 1;
+      }
+      for (int st = 0; st < 2; ++st)
+        if (lastf[st] >= 0) mbar_wait_drain(&bars[B_F + st], lastf[st]);
+      if (lastu >= 0) mbar_wait_drain(&bars[B_UF], lastu);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA
+      constexpr uint32_t id_kmn = idesc_bf16(128, 128, 0, 1);
+      constexpr uint32_t id_mnmn = idesc_bf16(128, 128, 1, 1);
+      for (int i = 0; i < nck; ++i) {
+        const int st = i & 1;
+        const uint32_t stage = sb + st * kStStage;
+        if (!mbar_wait(&bars[B_SR], i & 1, abort_flag, p.err)) break;
+        if (!mbar_wait(&bars[B_F + st], (i >> 1) & 1, abort_flag, p.err)) break;
+        fence_after_sync();
+        // [W; Q~] S0 -> columns 128-255
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          mma_ss_lo(tmem + 128, desc_lo_kmajor(stage + (s >> 2) * 16384 + (s & 3) * 32),
+                    desc_lo_mnmajor(sb + kOffSop + s * 2048), id_kmn, s > 0 ? 1u : 0u);
+        mma_commit(&bars[B_M1]);
+        if (!mbar_wait(&bars[B_VR], i & 1, abort_flag, p.err)) break;
+        fence_after_sync();
+        // rows 64-127: Q~ S0 + P V';  state: e^{gam_L} S0 + K~^T V'
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          mma_ss_lo(tmem + 128, desc_lo_kmajor(stage + kOffA2 + s * 32), desc_lo_mn8k(sb + kOffVop + s * 2048),
+                    id_kmn, 1u);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          mma_ss_lo(tmem, desc_lo_mn8k(stage + kOffKt + s * 2048), desc_lo_mn8k(sb + kOffVop + s * 2048), id_mnmn,
+                    1u);
+        mma_commit(&bars[B_M2]);
+        mma_commit(&bars[B_E + st]);
+      }
+      mma_commit(&bars[B_DRAIN]);
+      mbar_wait_drain(&bars[B_DRAIN], 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int r = threadIdx.x;   // TMEM lane: the state's k row; of columns 128-255 the chunk row
+    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    uint32_t v[32];
+    {
+      const float* src = par >= 0 ? p.state + (((size_t)par * p.H + h) * kGd + r) * kGd : nullptr;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = src ? __float_as_uint(src[cc * 32 + q]) : 0u;
+        tmem_st32(tmem + lrow + cc * 32, v);
+      }
+      tmem_st_wait();
+    }
+    bool ok = true;
+    for (int i = 0; ok && i < nck; ++i) {
+      const int row = (c0 + i) * p.H + h;
+      const int L = p.chunk_len[c0 + i], x0 = p.chunk_start[c0 + i];
+      const float dec = p.decay[row];
+      // S0 -> bf16 operand (k rows, v contiguous in two 64-column halves); S <- e^{gam_L} S0
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(tmem + lrow + cc * 32, v);
+        tmem_ld_wait();
+        uint8_t* half = sm + kOffSop + (cc >> 1) * 16384 + r * 128;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = (cc & 1) * 4 + jj;
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(v[8 * jj + 0]), __uint_as_float(v[8 * jj + 1]));
+          w.y = pack_bf16x2(__uint_as_float(v[8 * jj + 2]), __uint_as_float(v[8 * jj + 3]));
+          w.z = pack_bf16x2(__uint_as_float(v[8 * jj + 4]), __uint_as_float(v[8 * jj + 5]));
+          w.w = pack_bf16x2(__uint_as_float(v[8 * jj + 6]), __uint_as_float(v[8 * jj + 7]));
+          *reinterpret_cast<uint4*>(half + ((j ^ (r & 7)) << 4)) = w;
+        }
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * dec);
+        tmem_st32(tmem + lrow + cc * 32, v);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_SR]);
+
+      // V' = U^ - W S0 on rows 0-63 (warps 0, 1)
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_M1], i & 1, abort_flag, p.err))) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      if (warp < 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_UF], i & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          tmem_ld32(tmem + lrow + 128 + cc * 32, v);
+          tmem_ld_wait();
+          uint8_t* half = sm + kOffVop + (cc >> 1) * 8192 + r * 128;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int col = cc * 32 + 8 * jj + e;
+              f[e] = ut_s[col * kGc + r] - __uint_as_float(v[8 * jj + e]);
+            }
+            const int j = (cc & 1) * 4 + jj;
+            uint4 w;
+            w.x = pack_bf16x2(f[0], f[1]);
+            w.y = pack_bf16x2(f[2], f[3]);
+            w.z = pack_bf16x2(f[4], f[5]);
+            w.w = pack_bf16x2(f[6], f[7]);
+            *reinterpret_cast<uint4*>(half + ((j ^ (r & 7)) << 4)) = w;
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[B_VR]);
+        if (warp < 2) mbar_arrive(&bars[B_UE]);
+      }
+
+      // O rows (warps 2, 3; chunk row r - 64)
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_M2], i & 1, abort_flag, p.err))) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      if (warp >= 2) {
+        const int t = r - 64;
+        float* dst = p.o + ((size_t)(x0 + t) * p.H + h) * kGd;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          tmem_ld32(tmem + lrow + 128 + cc * 32, v);
+          tmem_ld_wait();
+          if (t < L) {
+            float4* d4 = reinterpret_cast<float4*>(dst + cc * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                  __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          }
+        }
+      }
+    }
+    if (ok) {   // the segment's final state, for its children
+      float* dst = p.state + (((size_t)sidx * p.H + h) * kGd + r) * kGd;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(tmem + lrow + cc * 32, v);
+        tmem_ld_wait();
+        float4* d4 = reinterpret_cast<float4*>(dst + cc * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                              __uint_as_float(v[4 * q + 3]));
+      }
+    }
+  }
+
+  __syncwarp();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 5) tmem_dealloc(tmem, 256);
+}
+
+struct GdnLayout {
+  size_t y, wq, kt, pm, ut, decay, state, total;
+};
+
+GdnLayout gdn_layout(int64_t N, int H, int64_t n_chunk, int64_t n_seg) {
+  GdnLayout L;
+  size_t o = 256;   // the error word
+  const int64_t C = 3LL * H * kGd, rows = n_chunk * H;
+  L.y = o;
+  o += align256((size_t)N * C * 2);
+  L.wq = o;
+  o += align256((size_t)rows * 128 * kGd * 2);
+  L.kt = o;
+  o += align256((size_t)rows * kGc * kGd * 2);
+  L.pm = o;
+  o += align256((size_t)rows * kGc * kGc * 2);
+  L.ut = o;
+  o += align256((size_t)rows * kGd * kGc * 4);
+  L.decay = o;
+  o += align256((size_t)rows * 4);
+  L.state = o;
+  o += align256((size_t)n_seg * H * kGd * kGd * 4);
+  L.total = o;
+  return L;
+}
+
+stp_status check_gdn_desc(const stp_gdn_desc* d) {
+  if (!d) return fail(STP_EINVAL, "GDN descriptor is NULL");
+  if (d->n_rows < 0 || d->row_len <= 0 || (int64_t)d->n_rows * d->row_len > (1 << 26))
+    return fail(STP_EINVAL, "need n_rows >= 0, row_len > 0 and at most 2^26 tokens");
+  if (d->head_dim != kGd) return fail(STP_EUNSUPPORTED, "head_dim must be 128 (got %d)", d->head_dim);
+  if (d->n_heads < 1 || d->n_heads > 64) return fail(STP_EUNSUPPORTED, "n_heads must lie in [1, 64]");
+  if (!std::isfinite(d->scale)) return fail(STP_EINVAL, "scale is not finite");
+  return STP_OK;
+}
+
+stp_status check_plan(const stp_gdn_desc* d, const int32_t* w) {
+  if (!w) return fail(STP_EINVAL, "GDN plan is NULL");
+  if (w[GP_MAGIC] != kGdnMagic) return fail(STP_EINVAL, "not a GDN plan (bad magic word)");
+  if ((int64_t)w[GP_N] != (int64_t)d->n_rows * d->row_len)
+    return fail(STP_EINVAL, "the plan covers %d tokens, the descriptor %lld", w[GP_N],
+                (long long)d->n_rows * d->row_len);
+  return STP_OK;
+}
+
+}  // namespace
+}  // namespace stp
+
+using namespace stp;
+
+extern "C" stp_status stp_gdn_workspace_size(const stp_gdn_desc* desc, const void* plan, size_t* ws_bytes) {
+  clear_error();
+  stp_status st = check_gdn_desc(desc);
+  if (st) return st;
+  const int32_t* w = static_cast<const int32_t*>(plan);
+  if ((st = check_plan(desc, w))) return st;
+  if (!ws_bytes) return fail(STP_EINVAL, "stp_gdn_workspace_size: NULL output");
+  *ws_bytes = gdn_layout(w[GP_N], desc->n_heads, w[GP_NCHUNK], w[GP_NSEG]).total;
+  return STP_OK;
+}
+
+extern "C" stp_status stp_gdn_fwd(const stp_gdn_desc* desc, const void* plan, const void* d_plan, const void* x,
+                                  const float* conv_w, const float* g, const float* beta, float* o, void* d_ws,
+                                  void* stream) {
+  clear_error();
+  stp_status st = check_gdn_desc(desc);
+  if (st) return st;
+  const int32_t* w = static_cast<const int32_t*>(plan);
+  if ((st = check_plan(desc, w))) return st;
+  if (!d_plan || !x || !conv_w || !g || !beta || !o || !d_ws)
+    return fail(STP_EINVAL, "stp_gdn_fwd: NULL device pointer");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(conv_w) | reinterpret_cast<uintptr_t>(o)) & 15 ||
+      (reinterpret_cast<uintptr_t>(d_ws) | reinterpret_cast<uintptr_t>(d_plan)) & 255)
+    return fail(STP_EINVAL, "stp_gdn_fwd: x, conv_w, o 16-byte, d_plan and ws 256-byte aligned");
+  const int N = w[GP_N], H = desc->n_heads, n_chunk = w[GP_NCHUNK], n_seg = w[GP_NSEG], n_depth = w[GP_NDEPTH];
+  if (N == 0) return STP_OK;
+  const int32_t* dp = static_cast<const int32_t*>(d_plan);
+  GdnParams p;
+  p.N = N;
+  p.H = H;
+  p.C = 3 * H * kGd;
+  p.seg0 = 0;
+  p.scale = desc->scale;
+  p.prev = dp + w[GP_PREV];
+  p.seg_len = dp + w[GP_SEG_LEN];
+  p.seg_parent = dp + w[GP_SEG_PARENT];
+  p.seg_chunk0 = dp + w[GP_SEG_CHUNK0];
+  p.chunk_start = dp + w[GP_CHUNK_START];
+  p.chunk_len = dp + w[GP_CHUNK_LEN];
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.conv_w = conv_w;
+  p.g = g;
+  p.beta = beta;
+  char* ws = static_cast<char*>(d_ws);
+  const GdnLayout L = gdn_layout(N, H, n_chunk, n_seg);
+  p.err = reinterpret_cast<uint32_t*>(ws);
+  p.y = reinterpret_cast<__nv_bfloat16*>(ws + L.y);
+  p.wq = reinterpret_cast<__nv_bfloat16*>(ws + L.wq);
+  p.kt = reinterpret_cast<__nv_bfloat16*>(ws + L.kt);
+  p.pm = reinterpret_cast<__nv_bfloat16*>(ws + L.pm);
+  p.ut = reinterpret_cast<float*>(ws + L.ut);
+  p.decay = reinterpret_cast<float*>(ws + L.decay);
+  p.state = reinterpret_cast<float*>(ws + L.state);
+  p.o = o;
+  CUtensorMap mwq, mkt, mpm;
+  if (n_chunk > 0 &&
+      (!make_map_2d(&mwq, p.wq, (int64_t)n_chunk * H * 128, kGd, 128) ||
+       !make_map_2d(&mkt, p.kt, (int64_t)n_chunk * H * kGc, kGd, kGc) ||
+       !make_map_2d(&mpm, p.pm, (int64_t)n_chunk * H * kGc, kGc, kGc)))
+    return fail(STP_ECUDA, "stp_gdn_fwd: tensor map encoding failed");
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(gdn_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStSmem);
+  });
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = attr_err;
+  if (e == cudaSuccess) e = cudaMemsetAsync(p.err, 0, 4, s);
+  if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e));
+  gdn_conv_kernel<<<(unsigned)N, kConvThreads, 0, s>>>(p);
+  if (n_chunk > 0) gdn_prep_kernel<<<(unsigned)(n_chunk * H), kPrepThreads, kPrepSmem, s>>>(p);
+  const int32_t* depth_off = w + w[GP_DEPTH_OFF];
+  for (int d = 0; d < n_depth; ++d) {
+    const int n = depth_off[d + 1] - depth_off[d];
+    if (n <= 0) continue;
+    p.seg0 = depth_off[d];
+    gdn_state_kernel<<<(unsigned)(n * H), kStThreads, kStSmem, s>>>(mwq, mkt, mpm, p);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e));
+  return STP_OK;
+}

@@ -29,6 +29,7 @@ EXPORTED = ["stp_pack", "stp_plan_info", "stp_plan_write", "stp_plan_rows_of", "
             "stp_attn_fwd", "stp_attn_bwd", "stp_step_scratch_size", "stp_attn_step_host",
             "stp_index_workspace_size", "stp_index_topk",
             "stp_logprob_workspace_size", "stp_logprob_gather",
+            "stp_gdn_plan_bound", "stp_gdn_plan", "stp_gdn_workspace_size", "stp_gdn_fwd",
             "stp_device_status", "stp_last_error", "stp_version"]
 
 
@@ -53,6 +54,11 @@ class IndexDesc(ctypes.Structure):
 class LogprobDesc(ctypes.Structure):
     _fields_ = [("n_rows", ctypes.c_int32), ("row_len", ctypes.c_int32), ("hidden", ctypes.c_int32),
                 ("vocab", ctypes.c_int32)]
+
+
+class GdnDesc(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int32), ("row_len", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("scale", ctypes.c_float)]
 
 
 class AttnDesc(ctypes.Structure):
@@ -124,6 +130,14 @@ def lib():
         L.stp_logprob_workspace_size.restype = st
         L.stp_logprob_gather.argtypes = [ctypes.POINTER(LogprobDesc)] + [_P] * 7
         L.stp_logprob_gather.restype = st
+        L.stp_gdn_plan_bound.argtypes = [ctypes.POINTER(GdnDesc), _SZ]
+        L.stp_gdn_plan_bound.restype = st
+        L.stp_gdn_plan.argtypes = [ctypes.POINTER(GdnDesc), _I32P, _I32P, _P, ctypes.c_size_t]
+        L.stp_gdn_plan.restype = st
+        L.stp_gdn_workspace_size.argtypes = [ctypes.POINTER(GdnDesc), _P, _SZ]
+        L.stp_gdn_workspace_size.restype = st
+        L.stp_gdn_fwd.argtypes = [ctypes.POINTER(GdnDesc)] + [_P] * 9
+        L.stp_gdn_fwd.restype = st
         L.stp_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
         L.stp_device_status.restype = st
         L.stp_last_error.argtypes = []
@@ -394,6 +408,56 @@ def stp_logprob_gather(desc: LogprobDesc, hidden, w_vocab, token_ids, loss_mask,
     _check(lib().stp_logprob_gather(ctypes.byref(desc), _dptr(hidden), _dptr(w_vocab), _dptr(token_ids),
                                     _dptr(loss_mask), _dptr(logprob), _dptr(ws), _stream(stream)),
            "stp_logprob_gather")
+
+
+# plan header fields (int32 words), as the library writes them
+GP_MAGIC, GP_N, GP_NSEG, GP_NCHUNK, GP_NDEPTH, GP_WORDS, GP_PREV, GP_SEG_START, GP_SEG_LEN, GP_SEG_PARENT, \
+    GP_SEG_CHUNK0, GP_DEPTH_OFF, GP_CHUNK_START, GP_CHUNK_LEN, GP_MAX_DEPTH_SEGS = range(15)
+
+
+def gdn_desc(n_rows, row_len, n_heads, head_dim=128, scale=None) -> GdnDesc:
+    return GdnDesc(n_rows, row_len, n_heads, head_dim, head_dim ** -0.5 if scale is None else scale)
+
+
+def stp_gdn_plan_bound(desc: GdnDesc) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().stp_gdn_plan_bound(ctypes.byref(desc), ctypes.byref(out)), "stp_gdn_plan_bound")
+    return out.value
+
+
+def stp_gdn_plan(desc: GdnDesc, subtree_end: np.ndarray, row_used=None) -> np.ndarray:
+    """Host plan (int32 words, trimmed to the words used) of the tree-aware GDN."""
+    se = np.ascontiguousarray(subtree_end, dtype=np.int32)
+    used = None if row_used is None else np.ascontiguousarray(row_used, dtype=np.int32)
+    nbytes = stp_gdn_plan_bound(desc)
+    buf = np.zeros(nbytes // 4, np.int32)
+    _check(lib().stp_gdn_plan(ctypes.byref(desc), _ptr(se, ctypes.c_int32), _ptr(used, ctypes.c_int32),
+                              buf.ctypes.data_as(_P), nbytes), "stp_gdn_plan")
+    return buf[: buf[GP_WORDS]].copy()
+
+
+def gdn_plan_arrays(plan: np.ndarray) -> dict:
+    """Named views of a host plan's arrays."""
+    w = plan
+    n, ns, nc, nd = w[GP_N], w[GP_NSEG], w[GP_NCHUNK], w[GP_NDEPTH]
+    at = lambda f, k: w[w[f]: w[f] + k]  # noqa: E731
+    return {"prev": at(GP_PREV, n), "seg_start": at(GP_SEG_START, ns), "seg_len": at(GP_SEG_LEN, ns),
+            "seg_parent": at(GP_SEG_PARENT, ns), "seg_chunk0": at(GP_SEG_CHUNK0, ns),
+            "depth_off": at(GP_DEPTH_OFF, nd + 1), "chunk_start": at(GP_CHUNK_START, nc),
+            "chunk_len": at(GP_CHUNK_LEN, nc)}
+
+
+def stp_gdn_workspace_size(desc: GdnDesc, plan: np.ndarray) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().stp_gdn_workspace_size(ctypes.byref(desc), plan.ctypes.data_as(_P), ctypes.byref(out)),
+           "stp_gdn_workspace_size")
+    return out.value
+
+
+def stp_gdn_fwd(desc: GdnDesc, plan: np.ndarray, d_plan, x, conv_w, g, beta, o, ws, stream=None):
+    _check(lib().stp_gdn_fwd(ctypes.byref(desc), plan.ctypes.data_as(_P), _dptr(d_plan), _dptr(x),
+                             _dptr(conv_w), _dptr(g), _dptr(beta), _dptr(o), _dptr(ws), _stream(stream)),
+           "stp_gdn_fwd")
 
 
 def stp_device_status(ws, stream=None) -> int:

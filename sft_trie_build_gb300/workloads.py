@@ -390,3 +390,20 @@ def logprob_tensors(n_positions: int, hidden: int, vocab: int, seed: int = 0, lo
     h = torch.randn(n_positions, hidden, generator=g).to(torch.bfloat16)
     w = (torch.randn(vocab, hidden, generator=g) * (logit_std / float(hidden) ** 0.5)).to(torch.bfloat16)
     return h.to(device), w.to(device)
+
+
+def gdn_tensors(n_tokens: int, n_heads: int, head_dim: int = 128, seed: int = 0, device="cpu"):
+    """Gated DeltaNet layer-core inputs: x [N, 3 H d] (the projected q | k | v)
+    drawn N(0, 1) and rounded to bf16; conv_w [3 H d, 4] N(0, 1/4) float32;
+    g [N, H] = log(U[0.85, 1)) (per-token decays near 1) and beta [N, H] =
+    sigmoid(N(0, 1)), float32; seeded CPU torch generator."""
+    import torch
+
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed))
+    C = 3 * n_heads * head_dim
+    x = torch.randn(n_tokens, C, generator=gen).to(torch.bfloat16)
+    conv_w = torch.randn(C, 4, generator=gen) * 0.5
+    g = torch.log(0.85 + 0.15 * torch.rand(n_tokens, n_heads, generator=gen))
+    beta = torch.sigmoid(torch.randn(n_tokens, n_heads, generator=gen))
+    return tuple(t.to(device) for t in (x, conv_w, g, beta))

@@ -1,0 +1,53 @@
+"""Runs stp_gdn_fwd on a packed plan and evaluates the oracle on the same inputs."""
+import numpy as np
+import torch
+
+from oracle import gdn as OG
+from sft_trie_build_gb300 import stp
+from sft_trie_build_gb300 import workloads as W
+
+
+def run_gdn(plan_o, H, seed=0, reps=1):
+    R, T = plan_o.n_rows, plan_o.row_len
+    desc = stp.gdn_desc(R, T, H)
+    plan = stp.stp_gdn_plan(desc, plan_o.subtree_end, np.asarray(plan_o.used, np.int32))
+    d_plan = torch.from_numpy(plan).cuda()
+    x, cw, g, beta = W.gdn_tensors(R * T, H, 128, seed)
+    ws = torch.empty(stp.stp_gdn_workspace_size(desc, plan), dtype=torch.uint8, device="cuda")
+    o = torch.full((R * T, H, 128), float("nan"), device="cuda")
+    args = (x.cuda(), cw.cuda(), g.cuda(), beta.cuda())
+    outs = []
+    for _ in range(reps):
+        stp.stp_gdn_fwd(desc, plan, d_plan, *args, o, ws)
+        torch.cuda.synchronize()
+        outs.append(o.cpu().numpy().copy())
+    return outs, stp.stp_device_status(ws), (x, cw, g, beta), desc.scale
+
+
+def oracle_rows(plan_o, H, inputs, scale):
+    x, cw, g, beta = inputs
+    T = plan_o.row_len
+    out = []
+    for r in range(plan_o.n_rows):
+        sl = slice(r * T, (r + 1) * T)
+        out.append(OG.gdn_row(plan_o, r, x[sl].float().numpy(), cw.numpy(), g[sl].numpy(), beta[sl].numpy(),
+                              H, 128, scale))
+    return np.concatenate(out)
+
+
+def oracle_sequence_heads(plan_o, seq_index, offsets, heads, inputs, scale):
+    """Oracle outputs [len, len(heads), 128] of one sequence, unpacked, with the
+    inputs read at its packed positions (gather_index)."""
+    x, cw, g, beta = inputs
+    idx = plan_o.gather_index[offsets[seq_index]: offsets[seq_index + 1]]
+    xs = x[torch.from_numpy(idx)].float().numpy()
+    L = len(idx)
+    prev = np.arange(L) - 1
+    y = OG.conv_path(xs, cw.numpy(), prev)
+    H = g.shape[1]
+    q, k, v = OG.split_heads(y, H, 128)
+    outs = []
+    for h in heads:
+        outs.append(OG.delta_rule(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], g.numpy()[idx][:, h:h + 1],
+                                  beta.numpy()[idx][:, h:h + 1], prev, scale)[:, 0])
+    return np.stack(outs, 1), idx

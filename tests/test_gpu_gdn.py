@@ -1,0 +1,78 @@
+"""Tree-aware Gated DeltaNet forward on the GPU (stp_gdn_fwd) against the
+float64 oracle (oracle/gdn.py) on the same inputs (x rounded to bf16).
+
+Tolerance: the path convolution and the normalization run in float32, but
+q, k, v and every per-chunk tensor-core operand (W, Q~, K~, P, the state and
+V') are rounded to bf16 (relative 2^-9) with float32 sums, and the state is
+carried in float32 from chunk to chunk; so max |o - oracle| <= 2e-2 max |o|
+and the mean error <= 2e-3 max |o|.  Pads give exactly 0 and repeated calls
+are bit-identical.
+"""
+import numpy as np
+import pytest
+
+from gdn_helpers import oracle_rows, oracle_sequence_heads, run_gdn
+from oracle import pack as OP
+from sft_trie_build_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _compare(po, H, seed=1):
+    outs, status, inputs, scale = run_gdn(po, H, seed=seed, reps=2)
+    assert status == 0
+    o = outs[0]
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    ref = oracle_rows(po, H, inputs, scale)
+    T = po.row_len
+    real = np.concatenate([np.arange(r * T, r * T + po.used[r]) for r in range(po.n_rows)])
+    pads = np.setdiff1d(np.arange(len(o)), real)
+    assert np.all(o[pads] == 0.0)
+    scale_ref = np.abs(ref[real]).max()
+    d = np.abs(o[real] - ref[real])
+    assert d.max() <= 2e-2 * scale_ref, (d.max(), scale_ref)
+    assert d.mean() <= 2e-3 * scale_ref, (d.mean(), scale_ref)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_random_forests(seed):
+    """Single-token segments, ragged chunks, forks at every depth, pads."""
+    b = W.random_forest(seed, n_roots=3, max_depth=3, max_children=3, len_lo=1, len_hi=150, row_len=512,
+                        min_shared=4, vocab=41)
+    _compare(OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared), H=2, seed=seed)
+
+
+def test_deep_narrow_tree():
+    b = W.random_forest(11, n_roots=1, max_depth=6, max_children=2, len_lo=20, len_hi=90, row_len=1024,
+                        min_shared=4, vocab=41)
+    _compare(OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared), H=1, seed=4)
+
+
+def test_long_chain_many_chunks():
+    rng = np.random.default_rng(5)
+    seq = rng.integers(1, 1000, 1000).astype(np.int32)
+    po = OP.pack([seq], [np.zeros(1000, np.uint8)], 1024, 64)
+    _compare(po, H=2, seed=5)
+
+
+def test_tiny_workload():
+    b = W.tiny(0)
+    _compare(OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared), H=3, seed=2)
+
+
+def test_grpo_row_sampled():
+    """The benchmarked shape: the GRPO row (a 5000-token prefix forked into 16
+    rollouts), 16 heads of 128; two rollouts, unpacked, on two heads each."""
+    b = W.grpo(seed=W.CONFIG_SEEDS["grpo"])
+    po = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared)
+    H = 16
+    outs, status, inputs, scale = run_gdn(po, H, seed=0)
+    assert status == 0
+    o = outs[0]
+    offs = np.concatenate([[0], np.cumsum([len(s) for s in b.seqs])])
+    for s, heads in ((0, (0, 7)), (9, (3, 15))):
+        want, idx = oracle_sequence_heads(po, s, offs, heads, inputs, scale)
+        got = o[idx][:, list(heads)]
+        m = np.abs(want).max()
+        d = np.abs(got - want)
+        assert d.max() <= 2e-2 * m and d.mean() <= 2e-3 * m, (d.max(), d.mean(), m)
