@@ -128,6 +128,45 @@ def _logprob(tok, mask, dev, peak, hidden=4096, vocab=151936, reps=10) -> dict:
             "launches_per_call": 3}
 
 
+def _gdn(meta, dev, heads=16, reps=10) -> dict:
+    """Tree-aware Gated DeltaNet layer core (forward) over the packed row:
+    path convolution, per-chunk prep and one state pass per tree depth
+    (stp_gdn_fwd), 16 heads of 128."""
+    import torch
+    from sft_trie_build_gb300 import stp
+
+    se = meta["subtree_end"]
+    R, T = se.shape
+    # real tokens per row: one past the last row position any sequence occupies (pads follow)
+    gi = np.asarray(meta["gather_index"])
+    used = np.zeros(R, np.int64)
+    np.maximum.at(used, gi // T, gi % T + 1)
+    desc = stp.gdn_desc(R, T, heads)
+    t0 = time.perf_counter()
+    plan = stp.stp_gdn_plan(desc, se, used.astype(np.int32))
+    plan_ms = 1e3 * (time.perf_counter() - t0)
+    d_plan = torch.from_numpy(plan).to(dev)
+    x, cw, g, beta = (t.to(dev) for t in W.gdn_tensors(R * T, heads, 128, seed=31))
+    ws = torch.empty(stp.stp_gdn_workspace_size(desc, plan), dtype=torch.uint8, device=dev)
+    o = torch.empty(R * T, heads, 128, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        stp.stp_gdn_fwd(desc, plan, d_plan, x, cw, g, beta, o, ws)
+    torch.cuda.synchronize()
+    assert stp.stp_device_status(ws) == stp.STP_OK
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        stp.stp_gdn_fwd(desc, plan, d_plan, x, cw, g, beta, o, ws)
+    e.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(e) / reps
+    real = int(used.sum())
+    return {"heads": heads, "head_dim": 128, "tokens": real, "segments": int(plan[stp.GP_NSEG]),
+            "chunks": int(plan[stp.GP_NCHUNK]), "depths": int(plan[stp.GP_NDEPTH]), "ms": ms,
+            "tokens_per_s": real / (ms / 1e3), "host_plan_ms": plan_ms,
+            "launches_per_call": 2 + int(plan[stp.GP_NDEPTH])}
+
+
 def _what_if(n_candidates: int = 64, groups_per_candidate: int = 8) -> dict:
     """Host 'what if' planning: rows that candidate batches (whole groups drawn
     from the curriculum pool) would need, global tree vs one tree per group,
@@ -504,6 +543,7 @@ def main():
         line["what_if"] = _what_if()
         line["indexer"] = _indexer(R, T, se, buf.tile_meta, desc.max_tile_pairs, useful, dev)
         line["logprob"] = _logprob(meta0["token_ids"], meta0["loss_mask"], dev, peak)
+        line["gdn"] = _gdn(meta0, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import pack as OP
         plan_o = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared, b.family)

@@ -12,12 +12,13 @@
 //   S_L   = e^{gam_L} S0 + (diag(e^{gam_L - gam}) K)^T V'
 // (the WY form of the delta rule: substituting the recurrence into itself
 // chunk by chunk).  Three kernels:
-//   gdn_conv_kernel   one block per token: width-4 causal convolution along
-//                     the token's path (prev pointers of the plan), SiLU, unit
-//                     q and k heads; pads get o = 0.
+//   gdn_conv_kernel   one block per (64 tokens, q / k / v head): width-4 causal
+//                     convolution along each token's path (prev pointers of
+//                     the plan), SiLU, unit q and k heads; pads get o = 0.
 //   gdn_prep_kernel   one block per (chunk, head), float32 on the CUDA cores:
-//                     A by dot products, the unit-lower-triangular solve for U^
-//                     and W (one column per thread), and the chunk's operands
+//                     A by 4 x 4 register-blocked dot products, the
+//                     unit-lower-triangular solve for U^ and W (one column per
+//                     thread), and the chunk's operands
 //                     W | Q~ (Q~ = scale e^{gam} Q), K~ = e^{gam_L - gam} K,
 //                     P = scale (Q K^T o Gamma) in bf16, U^ transposed in
 //                     float32 and e^{gam_L}.  Nothing here depends on a state.
@@ -49,17 +50,23 @@ constexpr int kConvThreads = 256;
 constexpr int kPrepThreads = 256;
 constexpr int kStThreads = 192;   // warps 0-3 epilogue, 4 loads, 5 MMA
 
-// gdn_prep_kernel shared memory (floats): q, k [64][129], A [64][65], gam, beta [64]; v as bf16 [64][128]
-constexpr int kPrepLd = 129;
-constexpr int kPrepSmem = (2 * kGc * kPrepLd + kGc * 65 + 2 * kGc) * 4 + kGc * kGd * 2;
+// gdn_prep_kernel shared memory (floats): q, k [64][132], A [64][68], gam, beta [64]; v as bf16 [64][128].
+// Row strides keep float4 rows aligned and the 8 rows a quarter warp reads in distinct banks.
+constexpr int kPrepLd = 132, kPrepLa = 68;
+constexpr int kPrepSmem = (2 * kGc * kPrepLd + kGc * kPrepLa + 2 * kGc) * 4 + kGc * kGd * 2;
 
-// gdn_state_kernel shared memory, from a 1024-byte aligned base
-constexpr int kStStage = 65536;                 // W|Q~ 32 KB, K~ 16 KB, [zeros 8 KB | P 8 KB]
-constexpr int kOffKt = 32768, kOffA2 = 49152, kOffP = 57344;
+// gdn_state_kernel shared memory, from a 1024-byte aligned base.  A stage holds
+// [Q~; W] (32 KB), K~ (16 KB) and P (8 KB); P is the top half of a 128-row MMA
+// operand whose bottom half is whatever the next 8 KB hold -- it only adds
+// to accumulator rows 64-127 (W S0) after they have been read.
+constexpr int kStStage = 57344;
+constexpr int kOffKt = 32768, kOffP = 49152;
 constexpr int kOffSop = 2 * kStStage;           // S0 as a bf16 operand, 32 KB
 constexpr int kOffVop = kOffSop + 32768;        // V' as a bf16 operand, 16 KB
 constexpr int kOffUt = kOffVop + 16384;         // U^ transposed, float32, 32 KB
-constexpr int kOffBar = kOffUt + 32768;
+constexpr int kOstLd = 528;                     // output staging: 64 rows of 512 B, padded
+constexpr int kOffOst = kOffUt + 32768;
+constexpr int kOffBar = kOffOst + 64 * kOstLd;
 constexpr int kStSmem = kOffBar + 256 + 1024;
 
 struct GdnParams {
@@ -76,7 +83,7 @@ struct GdnParams {
   const float* g;           // [N, H]
   const float* beta;        // [N, H]
   __nv_bfloat16* y;         // [N, C]
-  __nv_bfloat16* wq;        // [n_chunk H 128, 128]  rows 0-63 W, 64-127 Q~
+  __nv_bfloat16* wq;        // [n_chunk H 128, 128]  rows 0-63 Q~, 64-127 W
   __nv_bfloat16* kt;        // [n_chunk H 64, 128]
   __nv_bfloat16* pm;        // [n_chunk H 64, 64]
   float* ut;                // [n_chunk H, 128, 64]
@@ -142,65 +149,74 @@ __device__ __forceinline__ void unpack8(const uint4 r, float* f) {
 }
 
 // ---------------------------------------------------------------------------
-// Path convolution + SiLU + unit q, k heads.  Vectors of 8 channels; the 16
-// vectors of one head sit on 16 consecutive lanes.
+// Path convolution + SiLU + unit q, k heads.  Block = (64 tokens, one group of
+// 128 channels: a q, k or v head); thread = (token of 16, 8 channels), so the
+// 16 lanes of one token hold one head and its weights stay in registers.
 __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const GdnParams p) {
-  const int x = blockIdx.x;
-  const int p1 = p.prev[x];
-  if (p1 == -2) {   // pad
-    float4* o4 = reinterpret_cast<float4*>(p.o + (size_t)x * p.H * kGd);
-    for (int i = threadIdx.x; i < p.H * kGd / 4; i += blockDim.x) o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    return;
+  const int grp = blockIdx.y, lt = threadIdx.x >> 4, vec = threadIdx.x & 15;
+  const int ch = grp * kGd + vec * 8;
+  const bool is_qk = grp < 2 * p.H;
+  __shared__ int taps[64][3];   // the 1, 2 and 3 tokens back on each token's path (-2: pad or past the end)
+  if (threadIdx.x < 64) {
+    const int x = blockIdx.x * 64 + threadIdx.x;
+    const int p1 = x < p.N ? p.prev[x] : -2;
+    const int p2 = p1 >= 0 ? p.prev[p1] : -1;
+    taps[threadIdx.x][0] = p1;
+    taps[threadIdx.x][1] = p2;
+    taps[threadIdx.x][2] = p2 >= 0 ? p.prev[p2] : -1;
   }
-  const int p2 = p1 >= 0 ? p.prev[p1] : -1;
-  const int p3 = p2 >= 0 ? p.prev[p2] : -1;
-  const int src[4] = {p3, p2, p1, x};   // taps 0..3
-  const int nvec = p.C / 8, qk_vecs = 2 * p.H * (kGd / 8);
-  for (int base = 0; base < nvec; base += blockDim.x) {
-    const int v = base + threadIdx.x;
-    const bool valid = v < nvec;
+  float4 wv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) wv[i] = reinterpret_cast<const float4*>(p.conv_w)[ch + i];
+  __syncthreads();
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int x = blockIdx.x * 64 + it * 16 + lt;
+    const bool in = x < p.N;
+    const int p1 = taps[it * 16 + lt][0];
+    if (p1 == -2) {
+      if (in && grp < p.H) {   // a pad: o = 0 for head grp
+        float4* o4 = reinterpret_cast<float4*>(p.o + ((size_t)x * p.H + grp) * kGd + vec * 8);
+        o4[0] = o4[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      continue;   // all 16 lanes of a token take the same branch
+    }
+    const int src[4] = {taps[it * 16 + lt][2], taps[it * 16 + lt][1], p1, x};   // taps 0..3
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    if (valid) {
-      const float4* w4 = reinterpret_cast<const float4*>(p.conv_w) + (size_t)v * 8;
-      float4 wv[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) wv[i] = w4[i];
+    for (int t = 0; t < 4; ++t) {
+      if (src[t] < 0) continue;
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(p.x + (size_t)src[t] * p.C + ch), f);
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        if (src[t] < 0) continue;
-        float f[8];
-        unpack8(*reinterpret_cast<const uint4*>(p.x + (size_t)src[t] * p.C + v * 8), f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float w = t == 0 ? wv[i].x : t == 1 ? wv[i].y : t == 2 ? wv[i].z : wv[i].w;
-          acc[i] = fmaf(w, f[i], acc[i]);
-        }
+      for (int i = 0; i < 8; ++i) {
+        const float w = t == 0 ? wv[i].x : t == 1 ? wv[i].y : t == 2 ? wv[i].z : wv[i].w;
+        acc[i] = fmaf(w, f[i], acc[i]);
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (1.f + expf(-acc[i]));
     }
-    float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(acc[i], acc[i], ss);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-    if (valid) {
-      if (v < qk_vecs) {
-        const float r = rsqrtf(ss + 1e-6f);
+    for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (1.f + expf(-acc[i]));
+    if (is_qk) {
+      float ss = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] *= r;
-      }
-      uint4 out;
-      out.x = pack_bf16x2(acc[0], acc[1]);
-      out.y = pack_bf16x2(acc[2], acc[3]);
-      out.z = pack_bf16x2(acc[4], acc[5]);
-      out.w = pack_bf16x2(acc[6], acc[7]);
-      *reinterpret_cast<uint4*>(p.y + (size_t)x * p.C + v * 8) = out;
+      for (int i = 0; i < 8; ++i) ss = fmaf(acc[i], acc[i], ss);
+      const unsigned grpmask = 0xffffu << (threadIdx.x & 16);
+      ss += __shfl_xor_sync(grpmask, ss, 8);
+      ss += __shfl_xor_sync(grpmask, ss, 4);
+      ss += __shfl_xor_sync(grpmask, ss, 2);
+      ss += __shfl_xor_sync(grpmask, ss, 1);
+      const float r = rsqrtf(ss + 1e-6f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] *= r;
     }
+    uint4 out;
+    out.x = pack_bf16x2(acc[0], acc[1]);
+    out.y = pack_bf16x2(acc[2], acc[3]);
+    out.z = pack_bf16x2(acc[4], acc[5]);
+    out.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(p.y + (size_t)x * p.C + ch) = out;
   }
 }
 
@@ -208,10 +224,10 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const GdnParams 
 // Per (chunk, head): everything of the chunk that does not depend on a state.
 __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const GdnParams p) {
   extern __shared__ float psm[];
-  float* sq = psm;                         // [64][129]
-  float* sk = sq + kGc * kPrepLd;          // [64][129]
-  float* sA = sk + kGc * kPrepLd;          // [64][65]
-  float* sgam = sA + kGc * 65;             // [64]
+  float* sq = psm;                         // [64][132]
+  float* sk = sq + kGc * kPrepLd;          // [64][132]
+  float* sA = sk + kGc * kPrepLd;          // [64][68]
+  float* sgam = sA + kGc * kPrepLa;        // [64]
   float* sbeta = sgam + kGc;               // [64]
   __nv_bfloat16* sv = reinterpret_cast<__nv_bfloat16*>(sbeta + kGc);   // [64][128]
   const int tid = threadIdx.x;
@@ -233,11 +249,12 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const GdnParams 
 #pragma unroll
       for (int j = 0; j < 8; ++j) fq[j] = fk[j] = 0.f;
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      sq[t * kPrepLd + c + j] = fq[j];
-      sk[t * kPrepLd + c + j] = fk[j];
-    }
+    float4* q4 = reinterpret_cast<float4*>(sq + t * kPrepLd + c);
+    float4* k4 = reinterpret_cast<float4*>(sk + t * kPrepLd + c);
+    q4[0] = make_float4(fq[0], fq[1], fq[2], fq[3]);
+    q4[1] = make_float4(fq[4], fq[5], fq[6], fq[7]);
+    k4[0] = make_float4(fk[0], fk[1], fk[2], fk[3]);
+    k4[1] = make_float4(fk[4], fk[5], fk[6], fk[7]);
     *reinterpret_cast<uint4*>(sv + t * kGd + c) = rv;
   }
   if (tid < kGc) {
@@ -261,50 +278,67 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const GdnParams 
   }
   __syncthreads();
 
-  // K K^T and Q K^T: thread = (row i, 16 columns j0..j0+15)
+  // K K^T and Q K^T, 4 x 4 per thread: rows i = ib + 16 ii, columns j = jb + 16 jj
   {
-    const int i = tid >> 2, j0 = (tid & 3) * 16;
-    float kk[16], qk[16];
+    const int ib = tid >> 4, jb = tid & 15;
+    float kk[4][4], qk[4][4];
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj) kk[jj] = qk[jj] = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < kGd; ++c) {
-      const float ki = sk[i * kPrepLd + c], qi = sq[i * kPrepLd + c];
+    for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const float kj = sk[(j0 + jj) * kPrepLd + c];
-        kk[jj] = fmaf(ki, kj, kk[jj]);
-        qk[jj] = fmaf(qi, kj, qk[jj]);
+      for (int b = 0; b < 4; ++b) kk[a][b] = qk[a][b] = 0.f;
+#pragma unroll 2
+    for (int c = 0; c < kGd; c += 4) {
+      float4 ki[4], qi[4], kj[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        ki[a] = *reinterpret_cast<const float4*>(sk + (ib + 16 * a) * kPrepLd + c);
+        qi[a] = *reinterpret_cast<const float4*>(sq + (ib + 16 * a) * kPrepLd + c);
+        kj[a] = *reinterpret_cast<const float4*>(sk + (jb + 16 * a) * kPrepLd + c);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          kk[a][b] = fmaf(ki[a].x, kj[b].x, fmaf(ki[a].y, kj[b].y, fmaf(ki[a].z, kj[b].z, fmaf(ki[a].w, kj[b].w, kk[a][b]))));
+          qk[a][b] = fmaf(qi[a].x, kj[b].x, fmaf(qi[a].y, kj[b].y, fmaf(qi[a].z, kj[b].z, fmaf(qi[a].w, kj[b].w, qk[a][b]))));
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int i = ib + 16 * a;
+      const float gi = sgam[i], bi = sbeta[i];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int j = jb + 16 * b;
+        const float de = j <= i ? expf(gi - sgam[j]) : 0.f;
+        sA[i * kPrepLa + j] = j < i ? bi * de * kk[a][b] : 0.f;
+        p.pm[(row * kGc + i) * kGc + j] = __float2bfloat16_rn((j <= i && i < L) ? p.scale * de * qk[a][b] : 0.f);
       }
     }
-    const float gi = sgam[i], bi = sbeta[i];
-    uint32_t pw[8];
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj) {
-      const int j = j0 + jj;
-      const float de = j <= i ? expf(gi - sgam[j]) : 0.f;
-      sA[i * 65 + j] = j < i ? bi * de * kk[jj] : 0.f;
-      qk[jj] = (j <= i && i < L) ? p.scale * de * qk[jj] : 0.f;
-    }
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) pw[jj] = pack_bf16x2(qk[2 * jj], qk[2 * jj + 1]);
-    uint4* dst = reinterpret_cast<uint4*>(p.pm + (row * kGc + i) * kGc + j0);
-    dst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-    dst[1] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
   }
   __syncthreads();
 
   // (I + A) X = B by forward substitution, one column per thread:
-  // columns 0-127 give U^ (B = beta V), 128-255 give W (B = beta e^gam K)
+  // columns 0-127 give U^ (B = beta V), 128-255 give W (B = beta e^gam K).
+  // A is strictly lower with zeros above, so row t can be read 4 wide up to
+  // the multiple of 4 past t - 1 (those X are still 0).
   {
     const int col = tid;
     float X[kGc];
+#pragma unroll
+    for (int t = 0; t < kGc; ++t) X[t] = 0.f;
 #pragma unroll
     for (int t = 0; t < kGc; ++t) {
       float b = col < kGd ? sbeta[t] * __bfloat162float(sv[t * kGd + col])
                           : sbeta[t] * expf(sgam[t]) * sk[t * kPrepLd + col - kGd];
 #pragma unroll
-      for (int s = 0; s < t; ++s) b = fmaf(-sA[t * 65 + s], X[s], b);
+      for (int s4 = 0; s4 < t; s4 += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(sA + t * kPrepLa + s4);
+        b = fmaf(-a.x, X[s4], b);
+        b = fmaf(-a.y, X[s4 + 1], b);
+        b = fmaf(-a.z, X[s4 + 2], b);
+        b = fmaf(-a.w, X[s4 + 3], b);
+      }
       X[t] = b;
     }
     if (col < kGd) {
@@ -312,25 +346,30 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const GdnParams 
 #pragma unroll
       for (int t = 0; t < kGc; t += 4) u4[t / 4] = make_float4(X[t], X[t + 1], X[t + 2], X[t + 3]);
     } else {
-      __nv_bfloat16* w = p.wq + row * 128 * kGd + (col - kGd);
+      __nv_bfloat16* w = p.wq + (row * 128 + kGc) * kGd + (col - kGd);
 #pragma unroll
       for (int t = 0; t < kGc; ++t) w[(size_t)t * kGd] = __float2bfloat16_rn(X[t]);
     }
   }
-  // Q~ rows (64..127 of the W|Q~ tile) and K~
+  // Q~ (rows 0..63 of the Q~|W tile) and K~
   const float gl = sgam[L - 1];
-  for (int i = tid; i < kGc * kGd; i += kPrepThreads) {
-    const int t = i / kGd, c = i % kGd;
-    const float qv = t < L ? p.scale * expf(sgam[t]) * sq[t * kPrepLd + c] : 0.f;
-    const float kv = t < L ? expf(gl - sgam[t]) * sk[t * kPrepLd + c] : 0.f;
-    p.wq[(row * 128 + kGc + t) * kGd + c] = __float2bfloat16_rn(qv);
-    p.kt[(row * kGc + t) * kGd + c] = __float2bfloat16_rn(kv);
+  for (int i = tid; i < kGc * kGd / 2; i += kPrepThreads) {
+    const int t = i / (kGd / 2), c = 2 * (i % (kGd / 2));
+    const float eq = t < L ? p.scale * expf(sgam[t]) : 0.f, ek = t < L ? expf(gl - sgam[t]) : 0.f;
+    reinterpret_cast<uint32_t*>(p.wq + (row * 128 + t) * kGd + c)[0] =
+        pack_bf16x2(eq * sq[t * kPrepLd + c], eq * sq[t * kPrepLd + c + 1]);
+    reinterpret_cast<uint32_t*>(p.kt + (row * kGc + t) * kGd + c)[0] =
+        pack_bf16x2(ek * sk[t * kPrepLd + c], ek * sk[t * kPrepLd + c + 1]);
   }
   if (tid == 0) p.decay[row] = expf(gl);
 }
 
 // ---------------------------------------------------------------------------
-// One CTA per (segment of this depth, head).
+// One CTA per (segment of this depth, head).  Per chunk i the critical chain is
+// E1(i) -> [Q~; W] S0 -> V'(i) -> P V', K~^T V' -> E1(i + 1); the output rows
+// of chunk i - 1 leave (through padded shared memory and one bulk copy per
+// row) while the tensor core works on chunk i, from the other of two
+// accumulator buffers.
 __global__ void __launch_bounds__(kStThreads, 1)
     gdn_state_kernel(const __grid_constant__ CUtensorMap mwq, const __grid_constant__ CUtensorMap mkt,
                      const __grid_constant__ CUtensorMap mpm, const GdnParams p) {
@@ -348,23 +387,19 @@ __global__ void __launch_bounds__(kStThreads, 1)
   const int par = p.seg_parent[sidx];
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < B_COUNT; ++b)
-      mbar_init(&bars[b], (b == B_SR || b == B_VR) ? 4 : b == B_UE ? 2 : 1);
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(&bars[b], (b == B_SR) ? 4 : (b == B_VR || b == B_UE) ? 2 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // the zero top halves of the [0; P] operand, both stages
-  for (int i = threadIdx.x; i < 2 * 512; i += kStThreads)
-    reinterpret_cast<uint4*>(sm + (i >> 9) * kStStage + kOffA2)[i & 511] = make_uint4(0, 0, 0, 0);
-  fence_proxy_async_smem();
   if (warp == 5) {
-    tmem_alloc(tmem_slot, 256);
+    tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  const uint32_t tmem = *tmem_slot;   // columns 0-127: the state S; 128-255: [W S0 ; Q~ S0 + P V']
+  // columns 0-127: the state S; 128 + 128 b (b = chunk parity): [Q~ S0 + P V' ; W S0]
+  const uint32_t tmem = *tmem_slot;
 
   if (warp == 4) {
     if (lane == 0) {
@@ -402,23 +437,22 @@ __global__ void __launch_bounds__(kStThreads, 1)
       constexpr uint32_t id_mnmn = idesc_bf16(128, 128, 1, 1);
       for (int i = 0; i < nck; ++i) {
         const int st = i & 1;
-        const uint32_t stage = sb + st * kStStage;
+        const uint32_t stage = sb + st * kStStage, d1 = tmem + 128 + 128 * (i & 1);
         if (!mbar_wait(&bars[B_SR], i & 1, abort_flag, p.err)) break;
         if (!mbar_wait(&bars[B_F + st], (i >> 1) & 1, abort_flag, p.err)) break;
         fence_after_sync();
-        // [W; Q~] S0 -> columns 128-255
+        // [Q~; W] S0
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_ss_lo(tmem + 128, desc_lo_kmajor(stage + (s >> 2) * 16384 + (s & 3) * 32),
+          mma_ss_lo(d1, desc_lo_kmajor(stage + (s >> 2) * 16384 + (s & 3) * 32),
                     desc_lo_mnmajor(sb + kOffSop + s * 2048), id_kmn, s > 0 ? 1u : 0u);
         mma_commit(&bars[B_M1]);
         if (!mbar_wait(&bars[B_VR], i & 1, abort_flag, p.err)) break;
         fence_after_sync();
-        // rows 64-127: Q~ S0 + P V';  state: e^{gam_L} S0 + K~^T V'
+        // rows 0-63: Q~ S0 + P V';  state: e^{gam_L} S0 + K~^T V'
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          mma_ss_lo(tmem + 128, desc_lo_kmajor(stage + kOffA2 + s * 32), desc_lo_mn8k(sb + kOffVop + s * 2048),
-                    id_kmn, 1u);
+          mma_ss_lo(d1, desc_lo_kmajor(stage + kOffP + s * 32), desc_lo_mn8k(sb + kOffVop + s * 2048), id_kmn, 1u);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
           mma_ss_lo(tmem, desc_lo_mn8k(stage + kOffKt + s * 2048), desc_lo_mn8k(sb + kOffVop + s * 2048), id_mnmn,
@@ -432,9 +466,19 @@ __global__ void __launch_bounds__(kStThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int r = threadIdx.x;   // TMEM lane: the state's k row; of columns 128-255 the chunk row
+    const int r = threadIdx.x;   // TMEM lane: the state's k row; of the accumulator, the chunk row
     const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-    uint32_t v[32];
+    uint32_t v[128];
+    // One padded 528-byte row per thread: a row in shared memory, then one bulk copy to HBM.
+    auto row_out = [&](uint8_t* buf, float* dst) {
+      bulk_wait_read0();   // the previous copy from this row has read it
+#pragma unroll
+      for (int q = 0; q < 32; ++q)
+        reinterpret_cast<uint4*>(buf)[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      fence_proxy_async_smem();
+      bulk_store(dst, buf, 512);
+      bulk_commit();
+    };
     {
       const float* src = par >= 0 ? p.state + (((size_t)par * p.H + h) * kGd + r) * kGd : nullptr;
 #pragma unroll 1
@@ -446,59 +490,78 @@ __global__ void __launch_bounds__(kStThreads, 1)
       tmem_st_wait();
     }
     bool ok = true;
+    // the chunk's scalars are read one chunk ahead
+    int L = p.chunk_len[c0], x0 = p.chunk_start[c0], L_prev = 0, x0_prev = 0;
+    float dec = p.decay[c0 * p.H + h];
     for (int i = 0; ok && i < nck; ++i) {
-      const int row = (c0 + i) * p.H + h;
-      const int L = p.chunk_len[c0 + i], x0 = p.chunk_start[c0 + i];
-      const float dec = p.decay[row];
-      // S0 -> bf16 operand (k rows, v contiguous in two 64-column halves); S <- e^{gam_L} S0
-#pragma unroll 1
+      int L_next = 0, x0_next = 0;
+      float dec_next = 0.f;
+      if (i + 1 < nck) {
+        L_next = p.chunk_len[c0 + i + 1];
+        x0_next = p.chunk_start[c0 + i + 1];
+        dec_next = p.decay[(c0 + i + 1) * p.H + h];
+      }
+      // E1: S0 -> bf16 operand (k rows, v contiguous in two 64-column halves); S <- e^{gam_L} S0
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lrow + cc * 32, v + 32 * cc);
+      tmem_ld_wait();
+#pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        tmem_ld32(tmem + lrow + cc * 32, v);
-        tmem_ld_wait();
         uint8_t* half = sm + kOffSop + (cc >> 1) * 16384 + r * 128;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
+          const uint32_t* e = v + 32 * cc + 8 * jj;
           const int j = (cc & 1) * 4 + jj;
           uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(v[8 * jj + 0]), __uint_as_float(v[8 * jj + 1]));
-          w.y = pack_bf16x2(__uint_as_float(v[8 * jj + 2]), __uint_as_float(v[8 * jj + 3]));
-          w.z = pack_bf16x2(__uint_as_float(v[8 * jj + 4]), __uint_as_float(v[8 * jj + 5]));
-          w.w = pack_bf16x2(__uint_as_float(v[8 * jj + 6]), __uint_as_float(v[8 * jj + 7]));
+          w.x = pack_bf16x2(__uint_as_float(e[0]), __uint_as_float(e[1]));
+          w.y = pack_bf16x2(__uint_as_float(e[2]), __uint_as_float(e[3]));
+          w.z = pack_bf16x2(__uint_as_float(e[4]), __uint_as_float(e[5]));
+          w.w = pack_bf16x2(__uint_as_float(e[6]), __uint_as_float(e[7]));
           *reinterpret_cast<uint4*>(half + ((j ^ (r & 7)) << 4)) = w;
         }
-#pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * dec);
-        tmem_st32(tmem + lrow + cc * 32, v);
       }
+#pragma unroll
+      for (int q = 0; q < 128; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * dec);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_st32(tmem + lrow + cc * 32, v + 32 * cc);
       tmem_st_wait();
       fence_proxy_async_smem();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_SR]);
 
-      // V' = U^ - W S0 on rows 0-63 (warps 0, 1)
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_M1], i & 1, abort_flag, p.err))) {
-        ok = false;
-        break;
-      }
-      fence_after_sync();
       if (warp < 2) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_UF], i & 1, abort_flag, p.err))) {
+        // E3 of the previous chunk: its output rows 0-63 of the other accumulator
+        if (i > 0) {
+          const uint32_t d1p = tmem + 128 + 128 * ((i - 1) & 1);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) tmem_ld32(d1p + lrow + cc * 32, v + 32 * cc);
+          tmem_ld_wait();
+          if (r < L_prev) row_out(sm + kOffOst + r * kOstLd, p.o + ((size_t)(x0_prev + r) * p.H + h) * kGd);
+        }
+      } else {
+        // E2: V' = U^ - W S0 on rows 64-127 (chunk row r - 64)
+        const int t = r - 64;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_M1], i & 1, abort_flag, p.err)) ||
+            !__all_sync(0xffffffffu, mbar_wait(&bars[B_UF], i & 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
-#pragma unroll 1
+        fence_after_sync();
+        const uint32_t d1 = tmem + 128 + 128 * (i & 1);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(d1 + lrow + cc * 32, v + 32 * cc);
+        tmem_ld_wait();
+#pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          tmem_ld32(tmem + lrow + 128 + cc * 32, v);
-          tmem_ld_wait();
-          uint8_t* half = sm + kOffVop + (cc >> 1) * 8192 + r * 128;
+          uint8_t* half = sm + kOffVop + (cc >> 1) * 8192 + t * 128;
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             float f[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int col = cc * 32 + 8 * jj + e;
-              f[e] = ut_s[col * kGc + r] - __uint_as_float(v[8 * jj + e]);
+              f[e] = ut_s[col * kGc + t] - __uint_as_float(v[col]);
             }
             const int j = (cc & 1) * 4 + jj;
             uint4 w;
@@ -506,61 +569,53 @@ __global__ void __launch_bounds__(kStThreads, 1)
             w.y = pack_bf16x2(f[2], f[3]);
             w.z = pack_bf16x2(f[4], f[5]);
             w.w = pack_bf16x2(f[6], f[7]);
-            *reinterpret_cast<uint4*>(half + ((j ^ (r & 7)) << 4)) = w;
+            *reinterpret_cast<uint4*>(half + ((j ^ (t & 7)) << 4)) = w;
           }
         }
         fence_proxy_async_smem();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars[B_VR]);
+          mbar_arrive(&bars[B_UE]);
+        }
       }
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[B_VR]);
-        if (warp < 2) mbar_arrive(&bars[B_UE]);
-      }
-
-      // O rows (warps 2, 3; chunk row r - 64)
+      // the state of the next chunk
       if (!__all_sync(0xffffffffu, mbar_wait(&bars[B_M2], i & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
       fence_after_sync();
-      if (warp >= 2) {
-        const int t = r - 64;
-        float* dst = p.o + ((size_t)(x0 + t) * p.H + h) * kGd;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          tmem_ld32(tmem + lrow + 128 + cc * 32, v);
-          tmem_ld_wait();
-          if (t < L) {
-            float4* d4 = reinterpret_cast<float4*>(dst + cc * 32);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                  __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-          }
-        }
-      }
+      L_prev = L;
+      x0_prev = x0;
+      L = L_next;
+      x0 = x0_next;
+      dec = dec_next;
     }
-    if (ok) {   // the segment's final state, for its children
-      float* dst = p.state + (((size_t)sidx * p.H + h) * kGd + r) * kGd;
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        tmem_ld32(tmem + lrow + cc * 32, v);
+    if (ok) {
+      if (warp < 2) {   // the last chunk's output rows
+        const uint32_t d1p = tmem + 128 + 128 * ((nck - 1) & 1);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(d1p + lrow + cc * 32, v + 32 * cc);
         tmem_ld_wait();
-        float4* d4 = reinterpret_cast<float4*>(dst + cc * 32);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
-                              __uint_as_float(v[4 * q + 3]));
+        if (r < L_prev) row_out(sm + kOffOst + r * kOstLd, p.o + ((size_t)(x0_prev + r) * p.H + h) * kGd);
       }
+      // the segment's final state, for its children (rows 64-127 go through the
+      // operand buffers, which no MMA reads any more)
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lrow + cc * 32, v + 32 * cc);
+      tmem_ld_wait();
+      uint8_t* buf = r < 64 ? sm + kOffOst + r * kOstLd : sm + kOffSop + (r - 64) * kOstLd;
+      row_out(buf, p.state + (((size_t)sidx * p.H + h) * kGd + r) * kGd);
     }
+    bulk_wait_all0();
   }
 
   __syncwarp();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 5) tmem_dealloc(tmem, 256);
+  if (warp == 5) tmem_dealloc(tmem, 512);
 }
 
 struct GdnLayout {
@@ -684,7 +739,7 @@ extern "C" stp_status stp_gdn_fwd(const stp_gdn_desc* desc, const void* plan, co
   cudaError_t e = attr_err;
   if (e == cudaSuccess) e = cudaMemsetAsync(p.err, 0, 4, s);
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e));
-  gdn_conv_kernel<<<(unsigned)N, kConvThreads, 0, s>>>(p);
+  gdn_conv_kernel<<<dim3((unsigned)((N + 63) / 64), (unsigned)(3 * H)), kConvThreads, 0, s>>>(p);
   if (n_chunk > 0) gdn_prep_kernel<<<(unsigned)(n_chunk * H), kPrepThreads, kPrepSmem, s>>>(p);
   const int32_t* depth_off = w + w[GP_DEPTH_OFF];
   for (int d = 0; d < n_depth; ++d) {
