@@ -72,7 +72,9 @@ constexpr int kStSmem = kOffBar + 256 + 1024;
 struct GdnParams {
   int N, H, C, seg0;
   float scale;
-  const int32_t* prev;
+  const int32_t* prev;      // token 1, 2 and 3 back on the path (-2 on prev: a pad)
+  const int32_t* prev2;
+  const int32_t* prev3;
   const int32_t* seg_len;
   const int32_t* seg_parent;
   const int32_t* seg_chunk0;
@@ -159,11 +161,10 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const GdnParams 
   __shared__ int taps[64][3];   // the 1, 2 and 3 tokens back on each token's path (-2: pad or past the end)
   if (threadIdx.x < 64) {
     const int x = blockIdx.x * 64 + threadIdx.x;
-    const int p1 = x < p.N ? p.prev[x] : -2;
-    const int p2 = p1 >= 0 ? p.prev[p1] : -1;
-    taps[threadIdx.x][0] = p1;
-    taps[threadIdx.x][1] = p2;
-    taps[threadIdx.x][2] = p2 >= 0 ? p.prev[p2] : -1;
+    const bool in = x < p.N;
+    taps[threadIdx.x][0] = in ? p.prev[x] : -2;
+    taps[threadIdx.x][1] = in ? p.prev2[x] : -1;
+    taps[threadIdx.x][2] = in ? p.prev3[x] : -1;
   }
   float4 wv[8];
 #pragma unroll
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const GdnParams 
       }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = acc[i] / (1.f + expf(-acc[i]));
+    for (int i = 0; i < 8; ++i) acc[i] = __fdividef(acc[i], 1.f + __expf(-acc[i]));
     if (is_qk) {
       float ss = 0.f;
 #pragma unroll
@@ -702,6 +703,8 @@ extern "C" stp_status stp_gdn_fwd(const stp_gdn_desc* desc, const void* plan, co
   p.seg0 = 0;
   p.scale = desc->scale;
   p.prev = dp + w[GP_PREV];
+  p.prev2 = dp + w[GP_PREV2];
+  p.prev3 = dp + w[GP_PREV3];
   p.seg_len = dp + w[GP_SEG_LEN];
   p.seg_parent = dp + w[GP_SEG_PARENT];
   p.seg_chunk0 = dp + w[GP_SEG_CHUNK0];

@@ -36,8 +36,8 @@ extern "C" stp_status stp_gdn_plan_bound(const stp_gdn_desc* desc, size_t* plan_
   if (st) return st;
   if (!plan_bytes) return fail(STP_EINVAL, "stp_gdn_plan_bound: NULL output");
   const size_t N = (size_t)desc->n_rows * desc->row_len;
-  // prev, 4 words per segment, depth offsets, 2 words per chunk (segments, chunks <= N)
-  *plan_bytes = 4 * (kGdnHeader + N + 4 * N + (N + 1) + 2 * N);
+  // prev (1, 2 and 3 back), 4 words per segment, depth offsets, 2 words per chunk (segments, chunks <= N)
+  *plan_bytes = 4 * (kGdnHeader + 3 * N + 4 * N + (N + 1) + 2 * N);
   return STP_OK;
 }
 
@@ -123,6 +123,8 @@ extern "C" stp_status stp_gdn_plan(const stp_gdn_desc* desc, const int32_t* subt
     o += n;
   };
   take(GP_PREV, N);
+  take(GP_PREV2, N);
+  take(GP_PREV3, N);
   take(GP_SEG_START, n_seg);
   take(GP_SEG_LEN, n_seg);
   take(GP_SEG_PARENT, n_seg);
@@ -138,6 +140,11 @@ extern "C" stp_status stp_gdn_plan(const stp_gdn_desc* desc, const int32_t* subt
   w[GP_WORDS] = (int32_t)o;
   w[GP_MAX_DEPTH_SEGS] = max_depth_segs;
   std::memcpy(w + w[GP_PREV], prev.data(), 4 * N);
+  for (int64_t x = 0; x < N; ++x) {   // two and three tokens back on the path (-1: none)
+    const int32_t p1 = prev[x], p2 = p1 >= 0 ? prev[p1] : -1;
+    w[w[GP_PREV2] + x] = p2;
+    w[w[GP_PREV3] + x] = p2 >= 0 ? prev[p2] : -1;
+  }
   int32_t c = 0;
   for (int32_t i = 0; i < n_seg; ++i) {
     const int32_t s = order[i];

@@ -412,7 +412,7 @@ def stp_logprob_gather(desc: LogprobDesc, hidden, w_vocab, token_ids, loss_mask,
 
 # plan header fields (int32 words), as the library writes them
 GP_MAGIC, GP_N, GP_NSEG, GP_NCHUNK, GP_NDEPTH, GP_WORDS, GP_PREV, GP_SEG_START, GP_SEG_LEN, GP_SEG_PARENT, \
-    GP_SEG_CHUNK0, GP_DEPTH_OFF, GP_CHUNK_START, GP_CHUNK_LEN, GP_MAX_DEPTH_SEGS = range(15)
+    GP_SEG_CHUNK0, GP_DEPTH_OFF, GP_CHUNK_START, GP_CHUNK_LEN, GP_MAX_DEPTH_SEGS, GP_PREV2, GP_PREV3 = range(17)
 
 
 def gdn_desc(n_rows, row_len, n_heads, head_dim=128, scale=None) -> GdnDesc:
@@ -441,7 +441,7 @@ def gdn_plan_arrays(plan: np.ndarray) -> dict:
     w = plan
     n, ns, nc, nd = w[GP_N], w[GP_NSEG], w[GP_NCHUNK], w[GP_NDEPTH]
     at = lambda f, k: w[w[f]: w[f] + k]  # noqa: E731
-    return {"prev": at(GP_PREV, n), "seg_start": at(GP_SEG_START, ns), "seg_len": at(GP_SEG_LEN, ns),
+    return {"prev": at(GP_PREV, n), "prev2": at(GP_PREV2, n), "prev3": at(GP_PREV3, n), "seg_start": at(GP_SEG_START, ns), "seg_len": at(GP_SEG_LEN, ns),
             "seg_parent": at(GP_SEG_PARENT, ns), "seg_chunk0": at(GP_SEG_CHUNK0, ns),
             "depth_off": at(GP_DEPTH_OFF, nd + 1), "chunk_start": at(GP_CHUNK_START, nc),
             "chunk_len": at(GP_CHUNK_LEN, nc)}

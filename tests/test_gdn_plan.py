@@ -26,6 +26,9 @@ def _check(plan_o, H=2):
         assert np.all(got[u:] == -2)
         exp = np.where(want[:u] >= 0, want[:u] + r * T, -1)
         assert np.array_equal(got[:u], exp)
+    back = lambda a: np.where(a >= 0, prev[np.maximum(a, 0)], -1)  # noqa: E731
+    p2 = back(prev)
+    assert np.array_equal(a["prev2"], p2) and np.array_equal(a["prev3"], back(p2))
     n_child = np.bincount(prev[prev >= 0], minlength=R * T)
     covered = np.zeros(R * T, np.int64)
     depth = np.full(len(a["seg_start"]), -1)
