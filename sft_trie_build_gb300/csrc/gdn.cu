@@ -15,8 +15,8 @@
 //   gdn_conv_kernel   one block per (64 tokens, q / k / v head): width-4 causal
 //                     convolution along each token's path (prev pointers of
 //                     the plan), SiLU, unit q and k heads; pads get o = 0.
-//   gdn_prep_kernel   one block per (chunk, head), float32 on the CUDA cores:
-//                     A by 4 x 4 register-blocked dot products, the
+//   gdn_prep_kernel   one block per (chunk, head): [Q K^T; K K^T] on the tensor
+//                     core, then in float32 on the CUDA cores the
 //                     unit-lower-triangular solve for U^ and W (one column per
 //                     thread), and the chunk's operands
 //                     W | Q~ (Q~ = scale e^{gam} Q), K~ = e^{gam_L - gam} K,
@@ -50,10 +50,14 @@ constexpr int kConvThreads = 256;
 constexpr int kPrepThreads = 256;
 constexpr int kStThreads = 192;   // warps 0-3 epilogue, 4 loads, 5 MMA
 
-// gdn_prep_kernel shared memory (floats): q, k [64][132], A [64][68], gam, beta [64]; v as bf16 [64][128].
-// Row strides keep float4 rows aligned and the 8 rows a quarter warp reads in distinct banks.
-constexpr int kPrepLd = 132, kPrepLa = 68;
-constexpr int kPrepSmem = (2 * kGc * kPrepLd + kGc * kPrepLa + 2 * kGc) * 4 + kGc * kGd * 2;
+// gdn_prep_kernel shared memory, from a 1024-byte aligned base: [Q; K] as a
+// 128 x 128 bf16 K-major operand (128-byte swizzle, two 64-column halves),
+// V bf16 [64][128], A float32 [64][68] (rows 16-byte aligned), gam, beta,
+// e^gam, e^{gam_L - gam} [64], the MMA barrier and the TMEM address.
+constexpr int kPrepLa = 68;
+constexpr int kPoV = 32768, kPoA = kPoV + 16384, kPoGam = kPoA + kGc * kPrepLa * 4, kPoBeta = kPoGam + 256,
+              kPoEg = kPoBeta + 256, kPoEk = kPoEg + 256, kPoBar = kPoEk + 256;
+constexpr int kPrepSmem = kPoBar + 64 + 1024;
 
 // gdn_state_kernel shared memory, from a 1024-byte aligned base.  A stage holds
 // [Q~; W] (32 KB), K~ (16 KB) and P (8 KB); P is the top half of a 128-row MMA
@@ -223,47 +227,77 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const GdnParams 
 
 // ---------------------------------------------------------------------------
 // Per (chunk, head): everything of the chunk that does not depend on a state.
-__global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const GdnParams p) {
-  extern __shared__ float psm[];
-  float* sq = psm;                         // [64][132]
-  float* sk = sq + kGc * kPrepLd;          // [64][132]
-  float* sA = sk + kGc * kPrepLd;          // [64][68]
-  float* sgam = sA + kGc * kPrepLa;        // [64]
-  float* sbeta = sgam + kGc;               // [64]
-  __nv_bfloat16* sv = reinterpret_cast<__nv_bfloat16*>(sbeta + kGc);   // [64][128]
-  const int tid = threadIdx.x;
+// [Q K^T; K K^T] is one tcgen05 pass (M = 128, N = 64, K = 128) into TMEM; the
+// triangular solve and the operand scaling run on the CUDA cores in float32.
+
+// bf16 element (m, c) of the swizzled [Q; K] operand
+__device__ __forceinline__ float qk_at(const uint8_t* tile, int m, int c) {
+  const uint16_t u = *reinterpret_cast<const uint16_t*>(tile + (c >> 6) * 16384 + m * 128 +
+                                                        ((((c & 63) >> 3) ^ (m & 7)) << 4) + (c & 7) * 2);
+  return __uint_as_float((uint32_t)u << 16);
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnParams p) {
+  extern __shared__ uint8_t prep_dyn[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(prep_dyn) + 1023) & ~uintptr_t(1023));
+  uint8_t* tile = sm;                                              // [Q; K]
+  __nv_bfloat16* sv = reinterpret_cast<__nv_bfloat16*>(sm + kPoV);  // [64][128]
+  float* sA = reinterpret_cast<float*>(sm + kPoA);                 // [64][68]
+  float* sgam = reinterpret_cast<float*>(sm + kPoGam);
+  float* sbeta = reinterpret_cast<float*>(sm + kPoBeta);
+  float* seg = reinterpret_cast<float*>(sm + kPoEg);               // e^{gam_t}
+  float* sek = reinterpret_cast<float*>(sm + kPoEk);               // e^{gam_L - gam_t}
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kPoBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ch = blockIdx.x / p.H, h = blockIdx.x % p.H;
   const int x0 = p.chunk_start[ch], L = p.chunk_len[ch];
   const int Hd = p.H * kGd;
   const size_t row = (size_t)ch * p.H + h;
 
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 64);
+    tmem_relinquish();
+  }
   for (int i = tid; i < kGc * 16; i += kPrepThreads) {
     const int t = i >> 4, c = (i & 15) * 8;
-    float fq[8], fk[8];
-    uint4 rv = make_uint4(0, 0, 0, 0);
+    uint4 rq = make_uint4(0, 0, 0, 0), rk = rq, rv = rq;
     if (t < L) {
       const __nv_bfloat16* yr = p.y + (size_t)(x0 + t) * p.C + h * kGd + c;
-      unpack8(*reinterpret_cast<const uint4*>(yr), fq);
-      unpack8(*reinterpret_cast<const uint4*>(yr + Hd), fk);
+      rq = *reinterpret_cast<const uint4*>(yr);
+      rk = *reinterpret_cast<const uint4*>(yr + Hd);
       rv = *reinterpret_cast<const uint4*>(yr + 2 * Hd);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) fq[j] = fk[j] = 0.f;
     }
-    float4* q4 = reinterpret_cast<float4*>(sq + t * kPrepLd + c);
-    float4* k4 = reinterpret_cast<float4*>(sk + t * kPrepLd + c);
-    q4[0] = make_float4(fq[0], fq[1], fq[2], fq[3]);
-    q4[1] = make_float4(fq[4], fq[5], fq[6], fq[7]);
-    k4[0] = make_float4(fk[0], fk[1], fk[2], fk[3]);
-    k4[1] = make_float4(fk[4], fk[5], fk[6], fk[7]);
+    const int off = (c >> 6) * 16384 + ((((c & 63) >> 3) ^ (t & 7)) << 4);
+    *reinterpret_cast<uint4*>(tile + off + t * 128) = rq;
+    *reinterpret_cast<uint4*>(tile + off + (kGc + t) * 128) = rk;
     *reinterpret_cast<uint4*>(sv + t * kGd + c) = rv;
   }
   if (tid < kGc) {
     sgam[tid] = tid < L ? p.g[(size_t)(x0 + tid) * p.H + h] : 0.f;
     sbeta[tid] = tid < L ? p.beta[(size_t)(x0 + tid) * p.H + h] : 0.f;
   }
+  fence_proxy_async_smem();
+  fence_before_sync();
   __syncthreads();
-  if (tid < 32) {   // inclusive prefix sum of g over the 64 rows
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  if (tid == 0) {
+    constexpr uint32_t idesc = idesc_bf16(128, 64, 0, 0);
+    const uint32_t tb = smem_u32(tile);
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      mma_ss_lo(tmem, desc_lo_kmajor(tb + (s >> 2) * 16384 + (s & 3) * 32),
+                desc_lo_kmajor(tb + (s >> 2) * 16384 + 8192 + (s & 3) * 32), idesc, s > 0 ? 1u : 0u);
+    mma_commit(bar);
+  }
+  if (tid < 32) {   // inclusive prefix sum of g over the 64 rows, and the row exponentials
     float a = sgam[tid], b = sgam[tid + 32];
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -274,50 +308,56 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const GdnParams 
       }
     }
     b += __shfl_sync(0xffffffffu, a, 31);
+    const float gl = __shfl_sync(0xffffffffu, (L - 1) < 32 ? a : b, (L - 1) & 31);
     sgam[tid] = a;
     sgam[tid + 32] = b;
+    seg[tid] = expf(a);
+    seg[tid + 32] = expf(b);
+    sek[tid] = expf(gl - a);
+    sek[tid + 32] = expf(gl - b);
   }
   __syncthreads();
 
-  // K K^T and Q K^T, 4 x 4 per thread: rows i = ib + 16 ii, columns j = jb + 16 jj
+  // A (strictly lower, from K K^T) and P (lower with the diagonal, from Q K^T):
+  // warp w reads TMEM rows 32 (w % 4) .. + 31, columns 32 (w / 4) .. + 31
   {
-    const int ib = tid >> 4, jb = tid & 15;
-    float kk[4][4], qk[4][4];
+    const bool ready = mbar_wait(bar, 0, abort_flag, p.err);
+    fence_after_sync();
+    uint32_t v[32];
+    const int m = 32 * (warp & 3) + lane, j0 = 32 * (warp >> 2);
+    tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + j0, v);
+    tmem_ld_wait();
+    if (m < kGc) {
+      const int i = m;
+      const float gi = sgam[i];
+      uint32_t pw[16];
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+      for (int q = 0; q < 32; q += 2) {
+        float f[2];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) kk[a][b] = qk[a][b] = 0.f;
-#pragma unroll 2
-    for (int c = 0; c < kGd; c += 4) {
-      float4 ki[4], qi[4], kj[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        ki[a] = *reinterpret_cast<const float4*>(sk + (ib + 16 * a) * kPrepLd + c);
-        qi[a] = *reinterpret_cast<const float4*>(sq + (ib + 16 * a) * kPrepLd + c);
-        kj[a] = *reinterpret_cast<const float4*>(sk + (jb + 16 * a) * kPrepLd + c);
-      }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          kk[a][b] = fmaf(ki[a].x, kj[b].x, fmaf(ki[a].y, kj[b].y, fmaf(ki[a].z, kj[b].z, fmaf(ki[a].w, kj[b].w, kk[a][b]))));
-          qk[a][b] = fmaf(qi[a].x, kj[b].x, fmaf(qi[a].y, kj[b].y, fmaf(qi[a].z, kj[b].z, fmaf(qi[a].w, kj[b].w, qk[a][b]))));
+        for (int e = 0; e < 2; ++e) {
+          const int j = j0 + q + e;
+          f[e] = (ready && j <= i && i < L) ? p.scale * expf(gi - sgam[j]) * __uint_as_float(v[q + e]) : 0.f;
         }
-    }
+        pw[q / 2] = pack_bf16x2(f[0], f[1]);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(p.pm + (row * kGc + i) * kGc + j0);
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const int i = ib + 16 * a;
+      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+    } else {
+      const int i = m - kGc;
       const float gi = sgam[i], bi = sbeta[i];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int j = jb + 16 * b;
-        const float de = j <= i ? expf(gi - sgam[j]) : 0.f;
-        sA[i * kPrepLa + j] = j < i ? bi * de * kk[a][b] : 0.f;
-        p.pm[(row * kGc + i) * kGc + j] = __float2bfloat16_rn((j <= i && i < L) ? p.scale * de * qk[a][b] : 0.f);
+      for (int q = 0; q < 32; ++q) {
+        const int j = j0 + q;
+        sA[i * kPrepLa + j] = (ready && j < i) ? bi * expf(gi - sgam[j]) * __uint_as_float(v[q]) : 0.f;
       }
     }
   }
+  fence_before_sync();
   __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 64);
 
   // (I + A) X = B by forward substitution, one column per thread:
   // columns 0-127 give U^ (B = beta V), 128-255 give W (B = beta e^gam K).
@@ -331,7 +371,7 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const GdnParams 
 #pragma unroll
     for (int t = 0; t < kGc; ++t) {
       float b = col < kGd ? sbeta[t] * __bfloat162float(sv[t * kGd + col])
-                          : sbeta[t] * expf(sgam[t]) * sk[t * kPrepLd + col - kGd];
+                          : sbeta[t] * seg[t] * qk_at(tile, kGc + t, col - kGd);
 #pragma unroll
       for (int s4 = 0; s4 < t; s4 += 4) {
         const float4 a = *reinterpret_cast<const float4*>(sA + t * kPrepLa + s4);
@@ -353,16 +393,15 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const GdnParams 
     }
   }
   // Q~ (rows 0..63 of the Q~|W tile) and K~
-  const float gl = sgam[L - 1];
   for (int i = tid; i < kGc * kGd / 2; i += kPrepThreads) {
     const int t = i / (kGd / 2), c = 2 * (i % (kGd / 2));
-    const float eq = t < L ? p.scale * expf(sgam[t]) : 0.f, ek = t < L ? expf(gl - sgam[t]) : 0.f;
+    const float eq = t < L ? p.scale * seg[t] : 0.f, ek = t < L ? sek[t] : 0.f;
     reinterpret_cast<uint32_t*>(p.wq + (row * 128 + t) * kGd + c)[0] =
-        pack_bf16x2(eq * sq[t * kPrepLd + c], eq * sq[t * kPrepLd + c + 1]);
+        pack_bf16x2(eq * qk_at(tile, t, c), eq * qk_at(tile, t, c + 1));
     reinterpret_cast<uint32_t*>(p.kt + (row * kGc + t) * kGd + c)[0] =
-        pack_bf16x2(ek * sk[t * kPrepLd + c], ek * sk[t * kPrepLd + c + 1]);
+        pack_bf16x2(ek * qk_at(tile, kGc + t, c), ek * qk_at(tile, kGc + t, c + 1));
   }
-  if (tid == 0) p.decay[row] = expf(gl);
+  if (tid == 0) p.decay[row] = expf(sgam[L - 1]);
 }
 
 // ---------------------------------------------------------------------------
