@@ -21,7 +21,9 @@ The layer core, per head h (state S of shape [d_k, d_v]):
     o_t        = scale * S_t^T q_t
 
 (the gated delta rule: decay the state, then move the value stored under
-k_t a fraction beta_t of the way toward v_t).
+k_t a fraction beta_t of the way toward v_t).  ``gdn_grads`` is its reverse
+mode for L = sum dO . o: a fork's state gradient is the sum over its
+children, accumulated as the tokens are visited last to first.
 
 Paths come from the packer's parent pointers (``oracle.attn.RowTree``),
 never from ``subtree_end``: the token before i on its path is the last
@@ -117,3 +119,98 @@ def gdn_sequence(x, conv_w, g, beta, H: int, d: int, scale: float) -> np.ndarray
     y = conv_path(np.asarray(x, np.float64), np.asarray(conv_w, np.float64), prev)
     q, k, v = split_heads(y, H, d)
     return delta_rule(q, k, v, np.asarray(g, np.float64), np.asarray(beta, np.float64), prev, scale)
+
+
+# ---------------------------------------------------------------------------
+# Backward (reverse mode through the same steps), for the loss
+#     L = sum_t sum_h dO[t, h] . o[t, h]
+# Tokens are visited in reverse order (a token's children come after it), so
+# when token t is reached its state gradient already holds the sum over all
+# of its children -- the fork's gradient is the sum of its branches'.
+# ---------------------------------------------------------------------------
+
+def _taps(prev: np.ndarray, t: int):
+    """(tap, source token) pairs: tap 3 is the token itself, tap 2 one back on
+    its path, ... as far as the path goes."""
+    out, j = [], t
+    for i in range(WIDTH - 1, -1, -1):
+        if j < 0:
+            break
+        out.append((i, j))
+        j = prev[j]
+    return out
+
+
+def gdn_grads(x, conv_w, g, beta, dO, prev, H: int, d: int, scale: float):
+    """(dx [T, C], dconv_w [C, 4], dg [T, H], dbeta [T, H]) of the layer core
+    over one row or sequence whose path predecessors are prev (prev[t] < t)."""
+    x = np.asarray(x, np.float64)
+    conv_w = np.asarray(conv_w, np.float64)
+    g = np.asarray(g, np.float64)
+    beta = np.asarray(beta, np.float64)
+    dO = np.asarray(dO, np.float64)
+    T, C = x.shape
+    z = np.zeros((T, C))
+    for t in range(T):
+        for i, j in _taps(prev, t):
+            z[t] += conv_w[:, i] * x[j]
+    sig = 1.0 / (1.0 + np.exp(-z))
+    y = z * sig
+    raw = [y[:, b * H * d:(b + 1) * H * d].reshape(T, H, d) for b in range(3)]
+    nrm = [np.sqrt((raw[b] ** 2).sum(-1, keepdims=True) + EPS) for b in range(2)]
+    q, k, v = raw[0] / nrm[0], raw[1] / nrm[1], raw[2]
+
+    S = np.zeros((T, H, d, d))
+    for t in range(T):
+        p = prev[t]
+        for h in range(H):
+            Sp = S[p, h] if p >= 0 else np.zeros((d, d))
+            a = np.exp(g[t, h])
+            S[t, h] = a * Sp + np.outer(k[t, h], beta[t, h] * (v[t, h] - a * Sp.T @ k[t, h]))
+
+    dS = np.zeros((T, H, d, d))
+    dq, dk, dv = np.zeros((T, H, d)), np.zeros((T, H, d)), np.zeros((T, H, d))
+    dg, dbeta = np.zeros((T, H)), np.zeros((T, H))
+    for t in range(T - 1, -1, -1):
+        p = prev[t]
+        for h in range(H):
+            Sp = S[p, h] if p >= 0 else np.zeros((d, d))
+            a, b = np.exp(g[t, h]), beta[t, h]
+            dSt = dS[t, h] + scale * np.outer(q[t, h], dO[t, h])
+            dq[t, h] = scale * S[t, h] @ dO[t, h]
+            w = Sp.T @ k[t, h]                      # the value stored under k before the write
+            res = v[t, h] - a * w
+            u = b * res
+            du = dSt.T @ k[t, h]
+            dk[t, h] += dSt @ u
+            dv[t, h] += b * du
+            dbeta[t, h] = du @ res
+            dr = b * du                             # gradient of res
+            dk[t, h] += -a * (Sp @ dr)
+            dg[t, h] = a * ((dSt * Sp).sum() - w @ dr)
+            if p >= 0:
+                dS[p, h] += a * dSt - a * np.outer(k[t, h], dr)
+
+    dy = np.zeros((T, C))
+    for b, dqk in enumerate((dq, dk)):
+        qn = (q, k)[b]
+        gr = (dqk - qn * (qn * dqk).sum(-1, keepdims=True)) / nrm[b]
+        dy[:, b * H * d:(b + 1) * H * d] = gr.reshape(T, H * d)
+    dy[:, 2 * H * d:] = dv.reshape(T, H * d)
+    dz = dy * sig * (1.0 + z * (1.0 - sig))
+    dx, dw = np.zeros((T, C)), np.zeros((C, WIDTH))
+    for t in range(T):
+        for i, j in _taps(prev, t):
+            dx[j] += conv_w[:, i] * dz[t]
+            dw[:, i] += x[j] * dz[t]
+    return dx, dw, dg, dbeta
+
+
+def gdn_row_grads(plan: Plan, r: int, x, conv_w, g, beta, dO, H: int, d: int, scale: float):
+    """Gradients of the layer core over row r of a packed plan (paths from parent pointers)."""
+    return gdn_grads(x, conv_w, g, beta, dO, path_prev(plan, r), H, d, scale)
+
+
+def gdn_sequence_grads(x, conv_w, g, beta, dO, H: int, d: int, scale: float):
+    """The same on one unpacked sequence (a plain chain)."""
+    return gdn_grads(x, conv_w, g, beta, dO, np.arange(len(x)) - 1, H, d, scale)

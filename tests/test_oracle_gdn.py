@@ -3,7 +3,9 @@ gated delta rule (beta = 0, exact associations under orthonormal keys, a
 single key reduces to an unrolled moving average, pure decay), the short
 convolution against a library convolution and its tap shifts, and the
 packed tree equal to the layer run on every unpacked sequence (state forks,
-zero roots, the convolution's hand-off across segments, join copies)."""
+zero roots, the convolution's hand-off across segments, join copies); its
+backward against central finite differences on a packed tree and against
+the summed gradients of the unpacked sequences."""
 import numpy as np
 import pytest
 from scipy.special import expit
@@ -146,3 +148,81 @@ def test_pads_are_their_own_roots():
     prev = OG.path_prev(plan, 0)
     assert np.all(prev[used:] == -1)
     assert np.all(prev[:used] < np.arange(used))
+
+
+def _fd_check(x, w, g, b, dO, prev, H, d, scale, rng, n=6):
+    grads = OG.gdn_grads(x, w, g, b, dO, prev, H, d, scale)
+
+    def loss(args):
+        y = OG.conv_path(args[0], args[1], prev)
+        q, k, v = OG.split_heads(y, H, d)
+        return (OG.delta_rule(q, k, v, args[2], args[3], prev, scale) * dO).sum()
+
+    base = [x, w, g, b]
+    eps = 1e-6
+    for a_i, grad in enumerate(grads):
+        for _ in range(n):
+            idx = tuple(int(rng.integers(0, s)) for s in base[a_i].shape)
+            plus = [t.copy() for t in base]
+            minus = [t.copy() for t in base]
+            plus[a_i][idx] += eps
+            minus[a_i][idx] -= eps
+            fd = (loss(plus) - loss(minus)) / (2 * eps)
+            assert abs(fd - grad[idx]) <= 1e-6 * (1 + abs(fd)), (a_i, idx, fd, grad[idx])
+
+
+def test_backward_matches_finite_differences_on_a_tree():
+    """Central differences in float64 on a packed row with forks and pads:
+    every input (x, the convolution weights, g, beta)."""
+    b = W.random_forest(5, n_roots=2, max_depth=2, max_children=3, len_lo=2, len_hi=8, row_len=64,
+                        min_shared=2, vocab=17)
+    plan = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared)
+    rng = np.random.default_rng(6)
+    H, d, T = 2, 3, plan.row_len
+    x = rng.standard_normal((T, 3 * H * d))
+    w = 0.5 * rng.standard_normal((3 * H * d, 4))
+    g = np.log(rng.uniform(0.6, 1.0, (T, H)))
+    beta = rng.uniform(0.1, 0.9, (T, H))
+    dO = rng.standard_normal((T, H, d))
+    _fd_check(x, w, g, beta, dO, OG.path_prev(plan, 0), H, d, 0.7, rng)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_backward_packed_equals_sum_over_unpacked(seed):
+    """With dO split evenly over the copies of a shared position, the packed
+    gradients equal the sum of the unpacked sequences' gradients: per input
+    token over its copies, and for the weights over all sequences (a
+    branch point's state gradient is the sum over its branches)."""
+    b = W.random_forest(seed, n_roots=2, max_depth=3, max_children=3, len_lo=2, len_hi=25, row_len=256,
+                        min_shared=3, vocab=29)
+    plan = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared)
+    rng = np.random.default_rng(seed)
+    H, d, scale = 2, 3, 0.5
+    R, T = plan.n_rows, plan.row_len
+    x = rng.standard_normal((R * T, 3 * H * d))
+    w = 0.5 * rng.standard_normal((3 * H * d, 4))
+    g = np.log(rng.uniform(0.7, 1.0, (R * T, H)))
+    beta = rng.uniform(0.1, 0.9, (R * T, H))
+    dO = rng.standard_normal((R * T, H, d))
+    mult = np.bincount(plan.gather_index, minlength=R * T).astype(np.float64)
+    dO_packed = np.where(mult[:, None, None] > 0, dO, 0.0)
+    want_x, want_g, want_b = np.zeros_like(x), np.zeros_like(g), np.zeros_like(beta)
+    want_w = np.zeros_like(w)
+    offs = np.concatenate([[0], np.cumsum([len(s) for s in b.seqs])])
+    for s in range(len(b.seqs)):
+        idx = plan.gather_index[offs[s]: offs[s + 1]]
+        gx, gw, gg, gb = OG.gdn_sequence_grads(x[idx], w, g[idx], beta[idx],
+                                                dO[idx] / mult[idx][:, None, None], H, d, scale)
+        np.add.at(want_x, idx, gx)
+        np.add.at(want_g, idx, gg)
+        np.add.at(want_b, idx, gb)
+        want_w += gw
+    got_w = np.zeros_like(w)
+    for r in range(R):
+        sl = slice(r * T, (r + 1) * T)
+        gx, gw, gg, gb = OG.gdn_row_grads(plan, r, x[sl], w, g[sl], beta[sl], dO_packed[sl], H, d, scale)
+        np.testing.assert_allclose(gx, want_x[sl], atol=1e-10)
+        np.testing.assert_allclose(gg, want_g[sl], atol=1e-10)
+        np.testing.assert_allclose(gb, want_b[sl], atol=1e-10)
+        got_w += gw
+    np.testing.assert_allclose(got_w, want_w, atol=1e-9)
