@@ -10,8 +10,10 @@
 //
 // Two kernels, both driven by the per-query-tile key-tile lists and the pair
 // numbering of stp_classify:
-//   index_scores_kernel  one CTA per (row, query tile): the tile's Q of every
-//                        indexer head once (TMA), its non-empty key tiles
+//   index_scores_kernel  one CTA per (row, query tile, piece of at most 8
+//                        entries of its key-tile list, so long ancestor lists
+//                        spread over the chip): the tile's Q of every
+//                        indexer head once (TMA), the piece's key tiles
 //                        through a two-stage ring; S_h = Q_h K^T on tcgen05
 //                        (four heads per pass in TMEM), and four epilogue
 //                        warps (thread = query = TMEM lane) accumulate
@@ -42,12 +44,13 @@ constexpr int kIdxSlots = 4;           // heads per TMEM pass (128 columns each)
 constexpr int kIdxQBytesMax = 131072;  // Q of all heads: H * D * 256 bytes
 constexpr int kIdxSmallBytes = 256;
 constexpr int kScoreTile = 128 * 128;  // floats per (pair) score tile
+constexpr int kIdxPiece = 8;           // key tiles of one query tile's list per scoring CTA
 constexpr int kSelThreads = 1024;  // 32 warps: 2 query groups x 16 key-tile ranges
 constexpr int kSelQ = 64;          // queries per selection CTA (half a query tile)
 constexpr int kSelSplit = 32 / (kSelQ / 32);
 
 struct IdxParams {
-  int R, T, NT, H, D, top_k;
+  int R, T, NT, H, D, top_k, splits;   // splits: scoring CTAs per query tile
   int64_t cap;
   const int32_t* se;
   const int32_t* csr_cnt;
@@ -108,9 +111,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = p.NT - 1 - (int)(blockIdx.x / p.R);   // longest lists first
-  const int r = (int)(blockIdx.x % p.R);
+  // CTA = (query tile, piece of at most kIdxPiece entries of its key-tile list)
+  const int piece = (int)(blockIdx.x % p.splits), rest = (int)(blockIdx.x / p.splits);
+  const int qt = p.NT - 1 - rest / p.R;   // longest lists first
+  const int r = rest % p.R;
   const int cnt = p.csr_cnt[(size_t)r * p.NT + qt];
+  const int e0 = piece * kIdxPiece, e1 = cnt < e0 + kIdxPiece ? cnt : e0 + kIdxPiece;
+  if (piece > 0 && e0 >= cnt) return;   // uniform over the CTA; piece 0 always checks the list
   const int32_t* list = p.csr + ((size_t)r * p.NT + qt) * p.NT;
   const int64_t pbase = (int64_t)p.row_base[r] + p.csr_off[(size_t)r * p.NT + qt];
   const int row0 = r * p.T;
@@ -145,8 +152,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         for (int db = 0; db < p.D / 64; ++db)
           tma_load_3d(big + h * tile_bytes + db * 16384, &tq, &bars[X_Q], db * 64, h, row0 + qt * 128);
       int issued[2] = {-1, -1};
-      for (int e = 0; e < cnt; ++e) {
-        const int st = e & 1, n = e >> 1, kt = list[e] >> 1;
+      for (int e = e0; e < e1; ++e) {
+        const int st = (e - e0) & 1, n = (e - e0) >> 1, kt = list[e] >> 1;
         if (kt < 0 || kt > qt) {
           *abort_flag = 1;
           atomicOr(p.err, kErrBadList);
@@ -172,9 +179,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       const int nk = p.D / 16;
       bool ok = mbar_wait(&bars[X_Q], 0, abort_flag, p.err);
       int u = 0;  // head passes issued so far
-      for (int e = 0; ok && e < cnt; ++e) {
-        const int st = e & 1;
-        if (!mbar_wait(&bars[X_KF + st], (e >> 1) & 1, abort_flag, p.err)) break;
+      for (int e = e0; ok && e < e1; ++e) {
+        const int st = (e - e0) & 1;
+        if (!mbar_wait(&bars[X_KF + st], ((e - e0) >> 1) & 1, abort_flag, p.err)) break;
         const uint32_t k_km = desc_lo_kmajor(big_s + q_bytes + st * tile_bytes);
         for (int hg = 0; ok && hg < n_groups; ++hg, ++u) {
           if (u > 0 && !mbar_wait(&bars[X_SFREE], (u - 1) & 1, abort_flag, p.err)) {
@@ -202,7 +209,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     const float* wrow = p.w + ((size_t)row0 + i) * p.H;
     bool ok = run;
     int u = 0;
-    for (int e = 0; ok && e < cnt; ++e) {
+    for (int e = e0; ok && e < e1; ++e) {
       const int ent = list[e], kt = ent >> 1, part = ent & 1;
       float acc[128];
 #pragma unroll
@@ -477,7 +484,8 @@ extern "C" stp_status stp_index_topk(const stp_index_desc* desc, const void* q, 
   }
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_index_topk: %s", cudaGetErrorString(e));
   const unsigned grid = (unsigned)(NT * desc->n_rows);
-  index_scores_kernel<<<grid, kIdxThreads, smem, s>>>(mq, mk, p);
+  p.splits = (NT + kIdxPiece - 1) / kIdxPiece;
+  index_scores_kernel<<<grid * p.splits, kIdxThreads, smem, s>>>(mq, mk, p);
   index_select_kernel<<<grid * (128 / kSelQ), kSelThreads, smem_sel, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_index_topk: %s", cudaGetErrorString(e));
