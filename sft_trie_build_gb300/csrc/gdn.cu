@@ -58,6 +58,8 @@ constexpr int kPrepLa = 68;
 constexpr int kPoV = 32768, kPoA = kPoV + 16384, kPoGam = kPoA + kGc * kPrepLa * 4, kPoBeta = kPoGam + 256,
               kPoEg = kPoBeta + 256, kPoEk = kPoEg + 256, kPoBar = kPoEk + 256;
 constexpr int kPrepSmem = kPoBar + 64 + 1024;
+constexpr int kStgLd = 257;   // output staging rows, after the solve: [64][257] float32 over the areas above
+static_assert(kGc * kStgLd * 4 <= kPoGam, "output staging must fit below the row scalars");
 
 // gdn_state_kernel shared memory, from a 1024-byte aligned base.  A stage holds
 // [Q~; W] (32 KB), K~ (16 KB) and P (8 KB); P is the top half of a 128-row MMA
@@ -359,13 +361,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnPara
   fence_after_sync();
   if (warp == 0) tmem_dealloc(tmem, 64);
 
+  // Q~ (rows 0..63 of the Q~|W tile) and K~
+  for (int i = tid; i < kGc * kGd / 2; i += kPrepThreads) {
+    const int t = i / (kGd / 2), c = 2 * (i % (kGd / 2));
+    const float eq = t < L ? p.scale * seg[t] : 0.f, ek = t < L ? sek[t] : 0.f;
+    reinterpret_cast<uint32_t*>(p.wq + (row * 128 + t) * kGd + c)[0] =
+        pack_bf16x2(eq * qk_at(tile, t, c), eq * qk_at(tile, t, c + 1));
+    reinterpret_cast<uint32_t*>(p.kt + (row * kGc + t) * kGd + c)[0] =
+        pack_bf16x2(ek * qk_at(tile, kGc + t, c), ek * qk_at(tile, kGc + t, c + 1));
+  }
+
   // (I + A) X = B by forward substitution, one column per thread:
   // columns 0-127 give U^ (B = beta V), 128-255 give W (B = beta e^gam K).
   // A is strictly lower with zeros above, so row t can be read 4 wide up to
   // the multiple of 4 past t - 1 (those X are still 0).
+  float X[kGc];
   {
     const int col = tid;
-    float X[kGc];
 #pragma unroll
     for (int t = 0; t < kGc; ++t) X[t] = 0.f;
 #pragma unroll
@@ -382,24 +394,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnPara
       }
       X[t] = b;
     }
-    if (col < kGd) {
-      float4* u4 = reinterpret_cast<float4*>(p.ut + (row * kGd + col) * kGc);
-#pragma unroll
-      for (int t = 0; t < kGc; t += 4) u4[t / 4] = make_float4(X[t], X[t + 1], X[t + 2], X[t + 3]);
-    } else {
-      __nv_bfloat16* w = p.wq + (row * 128 + kGc) * kGd + (col - kGd);
-#pragma unroll
-      for (int t = 0; t < kGc; ++t) w[(size_t)t * kGd] = __float2bfloat16_rn(X[t]);
-    }
   }
-  // Q~ (rows 0..63 of the Q~|W tile) and K~
+  // The columns go out through shared memory (the operand, V and A areas are
+  // free now), rows padded to 257 floats, so that the global stores are
+  // contiguous: U^ transposed ([column][t]) and W (rows 64..127 of the tile).
+  __syncthreads();
+  float* stg = reinterpret_cast<float*>(sm);   // [64][257]
+#pragma unroll
+  for (int t = 0; t < kGc; ++t) stg[t * kStgLd + tid] = X[t];
+  __syncthreads();
+  for (int i = tid; i < kGd * kGc / 4; i += kPrepThreads) {
+    const int col = i / (kGc / 4), t = 4 * (i % (kGc / 4));
+    reinterpret_cast<float4*>(p.ut + (row * kGd + col) * kGc)[t / 4] =
+        make_float4(stg[t * kStgLd + col], stg[(t + 1) * kStgLd + col], stg[(t + 2) * kStgLd + col],
+                    stg[(t + 3) * kStgLd + col]);
+  }
   for (int i = tid; i < kGc * kGd / 2; i += kPrepThreads) {
     const int t = i / (kGd / 2), c = 2 * (i % (kGd / 2));
-    const float eq = t < L ? p.scale * seg[t] : 0.f, ek = t < L ? sek[t] : 0.f;
-    reinterpret_cast<uint32_t*>(p.wq + (row * 128 + t) * kGd + c)[0] =
-        pack_bf16x2(eq * qk_at(tile, t, c), eq * qk_at(tile, t, c + 1));
-    reinterpret_cast<uint32_t*>(p.kt + (row * kGc + t) * kGd + c)[0] =
-        pack_bf16x2(ek * qk_at(tile, kGc + t, c), ek * qk_at(tile, kGc + t, c + 1));
+    reinterpret_cast<uint32_t*>(p.wq + (row * 128 + kGc + t) * kGd + c)[0] =
+        pack_bf16x2(stg[t * kStgLd + kGd + c], stg[t * kStgLd + kGd + c + 1]);
   }
   if (tid == 0) p.decay[row] = expf(sgam[L - 1]);
 }
