@@ -28,7 +28,7 @@ Sources (prefix-tree-packing page, furtherai.github.io):
   * attention section -- a DFS assigns increasing indices and every token
     has an [enter, exit] interval; ``subtree_end`` is the exit index.
 
-Readings where the pages are silent (each repeated in the design doc):
+Readings where the pages are silent:
   * the minimum length is tested on the agreed run, before the join copy is
     carved out of it;
   * a run shorter than the minimum is not emitted but pushed down into every
