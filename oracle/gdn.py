@@ -141,25 +141,10 @@ def _taps(prev: np.ndarray, t: int):
     return out
 
 
-def gdn_grads(x, conv_w, g, beta, dO, prev, H: int, d: int, scale: float):
-    """(dx [T, C], dconv_w [C, 4], dg [T, H], dbeta [T, H]) of the layer core
-    over one row or sequence whose path predecessors are prev (prev[t] < t)."""
-    x = np.asarray(x, np.float64)
-    conv_w = np.asarray(conv_w, np.float64)
-    g = np.asarray(g, np.float64)
-    beta = np.asarray(beta, np.float64)
-    dO = np.asarray(dO, np.float64)
-    T, C = x.shape
-    z = np.zeros((T, C))
-    for t in range(T):
-        for i, j in _taps(prev, t):
-            z[t] += conv_w[:, i] * x[j]
-    sig = 1.0 / (1.0 + np.exp(-z))
-    y = z * sig
-    raw = [y[:, b * H * d:(b + 1) * H * d].reshape(T, H, d) for b in range(3)]
-    nrm = [np.sqrt((raw[b] ** 2).sum(-1, keepdims=True) + EPS) for b in range(2)]
-    q, k, v = raw[0] / nrm[0], raw[1] / nrm[1], raw[2]
-
+def delta_rule_grads(q, k, v, g, beta, dO, prev, scale):
+    """(dq, dk, dv, dg, dbeta) [T, H, ...] of L = sum dO . o for the gated delta
+    rule alone (q, k, v given), each token continuing the state of prev[t]."""
+    T, H, d = q.shape
     S = np.zeros((T, H, d, d))
     for t in range(T):
         p = prev[t]
@@ -190,6 +175,28 @@ def gdn_grads(x, conv_w, g, beta, dO, prev, H: int, d: int, scale: float):
             dg[t, h] = a * ((dSt * Sp).sum() - w @ dr)
             if p >= 0:
                 dS[p, h] += a * dSt - a * np.outer(k[t, h], dr)
+    return dq, dk, dv, dg, dbeta
+
+
+def gdn_grads(x, conv_w, g, beta, dO, prev, H: int, d: int, scale: float):
+    """(dx [T, C], dconv_w [C, 4], dg [T, H], dbeta [T, H]) of the layer core
+    over one row or sequence whose path predecessors are prev (prev[t] < t)."""
+    x = np.asarray(x, np.float64)
+    conv_w = np.asarray(conv_w, np.float64)
+    g = np.asarray(g, np.float64)
+    beta = np.asarray(beta, np.float64)
+    dO = np.asarray(dO, np.float64)
+    T, C = x.shape
+    z = np.zeros((T, C))
+    for t in range(T):
+        for i, j in _taps(prev, t):
+            z[t] += conv_w[:, i] * x[j]
+    sig = 1.0 / (1.0 + np.exp(-z))
+    y = z * sig
+    raw = [y[:, b * H * d:(b + 1) * H * d].reshape(T, H, d) for b in range(3)]
+    nrm = [np.sqrt((raw[b] ** 2).sum(-1, keepdims=True) + EPS) for b in range(2)]
+    q, k, v = raw[0] / nrm[0], raw[1] / nrm[1], raw[2]
+    dq, dk, dv, dg, dbeta = delta_rule_grads(q, k, v, g, beta, dO, prev, scale)
 
     dy = np.zeros((T, C))
     for b, dqk in enumerate((dq, dk)):
