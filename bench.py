@@ -129,9 +129,10 @@ def _logprob(tok, mask, dev, peak, hidden=4096, vocab=151936, reps=10) -> dict:
 
 
 def _gdn(meta, dev, heads=16, reps=10) -> dict:
-    """Tree-aware Gated DeltaNet layer core (forward) over the packed row:
-    path convolution, per-chunk prep and one state pass per tree depth
-    (stp_gdn_fwd), 16 heads of 128."""
+    """Tree-aware Gated DeltaNet layer core over the packed row, 16 heads of
+    128: the forward (path convolution, per-chunk prep, one state pass per
+    tree depth; stp_gdn_fwd), then the training forward (stp_gdn_fwd_train)
+    and the backward (stp_gdn_bwd)."""
     import torch
     from sft_trie_build_gb300 import stp
 
@@ -161,10 +162,35 @@ def _gdn(meta, dev, heads=16, reps=10) -> dict:
     torch.cuda.synchronize()
     ms = a.elapsed_time(e) / reps
     real = int(used.sum())
-    return {"heads": heads, "head_dim": 128, "tokens": real, "segments": int(plan[stp.GP_NSEG]),
-            "chunks": int(plan[stp.GP_NCHUNK]), "depths": int(plan[stp.GP_NDEPTH]), "ms": ms,
-            "tokens_per_s": real / (ms / 1e3), "host_plan_ms": plan_ms,
-            "launches_per_call": 2 + int(plan[stp.GP_NDEPTH])}
+    out = {"heads": heads, "head_dim": 128, "tokens": real, "segments": int(plan[stp.GP_NSEG]),
+           "chunks": int(plan[stp.GP_NCHUNK]), "depths": int(plan[stp.GP_NDEPTH]), "ms": ms,
+           "tokens_per_s": real / (ms / 1e3), "host_plan_ms": plan_ms,
+           "launches_per_call": 2 + int(plan[stp.GP_NDEPTH])}
+    # training: the forward that keeps the chunk states, then the backward (float32 first version)
+    try:
+        tws = torch.empty(stp.stp_gdn_train_workspace_size(desc, plan), dtype=torch.uint8, device=dev)
+        d_o = torch.randn(R * T, heads, 128, device=dev)
+        dx = torch.empty(R * T, 3 * heads * 128, device=dev)
+        dw = torch.empty(3 * heads * 128, 4, device=dev)
+        dg = torch.empty(R * T, heads, device=dev)
+        db = torch.empty(R * T, heads, device=dev)
+        legs = {"fwd_train": lambda: stp.stp_gdn_fwd_train(desc, plan, d_plan, x, cw, g, beta, o, tws),
+                "bwd": lambda: stp.stp_gdn_bwd(desc, plan, d_plan, x, cw, g, beta, d_o, dx, dw, dg, db, tws)}
+        for _ in range(2):
+            legs["fwd_train"]()
+            legs["bwd"]()
+        torch.cuda.synchronize()
+        for name, fn in legs.items():
+            a.record()
+            for _ in range(3):
+                fn()
+            e.record()
+            torch.cuda.synchronize()
+            out[name + "_ms"] = a.elapsed_time(e) / 3
+        out["train_status"] = stp.stp_device_status(tws)
+    except Exception as exc:   # an auxiliary field: report, do not lose the bench line
+        out["train_error"] = repr(exc)
+    return out
 
 
 def _what_if(n_candidates: int = 64, groups_per_candidate: int = 8) -> dict:

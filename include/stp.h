@@ -466,6 +466,32 @@ stp_status stp_gdn_fwd(const stp_gdn_desc* desc, const void* plan, const void* d
                        void* stream);
 
 /*
+ * Training: the same forward, keeping every chunk's starting state in the
+ * workspace (stp_gdn_train_workspace_size bytes) for stp_gdn_bwd.
+ */
+stp_status stp_gdn_train_workspace_size(const stp_gdn_desc* desc, const void* plan, size_t* ws_bytes);
+stp_status stp_gdn_fwd_train(const stp_gdn_desc* desc, const void* plan, const void* d_plan, const void* x,
+                             const float* conv_w, const float* g, const float* beta, float* o, void* d_ws,
+                             void* stream);
+
+/*
+ * Backward of the layer core for L = sum d_o . o ([P1] GDN section: a child
+ * segment starts from its parent's final state, so the parent's final-state
+ * gradient is the sum over its children).  Call after stp_gdn_fwd_train
+ * with the same plan, inputs and workspace, on the same stream.
+ *   d_o       device float32 [R * T, H, d], 16-byte aligned
+ *   dx        device float32 [R * T, 3 H d], written in full (pads 0)
+ *   dconv_w   device float32 [3 H d, 4], written in full
+ *   dg, dbeta device float32 [R * T, H], written in full (pads 0)
+ * Float32 on the CUDA cores, from the forward's bf16 chunk operands; the
+ * convolution's input gradient is summed with float atomics (the last bits
+ * may differ from call to call).  Errors as for stp_gdn_fwd.
+ */
+stp_status stp_gdn_bwd(const stp_gdn_desc* desc, const void* plan, const void* d_plan, const void* x,
+                       const float* conv_w, const float* g, const float* beta, const float* d_o, float* dx,
+                       float* dconv_w, float* dg, float* dbeta, void* d_ws, void* stream);
+
+/*
  * Read the device error word of a workspace (fwd_ws or bwd_ws): synchronizes
  * the stream, then *out = STP_OK or STP_EDEVICE (a device check tripped or a
  * bounded wait ran out; the kernel returned early and its outputs are invalid).

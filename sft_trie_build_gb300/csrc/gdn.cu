@@ -35,6 +35,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "gdn_common.h"
 #include "internal.h"
 #include "layout.h"
 #include "tc_ptx.cuh"
@@ -97,6 +98,7 @@ struct GdnParams {
   float* ut;                // [n_chunk H, 128, 64]
   float* decay;             // [n_chunk H]
   float* state;             // [n_seg H, 128, 128]
+  float* s0;                // [n_chunk H, 128, 128] each chunk's starting state, or null (inference)
   float* o;                 // [N, H, 128]
   uint32_t* err;
 };
@@ -558,6 +560,13 @@ __global__ void __launch_bounds__(kStThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lrow + cc * 32, v + 32 * cc);
       tmem_ld_wait();
+      if (p.s0) {   // training: keep the chunk's starting state (row r) for the backward
+        float4* d4 = reinterpret_cast<float4*>(p.s0 + ((size_t)((c0 + i) * p.H + h) * kGd + r) * kGd);
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                              __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+      }
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint8_t* half = sm + kOffSop + (cc >> 1) * 16384 + r * 128;
@@ -671,75 +680,33 @@ __global__ void __launch_bounds__(kStThreads, 1)
   if (warp == 5) tmem_dealloc(tmem, 512);
 }
 
-struct GdnLayout {
-  size_t y, wq, kt, pm, ut, decay, state, total;
-};
-
-GdnLayout gdn_layout(int64_t N, int H, int64_t n_chunk, int64_t n_seg) {
-  GdnLayout L;
-  size_t o = 256;   // the error word
-  const int64_t C = 3LL * H * kGd, rows = n_chunk * H;
-  L.y = o;
-  o += align256((size_t)N * C * 2);
-  L.wq = o;
-  o += align256((size_t)rows * 128 * kGd * 2);
-  L.kt = o;
-  o += align256((size_t)rows * kGc * kGd * 2);
-  L.pm = o;
-  o += align256((size_t)rows * kGc * kGc * 2);
-  L.ut = o;
-  o += align256((size_t)rows * kGd * kGc * 4);
-  L.decay = o;
-  o += align256((size_t)rows * 4);
-  L.state = o;
-  o += align256((size_t)n_seg * H * kGd * kGd * 4);
-  L.total = o;
-  return L;
-}
-
-stp_status check_gdn_desc(const stp_gdn_desc* d) {
-  if (!d) return fail(STP_EINVAL, "GDN descriptor is NULL");
-  if (d->n_rows < 0 || d->row_len <= 0 || (int64_t)d->n_rows * d->row_len > (1 << 26))
-    return fail(STP_EINVAL, "need n_rows >= 0, row_len > 0 and at most 2^26 tokens");
-  if (d->head_dim != kGd) return fail(STP_EUNSUPPORTED, "head_dim must be 128 (got %d)", d->head_dim);
-  if (d->n_heads < 1 || d->n_heads > 64) return fail(STP_EUNSUPPORTED, "n_heads must lie in [1, 64]");
-  if (!std::isfinite(d->scale)) return fail(STP_EINVAL, "scale is not finite");
-  return STP_OK;
-}
-
-stp_status check_plan(const stp_gdn_desc* d, const int32_t* w) {
-  if (!w) return fail(STP_EINVAL, "GDN plan is NULL");
-  if (w[GP_MAGIC] != kGdnMagic) return fail(STP_EINVAL, "not a GDN plan (bad magic word)");
-  if ((int64_t)w[GP_N] != (int64_t)d->n_rows * d->row_len)
-    return fail(STP_EINVAL, "the plan covers %d tokens, the descriptor %lld", w[GP_N],
-                (long long)d->n_rows * d->row_len);
-  return STP_OK;
-}
-
 }  // namespace
 }  // namespace stp
 
 using namespace stp;
 
-extern "C" stp_status stp_gdn_workspace_size(const stp_gdn_desc* desc, const void* plan, size_t* ws_bytes) {
+namespace {
+
+stp_status ws_size(const stp_gdn_desc* desc, const void* plan, size_t* ws_bytes, bool train) {
   clear_error();
   stp_status st = check_gdn_desc(desc);
   if (st) return st;
   const int32_t* w = static_cast<const int32_t*>(plan);
-  if ((st = check_plan(desc, w))) return st;
+  if ((st = check_gdn_plan(desc, w))) return st;
   if (!ws_bytes) return fail(STP_EINVAL, "stp_gdn_workspace_size: NULL output");
-  *ws_bytes = gdn_layout(w[GP_N], desc->n_heads, w[GP_NCHUNK], w[GP_NSEG]).total;
+  const GdnLayout L = gdn_layout(w[GP_N], desc->n_heads, w[GP_NCHUNK], w[GP_NSEG]);
+  *ws_bytes = train ? L.train_total : L.total;
   return STP_OK;
 }
 
-extern "C" stp_status stp_gdn_fwd(const stp_gdn_desc* desc, const void* plan, const void* d_plan, const void* x,
-                                  const float* conv_w, const float* g, const float* beta, float* o, void* d_ws,
-                                  void* stream) {
+stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d_plan, const void* x,
+                       const float* conv_w, const float* g, const float* beta, float* o, void* d_ws, void* stream,
+                       bool train) {
   clear_error();
   stp_status st = check_gdn_desc(desc);
   if (st) return st;
   const int32_t* w = static_cast<const int32_t*>(plan);
-  if ((st = check_plan(desc, w))) return st;
+  if ((st = check_gdn_plan(desc, w))) return st;
   if (!d_plan || !x || !conv_w || !g || !beta || !o || !d_ws)
     return fail(STP_EINVAL, "stp_gdn_fwd: NULL device pointer");
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(conv_w) | reinterpret_cast<uintptr_t>(o)) & 15 ||
@@ -776,6 +743,7 @@ extern "C" stp_status stp_gdn_fwd(const stp_gdn_desc* desc, const void* plan, co
   p.ut = reinterpret_cast<float*>(ws + L.ut);
   p.decay = reinterpret_cast<float*>(ws + L.decay);
   p.state = reinterpret_cast<float*>(ws + L.state);
+  p.s0 = train ? reinterpret_cast<float*>(ws + L.s0) : nullptr;
   p.o = o;
   CUtensorMap mwq, mkt, mpm;
   if (n_chunk > 0 &&
@@ -806,4 +774,26 @@ extern "C" stp_status stp_gdn_fwd(const stp_gdn_desc* desc, const void* plan, co
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e));
   return STP_OK;
+}
+
+}  // namespace
+
+extern "C" stp_status stp_gdn_workspace_size(const stp_gdn_desc* desc, const void* plan, size_t* ws_bytes) {
+  return ws_size(desc, plan, ws_bytes, false);
+}
+
+extern "C" stp_status stp_gdn_train_workspace_size(const stp_gdn_desc* desc, const void* plan, size_t* ws_bytes) {
+  return ws_size(desc, plan, ws_bytes, true);
+}
+
+extern "C" stp_status stp_gdn_fwd(const stp_gdn_desc* desc, const void* plan, const void* d_plan, const void* x,
+                                  const float* conv_w, const float* g, const float* beta, float* o, void* d_ws,
+                                  void* stream) {
+  return gdn_forward(desc, plan, d_plan, x, conv_w, g, beta, o, d_ws, stream, false);
+}
+
+extern "C" stp_status stp_gdn_fwd_train(const stp_gdn_desc* desc, const void* plan, const void* d_plan,
+                                        const void* x, const float* conv_w, const float* g, const float* beta,
+                                        float* o, void* d_ws, void* stream) {
+  return gdn_forward(desc, plan, d_plan, x, conv_w, g, beta, o, d_ws, stream, true);
 }

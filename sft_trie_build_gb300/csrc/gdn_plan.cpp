@@ -36,8 +36,9 @@ extern "C" stp_status stp_gdn_plan_bound(const stp_gdn_desc* desc, size_t* plan_
   if (st) return st;
   if (!plan_bytes) return fail(STP_EINVAL, "stp_gdn_plan_bound: NULL output");
   const size_t N = (size_t)desc->n_rows * desc->row_len;
-  // prev (1, 2 and 3 back), 4 words per segment, depth offsets, 2 words per chunk (segments, chunks <= N)
-  *plan_bytes = 4 * (kGdnHeader + 3 * N + 4 * N + (N + 1) + 2 * N);
+  // prev (1, 2 and 3 back), 4 words per segment, depth offsets, 2 words per chunk, the child lists
+  // (segments, chunks <= N)
+  *plan_bytes = 4 * (kGdnHeader + 3 * N + 4 * N + (N + 1) + 2 * N + (N + 1) + N);
   return STP_OK;
 }
 
@@ -132,6 +133,8 @@ extern "C" stp_status stp_gdn_plan(const stp_gdn_desc* desc, const int32_t* subt
   take(GP_DEPTH_OFF, n_depth + 1);
   take(GP_CHUNK_START, n_chunk);
   take(GP_CHUNK_LEN, n_chunk);
+  take(GP_CHILD_OFF, n_seg + 1);
+  take(GP_CHILD, n_seg);
   w[GP_MAGIC] = kGdnMagic;
   w[GP_N] = (int32_t)N;
   w[GP_NSEG] = n_seg;
@@ -158,5 +161,21 @@ extern "C" stp_status stp_gdn_plan(const stp_gdn_desc* desc, const int32_t* subt
     }
   }
   for (int d = 0; d <= n_depth; ++d) w[w[GP_DEPTH_OFF] + d] = depth_off[d];
+  // children of each (sorted) segment, as a CSR list in the sorted numbering
+  {
+    int32_t* off = w + w[GP_CHILD_OFF];
+    int32_t* ch = w + w[GP_CHILD];
+    for (int32_t i = 0; i <= n_seg; ++i) off[i] = 0;
+    for (int32_t i = 0; i < n_seg; ++i) {
+      const int32_t par = w[w[GP_SEG_PARENT] + i];
+      if (par >= 0) ++off[par + 1];
+    }
+    for (int32_t i = 0; i < n_seg; ++i) off[i + 1] += off[i];
+    std::vector<int32_t> fill(off, off + n_seg);
+    for (int32_t i = 0; i < n_seg; ++i) {
+      const int32_t par = w[w[GP_SEG_PARENT] + i];
+      if (par >= 0) ch[fill[par]++] = i;
+    }
+  }
   return STP_OK;
 }

@@ -30,6 +30,7 @@ EXPORTED = ["stp_pack", "stp_plan_info", "stp_plan_write", "stp_plan_rows_of", "
             "stp_index_workspace_size", "stp_index_topk",
             "stp_logprob_workspace_size", "stp_logprob_gather",
             "stp_gdn_plan_bound", "stp_gdn_plan", "stp_gdn_workspace_size", "stp_gdn_fwd",
+            "stp_gdn_train_workspace_size", "stp_gdn_fwd_train", "stp_gdn_bwd",
             "stp_device_status", "stp_last_error", "stp_version"]
 
 
@@ -138,6 +139,12 @@ def lib():
         L.stp_gdn_workspace_size.restype = st
         L.stp_gdn_fwd.argtypes = [ctypes.POINTER(GdnDesc)] + [_P] * 9
         L.stp_gdn_fwd.restype = st
+        L.stp_gdn_train_workspace_size.argtypes = [ctypes.POINTER(GdnDesc), _P, _SZ]
+        L.stp_gdn_train_workspace_size.restype = st
+        L.stp_gdn_fwd_train.argtypes = [ctypes.POINTER(GdnDesc)] + [_P] * 9
+        L.stp_gdn_fwd_train.restype = st
+        L.stp_gdn_bwd.argtypes = [ctypes.POINTER(GdnDesc)] + [_P] * 13
+        L.stp_gdn_bwd.restype = st
         L.stp_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
         L.stp_device_status.restype = st
         L.stp_last_error.argtypes = []
@@ -412,7 +419,8 @@ def stp_logprob_gather(desc: LogprobDesc, hidden, w_vocab, token_ids, loss_mask,
 
 # plan header fields (int32 words), as the library writes them
 GP_MAGIC, GP_N, GP_NSEG, GP_NCHUNK, GP_NDEPTH, GP_WORDS, GP_PREV, GP_SEG_START, GP_SEG_LEN, GP_SEG_PARENT, \
-    GP_SEG_CHUNK0, GP_DEPTH_OFF, GP_CHUNK_START, GP_CHUNK_LEN, GP_MAX_DEPTH_SEGS, GP_PREV2, GP_PREV3 = range(17)
+    GP_SEG_CHUNK0, GP_DEPTH_OFF, GP_CHUNK_START, GP_CHUNK_LEN, GP_MAX_DEPTH_SEGS, GP_PREV2, GP_PREV3, \
+    GP_CHILD_OFF, GP_CHILD = range(19)
 
 
 def gdn_desc(n_rows, row_len, n_heads, head_dim=128, scale=None) -> GdnDesc:
@@ -444,7 +452,8 @@ def gdn_plan_arrays(plan: np.ndarray) -> dict:
     return {"prev": at(GP_PREV, n), "prev2": at(GP_PREV2, n), "prev3": at(GP_PREV3, n), "seg_start": at(GP_SEG_START, ns), "seg_len": at(GP_SEG_LEN, ns),
             "seg_parent": at(GP_SEG_PARENT, ns), "seg_chunk0": at(GP_SEG_CHUNK0, ns),
             "depth_off": at(GP_DEPTH_OFF, nd + 1), "chunk_start": at(GP_CHUNK_START, nc),
-            "chunk_len": at(GP_CHUNK_LEN, nc)}
+            "chunk_len": at(GP_CHUNK_LEN, nc), "child_off": at(GP_CHILD_OFF, ns + 1),
+            "child": at(GP_CHILD, w[w[GP_CHILD_OFF] + ns] if ns > 0 else 0)}
 
 
 def stp_gdn_workspace_size(desc: GdnDesc, plan: np.ndarray) -> int:
@@ -458,6 +467,26 @@ def stp_gdn_fwd(desc: GdnDesc, plan: np.ndarray, d_plan, x, conv_w, g, beta, o, 
     _check(lib().stp_gdn_fwd(ctypes.byref(desc), plan.ctypes.data_as(_P), _dptr(d_plan), _dptr(x),
                              _dptr(conv_w), _dptr(g), _dptr(beta), _dptr(o), _dptr(ws), _stream(stream)),
            "stp_gdn_fwd")
+
+
+def stp_gdn_train_workspace_size(desc: GdnDesc, plan: np.ndarray) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().stp_gdn_train_workspace_size(ctypes.byref(desc), plan.ctypes.data_as(_P), ctypes.byref(out)),
+           "stp_gdn_train_workspace_size")
+    return out.value
+
+
+def stp_gdn_fwd_train(desc: GdnDesc, plan: np.ndarray, d_plan, x, conv_w, g, beta, o, ws, stream=None):
+    _check(lib().stp_gdn_fwd_train(ctypes.byref(desc), plan.ctypes.data_as(_P), _dptr(d_plan), _dptr(x),
+                                   _dptr(conv_w), _dptr(g), _dptr(beta), _dptr(o), _dptr(ws), _stream(stream)),
+           "stp_gdn_fwd_train")
+
+
+def stp_gdn_bwd(desc: GdnDesc, plan: np.ndarray, d_plan, x, conv_w, g, beta, d_o, dx, dconv_w, dg, dbeta, ws,
+                stream=None):
+    _check(lib().stp_gdn_bwd(ctypes.byref(desc), plan.ctypes.data_as(_P), _dptr(d_plan), _dptr(x), _dptr(conv_w),
+                             _dptr(g), _dptr(beta), _dptr(d_o), _dptr(dx), _dptr(dconv_w), _dptr(dg), _dptr(dbeta),
+                             _dptr(ws), _stream(stream)), "stp_gdn_bwd")
 
 
 def stp_device_status(ws, stream=None) -> int:

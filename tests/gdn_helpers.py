@@ -51,3 +51,50 @@ def oracle_sequence_heads(plan_o, seq_index, offsets, heads, inputs, scale):
         outs.append(OG.delta_rule(q[:, h:h + 1], k[:, h:h + 1], v[:, h:h + 1], g.numpy()[idx][:, h:h + 1],
                                   beta.numpy()[idx][:, h:h + 1], prev, scale)[:, 0])
     return np.stack(outs, 1), idx
+
+
+def run_gdn_train(plan_o, H, seed=0):
+    """Training forward + backward for L = sum dO . o, dO ~ N(0, 1) on real
+    tokens and 0 on pads; returns (o, dx, dconv_w, dg, dbeta), the status,
+    the inputs and dO."""
+    R, T = plan_o.n_rows, plan_o.row_len
+    desc = stp.gdn_desc(R, T, H)
+    used = np.asarray(plan_o.used, np.int32)
+    plan = stp.stp_gdn_plan(desc, plan_o.subtree_end, used)
+    d_plan = torch.from_numpy(plan).cuda()
+    x, cw, g, beta = W.gdn_tensors(R * T, H, 128, seed)
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(1000 + seed)
+    dO = torch.randn(R * T, H, 128, generator=gen)
+    real = torch.zeros(R * T, dtype=torch.bool)
+    for r in range(R):
+        real[r * T: r * T + int(used[r])] = True
+    dO[~real] = 0.0
+    ws = torch.empty(stp.stp_gdn_train_workspace_size(desc, plan), dtype=torch.uint8, device="cuda")
+    dev = [t.cuda() for t in (x, cw, g, beta)]
+    o = torch.empty(R * T, H, 128, device="cuda")
+    dx = torch.empty(R * T, 3 * H * 128, device="cuda")
+    dw = torch.empty(3 * H * 128, 4, device="cuda")
+    dg = torch.empty(R * T, H, device="cuda")
+    db = torch.empty(R * T, H, device="cuda")
+    stp.stp_gdn_fwd_train(desc, plan, d_plan, *dev, o, ws)
+    stp.stp_gdn_bwd(desc, plan, d_plan, *dev, dO.cuda(), dx, dw, dg, db, ws)
+    torch.cuda.synchronize()
+    outs = tuple(t.cpu().numpy() for t in (o, dx, dw, dg, db))
+    return outs, stp.stp_device_status(ws), (x, cw, g, beta), dO.numpy(), desc.scale
+
+
+def oracle_row_grads(plan_o, H, inputs, dO, scale):
+    """(dx, dconv_w, dg, dbeta) of the oracle over every row of the plan."""
+    x, cw, g, beta = inputs
+    T = plan_o.row_len
+    dxs, dgs, dbs, dw = [], [], [], 0.0
+    for r in range(plan_o.n_rows):
+        sl = slice(r * T, (r + 1) * T)
+        gx, gw, gg, gb = OG.gdn_row_grads(plan_o, r, x[sl].float().numpy(), cw.numpy(), g[sl].numpy(),
+                                          beta[sl].numpy(), dO[sl], H, 128, scale)
+        dxs.append(gx)
+        dgs.append(gg)
+        dbs.append(gb)
+        dw = dw + gw
+    return np.concatenate(dxs), dw, np.concatenate(dgs), np.concatenate(dbs)

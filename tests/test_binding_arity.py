@@ -50,5 +50,11 @@ def test_gdn_calls():
         stp.stp_gdn_workspace_size(bad, plan)
     with pytest.raises(stp.StpError):
         stp.stp_gdn_fwd(bad, plan, None, None, None, None, None, None, None, stream=0)
+    with pytest.raises(stp.StpError):
+        stp.stp_gdn_train_workspace_size(bad, plan)
+    with pytest.raises(stp.StpError):
+        stp.stp_gdn_fwd_train(bad, plan, None, None, None, None, None, None, None, stream=0)
+    with pytest.raises(stp.StpError):
+        stp.stp_gdn_bwd(bad, plan, *([None] * 11), stream=0)
     with pytest.raises(stp.StpError):   # a plan that is not one
         stp.stp_gdn_workspace_size(desc, np.zeros_like(plan))

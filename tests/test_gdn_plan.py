@@ -50,6 +50,12 @@ def _check(plan_o, H=2):
         n = (L + 63) // 64
         assert np.array_equal(a["chunk_start"][c0: c0 + n], s + 64 * np.arange(n))
         assert np.array_equal(a["chunk_len"][c0: c0 + n], np.minimum(64, L - 64 * np.arange(n)))
+    kids = [[] for _ in a["seg_start"]]
+    for i, par in enumerate(a["seg_parent"]):
+        if par >= 0:
+            kids[par].append(i)
+    for i, want_kids in enumerate(kids):
+        assert list(a["child"][a["child_off"][i]: a["child_off"][i + 1]]) == want_kids
     real = prev != -2
     assert np.all(covered[real] == 1) and np.all(covered[~real] == 0)
     assert a["seg_chunk0"][-1] + (a["seg_len"][-1] + 63) // 64 == len(a["chunk_start"])
