@@ -99,3 +99,25 @@ def test_rejections():
     with pytest.raises(stp.StpError):   # reaches the library (argument marshalling) and fails its checks
         stp.stp_gdn_fwd(stp.gdn_desc(1, 8, 1, head_dim=64), plan, None, None, None, None, None, None, None,
                         stream=0)
+
+
+def test_edge_shapes():
+    """No rows; rows of pads only; single-token rows; a row of one chain."""
+    desc0 = stp.gdn_desc(0, 128, 2)
+    plan0 = stp.stp_gdn_plan(desc0, np.zeros((0, 128), np.int32))
+    assert plan0[stp.GP_N] == 0 and plan0[stp.GP_NSEG] == 0 and plan0[stp.GP_NCHUNK] == 0
+    assert stp.stp_gdn_workspace_size(desc0, plan0) > 0
+    T = 8
+    se = np.tile(np.arange(T, dtype=np.int32), (3, 1))
+    desc = stp.gdn_desc(3, T, 1)
+    plan = stp.stp_gdn_plan(desc, se, np.array([0, 1, T], np.int32))   # all pads; one token; T isolated tokens
+    a = stp.gdn_plan_arrays(plan)
+    assert np.all(a["prev"][:T] == -2)
+    assert a["prev"][T] == -1 and np.all(a["prev"][T + 1: 2 * T] == -2)
+    assert np.all(a["prev"][2 * T:] == -1)          # subtree_end = own index: every token its own root
+    assert len(a["seg_start"]) == 1 + T and np.all(a["seg_len"] == 1)
+    chain = np.full((1, 200), 199, np.int32)         # one sequence: every token sees all before it
+    plan = stp.stp_gdn_plan(stp.gdn_desc(1, 200, 1), chain)
+    a = stp.gdn_plan_arrays(plan)
+    assert np.array_equal(a["prev"], np.arange(200) - 1)
+    assert list(a["seg_len"]) == [200] and list(a["chunk_len"]) == [64, 64, 64, 8]
