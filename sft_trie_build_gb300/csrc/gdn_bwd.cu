@@ -85,7 +85,7 @@ __device__ __forceinline__ void bgemm(int K, FA A, FB B, FS store) {
   for (int i = 0; i < RM; ++i)
 #pragma unroll
     for (int j = 0; j < RN; ++j) acc[i][j] = 0.f;
-#pragma unroll 2
+#pragma unroll 8   // loads of eight k steps in flight: the operands mostly come from L2
   for (int k = 0; k < K; ++k) {
     float a[RM], b[RN];
 #pragma unroll
