@@ -98,3 +98,20 @@ def oracle_row_grads(plan_o, H, inputs, dO, scale):
         dbs.append(gb)
         dw = dw + gw
     return np.concatenate(dxs), dw, np.concatenate(dgs), np.concatenate(dbs)
+
+
+def oracle_head_grads(plan_o, r, inputs, dO, scale, H, heads):
+    """Oracle gradients of row r for some heads only: heads never mix in the
+    layer core (the convolution is per channel), so head h is the layer with
+    H = 1 on its own q, k, v channels.  {h: (channels, dx, dconv_w, dg, dbeta)}."""
+    x, cw, g, beta = inputs
+    T = plan_o.row_len
+    sl = slice(r * T, (r + 1) * T)
+    out = {}
+    for h in heads:
+        ch = np.concatenate([np.arange(b * H * 128 + h * 128, b * H * 128 + (h + 1) * 128) for b in range(3)])
+        gx, gw, gg, gb = OG.gdn_row_grads(plan_o, r, x[sl][:, ch].float().numpy(), cw.numpy()[ch],
+                                          g[sl][:, [h]].numpy(), beta[sl][:, [h]].numpy(), dO[sl][:, [h]],
+                                          1, 128, scale)
+        out[h] = (ch, gx, gw, gg[:, 0], gb[:, 0])
+    return out

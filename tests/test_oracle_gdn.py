@@ -226,3 +226,40 @@ def test_backward_packed_equals_sum_over_unpacked(seed):
         np.testing.assert_allclose(gb, want_b[sl], atol=1e-10)
         got_w += gw
     np.testing.assert_allclose(got_w, want_w, atol=1e-9)
+
+
+def test_backward_per_head_slices_equal_the_full_layer():
+    """Heads never mix: the layer on one head's channels (H = 1) gives that
+    head's slice of the full layer's gradients (what the full-size GPU test
+    compares against)."""
+    import sys
+    import os
+    import torch
+    sys.path.insert(0, os.path.dirname(__file__))
+    from gdn_helpers import oracle_head_grads, oracle_row_grads
+
+    b = W.random_forest(4, n_roots=2, max_depth=2, max_children=3, len_lo=2, len_hi=12, row_len=64,
+                        min_shared=2, vocab=17)
+    plan = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared)
+    H, d = 3, 128
+    gen = torch.Generator().manual_seed(3)
+    N = plan.n_rows * plan.row_len
+    x = torch.randn(N, 3 * H * d, generator=gen).to(torch.bfloat16)
+    cw = torch.randn(3 * H * d, 4, generator=gen) * 0.5
+    g = torch.log(0.85 + 0.15 * torch.rand(N, H, generator=gen))
+    beta = torch.sigmoid(torch.randn(N, H, generator=gen))
+    dO = np.random.default_rng(3).standard_normal((N, H, d))
+    full = oracle_row_grads(plan, H, (x, cw, g, beta), dO, 0.1)
+    T = plan.row_len
+    assert plan.n_rows > 1
+    wsum = {0: 0.0, 2: 0.0}
+    for r in range(plan.n_rows):
+        sl = slice(r * T, (r + 1) * T)
+        for h, (ch, gx, gw, gg, gb) in oracle_head_grads(plan, r, (x, cw, g, beta), dO, 0.1, H, (0, 2)).items():
+            np.testing.assert_allclose(gx, full[0][sl][:, ch], atol=1e-12)
+            np.testing.assert_allclose(gg, full[2][sl, h], atol=1e-12)
+            np.testing.assert_allclose(gb, full[3][sl, h], atol=1e-12)
+            wsum[h] = wsum[h] + gw
+    for h in (0, 2):
+        ch = np.concatenate([np.arange(bb * H * 128 + h * 128, bb * H * 128 + (h + 1) * 128) for bb in range(3)])
+        np.testing.assert_allclose(wsum[h], full[1][ch], atol=1e-12)
