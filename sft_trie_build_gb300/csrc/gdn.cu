@@ -11,7 +11,8 @@
 //   O     = scale (diag(e^{gam}) Q S0 + (Q K^T o Gamma) V'),  Gamma_ts = e^{gam_t - gam_s}, s <= t
 //   S_L   = e^{gam_L} S0 + (diag(e^{gam_L - gam}) K)^T V'
 // (the WY form of the delta rule: substituting the recurrence into itself
-// chunk by chunk).  Three kernels:
+// chunk by chunk).  Three kernels (the training forward also writes each
+// chunk's starting state S0 for the backward in gdn_bwd.cu):
 //   gdn_conv_kernel   one block per (64 tokens, q / k / v head): width-4 causal
 //                     convolution along each token's path (prev pointers of
 //                     the plan), SiLU, unit q and k heads; pads get o = 0.
@@ -19,12 +20,12 @@
 //                     core, then in float32 on the CUDA cores the
 //                     unit-lower-triangular solve for U^ and W (one column per
 //                     thread), and the chunk's operands
-//                     W | Q~ (Q~ = scale e^{gam} Q), K~ = e^{gam_L - gam} K,
+//                     [Q~; W] (Q~ = scale e^{gam} Q), K~ = e^{gam_L - gam} K,
 //                     P = scale (Q K^T o Gamma) in bf16, U^ transposed in
 //                     float32 and e^{gam_L}.  Nothing here depends on a state.
 //   gdn_state_kernel  one launch per depth, one CTA per (segment, head): the
 //                     state lives in TMEM (float32) for the whole segment; per
-//                     chunk the tensor core forms [W; Q~] S0, the epilogue warps
+//                     chunk the tensor core forms [Q~; W] S0, the epilogue warps
 //                     make V' = U^ - W S0, then O += P V' and S += K~^T V' (the
 //                     state pre-scaled by e^{gam_L}); the segment's final state
 //                     goes to HBM for its children.
@@ -363,7 +364,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnPara
   fence_after_sync();
   if (warp == 0) tmem_dealloc(tmem, 64);
 
-  // Q~ (rows 0..63 of the Q~|W tile) and K~
+  // Q~ (rows 0..63 of the [Q~; W] tile) and K~
   for (int i = tid; i < kGc * kGd / 2; i += kPrepThreads) {
     const int t = i / (kGd / 2), c = 2 * (i % (kGd / 2));
     const float eq = t < L ? p.scale * seg[t] : 0.f, ek = t < L ? sek[t] : 0.f;
