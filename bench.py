@@ -219,6 +219,215 @@ def _what_if(n_candidates: int = 64, groups_per_candidate: int = 8) -> dict:
             "rows_mean_tree_per_group": float(np.mean(rows_pf))}
 
 
+def _time_batch(b, name, dev, flush, reps=10, min_shared=None, seed=41):
+    """Packs batch `b` (stp_pack, optionally with another minimum shared run)
+    and times classification, forward and backward (forward only for the
+    float32 path) with CUDA events, L2 flushed before every repetition
+    (median of `reps`).  Returns (timings dict, plan info, host inputs)."""
+    import torch
+    from sft_trie_build_gb300 import stp
+
+    tokens, offsets, train = b.flat()
+    plan = stp.stp_pack(tokens, offsets, train, b.family, row_len=b.row_len,
+                        min_shared=b.min_shared if min_shared is None else min_shared)
+    info = stp.stp_plan_info(plan)
+    meta = stp.stp_plan_write(plan)
+    R, T = info["n_rows"], b.row_len
+    shape = W.attn_shape(name, R, T)
+    Hq, Hkv, D = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+    bf16 = shape.dtype == "bf16"
+    host = W.attn_tensors(shape, seed)
+    q, k, v, do = (x.to(dev) for x in host)
+    se_np = meta["subtree_end"]
+    desc = stp.Desc(R, T, Hq, Hkv, D, stp.STP_BF16 if bf16 else stp.STP_FP32, shape.scale,
+                    stp.stp_count_tile_pairs(se_np))
+    buf = stp.Buffers(desc, dev)
+    se = torch.from_numpy(se_np).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(R, Hq, T, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def once(m=None):
+        if m:
+            m[0].record()
+        stp.stp_classify(desc, se, buf.tile_meta)
+        if m:
+            m[1].record()
+        stp.stp_attn_fwd(desc, q, k, v, se, buf.tile_meta, o, lse, buf.fwd_ws)
+        if m:
+            m[2].record()
+        if bf16:
+            stp.stp_attn_bwd(desc, q, k, v, o, lse, do, se, buf.tile_meta, dq, dk, dv, buf.bwd_ws)
+        if m:
+            m[3].record()
+
+    for _ in range(3):
+        once()
+    torch.cuda.synchronize()
+    marks = []
+    for _ in range(reps):
+        flush.fill_(1)
+        m = (ev(), ev(), ev(), ev())
+        once(m)
+        marks.append(m)
+    torch.cuda.synchronize()
+    for ws in (buf.tile_meta, buf.fwd_ws) + ((buf.bwd_ws,) if bf16 else ()):
+        assert stp.stp_device_status(ws) == stp.STP_OK
+    t = {"classify_ms": statistics.median(a.elapsed_time(c) for a, c, _, _ in marks),
+         "fwd_ms": statistics.median(c.elapsed_time(f) for _, c, f, _ in marks),
+         "bwd_ms": statistics.median(f.elapsed_time(e) for _, _, f, e in marks) if bf16 else 0.0,
+         "ms": statistics.median(a.elapsed_time(e) for a, _, _, e in marks),
+         "tile_pairs": int(desc.max_tile_pairs), "shape": shape, "bf16": bf16}
+    del buf, q, k, v, do, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()
+    return t, info, host
+
+
+def _attn_config(name, dev, peak, flush, reps=10, oracle_heads=1) -> dict:
+    """One of the other workloads through the same calls (classification,
+    forward, backward; forward only for the float32 tiny row), with beside it
+    the float64 oracle on `oracle_heads` query heads of the same packed batch
+    (a bounded sample of the same work)."""
+    b = W.CONFIG_BATCHES[name](W.CONFIG_SEEDS[name])
+    t, info, host = _time_batch(b, name, dev, flush, reps)
+    shape, bf16 = t["shape"], t["bf16"]
+    R, T = info["n_rows"], b.row_len
+    Hq, Hkv, D = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+    useful = float(info["useful_pairs"])
+    flops = (14.0 if bf16 else 4.0) * D * Hq * useful
+    tot = t["ms"]
+    nt = T // 128
+    out = {"workload": b.info.get("name", name), "rows": R, "row_len": T, "sequences": b.n_seqs,
+           "heads": f"{Hq}/{Hkv}", "head_dim": D, "dtype": shape.dtype,
+           "passes": "classify+fwd+bwd" if bf16 else "classify+fwd",
+           "input_tokens": info["input_tokens"], "packed_tokens": info["packed_tokens"],
+           "useful_pairs_per_head": int(useful), "tile_pairs": t["tile_pairs"],
+           "tile_grid": f"{R} x {nt} x {nt}",
+           "classify_ms": t["classify_ms"], "fwd_ms": t["fwd_ms"], "bwd_ms": t["bwd_ms"], "ms": tot,
+           "useful_tflops": flops / (tot / 1e3) / 1e12,
+           "trajectories_per_s": b.n_seqs / (tot / 1e3),
+           "packed_tokens_per_s": info["packed_tokens"] / (tot / 1e3),
+           "l2": "flushed (512 MiB write) before every repetition; median of %d" % reps}
+    if bf16:
+        out["pct_of_bf16_peak"] = 100.0 * out["useful_tflops"] / peak
+        out["fwd_tflops"] = 4.0 * D * Hq * useful / (t["fwd_ms"] / 1e3) / 1e12
+        out["bwd_tflops"] = 10.0 * D * Hq * useful / (t["bwd_ms"] / 1e3) / 1e12
+    if oracle_heads:
+        from oracle import attn as OA
+        from oracle import pack as OP
+        plan_o = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared, b.family)
+        q_h, k_h, v_h, do_h = (x.float() for x in host)
+        if bf16:
+            dt, fl = oracle_sample(plan_o, q_h, k_h, v_h, do_h, shape.scale, oracle_heads)
+        else:
+            t0 = time.perf_counter()
+            OA.attn_fwd(plan_o, q_h[:, :, :oracle_heads], k_h[:, :, :1], v_h[:, :, :1], shape.scale)
+            dt = time.perf_counter() - t0
+            fl = 4.0 * D * oracle_heads * OA.useful_pairs(plan_o)
+        out["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
+                               "kind": "oracle", "seconds": dt,
+                               "sample": f"float64 NumPy oracle, {'fwd+bwd' if bf16 else 'fwd'} of "
+                                         f"{oracle_heads} of {Hq} query heads over the whole packed batch"}
+    return out
+
+
+def _list_mode(dev, peak, flush, reps=10) -> dict:
+    """The GRPO batch packed as a tree and without sharing ("list mode":
+    every sequence its own root, no shared run being long enough), rows of the
+    same length, through the same calls and timing (classification, forward,
+    backward); the pair token-throughput change / trajectory-throughput ratio
+    (attention only) sits beside the CoreWeave page's end-to-end 6.8x / -15%."""
+    b = _batch()
+    tree, tinfo, _ = _time_batch(b, WORKLOAD, dev, flush, reps, seed=43)
+    lst, linfo, _ = _time_batch(b, WORKLOAD, dev, flush, reps, min_shared=1 << 30, seed=43)
+    shape = lst["shape"]
+    D, Hq = shape.head_dim, shape.n_q_heads
+
+    def leg(t, info):
+        ms = t["ms"]
+        fl = 14.0 * D * Hq * float(info["useful_pairs"])
+        return {"rows": info["n_rows"], "packed_tokens": info["packed_tokens"],
+                "useful_pairs_per_head": int(info["useful_pairs"]), "ms": ms,
+                "useful_tflops": fl / (ms / 1e3) / 1e12,
+                "pct_of_bf16_peak": 100.0 * fl / (ms / 1e3) / 1e12 / peak,
+                "trajectories_per_s": b.n_seqs / (ms / 1e3),
+                "packed_tokens_per_s": info["packed_tokens"] / (ms / 1e3)}
+
+    lt, ll = leg(tree, tinfo), leg(lst, linfo)
+    return {"workload": f"the GRPO batch ({b.n_seqs} sequences of 5000 + U[100,1000] tokens), rows of "
+                        f"{b.row_len}: prefix tree vs list mode (no sharing: each sequence its own root)",
+            "tree": lt, "list": ll,
+            "token_throughput_change": lt["packed_tokens_per_s"] / ll["packed_tokens_per_s"] - 1.0,
+            "trajectory_throughput_ratio": lt["trajectories_per_s"] / ll["trajectories_per_s"],
+            "token_density": ll["packed_tokens"] / lt["packed_tokens"],
+            "pages_context": "CoreWeave ART-Optimized Megatron page: 6.8x trajectories/s at -15% tokens/s "
+                             "(end-to-end training step, GPU not named); ~8x theoretical bound"}
+
+
+def _planning_cost(reps=3) -> dict:
+    """Host planning cost of the packer (stp_pack: trie walk and placement
+    timed apart inside the call; stp_plan_write timed around the call) on the
+    global-tree curriculum batch at 1/4, 1, 4 and 16 times its 48 groups,
+    beside the prefix-tree-packing page's planning-cost table (a Python
+    implementation on unnamed hardware)."""
+    from sft_trie_build_gb300 import stp
+
+    page = {12: (105, 0.9, 1.4, 15), 48: (450, 9.6, 4.2, 61), 192: (1668, 42.0, 48.7, 227),
+            768: (6686, 291.2, 743.5, 918)}
+    out = []
+    for gpf in (4, 16, 64, 256):
+        b = W.curriculum(W.CONFIG_SEEDS["curriculum"], groups_per_family=gpf)
+        tokens, offsets, train = b.flat()
+        runs = []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            plan = stp.stp_pack(tokens, offsets, train, b.family, row_len=b.row_len, min_shared=b.min_shared)
+            t1 = time.perf_counter()
+            stp.stp_plan_write(plan)
+            t2 = time.perf_counter()
+            tm = stp.stp_plan_times(plan)
+            runs.append((tm["walk_ms"], tm["place_ms"], 1e3 * (t1 - t0), 1e3 * (t2 - t1)))
+        walk, place, pack, write = (statistics.median(r[i] for r in runs) for i in range(4))
+        groups = 3 * gpf
+        info = stp.stp_plan_info(plan)
+        row = {"groups": groups, "completions": b.n_seqs, "input_tokens": info["input_tokens"],
+               "rows": info["n_rows"], "tree_walk_ms": walk, "placement_ms": place, "stp_pack_ms": pack,
+               "materialize_ms": write}
+        if groups in page:
+            c, pw, pb, pr = page[groups]
+            row["page"] = {"completions": c, "tree_walk_ms": pw, "bin_packing_ms": pb, "rows": pr}
+        out.append(row)
+    return {"rows_of": "rows of 4096 tokens, min shared run 64, one global tree, host C++ packer, one thread",
+            "median_of": reps, "batches": out}
+
+
+def _classify_bandwidth(desc, se, tile_meta, reps=20) -> dict:
+    """Tile classification (three kernels) timed alone on the benchmarked row,
+    against its algorithmic bytes: subtree_end read once (4 B per token), the
+    class matrix written (1 B per tile pair), and per non-empty pair the two
+    list entries, the rank and the pair index (16 B)."""
+    import torch
+    from sft_trie_build_gb300 import stp
+
+    for _ in range(3):
+        stp.stp_classify(desc, se, tile_meta)
+    torch.cuda.synchronize()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        stp.stp_classify(desc, se, tile_meta)
+    e.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(e) / reps
+    R, T = desc.n_rows, desc.row_len
+    nt = T // 128
+    by = 4 * R * T + R * nt * nt + 16 * int(desc.max_tile_pairs)
+    return {"kernels": "tile_minmax_kernel + tile_lists_kernel + tile_pairs_kernel", "ms": ms,
+            "algorithmic_bytes": by, "achieved_gbs": by / (ms / 1e3) / 1e9,
+            "bound": "latency (the whole row's metadata is ~0.3 MB; back-to-back launches, L2-resident)"}
+
+
 def _batch(rank=0):
     return W.grpo(rank_seed(W.CONFIG_SEEDS[WORKLOAD], rank))
 
@@ -336,6 +545,7 @@ def main():
     ap.add_argument("--chunks", type=int, default=8, help="kv-head groups of the host-buffer step")
     args = ap.parse_args()
 
+    peak, hbm, peak_kind = _peaks()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -533,7 +743,6 @@ def main():
             "host-buffer step differs"
     e2e_value = world * step_flops * args.steps / (e_tot / 1e3) / 1e12
 
-    peak, hbm, peak_kind = _peaks()
     bwd_avg = statistics.mean(bwd_ms)
     achieved = bwd_flops / (bwd_avg / 1e3) / 1e12
     line = {
@@ -566,6 +775,17 @@ def main():
         "gpu_launches": 7 * args.steps,
     }
     if rank == 0:
+        line["classify"] = _classify_bandwidth(desc, se, buf.tile_meta)
+        cfgs = {}
+        for name in ("tiny", "curriculum", "deep", "bushy"):
+            try:
+                cfgs[name] = _attn_config(name, dev, peak, flush,
+                                          oracle_heads=0 if args.no_cpu_baseline else 1)
+            except Exception as exc:  # an auxiliary field: report, do not lose the bench line
+                cfgs[name] = {"error": repr(exc)}
+        line["configs"] = cfgs
+        line["list_mode"] = _list_mode(dev, peak, flush)
+        line["planning_cost"] = _planning_cost()
         line["what_if"] = _what_if()
         line["indexer"] = _indexer(R, T, se, buf.tile_meta, desc.max_tile_pairs, useful, dev)
         line["logprob"] = _logprob(meta0["token_ids"], meta0["loss_mask"], dev, peak)

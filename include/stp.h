@@ -132,6 +132,14 @@ stp_status stp_plan_info(const stp_plan* plan, stp_plan_info_t* info);
 stp_status stp_plan_write(const stp_plan* plan, int32_t* token_ids, int32_t* position_ids,
                           int32_t* subtree_end, uint8_t* loss_mask, int64_t* gather_index);
 
+/*
+ * stp_plan_times -- host wall time (milliseconds, steady clock) that stp_pack
+ * spent building this plan: the trie walk and the placement of the leaves
+ * into rows, measured apart ([P1] planning-cost table: "tree walk" and "bin
+ * packing" columns).  Both pointers must be non-NULL (STP_EINVAL otherwise).
+ */
+stp_status stp_plan_times(const stp_plan* plan, double* walk_ms, double* place_ms);
+
 /* Row index (bin) of every sequence, int32 [n_seqs] (host). */
 stp_status stp_plan_rows_of(const stp_plan* plan, int32_t* row_of_seq);
 

@@ -714,7 +714,12 @@ stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d
       (reinterpret_cast<uintptr_t>(d_ws) | reinterpret_cast<uintptr_t>(d_plan)) & 255)
     return fail(STP_EINVAL, "stp_gdn_fwd: x, conv_w, o 16-byte, d_plan and ws 256-byte aligned");
   const int N = w[GP_N], H = desc->n_heads, n_chunk = w[GP_NCHUNK], n_seg = w[GP_NSEG], n_depth = w[GP_NDEPTH];
-  if (N == 0) return STP_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    // nothing to compute, but the error word still starts this call cleared
+    const cudaError_t e0 = cudaMemsetAsync(d_ws, 0, 4, s);
+    return e0 == cudaSuccess ? STP_OK : fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e0));
+  }
   const int32_t* dp = static_cast<const int32_t*>(d_plan);
   GdnParams p;
   p.N = N;
@@ -759,7 +764,6 @@ stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(gdn_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStSmem);
   });
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = attr_err;
   if (e == cudaSuccess) e = cudaMemsetAsync(p.err, 0, 4, s);
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e));

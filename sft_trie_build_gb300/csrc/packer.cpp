@@ -27,6 +27,7 @@
 //     pass over the bin's segments in pre-order.
 #include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -210,6 +211,8 @@ struct stp_plan {
   std::vector<int32_t> row_of_seq;
   int64_t packed = 0;
   int64_t useful_pairs = 0;
+  double walk_ms = 0.0;   // host wall time of the trie walk inside stp_pack
+  double place_ms = 0.0;  // host wall time of the leaf placement inside stp_pack
 };
 
 namespace {
@@ -287,6 +290,8 @@ stp_status stp_pack(const int32_t* tokens, const int64_t* offsets, int32_t n_seq
       for (int32_t s = 0; s < n_seqs; ++s) fams.push_back({s});
     }
 
+    using clock = std::chrono::steady_clock;
+    const auto t_walk = clock::now();
     Walker w;
     w.tok = P->tokens.data();
     w.off = P->offsets.data();
@@ -314,6 +319,8 @@ stp_status stp_pack(const int32_t* tokens, const int64_t* offsets, int32_t n_seq
     }
     P->segs = std::move(w.segs);
     P->leaf_of = std::move(w.leaf_of);
+    const auto t_place = clock::now();
+    P->walk_ms = std::chrono::duration<double, std::milli>(t_place - t_walk).count();
 
     const size_t words = (P->segs.size() + 63) / 64;
     auto new_bin = [&]() -> Bin& {
@@ -358,6 +365,7 @@ stp_status stp_pack(const int32_t* tokens, const int64_t* offsets, int32_t n_seq
         }
       }
     }
+    P->place_ms = std::chrono::duration<double, std::milli>(clock::now() - t_place).count();
     P->row_of_seq.assign(n_seqs, -1);
     for (size_t b = 0; b < P->bins.size(); ++b) {
       Bin& bn = P->bins[b];
@@ -389,6 +397,14 @@ stp_status stp_plan_info(const stp_plan* P, stp_plan_info_t* info) {
   info->n_leaves = P->n_seqs;
   info->useful_pairs = P->useful_pairs;
   info->tree_token_ratio = P->packed ? (double)P->tokens.size() / (double)P->packed : 0.0;
+  return STP_OK;
+}
+
+stp_status stp_plan_times(const stp_plan* P, double* walk_ms, double* place_ms) {
+  stp::clear_error();
+  if (!P || !walk_ms || !place_ms) return fail(STP_EINVAL, "stp_plan_times: NULL argument");
+  *walk_ms = P->walk_ms;
+  *place_ms = P->place_ms;
   return STP_OK;
 }
 

@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "STP_OK", 1: "STP_EINVAL", 2: "STP_ETOOLONG", 3: "STP_ENOMEM"
 STP_GLOBAL, STP_PER_FAMILY, STP_IN_ORDER = 0, 1, 2
 STP_BF16, STP_FP32 = 0, 1
 
-EXPORTED = ["stp_pack", "stp_plan_info", "stp_plan_write", "stp_plan_rows_of", "stp_plan_free",
+EXPORTED = ["stp_pack", "stp_plan_info", "stp_plan_write", "stp_plan_rows_of", "stp_plan_times", "stp_plan_free",
             "stp_plan_rows", "stp_plan_rows_many",
             "stp_count_tile_pairs", "stp_workspace_size", "stp_classify", "stp_classify_noalloc", "stp_read_tile_classes",
             "stp_attn_fwd", "stp_attn_bwd", "stp_step_scratch_size", "stp_attn_step_host",
@@ -95,6 +95,8 @@ def lib():
         L.stp_plan_write.restype = st
         L.stp_plan_rows_of.argtypes = [_P, _I32P]
         L.stp_plan_rows_of.restype = st
+        L.stp_plan_times.argtypes = [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+        L.stp_plan_times.restype = st
         L.stp_plan_free.argtypes = [_P]
         L.stp_plan_free.restype = None
         L.stp_plan_rows.argtypes = [_I32P, _I64P, ctypes.c_int32, _U8P, _I32P, _I32P, ctypes.c_int32,
@@ -236,6 +238,13 @@ def stp_plan_write(plan: Plan, out=None) -> dict:
                                 _ptr(out.get("loss_mask"), ctypes.c_uint8),
                                 _ptr(out.get("gather_index"), ctypes.c_int64)), "stp_plan_write")
     return out
+
+
+def stp_plan_times(plan: Plan) -> dict:
+    """Host milliseconds stp_pack spent on the trie walk and on the placement."""
+    w, p = ctypes.c_double(), ctypes.c_double()
+    _check(lib().stp_plan_times(plan.handle, ctypes.byref(w), ctypes.byref(p)), "stp_plan_times")
+    return {"walk_ms": w.value, "place_ms": p.value}
 
 
 def stp_plan_rows_of(plan: Plan) -> np.ndarray:

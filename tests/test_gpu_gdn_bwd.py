@@ -45,3 +45,28 @@ def test_long_chain_many_chunks():
     rng = np.random.default_rng(5)
     seq = rng.integers(1, 1000, 700).astype(np.int32)
     _compare(OP.pack([seq], [np.zeros(700, np.uint8)], 768, 64), H=1, seed=5)
+
+
+def test_grpo_row_two_heads():
+    """The benchmarked shape, every element of two heads: the GRPO row (a
+    5000-token prefix, 79 chunks walked one after another, forked into 16
+    rollouts), 16 heads of 128.  Heads never mix in the layer core, so the
+    oracle of head h is the layer with one head on h's q, k, v channels."""
+    from gdn_helpers import oracle_head_grads
+
+    b = W.grpo(seed=W.CONFIG_SEEDS["grpo"])
+    po = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared)
+    H = 16
+    outs, status, inputs, dO, scale = run_gdn_train(po, H, seed=0)
+    assert status == 0
+    _, dx, dw, dg, db = outs
+    real = np.arange(po.used[0])
+    errs = {}
+    for h, (ch, gx, gw, gg, gb) in oracle_head_grads(po, 0, inputs, dO, scale, H, (0, 9)).items():
+        for name, got, ref in (("dx", dx[real][:, ch], gx[real]), ("dconv_w", dw[ch], gw),
+                               ("dg", dg[real, h], gg[real]), ("dbeta", db[real, h], gb[real])):
+            m = np.abs(ref).max()
+            d = np.abs(got - ref)
+            errs[(h, name)] = (float(d.max() / m), float(d.mean() / m))
+            assert d.max() <= 5e-2 * m and d.mean() <= 5e-3 * m, (h, name, d.max(), d.mean(), m)
+    print("\nGRPO row GDN backward, max / mean error relative to max |oracle|:", errs)

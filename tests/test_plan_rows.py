@@ -93,3 +93,15 @@ def test_errors(stp_lib):
     assert stp.stp_plan_rows(t, o, tr, b.family, [], row_len=b.row_len) == (0, 0)
     rows, packed = stp.stp_plan_rows_many(t, o, tr, b.family, [], row_len=b.row_len)
     assert len(rows) == 0 and len(packed) == 0
+
+
+def test_plan_times_are_reported(stp_lib):
+    """stp_plan_times gives the walk and placement times of the plan's own
+    stp_pack call: non-negative, and the placement of a many-group batch is
+    measurable."""
+    b = W.curriculum(W.CONFIG_SEEDS["curriculum"])
+    tokens, offsets, train = b.flat()
+    plan = stp.stp_pack(tokens, offsets, train, b.family, row_len=b.row_len, min_shared=b.min_shared)
+    t = stp.stp_plan_times(plan)
+    assert t["walk_ms"] >= 0.0 and t["place_ms"] >= 0.0
+    assert t["walk_ms"] + t["place_ms"] > 0.0
