@@ -201,6 +201,15 @@ typedef struct {
                              count); sizes the bf16 backward's dS workspace.
                              0 = every pair with key tile <= query tile,
                              R * NT * (NT + 1) / 2 with NT = T / 128            */
+  int32_t ds_groups;   /* bf16 backward: kv-head groups whose dS tiles the
+                          workspace holds at once.  The backward runs the kv
+                          heads in n = min(Hkv, 8) groups of whole kv heads,
+                          each on its own stream; with ds_groups in [1, n) a
+                          group reuses the slot of the group ds_groups before
+                          it and waits for that group's dQ pass, which bounds
+                          the workspace by ds_groups groups instead of Hq
+                          (less overlap between groups).  0 = n (all groups
+                          at once, fastest)                                  */
 } stp_attn_desc;
 
 /*
@@ -219,8 +228,10 @@ stp_status stp_count_tile_pairs(const int32_t* subtree_end, int32_t n_rows, int3
  *   fwd_ws     -- workspace of stp_attn_fwd (error word)
  *   bwd_ws     -- workspace of stp_attn_bwd (error word, per-query
  *                 Delta = dO . O and -LSE log2 e, and on the bf16 path one
- *                 32 KiB dS tile per (non-empty tile pair, query head), so
- *                 max_tile_pairs * Hq * 32 KiB)
+ *                 32 KiB dS tile per (non-empty tile pair, query head of
+ *                 the kv-head groups held at once), so
+ *                 max_tile_pairs * S * ceil(Hkv / n) * (Hq / Hkv) * 32 KiB
+ *                 with n = min(Hkv, 8) groups and S = ds_groups (or n))
  * Any pointer may be NULL.  Buffers must be 256-byte aligned.
  */
 stp_status stp_workspace_size(const stp_attn_desc* desc, size_t* tile_meta_bytes,

@@ -29,6 +29,7 @@ stp_status check_desc(const stp_attn_desc* d) {
     return fail(STP_EUNSUPPORTED, "fp32 needs head_dim 64 or 128 (got %d)", d->head_dim);
   if (!(d->scale > 0.f) || d->scale > 1e4f) return fail(STP_EINVAL, "scale must be positive");
   if (d->max_tile_pairs < 0) return fail(STP_EINVAL, "max_tile_pairs must be >= 0");
+  if (d->ds_groups < 0) return fail(STP_EINVAL, "ds_groups must be >= 0");
   if ((int64_t)d->n_rows * d->row_len * d->n_q_heads * d->head_dim > (int64_t)1 << 40)
     return fail(STP_EUNSUPPORTED, "problem too large");
   return STP_OK;
@@ -122,13 +123,16 @@ extern "C" stp_status stp_attn_bwd(const stp_attn_desc* desc, const void* q, con
   a.dk = dk;
   a.dv = dv;
   const int64_t cap = pair_capacity(desc->n_rows, desc->row_len / kTile, desc->max_tile_pairs);
-  const BwdWs w = bwd_ws_layout(desc->n_rows, desc->row_len, desc->n_q_heads, desc->dtype == STP_BF16, cap);
+  const BwdWs w = bwd_ws_layout(desc->n_rows, desc->row_len, desc->n_q_heads, desc->n_kv_heads,
+                                desc->dtype == STP_BF16, cap, desc->ds_groups);
   char* ws = static_cast<char*>(d_ws);
   a.err = reinterpret_cast<uint32_t*>(ws + w.err);
   a.delta = reinterpret_cast<float*>(ws + w.delta);
   a.nlse2 = desc->dtype == STP_BF16 ? reinterpret_cast<float*>(ws + w.nlse2) : nullptr;
   a.ds = desc->dtype == STP_BF16 ? ws + w.ds : nullptr;
   a.ds_cap = cap;
+  a.ds_slots = bwd_groups(desc->n_q_heads, desc->n_kv_heads, desc->ds_groups).slots;
+  a.ds_slot_bytes = w.slot_bytes;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaMemsetAsync(a.err, 0, 4, s);
   cudaError_t e;

@@ -90,14 +90,6 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H) {
 // Device helpers
 // ------------------------------------------------------------------------
 
-// Writes 8 consecutive bf16 values (columns 8c .. 8c+7 of row `row`) into a
-// K-major swizzled 128 x 128 tile.
-__device__ __forceinline__ void st_swizzled8(uint8_t* tile, int row, int c, uint4 v) {
-  uint8_t* half = tile + (c >> 3) * kHalfTile;
-  const int chunk = (c & 7) ^ (row & 7);
-  *reinterpret_cast<uint4*>(half + row * 128 + chunk * 16) = v;
-}
-
 struct FwdParams {
   int R, T, Hq, Hkv, NT, G, npairs;
   float scale_log2;
@@ -455,49 +447,67 @@ __global__ void __launch_bounds__(kThreads, 1)
 // bwd_tc_kernel, one CTA per (row r, kv head g, key tile kt): the key tile's
 // list of non-empty query tiles, times the G query heads of the group, gives
 // the iterations j = (query tile, head).  dK and dV accumulate in TMEM over
-// all iterations; each iteration's dS^T tile (bf16, the shared-memory operand
-// of the dK MMA) is also copied out to the workspace slot of its (pair, head).
-// 16 warps:
+// all iterations; each iteration's dS^T tile also goes out to the workspace
+// slot of its (pair, head), for the dQ kernel.
+// Tensor memory (512 columns, keys on lanes):
+//   0..127    S^T = K Q^T (f32); once read, dS^T as packed bf16 pairs over
+//             the first 32 columns of each 64-query half;
+//   128..255  dP^T = V dO^T (f32); once read, P^T as packed bf16 pairs over
+//             the first 32 columns of each half;
+//   256..383  dV += P^T dO (A from TMEM);  384..511  dK += dS^T Q (A from TMEM).
+// Neither P^T nor dS^T passes through shared memory: next to a stream of
+// MMAs whose operands are both in shared memory, shared-memory stores of the
+// elementwise warps wait hundreds of cycles each, so dS^T goes to TMEM for
+// the dK product and straight from registers to global memory for dQ, in a
+// layout where each warp's 16-byte stores are contiguous.
+// 12 warps:
 //   warps 0-7   elementwise, one thread per key (= TMEM lane); warps 0-3 take
-//               query columns 0..63, warps 4-7 columns 64..127:
-//               p = 2^(s scale log2e - LSE_i log2e) (masked on PARTIAL tiles
-//               with the thread's own subtree_end[j]), dS = p (dP - Delta_i);
-//               P^T goes back to TMEM as packed bf16 pairs over the consumed
-//               score columns, dS^T to shared memory once the previous tile
-//               there has been consumed;
-//   warp 8      dS^T store: one 32 KiB bulk copy per iteration, shared memory
-//               to the pair's slot; the tile is free again once the copy has
-//               read it and the dK MMA has finished with it;
-//   warps 9-11  no role (their registers go to the elementwise warps);
-//   warp 12     TMA: K, V once; Q, dO, -LSE log2e and -Delta of each
-//               iteration through a two-stage ring;
-//   warp 13     MMA issue and TMEM owner: S^T = K Q^T (columns 0..127),
-//               dP^T = V dO^T (128..255), dV += P^T dO (A from TMEM, 256..383),
-//               dK += dS^T Q (384..511).  After the elementwise pass of j it
-//               issues dV(j), S^T(j+1) (over P^T(j), which dV(j) read
-//               before), dK(j); dP^T(j+1) goes out earlier, once the pass of
-//               j has loaded dP^T(j), so it runs during that pass, and the
-//               pass of j+1 overlaps dK(j).
+//               query columns 0..63, warps 4-7 columns 64..127.  As soon as
+//               S^T(j) is in TMEM: p = 2^(s scale log2e - LSE_i log2e)
+//               (masked on PARTIAL tiles with the thread's own
+//               subtree_end[j]); once dP^T(j) is: dS = p (dP - Delta_i);
+//               P^T and dS^T back to TMEM, dS^T to the workspace;
+//   warp 8      TMA: K, V once; Q (with -LSE log2e and -Delta) and dO of each
+//               iteration through two 2-stage rings;
+//   warp 9      MMA issue and TMEM owner.  After the elementwise pass of j:
+//               dK(j) (reads dS^T(j) in the S^T columns), S^T(j+1) (over
+//               them), dV(j) (reads P^T(j) in the dP^T columns), dP^T(j+1)
+//               (over them).  The pass of j+1 starts its exponentials as soon
+//               as S^T(j+1) lands, while the tensor core runs dV(j) and
+//               dP^T(j+1).
+//   warps 10-11 no role (a full warpgroup for the register split).
 // dK (times scale) and dV leave TMEM once at the end.
+//
+// dS^T tile layout in the workspace (bf16, 32 KiB per (pair, head)): 16
+// blocks of 2048 bytes, block c holding query columns 8c..8c+7 of all 128
+// keys, 16 bytes per key: byte offset c * 2048 + key * 16.  As an MMA
+// operand with the queries as M (the dQ product) that is the no-swizzle
+// MN-major layout: 8 x 16-byte core matrices, 2048 bytes apart along the
+// queries and 128 bytes apart along the keys.
 //
 // dq_tc_kernel, one CTA per (row, kv head, query tile, up to four query heads
 // of the group): dQ_h = scale sum over the query tile's key tiles of dS K, the
 // dS tiles read back from the workspace and K by TMA, accumulated in TMEM
 // (128 columns per head).  Every dQ element is summed in one fixed order, and
 // no atomics are involved.
+//
+// The kv heads run in groups, each on its own stream (bwd_tc_kernel then
+// dq_tc_kernel); a group's dS tiles live in one of `slots` workspace slots,
+// and a group that reuses a slot waits for the dQ pass of the group before it.
 
 struct BwdParams {
   int R, T, Hq, Hkv, NT, G;
   int g0, ng;           // kv heads [g0, g0 + ng) of this launch
+  int slot_heads;       // query heads per pair in a dS slot
   float scale_log2;
-  int64_t cap;          // dS slots (pairs) in the workspace
+  int64_t cap;          // dS pairs per slot
   const int32_t* se;
   const int32_t* csc_cnt;
   const int32_t* csc;
   const int32_t* csc_pair;
   const float* nlse2;   // -LSE * log2 e
   const float* ndelta;  // -Delta
-  uint8_t* ds;          // [pair][Hq] dS^T tiles
+  uint8_t* ds;          // this launch's slot: [pair][slot_heads] dS^T tiles
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   float scale;
@@ -505,22 +515,23 @@ struct BwdParams {
 };
 
 enum {
-  C_KV = 0, C_QF = 1, C_QE = 3, C_SF = 5, C_DPF = 6, C_DR = 7, C_PSF = 8, C_DONE = 9, C_DRAIN = 10,
-  C_COUNT = 11
+  C_KV = 0, C_QF = 1, C_QE = 3, C_DF = 5, C_DE = 7, C_SF = 9, C_DPF = 10, C_DR = 11, C_DONE = 12,
+  C_DRAIN = 13, C_COUNT = 14
 };
-// shared memory: [K | V | Q0 | Q1 | dO0 | dO1 | dS^T] (1024-aligned, at the
-// start of dynamic shared memory) [vec0 | vec1] [barriers ...]
-constexpr int kBwdBigBytes = 7 * kTileBytes;
+// shared memory: [K | V | Q0 | Q1 | dO0 | dO1] (1024-aligned, at the start of
+// dynamic shared memory) [vec0 | vec1] [barriers ...]
+constexpr int kBwdBigBytes = 6 * kTileBytes;
 constexpr int kBwdVecBytes = 2 * 2 * 128 * 4;  // per stage: -LSE log2e and -Delta, 128 each
 constexpr int kBwdSmem = kBwdBigBytes + kBwdVecBytes + kSmallBytes;
 static_assert(kBwdSmem <= kSmemLimit, "backward shared memory");
-// 16 warps x 128 registers at launch, rebalanced with setmaxnreg:
-// 128 x (184 + 184 (elementwise) + 72 (store group) + 72 (control)) = 65536,
-// and per SM sub-partition (warps w, w+4, w+8, w+12) 512.
-constexpr int kBwdThreads = 512;
+constexpr int kDsBlock = 128 * 16;  // one 8-query block of a dS^T tile: 16 bytes per key
+// 12 warps x 168 registers at launch, rebalanced with setmaxnreg:
+// 256 x 216 (elementwise) + 128 x 72 (control) <= 384 x 168, and per SM
+// sub-partition (warps w, w+4, w+8) 216 + 216 + 72 <= 512.
+constexpr int kBwdThreads = 384;
 constexpr int kBwdPrefetch = 2;  // iterations ahead for the L2 prefetch of Q, dO
-constexpr int kBwdRegsMath = 184, kBwdRegsCtl = 72;
-static_assert(128 * (2 * kBwdRegsMath + 2 * kBwdRegsCtl) <= kBwdThreads * 128, "register split");
+constexpr int kBwdRegsMath = 216, kBwdRegsCtl = 72;
+static_assert(256 * kBwdRegsMath + 128 * kBwdRegsCtl <= kBwdThreads * 168, "register split");
 
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -533,14 +544,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + kBwdBigBytes + kBwdVecBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  const uint32_t k_s = big_s, v_s = big_s + kTileBytes, dst_s = big_s + 6 * kTileBytes;
-  uint8_t* dst_tile = big + 6 * kTileBytes;
+  const uint32_t k_s = big_s, v_s = big_s + kTileBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per_kt = p.R * p.ng;
   const int kt = (int)(blockIdx.x / per_kt);
   const int r = (blockIdx.x % per_kt) / p.ng;
-  const int g = p.g0 + (int)(blockIdx.x % p.ng);
+  const int gl = (int)(blockIdx.x % p.ng);  // kv head within this launch
+  const int g = p.g0 + gl;
   const int cnt = p.csc_cnt[(size_t)r * p.NT + kt];
   const int32_t* list = p.csc + ((size_t)r * p.NT + kt) * p.NT;
   const int n_it = cnt * p.G;
@@ -548,9 +559,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < C_COUNT; ++b)
-      // C_DPF, C_DR: one arrival per elementwise warp; C_PSF: the dK commit
-      // and the dS^T store
-      mbar_init(&bars[b], (b == C_DR || b == C_DPF) ? 8 : (b == C_PSF ? 2 : 1));
+      mbar_init(&bars[b], b == C_DR ? 8 : 1);  // C_DR: one arrival per elementwise warp
     *abort_flag = 0;
     if ((big_s & 1023u) != 0 || cnt <= 0 || cnt > p.NT) {
       *abort_flag = 1;
@@ -558,7 +567,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     fence_mbar_init();
   }
-  if (warp == 13) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -568,11 +577,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const bool run = !*abort_flag;
 
-  if (warp >= 12) {
+  if (warp >= 8) {
     regs_dec<kBwdRegsCtl>();
-    if (warp == 12 && lane == 0 && run) {
+    if (warp == 8 && lane == 0 && run) {
       // ---------------------------------------------------------- producer
-      int issued_q[2] = {-1, -1};
+      int issued_q[2] = {-1, -1}, issued_d[2] = {-1, -1};
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
@@ -603,87 +612,100 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_prefetch_l2_3d(&tdo, hf * 64, h2, row0 + qt2 * 128);
           }
         }
+        // Q (and the per-query vectors) of j: the stage frees once dK(j-2) is done
         if (j >= 2 && !mbar_wait(&bars[C_QE + st], (n - 1) & 1, abort_flag, p.err)) break;
-        mbar_expect_tx(&bars[C_QF + st], 2 * kTileBytes + 2 * 128 * 4);
+        mbar_expect_tx(&bars[C_QF + st], kTileBytes + 2 * 128 * 4);
         float* vs = vec + st * 256;
         const size_t at = ((size_t)r * p.Hq + h) * p.T + qt * 128;
         bulk_load(vs, p.nlse2 + at, 512, &bars[C_QF + st]);
         bulk_load(vs + 128, p.ndelta + at, 512, &bars[C_QF + st]);
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int hf = 0; hf < 2; ++hf)
           tma_load_3d(big + (2 + st) * kTileBytes + hf * kHalfTile, &tq, &bars[C_QF + st], hf * 64, h,
                       row0 + qt * 128);
-          tma_load_3d(big + (4 + st) * kTileBytes + hf * kHalfTile, &tdo, &bars[C_QF + st], hf * 64, h,
-                      row0 + qt * 128);
-        }
         issued_q[st] = n;
+        // dO of j: the stage frees once dV(j-2) is done
+        if (j >= 2 && !mbar_wait(&bars[C_DE + st], (n - 1) & 1, abort_flag, p.err)) break;
+        mbar_expect_tx(&bars[C_DF + st], kTileBytes);
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(big + (4 + st) * kTileBytes + hf * kHalfTile, &tdo, &bars[C_DF + st], hf * 64, h,
+                      row0 + qt * 128);
+        issued_d[st] = n;
       }
       mbar_wait_drain(&bars[C_KV], 0);
-      for (int st = 0; st < 2; ++st)
+      for (int st = 0; st < 2; ++st) {
         if (issued_q[st] >= 0) mbar_wait_drain(&bars[C_QF + st], issued_q[st] & 1);
-    } else if (warp == 13 && lane == 0 && run) {
+        if (issued_d[st] >= 0) mbar_wait_drain(&bars[C_DF + st], issued_d[st] & 1);
+      }
+    } else if (warp == 9 && lane == 0 && run) {
       // ---------------------------------------------------------- MMA issue
       constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
-      constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // dV (A in TMEM), dK
+      constexpr uint32_t id_kn = idesc_bf16(128, 128, 0, 1);  // dV, dK (A in TMEM)
       // descriptor low words; slice kk adds a constant to the start-address field
       const uint32_t k_km = desc_lo_kmajor(k_s), v_km = desc_lo_kmajor(v_s);
-      const uint32_t ds_km = desc_lo_kmajor(dst_s);
       const uint32_t q_km0 = desc_lo_kmajor(big_s + 2 * kTileBytes), do_km0 = desc_lo_kmajor(big_s + 4 * kTileBytes);
       const uint32_t q_mn0 = desc_lo_mnmajor(big_s + 2 * kTileBytes), do_mn0 = desc_lo_mnmajor(big_s + 4 * kTileBytes);
       constexpr uint32_t kStage = kTileBytes >> 4;  // one tile further in the ring
       auto km = [](int kk) { return (uint32_t)((kk >> 2) * (kHalfTile >> 4) + (kk & 3) * 2); };
       auto mn = [](int kk) { return (uint32_t)(kk * 128); };
+      // packed columns of query columns 16 kk .. 16 kk + 15 (first 32 columns of each half)
+      auto pk = [](int kk) { return (uint32_t)(kk < 4 ? kk * 8 : 64 + (kk - 4) * 8); };
       bool ok = mbar_wait(&bars[C_KV], 0, abort_flag, p.err);
       if (ok && n_it > 0) {
         ok = mbar_wait(&bars[C_QF], 0, abort_flag, p.err);
         if (ok) {
           fence_after_sync();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km0 + km(kk), id_kk, kk > 0);
-#pragma unroll
           for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, k_km + km(kk), q_km0 + km(kk), id_kk, kk > 0);
           mma_commit(&bars[C_SF]);
+          ok = mbar_wait(&bars[C_DF], 0, abort_flag, p.err);
+        }
+        if (ok) {
+          fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km0 + km(kk), id_kk, kk > 0);
+          mma_commit(&bars[C_DPF]);
         }
       }
 #pragma unroll 1
       for (int j = 0; ok && j < n_it; ++j) {
-        const uint32_t so = (j & 1) ? kStage : 0, so1 = (j & 1) ? 0 : kStage;
+        const int st = j & 1, st1 = (j + 1) & 1;
+        const uint32_t so = st ? kStage : 0, so1 = st ? 0 : kStage;
         const bool next = j + 1 < n_it;
-        // dP^T(j+1) as soon as the elementwise pass of j holds dP^T(j) in
-        // registers: the tensor core computes it during that pass
-        if (next) {
-          if (!mbar_wait(&bars[C_DPF], j & 1, abort_flag, p.err) ||
-              !mbar_wait(&bars[C_QF + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, p.err))
-            break;
-          fence_after_sync();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km0 + so1 + km(kk), id_kk, kk > 0);
-        }
         if (!mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err)) break;
         fence_after_sync();
-        // dV += P^T dO: P^T of query columns 16 kk..16 kk+15 sits in packed
-        // columns 8 kk (first half) or 64 + 8 (kk - 4) (second half)
+        // dK += dS^T Q, dS^T(j) in the S^T columns
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts_lo(tmem + 256, tmem + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), do_mn0 + so + mn(kk), id_kn,
-                    (j > 0 || kk > 0));
-        // S^T(j+1) over columns 0..127, after dV has read P^T(j) there
+          mma_ts_lo(tmem + 384, tmem + pk(kk), q_mn0 + so + mn(kk), id_kn, (j > 0 || kk > 0));
+        mma_commit(&bars[C_QE + st]);
+        // S^T(j+1) over them
         if (next) {
+          if (!mbar_wait(&bars[C_QF + st1], ((j + 1) >> 1) & 1, abort_flag, p.err)) break;
+          fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, k_km + km(kk), q_km0 + so1 + km(kk), id_kk, kk > 0);
           mma_commit(&bars[C_SF]);
         }
+        // dV += P^T dO, P^T(j) in the dP^T columns
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 384, ds_km + km(kk), q_mn0 + so + mn(kk), id_kn, (j > 0 || kk > 0));
-        mma_commit(&bars[C_QE + (j & 1)]);
-        mma_commit(&bars[C_PSF]);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts_lo(tmem + 256, tmem + 128 + pk(kk), do_mn0 + so + mn(kk), id_kn, (j > 0 || kk > 0));
+        mma_commit(&bars[C_DE + st]);
+        // dP^T(j+1) over them
+        if (next) {
+          if (!mbar_wait(&bars[C_DF + st1], ((j + 1) >> 1) & 1, abort_flag, p.err)) break;
+          fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km0 + so1 + km(kk), id_kk, kk > 0);
+          mma_commit(&bars[C_DPF]);
+        }
       }
       if (ok) mma_commit(&bars[C_DONE]);
       mma_commit(&bars[C_DRAIN]);
       mbar_wait_drain(&bars[C_DRAIN], 0);
     }
     __syncwarp();
-  } else if (warp < 8) {
+  } else {
     // ------------------------------------------------ per-key elementwise
     regs_inc<kBwdRegsMath>();
     const int half = warp >> 2;          // query columns 64 half .. 64 half + 63
@@ -693,12 +715,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_col = lane_base + half * 64, dp_col = lane_base + 128 + half * 64;
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+    const int32_t* pairs = p.csc_pair + ((size_t)r * p.NT + kt) * p.NT;
     bool ok = run;
     int ent = run ? list[0] : 0;
+    int pair = run ? pairs[0] : 0;
     for (int j = 0; ok && j < n_it; ++j) {
       const int st = j & 1;
-      const int qt = ent >> 1, part = ent & 1;
-      if (j + 1 < n_it) ent = list[(j + 1) / p.G];
+      const int qt = ent >> 1, part = ent & 1, pr_j = pair;
+      if (j + 1 < n_it) {
+        ent = list[(j + 1) / p.G];
+        pair = pairs[(j + 1) / p.G];
+      }
       const int q0 = qt * 128 + half * 64;
       const float* nl_s = vec + st * 256 + half * 64;   // -LSE log2 e per query column
       const float* nd_s = nl_s + 128;                   // -Delta per query column
@@ -709,56 +736,67 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       fence_after_sync();
-      // all 64 score and 64 dP columns of this half with one TMEM wait
-      uint32_t us[64], ud[64];
-      tmem_ld32(tmem + s_col, us);
-      tmem_ld32(tmem + s_col + 32, us + 32);
-      tmem_ld32(tmem + dp_col, ud);
-      tmem_ld32(tmem + dp_col + 32, ud + 32);
+      // P from S^T: 64 query columns of this half
+      uint32_t u[64];
+      tmem_ld32(tmem + s_col, u);
+      tmem_ld32(tmem + s_col + 32, u + 32);
       tmem_ld_wait();
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[C_DPF]);
-      uint32_t dd[32];                    // dS of the 64 columns, packed bf16 pairs
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {       // 16 query columns at a time
-        uint32_t pp[8];
+      for (int col = 0; col < 64; col += 4) {
+        const float4 nl4 = *reinterpret_cast<const float4*>(nl_s + col);
 #pragma unroll
-        for (int k = 0; k < 16; k += 4) {
-          const int col = c * 16 + k;
-          const float4 nl4 = *reinterpret_cast<const float4*>(nl_s + col);
-          const float4 nd4 = *reinterpret_cast<const float4*>(nd_s + col);
-#pragma unroll
-          for (int u2 = 0; u2 < 2; ++u2) {
-            const int cc = col + 2 * u2;
-            const float2 nl2 = u2 ? make_float2(nl4.z, nl4.w) : make_float2(nl4.x, nl4.y);
-            const float2 nd2 = u2 ? make_float2(nd4.z, nd4.w) : make_float2(nd4.x, nd4.y);
-            float2 y = __ffma2_rn(make_float2(__uint_as_float(us[cc]), __uint_as_float(us[cc + 1])), sl2, nl2);
-            if (part) {
-              const int i = q0 + cc;
-              if (!(jk <= i && se_j >= i)) y.x = -INFINITY;
-              if (!(jk <= i + 1 && se_j >= i + 1)) y.y = -INFINITY;
-            }
-            const float2 pr = make_float2(ex2(y.x), ex2(y.y));
-            const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(ud[cc]), __uint_as_float(ud[cc + 1])), nd2));
-            pp[(k >> 1) + u2] = pack_bf16x2(pr.x, pr.y);
-            dd[c * 8 + (k >> 1) + u2] = pack_bf16x2(ds.x, ds.y);
+        for (int u2 = 0; u2 < 2; ++u2) {
+          const int cc = col + 2 * u2;
+          const float2 nl2 = u2 ? make_float2(nl4.z, nl4.w) : make_float2(nl4.x, nl4.y);
+          float2 y = __ffma2_rn(make_float2(__uint_as_float(u[cc]), __uint_as_float(u[cc + 1])), sl2, nl2);
+          if (part) {
+            const int i = q0 + cc;
+            if (!(jk <= i && se_j >= i)) y.x = -INFINITY;
+            if (!(jk <= i + 1 && se_j >= i + 1)) y.y = -INFINITY;
           }
+          u[cc] = __float_as_uint(ex2(y.x));
+          u[cc + 1] = __float_as_uint(ex2(y.y));
         }
-        // packed P^T columns 8c..8c+7 of this half lie in score columns
-        // already read
-        tmem_st8(tmem + s_col + c * 8, pp);
       }
-      // dS^T(j-1) must have been read by its dK MMA and its store
-      if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars[C_PSF], (j - 1) & 1, abort_flag, p.err))) {
+      // dS = P (dP - Delta) once dP^T(j) is in TMEM
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[C_DPF], j & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
+      fence_after_sync();
+      uint32_t ud[64];
+      tmem_ld32(tmem + dp_col, ud);
+      tmem_ld32(tmem + dp_col + 32, ud + 32);
+      tmem_ld_wait();
+      uint32_t pp[32], dd[32];           // P and dS of the 64 columns, packed bf16 pairs
 #pragma unroll
-      for (int c = 0; c < 8; ++c)          // 16-byte chunk index of dS^T row t
-        st_swizzled8(dst_tile, t, half * 8 + c, make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]));
+      for (int col = 0; col < 64; col += 4) {
+        const float4 nd4 = *reinterpret_cast<const float4*>(nd_s + col);
+#pragma unroll
+        for (int u2 = 0; u2 < 2; ++u2) {
+          const int cc = col + 2 * u2;
+          const float2 nd2 = u2 ? make_float2(nd4.z, nd4.w) : make_float2(nd4.x, nd4.y);
+          const float2 pr = make_float2(__uint_as_float(u[cc]), __uint_as_float(u[cc + 1]));
+          const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(ud[cc]), __uint_as_float(ud[cc + 1])), nd2));
+          pp[cc >> 1] = pack_bf16x2(pr.x, pr.y);
+          dd[cc >> 1] = pack_bf16x2(ds.x, ds.y);
+        }
+      }
+      // P^T over the dP^T columns just read, dS^T over the S^T columns
+      tmem_st32(tmem + dp_col, pp);
+      tmem_st32(tmem + s_col, dd);
+      // dS^T row of this key to the (pair, head) slot: blocks 8 half .. 8 half + 7
+      if (pr_j >= 0 && pr_j < p.cap) {
+        uint8_t* tile = p.ds + ((size_t)pr_j * p.slot_heads + gl * p.G + j % p.G) * kDsTileBytes +
+                        (size_t)(half * 8) * kDsBlock + t * 16;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(tile + c * kDsBlock) =
+              make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]);
+      } else if (lane == 0) {
+        atomicOr(p.err, kErrCapacity);
+      }
       tmem_st_wait();
-      fence_proxy_async_smem();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C_DR]);
@@ -786,48 +824,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     }
-  } else {
-    // ------------------------------------------------ dS^T store (warp 8)
-    regs_dec<kBwdRegsCtl>();
-    if (warp == 8 && lane == 0 && run) {
-      const int32_t* pairs = p.csc_pair + ((size_t)r * p.NT + kt) * p.NT;
-      for (int j = 0; j < n_it; ++j) {
-        if (!mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err)) break;
-        const int pair = pairs[j / p.G], h = g * p.G + j % p.G;
-        if (pair < 0 || pair >= p.cap) {
-          atomicOr(p.err, kErrCapacity);
-        } else {
-          bulk_store(p.ds + ((size_t)pair * p.Hq + h) * kDsTileBytes, dst_tile, (uint32_t)kDsTileBytes);
-          bulk_commit();
-        }
-        bulk_wait_read0();
-        mbar_arrive(&bars[C_PSF]);
-      }
-      bulk_wait_all0();
-    }
-    __syncwarp();
   }
 
   __syncwarp();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 13) tmem_dealloc(tmem, 512);
+  if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
 struct DqParams {
   int R, T, Hq, Hkv, NT, G, nquad;
   int g0, ng;           // kv heads [g0, g0 + ng) of this launch
-  int64_t cap;
+  int slot_heads;       // query heads per pair in a dS slot
+  int64_t cap;          // dS pairs per slot
   const int32_t* csr_cnt;
   const int32_t* csr;
   const int32_t* csr_off;
   const int32_t* row_base;
-  const uint8_t* ds;
+  const uint8_t* ds;    // this launch's slot: [pair][slot_heads] dS^T tiles
   __nv_bfloat16* dq;
   float scale;
   uint32_t* err;
 };
+
+// No-swizzle shared-memory descriptor of a dS^T tile used as the MN-major A
+// operand of the dQ product (M = queries, K = keys): 8 x 16-byte core
+// matrices, 2048 bytes apart along M (stride-dimension offset) and 128 bytes
+// apart along K (leading-dimension offset).
+__device__ __forceinline__ uint64_t ds_desc(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(128u >> 4) << 16) |
+         ((uint64_t)(uint32_t(kDsBlock) >> 4) << 32) | (1ull << 46);
+}
 
 enum { Q_KF = 0, Q_KE = 2, Q_DF = 4, Q_DE = 8, Q_DONE = 12, Q_DRAIN = 13, Q_COUNT = 14 };
 // shared memory: [K0 | K1 | dS0 .. dS3] (1024-aligned) [barriers ...]
@@ -852,7 +880,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   int rem = blockIdx.x % per_qt;
   const int r = rem / (p.ng * p.nquad);
   rem %= p.ng * p.nquad;
-  const int g = p.g0 + rem / p.nquad, quad = rem % p.nquad;
+  const int gl = rem / p.nquad, quad = rem % p.nquad;  // kv head within this launch
+  const int g = p.g0 + gl;
   const int h0 = g * p.G + 4 * quad;
   const int nh = min(4, p.G - 4 * quad);
   const int cnt = p.csr_cnt[(size_t)r * p.NT + qt];
@@ -905,7 +934,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           break;
         }
         mbar_expect_tx(&bars[Q_DF + sd], (uint32_t)kDsTileBytes);
-        bulk_load(big + (2 + sd) * kTileBytes, p.ds + ((size_t)pair * p.Hq + h0 + hh) * kDsTileBytes,
+        bulk_load(big + (2 + sd) * kTileBytes,
+                  p.ds + ((size_t)pair * p.slot_heads + gl * p.G + 4 * quad + hh) * kDsTileBytes,
                   (uint32_t)kDsTileBytes, &bars[Q_DF + sd]);
         issued_d[sd] = d >> 2;
       }
@@ -935,10 +965,11 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           break;
         }
         fence_after_sync();
-        const uint32_t ds_mn = desc_lo_mnmajor(big_s + (2 + sd) * kTileBytes);
+        // slice kk = keys 16 kk .. 16 kk + 15: two core matrices along K, 256 bytes further
+        const uint64_t ds_a = ds_desc(big_s + (2 + sd) * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss_lo(tmem + hh * 128, ds_mn + mn(kk), k_mn + mn(kk), id_nn, (e > 0 || kk > 0));
+          mma_ss_a64(tmem + hh * 128, ds_a + (uint64_t)(kk * 16), k_mn + mn(kk), id_nn, (e > 0 || kk > 0));
         mma_commit(&bars[Q_DE + sd]);
       }
       if (ok) mma_commit(&bars[Q_KE + sk]);
@@ -1059,7 +1090,6 @@ namespace {
 // created on first use, handed out round-robin so that backward calls made
 // from different caller streams do not serialize on the same ones.  Every
 // enqueue sequence that uses the pool holds g_bwd_mu.
-constexpr int kBwdGroups = 8;   // kv-head groups of one backward call, at most
 constexpr int kBwdPool = 16;
 struct BwdStreams {
   bool ready = false;
@@ -1100,6 +1130,7 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
   bwd_delta_kernel<<<2048, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.o_in),
                                         static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.delta,
                                         a.nlse2, a.R, a.T, a.Hq);
+  const BwdGroups grp = bwd_groups(a.Hq, a.Hkv, a.ds_slots);
   BwdParams p;
   p.R = a.R;
   p.T = a.T;
@@ -1107,6 +1138,7 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
   p.Hkv = a.Hkv;
   p.NT = a.T / 128;
   p.G = a.Hq / a.Hkv;
+  p.slot_heads = grp.group_heads;
   p.scale_log2 = a.scale * kLog2e;
   p.scale = a.scale;
   p.cap = a.ds_cap;
@@ -1116,7 +1148,6 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
   p.csc_pair = a.csc_pair;
   p.nlse2 = a.nlse2;
   p.ndelta = a.delta;
-  p.ds = static_cast<uint8_t*>(a.ds);
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.err = a.err;
@@ -1128,12 +1159,12 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
   q.NT = p.NT;
   q.G = p.G;
   q.nquad = (p.G + 3) / 4;
+  q.slot_heads = grp.group_heads;
   q.cap = a.ds_cap;
   q.csr_cnt = a.csr_cnt;
   q.csr = a.csr;
   q.csr_off = a.csr_off;
   q.row_base = a.row_base;
-  q.ds = static_cast<const uint8_t*>(a.ds);
   q.dq = static_cast<__nv_bfloat16*>(a.dq);
   q.scale = a.scale;
   q.err = a.err;
@@ -1145,10 +1176,12 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  // The kv heads in up to kBwdGroups groups, each on its own stream: a group's
-  // dQ pass (HBM-bound) starts as soon as that group's dK/dV kernel is done
-  // and runs while the other groups compute.
-  const int n_groups = p.Hkv < kBwdGroups ? p.Hkv : kBwdGroups;
+  // The kv heads in grp.n groups, each on its own stream: a group's dQ pass
+  // (HBM-bound) starts as soon as that group's dK/dV kernel is done and runs
+  // while the other groups compute.  Group gi keeps its dS tiles in slot
+  // gi % slots; when slots < groups, it first waits for the dQ pass of group
+  // gi - slots, the slot's previous user.
+  const int n_groups = grp.n, slots = grp.slots;
   std::lock_guard<std::mutex> lock(g_bwd_mu);
   BwdStreams* bs = nullptr;
   if (n_groups > 1) {
@@ -1157,17 +1190,22 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
     e = cudaEventRecord(bs->fork, s);
     if (e != cudaSuccess) return e;
   }
+  int stream_of[kBwdGroups] = {};
   for (int gi = 0; gi < n_groups; ++gi) {
     const int g0 = gi * p.Hkv / n_groups, g1 = (gi + 1) * p.Hkv / n_groups;
     cudaStream_t sg = s;
     const int slot = n_groups > 1 ? (bs->next + gi) % kBwdPool : 0;
+    stream_of[gi] = slot;
     if (n_groups > 1) {
       sg = bs->s[slot];
       cudaError_t e = cudaStreamWaitEvent(sg, bs->fork, 0);
+      if (e == cudaSuccess && gi >= slots) e = cudaStreamWaitEvent(sg, bs->join[stream_of[gi - slots]], 0);
       if (e != cudaSuccess) return e;
     }
     p.g0 = q.g0 = g0;
     p.ng = q.ng = g1 - g0;
+    p.ds = static_cast<uint8_t*>(a.ds) + (size_t)(gi % slots) * a.ds_slot_bytes;
+    q.ds = p.ds;
     bwd_tc_kernel<<<(unsigned)(p.NT * p.R * p.ng), kBwdThreads, kBwdSmem, sg>>>(mq, mk, mv, mdo, p);
     dq_tc_kernel<<<(unsigned)(p.NT * p.R * q.ng * q.nquad), kDqThreads, kDqSmem, sg>>>(mk, q);
     if (n_groups > 1) {

@@ -248,8 +248,9 @@ extern "C" stp_status stp_workspace_size(const stp_attn_desc* desc, size_t* tile
   if (tile_meta_bytes) *tile_meta_bytes = tile_meta_layout(desc->n_rows, NT).total;
   if (fwd_ws_bytes) *fwd_ws_bytes = 256;
   if (bwd_ws_bytes)
-    *bwd_ws_bytes = bwd_ws_layout(desc->n_rows, desc->row_len, desc->n_q_heads, desc->dtype == STP_BF16,
-                                  pair_capacity(desc->n_rows, NT, desc->max_tile_pairs))
+    *bwd_ws_bytes = bwd_ws_layout(desc->n_rows, desc->row_len, desc->n_q_heads, desc->n_kv_heads,
+                                  desc->dtype == STP_BF16, pair_capacity(desc->n_rows, NT, desc->max_tile_pairs),
+                                  desc->ds_groups)
                         .total;
   return STP_OK;
 }

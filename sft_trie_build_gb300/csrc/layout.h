@@ -22,9 +22,11 @@
 // fwd workspace: err (uint32) only.
 // bwd workspace: err, delta float32 [R][Hq][T] (Delta on the float32 path,
 // -Delta on the bf16 path), and for the bf16 path nlse2 float32 [R][Hq][T]
-// (-LSE * log2 e) and ds, one bf16 128 x 128 tile of dS^T per (pair, query
-// head), pair-major, each stored as the backward kernel's shared-memory image
-// (two 64-query halves of [128 keys][64 queries], 128-byte swizzled).
+// (-LSE * log2 e) and ds: `slots` slots, each holding one bf16 128 x 128
+// tile of dS^T per (pair, query head of one kv-head group), pair-major; a
+// tile is 16 blocks of 2048 bytes, block c holding query columns 8c..8c+7 of
+// the 128 keys, 16 bytes per key.  The backward runs its kv heads in at most
+// kBwdGroups groups; a slot serves one group at a time.
 #pragma once
 
 #include <cstddef>
@@ -83,17 +85,35 @@ inline int64_t pair_capacity(int64_t R, int64_t NT, int64_t max_tile_pairs) {
   return max_tile_pairs > 0 ? max_tile_pairs : R * NT * (NT + 1) / 2;
 }
 
+// Groups of whole kv heads of one backward call (each launched on its own
+// stream): n = min(Hkv, kBwdGroups) groups, group i holding kv heads
+// [i Hkv / n, (i + 1) Hkv / n); `group_heads` query heads at most per group.
+constexpr int kBwdGroups = 8;
+struct BwdGroups {
+  int n, group_heads, slots;
+};
+inline BwdGroups bwd_groups(int Hq, int Hkv, int ds_groups) {
+  BwdGroups b;
+  b.n = Hkv < kBwdGroups ? Hkv : kBwdGroups;
+  b.group_heads = ((Hkv + b.n - 1) / b.n) * (Hq / Hkv);
+  b.slots = (ds_groups <= 0 || ds_groups > b.n) ? b.n : ds_groups;
+  return b;
+}
+
 struct BwdWs {
-  size_t err, delta, nlse2, ds, total;
+  size_t err, delta, nlse2, ds, slot_bytes, total;
 };
 
-inline BwdWs bwd_ws_layout(int64_t R, int64_t T, int64_t Hq, bool tensor_path, int64_t cap_pairs) {
+inline BwdWs bwd_ws_layout(int64_t R, int64_t T, int64_t Hq, int64_t Hkv, bool tensor_path, int64_t cap_pairs,
+                           int ds_groups) {
   BwdWs w;
+  const BwdGroups b = bwd_groups((int)Hq, (int)Hkv, ds_groups);
   size_t o = 0;
   w.err = o;    o += 256;
   w.delta = o;  o += align256(size_t(R * Hq * T) * 4);
   w.nlse2 = o;  o += tensor_path ? align256(size_t(R * Hq * T) * 4) : 0;
-  w.ds = o;     o += tensor_path ? size_t(cap_pairs) * size_t(Hq) * kDsTileBytes : 0;
+  w.slot_bytes = size_t(cap_pairs) * size_t(b.group_heads) * kDsTileBytes;
+  w.ds = o;     o += tensor_path ? size_t(b.slots) * w.slot_bytes : 0;
   w.total = o;
   return w;
 }

@@ -30,8 +30,10 @@ struct AttnArgs {
   const int32_t* csc_pair;
   float* delta;          // [R, Hq, T] (backward): Delta (fp32 path) or -Delta (bf16 path)
   float* nlse2;          // [R, Hq, T] (backward, bf16 path): -LSE * log2 e
-  void* ds;              // [pairs][Hq] bf16 dS^T tiles (backward, bf16 path)
-  int64_t ds_cap;        // pairs the ds buffer holds
+  void* ds;              // dS^T tile slots (backward, bf16 path)
+  int64_t ds_cap;        // pairs a slot holds
+  int ds_slots;          // slots (kv-head groups whose tiles are held at once)
+  size_t ds_slot_bytes;  // bytes per slot
   uint32_t* err;         // device error word of the workspace
 };
 

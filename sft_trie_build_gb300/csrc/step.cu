@@ -102,8 +102,10 @@ stp_status step_layout(const stp_attn_desc* d, int n_chunks, StepLayout& L) {
   c.dv = o;     o += kb;
   c.fwd_ws = o; o += align256(fws);
   c.bwd_ws = o; o += align256(bws);
-  c.bwd_err = c.bwd_ws + bwd_ws_layout(d->n_rows, d->row_len, L.cd.n_q_heads, d->dtype == STP_BF16,
-                                       pair_capacity(d->n_rows, d->row_len / kTile, d->max_tile_pairs))
+  c.bwd_err = c.bwd_ws + bwd_ws_layout(d->n_rows, d->row_len, L.cd.n_q_heads, L.cd.n_kv_heads,
+                                       d->dtype == STP_BF16,
+                                       pair_capacity(d->n_rows, d->row_len / kTile, d->max_tile_pairs),
+                                       L.cd.ds_groups)
                              .err;
   c.size = o;
   L.head = 256;

@@ -247,6 +247,16 @@ __device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint
       "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kDescHi));
 }
 
+// mma with a full 64-bit A descriptor and B given by its low word (high word kDescHi).
+__device__ __forceinline__ void mma_ss_a64(uint32_t d_tmem, uint64_t a_desc, uint32_t b_lo, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %5};\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, db, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kDescHi));
+}
+
 // Arrives on `bar` once every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(

@@ -67,7 +67,7 @@ class AttnDesc(ctypes.Structure):
                 ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("block_m", ctypes.c_int32), ("block_n", ctypes.c_int32),
-                ("max_tile_pairs", ctypes.c_int32)]
+                ("max_tile_pairs", ctypes.c_int32), ("ds_groups", ctypes.c_int32)]
 
 
 _lib = None
@@ -267,11 +267,12 @@ class Desc:
     dtype: int = STP_BF16
     scale: float = 0.0
     max_tile_pairs: int = 0   # 0 = every lower-triangular tile pair
+    ds_groups: int = 0        # kv-head groups whose dS tiles the backward holds at once (0 = all)
 
     def c(self) -> AttnDesc:
         sc = self.scale if self.scale > 0 else self.head_dim ** -0.5
         return AttnDesc(self.n_rows, self.row_len, self.n_q_heads, self.n_kv_heads, self.head_dim,
-                        self.dtype, sc, 128, 128, self.max_tile_pairs)
+                        self.dtype, sc, 128, 128, self.max_tile_pairs, self.ds_groups)
 
 
 def _pool(tokens, offsets, trainable, family):

@@ -160,6 +160,27 @@ def test_workspace_sizes_and_descriptor_checks(stp_lib):
             stp.stp_workspace_size(bad)
         assert e.value.status == code
     stp.stp_workspace_size(stp.Desc(1, 256, 1, 1, 64, stp.STP_FP32))
+    with pytest.raises(stp.StpError) as e:
+        stp.stp_workspace_size(stp.Desc(1, 1024, 8, 2, 128, stp.STP_BF16, ds_groups=-1))
+    assert e.value.status == stp.STP_EINVAL
+
+
+def test_bwd_workspace_bounded_by_groups_held(stp_lib):
+    """The dS part of the bf16 backward workspace scales with the kv-head
+    groups held at once (ds_groups), not with Hq: the deep 32K-row shape
+    (64 / 8 heads, 17605 tile pairs) needs 36.9 GB with every group's tiles
+    held, 4.6 GB per group."""
+    pairs, tile = 17605, 128 * 128 * 2
+    full = stp.stp_workspace_size(stp.Desc(1, 32768, 64, 8, 128, stp.STP_BF16, 0.0, pairs))[2]
+    per_group = pairs * 8 * tile
+    assert full >= 8 * per_group
+    for k in (1, 2, 4, 8, 100):
+        ws = stp.stp_workspace_size(stp.Desc(1, 32768, 64, 8, 128, stp.STP_BF16, 0.0, pairs, ds_groups=k))[2]
+        assert ws - full == (min(k, 8) - 8) * per_group
+    # more kv heads than groups: group i holds kv heads [i Hkv / 8, (i + 1) Hkv / 8)
+    a = stp.stp_workspace_size(stp.Desc(1, 1024, 32, 16, 128, stp.STP_BF16, 0.0, 10, ds_groups=1))[2]
+    b = stp.stp_workspace_size(stp.Desc(1, 1024, 32, 16, 128, stp.STP_BF16, 0.0, 10, ds_groups=2))[2]
+    assert b - a == 10 * 2 * 2 * tile
 
 
 def test_useful_pairs_match_oracle_visible_sets(stp_lib):
