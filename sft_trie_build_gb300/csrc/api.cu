@@ -127,8 +127,9 @@ extern "C" stp_status stp_attn_bwd(const stp_attn_desc* desc, const void* q, con
                                 desc->dtype == STP_BF16, cap, desc->ds_groups);
   char* ws = static_cast<char*>(d_ws);
   a.err = reinterpret_cast<uint32_t*>(ws + w.err);
-  a.delta = reinterpret_cast<float*>(ws + w.delta);
-  a.nlse2 = desc->dtype == STP_BF16 ? reinterpret_cast<float*>(ws + w.nlse2) : nullptr;
+  a.delta = desc->dtype == STP_BF16 ? nullptr : reinterpret_cast<float*>(ws + w.delta);
+  a.sbias = desc->dtype == STP_BF16 ? ws + w.sbias : nullptr;
+  a.dbias = desc->dtype == STP_BF16 ? ws + w.dbias : nullptr;
   a.ds = desc->dtype == STP_BF16 ? ws + w.ds : nullptr;
   a.ds_cap = cap;
   a.ds_slots = bwd_groups(desc->n_q_heads, desc->n_kv_heads, desc->ds_groups).slots;

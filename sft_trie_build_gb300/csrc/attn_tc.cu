@@ -450,32 +450,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 // all iterations; each iteration's dS^T tile also goes out to the workspace
 // slot of its (pair, head), for the dQ kernel.
 // Tensor memory (512 columns, keys on lanes):
-//   0..127    S^T = K Q^T (f32); once read, dS^T as packed bf16 pairs over
-//             the first 32 columns of each 64-query half;
-//   128..255  dP^T = V dO^T (f32); once read, P^T as packed bf16 pairs over
-//             the first 32 columns of each half;
+//   0..127    S^T = K Q^T (f32);
+//   128..255  dP^T = V dO^T (f32); once read, P^T and dS^T as packed bf16
+//             pairs: per 64-query half, P^T over its first 32 columns and
+//             dS^T over the next 32;
 //   256..383  dV += P^T dO (A from TMEM);  384..511  dK += dS^T Q (A from TMEM).
-// Neither P^T nor dS^T passes through shared memory: next to a stream of
-// MMAs whose operands are both in shared memory, shared-memory stores of the
-// elementwise warps wait hundreds of cycles each, so dS^T goes to TMEM for
-// the dK product and straight from registers to global memory for dQ, in a
-// layout where each warp's 16-byte stores are contiguous.
-// 12 warps:
+// The row terms of the softmax backward ride on the tensor core: one more
+// K = 16 slice per product, a column of ones against a bias tile, adds
+// -LSE_i / scale to every score of query i and -Delta_i to every dP, so the
+// elementwise pass needs no per-query constants (p = 2^(s' scale log2e),
+// dS = p dP'); each bias is split into three bf16 terms (hi + mid + lo,
+// about 24 significant bits), written per query tile by the Delta pass.
+// The S^T columns are free as soon as the elementwise pass has loaded them,
+// so S^T of the iteration after next is computed while that pass runs, and
+// the tensor core's order is dK(j), dV(j), dP^T(j+1), S^T(j+2): the pass of
+// j+1 starts with its scores already in TMEM, computes its exponentials
+// while dK(j) and dV(j) run, and waits only for dP^T(j+1).  Neither P^T nor
+// dS^T goes through shared memory (next to MMAs whose operands are both in
+// shared memory, shared-memory stores wait hundreds of cycles each), and the
+// elementwise warps do not store dS^T to global memory either: a store
+// warpgroup copies it from TMEM to the workspace while the next pass runs.
+// 16 warps:
 //   warps 0-7   elementwise, one thread per key (= TMEM lane); warps 0-3 take
-//               query columns 0..63, warps 4-7 columns 64..127.  As soon as
-//               S^T(j) is in TMEM: p = 2^(s scale log2e - LSE_i log2e)
-//               (masked on PARTIAL tiles with the thread's own
-//               subtree_end[j]); once dP^T(j) is: dS = p (dP - Delta_i);
-//               P^T and dS^T back to TMEM, dS^T to the workspace;
-//   warp 8      TMA: K, V once; Q (with -LSE log2e and -Delta) and dO of each
-//               iteration through two 2-stage rings;
-//   warp 9      MMA issue and TMEM owner.  After the elementwise pass of j:
-//               dK(j) (reads dS^T(j) in the S^T columns), S^T(j+1) (over
-//               them), dV(j) (reads P^T(j) in the dP^T columns), dP^T(j+1)
-//               (over them).  The pass of j+1 starts its exponentials as soon
-//               as S^T(j+1) lands, while the tensor core runs dV(j) and
-//               dP^T(j+1).
-//   warps 10-11 no role (a full warpgroup for the register split).
+//               query columns 0..63, warps 4-7 columns 64..127:
+//               p = 2^(s' scale log2e) (masked on PARTIAL tiles with the
+//               thread's own subtree_end[j]), then once dP^T(j) is in TMEM
+//               dS = p dP'; P^T and dS^T back to TMEM;
+//   warp 8      TMA: K, V once; Q with its score bias tile and dO with its dP
+//               bias tile, per iteration, through two 2-stage rings;
+//   warp 9      MMA issue and TMEM owner;
+//   warps 10-11 no role (a full warpgroup for the register split);
+//   warps 12-15 dS^T store: TMEM -> registers -> the (pair, head) slot, in a
+//               layout where each warp's 16-byte stores are contiguous.
 // dK (times scale) and dV leave TMEM once at the end.
 //
 // dS^T tile layout in the workspace (bf16, 32 KiB per (pair, head)): 16
@@ -505,8 +511,8 @@ struct BwdParams {
   const int32_t* csc_cnt;
   const int32_t* csc;
   const int32_t* csc_pair;
-  const float* nlse2;   // -LSE * log2 e
-  const float* ndelta;  // -Delta
+  const uint8_t* sbias; // [R][Hq][NT] bias tiles of the scores (-LSE / scale)
+  const uint8_t* dbias; // [R][Hq][NT] bias tiles of dP (-Delta)
   uint8_t* ds;          // this launch's slot: [pair][slot_heads] dS^T tiles
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -515,23 +521,33 @@ struct BwdParams {
 };
 
 enum {
-  C_KV = 0, C_QF = 1, C_QE = 3, C_DF = 5, C_DE = 7, C_SF = 9, C_DPF = 10, C_DR = 11, C_DONE = 12,
-  C_DRAIN = 13, C_COUNT = 14
+  C_KV = 0, C_QF = 1, C_QE = 3, C_DF = 5, C_DE = 7, C_SF = 9, C_SR = 10, C_DPF = 11, C_DR = 12, C_DSR = 13,
+  C_DONE = 14, C_DRAIN = 15, C_COUNT = 16
 };
 // shared memory: [K | V | Q0 | Q1 | dO0 | dO1] (1024-aligned, at the start of
-// dynamic shared memory) [vec0 | vec1] [barriers ...]
+// dynamic shared memory) [SB0 | SB1 | DB0 | DB1 | ONES] (4 KiB each: bias
+// tiles of the two ring stages, and the ones operand) [barriers ...]
 constexpr int kBwdBigBytes = 6 * kTileBytes;
-constexpr int kBwdVecBytes = 2 * 2 * 128 * 4;  // per stage: -LSE log2e and -Delta, 128 each
-constexpr int kBwdSmem = kBwdBigBytes + kBwdVecBytes + kSmallBytes;
+constexpr int kBwdBiasBytes = 5 * (int)kBiasTileBytes;
+constexpr int kBwdSmem = kBwdBigBytes + kBwdBiasBytes + kSmallBytes;
 static_assert(kBwdSmem <= kSmemLimit, "backward shared memory");
 constexpr int kDsBlock = 128 * 16;  // one 8-query block of a dS^T tile: 16 bytes per key
-// 12 warps x 168 registers at launch, rebalanced with setmaxnreg:
-// 256 x 216 (elementwise) + 128 x 72 (control) <= 384 x 168, and per SM
-// sub-partition (warps w, w+4, w+8) 216 + 216 + 72 <= 512.
-constexpr int kBwdThreads = 384;
+
+// Bias tile and ones operand: [128 rows][16] bf16, K-major without swizzle:
+// 8 x 16-byte core matrices, 128 bytes apart along K (leading-dimension
+// offset) and 256 bytes apart along the rows (stride-dimension offset); row
+// q, column k at byte (q / 8) 256 + (k / 8) 128 + (q % 8) 16 + (k % 8) 2.
+__device__ __forceinline__ uint64_t bias_desc(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(128u >> 4) << 16) | ((uint64_t)(256u >> 4) << 32) |
+         (1ull << 46);
+}
+// 16 warps x 128 registers at launch, rebalanced with setmaxnreg:
+// 128 x (192 + 192 (elementwise) + 56 (control) + 72 (store)) = 65536, and per
+// SM sub-partition (warps w, w+4, w+8, w+12) 512.
+constexpr int kBwdThreads = 512;
 constexpr int kBwdPrefetch = 2;  // iterations ahead for the L2 prefetch of Q, dO
-constexpr int kBwdRegsMath = 216, kBwdRegsCtl = 72;
-static_assert(256 * kBwdRegsMath + 128 * kBwdRegsCtl <= kBwdThreads * 168, "register split");
+constexpr int kBwdRegsMath = 192, kBwdRegsCtl = 56, kBwdRegsStore = 72;
+static_assert(128 * (2 * kBwdRegsMath + kBwdRegsCtl + kBwdRegsStore) <= kBwdThreads * 128, "register split");
 
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -540,8 +556,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* big = smem_raw;
   const uint32_t big_s = smem_u32(smem_raw);
-  float* vec = reinterpret_cast<float*>(smem_raw + kBwdBigBytes);  // [stage][-LSE log2e 128 | -Delta 128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + kBwdBigBytes + kBwdVecBytes);
+  uint8_t* bias = smem_raw + kBwdBigBytes;   // SB0 SB1 DB0 DB1 ONES
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + kBwdBigBytes + kBwdBiasBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t k_s = big_s, v_s = big_s + kTileBytes;
@@ -554,18 +570,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int g = p.g0 + gl;
   const int cnt = p.csc_cnt[(size_t)r * p.NT + kt];
   const int32_t* list = p.csc + ((size_t)r * p.NT + kt) * p.NT;
+  const int32_t* pairs = p.csc_pair + ((size_t)r * p.NT + kt) * p.NT;
   const int n_it = cnt * p.G;
   const int row0 = r * p.T;
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < C_COUNT; ++b)
-      mbar_init(&bars[b], b == C_DR ? 8 : 1);  // C_DR: one arrival per elementwise warp
+      // C_SR, C_DR: one arrival per elementwise warp; C_DSR: per store warp
+      mbar_init(&bars[b], (b == C_SR || b == C_DR) ? 8 : (b == C_DSR ? 4 : 1));
     *abort_flag = 0;
     if ((big_s & 1023u) != 0 || cnt <= 0 || cnt > p.NT) {
       *abort_flag = 1;
       atomicOr(p.err, (big_s & 1023u) != 0 ? kErrTmem : kErrBadList);
     }
     fence_mbar_init();
+  }
+  {
+    // the ones operand [128 keys][16]: 1 in columns 0-2 (bias tile layout)
+    const int e = threadIdx.x;  // one 16-byte row chunk per thread: 256 chunks
+    if (e < 256) {
+      const int key = e >> 1, kc = e & 1;
+      const uint32_t one = 0x3F80u;  // bf16 1.0
+      const uint4 v = kc ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(one | (one << 16), one, 0u, 0u);
+      *reinterpret_cast<uint4*>(bias + 4 * kBiasTileBytes + (key >> 3) * 256 + kc * 128 + (key & 7) * 16) = v;
+      fence_proxy_async_smem();
+    }
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
@@ -577,7 +606,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const bool run = !*abort_flag;
 
-  if (warp >= 8) {
+  if (warp >= 8 && warp < 12) {
     regs_dec<kBwdRegsCtl>();
     if (warp == 8 && lane == 0 && run) {
       // ---------------------------------------------------------- producer
@@ -614,18 +643,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         // Q (and the per-query vectors) of j: the stage frees once dK(j-2) is done
         if (j >= 2 && !mbar_wait(&bars[C_QE + st], (n - 1) & 1, abort_flag, p.err)) break;
-        mbar_expect_tx(&bars[C_QF + st], kTileBytes + 2 * 128 * 4);
-        float* vs = vec + st * 256;
-        const size_t at = ((size_t)r * p.Hq + h) * p.T + qt * 128;
-        bulk_load(vs, p.nlse2 + at, 512, &bars[C_QF + st]);
-        bulk_load(vs + 128, p.ndelta + at, 512, &bars[C_QF + st]);
+        const size_t bt = (((size_t)r * p.Hq + h) * p.NT + qt) * kBiasTileBytes;
+        mbar_expect_tx(&bars[C_QF + st], kTileBytes + (uint32_t)kBiasTileBytes);
+        bulk_load(bias + st * kBiasTileBytes, p.sbias + bt, (uint32_t)kBiasTileBytes, &bars[C_QF + st]);
         for (int hf = 0; hf < 2; ++hf)
           tma_load_3d(big + (2 + st) * kTileBytes + hf * kHalfTile, &tq, &bars[C_QF + st], hf * 64, h,
                       row0 + qt * 128);
         issued_q[st] = n;
         // dO of j: the stage frees once dV(j-2) is done
         if (j >= 2 && !mbar_wait(&bars[C_DE + st], (n - 1) & 1, abort_flag, p.err)) break;
-        mbar_expect_tx(&bars[C_DF + st], kTileBytes);
+        mbar_expect_tx(&bars[C_DF + st], kTileBytes + (uint32_t)kBiasTileBytes);
+        bulk_load(bias + (2 + st) * kBiasTileBytes, p.dbias + bt, (uint32_t)kBiasTileBytes, &bars[C_DF + st]);
         for (int hf = 0; hf < 2; ++hf)
           tma_load_3d(big + (4 + st) * kTileBytes + hf * kHalfTile, &tdo, &bars[C_DF + st], hf * 64, h,
                       row0 + qt * 128);
@@ -647,57 +675,72 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t kStage = kTileBytes >> 4;  // one tile further in the ring
       auto km = [](int kk) { return (uint32_t)((kk >> 2) * (kHalfTile >> 4) + (kk & 3) * 2); };
       auto mn = [](int kk) { return (uint32_t)(kk * 128); };
-      // packed columns of query columns 16 kk .. 16 kk + 15 (first 32 columns of each half)
-      auto pk = [](int kk) { return (uint32_t)(kk < 4 ? kk * 8 : 64 + (kk - 4) * 8); };
-      bool ok = mbar_wait(&bars[C_KV], 0, abort_flag, p.err);
-      if (ok && n_it > 0) {
-        ok = mbar_wait(&bars[C_QF], 0, abort_flag, p.err);
+      // packed P^T columns of query columns 16 kk .. 16 kk + 15 (dS^T: 32 further)
+      auto pk = [](int kk) { return (uint32_t)(128 + (kk >> 2) * 64 + (kk & 3) * 8); };
+      const uint32_t bias_s = smem_u32(bias);
+      const uint64_t ones = bias_desc(bias_s + 4 * (uint32_t)kBiasTileBytes);
+      auto issue_s = [&](int jj) {  // S^T(jj) = K Q(jj)^T, plus -LSE / scale per query
+        const uint32_t so = (jj & 1) ? kStage : 0;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, k_km + km(kk), q_km0 + so + km(kk), id_kk, kk > 0);
+        mma_ss(tmem, ones, bias_desc(bias_s + (jj & 1) * (uint32_t)kBiasTileBytes), id_kk, 1);
+        mma_commit(&bars[C_SF]);
+      };
+      auto issue_dp = [&](int jj) {  // dP^T(jj) = V dO(jj)^T, minus Delta per query
+        const uint32_t so = (jj & 1) ? kStage : 0;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km0 + so + km(kk), id_kk, kk > 0);
+        mma_ss(tmem + 128, ones, bias_desc(bias_s + (2 + (jj & 1)) * (uint32_t)kBiasTileBytes), id_kk, 1);
+        mma_commit(&bars[C_DPF]);
+      };
+      bool ok = mbar_wait(&bars[C_KV], 0, abort_flag, p.err) && mbar_wait(&bars[C_QF], 0, abort_flag, p.err);
+      if (ok) {
+        fence_after_sync();
+        issue_s(0);
+        ok = mbar_wait(&bars[C_DF], 0, abort_flag, p.err);
+      }
+      if (ok) {
+        fence_after_sync();
+        issue_dp(0);
+      }
+      // S^T(1) once the pass of 0 has loaded S^T(0)
+      if (ok && n_it > 1) {
+        ok = mbar_wait(&bars[C_SR], 0, abort_flag, p.err) && mbar_wait(&bars[C_QF + 1], 0, abort_flag, p.err);
         if (ok) {
           fence_after_sync();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, k_km + km(kk), q_km0 + km(kk), id_kk, kk > 0);
-          mma_commit(&bars[C_SF]);
-          ok = mbar_wait(&bars[C_DF], 0, abort_flag, p.err);
-        }
-        if (ok) {
-          fence_after_sync();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km0 + km(kk), id_kk, kk > 0);
-          mma_commit(&bars[C_DPF]);
+          issue_s(1);
         }
       }
 #pragma unroll 1
       for (int j = 0; ok && j < n_it; ++j) {
-        const int st = j & 1, st1 = (j + 1) & 1;
-        const uint32_t so = st ? kStage : 0, so1 = st ? 0 : kStage;
-        const bool next = j + 1 < n_it;
+        const int st = j & 1;
+        const uint32_t so = st ? kStage : 0;
         if (!mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err)) break;
         fence_after_sync();
-        // dK += dS^T Q, dS^T(j) in the S^T columns
+        // dK += dS^T Q and dV += P^T dO, both read from the dP^T columns
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts_lo(tmem + 384, tmem + pk(kk), q_mn0 + so + mn(kk), id_kn, (j > 0 || kk > 0));
+          mma_ts_lo(tmem + 384, tmem + pk(kk) + 32, q_mn0 + so + mn(kk), id_kn, (j > 0 || kk > 0));
         mma_commit(&bars[C_QE + st]);
-        // S^T(j+1) over them
-        if (next) {
-          if (!mbar_wait(&bars[C_QF + st1], ((j + 1) >> 1) & 1, abort_flag, p.err)) break;
-          fence_after_sync();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem, k_km + km(kk), q_km0 + so1 + km(kk), id_kk, kk > 0);
-          mma_commit(&bars[C_SF]);
-        }
-        // dV += P^T dO, P^T(j) in the dP^T columns
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts_lo(tmem + 256, tmem + 128 + pk(kk), do_mn0 + so + mn(kk), id_kn, (j > 0 || kk > 0));
+          mma_ts_lo(tmem + 256, tmem + pk(kk), do_mn0 + so + mn(kk), id_kn, (j > 0 || kk > 0));
         mma_commit(&bars[C_DE + st]);
-        // dP^T(j+1) over them
-        if (next) {
-          if (!mbar_wait(&bars[C_DF + st1], ((j + 1) >> 1) & 1, abort_flag, p.err)) break;
+        // dP^T(j+1) over them, once the store warps hold dS^T(j)
+        if (j + 1 < n_it) {
+          if (!mbar_wait(&bars[C_DSR], j & 1, abort_flag, p.err) ||
+              !mbar_wait(&bars[C_DF + ((j + 1) & 1)], ((j + 1) >> 1) & 1, abort_flag, p.err))
+            break;
           fence_after_sync();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss_lo(tmem + 128, v_km + km(kk), do_km0 + so1 + km(kk), id_kk, kk > 0);
-          mma_commit(&bars[C_DPF]);
+          issue_dp(j + 1);
+        }
+        // S^T(j+2) once the pass of j+1 has loaded S^T(j+1)
+        if (j + 2 < n_it) {
+          if (!mbar_wait(&bars[C_SR], (j + 1) & 1, abort_flag, p.err) ||
+              !mbar_wait(&bars[C_QF + st], ((j + 2) >> 1) & 1, abort_flag, p.err))
+            break;
+          fence_after_sync();
+          issue_s(j + 2);
         }
       }
       if (ok) mma_commit(&bars[C_DONE]);
@@ -705,6 +748,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_wait_drain(&bars[C_DRAIN], 0);
     }
     __syncwarp();
+  } else if (warp >= 12) {
+    // ------------------------------------------------ dS^T store (warps 12-15)
+    regs_dec<kBwdRegsStore>();
+    const int t = threadIdx.x & 127;     // key row = TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = run;
+    for (int j = 0; ok && j < n_it; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[C_DR], j & 1, abort_flag, p.err))) break;
+      fence_after_sync();
+      const int pr_j = pairs[j / p.G];
+      uint32_t d0[32], d1[32];           // dS^T of query columns 0..63 and 64..127
+      tmem_ld32(tmem + lane_base + 128 + 32, d0);
+      tmem_ld32(tmem + lane_base + 192 + 32, d1);
+      tmem_ld_wait();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C_DSR]);
+      if (pr_j >= 0 && pr_j < p.cap) {
+        uint8_t* tile = p.ds + ((size_t)pr_j * p.slot_heads + gl * p.G + j % p.G) * kDsTileBytes + t * 16;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(tile + c * kDsBlock) = make_uint4(d0[4 * c], d0[4 * c + 1], d0[4 * c + 2], d0[4 * c + 3]);
+          *reinterpret_cast<uint4*>(tile + (8 + c) * kDsBlock) =
+              make_uint4(d1[4 * c], d1[4 * c + 1], d1[4 * c + 2], d1[4 * c + 3]);
+        }
+      } else if (lane == 0) {
+        atomicOr(p.err, kErrCapacity);
+      }
+    }
   } else {
     // ------------------------------------------------ per-key elementwise
     regs_inc<kBwdRegsMath>();
@@ -715,40 +787,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_col = lane_base + half * 64, dp_col = lane_base + 128 + half * 64;
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
-    const int32_t* pairs = p.csc_pair + ((size_t)r * p.NT + kt) * p.NT;
     bool ok = run;
     int ent = run ? list[0] : 0;
-    int pair = run ? pairs[0] : 0;
     for (int j = 0; ok && j < n_it; ++j) {
-      const int st = j & 1;
-      const int qt = ent >> 1, part = ent & 1, pr_j = pair;
-      if (j + 1 < n_it) {
-        ent = list[(j + 1) / p.G];
-        pair = pairs[(j + 1) / p.G];
-      }
+      const int qt = ent >> 1, part = ent & 1;
+      if (j + 1 < n_it) ent = list[(j + 1) / p.G];
       const int q0 = qt * 128 + half * 64;
-      const float* nl_s = vec + st * 256 + half * 64;   // -LSE log2 e per query column
-      const float* nd_s = nl_s + 128;                   // -Delta per query column
-      const bool ready = mbar_wait(&bars[C_QF + st], (j >> 1) & 1, abort_flag, p.err) &&
-                         mbar_wait(&bars[C_SF], j & 1, abort_flag, p.err);
-      if (!__all_sync(0xffffffffu, ready)) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars[C_SF], j & 1, abort_flag, p.err))) {
         ok = false;
         break;
       }
       fence_after_sync();
-      // P from S^T: 64 query columns of this half
+      // P from S^T: 64 query columns of this half; the S^T columns are free
+      // for S^T(j+2) once loaded
       uint32_t u[64];
       tmem_ld32(tmem + s_col, u);
       tmem_ld32(tmem + s_col + 32, u + 32);
       tmem_ld_wait();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C_SR]);
 #pragma unroll
       for (int col = 0; col < 64; col += 4) {
-        const float4 nl4 = *reinterpret_cast<const float4*>(nl_s + col);
 #pragma unroll
         for (int u2 = 0; u2 < 2; ++u2) {
           const int cc = col + 2 * u2;
-          const float2 nl2 = u2 ? make_float2(nl4.z, nl4.w) : make_float2(nl4.x, nl4.y);
-          float2 y = __ffma2_rn(make_float2(__uint_as_float(u[cc]), __uint_as_float(u[cc + 1])), sl2, nl2);
+          float2 y = __fmul2_rn(make_float2(__uint_as_float(u[cc]), __uint_as_float(u[cc + 1])), sl2);
           if (part) {
             const int i = q0 + cc;
             if (!(jk <= i && se_j >= i)) y.x = -INFINITY;
@@ -771,31 +835,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t pp[32], dd[32];           // P and dS of the 64 columns, packed bf16 pairs
 #pragma unroll
       for (int col = 0; col < 64; col += 4) {
-        const float4 nd4 = *reinterpret_cast<const float4*>(nd_s + col);
 #pragma unroll
         for (int u2 = 0; u2 < 2; ++u2) {
           const int cc = col + 2 * u2;
-          const float2 nd2 = u2 ? make_float2(nd4.z, nd4.w) : make_float2(nd4.x, nd4.y);
           const float2 pr = make_float2(__uint_as_float(u[cc]), __uint_as_float(u[cc + 1]));
-          const float2 ds = __fmul2_rn(pr, __fadd2_rn(make_float2(__uint_as_float(ud[cc]), __uint_as_float(ud[cc + 1])), nd2));
+          const float2 ds = __fmul2_rn(pr, make_float2(__uint_as_float(ud[cc]), __uint_as_float(ud[cc + 1])));
           pp[cc >> 1] = pack_bf16x2(pr.x, pr.y);
           dd[cc >> 1] = pack_bf16x2(ds.x, ds.y);
         }
       }
-      // P^T over the dP^T columns just read, dS^T over the S^T columns
+      // P^T and dS^T over the dP^T columns just read
       tmem_st32(tmem + dp_col, pp);
-      tmem_st32(tmem + s_col, dd);
-      // dS^T row of this key to the (pair, head) slot: blocks 8 half .. 8 half + 7
-      if (pr_j >= 0 && pr_j < p.cap) {
-        uint8_t* tile = p.ds + ((size_t)pr_j * p.slot_heads + gl * p.G + j % p.G) * kDsTileBytes +
-                        (size_t)(half * 8) * kDsBlock + t * 16;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(tile + c * kDsBlock) =
-              make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]);
-      } else if (lane == 0) {
-        atomicOr(p.err, kErrCapacity);
-      }
+      tmem_st32(tmem + dp_col + 32, dd);
       tmem_st_wait();
       fence_before_sync();
       __syncwarp();
@@ -1011,15 +1062,29 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// Delta[r,h,i] = sum_d dO . O (bf16 in, f32 out); one warp per (row, token, head).
+// Delta[r,h,i] = sum_d dO . O (bf16 in, f32), one warp per (row, token, head);
+// writes the two bias tiles of the token's query tile: -LSE_i / scale and
+// -Delta_i, each as three bf16 terms (hi, mid, lo: hi = bf16(x), mid =
+// bf16(x - hi), lo = bf16(x - hi - mid)) in columns 0-2 of the query's row,
+// zeros elsewhere (layout of bias_desc).
+__device__ __forceinline__ uint4 bias_row(float x) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+  return make_uint4((uint32_t)__bfloat16_as_ushort(hi) | ((uint32_t)__bfloat16_as_ushort(mid) << 16),
+                    (uint32_t)__bfloat16_as_ushort(lo), 0u, 0u);
+}
+
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
                                                         const __nv_bfloat16* __restrict__ dout,
                                                         const float* __restrict__ lse,
-                                                        float* __restrict__ ndelta,
-                                                        float* __restrict__ nlse2, int R, int T,
-                                                        int Hq) {
+                                                        uint8_t* __restrict__ sbias,
+                                                        uint8_t* __restrict__ dbias, float inv_scale, int R,
+                                                        int T, int Hq) {
   const int lane = threadIdx.x & 31;
   const size_t rows = (size_t)R * T * Hq;
+  const int NT = T / 128;
   for (size_t w = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < rows; w += (size_t)gridDim.x * 8) {
     const uint2 a = reinterpret_cast<const uint2*>(o + w * 128)[lane];
     const uint2 b = reinterpret_cast<const uint2*>(dout + w * 128)[lane];
@@ -1033,13 +1098,17 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
     }
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane == 0) {
+    if (lane < 2) {
       const int h = (int)(w % Hq);
       const size_t ri = w / Hq;
       const size_t rr = ri / T, i = ri - rr * T;
-      const size_t at = (rr * Hq + h) * T + i;
-      ndelta[at] = -acc;
-      nlse2[at] = -lse[at] * kLog2e;
+      const size_t tile = ((rr * Hq + h) * NT + i / 128) * kBiasTileBytes;
+      const int q = (int)(i & 127);
+      const size_t at = tile + (q >> 3) * 256 + (q & 7) * 16;
+      uint8_t* dst = lane == 0 ? sbias : dbias;
+      const float x = lane == 0 ? -lse[(rr * Hq + h) * T + i] * inv_scale : -acc;
+      *reinterpret_cast<uint4*>(dst + at) = bias_row(x);
+      *reinterpret_cast<uint4*>(dst + at + 128) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
 }
@@ -1128,8 +1197,9 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
       !make_map(&mv, a.v, rows, a.Hkv) || !make_map(&mdo, a.dout, rows, a.Hq))
     return cudaErrorInvalidValue;
   bwd_delta_kernel<<<2048, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.o_in),
-                                        static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.delta,
-                                        a.nlse2, a.R, a.T, a.Hq);
+                                        static_cast<const __nv_bfloat16*>(a.dout), a.lse,
+                                        static_cast<uint8_t*>(a.sbias), static_cast<uint8_t*>(a.dbias),
+                                        1.f / a.scale, a.R, a.T, a.Hq);
   const BwdGroups grp = bwd_groups(a.Hq, a.Hkv, a.ds_slots);
   BwdParams p;
   p.R = a.R;
@@ -1146,8 +1216,8 @@ cudaError_t tc_bwd(const AttnArgs& a, cudaStream_t s) {
   p.csc_cnt = a.csc_cnt;
   p.csc = a.csc;
   p.csc_pair = a.csc_pair;
-  p.nlse2 = a.nlse2;
-  p.ndelta = a.delta;
+  p.sbias = static_cast<const uint8_t*>(a.sbias);
+  p.dbias = static_cast<const uint8_t*>(a.dbias);
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.err = a.err;

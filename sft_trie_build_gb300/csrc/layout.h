@@ -20,9 +20,11 @@
 // pairs are numbered query-tile major, key tiles ascending, rows in any order.
 //
 // fwd workspace: err (uint32) only.
-// bwd workspace: err, delta float32 [R][Hq][T] (Delta on the float32 path,
-// -Delta on the bf16 path), and for the bf16 path nlse2 float32 [R][Hq][T]
-// (-LSE * log2 e) and ds: `slots` slots, each holding one bf16 128 x 128
+// bwd workspace: err; on the float32 path delta float32 [R][Hq][T]; on the
+// bf16 path two bias tiles per (row, head, query tile), sbias and dbias
+// [R][Hq][NT] x 4 KiB (the row bias -LSE / scale of the scores and -Delta of
+// dP, each split into three bf16 terms, laid out as the B operand of one
+// K = 16 MMA: see bwd_delta_kernel), and ds: `slots` slots, each holding one bf16 128 x 128
 // tile of dS^T per (pair, query head of one kv-head group), pair-major; a
 // tile is 16 blocks of 2048 bytes, block c holding query columns 8c..8c+7 of
 // the 128 keys, 16 bytes per key.  The backward runs its kv heads in at most
@@ -100,8 +102,10 @@ inline BwdGroups bwd_groups(int Hq, int Hkv, int ds_groups) {
   return b;
 }
 
+constexpr size_t kBiasTileBytes = 4096;  // one query tile's bias: 128 queries x 16 bf16
+
 struct BwdWs {
-  size_t err, delta, nlse2, ds, slot_bytes, total;
+  size_t err, delta, sbias, dbias, ds, slot_bytes, total;
 };
 
 inline BwdWs bwd_ws_layout(int64_t R, int64_t T, int64_t Hq, int64_t Hkv, bool tensor_path, int64_t cap_pairs,
@@ -109,9 +113,11 @@ inline BwdWs bwd_ws_layout(int64_t R, int64_t T, int64_t Hq, int64_t Hkv, bool t
   BwdWs w;
   const BwdGroups b = bwd_groups((int)Hq, (int)Hkv, ds_groups);
   size_t o = 0;
+  const size_t bias = size_t(R * Hq * (T / kTile)) * kBiasTileBytes;
   w.err = o;    o += 256;
-  w.delta = o;  o += align256(size_t(R * Hq * T) * 4);
-  w.nlse2 = o;  o += tensor_path ? align256(size_t(R * Hq * T) * 4) : 0;
+  w.delta = o;  o += tensor_path ? 0 : align256(size_t(R * Hq * T) * 4);
+  w.sbias = o;  o += tensor_path ? bias : 0;
+  w.dbias = o;  o += tensor_path ? bias : 0;
   w.slot_bytes = size_t(cap_pairs) * size_t(b.group_heads) * kDsTileBytes;
   w.ds = o;     o += tensor_path ? size_t(b.slots) * w.slot_bytes : 0;
   w.total = o;

@@ -28,8 +28,9 @@ struct AttnArgs {
   const int32_t* csr_off;   // pair numbering of stp_classify (tile_meta)
   const int32_t* row_base;
   const int32_t* csc_pair;
-  float* delta;          // [R, Hq, T] (backward): Delta (fp32 path) or -Delta (bf16 path)
-  float* nlse2;          // [R, Hq, T] (backward, bf16 path): -LSE * log2 e
+  float* delta;          // [R, Hq, T] (backward, fp32 path): Delta
+  void* sbias;           // [R, Hq, NT] bias tiles of the scores (backward, bf16 path)
+  void* dbias;           // [R, Hq, NT] bias tiles of dP (backward, bf16 path)
   void* ds;              // dS^T tile slots (backward, bf16 path)
   int64_t ds_cap;        // pairs a slot holds
   int ds_slots;          // slots (kv-head groups whose tiles are held at once)
