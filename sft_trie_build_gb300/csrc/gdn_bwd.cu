@@ -10,16 +10,19 @@
 //           (T = (I + A)^{-1}), then through Q~, K~, P, A, U^ and W to dq, dk,
 //           dv, dbeta and dgam, and dg = the reverse cumulative sum of dgam
 //   tokens: through the unit-norm q, k heads, SiLU and the path convolution.
-// Three kernels, float32 on the CUDA cores throughout:
+// Three kernels:
 //   gdn_bwd_walk_kernel   one launch per depth, deepest first; one CTA per
 //                         (segment, head) walks its chunks last to first with
-//                         the state gradient in shared memory, starting from
-//                         the sum of its children's initial-state gradients.
+//                         the state gradient in TMEM, starting from the sum
+//                         of its children's start gradients; both products
+//                         per chunk on the tensor core (tcgen05).
 //   gdn_bwd_chunk_kernel  one CTA per (chunk, head): everything above that
-//                         needs only the chunk and its two state (gradient)s.
+//                         needs only the chunk and its two state (gradient)s,
+//                         its contractions on the tensor core (tcgen05).
 //   gdn_bwd_token_kernel  one block per (64 tokens, q / k / v head): the
 //                         convolution's input gradient (scattered to the
 //                         path's previous tokens) and weight gradient.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -28,9 +31,12 @@
 #include "gdn_common.h"
 #include "internal.h"
 #include "layout.h"
+#include "tc_ptx.cuh"
 
 namespace stp {
 namespace {
+
+using namespace tc;
 
 constexpr int kD = kGdnD, kC = kGdnChunk;
 constexpr int kBT = 256;   // threads of every backward kernel
@@ -68,154 +74,457 @@ struct GbParams {
   float* dconv_w;            // [C, 4]
   float* dg;                 // [N, H]
   float* dbeta;              // [N, H]
+  uint32_t* err;             // device error word of the workspace
 };
 
-__device__ __forceinline__ float bf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+typedef CUresult (*EncodeFnB)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-// C (M x N) = sum_{k < K} A(m, k) B(k, n) by 256 threads on a 16 x 16 grid;
-// each thread holds rows tm + 16 i and columns tn + 16 j and hands every
-// result to store(m, n, value).  The (m, n) -> thread map depends on M and
-// N only, so passes of the same shape may read-modify-write their outputs.
-template <int M, int N, typename FA, typename FB, typename FS>
-__device__ __forceinline__ void bgemm(int K, FA A, FB B, FS store) {
-  constexpr int RM = M / 16, RN = N / 16;
-  const int tm = threadIdx.x >> 4, tn = threadIdx.x & 15;
-  float acc[RM][RN];
-#pragma unroll
-  for (int i = 0; i < RM; ++i)
-#pragma unroll
-    for (int j = 0; j < RN; ++j) acc[i][j] = 0.f;
-#pragma unroll 8   // loads of eight k steps in flight: the operands mostly come from L2
-  for (int k = 0; k < K; ++k) {
-    float a[RM], b[RN];
-#pragma unroll
-    for (int i = 0; i < RM; ++i) a[i] = A(tm + 16 * i, k);
-#pragma unroll
-    for (int j = 0; j < RN; ++j) b[j] = B(k, tn + 16 * j);
-#pragma unroll
-    for (int i = 0; i < RM; ++i)
-#pragma unroll
-      for (int j = 0; j < RN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-  }
-#pragma unroll
-  for (int i = 0; i < RM; ++i)
-#pragma unroll
-    for (int j = 0; j < RN; ++j) store(tm + 16 * i, tn + 16 * j, acc[i][j]);
+EncodeFnB encode_bwd() {
+  static EncodeFnB fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* q = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) ==
+            cudaSuccess &&
+        r == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFnB>(q);
+  });
+  return fn;
+}
+
+// [rows, cols] bf16 as a 2-D tensor; boxes of 64 columns x box_rows rows, 128-byte swizzled.
+bool map_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, int box_rows) {
+  EncodeFnB enc = encode_bwd();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// MN-major 128-byte-swizzled operand whose 64-element halves lie 8 KB apart.
+__device__ __forceinline__ uint32_t desc_lo_mn8k(uint32_t addr) {
+  return ((addr & 0x3FFFFu) >> 4) | ((8192u >> 4) << 16);
 }
 
 // ---------------------------------------------------------------------------
-// Reverse walk of one (segment, head).
-constexpr int kWalkSmem = (2 * kD * kD + kC * kD) * 4 + (3 * kC * kD + kC * kC) * 2;
+// Reverse walk of one (segment, head) on the tensor core.  The state gradient
+// dS [d_k lanes][d_v columns] lives in TMEM (float32, columns 0-127) for the
+// whole segment, starting from the sum of the children's start gradients;
+// per chunk, last to first:
+//   E1  dS (= dS_n of this chunk) goes out (transposed, for the chunk pass),
+//       becomes the bf16 operand DSB, and is decayed in place by e^{gam_n};
+//       the chunk's dO rows become bf16 rows 0-63 of DOV;
+//   M1  dV' = P^T dO + K~ dS_n into columns 128-255 (rows = the chunk's
+//       tokens; lanes 64-127 see padding rows and are not read);
+//   E2  dV' goes out (transposed) and -dV' becomes rows 64-127 of DOV;
+//   M2  dS += [Q~^T | W^T] [dO ; -dV']  (the [Q~; W] tile read MN-major).
+// The segment's start gradient dS0 goes out at the end.
+// Warps 0-3 epilogue (thread = TMEM lane), warp 4 loads ([Q~; W], K~, P of
+// the next chunk into the other of two stages), warp 5 MMA and TMEM owner.
+// Global layouts written here (each warp's stores contiguous): dS_n of a
+// chunk and a segment's dS0 as [d_v][d_k], dV' of a chunk as [d_v][64].
+constexpr int kWkThreads = 192;
+constexpr int kWkStage = 57344;                  // [Q~; W] 32 KB | K~ 16 KB | P 8 KB
+constexpr int kWkOffKt = 32768, kWkOffP = 49152;
+constexpr int kWkOffDsb = 2 * kWkStage;          // dS_n bf16 [128 d_k][128 d_v], MN-major B
+constexpr int kWkOffDov = kWkOffDsb + 32768;     // [dO ; -dV'] bf16 [128][128], MN-major B
+constexpr int kWkOffBar = kWkOffDov + 32768;
+constexpr int kWkSmem = kWkOffBar + 256 + 1024;
+enum { W_F = 0, W_E = 2, W_E1 = 4, W_M1 = 5, W_E2 = 6, W_M2 = 7, W_DRAIN = 8, W_COUNT = 9 };
 
-__global__ void __launch_bounds__(kBT, 1) gdn_bwd_walk_kernel(const GbParams p) {
-  extern __shared__ float wsm[];
-  float* dS = wsm;                       // [128][128]
-  float* dSn = dS + kD * kD;             // [128][128]
-  float* sdVp = dSn + kD * kD;           // [64][128]
-  __nv_bfloat16* sQt = reinterpret_cast<__nv_bfloat16*>(sdVp + kC * kD);   // [64][128]
-  __nv_bfloat16* sW = sQt + kC * kD;     // [64][128]
-  __nv_bfloat16* sKt = sW + kC * kD;     // [64][128]
-  __nv_bfloat16* sP = sKt + kC * kD;     // [64][64]
-  const int tid = threadIdx.x;
+// Writes 8 bf16 (columns 8c .. 8c+7 of row `row`) into a 128-byte-swizzled
+// tile of `rows` rows whose two 64-column halves are rows * 128 bytes apart.
+__device__ __forceinline__ void st_sw8(uint8_t* tile, int rows, int row, int c, uint4 v) {
+  uint8_t* half = tile + (c >> 3) * rows * 128;
+  *reinterpret_cast<uint4*>(half + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = v;
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+__global__ void __launch_bounds__(kWkThreads, 1)
+    gdn_bwd_walk_kernel(const __grid_constant__ CUtensorMap mwq, const __grid_constant__ CUtensorMap mkt,
+                        const __grid_constant__ CUtensorMap mpm, const GbParams p) {
+  extern __shared__ uint8_t wsm_dyn[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(wsm_dyn) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kWkOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + W_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int seg = p.seg0 + (int)(blockIdx.x / p.H), h = (int)(blockIdx.x % p.H);
   const int c0 = p.seg_chunk0[seg], nck = (p.seg_len[seg] + kC - 1) / kC;
 
-  // the segment's end: the sum of its children's initial-state gradients
-  const int k0 = p.child_off[seg], k1 = p.child_off[seg + 1];
-  for (int e = tid; e < kD * kD; e += kBT) {
-    float a = 0.f;
-    for (int c = k0; c < k1; ++c) a += p.sgrad[((size_t)p.child[c] * p.H + h) * kD * kD + e];
-    dS[e] = a;
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < W_COUNT; ++b) mbar_init(&bars[b], b == W_E1 ? 4 : b == W_E2 ? 2 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-  for (int i = nck - 1; i >= 0; --i) {
-    const int c = c0 + i, L = p.chunk_len[c], x0 = p.chunk_start[c];
-    const size_t row = (size_t)c * p.H + h;
-    const float dec = p.decay[row];
-    const uint4* wq4 = reinterpret_cast<const uint4*>(p.wq + row * 128 * kD);
-    const uint4* kt4 = reinterpret_cast<const uint4*>(p.kt + row * kC * kD);
-    const uint4* pm4 = reinterpret_cast<const uint4*>(p.pm + row * kC * kC);
-    for (int e = tid; e < kC * kD / 8; e += kBT) {
-      reinterpret_cast<uint4*>(sQt)[e] = wq4[e];
-      reinterpret_cast<uint4*>(sW)[e] = wq4[kC * kD / 8 + e];
-      reinterpret_cast<uint4*>(sKt)[e] = kt4[e];
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 256);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ loads
+      tma_prefetch_desc(&mwq);
+      tma_prefetch_desc(&mkt);
+      tma_prefetch_desc(&mpm);
+      int last[2] = {-1, -1};
+      for (int n = 0; n < nck; ++n) {   // n-th chunk processed = chunk nck - 1 - n
+        const int st = n & 1;
+        if (n >= 2 && !mbar_wait(&bars[W_E + st], ((n >> 1) - 1) & 1, abort_flag, p.err)) break;
+        const int row = (c0 + nck - 1 - n) * p.H + h;
+        uint8_t* stage = sm + st * kWkStage;
+        mbar_expect_tx(&bars[W_F + st], 32768 + 16384 + 8192);
+        tma_load_2d(stage, &mwq, &bars[W_F + st], 0, row * 128);
+        tma_load_2d(stage + 16384, &mwq, &bars[W_F + st], 64, row * 128);
+        tma_load_2d(stage + kWkOffKt, &mkt, &bars[W_F + st], 0, row * kC);
+        tma_load_2d(stage + kWkOffKt + 8192, &mkt, &bars[W_F + st], 64, row * kC);
+        tma_load_2d(stage + kWkOffP, &mpm, &bars[W_F + st], 0, row * kC);
+        last[st] = (n >> 1) & 1;
+      }
+      for (int st = 0; st < 2; ++st)
+        if (last[st] >= 0) mbar_wait_drain(&bars[W_F + st], last[st]);
     }
-    for (int e = tid; e < kC * kC / 8; e += kBT) reinterpret_cast<uint4*>(sP)[e] = pm4[e];
-    __syncthreads();   // dS complete (children's sum or the previous chunk's dS0)
-    float4* de = reinterpret_cast<float4*>(p.dsend + row * kD * kD);
-    for (int e = tid; e < kD * kD / 4; e += kBT) de[e] = reinterpret_cast<const float4*>(dS)[e];
-    const float* dO = p.d_o + ((size_t)x0 * p.H + h) * kD;
-    const size_t dOs = (size_t)p.H * kD;   // token stride of dO
-    // dV' = P^T dO + K~ dS   (rows t >= L: P and K~ rows are zero)
-    float* gdvp = p.dvp + row * kC * kD;
-    bgemm<kC, kD>(
-        kC + kD,
-        [&](int m, int k) { return k < kC ? bf(sP + k * kC + m) : bf(sKt + m * kD + (k - kC)); },
-        [&](int k, int n) { return k < kC ? (k < L ? dO[k * dOs + n] : 0.f) : dS[(k - kC) * kD + n]; },
-        [&](int m, int n, float v) {
-          sdVp[m * kD + n] = v;
-          gdvp[m * kD + n] = v;
-        });
-    __syncthreads();
-    // dS0 = Q~^T dO + e^{gam_n} dS - W^T dV'
-    bgemm<kD, kD>(
-        2 * kC,
-        [&](int m, int k) { return k < kC ? bf(sQt + k * kD + m) : -bf(sW + (k - kC) * kD + m); },
-        [&](int k, int n) { return k < kC ? (k < L ? dO[k * dOs + n] : 0.f) : sdVp[(k - kC) * kD + n]; },
-        [&](int m, int n, float v) { dSn[m * kD + n] = v + dec * dS[m * kD + n]; });
-    __syncthreads();
-    float* t = dS;
-    dS = dSn;
-    dSn = t;
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA
+      constexpr uint32_t id_mnmn = idesc_bf16(128, 128, 1, 1);
+      constexpr uint32_t id_kmn = idesc_bf16(128, 128, 0, 1);
+      const uint32_t dsb = sb + kWkOffDsb, dov = sb + kWkOffDov;
+      for (int n = 0; n < nck; ++n) {
+        const int st = n & 1;
+        const uint32_t stage = sb + st * kWkStage;
+        if (!mbar_wait(&bars[W_F + st], (n >> 1) & 1, abort_flag, p.err)) break;
+        if (!mbar_wait(&bars[W_E1], n & 1, abort_flag, p.err)) break;
+        fence_after_sync();
+        // dV' = P^T dO (A = P read MN-major; its rows are the chunk's tokens) ...
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          mma_ss_lo(tmem + 128, desc_lo_mn8k(stage + kWkOffP + s * 2048), desc_lo_mnmajor(dov + s * 2048),
+                    id_mnmn, s > 0 ? 1u : 0u);
+        // ... + K~ dS_n (A = K~ K-major)
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          mma_ss_lo(tmem + 128, desc_lo_kmajor(stage + kWkOffKt + (s >> 2) * 8192 + (s & 3) * 32),
+                    desc_lo_mnmajor(dsb + s * 2048), id_kmn, 1u);
+        mma_commit(&bars[W_M1]);
+        if (!mbar_wait(&bars[W_E2], n & 1, abort_flag, p.err)) break;
+        fence_after_sync();
+        // dS += [Q~^T | W^T] [dO ; -dV']
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          mma_ss_lo(tmem, desc_lo_mnmajor(stage + s * 2048), desc_lo_mnmajor(dov + s * 2048), id_mnmn, 1u);
+        mma_commit(&bars[W_M2]);
+        mma_commit(&bars[W_E + st]);
+      }
+      mma_commit(&bars[W_DRAIN]);
+      mbar_wait_drain(&bars[W_DRAIN], 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int r = threadIdx.x;   // TMEM lane: d_k row of dS; token row of dV'
+    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    uint8_t* dsb = sm + kWkOffDsb;
+    uint8_t* dov = sm + kWkOffDov;
+    uint32_t v[32];
+    {   // the segment's end gradient: the sum of its children's start gradients
+      const int k0 = p.child_off[seg], k1 = p.child_off[seg + 1];
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          float a = 0.f;
+          for (int c = k0; c < k1; ++c)
+            a += p.sgrad[(((size_t)p.child[c] * p.H + h) * kD + cc * 32 + q) * kD + r];
+          v[q] = __float_as_uint(a);
+        }
+        tmem_st32(tmem + lrow + cc * 32, v);
+      }
+      tmem_st_wait();
+    }
+    bool ok = true;
+    for (int n = 0; ok && n < nck; ++n) {
+      const int c = c0 + nck - 1 - n, L = p.chunk_len[c], x0 = p.chunk_start[c];
+      const size_t row = (size_t)c * p.H + h;
+      const float dec = p.decay[row];
+      if (n > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[W_M2], (n - 1) & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+      }
+      // E1: dS_n out ([d_v][d_k]), to the bf16 operand, decayed in place
+      float* dse = p.dsend + row * kD * kD;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(tmem + lrow + cc * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 32; ++q) dse[(cc * 32 + q) * kD + r] = __uint_as_float(v[q]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st_sw8(dsb, 128, r, cc * 4 + j, pack8(reinterpret_cast<const float*>(v) + 8 * j));
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * dec);
+        tmem_st32(tmem + lrow + cc * 32, v);
+      }
+      // the chunk's dO rows: 64 rows x 16 chunks of 8 columns over the 128 threads
+      const float* dO = p.d_o + (size_t)x0 * p.H * kD + h * kD;
+#pragma unroll 2
+      for (int e = r; e < kC * 16; e += 128) {
+        const int t = e >> 4, c8 = e & 15;
+        float f[8];
+        if (t < L) {
+          const float4* src = reinterpret_cast<const float4*>(dO + (size_t)t * p.H * kD + c8 * 8);
+          const float4 a = src[0], b = src[1];
+          f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[k] = 0.f;
+        }
+        st_sw8(dov, 128, t, c8, pack8(f));
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[W_E1]);
+      // E2: dV' out ([d_v][64]) and -dV' into rows 64-127 of DOV
+      if (warp < 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[W_M1], n & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        float* dvo = p.dvp + row * kC * kD;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          tmem_ld32(tmem + 128 + lrow + cc * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 32; ++q) dvo[(cc * 32 + q) * kC + r] = __uint_as_float(v[q]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float f[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] = -__uint_as_float(v[8 * j + k]);
+            st_sw8(dov, 128, kC + r, cc * 4 + j, pack8(f));
+          }
+        }
+        fence_proxy_async_smem();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[W_E2]);
+      }
+    }
+    if (ok && (nck == 0 || __all_sync(0xffffffffu, mbar_wait(&bars[W_M2], (nck - 1) & 1, abort_flag, p.err)))) {
+      fence_after_sync();
+      // the segment's start gradient dS0 ([d_v][d_k])
+      float* sg = p.sgrad + ((size_t)seg * p.H + h) * kD * kD;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(tmem + lrow + cc * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 32; ++q) sg[(cc * 32 + q) * kD + r] = __uint_as_float(v[q]);
+      }
+    }
   }
-  float4* sg = reinterpret_cast<float4*>(p.sgrad + ((size_t)seg * p.H + h) * kD * kD);
-  for (int e = tid; e < kD * kD / 4; e += kBT) sg[e] = reinterpret_cast<const float4*>(dS)[e];
+
+  __syncwarp();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 5) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
-// Chunk-local gradients of one (chunk, head).
-constexpr int kChunkSmem = 8 * kC * kC * 4 + 6 * kC * 4;
+// Chunk-local gradients of one (chunk, head) on the tensor core.  With the
+// chunk's tokens t, s < L <= 64, gam = the in-chunk cumulative log decay,
+// Gam_ts = e^{gam_t - gam_s}, ek_t = e^{gam_{L-1} - gam_t}, B_U = diag(beta) V,
+// B_W = diag(beta e^gam) K, A_ts = beta_t Gam_ts k_t . k_s (s < t), T =
+// (I + A)^{-1}, and the walk's dS_n and dV' (dU^ = dV'):
+//   dQ~ = dO S0^T                   dW = -dV' S0^T        V' = U^ - W S0
+//   dK~ = V' dS_n^T                 dP = dO V'^T (s <= t)
+//   dT  = dV' B_U^T + dW B_W^T      dA = -lower(T^T dT T^T)
+//   dq  = scale e^gam dQ~ + scale (dP o Gam) K
+//   dk  = ek dK~ + scale (dP o Gam)^T Q + (M + M^T) K + beta e^gam T^T dW,
+//         M_ts = dA_ts beta_t Gam_ts
+//   dv  = beta T^T dV'
+// and the beta / gam terms of each factor (row and column sums of elementwise
+// products).  Each of dq, dk, dv is one TMEM accumulator: its first product
+// lands there and the others are added by MMAs whose A rows carry the row
+// factors (dq_t = scale e^{gam_t} (dQ~_t + sum_s e^{-gam_s} dP_ts k_s), dk_t =
+// ek_t (dK~_t + ...)), so nothing is re-read from memory.  Products with 64
+// rows run as M = 128 MMAs whose rows 64-127 read padding and are not used.
+// T comes from forward substitution on the CUDA cores.  One CTA of 128
+// threads (thread = TMEM lane), thread 0 issues the MMAs; the stages below
+// are separated by MMA commits and block barriers.
+constexpr int kCkThreads = 128;
+// shared memory (1024-aligned): bf16 operand tiles, 128-byte swizzled in
+// 64-column halves (half stride = rows x 128 bytes)
+constexpr int kCkYQ = 0, kCkYK = 16384, kCkYV = 32768;      // q^, k^, v [64][128]
+constexpr int kCkDODV = 49152;                                // [dO ; dV'] [128][128]
+constexpr int kCkVP = 81920, kCkDW = 98304;                   // V', dW [64][128]
+constexpr int kCkR = 114688;                                  // phase region
+constexpr int kCkS0 = kCkR, kCkDS = kCkR + 32768, kCkW = kCkR + 65536;   // S0, dS_n [128][128], W [64][128]
+constexpr int kCkTb = kCkR, kCkDT = kCkR + 8192, kCkYb = kCkR + 16384, kCkAq = kCkR + 24576,
+              kCkAa = kCkR + 32768, kCkAb = kCkR + 40960, kCkAc = kCkR + 49152;   // [64][64] tiles
+// float32 [64][64] scratch, element (r, c) at r * 64 + (c ^ (r % 32)) (conflict-free
+// rows and columns); F3 in the phase region, F4 over V' and F5 over v (both
+// read by the stage-B MMAs only), F1 (GK) and F2 (T) for the whole kernel
+constexpr int kCkF3 = kCkR + 57344, kCkF4 = kCkVP, kCkF5 = kCkYV;
+constexpr int kCkF1 = kCkR + 81920, kCkF2 = kCkF1 + 16384;
+constexpr int kCkSc = kCkF2 + 16384;                          // scalars: gam eg ek beta dgam dbeta misc [64] each
+constexpr int kCkBar = kCkSc + 7 * 64 * 4;
+constexpr int kCkSmem = kCkBar + 64;
+static_assert(kCkF3 + 16384 <= kCkF1 && kCkSmem <= 232448, "chunk kernel shared memory");
+__device__ __forceinline__ int fx(int r, int c) { return r * 64 + (c ^ (r & 31)); }
+enum { K_A = 0, K_B = 1, K_C = 2, K_D = 3, K_E = 4, K_COUNT = 5 };
 
-__global__ void __launch_bounds__(kBT, 1) gdn_bwd_chunk_kernel(const GbParams p) {
-  extern __shared__ float csm[];
-  float* sKK = csm;                 // each [64][64]
-  float* sQK = sKK + kC * kC;
-  float* sA = sQK + kC * kC;
-  float* sT = sA + kC * kC;
-  float* sdP = sT + kC * kC;
-  float* sdT = sdP + kC * kC;
-  float* sX = sdT + kC * kC;
-  float* sdA = sX + kC * kC;
-  float* gam = sdA + kC * kC;       // each [64]
-  float* bt = gam + kC;
-  float* eg = bt + kC;
-  float* ek = eg + kC;
-  float* dgam = ek + kC;
-  float* dbt = dgam + kC;
-  const int tid = threadIdx.x;
+// descriptor low words of operand tiles: K-major with `rows` rows (slice kk of
+// 16 columns), MN-major with `rows` rows = K (slice kk of 16 rows)
+__device__ __forceinline__ uint32_t kmaj(uint32_t base, int rows, int kk) {
+  return desc_lo_kmajor(base + (kk >> 2) * rows * 128 + (kk & 3) * 32);
+}
+__device__ __forceinline__ uint32_t mnmaj(uint32_t base, int rows, int kk) {
+  return ((base + kk * 2048) & 0x3FFFFu) >> 4 | (((uint32_t)(rows * 128) >> 4) << 16);
+}
+
+__global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbParams p) {
+  extern __shared__ __align__(1024) uint8_t csm[];
+  const uint32_t sb = smem_u32(csm);
+  float* F1 = reinterpret_cast<float*>(csm + kCkF1);   // GK_ts = Gam_ts k_t . k_s (s < t < L)
+  float* F2 = reinterpret_cast<float*>(csm + kCkF2);   // T
+  float* F3 = reinterpret_cast<float*>(csm + kCkF3);
+  float* F4 = reinterpret_cast<float*>(csm + kCkF4);
+  float* F5 = reinterpret_cast<float*>(csm + kCkF5);
+  float* gam = reinterpret_cast<float*>(csm + kCkSc);
+  float* eg = gam + 64;
+  float* ek = eg + 64;
+  float* bt = ek + 64;
+  float* dgam = bt + 64;
+  float* dbt = dgam + 64;
+  float* misc = dbt + 64;   // misc[0]: <dS_n, S0>
+  uint64_t* bars = reinterpret_cast<uint64_t*>(csm + kCkBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + K_COUNT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ch = (int)(blockIdx.x / p.H), h = (int)(blockIdx.x % p.H);
   const int x0 = p.chunk_start[ch], L = p.chunk_len[ch];
   const size_t row = (size_t)ch * p.H + h;
   const int Hd = p.H * kD;
   const float sc = p.scale;
-  const __nv_bfloat16* yq = p.y + (size_t)x0 * p.C + h * kD;
-  auto q = [&](int t, int k) { return t < L ? bf(yq + (size_t)t * p.C + k) : 0.f; };
-  auto kk = [&](int t, int k) { return t < L ? bf(yq + (size_t)t * p.C + Hd + k) : 0.f; };
-  auto vv = [&](int t, int k) { return t < L ? bf(yq + (size_t)t * p.C + 2 * Hd + k) : 0.f; };
-  const float* S0 = p.s0 + row * kD * kD;
-  const float* dSe = p.dsend + row * kD * kD;
-  const float* dVp = p.dvp + row * kC * kD;
-  const float* dOb = p.d_o + ((size_t)x0 * p.H + h) * kD;
-  const size_t dOs = (size_t)p.H * kD;
-  auto dO = [&](int t, int j) { return t < L ? dOb[t * dOs + j] : 0.f; };
-  const float* Uh = p.ut + row * kD * kC;   // U^[t][j] at j * 64 + t
-  const __nv_bfloat16* Wb = p.wq + (row * 128 + kC) * kD;
-  float* Vp = p.scr + row * 2 * kC * kD;
-  float* dW = Vp + kC * kD;
-  float* dq = p.dqkv + (size_t)x0 * p.C + h * kD;
-  float* dk = dq + Hd;
-  float* dv = dq + 2 * Hd;
+  const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+  // TMEM columns: dq 0-127, dk 128-255 (first V' = W S0), 256-319 KK then dP
+  // then dA', 320-383 R1 = dV' V^T, 384-447 R2 = dW K^T (320-447 later dv),
+  // 448-511 Y = T^T dT
+  constexpr uint32_t cDQ = 0, cDK = 128, cX = 256, cR1 = 320, cR2 = 384, cDV = 320, cY = 448;
 
-  if (tid < 32) {   // gam = inclusive prefix sum of g; beta; e^gam; e^{gam_n - gam}
+  if (tid == 0) {
+    for (int b = 0; b < K_COUNT; ++b) mbar_init(&bars[b], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  // ---- loads: q^ k^ v rows, [dO ; dV'], W (bf16 operand tiles); S0 and dS_n
+  // rows (thread = d_k row), with the decay term <dS_n, S0>
+  {
+    const __nv_bfloat16* y = p.y + (size_t)x0 * p.C + h * kD;
+    for (int e = tid; e < 64 * 16; e += kCkThreads) {
+      const int t = e >> 4, c8 = e & 15;
+      uint4 rq = make_uint4(0, 0, 0, 0), rk = rq, rv = rq, rw = rq;
+      if (t < L) {
+        const __nv_bfloat16* yr = y + (size_t)t * p.C + c8 * 8;
+        rq = *reinterpret_cast<const uint4*>(yr);
+        rk = *reinterpret_cast<const uint4*>(yr + Hd);
+        rv = *reinterpret_cast<const uint4*>(yr + 2 * Hd);
+      }
+      rw = *reinterpret_cast<const uint4*>(p.wq + (row * 128 + kC + t) * kD + c8 * 8);   // zero rows past L
+      st_sw8(csm + kCkYQ, 64, t, c8, rq);
+      st_sw8(csm + kCkYK, 64, t, c8, rk);
+      st_sw8(csm + kCkYV, 64, t, c8, rv);
+      st_sw8(csm + kCkW, 64, t, c8, rw);
+      float f[8];
+      if (t < L) {
+        const float4* src = reinterpret_cast<const float4*>(p.d_o + ((size_t)(x0 + t) * p.H + h) * kD + c8 * 8);
+        const float4 a = src[0], b = src[1];
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] = 0.f;
+      }
+      st_sw8(csm + kCkDODV, 128, t, c8, pack8(f));
+    }
+    // dV' rows from [d_v][64]: thread = token (lanes 0-63), the other half idle here
+    const float* dvp = p.dvp + row * kC * kD;
+    if (tid < 64) {
+#pragma unroll 1
+      for (int c8 = 0; c8 < 16; ++c8) {
+        float f[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] = dvp[(c8 * 8 + k) * kC + tid];
+        st_sw8(csm + kCkDODV, 128, kC + tid, c8, pack8(f));
+      }
+    }
+    // S0 row r (row-major [d_k][d_v]) and dS_n row r (stored [d_v][d_k])
+    const int r = tid;
+    const float* s0r = p.s0 + (row * kD + r) * kD;
+    const float* dse = p.dsend + row * kD * kD;
+    float dot = 0.f;
+#pragma unroll 1
+    for (int c8 = 0; c8 < 16; ++c8) {
+      const float4 a = reinterpret_cast<const float4*>(s0r)[2 * c8], b = reinterpret_cast<const float4*>(s0r)[2 * c8 + 1];
+      const float fs[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      float fd[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        fd[k] = dse[(c8 * 8 + k) * kD + r];
+        dot = fmaf(fs[k], fd[k], dot);
+      }
+      st_sw8(csm + kCkS0, 128, r, c8, pack8(fs));
+      st_sw8(csm + kCkDS, 128, r, c8, pack8(fd));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (tid < 64) {
+      dgam[tid] = 0.f;
+      dbt[tid] = 0.f;
+    }
+    if (tid == 0) misc[0] = 0.f;
+    __syncthreads();
+    if (lane == 0) atomicAdd(&misc[0], dot);
+  }
+  if (tid < 32) {   // gam = inclusive prefix sum of g over the chunk; beta; e^gam; e^{gam_{L-1} - gam}
     float a = tid < L ? p.g[(size_t)(x0 + tid) * p.H + h] : 0.f;
     float b = tid + 32 < L ? p.g[(size_t)(x0 + tid + 32) * p.H + h] : 0.f;
 #pragma unroll
@@ -234,144 +543,360 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_chunk_kernel(const GbParams p)
     eg[tid + 32] = expf(b);
     ek[tid] = expf(gl - a);
     ek[tid + 32] = expf(gl - b);
-  }
-  if (tid < kC) {
     bt[tid] = tid < L ? p.beta[(size_t)(x0 + tid) * p.H + h] : 0.f;
-    dgam[tid] = 0.f;
-    dbt[tid] = 0.f;
+    bt[tid + 32] = tid + 32 < L ? p.beta[(size_t)(x0 + tid + 32) * p.H + h] : 0.f;
   }
+  fence_proxy_async_smem();
+  fence_before_sync();
   __syncthreads();
-  // K K^T, Q K^T
-  bgemm<kC, kC>(kD, [&](int m, int k) { return kk(m, k); }, [&](int k, int n) { return kk(n, k); },
-                [&](int m, int n, float v) { sKK[m * kC + n] = v; });
-  bgemm<kC, kC>(kD, [&](int m, int k) { return q(m, k); }, [&](int k, int n) { return kk(n, k); },
-                [&](int m, int n, float v) { sQK[m * kC + n] = v; });
-  __syncthreads();
-  for (int e = tid; e < kC * kC; e += kBT) {
-    const int t = e / kC, s = e % kC;
-    sA[e] = (s < t && t < L) ? bt[t] * expf(gam[t] - gam[s]) * sKK[e] : 0.f;
-  }
-  __syncthreads();
-  if (tid < kC) {   // T = (I + A)^{-1}, column tid, by forward substitution
-    const int j = tid;
-    for (int t = 0; t < kC; ++t) {
-      float x = t == j ? 1.f : 0.f;
-      for (int s = j; s < t; ++s) x = fmaf(-sA[t * kC + s], sT[s * kC + j], x);
-      sT[t * kC + j] = x;
-    }
-  }
-  __syncthreads();
-  // V' = U^ - W S0
-  bgemm<kC, kD>(kD, [&](int m, int k) { return bf(Wb + m * kD + k); }, [&](int k, int n) { return S0[k * kD + n]; },
-                [&](int m, int n, float v) { Vp[m * kD + n] = Uh[n * kC + m] - v; });
-  __syncthreads();
-  // dP = dO V'^T;  dW = -dV' S0^T
-  bgemm<kC, kC>(kD, [&](int m, int k) { return dO(m, k); }, [&](int k, int n) { return Vp[n * kD + k]; },
-                [&](int m, int n, float v) { sdP[m * kC + n] = v; });
-  bgemm<kC, kD>(kD, [&](int m, int k) { return dVp[m * kD + k]; }, [&](int k, int n) { return S0[n * kD + k]; },
-                [&](int m, int n, float v) { dW[m * kD + n] = -v; });
-  __syncthreads();
-  // dT = dV' (beta V)^T + dW (beta e^gam K)^T
-  bgemm<kC, kC>(
-      2 * kD, [&](int m, int k) { return k < kD ? dVp[m * kD + k] : dW[m * kD + (k - kD)]; },
-      [&](int k, int n) { return k < kD ? bt[n] * vv(n, k) : bt[n] * eg[n] * kk(n, k - kD); },
-      [&](int m, int n, float v) { sdT[m * kC + n] = v; });
-  __syncthreads();
-  bgemm<kC, kC>(kC, [&](int m, int k) { return sT[k * kC + m]; }, [&](int k, int n) { return sdT[k * kC + n]; },
-                [&](int m, int n, float v) { sX[m * kC + n] = v; });
-  __syncthreads();
-  bgemm<kC, kC>(kC, [&](int m, int k) { return sX[m * kC + k]; }, [&](int k, int n) { return sT[n * kC + k]; },
-                [&](int m, int n, float v) { sdA[m * kC + n] = (n < m && m < L) ? -v : 0.f; });
-  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  if (tid == 0) atomicAdd(&dgam[L - 1], eg[L - 1] * misc[0]);   // decay term: e^{gam_{L-1}} <dS_n, S0>
 
-  // dq = scale e^gam dQ~ + scale (dP o Gamma) K, with dgam += dQ~ . Q~
-  bgemm<kC, kD>(kD, [&](int m, int k) { return dO(m, k); }, [&](int k, int n) { return S0[n * kD + k]; },
-                [&](int m, int n, float v) {
-                  if (m < L) {
-                    dq[(size_t)m * p.C + n] = sc * eg[m] * v;
-                    atomicAdd(&dgam[m], v * sc * eg[m] * q(m, n));
-                  }
-                });
-  bgemm<kC, kD>(
-      kC, [&](int m, int k) { return k <= m ? sc * sdP[m * kC + k] * expf(gam[m] - gam[k]) : 0.f; },
-      [&](int k, int n) { return kk(k, n); },
-      [&](int m, int n, float v) {
-        if (m < L) dq[(size_t)m * p.C + n] += v;
-      });
-  // dk = e^{gam_n - gam} dK~ (dK~ = V' dS_n^T), with the K~ terms of dgam
-  bgemm<kC, kD>(kD, [&](int m, int k) { return Vp[m * kD + k]; }, [&](int k, int n) { return dSe[n * kD + k]; },
-                [&](int m, int n, float v) {
-                  if (m < L) {
-                    dk[(size_t)m * p.C + n] = ek[m] * v;
-                    const float c = v * ek[m] * kk(m, n);
-                    atomicAdd(&dgam[m], -c);
-                    atomicAdd(&dgam[L - 1], c);
-                  }
-                });
-  // + scale (dP o Gamma)^T Q
-  bgemm<kC, kD>(
-      kC, [&](int m, int k) { return m <= k ? sc * sdP[k * kC + m] * expf(gam[k] - gam[m]) : 0.f; },
-      [&](int k, int n) { return q(k, n); },
-      [&](int m, int n, float v) {
-        if (m < L) dk[(size_t)m * p.C + n] += v;
-      });
-  // + the A terms: M = dA o E (E_ts = e^{gam_t - gam_s}, s < t); dk_t += beta_t M_t. K, dk_s += sum_t beta_t M_ts k_t
-  bgemm<kC, kD>(
-      kC, [&](int m, int k) { return k < m ? bt[m] * sdA[m * kC + k] * expf(gam[m] - gam[k]) : 0.f; },
-      [&](int k, int n) { return kk(k, n); },
-      [&](int m, int n, float v) {
-        if (m < L) dk[(size_t)m * p.C + n] += v;
-      });
-  bgemm<kC, kD>(
-      kC, [&](int m, int k) { return m < k ? bt[k] * sdA[k * kC + m] * expf(gam[k] - gam[m]) : 0.f; },
-      [&](int k, int n) { return kk(k, n); },
-      [&](int m, int n, float v) {
-        if (m < L) dk[(size_t)m * p.C + n] += v;
-      });
-  // + beta e^gam dB_W (dB_W = T^T dW), with its beta and gam terms
-  bgemm<kC, kD>(kC, [&](int m, int k) { return sT[k * kC + m]; }, [&](int k, int n) { return dW[k * kD + n]; },
-                [&](int m, int n, float v) {
-                  if (m < L) {
-                    const float km = kk(m, n);
-                    dk[(size_t)m * p.C + n] += bt[m] * eg[m] * v;
-                    atomicAdd(&dbt[m], eg[m] * v * km);
-                    atomicAdd(&dgam[m], bt[m] * eg[m] * v * km);
-                  }
-                });
-  // dv = beta dB_U (dB_U = T^T dV'), with its beta term
-  bgemm<kC, kD>(kC, [&](int m, int k) { return sT[k * kC + m]; }, [&](int k, int n) { return dVp[k * kD + n]; },
-                [&](int m, int n, float v) {
-                  if (m < L) {
-                    dv[(size_t)m * p.C + n] = bt[m] * v;
-                    atomicAdd(&dbt[m], v * vv(m, n));
-                  }
-                });
-  // the P and A terms of dgam, the A term of dbeta
-  for (int e = tid; e < kC * kC; e += kBT) {
-    const int t = e / kC, s = e % kC;
-    if (s <= t && t < L) {
-      const float E = expf(gam[t] - gam[s]);
-      const float c = sdP[e] * sc * sQK[e] * E;
-      atomicAdd(&dgam[t], c);
-      atomicAdd(&dgam[s], -c);
-      if (s < t) {
-        const float c2 = sdA[e] * sA[e];
-        atomicAdd(&dgam[t], c2);
-        atomicAdd(&dgam[s], -c2);
-        atomicAdd(&dbt[t], sdA[e] * E * sKK[e]);
+  // ---- stage A: [dQ~ ; -dW] = [dO ; dV'] S0^T, W S0, K K^T
+  if (tid == 0) {
+    constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0), id_kmn = idesc_bf16(128, 128, 0, 1);
+    constexpr uint32_t id_kk64 = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ss_lo(tmem + cDQ, kmaj(sb + kCkDODV, 128, kk), kmaj(sb + kCkS0, 128, kk), id_kk, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ss_lo(tmem + cDK, kmaj(sb + kCkW, 64, kk), mnmaj(sb + kCkS0, 128, kk), id_kmn, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ss_lo(tmem + cX, kmaj(sb + kCkYK, 64, kk), kmaj(sb + kCkYK, 64, kk), id_kk64, kk > 0);
+    mma_commit(&bars[K_A]);
+  }
+  bool ok = __all_sync(0xffffffffu, mbar_wait(&bars[K_A], 0, abort_flag, p.err));
+  fence_after_sync();
+  uint32_t v[32];
+  if (ok) {
+    if (tid < 64) {
+      const int t = tid;
+      // dgam_t += scale e^{gam_t} dQ~_t . q_t (q from the y rows)
+      const __nv_bfloat16* qr = p.y + (size_t)(x0 + t) * p.C + h * kD;
+      float dq = 0.f;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(tmem + cDQ + lrow + cc * 32, v);
+        tmem_ld_wait();
+        if (t < L)
+#pragma unroll
+          for (int q = 0; q < 32; ++q) dq = fmaf(__uint_as_float(v[q]), __bfloat162float(qr[cc * 32 + q]), dq);
+      }
+      if (t < L) atomicAdd(&dgam[t], sc * eg[t] * dq);
+      // V' = U^ - W S0 -> operand tile
+      const float* ut = p.ut + row * kD * kC;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(tmem + cDK + lrow + cc * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float f[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int col = cc * 32 + 8 * j + k;
+            f[k] = ut[col * kC + t] - __uint_as_float(v[8 * j + k]);
+          }
+          st_sw8(csm + kCkVP, 64, t, cc * 4 + j, pack8(f));
+        }
+      }
+      // GK_ts = Gam_ts (k_t . k_s), s < t < L
+#pragma unroll 1
+      for (int cc = 0; cc < 2; ++cc) {
+        tmem_ld32(tmem + cX + lrow + cc * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const int s = cc * 32 + q;
+          F1[fx(t, s)] = (s < t && t < L) ? expf(gam[t] - gam[s]) * __uint_as_float(v[q]) : 0.f;
+        }
+      }
+    } else {
+      // dW = -(dV' S0^T) -> operand tile (rows 64-127 of the stacked product)
+      const int t = tid - 64;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(tmem + cDQ + lrow + cc * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float f[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[k] = -__uint_as_float(v[8 * j + k]);
+          st_sw8(csm + kCkDW, 64, t, cc * 4 + j, pack8(f));
+        }
       }
     }
   }
-  // the decay term: dgam_{n-1} += e^{gam_n} <dS_n, S0>
-  {
-    float part = 0.f;
-    for (int e = tid; e < kD * kD; e += kBT) part = fmaf(dSe[e], S0[e], part);
+  fence_proxy_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+
+  // ---- stage B: dK~ = V' dS_n^T (into dk), dP = dO V'^T, R1 = dV' V^T, R2 = dW K^T;
+  // meanwhile T = (I + A)^{-1}, A_ts = beta_t GK_ts, one column per thread
+  if (ok && tid == 0) {
+    constexpr uint32_t id_kk = idesc_bf16(128, 128, 0, 0), id_kk64 = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if ((tid & 31) == 0) atomicAdd(&dgam[L - 1], eg[L - 1] * part);
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ss_lo(tmem + cDK, kmaj(sb + kCkVP, 64, kk), kmaj(sb + kCkDS, 128, kk), id_kk, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ss_lo(tmem + cX, kmaj(sb + kCkDODV, 128, kk), kmaj(sb + kCkVP, 64, kk), id_kk64, kk > 0);
+    // dV' = rows 64-127 of [dO ; dV']: start 64 rows into each half
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ss_lo(tmem + cR1, kmaj(sb + kCkDODV + 64 * 128, 128, kk), kmaj(sb + kCkYV, 64, kk), id_kk64, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_ss_lo(tmem + cR2, kmaj(sb + kCkDW, 64, kk), kmaj(sb + kCkYK, 64, kk), id_kk64, kk > 0);
+    mma_commit(&bars[K_B]);
+  }
+  if (tid < 64) {
+    const int j = tid;
+    for (int t = 0; t < 64; ++t) {
+      float x = t == j ? 1.f : 0.f;
+      if (t > j) {
+        const float b = bt[t];
+        for (int s = j; s < t; ++s) x = fmaf(-b * F1[fx(t, s)], F2[fx(s, j)], x);
+      }
+      F2[fx(t, j)] = x;
+    }
+  }
+  ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars[K_B], 0, abort_flag, p.err));
+  fence_after_sync();
+  __syncthreads();   // T complete; the S0 / dS_n / W tiles are no longer read
+
+  // ---- epilogue B (thread t < 64 = row t): the dK~ and dP terms, dT, and the
+  // operand tiles of stage C
+  float myc = 0.f;   // ek_t dK~_t . k_t
+  if (ok && tid < 64) {
+    const int t = tid;
+    const __nv_bfloat16* kr = p.y + (size_t)(x0 + t) * p.C + Hd + h * kD;
+    float c = 0.f;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      tmem_ld32(tmem + cDK + lrow + cc * 32, v);
+      tmem_ld_wait();
+      if (t < L)
+#pragma unroll
+        for (int q = 0; q < 32; ++q) c = fmaf(__uint_as_float(v[q]), __bfloat162float(kr[cc * 32 + q]), c);
+    }
+    myc = t < L ? ek[t] * c : 0.f;
+    // dP row t (masked s <= t < L) with P row t: E_ts = dP_ts P_ts; Aq, Aa rows
+    const __nv_bfloat16* pr = p.pm + (row * kC + t) * kC;
+    float esum = 0.f;
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+      tmem_ld32(tmem + cX + lrow + cc * 32, v);
+      tmem_ld_wait();
+      float aq[32], aa[32];
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int s = cc * 32 + q;
+        const float dp = (s <= t && t < L) ? __uint_as_float(v[q]) : 0.f;
+        const float e = dp * __bfloat162float(pr[s]);
+        F5[fx(t, s)] = e;
+        esum += e;
+        aq[q] = dp * __expf(-gam[s]);
+        aa[q] = sc * dp * __expf(gam[t] - gam[L - 1]);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        st_sw8(csm + kCkAq, 64, t, cc * 4 + j, pack8(aq + 8 * j));
+        st_sw8(csm + kCkAa, 64, t, cc * 4 + j, pack8(aa + 8 * j));
+      }
+    }
+    atomicAdd(&dgam[t], esum);
+    // dT_ts = beta_s R1_ts + beta_s e^{gam_s} R2_ts; the T o R1, T o R2 terms
+    float r1[32], r2[32];
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+      tmem_ld32(tmem + cR1 + lrow + cc * 32, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 32; ++q) r1[q] = __uint_as_float(v[q]);
+      tmem_ld32(tmem + cR2 + lrow + cc * 32, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 32; ++q) r2[q] = __uint_as_float(v[q]);
+      float dt[32];
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int s = cc * 32 + q;
+        dt[q] = bt[s] * (r1[q] + eg[s] * r2[q]);
+        const float T_ts = F2[fx(t, s)];
+        F3[fx(t, s)] = T_ts * r1[q];
+        F4[fx(t, s)] = T_ts * r2[q];
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) st_sw8(csm + kCkDT, 64, t, cc * 4 + j, pack8(dt + 8 * j));
+    }
+    // T (bf16, rows s) and Ac (MN-major: row s holds beta_t e^{2 gam_t - gam_{L-1}} T_st)
+    {
+      float tb[64], ac[64];
+#pragma unroll
+      for (int u = 0; u < 64; ++u) {
+        tb[u] = F2[fx(t, u)];
+        ac[u] = tb[u] * bt[u] * __expf(2.f * gam[u] - gam[L - 1]);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        st_sw8(csm + kCkTb, 64, t, j, pack8(tb + 8 * j));
+        st_sw8(csm + kCkAc, 64, t, j, pack8(ac + 8 * j));
+      }
+    }
+  }
+  {   // dgam: the dK~ term (sum over rows to L-1, minus its own row)
+    float c = myc;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+    if (tid < 64) {
+      atomicAdd(&dgam[tid], -myc);
+      if (lane == 0) atomicAdd(&dgam[L - 1], c);
+    }
+  }
+  fence_proxy_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (tid < 64) {   // column sums: the P term of dgam, and the B_U / B_W terms of dbeta, dgam
+    const int u = tid;
+    float e = 0.f, a1 = 0.f, a2 = 0.f;
+    for (int s = 0; s < 64; ++s) {
+      e += F5[fx(s, u)];
+      a1 += F3[fx(s, u)];
+      a2 += F4[fx(s, u)];
+    }
+    atomicAdd(&dgam[u], -e + bt[u] * eg[u] * a2);
+    atomicAdd(&dbt[u], a1 + eg[u] * a2);
+  }
+
+  // ---- stage C: Y = T^T dT; dq += Aq K; dk += Aa Q + Ac dW
+  if (ok && tid == 0) {
+    constexpr uint32_t id_mm64 = idesc_bf16(128, 64, 1, 1), id_kmn = idesc_bf16(128, 128, 0, 1),
+                       id_mmn = idesc_bf16(128, 128, 1, 1);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_ss_lo(tmem + cY, mnmaj(sb + kCkTb, 64, kk), mnmaj(sb + kCkDT, 64, kk), id_mm64, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_ss_lo(tmem + cDQ, kmaj(sb + kCkAq, 64, kk), mnmaj(sb + kCkYK, 64, kk), id_kmn, 1u);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_ss_lo(tmem + cDK, mnmaj(sb + kCkAa, 64, kk), mnmaj(sb + kCkYQ, 64, kk), id_mmn, 1u);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_ss_lo(tmem + cDK, mnmaj(sb + kCkAc, 64, kk), mnmaj(sb + kCkDW, 64, kk), id_mmn, 1u);
+    mma_commit(&bars[K_C]);
+  }
+  ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars[K_C], 0, abort_flag, p.err));
+  fence_after_sync();
+  if (ok && tid < 64) {
+    const int t = tid;
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+      tmem_ld32(tmem + cY + lrow + cc * 32, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) st_sw8(csm + kCkYb, 64, t, cc * 4 + j, pack8(reinterpret_cast<const float*>(v) + 8 * j));
+    }
+  }
+  fence_proxy_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+
+  // ---- stage D: dA' = Y T^T;  dA = -dA' on s < t < L
+  if (ok && tid == 0) {
+    constexpr uint32_t id_kk64 = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_ss_lo(tmem + cX, kmaj(sb + kCkYb, 64, kk), kmaj(sb + kCkTb, 64, kk), id_kk64, kk > 0);
+    mma_commit(&bars[K_D]);
+  }
+  ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars[K_D], 0, abort_flag, p.err));
+  fence_after_sync();
+  if (ok && tid < 64) {
+    const int t = tid;
+    float ga = 0.f, gb = 0.f;
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+      tmem_ld32(tmem + cX + lrow + cc * 32, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int s = cc * 32 + q;
+        const float da = (s < t && t < L) ? -__uint_as_float(v[q]) : 0.f;
+        const float gk = F1[fx(t, s)];
+        ga += da * bt[t] * gk;                    // dA_ts A_ts
+        gb += da * gk;                            // dbeta term
+        F3[fx(t, s)] = da * bt[t] * __expf(gam[t] - gam[s]);   // M_ts
+        F4[fx(t, s)] = da * bt[t] * gk;
+      }
+    }
+    atomicAdd(&dgam[t], ga);
+    atomicAdd(&dbt[t], gb);
   }
   __syncthreads();
-  if (tid < 32) {   // dg = reverse cumulative sum of dgam over the chunk's tokens
+  if (ok && tid < 64) {
+    const int t = tid;
+    float col = 0.f, ab[64];
+    const float et = __expf(gam[t] - gam[L - 1]);
+#pragma unroll
+    for (int s = 0; s < 64; ++s) {
+      col += F4[fx(s, t)];
+      ab[s] = et * (F3[fx(t, s)] + F3[fx(s, t)]);
+    }
+    atomicAdd(&dgam[t], -col);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) st_sw8(csm + kCkAb, 64, t, j, pack8(ab + 8 * j));
+  }
+  fence_proxy_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+
+  // ---- stage E: dk += Ab K;  dv = T^T dV'
+  if (ok && tid == 0) {
+    constexpr uint32_t id_kmn = idesc_bf16(128, 128, 0, 1), id_mmn = idesc_bf16(128, 128, 1, 1);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_ss_lo(tmem + cDK, kmaj(sb + kCkAb, 64, kk), mnmaj(sb + kCkYK, 64, kk), id_kmn, 1u);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_ss_lo(tmem + cDV, mnmaj(sb + kCkTb, 64, kk), mnmaj(sb + kCkDODV + 64 * 128, 128, kk), id_mmn, kk > 0);
+    mma_commit(&bars[K_E]);
+  }
+  ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars[K_E], 0, abort_flag, p.err));
+  fence_after_sync();
+  if (ok && tid < 64) {
+    // TMEM loads are warp-collective: every lane loads, rows t < L are stored
+    const int t = tid;
+    float* dqo = p.dqkv + (size_t)(x0 + t) * p.C + h * kD;
+    const float fq = sc * eg[t], fk = ek[t], fv = bt[t];
+#pragma unroll 1
+    for (int part = 0; part < 3; ++part) {
+      const uint32_t col0 = part == 0 ? cDQ : part == 1 ? cDK : cDV;
+      const float f = part == 0 ? fq : part == 1 ? fk : fv;
+      float4* dst = reinterpret_cast<float4*>(dqo + part * Hd);
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(tmem + col0 + lrow + cc * 32, v);
+        tmem_ld_wait();
+        if (t < L)
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[cc * 8 + q] = make_float4(f * __uint_as_float(v[4 * q]), f * __uint_as_float(v[4 * q + 1]),
+                                          f * __uint_as_float(v[4 * q + 2]), f * __uint_as_float(v[4 * q + 3]));
+      }
+    }
+  }
+  __syncthreads();
+  if (ok && tid < 32) {   // dg = reverse cumulative sum of dgam over the chunk's tokens; dbeta
     float a = tid + 32 < L ? dgam[tid + 32] : 0.f, b = tid < L ? dgam[tid] : 0.f;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -381,7 +906,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_chunk_kernel(const GbParams p)
         b += ub;
       }
     }
-    b += __shfl_sync(0xffffffffu, a, 0);   // the whole upper half
+    b += __shfl_sync(0xffffffffu, a, 0);
     if (tid < L) {
       p.dg[(size_t)(x0 + tid) * p.H + h] = b;
       p.dbeta[(size_t)(x0 + tid) * p.H + h] = dbt[tid];
@@ -391,6 +916,11 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_chunk_kernel(const GbParams p)
       p.dbeta[(size_t)(x0 + tid + 32) * p.H + h] = dbt[tid + 32];
     }
   }
+  if (!ok && tid == 0) atomicOr(p.err, kErrTimeout);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -552,12 +1082,19 @@ extern "C" stp_status stp_gdn_bwd(const stp_gdn_desc* desc, const void* plan, co
   p.dconv_w = dconv_w;
   p.dg = dg;
   p.dbeta = dbeta;
+  p.err = reinterpret_cast<uint32_t*>(ws);
+  CUtensorMap mwq, mkt, mpm;
+  if (n_chunk > 0 &&
+      (!map_2d(&mwq, p.wq, (int64_t)n_chunk * H * 128, kD, 128) ||
+       !map_2d(&mkt, p.kt, (int64_t)n_chunk * H * kC, kD, kC) ||
+       !map_2d(&mpm, p.pm, (int64_t)n_chunk * H * kC, kC, kC)))
+    return fail(STP_ECUDA, "stp_gdn_bwd: tensor map encoding failed");
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(gdn_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWalkSmem);
+    attr_err = cudaFuncSetAttribute(gdn_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWkSmem);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(gdn_bwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChunkSmem);
+      attr_err = cudaFuncSetAttribute(gdn_bwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCkSmem);
   });
   if (attr_err != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_bwd: %s", cudaGetErrorString(attr_err));
   // pads keep dq^, dk^, dv = 0 (the chunk kernel writes real tokens only)
@@ -568,9 +1105,9 @@ extern "C" stp_status stp_gdn_bwd(const stp_gdn_desc* desc, const void* plan, co
     const int n = depth_off[d + 1] - depth_off[d];
     if (n <= 0) continue;
     p.seg0 = depth_off[d];
-    gdn_bwd_walk_kernel<<<(unsigned)(n * H), kBT, kWalkSmem, s>>>(p);
+    gdn_bwd_walk_kernel<<<(unsigned)(n * H), kWkThreads, kWkSmem, s>>>(mwq, mkt, mpm, p);
   }
-  if (n_chunk > 0) gdn_bwd_chunk_kernel<<<(unsigned)(n_chunk * H), kBT, kChunkSmem, s>>>(p);
+  if (n_chunk > 0) gdn_bwd_chunk_kernel<<<(unsigned)(n_chunk * H), kCkThreads, kCkSmem, s>>>(p);
   gdn_bwd_token_kernel<<<dim3((unsigned)((N + 63) / 64), (unsigned)(3 * H)), kBT, 0, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_bwd: %s", cudaGetErrorString(e));
