@@ -455,8 +455,9 @@ stp_status stp_gdn_plan_bound(const stp_gdn_desc* desc, size_t* plan_bytes);
  * stp_plan_write) and the number of real tokens of each row (host int32 [R],
  * or NULL when no row holds pads; tokens at or past it are pads, which get
  * o = 0), writes the plan into `plan` (host, >= stp_gdn_plan_bound bytes):
- * the path predecessor of every token, the segments sorted by depth with
- * their parents, and the 64-token chunks.  Its word 5 is the number of int32
+ * the path predecessor of every token and its successors (the tokens whose
+ * predecessor it is), the segments sorted by depth with their parents, and
+ * the 64-token chunks.  Its word 5 is the number of int32
  * words used; copy at least that much to the device for stp_gdn_fwd.
  * Errors: STP_EINVAL (NULL, short buffer, subtree_end outside [x, T) or not
  * nested, row_used outside [0, T]).
@@ -502,9 +503,12 @@ stp_status stp_gdn_fwd_train(const stp_gdn_desc* desc, const void* plan, const v
  *   dx        device float32 [R * T, 3 H d], written in full (pads 0)
  *   dconv_w   device float32 [3 H d, 4], written in full
  *   dg, dbeta device float32 [R * T, H], written in full (pads 0)
- * Float32 on the CUDA cores, from the forward's bf16 chunk operands; the
- * convolution's input gradient is summed with float atomics (the last bits
- * may differ from call to call).  Errors as for stp_gdn_fwd.
+ * The contractions run on the tensor core (bf16 operands, float32
+ * accumulation, from the forward's bf16 chunk operands); every output is
+ * summed in one fixed order (no float atomics), so repeated calls give the
+ * same bits.  Device-side checks are OR-ed into the workspace's error word,
+ * which stp_gdn_fwd_train clears: after the pair, stp_device_status on d_ws
+ * reports a failure of either call.  Errors as for stp_gdn_fwd.
  */
 stp_status stp_gdn_bwd(const stp_gdn_desc* desc, const void* plan, const void* d_plan, const void* x,
                        const float* conv_w, const float* g, const float* beta, const float* d_o, float* dx,

@@ -99,7 +99,7 @@ struct GdnParams {
   float* ut;                // [n_chunk H, 128, 64]
   float* decay;             // [n_chunk H]
   float* state;             // [n_seg H, 128, 128]
-  float* s0;                // [n_chunk H, 128, 128] each chunk's starting state, or null (inference)
+  float* s0;                // [n_chunk H, 128 d_v, 128 d_k] each chunk's starting state, or null (inference)
   float* o;                 // [N, H, 128]
   uint32_t* err;
 };
@@ -561,12 +561,10 @@ __global__ void __launch_bounds__(kStThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lrow + cc * 32, v + 32 * cc);
       tmem_ld_wait();
-      if (p.s0) {   // training: keep the chunk's starting state (row r) for the backward
-        float4* d4 = reinterpret_cast<float4*>(p.s0 + ((size_t)((c0 + i) * p.H + h) * kGd + r) * kGd);
+      if (p.s0) {   // training: keep the chunk's starting state for the backward, as [d_v][d_k]
+        float* d = p.s0 + (size_t)((c0 + i) * p.H + h) * kGd * kGd + r;
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          d4[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                              __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        for (int q = 0; q < 128; ++q) d[q * kGd] = __uint_as_float(v[q]);
       }
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {

@@ -19,9 +19,17 @@
 //   gdn_bwd_chunk_kernel  one CTA per (chunk, head): everything above that
 //                         needs only the chunk and its two state (gradient)s,
 //                         its contractions on the tensor core (tcgen05).
-//   gdn_bwd_token_kernel  one block per (64 tokens, q / k / v head): the
-//                         convolution's input gradient (scattered to the
-//                         path's previous tokens) and weight gradient.
+//   gdn_bwd_token_kernel  one block per (64 tokens, q / k / v head): back
+//                         through the unit-norm heads and SiLU to dz, the
+//                         gradient of the convolution's output (in place of
+//                         dy), and the block's share of the weight gradient;
+//   gdn_bwd_dx_kernel     the convolution's input gradient of each token,
+//                         gathered from the tokens that read it: itself, its
+//                         path successors and theirs, three steps down (the
+//                         plan's successor lists), in a fixed order;
+//   gdn_bwd_dw_kernel     the weight gradient: the blocks' shares summed in
+//                         block order.
+// No float atomics: every output is summed in one fixed order.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -64,12 +72,14 @@ struct GbParams {
   const __nv_bfloat16* pm;   // [rows 64, 64]
   const float* ut;           // [rows, d, 64]
   const float* decay;        // [rows]
-  const float* s0;           // [rows, d, d]
+  const float* s0;           // [rows, d_v, d_k]
   float* dsend;              // [rows, d, d]
   float* dvp;                // [rows, 64, d]
   float* sgrad;              // [n_seg H, d, d]
   float* dqkv;               // [N, C]
-  float* scr;                // [rows, 2, 64, d]  V', dW
+  float* dwp;                // [N / 64 blocks, C, 4] weight-gradient shares
+  const int32_t* succ_off;   // [N + 1] successor lists (CSR) of every token
+  const int32_t* succ;
   float* dx;                 // [N, C]
   float* dconv_w;            // [C, 4]
   float* dg;                 // [N, H]
@@ -128,7 +138,9 @@ __device__ __forceinline__ uint32_t desc_lo_mn8k(uint32_t addr) {
 // per chunk, last to first:
 //   E1  dS (= dS_n of this chunk) goes out (transposed, for the chunk pass),
 //       becomes the bf16 operand DSB, and is decayed in place by e^{gam_n};
-//       the chunk's dO rows become bf16 rows 0-63 of DOV;
+//       the chunk's dO rows become bf16 rows 0-63 of its DOV buffer (two
+//       buffers alternate, so these writes never wait for the products of
+//       the chunk before);
 //   M1  dV' = P^T dO + K~ dS_n into columns 128-255 (rows = the chunk's
 //       tokens; lanes 64-127 see padding rows and are not read);
 //   E2  dV' goes out (transposed) and -dV' becomes rows 64-127 of DOV;
@@ -142,8 +154,8 @@ constexpr int kWkThreads = 192;
 constexpr int kWkStage = 57344;                  // [Q~; W] 32 KB | K~ 16 KB | P 8 KB
 constexpr int kWkOffKt = 32768, kWkOffP = 49152;
 constexpr int kWkOffDsb = 2 * kWkStage;          // dS_n bf16 [128 d_k][128 d_v], MN-major B
-constexpr int kWkOffDov = kWkOffDsb + 32768;     // [dO ; -dV'] bf16 [128][128], MN-major B
-constexpr int kWkOffBar = kWkOffDov + 32768;
+constexpr int kWkOffDov = kWkOffDsb + 32768;     // 2 x [dO ; -dV'] bf16 [128][128], MN-major B
+constexpr int kWkOffBar = kWkOffDov + 2 * 32768;
 constexpr int kWkSmem = kWkOffBar + 256 + 1024;
 enum { W_F = 0, W_E = 2, W_E1 = 4, W_M1 = 5, W_E2 = 6, W_M2 = 7, W_DRAIN = 8, W_COUNT = 9 };
 
@@ -215,10 +227,10 @@ __global__ void __launch_bounds__(kWkThreads, 1)
       // ------------------------------------------------------------ MMA
       constexpr uint32_t id_mnmn = idesc_bf16(128, 128, 1, 1);
       constexpr uint32_t id_kmn = idesc_bf16(128, 128, 0, 1);
-      const uint32_t dsb = sb + kWkOffDsb, dov = sb + kWkOffDov;
+      const uint32_t dsb = sb + kWkOffDsb;
       for (int n = 0; n < nck; ++n) {
         const int st = n & 1;
-        const uint32_t stage = sb + st * kWkStage;
+        const uint32_t stage = sb + st * kWkStage, dov = sb + kWkOffDov + st * 32768;
         if (!mbar_wait(&bars[W_F + st], (n >> 1) & 1, abort_flag, p.err)) break;
         if (!mbar_wait(&bars[W_E1], n & 1, abort_flag, p.err)) break;
         fence_after_sync();
@@ -251,8 +263,31 @@ __global__ void __launch_bounds__(kWkThreads, 1)
     const int r = threadIdx.x;   // TMEM lane: d_k row of dS; token row of dV'
     const uint32_t lrow = (uint32_t)(warp * 32) << 16;
     uint8_t* dsb = sm + kWkOffDsb;
-    uint8_t* dov = sm + kWkOffDov;
     uint32_t v[32];
+    // dO rows of the n-th chunk processed into DOV buffer n % 2 (rows 0-63):
+    // 64 rows x 16 pieces of 8 columns, 8 pieces per thread, all loads in flight at once
+    auto load_do = [&](int n) {
+      const int c = c0 + nck - 1 - n, L = p.chunk_len[c], x0 = p.chunk_start[c];
+      uint8_t* dov = sm + kWkOffDov + (n & 1) * 32768;
+      const float* dO = p.d_o + (size_t)x0 * p.H * kD + h * kD;
+      float4 a[8], b[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int e = threadIdx.x + 128 * k, t = e >> 4, c8 = e & 15;
+        a[k] = b[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < L) {
+          const float4* src = reinterpret_cast<const float4*>(dO + (size_t)t * p.H * kD + c8 * 8);
+          a[k] = src[0];
+          b[k] = src[1];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int e = threadIdx.x + 128 * k, t = e >> 4, c8 = e & 15;
+        const float f[8] = {a[k].x, a[k].y, a[k].z, a[k].w, b[k].x, b[k].y, b[k].z, b[k].w};
+        st_sw8(dov, 128, t, c8, pack8(f));
+      }
+    };
     {   // the segment's end gradient: the sum of its children's start gradients
       const int k0 = p.child_off[seg], k1 = p.child_off[seg + 1];
 #pragma unroll 1
@@ -273,6 +308,10 @@ __global__ void __launch_bounds__(kWkThreads, 1)
       const int c = c0 + nck - 1 - n, L = p.chunk_len[c], x0 = p.chunk_start[c];
       const size_t row = (size_t)c * p.H + h;
       const float dec = p.decay[row];
+      // this chunk's dO rows: their DOV buffer was last read by the products
+      // of chunk n - 2, complete before E1 of chunk n - 1, so the loads
+      // overlap the products of chunk n - 1
+      load_do(n);
       if (n > 0) {
         if (!__all_sync(0xffffffffu, mbar_wait(&bars[W_M2], (n - 1) & 1, abort_flag, p.err))) {
           ok = false;
@@ -294,28 +333,13 @@ __global__ void __launch_bounds__(kWkThreads, 1)
         for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * dec);
         tmem_st32(tmem + lrow + cc * 32, v);
       }
-      // the chunk's dO rows: 64 rows x 16 chunks of 8 columns over the 128 threads
-      const float* dO = p.d_o + (size_t)x0 * p.H * kD + h * kD;
-#pragma unroll 2
-      for (int e = r; e < kC * 16; e += 128) {
-        const int t = e >> 4, c8 = e & 15;
-        float f[8];
-        if (t < L) {
-          const float4* src = reinterpret_cast<const float4*>(dO + (size_t)t * p.H * kD + c8 * 8);
-          const float4 a = src[0], b = src[1];
-          f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) f[k] = 0.f;
-        }
-        st_sw8(dov, 128, t, c8, pack8(f));
-      }
       tmem_st_wait();
       fence_proxy_async_smem();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[W_E1]);
-      // E2: dV' out ([d_v][64]) and -dV' into rows 64-127 of DOV
+      // E2: dV' out ([d_v][64]) and -dV' into rows 64-127 of this chunk's DOV
+      uint8_t* dov = sm + kWkOffDov + (n & 1) * 32768;
       if (warp < 2) {
         if (!__all_sync(0xffffffffu, mbar_wait(&bars[W_M1], n & 1, abort_flag, p.err))) {
           ok = false;
@@ -387,6 +411,32 @@ __global__ void __launch_bounds__(kWkThreads, 1)
 // threads (thread = TMEM lane), thread 0 issues the MMAs; the stages below
 // are separated by MMA commits and block barriers.
 constexpr int kCkThreads = 128;
+
+__device__ __forceinline__ void unpack8(const uint4 r, float* f) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// Dot product of 32 float32 values with columns 32 cc .. 32 cc + 31 of row
+// `row` of a 128-byte-swizzled bf16 tile with `rows` rows.
+__device__ __forceinline__ float dot32_sw(const uint8_t* tile, int rows, int row, int cc, const uint32_t* v) {
+  float d = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c8 = cc * 4 + j;
+    const uint4 r = *reinterpret_cast<const uint4*>(tile + (c8 >> 3) * rows * 128 + row * 128 +
+                                                    (((c8 & 7) ^ (row & 7)) << 4));
+    float f[8];
+    unpack8(r, f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) d = fmaf(__uint_as_float(v[8 * j + k]), f[k], d);
+  }
+  return d;
+}
 // shared memory (1024-aligned): bf16 operand tiles, 128-byte swizzled in
 // 64-column halves (half stride = rows x 128 bytes)
 constexpr int kCkYQ = 0, kCkYK = 16384, kCkYV = 32768;      // q^, k^, v [64][128]
@@ -431,7 +481,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
   float* bt = ek + 64;
   float* dgam = bt + 64;
   float* dbt = dgam + 64;
-  float* misc = dbt + 64;   // misc[0]: <dS_n, S0>
+  float* misc = dbt + 64;   // per-warp partials: [0..3] <dS_n, S0>, [4..5] the dK~ term
   uint64_t* bars = reinterpret_cast<uint64_t*>(csm + kCkBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + K_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -460,6 +510,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
   // rows (thread = d_k row), with the decay term <dS_n, S0>
   {
     const __nv_bfloat16* y = p.y + (size_t)x0 * p.C + h * kD;
+#pragma unroll 4
     for (int e = tid; e < 64 * 16; e += kCkThreads) {
       const int t = e >> 4, c8 = e & 15;
       uint4 rq = make_uint4(0, 0, 0, 0), rk = rq, rv = rq, rw = rq;
@@ -485,34 +536,36 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
       }
       st_sw8(csm + kCkDODV, 128, t, c8, pack8(f));
     }
-    // dV' rows from [d_v][64]: thread = token (lanes 0-63), the other half idle here
-    const float* dvp = p.dvp + row * kC * kD;
-    if (tid < 64) {
-#pragma unroll 1
-      for (int c8 = 0; c8 < 16; ++c8) {
-        float f[8];
+    // dV' rows from [d_v][64]: thread = (token, half of the d_v columns)
+    {
+      const float* dvp = p.dvp + row * kC * kD;
+      const int t = tid & 63, c0 = (tid >> 6) * 8;
+      float f[64];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) f[k] = dvp[(c8 * 8 + k) * kC + tid];
-        st_sw8(csm + kCkDODV, 128, kC + tid, c8, pack8(f));
-      }
+      for (int k = 0; k < 64; ++k) f[k] = dvp[(c0 * 8 + k) * kC + t];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) st_sw8(csm + kCkDODV, 128, kC + t, c0 + j, pack8(f + 8 * j));
     }
-    // S0 row r (row-major [d_k][d_v]) and dS_n row r (stored [d_v][d_k])
+    // S0 row r and dS_n row r (both stored [d_v][d_k]: thread r reads column r)
     const int r = tid;
-    const float* s0r = p.s0 + (row * kD + r) * kD;
+    const float* s0t = p.s0 + row * kD * kD;
     const float* dse = p.dsend + row * kD * kD;
     float dot = 0.f;
 #pragma unroll 1
-    for (int c8 = 0; c8 < 16; ++c8) {
-      const float4 a = reinterpret_cast<const float4*>(s0r)[2 * c8], b = reinterpret_cast<const float4*>(s0r)[2 * c8 + 1];
-      const float fs[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      float fd[8];
+    for (int c32 = 0; c32 < 4; ++c32) {
+      float fs[32], fd[32];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        fd[k] = dse[(c8 * 8 + k) * kD + r];
-        dot = fmaf(fs[k], fd[k], dot);
+      for (int k = 0; k < 32; ++k) {
+        fs[k] = s0t[(c32 * 32 + k) * kD + r];
+        fd[k] = dse[(c32 * 32 + k) * kD + r];
       }
-      st_sw8(csm + kCkS0, 128, r, c8, pack8(fs));
-      st_sw8(csm + kCkDS, 128, r, c8, pack8(fd));
+#pragma unroll
+      for (int k = 0; k < 32; ++k) dot = fmaf(fs[k], fd[k], dot);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        st_sw8(csm + kCkS0, 128, r, c32 * 4 + j, pack8(fs + 8 * j));
+        st_sw8(csm + kCkDS, 128, r, c32 * 4 + j, pack8(fd + 8 * j));
+      }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
@@ -520,9 +573,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
       dgam[tid] = 0.f;
       dbt[tid] = 0.f;
     }
-    if (tid == 0) misc[0] = 0.f;
-    __syncthreads();
-    if (lane == 0) atomicAdd(&misc[0], dot);
+    if (lane == 0) misc[warp] = dot;
   }
   if (tid < 32) {   // gam = inclusive prefix sum of g over the chunk; beta; e^gam; e^{gam_{L-1} - gam}
     float a = tid < L ? p.g[(size_t)(x0 + tid) * p.H + h] : 0.f;
@@ -551,7 +602,6 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  if (tid == 0) atomicAdd(&dgam[L - 1], eg[L - 1] * misc[0]);   // decay term: e^{gam_{L-1}} <dS_n, S0>
 
   // ---- stage A: [dQ~ ; -dW] = [dO ; dV'] S0^T, W S0, K K^T
   if (tid == 0) {
@@ -574,18 +624,15 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
   if (ok) {
     if (tid < 64) {
       const int t = tid;
-      // dgam_t += scale e^{gam_t} dQ~_t . q_t (q from the y rows)
-      const __nv_bfloat16* qr = p.y + (size_t)(x0 + t) * p.C + h * kD;
+      // dgam_t += scale e^{gam_t} dQ~_t . q_t (q row t from its operand tile)
       float dq = 0.f;
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         tmem_ld32(tmem + cDQ + lrow + cc * 32, v);
         tmem_ld_wait();
-        if (t < L)
-#pragma unroll
-          for (int q = 0; q < 32; ++q) dq = fmaf(__uint_as_float(v[q]), __bfloat162float(qr[cc * 32 + q]), dq);
+        dq += dot32_sw(csm + kCkYQ, 64, t, cc, v);
       }
-      if (t < L) atomicAdd(&dgam[t], sc * eg[t] * dq);
+      if (t < L) dgam[t] += sc * eg[t] * dq;
       // V' = U^ - W S0 -> operand tile
       const float* ut = p.ut + row * kD * kC;
 #pragma unroll 1
@@ -656,14 +703,20 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
     mma_commit(&bars[K_B]);
   }
   if (tid < 64) {
+    // column j of T in registers: T_tj = [t == j] - beta_t sum_{s < t} GK_ts T_sj
+    // (T_sj = 0 for s < j, so every row is summed over s < t)
     const int j = tid;
+    float X[64];
+#pragma unroll
     for (int t = 0; t < 64; ++t) {
-      float x = t == j ? 1.f : 0.f;
-      if (t > j) {
-        const float b = bt[t];
-        for (int s = j; s < t; ++s) x = fmaf(-b * F1[fx(t, s)], F2[fx(s, j)], x);
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int s = 0; s < t; s += 2) {
+        a0 = fmaf(F1[fx(t, s)], X[s], a0);
+        if (s + 1 < t) a1 = fmaf(F1[fx(t, s + 1)], X[s + 1], a1);
       }
-      F2[fx(t, j)] = x;
+      X[t] = (t == j ? 1.f : 0.f) - bt[t] * (a0 + a1);
+      F2[fx(t, j)] = X[t];
     }
   }
   ok = __all_sync(0xffffffffu, ok && mbar_wait(&bars[K_B], 0, abort_flag, p.err));
@@ -675,22 +728,22 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
   float myc = 0.f;   // ek_t dK~_t . k_t
   if (ok && tid < 64) {
     const int t = tid;
-    const __nv_bfloat16* kr = p.y + (size_t)(x0 + t) * p.C + Hd + h * kD;
     float c = 0.f;
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
       tmem_ld32(tmem + cDK + lrow + cc * 32, v);
       tmem_ld_wait();
-      if (t < L)
-#pragma unroll
-        for (int q = 0; q < 32; ++q) c = fmaf(__uint_as_float(v[q]), __bfloat162float(kr[cc * 32 + q]), c);
+      c += dot32_sw(csm + kCkYK, 64, t, cc, v);
     }
     myc = t < L ? ek[t] * c : 0.f;
     // dP row t (masked s <= t < L) with P row t: E_ts = dP_ts P_ts; Aq, Aa rows
-    const __nv_bfloat16* pr = p.pm + (row * kC + t) * kC;
+    const uint4* pr4 = reinterpret_cast<const uint4*>(p.pm + (row * kC + t) * kC);
     float esum = 0.f;
 #pragma unroll 1
     for (int cc = 0; cc < 2; ++cc) {
+      float pf[32];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) unpack8(pr4[cc * 4 + j], pf + 8 * j);
       tmem_ld32(tmem + cX + lrow + cc * 32, v);
       tmem_ld_wait();
       float aq[32], aa[32];
@@ -698,7 +751,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
       for (int q = 0; q < 32; ++q) {
         const int s = cc * 32 + q;
         const float dp = (s <= t && t < L) ? __uint_as_float(v[q]) : 0.f;
-        const float e = dp * __bfloat162float(pr[s]);
+        const float e = dp * pf[q];
         F5[fx(t, s)] = e;
         esum += e;
         aq[q] = dp * __expf(-gam[s]);
@@ -710,7 +763,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
         st_sw8(csm + kCkAa, 64, t, cc * 4 + j, pack8(aa + 8 * j));
       }
     }
-    atomicAdd(&dgam[t], esum);
+    dgam[t] += esum;
     // dT_ts = beta_s R1_ts + beta_s e^{gam_s} R2_ts; the T o R1, T o R2 terms
     float r1[32], r2[32];
 #pragma unroll 1
@@ -755,8 +808,8 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
     if (tid < 64) {
-      atomicAdd(&dgam[tid], -myc);
-      if (lane == 0) atomicAdd(&dgam[L - 1], c);
+      dgam[tid] -= myc;
+      if (lane == 0) misc[4 + warp] = c;
     }
   }
   fence_proxy_async_smem();
@@ -771,8 +824,8 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
       a1 += F3[fx(s, u)];
       a2 += F4[fx(s, u)];
     }
-    atomicAdd(&dgam[u], -e + bt[u] * eg[u] * a2);
-    atomicAdd(&dbt[u], a1 + eg[u] * a2);
+    dgam[u] += -e + bt[u] * eg[u] * a2;
+    dbt[u] += a1 + eg[u] * a2;
   }
 
   // ---- stage C: Y = T^T dT; dq += Aq K; dk += Aa Q + Ac dW
@@ -838,8 +891,8 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
         F4[fx(t, s)] = da * bt[t] * gk;
       }
     }
-    atomicAdd(&dgam[t], ga);
-    atomicAdd(&dbt[t], gb);
+    dgam[t] += ga;
+    dbt[t] += gb;
   }
   __syncthreads();
   if (ok && tid < 64) {
@@ -851,7 +904,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
       col += F4[fx(s, t)];
       ab[s] = et * (F3[fx(t, s)] + F3[fx(s, t)]);
     }
-    atomicAdd(&dgam[t], -col);
+    dgam[t] -= col;
 #pragma unroll
     for (int j = 0; j < 8; ++j) st_sw8(csm + kCkAb, 64, t, j, pack8(ab + 8 * j));
   }
@@ -896,6 +949,9 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
     }
   }
   __syncthreads();
+  if (tid == 0)   // the terms of row L-1 summed over rows or warps: the dK~ term, then the decay term
+    dgam[L - 1] += (misc[4] + misc[5]) + eg[L - 1] * (((misc[0] + misc[1]) + misc[2]) + misc[3]);
+  __syncthreads();
   if (ok && tid < 32) {   // dg = reverse cumulative sum of dgam over the chunk's tokens; dbeta
     float a = tid + 32 < L ? dgam[tid + 32] : 0.f, b = tid < L ? dgam[tid] : 0.f;
 #pragma unroll
@@ -924,12 +980,41 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
 }
 
 // ---------------------------------------------------------------------------
-// Back through the unit-norm heads, SiLU and the path convolution.
-__global__ void __launch_bounds__(kBT) gdn_bwd_token_kernel(const GbParams p) {
+// Back through the unit-norm heads and SiLU: dz of every (token, channel),
+// written over dy; and the block's share of the weight gradient,
+// dw[c][tap] = sum over its tokens of x[source of the tap] dz.  Block = (64
+// tokens, one group of 128 channels: a q, k or v head); thread = (4 tokens,
+// 8 channels), so the 16 lanes of one token hold one head.  Every load of the
+// thread's four tokens is issued before any is used.
+__global__ void __launch_bounds__(kBT, 1) gdn_bwd_token_kernel(const GbParams p) {
   __shared__ float red[16][16][33];   // [token lane][vector][8 channels x 4 taps]
   const int grp = blockIdx.y, lt = threadIdx.x >> 4, vec = threadIdx.x & 15;
   const int ch = grp * kD + vec * 8;
   const bool is_qk = grp < 2 * p.H;
+  const unsigned grpmask = 0xffffu << (threadIdx.x & 16);
+  int src[4][4];   // [token][tap]: the sources of taps 0..3 (-1: none; tap 2 = -2: a pad)
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int x = blockIdx.x * 64 + it * 16 + lt;
+    const bool in = x < p.N;
+    src[it][2] = in ? p.prev[x] : -2;
+    src[it][1] = in ? p.prev2[x] : -1;
+    src[it][0] = in ? p.prev3[x] : -1;
+    src[it][3] = x;
+  }
+  uint4 xr[4][4];
+  float4 dya[4], dyb[4];
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const bool real = src[it][2] != -2;
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      xr[it][t] = (real && src[it][t] >= 0) ? *reinterpret_cast<const uint4*>(p.x + (size_t)src[it][t] * p.C + ch)
+                                            : make_uint4(0, 0, 0, 0);
+    const float4* d = reinterpret_cast<const float4*>(p.dqkv + (size_t)src[it][3] * p.C + ch);
+    dya[it] = real ? d[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+    dyb[it] = real ? d[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float4 wv[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) wv[i] = reinterpret_cast<const float4*>(p.conv_w)[ch + i];
@@ -938,36 +1023,22 @@ __global__ void __launch_bounds__(kBT) gdn_bwd_token_kernel(const GbParams p) {
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int t = 0; t < 4; ++t) dw[i][t] = 0.f;
-  const unsigned grpmask = 0xffffu << (threadIdx.x & 16);
-#pragma unroll 1
+#pragma unroll
   for (int it = 0; it < 4; ++it) {
-    const int x = blockIdx.x * 64 + it * 16 + lt;
-    const int p1 = x < p.N ? p.prev[x] : -2;
-    if (p1 == -2) continue;   // a pad or past the end: the same for all 16 lanes of the token
-    const int src[4] = {p.prev3[x], p.prev2[x], p1, x};
-    float z[8], xin[4][8];
+    const bool real = src[it][2] != -2;   // the same for all 16 lanes of the token
+    float xin[4][8], z[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) z[i] = 0.f;
+    for (int t = 0; t < 4; ++t) unpack8(xr[it][t], xin[t]);
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xin[t][i] = 0.f;
-      if (src[t] < 0) continue;
-      const __nv_bfloat16* xr = p.x + (size_t)src[t] * p.C + ch;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        xin[t][i] = __bfloat162float(xr[i]);
-        const float w = t == 0 ? wv[i].x : t == 1 ? wv[i].y : t == 2 ? wv[i].z : wv[i].w;
-        z[i] = fmaf(w, xin[t][i], z[i]);
-      }
-    }
+    for (int i = 0; i < 8; ++i)
+      z[i] = fmaf(wv[i].x, xin[0][i], fmaf(wv[i].y, xin[1][i], fmaf(wv[i].z, xin[2][i], wv[i].w * xin[3][i])));
+    const float dy0[8] = {dya[it].x, dya[it].y, dya[it].z, dya[it].w, dyb[it].x, dyb[it].y, dyb[it].z, dyb[it].w};
     float sg[8], y[8], dy[8];
-    const float* dyin = p.dqkv + (size_t)x * p.C + ch;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       sg[i] = 1.f / (1.f + expf(-z[i]));
       y[i] = z[i] * sg[i];
-      dy[i] = dyin[i];
+      dy[i] = dy0[i];
     }
     if (is_qk) {   // y^ = y / n,  dy = (dy^ - y^ (y^ . dy^)) / n
       float ss = 0.f;
@@ -988,31 +1059,85 @@ __global__ void __launch_bounds__(kBT) gdn_bwd_token_kernel(const GbParams p) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) dy[i] = (dy[i] - y[i] * rn * dot) * rn;
     }
+    if (!real) continue;
+    float dz[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float dz = dy[i] * sg[i] * (1.f + z[i] * (1.f - sg[i]));
+      dz[i] = dy[i] * sg[i] * (1.f + z[i] * (1.f - sg[i]));
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        if (src[t] < 0) continue;
-        const float w = t == 0 ? wv[i].x : t == 1 ? wv[i].y : t == 2 ? wv[i].z : wv[i].w;
-        atomicAdd(p.dx + (size_t)src[t] * p.C + ch + i, w * dz);
-        dw[i][t] = fmaf(xin[t][i], dz, dw[i][t]);
-      }
+      for (int t = 0; t < 4; ++t) dw[i][t] = fmaf(xin[t][i], dz[i], dw[i][t]);
     }
+    float4* o = reinterpret_cast<float4*>(p.dqkv + (size_t)src[it][3] * p.C + ch);
+    o[0] = make_float4(dz[0], dz[1], dz[2], dz[3]);
+    o[1] = make_float4(dz[4], dz[5], dz[6], dz[7]);
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int t = 0; t < 4; ++t) red[lt][vec][i * 4 + t] = dw[i][t];
   __syncthreads();
-  if (threadIdx.x < 16 * 32) {
-    for (int e = threadIdx.x; e < 16 * 32; e += kBT) {
-      const int vv = e / 32, j = e % 32;
-      float a = 0.f;
-      for (int l = 0; l < 16; ++l) a += red[l][vv][j];
-      atomicAdd(p.dconv_w + (size_t)(grp * kD + vv * 8 + j / 4) * 4 + (j % 4), a);
-    }
+  // this block's share, [block][channel][tap]: 128 channels x 4 taps, tokens summed in lane order
+  float* share = p.dwp + ((size_t)blockIdx.x * p.C + grp * kD) * 4;
+  for (int e = threadIdx.x; e < 16 * 32; e += kBT) {
+    const int vv = e / 32, j = e % 32;
+    float a = 0.f;
+    for (int l = 0; l < 16; ++l) a += red[l][vv][j];
+    share[(vv * 8 + j / 4) * 4 + (j % 4)] = a;
   }
+}
+
+// dx[j] = w3 dz[j] + sum over successors i of (w2 dz[i] + sum over successors
+// k of i of (w1 dz[k] + sum over successors l of k of w0 dz[l])): every token
+// that reads x[j] through a tap, summed in successor-list order.  Same block
+// and thread shape as the token kernel; pads get 0.
+__global__ void __launch_bounds__(kBT) gdn_bwd_dx_kernel(const GbParams p) {
+  const int grp = blockIdx.y, lt = threadIdx.x >> 4, vec = threadIdx.x & 15;
+  const int ch = grp * kD + vec * 8;
+  float4 wv[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) wv[i] = reinterpret_cast<const float4*>(p.conv_w)[ch + i];
+  auto add = [&](float* acc, int src, int tap) {
+    const float* d = p.dqkv + (size_t)src * p.C + ch;
+    const float4 a = reinterpret_cast<const float4*>(d)[0], b = reinterpret_cast<const float4*>(d)[1];
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float w = tap == 0 ? wv[i].x : tap == 1 ? wv[i].y : tap == 2 ? wv[i].z : wv[i].w;
+      acc[i] = fmaf(w, v[i], acc[i]);
+    }
+  };
+#pragma unroll 1
+  for (int it = 0; it < 4; ++it) {
+    const int x = blockIdx.x * 64 + it * 16 + lt;
+    if (x >= p.N) continue;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    if (p.prev[x] != -2) {
+      add(acc, x, 3);
+      for (int a = p.succ_off[x]; a < p.succ_off[x + 1]; ++a) {
+        const int i1 = p.succ[a];
+        add(acc, i1, 2);
+        for (int b = p.succ_off[i1]; b < p.succ_off[i1 + 1]; ++b) {
+          const int i2 = p.succ[b];
+          add(acc, i2, 1);
+          for (int c = p.succ_off[i2]; c < p.succ_off[i2 + 1]; ++c) add(acc, p.succ[c], 0);
+        }
+      }
+    }
+    float4* out = reinterpret_cast<float4*>(p.dx + (size_t)x * p.C + ch);
+    out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+// dconv_w[c][tap] = the blocks' shares summed in block order; one thread per (c, tap).
+__global__ void __launch_bounds__(kBT) gdn_bwd_dw_kernel(const GbParams p, int n_blocks) {
+  const int e = blockIdx.x * kBT + threadIdx.x;
+  if (e >= p.C * 4) return;
+  float a = 0.f;
+  for (int b = 0; b < n_blocks; ++b) a += p.dwp[(size_t)b * p.C * 4 + e];
+  p.dconv_w[e] = a;
 }
 
 }  // namespace
@@ -1038,7 +1163,6 @@ extern "C" stp_status stp_gdn_bwd(const stp_gdn_desc* desc, const void* plan, co
   const int C = 3 * H * kD;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(dconv_w, 0, (size_t)C * 4 * 4, s);
-  if (e == cudaSuccess && N > 0) e = cudaMemsetAsync(dx, 0, (size_t)N * C * 4, s);
   if (e == cudaSuccess && N > 0) e = cudaMemsetAsync(dg, 0, (size_t)N * H * 4, s);
   if (e == cudaSuccess && N > 0) e = cudaMemsetAsync(dbeta, 0, (size_t)N * H * 4, s);
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_bwd: %s", cudaGetErrorString(e));
@@ -1077,7 +1201,9 @@ extern "C" stp_status stp_gdn_bwd(const stp_gdn_desc* desc, const void* plan, co
   p.dvp = reinterpret_cast<float*>(ws + Lw.dvp);
   p.sgrad = reinterpret_cast<float*>(ws + Lw.sgrad);
   p.dqkv = reinterpret_cast<float*>(ws + Lw.dqkv);
-  p.scr = reinterpret_cast<float*>(ws + Lw.scr);
+  p.dwp = reinterpret_cast<float*>(ws + Lw.dwp);
+  p.succ_off = dp + w[GP_SUCC_OFF];
+  p.succ = dp + w[GP_SUCC];
   p.dx = dx;
   p.dconv_w = dconv_w;
   p.dg = dg;
@@ -1108,7 +1234,10 @@ extern "C" stp_status stp_gdn_bwd(const stp_gdn_desc* desc, const void* plan, co
     gdn_bwd_walk_kernel<<<(unsigned)(n * H), kWkThreads, kWkSmem, s>>>(mwq, mkt, mpm, p);
   }
   if (n_chunk > 0) gdn_bwd_chunk_kernel<<<(unsigned)(n_chunk * H), kCkThreads, kCkSmem, s>>>(p);
-  gdn_bwd_token_kernel<<<dim3((unsigned)((N + 63) / 64), (unsigned)(3 * H)), kBT, 0, s>>>(p);
+  const unsigned n_blocks = (unsigned)((N + 63) / 64);
+  gdn_bwd_token_kernel<<<dim3(n_blocks, (unsigned)(3 * H)), kBT, 0, s>>>(p);
+  gdn_bwd_dx_kernel<<<dim3(n_blocks, (unsigned)(3 * H)), kBT, 0, s>>>(p);
+  gdn_bwd_dw_kernel<<<(unsigned)((C * 4 + kBT - 1) / kBT), kBT, 0, s>>>(p, (int)n_blocks);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_bwd: %s", cudaGetErrorString(e));
   return STP_OK;

@@ -17,7 +17,7 @@ constexpr int kGdnD = 128;   // head dim
 // starting state (s0) for the backward, which adds its own buffers.
 struct GdnLayout {
   size_t y, wq, kt, pm, ut, decay, state, total;          // forward
-  size_t s0, dsend, dvp, sgrad, dqkv, scr, train_total;   // training
+  size_t s0, dsend, dvp, sgrad, dqkv, dwp, train_total;   // training
 };
 
 inline GdnLayout gdn_layout(int64_t N, int H, int64_t n_chunk, int64_t n_seg) {
@@ -36,12 +36,12 @@ inline GdnLayout gdn_layout(int64_t N, int H, int64_t n_chunk, int64_t n_seg) {
   take(L.decay, (size_t)rows * 4);                    // e^{gam_L}
   take(L.state, (size_t)n_seg * H * kGdnD * kGdnD * 4);   // final state of each (segment, head)
   L.total = o;
-  take(L.s0, (size_t)rows * kGdnD * kGdnD * 4);       // starting state of each (chunk, head)
-  take(L.dsend, (size_t)rows * kGdnD * kGdnD * 4);    // state gradient at each chunk's end
-  take(L.dvp, (size_t)rows * kGdnChunk * kGdnD * 4);  // dV' per (chunk, head)
-  take(L.sgrad, (size_t)n_seg * H * kGdnD * kGdnD * 4);   // state gradient at each segment's start
-  take(L.dqkv, (size_t)N * C * 4);                    // dq^ | dk^ | dv, float32
-  take(L.scr, (size_t)rows * 2 * kGdnChunk * kGdnD * 4);  // V' and dW per (chunk, head)
+  take(L.s0, (size_t)rows * kGdnD * kGdnD * 4);       // starting state of each (chunk, head), [d_v][d_k]
+  take(L.dsend, (size_t)rows * kGdnD * kGdnD * 4);    // state gradient at each chunk's end, [d_v][d_k]
+  take(L.dvp, (size_t)rows * kGdnChunk * kGdnD * 4);  // dV' per (chunk, head), [d_v][64]
+  take(L.sgrad, (size_t)n_seg * H * kGdnD * kGdnD * 4);   // state gradient at each segment's start, [d_v][d_k]
+  take(L.dqkv, (size_t)N * C * 4);                    // dq^ | dk^ | dv, then dz (the convolution's output gradient)
+  take(L.dwp, (size_t)((N + 63) / 64) * C * 4 * 4);   // convolution weight gradient per 64-token block
   L.train_total = o;
   return L;
 }

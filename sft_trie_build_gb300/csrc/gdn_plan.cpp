@@ -37,8 +37,8 @@ extern "C" stp_status stp_gdn_plan_bound(const stp_gdn_desc* desc, size_t* plan_
   if (!plan_bytes) return fail(STP_EINVAL, "stp_gdn_plan_bound: NULL output");
   const size_t N = (size_t)desc->n_rows * desc->row_len;
   // prev (1, 2 and 3 back), 4 words per segment, depth offsets, 2 words per chunk, the child lists
-  // (segments, chunks <= N)
-  *plan_bytes = 4 * (kGdnHeader + 3 * N + 4 * N + (N + 1) + 2 * N + (N + 1) + N);
+  // (segments, chunks <= N), the token successor lists
+  *plan_bytes = 4 * (kGdnHeader + 3 * N + 4 * N + (N + 1) + 2 * N + (N + 1) + N + (N + 1) + N);
   return STP_OK;
 }
 
@@ -135,6 +135,10 @@ extern "C" stp_status stp_gdn_plan(const stp_gdn_desc* desc, const int32_t* subt
   take(GP_CHUNK_LEN, n_chunk);
   take(GP_CHILD_OFF, n_seg + 1);
   take(GP_CHILD, n_seg);
+  int64_t n_succ = 0;
+  for (int64_t x = 0; x < N; ++x) n_succ += prev[x] >= 0;
+  take(GP_SUCC_OFF, N + 1);
+  take(GP_SUCC, n_succ);
   w[GP_MAGIC] = kGdnMagic;
   w[GP_N] = (int32_t)N;
   w[GP_NSEG] = n_seg;
@@ -176,6 +180,20 @@ extern "C" stp_status stp_gdn_plan(const stp_gdn_desc* desc, const int32_t* subt
       const int32_t par = w[w[GP_SEG_PARENT] + i];
       if (par >= 0) ch[fill[par]++] = i;
     }
+  }
+  // successors of every token (the tokens whose path predecessor it is), in
+  // token order, as a CSR list: the convolution's input gradient of a token
+  // gathers from them
+  {
+    int32_t* off = w + w[GP_SUCC_OFF];
+    int32_t* sc = w + w[GP_SUCC];
+    for (int64_t x = 0; x <= N; ++x) off[x] = 0;
+    for (int64_t x = 0; x < N; ++x)
+      if (prev[x] >= 0) ++off[prev[x] + 1];
+    for (int64_t x = 0; x < N; ++x) off[x + 1] += off[x];
+    std::vector<int32_t> fill(off, off + N);
+    for (int64_t x = 0; x < N; ++x)
+      if (prev[x] >= 0) sc[fill[prev[x]]++] = (int32_t)x;
   }
   return STP_OK;
 }

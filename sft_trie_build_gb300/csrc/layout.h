@@ -73,12 +73,12 @@ constexpr size_t kDsTileBytes = 128 * 128 * 2;  // one bf16 dS^T tile
 // Gated DeltaNet: tokens per chunk of the chunked recurrence, and the layout
 // of the host plan (int32 words; a header of kGdnHeader words, then arrays).
 constexpr int kGdnChunk = 64;
-constexpr int kGdnHeader = 20;
+constexpr int kGdnHeader = 24;
 constexpr int32_t kGdnMagic = 0x31444e47;  // "GDN1"
 enum GdnPlanField {
   GP_MAGIC = 0, GP_N, GP_NSEG, GP_NCHUNK, GP_NDEPTH, GP_WORDS, GP_PREV, GP_SEG_START, GP_SEG_LEN,
   GP_SEG_PARENT, GP_SEG_CHUNK0, GP_DEPTH_OFF, GP_CHUNK_START, GP_CHUNK_LEN, GP_MAX_DEPTH_SEGS, GP_PREV2, GP_PREV3,
-  GP_CHILD_OFF, GP_CHILD
+  GP_CHILD_OFF, GP_CHILD, GP_SUCC_OFF, GP_SUCC
 };
 
 // Non-empty pairs the dS workspace holds: the descriptor's max_tile_pairs, or

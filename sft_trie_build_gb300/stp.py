@@ -430,7 +430,7 @@ def stp_logprob_gather(desc: LogprobDesc, hidden, w_vocab, token_ids, loss_mask,
 # plan header fields (int32 words), as the library writes them
 GP_MAGIC, GP_N, GP_NSEG, GP_NCHUNK, GP_NDEPTH, GP_WORDS, GP_PREV, GP_SEG_START, GP_SEG_LEN, GP_SEG_PARENT, \
     GP_SEG_CHUNK0, GP_DEPTH_OFF, GP_CHUNK_START, GP_CHUNK_LEN, GP_MAX_DEPTH_SEGS, GP_PREV2, GP_PREV3, \
-    GP_CHILD_OFF, GP_CHILD = range(19)
+    GP_CHILD_OFF, GP_CHILD, GP_SUCC_OFF, GP_SUCC = range(21)
 
 
 def gdn_desc(n_rows, row_len, n_heads, head_dim=128, scale=None) -> GdnDesc:
@@ -463,7 +463,8 @@ def gdn_plan_arrays(plan: np.ndarray) -> dict:
             "seg_parent": at(GP_SEG_PARENT, ns), "seg_chunk0": at(GP_SEG_CHUNK0, ns),
             "depth_off": at(GP_DEPTH_OFF, nd + 1), "chunk_start": at(GP_CHUNK_START, nc),
             "chunk_len": at(GP_CHUNK_LEN, nc), "child_off": at(GP_CHILD_OFF, ns + 1),
-            "child": at(GP_CHILD, w[w[GP_CHILD_OFF] + ns] if ns > 0 else 0)}
+            "child": at(GP_CHILD, w[w[GP_CHILD_OFF] + ns] if ns > 0 else 0),
+            "succ_off": at(GP_SUCC_OFF, n + 1), "succ": at(GP_SUCC, w[w[GP_SUCC_OFF] + n] if n > 0 else 0)}
 
 
 def stp_gdn_workspace_size(desc: GdnDesc, plan: np.ndarray) -> int:

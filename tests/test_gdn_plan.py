@@ -58,6 +58,11 @@ def _check(plan_o, H=2):
         assert list(a["child"][a["child_off"][i]: a["child_off"][i + 1]]) == want_kids
     real = prev != -2
     assert np.all(covered[real] == 1) and np.all(covered[~real] == 0)
+    # successor lists: exactly the tokens whose path predecessor is x, ascending
+    so, sl = a["succ_off"], a["succ"]
+    for x in np.flatnonzero(n_child > 0).tolist() + [0, R * T - 1]:
+        assert list(sl[so[x]: so[x + 1]]) == list(np.flatnonzero(prev == x))
+    assert so[-1] == int((prev >= 0).sum()) and np.array_equal(np.diff(so), np.bincount(prev[prev >= 0], minlength=R * T))
     assert a["seg_chunk0"][-1] + (a["seg_len"][-1] + 63) // 64 == len(a["chunk_start"])
     return plan
 

@@ -2,11 +2,13 @@
 against the float64 oracle's reverse mode (oracle.gdn.gdn_row_grads) on the
 same inputs, for L = sum dO . o with dO ~ N(0, 1) on real tokens.
 
-Tolerance: the state gradients run in float32 but read the forward's bf16
-chunk operands (P, K~, Q~, W; relative 2^-9) and the forward states come
-from bf16 tensor-core products, so every gradient (dx, the convolution
-weights, dg, dbeta) stays within 5e-2 of its largest magnitude, mean error
-within 5e-3; pads get exactly 0.
+Tolerance: every product of the backward takes bf16 operands (relative
+rounding 2^-9 = 2e-3) with float32 sums, on top of the forward's bf16 chunk
+operands; a gradient passes through at most three such roundings in a chain
+(e.g. dS_n -> dV' -> dW -> dT -> dA -> dk), each adding about 2e-3 of its
+input's scale, so the error stays within 2e-2 of the gradient's largest
+magnitude (mean within 2e-3), the bar of the forward.  Observed on the GRPO
+row: at most 5.8e-3 (max) and 6.6e-4 (mean).  Pads get exactly 0.
 """
 import numpy as np
 import pytest
@@ -31,7 +33,8 @@ def _compare(po, H, seed):
                            ("dg", dg[real], want[2][real]), ("dbeta", db[real], want[3][real])):
         m = np.abs(ref).max()
         d = np.abs(got - ref)
-        assert d.max() <= 5e-2 * m and d.mean() <= 5e-3 * m, (name, d.max(), d.mean(), m)
+        print(name, float(d.max() / m), float(d.mean() / m))
+        assert d.max() <= 2e-2 * m and d.mean() <= 2e-3 * m, (name, d.max(), d.mean(), m)
 
 
 @pytest.mark.parametrize("seed", range(2))
@@ -68,5 +71,17 @@ def test_grpo_row_two_heads():
             m = np.abs(ref).max()
             d = np.abs(got - ref)
             errs[(h, name)] = (float(d.max() / m), float(d.mean() / m))
-            assert d.max() <= 5e-2 * m and d.mean() <= 5e-3 * m, (h, name, d.max(), d.mean(), m)
+            assert d.max() <= 2e-2 * m and d.mean() <= 2e-3 * m, (h, name, d.max(), d.mean(), m)
     print("\nGRPO row GDN backward, max / mean error relative to max |oracle|:", errs)
+
+
+def test_repeat_bit_identical():
+    """Every gradient is summed in one fixed order: two backward calls on the
+    same inputs give the same bits."""
+    b = W.random_forest(3, n_roots=3, max_depth=3, max_children=3, len_lo=1, len_hi=150, row_len=512,
+                        min_shared=4, vocab=41)
+    po = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared)
+    a = run_gdn_train(po, 2, seed=3)[0]
+    c = run_gdn_train(po, 2, seed=3)[0]
+    for x, y in zip(a, c):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
