@@ -10,7 +10,7 @@ import socket
 import numpy as np
 import pytest
 
-from sft_trie_build_gb300.shard import shard_units, unit_runs
+from sft_trie_build_gb300.shard import row_useful_pairs, shard_units, shard_units_weighted, unit_runs
 
 
 def _free_port():
@@ -42,9 +42,17 @@ def _rank_main(rank, world, port, out_dir):
         u0, u1 = shard_units(cinfo["n_rows"], 8, world, rank)
         shards = [None] * world
         dist.all_gather_object(shards, (u0, u1))
+        cplan = stp.stp_pack(ct, co, ctr, c.family, row_len=c.row_len, min_shared=64)
+        cmeta = stp.stp_plan_write(cplan)
+        gi = cmeta["gather_index"]
+        used = np.zeros(cinfo["n_rows"], np.int64)
+        np.maximum.at(used, gi // c.row_len, gi % c.row_len + 1)
+        work = row_useful_pairs(cmeta["position_ids"], used)
+        wshards = [None] * world
+        dist.all_gather_object(wshards, shard_units_weighted(work, 8, world, rank))
         t_max = max_over_ranks(10.0 + rank)
         np.savez(os.path.join(out_dir, f"rank{rank}.npz"), se=se, seed=b.seed, pairs=info["useful_pairs"],
-                 shards=np.array(shards), n_rows=cinfo["n_rows"], t_max=t_max)
+                 shards=np.array(shards), wshards=np.array(wshards), n_rows=cinfo["n_rows"], t_max=t_max)
     finally:
         dist.destroy_process_group()
 
@@ -65,10 +73,12 @@ def test_two_gloo_ranks(stp_lib, tmp_path):
     shards = r0["shards"]
     assert np.array_equal(shards, r1["shards"])
     n_units = int(r0["n_rows"]) * 8
-    covered = np.zeros(n_units, int)
-    for u0, u1 in shards:
-        covered[u0:u1] += 1
-    assert (covered == 1).all()
+    for sh in (shards, r0["wshards"]):
+        covered = np.zeros(n_units, int)
+        for u0, u1 in sh:
+            covered[u0:u1] += 1
+        assert (covered == 1).all()
+    assert np.array_equal(r0["wshards"], r1["wshards"])
 
 
 @pytest.mark.parametrize("rows,heads,world", [(1, 8, 2), (28, 8, 3), (5, 3, 4), (2, 1, 4)])
@@ -83,3 +93,38 @@ def test_shard_units_partition(rows, heads, world):
             seen[r * heads + g0: r * heads + g1] += 1
     assert (seen == 1).all()
     assert max(sizes) - min(sizes) <= 1
+
+
+@pytest.mark.parametrize("world", [2, 3, 4, 7])
+def test_weighted_shards_balance_work(stp_lib, world):
+    """On the global-tree batch (28 rows of very different work), work-weighted
+    shards partition the units, each rank's work stays within one unit's
+    weight of the mean, and the busiest rank carries no more than with
+    equal-count shards.  The work of a row is checked against the packer's
+    own count (stp_plan_info)."""
+    from sft_trie_build_gb300 import stp
+    from sft_trie_build_gb300 import workloads as W
+
+    c = W.curriculum(W.CONFIG_SEEDS["curriculum"])
+    t, o, tr = c.flat()
+    plan = stp.stp_pack(t, o, tr, c.family, row_len=c.row_len, min_shared=64)
+    info = stp.stp_plan_info(plan)
+    meta = stp.stp_plan_write(plan)
+    gi = meta["gather_index"]
+    R, H = info["n_rows"], 8
+    used = np.zeros(R, np.int64)
+    np.maximum.at(used, gi // c.row_len, gi % c.row_len + 1)
+    work = row_useful_pairs(meta["position_ids"], used)
+    assert int(work.sum()) == info["useful_pairs"]
+    unit_w = np.repeat(work, H)
+    covered = np.zeros(R * H, int)
+    wmax, cmax = 0, 0
+    for rank in range(world):
+        u0, u1 = shard_units_weighted(work, H, world, rank)
+        covered[u0:u1] += 1
+        wmax = max(wmax, unit_w[u0:u1].sum())
+        a, b = shard_units(R, H, world, rank)
+        cmax = max(cmax, unit_w[a:b].sum())
+    assert (covered == 1).all()
+    assert wmax <= unit_w.sum() / world + unit_w.max()
+    assert wmax <= cmax
