@@ -1062,7 +1062,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// Delta[r,h,i] = sum_d dO . O (bf16 in, f32), one warp per (row, token, head);
+// Delta[r,h,i] = sum_d dO . O (bf16 in, f32) for every (row, token, head);
 // writes the two bias tiles of the token's query tile: -LSE_i / scale and
 // -Delta_i, each as three bf16 terms (hi, mid, lo: hi = bf16(x), mid =
 // bf16(x - hi), lo = bf16(x - hi - mid)) in columns 0-2 of the query's row,
@@ -1082,33 +1082,51 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
                                                         uint8_t* __restrict__ sbias,
                                                         uint8_t* __restrict__ dbias, float inv_scale, int R,
                                                         int T, int Hq) {
-  const int lane = threadIdx.x & 31;
+  // 16 lanes per (token, head) row of 128 values, 16 bytes of O and of dO per
+  // lane; each half-warp takes kRowsPer rows per pass with all their loads
+  // issued first, so that enough bytes are in flight to stream O and dO
+  constexpr int kRowsPer = 4;
+  const int hl = threadIdx.x & 15;
+  const unsigned hmask = 0xffffu << (threadIdx.x & 16);   // the half-warps loop independently
   const size_t rows = (size_t)R * T * Hq;
   const int NT = T / 128;
-  for (size_t w = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < rows; w += (size_t)gridDim.x * 8) {
-    const uint2 a = reinterpret_cast<const uint2*>(o + w * 128)[lane];
-    const uint2 b = reinterpret_cast<const uint2*>(dout + w * 128)[lane];
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-    float acc = 0.f;
+  const size_t n_half = (size_t)gridDim.x * (blockDim.x / 16);
+  for (size_t w0 = ((size_t)blockIdx.x * (blockDim.x / 16) + (threadIdx.x >> 4)) * kRowsPer; w0 < rows;
+       w0 += n_half * kRowsPer) {
+    uint4 a[kRowsPer], b[kRowsPer];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const float2 x = __bfloat1622float2(a2[k]), y = __bfloat1622float2(b2[k]);
-      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    for (int k = 0; k < kRowsPer; ++k) {
+      const size_t w = w0 + k;
+      a[k] = b[k] = make_uint4(0, 0, 0, 0);
+      if (w < rows) {
+        a[k] = reinterpret_cast<const uint4*>(o + w * 128)[hl];
+        b[k] = reinterpret_cast<const uint4*>(dout + w * 128)[hl];
+      }
     }
 #pragma unroll
-    for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    if (lane < 2) {
-      const int h = (int)(w % Hq);
-      const size_t ri = w / Hq;
-      const size_t rr = ri / T, i = ri - rr * T;
-      const size_t tile = ((rr * Hq + h) * NT + i / 128) * kBiasTileBytes;
-      const int q = (int)(i & 127);
-      const size_t at = tile + (q >> 3) * 256 + (q & 7) * 16;
-      uint8_t* dst = lane == 0 ? sbias : dbias;
-      const float x = lane == 0 ? -lse[(rr * Hq + h) * T + i] * inv_scale : -acc;
-      *reinterpret_cast<uint4*>(dst + at) = bias_row(x);
-      *reinterpret_cast<uint4*>(dst + at + 128) = make_uint4(0u, 0u, 0u, 0u);
+    for (int k = 0; k < kRowsPer; ++k) {
+      const size_t w = w0 + k;
+      const uint32_t wa[4] = {a[k].x, a[k].y, a[k].z, a[k].w}, wb[4] = {b[k].x, b[k].y, b[k].z, b[k].w};
+      float acc = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc = fmaf(__uint_as_float(wa[q] << 16), __uint_as_float(wb[q] << 16), acc);
+        acc = fmaf(__uint_as_float(wa[q] & 0xffff0000u), __uint_as_float(wb[q] & 0xffff0000u), acc);
+      }
+#pragma unroll
+      for (int sft = 8; sft > 0; sft >>= 1) acc += __shfl_xor_sync(hmask, acc, sft);
+      if (w < rows && hl < 2) {
+        const int h = (int)(w % Hq);
+        const size_t ri = w / Hq;
+        const size_t rr = ri / T, i = ri - rr * T;
+        const size_t tile = ((rr * Hq + h) * NT + i / 128) * kBiasTileBytes;
+        const int q = (int)(i & 127);
+        const size_t at = tile + (q >> 3) * 256 + (q & 7) * 16;
+        uint8_t* dst = hl == 0 ? sbias : dbias;
+        const float x = hl == 0 ? -lse[(rr * Hq + h) * T + i] * inv_scale : -acc;
+        *reinterpret_cast<uint4*>(dst + at) = bias_row(x);
+        *reinterpret_cast<uint4*>(dst + at + 128) = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
   }
 }
