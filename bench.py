@@ -166,7 +166,7 @@ def _gdn(meta, dev, heads=16, reps=10) -> dict:
            "chunks": int(plan[stp.GP_NCHUNK]), "depths": int(plan[stp.GP_NDEPTH]), "ms": ms,
            "tokens_per_s": real / (ms / 1e3), "host_plan_ms": plan_ms,
            "launches_per_call": 2 + int(plan[stp.GP_NDEPTH])}
-    # training: the forward that keeps the chunk states, then the backward (float32 first version)
+    # training: the forward that keeps the chunk states, then the backward
     try:
         tws = torch.empty(stp.stp_gdn_train_workspace_size(desc, plan), dtype=torch.uint8, device=dev)
         d_o = torch.randn(R * T, heads, 128, device=dev)
@@ -535,6 +535,87 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+PROFILE_CASES = ("attn", "classify", "index", "logprob", "gdn", "gdn_train")
+
+
+def profile_case(name: str, reps: int) -> None:
+    """Untimed calls of one component on the benchmarked workload (one warm
+    call, then `reps`), for a profiler to capture: the command behind the
+    ncu summaries.  The attention keeps the dS tiles of two kv-head groups at
+    a time (results identical to all groups at once), so the case holds about
+    1.5 GB on the device."""
+    import torch
+
+    from sft_trie_build_gb300 import stp
+
+    dev = torch.device("cuda", 0)
+    b = _batch(0)
+    tokens, offsets, train = b.flat()
+    plan = stp.stp_pack(tokens, offsets, train, b.family, row_len=b.row_len, min_shared=b.min_shared)
+    info = stp.stp_plan_info(plan)
+    R, T = info["n_rows"], info["row_len"]
+    meta = stp.stp_plan_write(plan)
+    shape = W.attn_shape(WORKLOAD, R, T)
+    desc = stp.Desc(R, T, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, stp.STP_BF16, shape.scale,
+                    stp.stp_count_tile_pairs(meta["subtree_end"]), ds_groups=2)
+    buf = stp.Buffers(desc, dev)
+    se = torch.from_numpy(np.ascontiguousarray(meta["subtree_end"])).to(dev)
+    calls = []
+    if name in ("attn", "classify"):
+        q, k, v, do = (x.to(dev) for x in W.attn_tensors(shape, 17))
+        o, dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        lse = torch.empty(R, shape.n_q_heads, T, dtype=torch.float32, device=dev)
+
+        def attn():
+            stp.stp_classify(desc, se, buf.tile_meta)
+            if name == "attn":
+                stp.stp_attn_fwd(desc, q, k, v, se, buf.tile_meta, o, lse, buf.fwd_ws)
+                stp.stp_attn_bwd(desc, q, k, v, o, lse, do, se, buf.tile_meta, dq, dk, dv, buf.bwd_ws)
+        calls.append(attn)
+    elif name == "index":
+        stp.stp_classify(desc, se, buf.tile_meta)
+        q, k, w = (x.to(dev) for x in W.index_tensors(R, T, 8, 64, seed=23))
+        idesc = stp.index_desc(R, T, 8, 64, 512, desc.max_tile_pairs)
+        ws = torch.empty(stp.stp_index_workspace_size(idesc), dtype=torch.uint8, device=dev)
+        idx = torch.empty(R, T, 512, dtype=torch.int32, device=dev)
+        sc = torch.empty(R, T, 512, dtype=torch.float32, device=dev)
+        calls.append(lambda: stp.stp_index_topk(idesc, q, k, w, se, buf.tile_meta, idx, sc, ws))
+    elif name == "logprob":
+        h, w = (x.to(dev) for x in W.logprob_tensors(R * T, 4096, 151936, seed=29))
+        tok = torch.from_numpy(np.ascontiguousarray(meta["token_ids"])).to(dev)
+        mask = torch.from_numpy(np.ascontiguousarray(meta["loss_mask"])).to(dev)
+        ldesc = stp.logprob_desc(R, T, 4096, 151936)
+        ws = torch.empty(stp.stp_logprob_workspace_size(ldesc), dtype=torch.uint8, device=dev)
+        out = torch.empty(R * T, dtype=torch.float32, device=dev)
+        calls.append(lambda: stp.stp_logprob_gather(ldesc, h, w, tok, mask, out, ws))
+    else:   # gdn, gdn_train
+        gi = np.asarray(meta["gather_index"])
+        used = np.zeros(R, np.int64)
+        np.maximum.at(used, gi // T, gi % T + 1)
+        gdesc = stp.gdn_desc(R, T, 16)
+        gplan = stp.stp_gdn_plan(gdesc, meta["subtree_end"], used.astype(np.int32))
+        d_plan = torch.from_numpy(gplan).to(dev)
+        x, cw, g, beta = (t.to(dev) for t in W.gdn_tensors(R * T, 16, 128, seed=31))
+        o = torch.empty(R * T, 16, 128, dtype=torch.float32, device=dev)
+        if name == "gdn":
+            ws = torch.empty(stp.stp_gdn_workspace_size(gdesc, gplan), dtype=torch.uint8, device=dev)
+            calls.append(lambda: stp.stp_gdn_fwd(gdesc, gplan, d_plan, x, cw, g, beta, o, ws))
+        else:
+            ws = torch.empty(stp.stp_gdn_train_workspace_size(gdesc, gplan), dtype=torch.uint8, device=dev)
+            d_o = torch.randn(R * T, 16, 128, device=dev)
+            dx = torch.empty(R * T, 3 * 16 * 128, device=dev)
+            dw = torch.empty(3 * 16 * 128, 4, device=dev)
+            dg = torch.empty(R * T, 16, device=dev)
+            db = torch.empty(R * T, 16, device=dev)
+            calls.append(lambda: stp.stp_gdn_fwd_train(gdesc, gplan, d_plan, x, cw, g, beta, o, ws))
+            calls.append(lambda: stp.stp_gdn_bwd(gdesc, gplan, d_plan, x, cw, g, beta, d_o, dx, dw, dg, db, ws))
+    for _ in range(1 + reps):
+        for fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": name, "calls": 1 + reps, "workload": WORKLOAD}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -543,7 +624,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--chunks", type=int, default=8, help="kv-head groups of the host-buffer step")
+    ap.add_argument("--profile", choices=PROFILE_CASES, default=None,
+                    help="run one component untimed (1 + --reps calls) for a profiler; prints no bench line")
+    ap.add_argument("--reps", type=int, default=1)
     args = ap.parse_args()
+    if args.profile:
+        profile_case(args.profile, args.reps)
+        return
 
     peak, hbm, peak_kind = _peaks()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -772,7 +859,8 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e_tot / args.steps, "call": "stp_attn_step_host", "kv_head_groups": n_chunks,
                 "steps_in_flight": 2, "l2": "not flushed: every step re-uploads 336 MB of inputs (> L2)"},
-        "gpu_launches": 7 * args.steps,
+        # per step: three classification kernels, the forward, Delta, and dK/dV + dQ per kv-head group
+        "gpu_launches": (5 + 2 * min(Hkv, 8)) * args.steps,
     }
     if rank == 0:
         line["classify"] = _classify_bandwidth(desc, se, buf.tile_meta)

@@ -15,11 +15,14 @@
 // chunk's starting state S0 for the backward in gdn_bwd.cu):
 //   gdn_conv_kernel   one block per (64 tokens, q / k / v head): width-4 causal
 //                     convolution along each token's path (prev pointers of
-//                     the plan), SiLU, unit q and k heads; pads get o = 0.
+//                     the plan; the block's rows arrive by one TMA copy),
+//                     SiLU, unit q and k heads; pads get o = 0.
 //   gdn_prep_kernel   one block per (chunk, head): [Q K^T; K K^T] on the tensor
-//                     core, then in float32 on the CUDA cores the
-//                     unit-lower-triangular solve for U^ and W (one column per
-//                     thread), and the chunk's operands
+//                     core; T = (I + A)^{-1} of the unit-lower-triangular
+//                     system in float32 on 64 threads (a column each); then
+//                     U^ = T diag(beta) V and W = T diag(beta e^gam) K on the
+//                     tensor core (T split into bf16 hi + lo, so the products
+//                     keep ~16 bits), and the chunk's operands
 //                     [Q~; W] (Q~ = scale e^{gam} Q), K~ = e^{gam_L - gam} K,
 //                     P = scale (Q K^T o Gamma) in bf16, U^ transposed in
 //                     float32 and e^{gam_L}.  Nothing here depends on a state.
@@ -53,15 +56,17 @@ constexpr int kPrepThreads = 256;
 constexpr int kStThreads = 192;   // warps 0-3 epilogue, 4 loads, 5 MMA
 
 // gdn_prep_kernel shared memory, from a 1024-byte aligned base: [Q; K] as a
-// 128 x 128 bf16 K-major operand (128-byte swizzle, two 64-column halves),
-// V bf16 [64][128], A float32 [64][68] (rows 16-byte aligned), gam, beta,
-// e^gam, e^{gam_L - gam} [64], the MMA barrier and the TMEM address.
+// 128 x 128 bf16 K-major operand (128-byte swizzle, two 64-column halves);
+// V bf16 as a 64 x 128 MN-major operand (two 64-column halves of 64 rows);
+// A float32 column-major [64][68] (columns 16-byte aligned); the two split
+// halves (hi, lo) of [T diag(beta); T diag(beta e^gam)] as 128 x 64 bf16
+// K-major operands; gam, beta, e^gam, e^{gam_L - gam} [64]; the MMA barrier
+// and the TMEM address.
 constexpr int kPrepLa = 68;
-constexpr int kPoV = 32768, kPoA = kPoV + 16384, kPoGam = kPoA + kGc * kPrepLa * 4, kPoBeta = kPoGam + 256,
+constexpr int kPoV = 32768, kPoA = kPoV + 16384, kPoT = 67584, kPoGam = kPoT + 32768, kPoBeta = kPoGam + 256,
               kPoEg = kPoBeta + 256, kPoEk = kPoEg + 256, kPoBar = kPoEk + 256;
 constexpr int kPrepSmem = kPoBar + 64 + 1024;
-constexpr int kStgLd = 257;   // output staging rows, after the solve: [64][257] float32 over the areas above
-static_assert(kGc * kStgLd * 4 <= kPoGam, "output staging must fit below the row scalars");
+static_assert(kPoA + kGc * kPrepLa * 4 <= kPoT && kPoT % 1024 == 0, "prep shared-memory layout");
 
 // gdn_state_kernel shared memory, from a 1024-byte aligned base.  A stage holds
 // [Q~; W] (32 KB), K~ (16 KB) and P (8 KB); P is the top half of a 128-row MMA
@@ -137,6 +142,20 @@ bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, int b
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// x [rows, cols] bf16 as a 2-D tensor; boxes of 128 columns x kConvRows rows,
+// no swizzle (rows of 256 bytes in shared memory).
+bool make_map_x(CUtensorMap* m, const void* base, int64_t rows, int cols, int box_rows) {
+  EncodeFn enc = encode_gdn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 __device__ __forceinline__ void tma_load_2d_g(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -148,6 +167,11 @@ __device__ __forceinline__ void tma_load_2d_g(void* dst, const CUtensorMap* map,
 // MN-major 128-byte-swizzled operand whose 64-element halves lie 8 KB apart.
 __device__ __forceinline__ uint32_t desc_lo_mn8k(uint32_t addr) {
   return ((addr & 0x3FFFFu) >> 4) | ((8192u >> 4) << 16);
+}
+
+// The same with the halves 16 KB apart (the K rows of the [Q; K] tile).
+__device__ __forceinline__ uint32_t desc_lo_mn16k(uint32_t addr) {
+  return ((addr & 0x3FFFFu) >> 4) | ((16384u >> 4) << 16);
 }
 
 __device__ __forceinline__ void unpack8(const uint4 r, float* f) {
@@ -162,14 +186,31 @@ __device__ __forceinline__ void unpack8(const uint4 r, float* f) {
 // ---------------------------------------------------------------------------
 // Path convolution + SiLU + unit q, k heads.  Block = (64 tokens, one group of
 // 128 channels: a q, k or v head); thread = (token of 16, 8 channels), so the
-// 16 lanes of one token hold one head and its weights stay in registers.
-__global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const GdnParams p) {
-  const int grp = blockIdx.y, lt = threadIdx.x >> 4, vec = threadIdx.x & 15;
-  const int ch = grp * kGd + vec * 8;
-  const bool is_qk = grp < 2 * p.H;
+// 16 lanes of a token hold one head and its weights stay in registers.  One
+// TMA copy brings the block's x rows xb-3 .. xb+63 of the group (zero rows
+// outside the tensor) into shared memory; inside a segment the taps of token
+// x are x-3 .. x, all in that tile, and a tap is read from memory only where
+// the path turns (a segment's first tokens, whose taps lie in the parent).
+constexpr int kConvRows = 64 + 3;
+
+__global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_constant__ CUtensorMap mx,
+                                                                const GdnParams p) {
+  __shared__ __align__(128) uint8_t xs[kConvRows * kGd * 2];   // [67 rows][128 channels] bf16
   __shared__ int taps[64][3];   // the 1, 2 and 3 tokens back on each token's path (-2: pad or past the end)
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const int grp = blockIdx.y, lt = threadIdx.x >> 4, vec = threadIdx.x & 15;
+  const int ch = grp * kGd + vec * 8, xb = blockIdx.x * 64;
+  const bool is_qk = grp < 2 * p.H;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    mbar_expect_tx(&bar, kConvRows * kGd * 2);
+    tma_load_2d_g(xs, &mx, &bar, grp * kGd, xb - 3);
+  }
   if (threadIdx.x < 64) {
-    const int x = blockIdx.x * 64 + threadIdx.x;
+    const int x = xb + threadIdx.x;
     const bool in = x < p.N;
     taps[threadIdx.x][0] = in ? p.prev[x] : -2;
     taps[threadIdx.x][1] = in ? p.prev2[x] : -1;
@@ -179,11 +220,15 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const GdnParams 
 #pragma unroll
   for (int i = 0; i < 8; ++i) wv[i] = reinterpret_cast<const float4*>(p.conv_w)[ch + i];
   __syncthreads();
+  if (!mbar_wait(&bar, 0, &abort_flag, p.err)) {   // gave up: let the copy land, then leave
+    mbar_wait_drain(&bar, 0);
+    return;
+  }
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
-    const int x = blockIdx.x * 64 + it * 16 + lt;
+    const int tl = it * 16 + lt, x = xb + tl;
     const bool in = x < p.N;
-    const int p1 = taps[it * 16 + lt][0];
+    const int p1 = taps[tl][0];
     if (p1 == -2) {
       if (in && grp < p.H) {   // a pad: o = 0 for head grp
         float4* o4 = reinterpret_cast<float4*>(p.o + ((size_t)x * p.H + grp) * kGd + vec * 8);
@@ -191,15 +236,19 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const GdnParams 
       }
       continue;   // all 16 lanes of a token take the same branch
     }
-    const int src[4] = {taps[it * 16 + lt][2], taps[it * 16 + lt][1], p1, x};   // taps 0..3
+    const int src[4] = {taps[tl][2], taps[tl][1], p1, x};   // taps 0..3
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       if (src[t] < 0) continue;
+      const int r = src[t] - (xb - 3);
+      const uint4 v = (r >= 0 && r < kConvRows)
+                          ? *reinterpret_cast<const uint4*>(xs + r * (kGd * 2) + vec * 16)
+                          : *reinterpret_cast<const uint4*>(p.x + (size_t)src[t] * p.C + ch);
       float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(p.x + (size_t)src[t] * p.C + ch), f);
+      unpack8(v, f);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float w = t == 0 ? wv[i].x : t == 1 ? wv[i].y : t == 2 ? wv[i].z : wv[i].w;
@@ -233,21 +282,17 @@ __global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const GdnParams 
 // ---------------------------------------------------------------------------
 // Per (chunk, head): everything of the chunk that does not depend on a state.
 // [Q K^T; K K^T] is one tcgen05 pass (M = 128, N = 64, K = 128) into TMEM; the
-// triangular solve and the operand scaling run on the CUDA cores in float32.
-
-// bf16 element (m, c) of the swizzled [Q; K] operand
-__device__ __forceinline__ float qk_at(const uint8_t* tile, int m, int c) {
-  const uint16_t u = *reinterpret_cast<const uint16_t*>(tile + (c >> 6) * 16384 + m * 128 +
-                                                        ((((c & 63) >> 3) ^ (m & 7)) << 4) + (c & 7) * 2);
-  return __uint_as_float((uint32_t)u << 16);
-}
+// inverse of the unit-lower-triangular I + A runs on the CUDA cores in
+// float32, and its products with V and K are two more tcgen05 passes
+// (M = 128, N = 128, K = 64, hi and lo halves of T accumulated).
 
 __global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnParams p) {
   extern __shared__ uint8_t prep_dyn[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(prep_dyn) + 1023) & ~uintptr_t(1023));
   uint8_t* tile = sm;                                              // [Q; K]
-  __nv_bfloat16* sv = reinterpret_cast<__nv_bfloat16*>(sm + kPoV);  // [64][128]
-  float* sA = reinterpret_cast<float*>(sm + kPoA);                 // [64][68]
+  uint8_t* sv = sm + kPoV;                                         // V, MN-major operand
+  float* sA = reinterpret_cast<float*>(sm + kPoA);                 // [64 columns][68]
+  uint8_t* sT = sm + kPoT;                                         // [T'; T''] hi, then lo
   float* sgam = reinterpret_cast<float*>(sm + kPoGam);
   float* sbeta = reinterpret_cast<float*>(sm + kPoBeta);
   float* seg = reinterpret_cast<float*>(sm + kPoEg);               // e^{gam_t}
@@ -267,22 +312,31 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnPara
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, 64);
+    tmem_alloc(tmem_slot, 256);
     tmem_relinquish();
   }
-  for (int i = tid; i < kGc * 16; i += kPrepThreads) {
-    const int t = i >> 4, c = (i & 15) * 8;
-    uint4 rq = make_uint4(0, 0, 0, 0), rk = rq, rv = rq;
-    if (t < L) {
-      const __nv_bfloat16* yr = p.y + (size_t)(x0 + t) * p.C + h * kGd + c;
-      rq = *reinterpret_cast<const uint4*>(yr);
-      rk = *reinterpret_cast<const uint4*>(yr + Hd);
-      rv = *reinterpret_cast<const uint4*>(yr + 2 * Hd);
+  {   // all twelve 16-byte loads of a thread in flight before any is stored
+    constexpr int kIt = kGc * 16 / kPrepThreads;
+    uint4 rq[kIt], rk[kIt], rv[kIt];
+#pragma unroll
+    for (int u = 0; u < kIt; ++u) {
+      const int i = tid + u * kPrepThreads, t = i >> 4, c = (i & 15) * 8;
+      rq[u] = rk[u] = rv[u] = make_uint4(0, 0, 0, 0);
+      if (t < L) {
+        const __nv_bfloat16* yr = p.y + (size_t)(x0 + t) * p.C + h * kGd + c;
+        rq[u] = *reinterpret_cast<const uint4*>(yr);
+        rk[u] = *reinterpret_cast<const uint4*>(yr + Hd);
+        rv[u] = *reinterpret_cast<const uint4*>(yr + 2 * Hd);
+      }
     }
-    const int off = (c >> 6) * 16384 + ((((c & 63) >> 3) ^ (t & 7)) << 4);
-    *reinterpret_cast<uint4*>(tile + off + t * 128) = rq;
-    *reinterpret_cast<uint4*>(tile + off + (kGc + t) * 128) = rk;
-    *reinterpret_cast<uint4*>(sv + t * kGd + c) = rv;
+#pragma unroll
+    for (int u = 0; u < kIt; ++u) {
+      const int i = tid + u * kPrepThreads, t = i >> 4, c = (i & 15) * 8;
+      const int off = (c >> 6) * 16384 + ((((c & 63) >> 3) ^ (t & 7)) << 4);
+      *reinterpret_cast<uint4*>(tile + off + t * 128) = rq[u];
+      *reinterpret_cast<uint4*>(tile + off + (kGc + t) * 128) = rk[u];
+      *reinterpret_cast<uint4*>(sv + (c >> 6) * 8192 + t * 128 + ((((c & 63) >> 3) ^ (t & 7)) << 4)) = rv[u];
+    }
   }
   if (tid < kGc) {
     sgam[tid] = tid < L ? p.g[(size_t)(x0 + tid) * p.H + h] : 0.f;
@@ -342,7 +396,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnPara
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int j = j0 + q + e;
-          f[e] = (ready && j <= i && i < L) ? p.scale * expf(gi - sgam[j]) * __uint_as_float(v[q + e]) : 0.f;
+          f[e] = (ready && j <= i && i < L) ? p.scale * __expf(gi - sgam[j]) * __uint_as_float(v[q + e]) : 0.f;
         }
         pw[q / 2] = pack_bf16x2(f[0], f[1]);
       }
@@ -355,69 +409,120 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnPara
 #pragma unroll
       for (int q = 0; q < 32; ++q) {
         const int j = j0 + q;
-        sA[i * kPrepLa + j] = (ready && j < i) ? bi * expf(gi - sgam[j]) * __uint_as_float(v[q]) : 0.f;
+        sA[j * kPrepLa + i] = (ready && j < i) ? bi * __expf(gi - sgam[j]) * __uint_as_float(v[q]) : 0.f;
       }
     }
   }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 0) tmem_dealloc(tmem, 64);
 
-  // Q~ (rows 0..63 of the [Q~; W] tile) and K~
-  for (int i = tid; i < kGc * kGd / 2; i += kPrepThreads) {
-    const int t = i / (kGd / 2), c = 2 * (i % (kGd / 2));
-    const float eq = t < L ? p.scale * seg[t] : 0.f, ek = t < L ? sek[t] : 0.f;
-    reinterpret_cast<uint32_t*>(p.wq + (row * 128 + t) * kGd + c)[0] =
-        pack_bf16x2(eq * qk_at(tile, t, c), eq * qk_at(tile, t, c + 1));
-    reinterpret_cast<uint32_t*>(p.kt + (row * kGc + t) * kGd + c)[0] =
-        pack_bf16x2(ek * qk_at(tile, kGc + t, c), ek * qk_at(tile, kGc + t, c + 1));
-  }
-
-  // (I + A) X = B by forward substitution, one column per thread:
-  // columns 0-127 give U^ (B = beta V), 128-255 give W (B = beta e^gam K).
-  // A is strictly lower with zeros above, so row t can be read 4 wide up to
-  // the multiple of 4 past t - 1 (those X are still 0).
-  float X[kGc];
-  {
-    const int col = tid;
+  if (warp < 2) {
+    // T = (I + A)^{-1}, column s per thread, column-oriented substitution
+    // (once T[t][s] is final it is taken out of every later row).  A is
+    // column-major with zeros on and above the diagonal, so column t is read
+    // 4 wide from the multiple of 4 at or below t + 1.  Then T' = T diag(beta)
+    // and T'' = T diag(beta e^gam), split into bf16 hi + lo, go to the
+    // operand tiles (rows 0-63 T', rows 64-127 T'', K index s).
+    const int sc = tid;
+    float x[kGc];
 #pragma unroll
-    for (int t = 0; t < kGc; ++t) X[t] = 0.f;
+    for (int t = 0; t < kGc; ++t) x[t] = t == sc ? 1.f : 0.f;
+#pragma unroll
+    for (int t = 0; t < kGc - 1; ++t) {
+      const float xt = x[t];
+#pragma unroll
+      for (int r4 = ((t + 1) & ~3); r4 < kGc; r4 += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(sA + t * kPrepLa + r4);
+        x[r4] = fmaf(-a.x, xt, x[r4]);
+        x[r4 + 1] = fmaf(-a.y, xt, x[r4 + 1]);
+        x[r4 + 2] = fmaf(-a.z, xt, x[r4 + 2]);
+        x[r4 + 3] = fmaf(-a.w, xt, x[r4 + 3]);
+      }
+    }
+    const float b1 = sbeta[sc], b2 = sbeta[sc] * seg[sc];
+    const int kcol = ((sc >> 3) << 4) + (sc & 7) * 2;
 #pragma unroll
     for (int t = 0; t < kGc; ++t) {
-      float b = col < kGd ? sbeta[t] * __bfloat162float(sv[t * kGd + col])
-                          : sbeta[t] * seg[t] * qk_at(tile, kGc + t, col - kGd);
 #pragma unroll
-      for (int s4 = 0; s4 < t; s4 += 4) {
-        const float4 a = *reinterpret_cast<const float4*>(sA + t * kPrepLa + s4);
-        b = fmaf(-a.x, X[s4], b);
-        b = fmaf(-a.y, X[s4 + 1], b);
-        b = fmaf(-a.z, X[s4 + 2], b);
-        b = fmaf(-a.w, X[s4 + 3], b);
+      for (int part = 0; part < 2; ++part) {
+        const int m = part * kGc + t;
+        const float v = x[t] * (part ? b2 : b1);
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+        const int off = m * 128 + (kcol ^ ((m & 7) << 4));
+        *reinterpret_cast<__nv_bfloat16*>(sT + off) = hi;
+        *reinterpret_cast<__nv_bfloat16*>(sT + 16384 + off) = lo;
       }
-      X[t] = b;
+    }
+  } else {
+    // Q~ (rows 0..63 of the [Q~; W] tile) and K~, 8 channels (16 bytes) per item
+    for (int it = tid - 64; it < 2 * kGc * 16; it += kPrepThreads - 64) {
+      const int m = it >> 4, c = (it & 15) * 8, t = m & (kGc - 1);   // m < 64: a Q row, else a K row
+      const float sc = t < L ? (m < kGc ? p.scale * seg[t] : sek[t]) : 0.f;
+      const uint4 r = *reinterpret_cast<const uint4*>(tile + (c >> 6) * 16384 + m * 128 +
+                                                      ((((c & 63) >> 3) ^ (m & 7)) << 4));
+      float f[8];
+      unpack8(r, f);
+      const uint4 o = make_uint4(pack_bf16x2(sc * f[0], sc * f[1]), pack_bf16x2(sc * f[2], sc * f[3]),
+                                 pack_bf16x2(sc * f[4], sc * f[5]), pack_bf16x2(sc * f[6], sc * f[7]));
+      __nv_bfloat16* dst = m < kGc ? p.wq + (row * 128 + t) * kGd + c : p.kt + (row * kGc + t) * kGd + c;
+      *reinterpret_cast<uint4*>(dst) = o;
     }
   }
-  // The columns go out through shared memory (the operand, V and A areas are
-  // free now), rows padded to 257 floats, so that the global stores are
-  // contiguous: U^ transposed ([column][t]) and W (rows 64..127 of the tile).
+  fence_proxy_async_smem();
+  fence_before_sync();
   __syncthreads();
-  float* stg = reinterpret_cast<float*>(sm);   // [64][257]
+  fence_after_sync();
+  // [T'; T''] (hi + lo) x V into columns 0-127 (rows 0-63: U^ = T' V) and
+  // x K into columns 128-255 (rows 64-127: W = T'' K); the [Q K^T; K K^T]
+  // accumulator in columns 0-63 was read above.
+  if (tid == 0) {
+    constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 1);
+    const uint32_t ta = smem_u32(sT), tv = smem_u32(sv), tk = smem_u32(tile) + 8192;
 #pragma unroll
-  for (int t = 0; t < kGc; ++t) stg[t * kStgLd + tid] = X[t];
-  __syncthreads();
-  for (int i = tid; i < kGd * kGc / 4; i += kPrepThreads) {
-    const int col = i / (kGc / 4), t = 4 * (i % (kGc / 4));
-    reinterpret_cast<float4*>(p.ut + (row * kGd + col) * kGc)[t / 4] =
-        make_float4(stg[t * kStgLd + col], stg[(t + 1) * kStgLd + col], stg[(t + 2) * kStgLd + col],
-                    stg[(t + 3) * kStgLd + col]);
+    for (int hl = 0; hl < 2; ++hl)
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const uint32_t a = desc_lo_kmajor(ta + hl * 16384 + s4 * 32);
+        mma_ss_lo(tmem, a, desc_lo_mn8k(tv + s4 * 2048), idesc, (hl | s4) ? 1u : 0u);
+        mma_ss_lo(tmem + 128, a, desc_lo_mn16k(tk + s4 * 2048), idesc, (hl | s4) ? 1u : 0u);
+      }
+    mma_commit(bar);
   }
-  for (int i = tid; i < kGc * kGd / 2; i += kPrepThreads) {
-    const int t = i / (kGd / 2), c = 2 * (i % (kGd / 2));
-    reinterpret_cast<uint32_t*>(p.wq + (row * 128 + kGc + t) * kGd + c)[0] =
-        pack_bf16x2(stg[t * kStgLd + kGd + c], stg[t * kStgLd + kGd + c + 1]);
+  {
+    const bool ready = mbar_wait(bar, 1, abort_flag, p.err);
+    fence_after_sync();
+    // warp w reads TMEM rows 32 (w % 4) .. + 31 (thread = row), columns half (w / 4) of 64
+    const int q4 = warp & 3, half = warp >> 2, m = 32 * q4 + lane;
+    const uint32_t lrow = (uint32_t)(32 * q4) << 16;
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t v[32];
+      const int d0 = half * 64 + cc * 32;
+      tmem_ld32(tmem + lrow + (q4 < 2 ? 0 : 128) + d0, v);
+      tmem_ld_wait();
+      if (!ready) continue;
+      if (q4 < 2) {   // U^ transposed: [d][t], a warp writes 128 contiguous bytes per d
+        float* dst = p.ut + (row * kGd + d0) * kGc + m;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dst[(size_t)j * kGc] = __uint_as_float(v[j]);
+      } else {        // W: bf16 rows 64..127 of the [Q~; W] tile
+        uint4* dst = reinterpret_cast<uint4*>(p.wq + (row * 128 + m) * kGd + d0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
+                              pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                              pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                              pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+      }
+    }
   }
   if (tid == 0) p.decay[row] = expf(sgam[L - 1]);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
@@ -749,7 +854,9 @@ stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d
   p.state = reinterpret_cast<float*>(ws + L.state);
   p.s0 = train ? reinterpret_cast<float*>(ws + L.s0) : nullptr;
   p.o = o;
-  CUtensorMap mwq, mkt, mpm;
+  CUtensorMap mwq, mkt, mpm, mx;
+  if (N > 0 && !make_map_x(&mx, p.x, N, (int)p.C, kConvRows))
+    return fail(STP_ECUDA, "stp_gdn_fwd: tensor map encoding failed");
   if (n_chunk > 0 &&
       (!make_map_2d(&mwq, p.wq, (int64_t)n_chunk * H * 128, kGd, 128) ||
        !make_map_2d(&mkt, p.kt, (int64_t)n_chunk * H * kGc, kGd, kGc) ||
@@ -765,7 +872,7 @@ stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d
   cudaError_t e = attr_err;
   if (e == cudaSuccess) e = cudaMemsetAsync(p.err, 0, 4, s);
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e));
-  gdn_conv_kernel<<<dim3((unsigned)((N + 63) / 64), (unsigned)(3 * H)), kConvThreads, 0, s>>>(p);
+  if (N > 0) gdn_conv_kernel<<<dim3((unsigned)((N + 63) / 64), (unsigned)(3 * H)), kConvThreads, 0, s>>>(mx, p);
   if (n_chunk > 0) gdn_prep_kernel<<<(unsigned)(n_chunk * H), kPrepThreads, kPrepSmem, s>>>(p);
   const int32_t* depth_off = w + w[GP_DEPTH_OFF];
   for (int d = 0; d < n_depth; ++d) {

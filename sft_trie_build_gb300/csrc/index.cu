@@ -15,15 +15,20 @@
 //                        spread over the chip): the tile's Q of every
 //                        indexer head once (TMA), the piece's key tiles
 //                        through a two-stage ring; S_h = Q_h K^T on tcgen05
-//                        (four heads per pass in TMEM), and four epilogue
-//                        warps (thread = query = TMEM lane) accumulate
+//                        (two heads per pass, two passes' accumulators in
+//                        TMEM, so the next pass runs while the epilogue reads
+//                        this one), and eight epilogue
+//                        warps (thread = query = TMEM lane, each warp half
+//                        of the keys) accumulate
 //                        w * relu(S) in registers, apply the predicate on
-//                        PARTIAL tiles and write the tile's scores key-major
-//                        ([128 keys][128 queries] fp32) to the pair's slot.
-//   index_select_kernel  one CTA per (row, query tile): byte-wise radix
-//                        select of each query's k-th largest candidate score
-//                        (histograms in shared memory), then the keys above
-//                        it, and the ties it needs, emitted in ascending order.
+//                        PARTIAL tiles and write the tile's scores
+//                        query-major ([128 queries][128 keys] fp32: one
+//                        512-byte row per query) to the pair's slot.
+//   index_select_kernel  one warp per query: byte-wise radix select of its
+//                        k-th largest candidate score over its score rows (a
+//                        256-bin histogram in shared memory per warp),
+//                        then the keys above it, and the ties it needs,
+//                        emitted in ascending order.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -39,15 +44,14 @@ namespace {
 
 using namespace tc;
 
-constexpr int kIdxThreads = 192;       // warps 0-3 epilogue, warp 4 TMA, warp 5 MMA
-constexpr int kIdxSlots = 4;           // heads per TMEM pass (128 columns each)
+constexpr int kIdxThreads = 320;       // warps 0-7 epilogue, warp 8 TMA, warp 9 MMA
+constexpr int kIdxTma = 8, kIdxMma = 9;
+constexpr int kIdxMaxHeads = 8;        // n_heads * head_dim <= 512 and head_dim >= 64
+constexpr int kIdxSlots = 2;           // heads per TMEM pass (128 columns each); two passes' buffers
 constexpr int kIdxQBytesMax = 131072;  // Q of all heads: H * D * 256 bytes
 constexpr int kIdxSmallBytes = 256;
-constexpr int kScoreTile = 128 * 128;  // floats per (pair) score tile
+constexpr int kScoreTile = 128 * 128;  // keys per (pair) score tile
 constexpr int kIdxPiece = 8;           // key tiles of one query tile's list per scoring CTA
-constexpr int kSelThreads = 1024;  // 32 warps: 2 query groups x 16 key-tile ranges
-constexpr int kSelQ = 64;          // queries per selection CTA (half a query tile)
-constexpr int kSelSplit = 32 / (kSelQ / 32);
 
 struct IdxParams {
   int R, T, NT, H, D, top_k, splits;   // splits: scoring CTAs per query tile
@@ -58,13 +62,13 @@ struct IdxParams {
   const int32_t* csr_off;
   const int32_t* row_base;
   const float* w;       // [R*T, H]
-  float* scores;        // [cap][128 keys][128 queries]
+  uint32_t* scores;     // [cap][128 queries][128 keys]: order keys of the scores, 0 = not visible
   int32_t* out_idx;     // [R*T, k]
   float* out_score;     // [R*T, k]
   uint32_t* err;
 };
 
-enum { X_Q = 0, X_KF = 1, X_KE = 3, X_SF = 5, X_SFREE = 6, X_DRAIN = 7, X_COUNT = 8 };
+enum { X_Q = 0, X_KF = 1, X_KE = 3, X_SF = 5, X_SFREE = 7, X_DRAIN = 9, X_COUNT = 10 };
 
 typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -98,6 +102,18 @@ bool make_map_d(CUtensorMap* m, const void* base, int64_t rows, int H, int D) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// float -> uint32 with the same order (larger float, larger key).  Every
+// float but a NaN maps above 0 (-inf to 0x007fffff), so 0 is free to mark a
+// key that is not visible.
+__device__ __forceinline__ uint32_t order_key(float s) {
+  const uint32_t u = __float_as_uint(s);
+  return (u >> 31) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key >> 31) ? (key & 0x7fffffffu) : ~key);
+}
+
 __global__ void __launch_bounds__(kIdxThreads, 1)
     index_scores_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                         const IdxParams p) {
@@ -124,7 +140,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   const int n_groups = (p.H + kIdxSlots - 1) / kIdxSlots;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < X_COUNT; ++b) mbar_init(&bars[b], b == X_SFREE ? 4 : 1);
+    for (int b = 0; b < X_COUNT; ++b) mbar_init(&bars[b], (b == X_SFREE || b == X_SFREE + 1) ? 8 : 1);
     *abort_flag = 0;
     if ((big_s & 1023u) != 0 || cnt <= 0 || cnt > p.NT) {
       *abort_flag = 1;
@@ -132,7 +148,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     }
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kIdxMma) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -142,7 +158,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const bool run = !*abort_flag;
 
-  if (warp == 4) {
+  if (warp == kIdxTma) {
     if (lane == 0 && run) {
       // ------------------------------------------------------------ loads
       tma_prefetch_desc(&tq);
@@ -171,7 +187,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (issued[st] >= 0) mbar_wait_drain(&bars[X_KF + st], issued[st] & 1);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kIdxMma) {
     if (lane == 0 && run) {
       // ------------------------------------------------------------ MMA
       constexpr uint32_t idesc = idesc_bf16(128, 128, 0, 0);
@@ -184,16 +200,19 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         if (!mbar_wait(&bars[X_KF + st], ((e - e0) >> 1) & 1, abort_flag, p.err)) break;
         const uint32_t k_km = desc_lo_kmajor(big_s + q_bytes + st * tile_bytes);
         for (int hg = 0; ok && hg < n_groups; ++hg, ++u) {
-          if (u > 0 && !mbar_wait(&bars[X_SFREE], (u - 1) & 1, abort_flag, p.err)) {
+          // pass u fills buffer u & 1 once the epilogue has read pass u - 2 from it
+          const int bu = u & 1;
+          if (u > 1 && !mbar_wait(&bars[X_SFREE + bu], ((u - 2) >> 1) & 1, abort_flag, p.err)) {
             ok = false;
             break;
           }
           fence_after_sync();
           for (int hs = 0; hs < kIdxSlots && kIdxSlots * hg + hs < p.H; ++hs) {
             const uint32_t q_km = desc_lo_kmajor(big_s + (kIdxSlots * hg + hs) * tile_bytes);
-            for (int kk = 0; kk < nk; ++kk) mma_ss_lo(tmem + hs * 128, q_km + km(kk), k_km + km(kk), idesc, kk > 0);
+            for (int kk = 0; kk < nk; ++kk)
+              mma_ss_lo(tmem + bu * 256 + hs * 128, q_km + km(kk), k_km + km(kk), idesc, kk > 0);
           }
-          mma_commit(&bars[X_SF]);
+          mma_commit(&bars[X_SF + bu]);
         }
         if (ok) mma_commit(&bars[X_KE + st]);
       }
@@ -203,37 +222,47 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int il = threadIdx.x;                 // query row = TMEM lane
+    // warp w: query rows 32 (w % 4) .. + 31 (thread = TMEM lane), keys 64 (w / 4) .. + 63
+    const int il = 32 * (warp & 3) + lane, kh = 64 * (warp >> 2);
     const int i = qt * 128 + il;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const float* wrow = p.w + ((size_t)row0 + i) * p.H;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    float wreg[kIdxMaxHeads];   // this query's head weights
+    {
+      const float* wrow = p.w + ((size_t)row0 + i) * p.H;
+#pragma unroll
+      for (int h = 0; h < kIdxMaxHeads; ++h) wreg[h] = h < p.H ? wrow[h] : 0.f;
+    }
     bool ok = run;
     int u = 0;
     for (int e = e0; ok && e < e1; ++e) {
       const int ent = list[e], kt = ent >> 1, part = ent & 1;
-      float acc[128];
+      float acc[64];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+      for (int j = 0; j < 64; ++j) acc[j] = 0.f;
       for (int hg = 0; hg < n_groups; ++hg, ++u) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars[X_SF], u & 1, abort_flag, p.err))) {
+        const int bu = u & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars[X_SF + bu], (u >> 1) & 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
         fence_after_sync();
-        for (int hs = 0; hs < kIdxSlots && kIdxSlots * hg + hs < p.H; ++hs) {
-          const float wi = wrow[kIdxSlots * hg + hs];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t x[32];
-            tmem_ld32(tmem + lane_base + hs * 128 + c * 32, x);
-            tmem_ld_wait();
+        for (int hs = 0; hs < kIdxSlots; ++hs) {
+          if (kIdxSlots * hg + hs >= p.H) break;
+          float wi = wreg[0];
 #pragma unroll
-            for (int m = 0; m < 32; ++m) acc[c * 32 + m] = fmaf(wi, fmaxf(__uint_as_float(x[m]), 0.f), acc[c * 32 + m]);
-          }
+          for (int h = 1; h < kIdxMaxHeads; ++h)
+            if (h == kIdxSlots * hg + hs) wi = wreg[h];
+          uint32_t x[64];
+          tmem_ld32(tmem + lane_base + bu * 256 + hs * 128 + kh, x);
+          tmem_ld32(tmem + lane_base + bu * 256 + hs * 128 + kh + 32, x + 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int m = 0; m < 64; ++m) acc[m] = fmaf(wi, fmaxf(__uint_as_float(x[m]), 0.f), acc[m]);
         }
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[X_SFREE]);
+        if (lane == 0) mbar_arrive(&bars[X_SFREE + bu]);
       }
       if (!ok) break;
       const int64_t pair = pbase + e;
@@ -241,13 +270,19 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         atomicOr(p.err, kErrCapacity);
         continue;
       }
-      float* out = p.scores + (size_t)pair * kScoreTile + il;
-      const int32_t* se_tile = p.se + (size_t)row0 + kt * 128;
+      // query-major: the thread's 64 keys are one contiguous 256-byte piece of its row
+      uint4* out = reinterpret_cast<uint4*>(p.scores + (size_t)pair * kScoreTile + il * 128 + kh);
+      const int32_t* se_tile = p.se + (size_t)row0 + kt * 128 + kh;
 #pragma unroll
-      for (int j = 0; j < 128; ++j) {
-        const int jk = kt * 128 + j;
-        const bool vis = !part || (jk <= i && __ldg(se_tile + j) >= i);
-        out[j * 128] = vis ? acc[j] : -INFINITY;   // key-major: a warp writes 128 contiguous bytes
+      for (int j = 0; j < 64; j += 4) {
+        uint32_t v[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int jk = kt * 128 + kh + j + m;
+          const bool vis = !part || (jk <= i && __ldg(se_tile + j + m) >= i);
+          v[m] = vis ? order_key(acc[j + m]) : 0u;
+        }
+        out[j / 4] = make_uint4(v[0], v[1], v[2], v[3]);
       }
     }
   }
@@ -256,35 +291,46 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == kIdxMma) tmem_dealloc(tmem, 512);
 }
 
-// float -> uint32 with the same order (larger float, larger key)
-__device__ __forceinline__ uint32_t order_key(float s) {
-  const uint32_t u = __float_as_uint(s);
-  return (u >> 31) ? ~u : (u | 0x80000000u);
+
+// One warp per query; a CTA holds eight consecutive queries of one query tile
+// (longest lists first).  The query's candidates are its key rows in the
+// tile pairs of its list (the scores' order keys, 0 where a key is not
+// visible): one 512-byte row per key tile, a uint4 per lane, so every pass
+// is one coalesced 16-byte load per lane and key tile, and after the first
+// pass the rows come from L1/L2.  Byte-wise radix passes, most significant
+// first, build the query's 256-bin histogram in shared memory and narrow the
+// prefix of the k-th largest key; they stop as soon as every key left under
+// the prefix is needed.  The emit pass walks the list in ascending key
+// order: keys above the prefix, then the ones equal to it until the k are
+// complete (ties to the smaller key index), their output offsets from warp
+// prefix sums.
+constexpr int kSelWarps = 8;
+constexpr int kSelBatch = 8;    // key tiles whose rows one lane has in flight
+
+template <typename F>
+__device__ __forceinline__ void for_rows(const uint32_t* base, int cnt, int lane, F&& f) {
+  for (int e0 = 0; e0 < cnt; e0 += kSelBatch) {
+    uint4 v[kSelBatch];
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u)
+      if (e0 + u < cnt) v[u] = __ldg(reinterpret_cast<const uint4*>(base + (size_t)(e0 + u) * kScoreTile) + lane);
+#pragma unroll
+    for (int u = 0; u < kSelBatch; ++u)
+      if (e0 + u < cnt) f(e0 + u, v[u]);
+  }
 }
 
-// One CTA per (row, half a query tile), 32 warps: warp w serves queries
-// 32 (w % 2) .. +31 of the half (lane = query) over the (w / 2)-th of sixteen
-// contiguous ranges of the tile's key-tile list.  Four byte-wise radix passes build each
-// query's histogram in shared memory (atomics across the eight ranges) and
-// pin the k-th largest score; a counting pass then gives every range its
-// output offset, so the ranges emit in parallel and the keys still come out
-// in ascending order, ties to the smaller key index.
-__global__ void __launch_bounds__(kSelThreads) index_select_kernel(const IdxParams p) {
-  extern __shared__ uint32_t hist[];   // [256 bins][kSelQ queries]
-  __shared__ uint32_t s_prefix[kSelQ], s_mask[kSelQ];
-  __shared__ int s_rem[kSelQ], s_all[kSelQ];
-  __shared__ int s_gt[kSelSplit][kSelQ], s_eq[kSelSplit][kSelQ];
-  constexpr int kHalves = 128 / kSelQ;
-  const int qt = p.NT - 1 - (int)(blockIdx.x / (p.R * kHalves));
-  const int r = (int)(blockIdx.x / kHalves % p.R), half = (int)(blockIdx.x % kHalves);
+__global__ void __launch_bounds__(kSelWarps * 32) index_select_kernel(const IdxParams p) {
+  __shared__ __align__(16) uint32_t hist_all[kSelWarps * 256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kGroups = kSelQ / 32;
-  const int qg = warp % kGroups, ts = warp / kGroups;
-  const int ql = qg * 32 + lane;               // query within the CTA
-  const int il = half * kSelQ + ql, i = qt * 128 + il;
+  constexpr int kPerTile = 128 / kSelWarps;   // CTAs per query tile
+  const int qt = p.NT - 1 - (int)(blockIdx.x / (p.R * kPerTile));
+  const int r = (int)(blockIdx.x / kPerTile % p.R);
+  const int il = (int)(blockIdx.x % kPerTile) * kSelWarps + warp, i = qt * 128 + il;
+  uint32_t* hist = hist_all + warp * 256;
   const int cnt = p.csr_cnt[(size_t)r * p.NT + qt];
   const int32_t* list = p.csr + ((size_t)r * p.NT + qt) * p.NT;
   const int64_t pbase = (int64_t)p.row_base[r] + p.csr_off[(size_t)r * p.NT + qt];
@@ -293,114 +339,128 @@ __global__ void __launch_bounds__(kSelThreads) index_select_kernel(const IdxPara
   float* os = p.out_score + ((size_t)r * p.T + i) * k;
   if (cnt <= 0 || cnt > p.NT || pbase + cnt > p.cap) {   // uniform over the CTA
     if (threadIdx.x == 0) atomicOr(p.err, cnt <= 0 || cnt > p.NT ? kErrBadList : kErrCapacity);
-    if (ts == 0)
-      for (int n = 0; n < k; ++n) {
-        oi[n] = -1;
-        os[n] = -INFINITY;
-      }
-    return;
-  }
-  const int e0 = ts * cnt / kSelSplit, e1 = (ts + 1) * cnt / kSelSplit;
-  auto tile = [&](int e) { return p.scores + (size_t)(pbase + e) * kScoreTile + il; };
-  if (threadIdx.x < kSelQ) {
-    s_prefix[threadIdx.x] = 0;
-    s_mask[threadIdx.x] = 0;
-    s_rem[threadIdx.x] = k;
-    s_all[threadIdx.x] = 0;
-  }
-  for (int b = 3; b >= 0; --b) {
-    for (int x = threadIdx.x; x < 256 * kSelQ; x += kSelThreads) hist[x] = 0;
-    __syncthreads();
-    const uint32_t prefix = s_prefix[ql], mask = s_mask[ql];
-    if (!s_all[ql]) {
-      for (int e = e0; e < e1; ++e) {
-        const float* t = tile(e);
-        for (int j = 0; j < 128; ++j) {
-          const float sc = t[j * 128];
-          if (sc == -INFINITY) continue;
-          const uint32_t key = order_key(sc);
-          if ((key & mask) == prefix) atomicAdd(&hist[((key >> (8 * b)) & 255u) * kSelQ + ql], 1u);
-        }
-      }
-    }
-    __syncthreads();
-    if (threadIdx.x < kSelQ) {
-      const int q = threadIdx.x;
-      if (b == 3) {
-        int total = 0;
-        for (int bin = 0; bin < 256; ++bin) total += (int)hist[bin * kSelQ + q];
-        if (total <= k) s_all[q] = 1;
-      }
-      if (!s_all[q]) {
-        const int remaining = s_rem[q];
-        int cum = 0;
-        for (int bin = 255; bin >= 0; --bin) {
-          const int c = (int)hist[bin * kSelQ + q];
-          if (cum + c >= remaining) {
-            s_prefix[q] |= (uint32_t)bin << (8 * b);
-            s_rem[q] = remaining - cum;
-            break;
-          }
-          cum += c;
-        }
-        s_mask[q] |= 255u << (8 * b);
-      }
-    }
-    __syncthreads();
-  }
-  const uint32_t thr = s_prefix[ql];
-  const int ties = s_rem[ql];
-  const bool all = s_all[ql] != 0;
-  // counting pass: keys above the threshold and keys equal to it, per range
-  int gt = 0, eq = 0;
-  for (int e = e0; e < e1; ++e) {
-    const float* t = tile(e);
-    for (int j = 0; j < 128; ++j) {
-      const float sc = t[j * 128];
-      if (sc == -INFINITY) continue;
-      if (all) {
-        ++gt;
-      } else {
-        const uint32_t key = order_key(sc);
-        gt += key > thr;
-        eq += key == thr;
-      }
-    }
-  }
-  s_gt[ts][ql] = gt;
-  s_eq[ts][ql] = eq;
-  __syncthreads();
-  int before = 0, eq_before = 0;
-  for (int t2 = 0; t2 < ts; ++t2) {
-    before += s_gt[t2][ql];
-    eq_before += s_eq[t2][ql];
-  }
-  int n = before + (all ? 0 : min(ties, eq_before));
-  int my_ties = all ? 0 : max(0, min(eq, ties - eq_before));
-  for (int e = e0; e < e1; ++e) {
-    const float* t = tile(e);
-    const int kt = list[e] >> 1;
-    for (int j = 0; j < 128; ++j) {
-      const float sc = t[j * 128];
-      if (sc == -INFINITY) continue;
-      bool take = all;
-      if (!all) {
-        const uint32_t key = order_key(sc);
-        take = key > thr || (key == thr && my_ties > 0);
-        if (key == thr && my_ties > 0) --my_ties;
-      }
-      if (take) {
-        oi[n] = kt * 128 + j;
-        os[n] = sc;
-        ++n;
-      }
-    }
-  }
-  if (ts == kSelSplit - 1)
-    for (; n < k; ++n) {
+    for (int n = lane; n < k; n += 32) {
       oi[n] = -1;
       os[n] = -INFINITY;
     }
+    return;
+  }
+  const uint32_t* base = p.scores + (size_t)pbase * kScoreTile + (size_t)il * 128;
+
+  // Candidates of a pass: visible keys (key != 0) whose masked bits equal the
+  // prefix.  After the passes, "all" (at most k visible keys) is the prefix 0
+  // under a full mask: then every visible key counts as above it.
+  uint32_t prefix = 0, mask = 0;
+  int rem = k;
+#pragma unroll 1
+  for (int d = 3; d >= 0; --d) {
+    const int sh = 8 * d;
+#pragma unroll
+    for (int b = 0; b < 8; b += 4) *reinterpret_cast<uint4*>(hist + lane * 8 + b) = make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    for_rows(base, cnt, lane, [&](int, const uint4& v) {
+      const uint32_t key[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+        if ((key[m] & mask) == prefix && key[m]) atomicAdd(&hist[(key[m] >> sh) & 255u], 1u);
+    });
+    __syncwarp();
+    // lane holds bins 8 lane .. 8 lane + 7; count the keys in the bins of the lanes above
+    uint32_t c8[8];
+    int s = 0;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      c8[b] = hist[lane * 8 + b];
+      s += (int)c8[b];
+    }
+    int incl = s;   // keys in the bins of this lane and the lanes above it
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_down_sync(0xffffffffu, incl, o);
+      if (lane + o < 32) incl += t;
+    }
+    const int above = incl - s;
+    if (d == 3 && __shfl_sync(0xffffffffu, incl, 0) <= k) {   // at most k visible keys: take them all
+      prefix = 0;
+      mask = 0xffffffffu;
+      break;
+    }
+    // the lane whose range holds the rem-th largest key picks the bin
+    const bool mine = above < rem && rem <= above + s;
+    int bin = 0, cum = above, cb = 0;
+    if (mine) {
+#pragma unroll
+      for (int b = 7; b >= 0; --b) {
+        if (cum + (int)c8[b] >= rem) {
+          bin = lane * 8 + b;
+          cb = (int)c8[b];
+          break;
+        }
+        cum += (int)c8[b];
+      }
+    }
+    const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+    bin = __shfl_sync(0xffffffffu, bin, src);
+    cum = __shfl_sync(0xffffffffu, cum, src);
+    cb = __shfl_sync(0xffffffffu, cb, src);
+    prefix |= (uint32_t)bin << sh;
+    mask |= 255u << sh;
+    rem -= cum;
+    if (cb == rem) break;   // every key under the prefix is taken
+    __syncwarp();           // the bins were read before the next pass clears them
+  }
+
+  // emit in ascending key order; lane holds keys 4 lane .. 4 lane + 3 of each tile
+  int n_out = 0, ties = 0;
+  for_rows(base, cnt, lane, [&](int e, const uint4& v) {
+    const uint32_t key[4] = {v.x, v.y, v.z, v.w};
+    bool gt[4], eq[4];
+    int ne = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t km = key[m] & mask;
+      gt[m] = km > prefix;                   // above the prefix (0 never is)
+      eq[m] = km == prefix && key[m] != 0u;  // under it: a tie candidate
+      ne += eq[m];
+    }
+    // ties before this lane (inclusive scan of ne over lanes)
+    int tin = ne;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, tin, o);
+      if (lane >= o) tin += t;
+    }
+    int trank = ties + tin - ne;
+    bool take[4];
+    int nt = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      take[m] = gt[m] || (eq[m] && trank < rem);
+      trank += eq[m];
+      nt += take[m];
+    }
+    ties += __shfl_sync(0xffffffffu, tin, 31);
+    int pin = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, pin, o);
+      if (lane >= o) pin += t;
+    }
+    int at = n_out + pin - nt;
+    const int kt = list[e] >> 1;
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      if (take[m]) {
+        oi[at] = kt * 128 + lane * 4 + m;
+        os[at] = key_value(key[m]);
+        ++at;
+      }
+    n_out += __shfl_sync(0xffffffffu, pin, 31);
+  });
+  for (int n = n_out + lane; n < k; n += 32) {
+    oi[n] = -1;
+    os[n] = -INFINITY;
+  }
 }
 
 stp_status check_index_desc(const stp_index_desc* d) {
@@ -428,7 +488,7 @@ extern "C" stp_status stp_index_workspace_size(const stp_index_desc* desc, size_
   if (st) return st;
   if (!ws_bytes) return fail(STP_EINVAL, "stp_index_workspace_size: NULL output");
   const int64_t cap = pair_capacity(desc->n_rows, desc->row_len / kTile, desc->max_tile_pairs);
-  *ws_bytes = 256 + (size_t)cap * kScoreTile * sizeof(float);
+  *ws_bytes = 256 + (size_t)cap * kScoreTile * sizeof(uint32_t);
   return STP_OK;
 }
 
@@ -463,7 +523,7 @@ extern "C" stp_status stp_index_topk(const stp_index_desc* desc, const void* q, 
   p.row_base = reinterpret_cast<const int32_t*>(tm + m.row_base);
   p.w = w;
   p.err = static_cast<uint32_t*>(d_ws);
-  p.scores = reinterpret_cast<float*>(static_cast<char*>(d_ws) + 256);
+  p.scores = reinterpret_cast<uint32_t*>(static_cast<char*>(d_ws) + 256);
   p.out_idx = topk_idx;
   p.out_score = topk_score;
   const int64_t rows = (int64_t)desc->n_rows * desc->row_len;
@@ -473,20 +533,17 @@ extern "C" stp_status stp_index_topk(const stp_index_desc* desc, const void* q, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(p.err, 0, 4, s);
   const int smem = p.H * 128 * p.D * 2 + 2 * 128 * p.D * 2 + kIdxSmallBytes;
-  const int smem_sel = 256 * kSelQ * 4;
   static bool attr = false;
   if (e == cudaSuccess && !attr) {
     e = cudaFuncSetAttribute(index_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kIdxQBytesMax + 2 * 128 * 128 * 2 + kIdxSmallBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(index_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_sel);
     attr = e == cudaSuccess;
   }
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_index_topk: %s", cudaGetErrorString(e));
   const unsigned grid = (unsigned)(NT * desc->n_rows);
   p.splits = (NT + kIdxPiece - 1) / kIdxPiece;
   index_scores_kernel<<<grid * p.splits, kIdxThreads, smem, s>>>(mq, mk, p);
-  index_select_kernel<<<grid * (128 / kSelQ), kSelThreads, smem_sel, s>>>(p);
+  index_select_kernel<<<grid * (128 / kSelWarps), kSelWarps * 32, 0, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_index_topk: %s", cudaGetErrorString(e));
   return STP_OK;

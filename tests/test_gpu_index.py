@@ -112,6 +112,46 @@ def test_grpo_sampled_queries(stp_lib, heads, dim):
         _check_query(rt, int(i), qn, kn, wn, 512, idx[0, i], sc[0, i])
 
 
+@pytest.mark.parametrize("top_k", [5, 100, 512])
+def test_exact_ties_go_to_smaller_keys(stp_lib, top_k):
+    """Scores with exact ties: every key row is one of three vectors (so a
+    query's scores take at most three values, each computed identically),
+    and with w = 0 every score is 0.  The selection is then unique: by score,
+    ties to the smaller key index; compared exactly, on random forests and
+    the GRPO row's first, middle and last query tiles."""
+    cases = []
+    b = W.random_forest(5, n_roots=3, max_depth=3, max_children=3, len_lo=8, len_hi=300, row_len=2048,
+                        min_shared=16, vocab=W.VOCAB)
+    cases.append(b)
+    cases.append(W.CONFIG_BATCHES["grpo"](W.CONFIG_SEEDS["grpo"]))
+    for bi, b in enumerate(cases):
+        out, info, ref = pack_both(b)
+        se = out["subtree_end"]
+        R, T = se.shape
+        q, k, w = W.index_tensors(R, T, 2, 64, seed=11 + bi)
+        g = torch.Generator().manual_seed(7 + bi)
+        basis = torch.randn(3, 64, generator=g) * torch.tensor([[1.0], [2.0], [4.0]])
+        pick = torch.randint(0, 3, (R, T), generator=g)
+        k = basis[pick].to(torch.bfloat16)
+        for zero_w in (False, True):
+            wc = torch.zeros_like(w) if zero_w else w
+            idx, sc, st = _run(se, q, k, wc, top_k)
+            assert st == stp.STP_OK
+            qn, kn, wn = q.double().numpy(), k.double().numpy(), wc.double().numpy()
+            queries = range(T) if T <= 2048 else [*range(0, 128), *range(8192, 8320), *range(T - 128, T)]
+            for r in range(R):
+                rt = OA.RowTree(ref, r)
+                for i in queries:
+                    cand = rt.visible(i)
+                    s = OI.scores(qn[r], kn[r], wn[r], i, cand)
+                    order = np.lexsort((cand, -s))[:top_k]
+                    want = np.sort(cand[order])
+                    got = idx[r, i][idx[r, i] >= 0]
+                    assert np.array_equal(got, want), (bi, zero_w, r, i)
+                    if zero_w:
+                        assert np.all(sc[r, i][: len(want)] == 0.0)
+
+
 def test_capacity_too_small_is_flagged(stp_lib):
     b = W.random_forest(3, n_roots=2, max_depth=2, max_children=3, len_lo=8, len_hi=100, row_len=512,
                         min_shared=16, vocab=W.VOCAB)
