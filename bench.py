@@ -49,11 +49,14 @@ WORKLOAD_DESC = ("one GRPO group: 5000-token non-trainable system prefix + 16 tr
 METRIC = "tree-attn fwd+bwd useful TFLOP/s (% of BF16 peak) and trajectories/s on 1 GB300"
 
 
-# DRAM bytes (read + write) of one backward on the workload above, from an ncu
-# capture of one kv-head group's bwd_tc_kernel (69.5e6 + 463.0e6) and
-# dq_tc_kernel (519.0e6 + 9.9e6) launches, times the 8 groups (every kv head
-# has the same tile structure); to be retaken whenever either kernel changes.
-BWD_DRAM_BYTES = 8 * (69.511936e6 + 462.977280e6 + 519.038976e6 + 9.910528e6)
+# DRAM bytes (read + write) of one backward call on the workload above, from
+# one ncu capture of every launch of the second call of
+#   python bench.py --profile attn --reps 1
+# (dram__bytes_read.sum + dram__bytes_write.sum, -s 21 -c 21): bwd_delta_kernel
+# 270.6e6 + 22.4e6, the eight bwd_tc_kernel launches 517.5e6 + 3688.2e6, the
+# eight dq_tc_kernel launches 4152.4e6 + 54.0e6.  To be retaken whenever one of
+# the three kernels changes.
+BWD_DRAM_BYTES = 270569728 + 22377472 + 517479680 + 3688181248 + 4152399872 + 54017280
 
 
 def _peaks():
@@ -165,7 +168,8 @@ def _gdn(meta, dev, heads=16, reps=10) -> dict:
     out = {"heads": heads, "head_dim": 128, "tokens": real, "segments": int(plan[stp.GP_NSEG]),
            "chunks": int(plan[stp.GP_NCHUNK]), "depths": int(plan[stp.GP_NDEPTH]), "ms": ms,
            "tokens_per_s": real / (ms / 1e3), "host_plan_ms": plan_ms,
-           "launches_per_call": 2 + int(plan[stp.GP_NDEPTH])}
+           # convolution, the preparation (split in two launches when there are deeper segments), a walk per depth
+           "launches_per_call": 1 + (2 if int(plan[stp.GP_NDEPTH]) > 1 else 1) + int(plan[stp.GP_NDEPTH])}
     # training: the forward that keeps the chunk states, then the backward
     try:
         tws = torch.empty(stp.stp_gdn_train_workspace_size(desc, plan), dtype=torch.uint8, device=dev)
@@ -853,8 +857,8 @@ def main():
                                "dq_tc_kernel (dQ from the dS tiles)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} bf16 burst", "traffic": BWD_DRAM_BYTES,
-                     "traffic_note": "dram read+write bytes of bwd_tc_kernel + dq_tc_kernel for one kv-head "
-                                     "group (one ncu launch each) x 8 groups; the dS round trip is ~7.9 GB of it"},
+                     "traffic_note": "dram read+write bytes of one backward call (Delta pass, 8 x dK/dV, "
+                                     "8 x dQ) from one ncu capture; the dS round trip is ~7.8 GB of it"},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e_tot / args.steps, "call": "stp_attn_step_host", "kv_head_groups": n_chunks,

@@ -19,7 +19,8 @@
 //                     SiLU, unit q and k heads; pads get o = 0.
 //   gdn_prep_kernel   one block per (chunk, head): [Q K^T; K K^T] on the tensor
 //                     core; T = (I + A)^{-1} of the unit-lower-triangular
-//                     system in float32 on 64 threads (a column each); then
+//                     system in float32 (two 32 x 32 diagonal blocks by
+//                     substitution, the off-diagonal one by two products); then
 //                     U^ = T diag(beta) V and W = T diag(beta e^gam) K on the
 //                     tensor core (T split into bf16 hi + lo, so the products
 //                     keep ~16 bits), and the chunk's operands
@@ -36,6 +37,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -83,7 +85,7 @@ constexpr int kOffBar = kOffOst + 64 * kOstLd;
 constexpr int kStSmem = kOffBar + 256 + 1024;
 
 struct GdnParams {
-  int N, H, C, seg0;
+  int N, H, C, seg0, chunk0;   // seg0, chunk0: first segment / chunk of a launch
   float scale;
   const int32_t* prev;      // token 1, 2 and 3 back on the path (-2 on prev: a pad)
   const int32_t* prev2;
@@ -184,98 +186,137 @@ __device__ __forceinline__ void unpack8(const uint4 r, float* f) {
 }
 
 // ---------------------------------------------------------------------------
-// Path convolution + SiLU + unit q, k heads.  Block = (64 tokens, one group of
-// 128 channels: a q, k or v head); thread = (token of 16, 8 channels), so the
-// 16 lanes of a token hold one head and its weights stay in registers.  One
-// TMA copy brings the block's x rows xb-3 .. xb+63 of the group (zero rows
-// outside the tensor) into shared memory; inside a segment the taps of token
-// x are x-3 .. x, all in that tile, and a tap is read from memory only where
-// the path turns (a segment's first tokens, whose taps lie in the parent).
+// Path convolution + SiLU + unit q, k heads.  Unit of work = (64 tokens, one
+// group of 128 channels: a q, k or v head); thread = (token of 16, 8
+// channels), so the 16 lanes of a token hold one head.  A CTA keeps one
+// channel group (its weights stay in registers) and walks token blocks
+// bx0, bx0 + S, ...; one TMA copy per block brings the x rows xb-3 .. xb+63
+// of the group (zero rows outside the tensor) into shared memory, the next
+// block's copy and path pointers in flight while this one is computed.
+// Inside a segment the taps of token x are x-3 .. x, all in the tile; a tap
+// is read from memory only where the path turns (a segment's first tokens,
+// whose taps lie in the parent).
 constexpr int kConvRows = 64 + 3;
+constexpr int kConvBuf = kConvRows * kGd * 2;   // one block's rows, bf16
 
-__global__ void __launch_bounds__(kConvThreads) gdn_conv_kernel(const __grid_constant__ CUtensorMap mx,
-                                                                const GdnParams p) {
-  __shared__ __align__(128) uint8_t xs[kConvRows * kGd * 2];   // [67 rows][128 channels] bf16
-  __shared__ int taps[64][3];   // the 1, 2 and 3 tokens back on each token's path (-2: pad or past the end)
-  __shared__ __align__(8) uint64_t bar;
+__global__ void __launch_bounds__(kConvThreads, 4) gdn_conv_kernel(const __grid_constant__ CUtensorMap mx,
+                                                                   const GdnParams p, int S) {
+  __shared__ __align__(128) uint8_t xs[2][kConvBuf];   // [67 rows][128 channels] bf16, two blocks
+  __shared__ int taps[2][64][3];   // the 1, 2 and 3 tokens back on each token's path (-2: pad or past the end)
+  __shared__ __align__(8) uint64_t bars[2];
   __shared__ int abort_flag;
-  const int grp = blockIdx.y, lt = threadIdx.x >> 4, vec = threadIdx.x & 15;
-  const int ch = grp * kGd + vec * 8, xb = blockIdx.x * 64;
+  const int G = 3 * p.H, nbx = (p.N + 63) / 64;
+  const int grp = blockIdx.x % G, bx0 = blockIdx.x / G;
+  const int lt = threadIdx.x >> 4, vec = threadIdx.x & 15;
+  const int ch = grp * kGd + vec * 8;
   const bool is_qk = grp < 2 * p.H;
+  auto load_taps = [&](int bx, int& t0, int& t1, int& t2) {
+    const int x = bx * 64 + threadIdx.x;
+    const bool in = x < p.N;
+    t0 = in ? p.prev[x] : -2;
+    t1 = in ? p.prev2[x] : -1;
+    t2 = in ? p.prev3[x] : -1;
+  };
   if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
     abort_flag = 0;
     fence_mbar_init();
-    mbar_expect_tx(&bar, kConvRows * kGd * 2);
-    tma_load_2d_g(xs, &mx, &bar, grp * kGd, xb - 3);
+    if (bx0 < nbx) {
+      mbar_expect_tx(&bars[0], kConvBuf);
+      tma_load_2d_g(xs[0], &mx, &bars[0], grp * kGd, bx0 * 64 - 3);
+    }
   }
-  if (threadIdx.x < 64) {
-    const int x = xb + threadIdx.x;
-    const bool in = x < p.N;
-    taps[threadIdx.x][0] = in ? p.prev[x] : -2;
-    taps[threadIdx.x][1] = in ? p.prev2[x] : -1;
-    taps[threadIdx.x][2] = in ? p.prev3[x] : -1;
+  if (threadIdx.x < 64 && bx0 < nbx) {
+    int t0, t1, t2;
+    load_taps(bx0, t0, t1, t2);
+    taps[0][threadIdx.x][0] = t0;
+    taps[0][threadIdx.x][1] = t1;
+    taps[0][threadIdx.x][2] = t2;
   }
   float4 wv[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) wv[i] = reinterpret_cast<const float4*>(p.conv_w)[ch + i];
   __syncthreads();
-  if (!mbar_wait(&bar, 0, &abort_flag, p.err)) {   // gave up: let the copy land, then leave
-    mbar_wait_drain(&bar, 0);
-    return;
-  }
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int tl = it * 16 + lt, x = xb + tl;
-    const bool in = x < p.N;
-    const int p1 = taps[tl][0];
-    if (p1 == -2) {
-      if (in && grp < p.H) {   // a pad: o = 0 for head grp
-        float4* o4 = reinterpret_cast<float4*>(p.o + ((size_t)x * p.H + grp) * kGd + vec * 8);
-        o4[0] = o4[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  int j = 0;
+  for (int bx = bx0; bx < nbx; bx += S, ++j) {
+    const int buf = j & 1, nb = bx + S;
+    int n0 = -2, n1 = -1, n2 = -1;
+    if (nb < nbx) {   // the next block: its rows by TMA (that buffer was freed by the barrier
+                      // that ended the previous block), its path pointers into registers
+      if (threadIdx.x == 0) {
+        mbar_expect_tx(&bars[buf ^ 1], kConvBuf);
+        tma_load_2d_g(xs[buf ^ 1], &mx, &bars[buf ^ 1], grp * kGd, nb * 64 - 3);
       }
-      continue;   // all 16 lanes of a token take the same branch
+      if (threadIdx.x < 64) load_taps(nb, n0, n1, n2);
     }
-    const int src[4] = {taps[tl][2], taps[tl][1], p1, x};   // taps 0..3
-    float acc[8];
+    if (!__syncthreads_and(mbar_wait(&bars[buf], (j >> 1) & 1, &abort_flag, p.err))) {
+      // gave up: let the copies in flight land, then leave
+      mbar_wait_drain(&bars[buf], (j >> 1) & 1);
+      if (nb < nbx) mbar_wait_drain(&bars[buf ^ 1], ((j + 1) >> 1) & 1);
+      return;
+    }
+    const int xb = bx * 64;
+    const uint8_t* xt = xs[buf];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      if (src[t] < 0) continue;
-      const int r = src[t] - (xb - 3);
-      const uint4 v = (r >= 0 && r < kConvRows)
-                          ? *reinterpret_cast<const uint4*>(xs + r * (kGd * 2) + vec * 16)
-                          : *reinterpret_cast<const uint4*>(p.x + (size_t)src[t] * p.C + ch);
-      float f[8];
-      unpack8(v, f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float w = t == 0 ? wv[i].x : t == 1 ? wv[i].y : t == 2 ? wv[i].z : wv[i].w;
-        acc[i] = fmaf(w, f[i], acc[i]);
+    for (int it = 0; it < 4; ++it) {
+      const int tl = it * 16 + lt, x = xb + tl;
+      const bool in = x < p.N;
+      const int p1 = taps[buf][tl][0];
+      if (p1 == -2) {
+        if (in && grp < p.H) {   // a pad: o = 0 for head grp
+          float4* o4 = reinterpret_cast<float4*>(p.o + ((size_t)x * p.H + grp) * kGd + vec * 8);
+          o4[0] = o4[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        continue;   // all 16 lanes of a token take the same branch
       }
+      const int src[4] = {taps[buf][tl][2], taps[buf][tl][1], p1, x};   // taps 0..3
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        if (src[t] < 0) continue;
+        const int r = src[t] - (xb - 3);
+        const uint4 v = (r >= 0 && r < kConvRows)
+                            ? *reinterpret_cast<const uint4*>(xt + r * (kGd * 2) + vec * 16)
+                            : *reinterpret_cast<const uint4*>(p.x + (size_t)src[t] * p.C + ch);
+        float f[8];
+        unpack8(v, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float w = t == 0 ? wv[i].x : t == 1 ? wv[i].y : t == 2 ? wv[i].z : wv[i].w;
+          acc[i] = fmaf(w, f[i], acc[i]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = __fdividef(acc[i], 1.f + __expf(-acc[i]));
+      if (is_qk) {
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(acc[i], acc[i], ss);
+        const unsigned grpmask = 0xffffu << (threadIdx.x & 16);
+        ss += __shfl_xor_sync(grpmask, ss, 8);
+        ss += __shfl_xor_sync(grpmask, ss, 4);
+        ss += __shfl_xor_sync(grpmask, ss, 2);
+        ss += __shfl_xor_sync(grpmask, ss, 1);
+        const float r = rsqrtf(ss + 1e-6f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] *= r;
+      }
+      uint4 out;
+      out.x = pack_bf16x2(acc[0], acc[1]);
+      out.y = pack_bf16x2(acc[2], acc[3]);
+      out.z = pack_bf16x2(acc[4], acc[5]);
+      out.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(p.y + (size_t)x * p.C + ch) = out;
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = __fdividef(acc[i], 1.f + __expf(-acc[i]));
-    if (is_qk) {
-      float ss = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) ss = fmaf(acc[i], acc[i], ss);
-      const unsigned grpmask = 0xffffu << (threadIdx.x & 16);
-      ss += __shfl_xor_sync(grpmask, ss, 8);
-      ss += __shfl_xor_sync(grpmask, ss, 4);
-      ss += __shfl_xor_sync(grpmask, ss, 2);
-      ss += __shfl_xor_sync(grpmask, ss, 1);
-      const float r = rsqrtf(ss + 1e-6f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] *= r;
+    if (threadIdx.x < 64 && nb < nbx) {
+      taps[buf ^ 1][threadIdx.x][0] = n0;
+      taps[buf ^ 1][threadIdx.x][1] = n1;
+      taps[buf ^ 1][threadIdx.x][2] = n2;
     }
-    uint4 out;
-    out.x = pack_bf16x2(acc[0], acc[1]);
-    out.y = pack_bf16x2(acc[2], acc[3]);
-    out.z = pack_bf16x2(acc[4], acc[5]);
-    out.w = pack_bf16x2(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(p.y + (size_t)x * p.C + ch) = out;
+    __syncthreads();   // this block's rows and pointers are read; the next block's pointers are in
   }
 }
 
@@ -301,7 +342,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnPara
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ch = blockIdx.x / p.H, h = blockIdx.x % p.H;
+  const int ch = p.chunk0 + (int)(blockIdx.x / p.H), h = blockIdx.x % p.H;
   const int x0 = p.chunk_start[ch], L = p.chunk_len[ch];
   const int Hd = p.H * kGd;
   const size_t row = (size_t)ch * p.H + h;
@@ -417,57 +458,117 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_prep_kernel(const GdnPara
   __syncthreads();
   fence_after_sync();
 
+  // Q~ (rows 0..63 of the [Q~; W] tile) and K~, 8 channels (16 bytes) per item
+  for (int it = tid; it < 2 * kGc * 16; it += kPrepThreads) {
+    const int m = it >> 4, c = (it & 15) * 8, t = m & (kGc - 1);   // m < 64: a Q row, else a K row
+    const float sc = t < L ? (m < kGc ? p.scale * seg[t] : sek[t]) : 0.f;
+    const uint4 r = *reinterpret_cast<const uint4*>(tile + (c >> 6) * 16384 + m * 128 +
+                                                    ((((c & 63) >> 3) ^ (m & 7)) << 4));
+    float f[8];
+    unpack8(r, f);
+    const uint4 o = make_uint4(pack_bf16x2(sc * f[0], sc * f[1]), pack_bf16x2(sc * f[2], sc * f[3]),
+                               pack_bf16x2(sc * f[4], sc * f[5]), pack_bf16x2(sc * f[6], sc * f[7]));
+    __nv_bfloat16* dst = m < kGc ? p.wq + (row * 128 + t) * kGd + c : p.kt + (row * kGc + t) * kGd + c;
+    *reinterpret_cast<uint4*>(dst) = o;
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+
+  // T = (I + A)^{-1} in 32 x 32 blocks: T11 = (I + A11)^{-1} and
+  // T22 = (I + A22)^{-1} (one warp each, a column per thread, column-oriented
+  // substitution: once an entry is final it is taken out of every later
+  // row), then T21 = -T22 (A21 T11).  T is kept float32 row-major [64][64]
+  // over the Q rows of the tile (read above): rows 0-31 in the first 8 KB
+  // half, rows 32-63 in the second; A21 T11 goes over A22's columns of A.
+  auto trow = [&](int t) { return reinterpret_cast<float*>(tile + (t >> 5) * 16384 + (t & 31) * 256); };
+  float* sM = sA + 32 * kPrepLa;   // [32][32] row-major
   if (warp < 2) {
-    // T = (I + A)^{-1}, column s per thread, column-oriented substitution
-    // (once T[t][s] is final it is taken out of every later row).  A is
-    // column-major with zeros on and above the diagonal, so column t is read
-    // 4 wide from the multiple of 4 at or below t + 1.  Then T' = T diag(beta)
-    // and T'' = T diag(beta e^gam), split into bf16 hi + lo, go to the
-    // operand tiles (rows 0-63 T', rows 64-127 T'', K index s).
-    const int sc = tid;
-    float x[kGc];
+    const int b0 = 32 * warp, cc = b0 + lane;   // block rows / columns b0 .. b0 + 31; this thread's column
+    float x[32];
 #pragma unroll
-    for (int t = 0; t < kGc; ++t) x[t] = t == sc ? 1.f : 0.f;
+    for (int t = 0; t < 32; ++t) x[t] = t == lane ? 1.f : 0.f;
 #pragma unroll
-    for (int t = 0; t < kGc - 1; ++t) {
+    for (int t = 0; t < 31; ++t) {
       const float xt = x[t];
 #pragma unroll
-      for (int r4 = ((t + 1) & ~3); r4 < kGc; r4 += 4) {
-        const float4 a = *reinterpret_cast<const float4*>(sA + t * kPrepLa + r4);
+      for (int r4 = ((t + 1) & ~3); r4 < 32; r4 += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(sA + (b0 + t) * kPrepLa + b0 + r4);
         x[r4] = fmaf(-a.x, xt, x[r4]);
         x[r4 + 1] = fmaf(-a.y, xt, x[r4 + 1]);
         x[r4 + 2] = fmaf(-a.z, xt, x[r4 + 2]);
         x[r4 + 3] = fmaf(-a.w, xt, x[r4 + 3]);
       }
     }
-    const float b1 = sbeta[sc], b2 = sbeta[sc] * seg[sc];
-    const int kcol = ((sc >> 3) << 4) + (sc & 7) * 2;
 #pragma unroll
-    for (int t = 0; t < kGc; ++t) {
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const int m = part * kGc + t;
-        const float v = x[t] * (part ? b2 : b1);
-        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-        const int off = m * 128 + (kcol ^ ((m & 7) << 4));
-        *reinterpret_cast<__nv_bfloat16*>(sT + off) = hi;
-        *reinterpret_cast<__nv_bfloat16*>(sT + 16384 + off) = lo;
-      }
-    }
+    for (int t = 0; t < 32; ++t) trow(b0 + t)[cc] = x[t];
   } else {
-    // Q~ (rows 0..63 of the [Q~; W] tile) and K~, 8 channels (16 bytes) per item
-    for (int it = tid - 64; it < 2 * kGc * 16; it += kPrepThreads - 64) {
-      const int m = it >> 4, c = (it & 15) * 8, t = m & (kGc - 1);   // m < 64: a Q row, else a K row
-      const float sc = t < L ? (m < kGc ? p.scale * seg[t] : sek[t]) : 0.f;
-      const uint4 r = *reinterpret_cast<const uint4*>(tile + (c >> 6) * 16384 + m * 128 +
-                                                      ((((c & 63) >> 3) ^ (m & 7)) << 4));
-      float f[8];
-      unpack8(r, f);
-      const uint4 o = make_uint4(pack_bf16x2(sc * f[0], sc * f[1]), pack_bf16x2(sc * f[2], sc * f[3]),
-                                 pack_bf16x2(sc * f[4], sc * f[5]), pack_bf16x2(sc * f[6], sc * f[7]));
-      __nv_bfloat16* dst = m < kGc ? p.wq + (row * 128 + t) * kGd + c : p.kt + (row * kGc + t) * kGd + c;
-      *reinterpret_cast<uint4*>(dst) = o;
+    for (int it = tid - 64; it < 32 * 32; it += kPrepThreads - 64) trow(it >> 5)[32 + (it & 31)] = 0.f;   // T12
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  {   // M = A21 T11: thread = (row r, columns 4 c4 .. + 3)
+    const int r = tid >> 3, c4 = (tid & 7) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float a = sA[k * kPrepLa + 32 + r];
+      const float4 tv = *reinterpret_cast<const float4*>(trow(k) + c4);
+      acc.x = fmaf(a, tv.x, acc.x);
+      acc.y = fmaf(a, tv.y, acc.y);
+      acc.z = fmaf(a, tv.z, acc.z);
+      acc.w = fmaf(a, tv.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(sM + r * 32 + c4) = acc;   // A22 was last read before the barrier above
+  }
+  __syncthreads();
+  {   // T21 = -T22 M
+    const int r = tid >> 3, c4 = (tid & 7) * 4;
+    const float* t22 = trow(32 + r) + 32;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+      const float a = t22[k];
+      const float4 mv = *reinterpret_cast<const float4*>(sM + k * 32 + c4);
+      acc.x = fmaf(a, mv.x, acc.x);
+      acc.y = fmaf(a, mv.y, acc.y);
+      acc.z = fmaf(a, mv.z, acc.z);
+      acc.w = fmaf(a, mv.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(trow(32 + r) + c4) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  __syncthreads();
+  // T' = T diag(beta) and T'' = T diag(beta e^gam), split into bf16 hi + lo,
+  // to the operand tiles (rows 0-63 T', rows 64-127 T'', K index s); an item
+  // is one 16-byte chunk (8 columns) of one row
+  for (int it = tid; it < kGc * 8; it += kPrepThreads) {
+    const int t = it >> 3, s0 = (it & 7) * 8;
+    const float* tr = trow(t) + s0;
+    float f[8];
+    *reinterpret_cast<float4*>(f) = *reinterpret_cast<const float4*>(tr);
+    *reinterpret_cast<float4*>(f + 4) = *reinterpret_cast<const float4*>(tr + 4);
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        float v[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int sc = s0 + e + q;
+          v[q] = f[e + q] * (part ? sbeta[sc] * seg[sc] : sbeta[sc]);
+        }
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[0], v[1]);
+        const float2 hf = __bfloat1622float2(h2);
+        const __nv_bfloat162 l2 = __floats2bfloat162_rn(v[0] - hf.x, v[1] - hf.y);
+        hw[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+        lw[e / 2] = *reinterpret_cast<const uint32_t*>(&l2);
+      }
+      const int m = part * kGc + t;
+      const int off = m * 128 + (((s0 >> 3) ^ (m & 7)) << 4);
+      *reinterpret_cast<uint4*>(sT + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(sT + 16384 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
   }
   fence_proxy_async_smem();
@@ -803,6 +904,39 @@ stp_status ws_size(const stp_gdn_desc* desc, const void* plan, size_t* ws_bytes,
   return STP_OK;
 }
 
+// Two library streams per device for the forward: "hi" (the greatest
+// priority) prepares the chunks of depth 0 and runs their state walk, "aux"
+// prepares the other depths' chunks meanwhile.
+struct GdnStreams {
+  bool ready = false;
+  cudaStream_t hi = nullptr, aux = nullptr;
+  cudaEvent_t fork = nullptr, join_hi = nullptr, join_aux = nullptr;
+};
+std::mutex g_gdn_mu;
+GdnStreams g_gdn_streams[64];
+
+cudaError_t gdn_streams(GdnStreams** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_gdn_mu);
+  GdnStreams& g = g_gdn_streams[dev];
+  if (!g.ready) {
+    int least = 0, greatest = 0;
+    e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&g.hi, cudaStreamNonBlocking, greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g.aux, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g.join_hi, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g.join_aux, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+    g.ready = true;
+  }
+  *out = &g;
+  return cudaSuccess;
+}
+
 stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d_plan, const void* x,
                        const float* conv_w, const float* g, const float* beta, float* o, void* d_ws, void* stream,
                        bool train) {
@@ -829,6 +963,7 @@ stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d
   p.H = H;
   p.C = 3 * H * kGd;
   p.seg0 = 0;
+  p.chunk0 = 0;
   p.scale = desc->scale;
   p.prev = dp + w[GP_PREV];
   p.prev2 = dp + w[GP_PREV2];
@@ -872,14 +1007,56 @@ stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d
   cudaError_t e = attr_err;
   if (e == cudaSuccess) e = cudaMemsetAsync(p.err, 0, 4, s);
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e));
-  if (N > 0) gdn_conv_kernel<<<dim3((unsigned)((N + 63) / 64), (unsigned)(3 * H)), kConvThreads, 0, s>>>(mx, p);
-  if (n_chunk > 0) gdn_prep_kernel<<<(unsigned)(n_chunk * H), kPrepThreads, kPrepSmem, s>>>(p);
+  if (N > 0) {
+    // a CTA per (channel group, one of S token-block strides): 4 resident per SM
+    static int n_sm = 0;
+    if (n_sm == 0) {
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) !=
+                                                    cudaSuccess || n_sm <= 0)
+        n_sm = 148;
+    }
+    const int G = 3 * H, nbx = (N + 63) / 64;
+    const int S = std::max(1, std::min(nbx, 4 * n_sm / G));
+    gdn_conv_kernel<<<(unsigned)(G * S), kConvThreads, 0, s>>>(mx, p, S);
+  }
+  // The chunks of depth 0 are prepared and walked on a high-priority stream
+  // (the walk is one CTA per head and root segment: a few SMs), while the
+  // other depths' chunks are prepared on a second stream; the deeper walks
+  // wait for both.  Chunks are numbered depth by depth.
   const int32_t* depth_off = w + w[GP_DEPTH_OFF];
-  for (int d = 0; d < n_depth; ++d) {
+  const int32_t* seg_chunk0 = w + w[GP_SEG_CHUNK0];
+  const int c1 = n_depth > 1 ? seg_chunk0[depth_off[1]] : n_chunk;   // first chunk below depth 0
+  auto walk = [&](int d, cudaStream_t st) {
     const int n = depth_off[d + 1] - depth_off[d];
-    if (n <= 0) continue;
-    p.seg0 = depth_off[d];
-    gdn_state_kernel<<<(unsigned)(n * H), kStThreads, kStSmem, s>>>(mwq, mkt, mpm, p);
+    if (n <= 0) return;
+    GdnParams q = p;
+    q.seg0 = depth_off[d];
+    gdn_state_kernel<<<(unsigned)(n * H), kStThreads, kStSmem, st>>>(mwq, mkt, mpm, q);
+  };
+  GdnStreams* gs = nullptr;
+  if (c1 < n_chunk) {
+    if ((e = gdn_streams(&gs)) != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lock(g_gdn_mu);
+    e = cudaEventRecord(gs->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(gs->hi, gs->fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(gs->aux, gs->fork, 0);
+    if (e == cudaSuccess) {
+      if (c1 > 0) gdn_prep_kernel<<<(unsigned)(c1 * H), kPrepThreads, kPrepSmem, gs->hi>>>(p);
+      walk(0, gs->hi);
+      GdnParams q = p;
+      q.chunk0 = c1;
+      gdn_prep_kernel<<<(unsigned)((n_chunk - c1) * H), kPrepThreads, kPrepSmem, gs->aux>>>(q);
+      e = cudaEventRecord(gs->join_hi, gs->hi);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(gs->join_aux, gs->aux);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, gs->join_hi, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, gs->join_aux, 0);
+    if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e));
+    for (int d = 1; d < n_depth; ++d) walk(d, s);
+  } else {
+    if (n_chunk > 0) gdn_prep_kernel<<<(unsigned)(n_chunk * H), kPrepThreads, kPrepSmem, s>>>(p);
+    for (int d = 0; d < n_depth; ++d) walk(d, s);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e));
