@@ -243,9 +243,13 @@ def _time_batch(b, name, dev, flush, reps=10, min_shared=None, seed=41):
     host = W.attn_tensors(shape, seed)
     q, k, v, do = (x.to(dev) for x in host)
     se_np = meta["subtree_end"]
-    desc = stp.Desc(R, T, Hq, Hkv, D, stp.STP_BF16 if bf16 else stp.STP_FP32, shape.scale,
-                    stp.stp_count_tile_pairs(se_np))
+    pairs = stp.stp_count_tile_pairs(se_np)
+    # dS tiles of two kv-head groups at a time where all groups' would pass 8 GB
+    ds_groups = 2 if bf16 and pairs * Hq * 32768 > 8e9 else 0
+    desc = stp.Desc(R, T, Hq, Hkv, D, stp.STP_BF16 if bf16 else stp.STP_FP32, shape.scale, pairs,
+                    ds_groups=ds_groups)
     buf = stp.Buffers(desc, dev)
+    ws_bytes = sum(stp.stp_workspace_size(desc))
     se = torch.from_numpy(se_np).to(dev)
     o = torch.empty_like(q)
     lse = torch.empty(R, Hq, T, dtype=torch.float32, device=dev)
@@ -282,7 +286,8 @@ def _time_batch(b, name, dev, flush, reps=10, min_shared=None, seed=41):
          "fwd_ms": statistics.median(c.elapsed_time(f) for _, c, f, _ in marks),
          "bwd_ms": statistics.median(f.elapsed_time(e) for _, _, f, e in marks) if bf16 else 0.0,
          "ms": statistics.median(a.elapsed_time(e) for a, _, _, e in marks),
-         "tile_pairs": int(desc.max_tile_pairs), "shape": shape, "bf16": bf16}
+         "tile_pairs": int(desc.max_tile_pairs), "shape": shape, "bf16": bf16,
+         "ds_groups_held": ds_groups or min(Hkv, 8), "device_workspace_gb": ws_bytes / 1e9}
     del buf, q, k, v, do, o, lse, dq, dk, dv
     torch.cuda.empty_cache()
     return t, info, host
@@ -312,7 +317,8 @@ def _attn_config(name, dev, peak, flush, reps=10, oracle_heads=1) -> dict:
            "useful_tflops": flops / (tot / 1e3) / 1e12,
            "trajectories_per_s": b.n_seqs / (tot / 1e3),
            "packed_tokens_per_s": info["packed_tokens"] / (tot / 1e3),
-           "l2": "flushed (512 MiB write) before every repetition; median of %d" % reps}
+           "l2": "flushed (512 MiB write) before every repetition; median of %d" % reps,
+           "ds_groups_held": t["ds_groups_held"], "device_workspace_gb": t["device_workspace_gb"]}
     if bf16:
         out["pct_of_bf16_peak"] = 100.0 * out["useful_tflops"] / peak
         out["fwd_tflops"] = 4.0 * D * Hq * useful / (t["fwd_ms"] / 1e3) / 1e12

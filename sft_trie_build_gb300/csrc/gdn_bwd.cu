@@ -10,7 +10,7 @@
 //           (T = (I + A)^{-1}), then through Q~, K~, P, A, U^ and W to dq, dk,
 //           dv, dbeta and dgam, and dg = the reverse cumulative sum of dgam
 //   tokens: through the unit-norm q, k heads, SiLU and the path convolution.
-// Three kernels:
+// Five kernels:
 //   gdn_bwd_walk_kernel   one launch per depth, deepest first; one CTA per
 //                         (segment, head) walks its chunks last to first with
 //                         the state gradient in TMEM, starting from the sum
