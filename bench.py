@@ -53,10 +53,10 @@ METRIC = "tree-attn fwd+bwd useful TFLOP/s (% of BF16 peak) and trajectories/s o
 # one ncu capture of every launch of the second call of
 #   python bench.py --profile attn --reps 1
 # (dram__bytes_read.sum + dram__bytes_write.sum, -s 21 -c 21): bwd_delta_kernel
-# 270.6e6 + 22.4e6, the eight bwd_tc_kernel launches 517.5e6 + 3688.2e6, the
-# eight dq_tc_kernel launches 4152.4e6 + 54.0e6.  To be retaken whenever one of
+# 270.6e6 + 22.5e6, the eight bwd_tc_kernel launches 617.7e6 + 3677.4e6, the
+# eight dq_tc_kernel launches 4152.4e6 + 53.9e6.  To be retaken whenever one of
 # the three kernels changes.
-BWD_DRAM_BYTES = 270569728 + 22377472 + 517479680 + 3688181248 + 4152399872 + 54017280
+BWD_DRAM_BYTES = 270605568 + 22479360 + 617688576 + 3677362176 + 4152424448 + 53880832
 
 
 def _peaks():
