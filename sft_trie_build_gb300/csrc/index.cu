@@ -257,8 +257,14 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           tmem_ld32(tmem + lane_base + bu * 256 + hs * 128 + kh, x);
           tmem_ld32(tmem + lane_base + bu * 256 + hs * 128 + kh + 32, x + 32);
           tmem_ld_wait();
+          const float2 w2 = make_float2(wi, wi);
 #pragma unroll
-          for (int m = 0; m < 64; ++m) acc[m] = fmaf(wi, fmaxf(__uint_as_float(x[m]), 0.f), acc[m]);
+          for (int m = 0; m < 64; m += 2) {   // two columns per packed FFMA
+            const float2 r2 = make_float2(fmaxf(__uint_as_float(x[m]), 0.f), fmaxf(__uint_as_float(x[m + 1]), 0.f));
+            const float2 a2 = __ffma2_rn(w2, r2, make_float2(acc[m], acc[m + 1]));
+            acc[m] = a2.x;
+            acc[m + 1] = a2.y;
+          }
         }
         fence_before_sync();
         __syncwarp();

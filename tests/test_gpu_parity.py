@@ -177,9 +177,13 @@ def test_misaligned_pointer_rejected():
 
 def _sample_checks(name, n_queries=24, n_keys=6, seed=0):
     b = W.CONFIG_BATCHES[name](W.CONFIG_SEEDS[name])
+    _sample_checks_batch(b, lambda R, T: W.attn_shape(name, R, T), n_queries, n_keys, seed)
+
+
+def _sample_checks_batch(b, shape_of, n_queries=24, n_keys=6, seed=0):
     out, info, ref = pack_both(b)
     R, T = info["n_rows"], b.row_len
-    shape = W.attn_shape(name, R, T)
+    shape = shape_of(R, T)
     q, k, v, do = W.attn_tensors(shape, seed)
     g = GpuRun(out["subtree_end"], shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
                stp.STP_BF16, shape.scale, q, k, v, do).run()
@@ -231,6 +235,18 @@ def _sample_checks(name, n_queries=24, n_keys=6, seed=0):
 @pytest.mark.parametrize("name", ["grpo", "curriculum", "deep", "bushy"])
 def test_bf16_workload_sampled(name):
     _sample_checks(name)
+
+
+def test_bf16_longest_rows_sampled():
+    """The longest rows the library accepts: the prefix-tree-packing page's
+    32-rollout batch packed into two rows of 131072 tokens (130,105 and
+    122,114 used; lists of up to ~220 key tiles), two query heads on one kv
+    head, bf16: classification, forward and backward in one launch each;
+    sampled queries (O, LSE, dQ) and keys near leaf ends (dK, dV) against
+    the oracle, and the sum identities over every key."""
+    b = W.rollout32(0)
+    _sample_checks_batch(b, lambda R, T: W.AttnShape(R, T, 2, 1, 128, "bf16", 128 ** -0.5, 0.5),
+                         n_queries=16, n_keys=6, seed=3)
 
 
 # --- bounded dS workspace ----------------------------------------------------
