@@ -433,7 +433,7 @@ def _classify_bandwidth(desc, se, tile_meta, reps=20) -> dict:
     R, T = desc.n_rows, desc.row_len
     nt = T // 128
     by = 4 * R * T + R * nt * nt + 16 * int(desc.max_tile_pairs)
-    return {"kernels": "tile_minmax_kernel + tile_lists_kernel + tile_pairs_kernel", "ms": ms,
+    return {"kernels": "tile_minmax_kernel + tile_lists_kernel + tile_pairs_kernel + tile_pair_index_kernel", "ms": ms,
             "algorithmic_bytes": by, "achieved_gbs": by / (ms / 1e3) / 1e9,
             "bound": "latency (the whole row's metadata is ~0.3 MB; back-to-back launches, L2-resident)"}
 
@@ -869,8 +869,8 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e_tot / args.steps, "call": "stp_attn_step_host", "kv_head_groups": n_chunks,
                 "steps_in_flight": 2, "l2": "not flushed: every step re-uploads 336 MB of inputs (> L2)"},
-        # per step: three classification kernels, the forward, Delta, and dK/dV + dQ per kv-head group
-        "gpu_launches": (5 + 2 * min(Hkv, 8)) * args.steps,
+        # per step: four classification kernels, the forward, Delta, and dK/dV + dQ per kv-head group
+        "gpu_launches": (6 + 2 * min(Hkv, 8)) * args.steps,
     }
     if rank == 0:
         line["classify"] = _classify_bandwidth(desc, se, buf.tile_meta)

@@ -131,21 +131,15 @@ __global__ void __launch_bounds__(128) tile_lists_kernel(int NT, const int32_t* 
 }
 
 // One block (1024 threads) per row: exclusive scan of the row's csr counts
-// (NT <= 1024), a contiguous range of pair indices for the row taken from a
-// global counter (rows in any order), and the pair index of every csc entry.
+// (NT <= 1024) into csr_off, and a contiguous range of pair indices for the
+// row taken from a global counter (rows in any order) into row_base.
 __global__ void __launch_bounds__(1024) tile_pairs_kernel(int NT, int64_t cap,
                                                           const int32_t* __restrict__ csr_cnt,
-                                                          const int32_t* __restrict__ csc_cnt,
-                                                          const int32_t* __restrict__ csc,
-                                                          const int32_t* __restrict__ crank,
                                                           int32_t* __restrict__ csr_off,
                                                           int32_t* __restrict__ row_base,
-                                                          int32_t* __restrict__ csc_pair,
                                                           int32_t* __restrict__ pair_count,
                                                           uint32_t* __restrict__ err) {
-  __shared__ int s_off[1024];
   __shared__ int s_warp[32];
-  __shared__ int s_base;
   const int r = blockIdx.x, t = threadIdx.x, lane = t & 31, w = t >> 5;
   const int c = t < NT ? csr_cnt[(size_t)r * NT + t] : 0;
   int x = c;  // inclusive scan: within the warp, then over warp totals
@@ -167,23 +161,31 @@ __global__ void __launch_bounds__(1024) tile_pairs_kernel(int NT, int64_t cap,
   }
   __syncthreads();
   const int incl = x + (w > 0 ? s_warp[w - 1] : 0);
-  s_off[t] = incl - c;
+  if (t < NT) csr_off[(size_t)r * NT + t] = incl - c;
   if (t == 1023) {
     const int total = incl;
     const int base = atomicAdd(pair_count, total);
     if ((int64_t)base + total > cap) atomicOr(err, kErrCapacity);
-    s_base = base;
     row_base[r] = base;
   }
-  __syncthreads();
-  if (t < NT) csr_off[(size_t)r * NT + t] = s_off[t];
-  const int base = s_base;
-  for (int idx = t; idx < NT * NT; idx += 1024) {
-    const int kt = idx / NT, e = idx - kt * NT;
-    if (e < csc_cnt[(size_t)r * NT + kt]) {
-      const int qt = csc[((size_t)r * NT + kt) * NT + e] >> 1;
-      csc_pair[((size_t)r * NT + kt) * NT + e] = base + s_off[qt] + crank[((size_t)r * NT + qt) * NT + kt];
-    }
+}
+
+// One block per (key tile, row): the pair index of every entry of the key
+// tile's query list, row_base[r] + csr_off[r][qt] + the key tile's rank in
+// the query tile's list.
+__global__ void __launch_bounds__(128) tile_pair_index_kernel(int NT, const int32_t* __restrict__ csc_cnt,
+                                                              const int32_t* __restrict__ csc,
+                                                              const int32_t* __restrict__ crank,
+                                                              const int32_t* __restrict__ csr_off,
+                                                              const int32_t* __restrict__ row_base,
+                                                              int32_t* __restrict__ csc_pair) {
+  const int kt = blockIdx.x, r = blockIdx.y;
+  const int n = csc_cnt[(size_t)r * NT + kt];
+  const int base = row_base[r];
+  const size_t at = ((size_t)r * NT + kt) * NT;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int qt = csc[at + e] >> 1;
+    csc_pair[at + e] = base + csr_off[(size_t)r * NT + qt] + crank[((size_t)r * NT + qt) * NT + kt];
   }
 }
 
@@ -201,12 +203,12 @@ cudaError_t launch_lists(const stp_attn_desc* d, const int32_t* kmin, const int3
       reinterpret_cast<int32_t*>(base + m.csc_cnt), reinterpret_cast<int32_t*>(base + m.csc),
       reinterpret_cast<int32_t*>(base + m.crank));
   tile_pairs_kernel<<<d->n_rows, 1024, 0, s>>>(
-      NT, pair_capacity(d->n_rows, NT, d->max_tile_pairs),
-      reinterpret_cast<const int32_t*>(base + m.csr_cnt),
-      reinterpret_cast<const int32_t*>(base + m.csc_cnt),
-      reinterpret_cast<const int32_t*>(base + m.csc), reinterpret_cast<const int32_t*>(base + m.crank),
-      reinterpret_cast<int32_t*>(base + m.csr_off), reinterpret_cast<int32_t*>(base + m.row_base),
-      reinterpret_cast<int32_t*>(base + m.csc_pair), pair_count, err);
+      NT, pair_capacity(d->n_rows, NT, d->max_tile_pairs), reinterpret_cast<const int32_t*>(base + m.csr_cnt),
+      reinterpret_cast<int32_t*>(base + m.csr_off), reinterpret_cast<int32_t*>(base + m.row_base), pair_count, err);
+  tile_pair_index_kernel<<<grid, 128, 0, s>>>(
+      NT, reinterpret_cast<const int32_t*>(base + m.csc_cnt), reinterpret_cast<const int32_t*>(base + m.csc),
+      reinterpret_cast<const int32_t*>(base + m.crank), reinterpret_cast<const int32_t*>(base + m.csr_off),
+      reinterpret_cast<const int32_t*>(base + m.row_base), reinterpret_cast<int32_t*>(base + m.csc_pair));
   return cudaGetLastError();
 }
 
