@@ -443,9 +443,11 @@ def _batch(rank=0):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons every 50 ms; `stop(t0, t1)`
+    keeps the samples taken between two host wall-clock times (the timed
+    region) and summarizes those."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -457,34 +459,42 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
+        import datetime
+
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        sms, mx, reasons, power = [], None, set(), []
+        sms, mx, reasons, power, total = [], None, set(), [], 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 8:
+            if len(f) < 9:
                 continue
             try:
-                sms.append(float(f[0]))
-                mx = float(f[1])
-                power.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, smx, pw = float(f[1]), float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, val in zip(names, f[4:8]):
+            total += 1
+            if t0 is not None and not (t0 <= ts <= t1):
+                continue
+            sms.append(sm)
+            mx = smx
+            power.append(pw)
+            for n, val in zip(names, f[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sms),
-                "power_w_max": max(power) if power else None}
+                "reasons": sorted(reasons), "samples": len(sms), "samples_total": total,
+                "power_w_max": max(power) if power else None,
+                "window": "samples taken inside the timed region (every 50 ms)"}
 
 
 def _gpu_id(torch, dev):
@@ -629,7 +639,7 @@ def profile_case(name: str, reps: int) -> None:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -750,7 +760,8 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
-    time.sleep(0.3)
+    time.sleep(0.3)   # nvidia-smi's first sample
+    t_start = time.time()
     steps = []
     pack_ms.clear()
     for i in range(args.steps):
@@ -764,7 +775,8 @@ def main():
         cur ^= 1
         pack(cur)  # the next step's batch, while this one runs
     torch.cuda.synchronize()
-    clocks = sampler.stop()
+    t_end = time.time()
+    clocks = sampler.stop(t_start, t_end)
     if world > 1:
         dist.barrier()
     step_ms = [a.elapsed_time(e) for a, _, _, _, e in steps]
