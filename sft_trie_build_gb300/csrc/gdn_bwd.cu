@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "gdn_common.h"
@@ -115,6 +116,21 @@ bool map_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, int box_ro
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [rows, cols] of `esize`-byte elements as a 2-D tensor; boxes of 128 columns
+// x box_rows rows, no swizzle (rows of 128 elements in shared memory).
+bool map_rows(CUtensorMap* m, const void* base, CUtensorMapDataType type, int esize, int64_t rows, int cols,
+              int box_rows) {
+  EncodeFnB enc = encode_bwd();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * esize};
+  cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -658,7 +674,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
           const int s = cc * 32 + q;
-          F1[fx(t, s)] = (s < t && t < L) ? expf(gam[t] - gam[s]) * __uint_as_float(v[q]) : 0.f;
+          F1[fx(t, s)] = (s < t && t < L) ? __expf(gam[t] - gam[s]) * __uint_as_float(v[q]) : 0.f;
         }
       }
     } else {
@@ -982,120 +998,201 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
 // ---------------------------------------------------------------------------
 // Back through the unit-norm heads and SiLU: dz of every (token, channel),
 // written over dy; and the block's share of the weight gradient,
-// dw[c][tap] = sum over its tokens of x[source of the tap] dz.  Block = (64
+// dw[c][tap] = sum over its tokens of x[source of the tap] dz.  Unit = (64
 // tokens, one group of 128 channels: a q, k or v head); thread = (4 tokens,
-// 8 channels), so the 16 lanes of one token hold one head.  Every load of the
-// thread's four tokens is issued before any is used.
-__global__ void __launch_bounds__(kBT, 1) gdn_bwd_token_kernel(const GbParams p) {
-  __shared__ float red[16][16][33];   // [token lane][vector][8 channels x 4 taps]
-  const int grp = blockIdx.y, lt = threadIdx.x >> 4, vec = threadIdx.x & 15;
+// 8 channels), so the 16 lanes of one token hold one head.
+// A CTA keeps one channel group (its weights in registers) and walks token
+// blocks bx0, bx0 + S, ...: per block one TMA copy brings the x rows
+// xb-3 .. xb+63 of the group (bf16, zero rows outside the tensor) and one the
+// block's dy^ rows (f32), the next block's copies in flight while this one
+// is computed.  Per block the weight-gradient share is summed in a fixed
+// order (the two token lanes of a warp, then the warps) and written to the
+// block's slot, so the sum over blocks stays in block order.
+constexpr int kTkRows = 64 + 3;
+constexpr int kTkX = kTkRows * kD * 2;      // x rows, bf16
+constexpr int kTkY = 64 * kD * 4;           // dy^ rows, f32
+constexpr int kTkBuf = kTkX + kTkY;
+constexpr int kTkRed = (kBT / 32) * 16 * 33 * 4;   // [warp][vector][8 channels x 4 taps (+1)]
+constexpr int kTkSmem = 2 * kTkBuf + kTkRed + 64;
+
+__global__ void __launch_bounds__(kBT, 1) gdn_bwd_token_kernel(const __grid_constant__ CUtensorMap mx,
+                                                               const __grid_constant__ CUtensorMap my,
+                                                               const GbParams p, int S) {
+  extern __shared__ __align__(128) uint8_t tsm[];
+  float* red = reinterpret_cast<float*>(tsm + 2 * kTkBuf);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tsm + 2 * kTkBuf + kTkRed);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2);
+  __shared__ int taps[2][64][3];
+  const int G = 3 * p.H, nbx = (p.N + 63) / 64;
+  const int grp = blockIdx.x % G, bx0 = blockIdx.x / G;
+  const int warp = threadIdx.x >> 5, lt = threadIdx.x >> 4, vec = threadIdx.x & 15;
   const int ch = grp * kD + vec * 8;
   const bool is_qk = grp < 2 * p.H;
   const unsigned grpmask = 0xffffu << (threadIdx.x & 16);
-  int src[4][4];   // [token][tap]: the sources of taps 0..3 (-1: none; tap 2 = -2: a pad)
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int x = blockIdx.x * 64 + it * 16 + lt;
+  auto issue = [&](int bx, int buf) {
+    mbar_expect_tx(&bars[buf], kTkBuf);
+    tma_load_2d(tsm + buf * kTkBuf, &mx, &bars[buf], grp * kD, bx * 64 - 3);
+    tma_load_2d(tsm + buf * kTkBuf + kTkX, &my, &bars[buf], grp * kD, bx * 64);
+  };
+  auto load_taps = [&](int bx, int& t0, int& t1, int& t2) {
+    const int x = bx * 64 + threadIdx.x;
     const bool in = x < p.N;
-    src[it][2] = in ? p.prev[x] : -2;
-    src[it][1] = in ? p.prev2[x] : -1;
-    src[it][0] = in ? p.prev3[x] : -1;
-    src[it][3] = x;
+    t0 = in ? p.prev[x] : -2;
+    t1 = in ? p.prev2[x] : -1;
+    t2 = in ? p.prev3[x] : -1;
+  };
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    if (bx0 < nbx) issue(bx0, 0);
   }
-  uint4 xr[4][4];
-  float4 dya[4], dyb[4];
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const bool real = src[it][2] != -2;
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-      xr[it][t] = (real && src[it][t] >= 0) ? *reinterpret_cast<const uint4*>(p.x + (size_t)src[it][t] * p.C + ch)
-                                            : make_uint4(0, 0, 0, 0);
-    const float4* d = reinterpret_cast<const float4*>(p.dqkv + (size_t)src[it][3] * p.C + ch);
-    dya[it] = real ? d[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-    dyb[it] = real ? d[1] : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+  if (threadIdx.x < 64 && bx0 < nbx) load_taps(bx0, taps[0][threadIdx.x][0], taps[0][threadIdx.x][1], taps[0][threadIdx.x][2]);
   float4 wv[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) wv[i] = reinterpret_cast<const float4*>(p.conv_w)[ch + i];
-  float dw[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int t = 0; t < 4; ++t) dw[i][t] = 0.f;
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const bool real = src[it][2] != -2;   // the same for all 16 lanes of the token
-    float xin[4][8], z[8];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) unpack8(xr[it][t], xin[t]);
+  __syncthreads();
+  int j = 0;
+  for (int bx = bx0; bx < nbx; bx += S, ++j) {
+    const int buf = j & 1, nb = bx + S;
+    int n0 = -2, n1 = -1, n2 = -1;
+    if (nb < nbx) {   // the next block (that buffer was freed by the barrier ending the previous block)
+      if (threadIdx.x == 0) issue(nb, buf ^ 1);
+      if (threadIdx.x < 64) load_taps(nb, n0, n1, n2);
+    }
+    if (!__syncthreads_and(mbar_wait(&bars[buf], (j >> 1) & 1, abort_flag, p.err))) {
+      mbar_wait_drain(&bars[buf], (j >> 1) & 1);
+      if (nb < nbx) mbar_wait_drain(&bars[buf ^ 1], ((j + 1) >> 1) & 1);
+      return;
+    }
+    const int xb = bx * 64;
+    const uint8_t* xt = tsm + buf * kTkBuf;
+    const float* yt = reinterpret_cast<const float*>(tsm + buf * kTkBuf + kTkX);
+    float dw[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      z[i] = fmaf(wv[i].x, xin[0][i], fmaf(wv[i].y, xin[1][i], fmaf(wv[i].z, xin[2][i], wv[i].w * xin[3][i])));
-    const float dy0[8] = {dya[it].x, dya[it].y, dya[it].z, dya[it].w, dyb[it].x, dyb[it].y, dyb[it].z, dyb[it].w};
-    float sg[8], y[8], dy[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      sg[i] = 1.f / (1.f + expf(-z[i]));
-      y[i] = z[i] * sg[i];
-      dy[i] = dy0[i];
+      for (int t = 0; t < 4; ++t) dw[i][t] = 0.f;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int tl = it * 16 + lt, x = xb + tl;
+      const int p1 = taps[buf][tl][0];
+      const bool real = p1 != -2;   // the same for all 16 lanes of the token
+      const int src[4] = {taps[buf][tl][2], taps[buf][tl][1], p1, x};
+      float xin[4][8], z[8];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        uint4 r = make_uint4(0, 0, 0, 0);
+        if (real && src[t] >= 0) {
+          const int rr = src[t] - (xb - 3);
+          r = (rr >= 0 && rr < kTkRows) ? *reinterpret_cast<const uint4*>(xt + rr * (kD * 2) + vec * 16)
+                                        : *reinterpret_cast<const uint4*>(p.x + (size_t)src[t] * p.C + ch);
+        }
+        unpack8(r, xin[t]);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        z[i] = fmaf(wv[i].x, xin[0][i], fmaf(wv[i].y, xin[1][i], fmaf(wv[i].z, xin[2][i], wv[i].w * xin[3][i])));
+      float dy[8];
+      {
+        const float4 da = *reinterpret_cast<const float4*>(yt + tl * kD + vec * 8);
+        const float4 db = *reinterpret_cast<const float4*>(yt + tl * kD + vec * 8 + 4);
+        const float d8[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dy[i] = real ? d8[i] : 0.f;
+      }
+      float sg[8], y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        sg[i] = __fdividef(1.f, 1.f + __expf(-z[i]));
+        y[i] = z[i] * sg[i];
+      }
+      if (is_qk) {   // y^ = y / n,  dy = (dy^ - y^ (y^ . dy^)) / n
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(y[i], y[i], ss);
+        ss += __shfl_xor_sync(grpmask, ss, 8);
+        ss += __shfl_xor_sync(grpmask, ss, 4);
+        ss += __shfl_xor_sync(grpmask, ss, 2);
+        ss += __shfl_xor_sync(grpmask, ss, 1);
+        const float rn = rsqrtf(ss + 1e-6f);
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dot = fmaf(y[i] * rn, dy[i], dot);
+        dot += __shfl_xor_sync(grpmask, dot, 8);
+        dot += __shfl_xor_sync(grpmask, dot, 4);
+        dot += __shfl_xor_sync(grpmask, dot, 2);
+        dot += __shfl_xor_sync(grpmask, dot, 1);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dy[i] = (dy[i] - y[i] * rn * dot) * rn;
+      }
+      if (!real) continue;
+      float dz[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        dz[i] = dy[i] * sg[i] * (1.f + z[i] * (1.f - sg[i]));
+#pragma unroll
+        for (int t = 0; t < 4; ++t) dw[i][t] = fmaf(xin[t][i], dz[i], dw[i][t]);
+      }
+      float4* o = reinterpret_cast<float4*>(p.dqkv + (size_t)x * p.C + ch);
+      o[0] = make_float4(dz[0], dz[1], dz[2], dz[3]);
+      o[1] = make_float4(dz[4], dz[5], dz[6], dz[7]);
     }
-    if (is_qk) {   // y^ = y / n,  dy = (dy^ - y^ (y^ . dy^)) / n
-      float ss = 0.f;
+    // this block's weight-gradient share: the warp's two token lanes (lane
+    // and lane ^ 16), then the eight warps in order
 #pragma unroll
-      for (int i = 0; i < 8; ++i) ss = fmaf(y[i], y[i], ss);
-      ss += __shfl_xor_sync(grpmask, ss, 8);
-      ss += __shfl_xor_sync(grpmask, ss, 4);
-      ss += __shfl_xor_sync(grpmask, ss, 2);
-      ss += __shfl_xor_sync(grpmask, ss, 1);
-      const float rn = rsqrtf(ss + 1e-6f);
-      float dot = 0.f;
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) dot = fmaf(y[i] * rn, dy[i], dot);
-      dot += __shfl_xor_sync(grpmask, dot, 8);
-      dot += __shfl_xor_sync(grpmask, dot, 4);
-      dot += __shfl_xor_sync(grpmask, dot, 2);
-      dot += __shfl_xor_sync(grpmask, dot, 1);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dy[i] = (dy[i] - y[i] * rn * dot) * rn;
+      for (int t = 0; t < 4; ++t) {
+        const float v = dw[i][t] + __shfl_xor_sync(0xffffffffu, dw[i][t], 16);
+        if ((threadIdx.x & 16) == 0) red[(warp * 16 + vec) * 33 + i * 4 + t] = v;
+      }
+    if (threadIdx.x < 64 && nb < nbx) {
+      taps[buf ^ 1][threadIdx.x][0] = n0;
+      taps[buf ^ 1][threadIdx.x][1] = n1;
+      taps[buf ^ 1][threadIdx.x][2] = n2;
     }
-    if (!real) continue;
-    float dz[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      dz[i] = dy[i] * sg[i] * (1.f + z[i] * (1.f - sg[i]));
-#pragma unroll
-      for (int t = 0; t < 4; ++t) dw[i][t] = fmaf(xin[t][i], dz[i], dw[i][t]);
+    __syncthreads();
+    float* share = p.dwp + ((size_t)bx * p.C + grp * kD) * 4;
+    for (int e = threadIdx.x; e < 16 * 32; e += kBT) {
+      const int vv = e / 32, q = e % 32;
+      float acc = 0.f;
+      for (int w = 0; w < kBT / 32; ++w) acc += red[(w * 16 + vv) * 33 + q];
+      share[(vv * 8 + q / 4) * 4 + (q % 4)] = acc;
     }
-    float4* o = reinterpret_cast<float4*>(p.dqkv + (size_t)src[it][3] * p.C + ch);
-    o[0] = make_float4(dz[0], dz[1], dz[2], dz[3]);
-    o[1] = make_float4(dz[4], dz[5], dz[6], dz[7]);
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int t = 0; t < 4; ++t) red[lt][vec][i * 4 + t] = dw[i][t];
-  __syncthreads();
-  // this block's share, [block][channel][tap]: 128 channels x 4 taps, tokens summed in lane order
-  float* share = p.dwp + ((size_t)blockIdx.x * p.C + grp * kD) * 4;
-  for (int e = threadIdx.x; e < 16 * 32; e += kBT) {
-    const int vv = e / 32, j = e % 32;
-    float a = 0.f;
-    for (int l = 0; l < 16; ++l) a += red[l][vv][j];
-    share[(vv * 8 + j / 4) * 4 + (j % 4)] = a;
+    __syncthreads();   // red and this block's buffers are free for the next block
   }
 }
+
 
 // dx[j] = w3 dz[j] + sum over successors i of (w2 dz[i] + sum over successors
 // k of i of (w1 dz[k] + sum over successors l of k of w0 dz[l])): every token
 // that reads x[j] through a tap, summed in successor-list order.  Same block
 // and thread shape as the token kernel; pads get 0.
 __global__ void __launch_bounds__(kBT) gdn_bwd_dx_kernel(const GbParams p) {
+  // successor counts and first successors of the block's tokens and the
+  // three after them: inside a segment a token's readers are just the next
+  // three tokens, read directly; elsewhere (segment ends, branch points) the
+  // successor lists are walked
+  __shared__ int s_off[68], s_first[67];
   const int grp = blockIdx.y, lt = threadIdx.x >> 4, vec = threadIdx.x & 15;
   const int ch = grp * kD + vec * 8;
+  const int x0 = blockIdx.x * 64;
+  if (threadIdx.x < 68) {
+    const int t = x0 + (int)threadIdx.x;
+    s_off[threadIdx.x] = t <= p.N ? p.succ_off[t] : -1;
+  }
+  __syncthreads();
+  if (threadIdx.x < 67) {
+    const int t = x0 + (int)threadIdx.x;
+    s_first[threadIdx.x] =
+        (t < p.N && s_off[threadIdx.x + 1] - s_off[threadIdx.x] == 1) ? p.succ[s_off[threadIdx.x]] : -1;
+  }
   float4 wv[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) wv[i] = reinterpret_cast<const float4*>(p.conv_w)[ch + i];
+  __syncthreads();
   auto add = [&](float* acc, int src, int tap) {
     const float* d = p.dqkv + (size_t)src * p.C + ch;
     const float4 a = reinterpret_cast<const float4*>(d)[0], b = reinterpret_cast<const float4*>(d)[1];
@@ -1108,20 +1205,41 @@ __global__ void __launch_bounds__(kBT) gdn_bwd_dx_kernel(const GbParams p) {
   };
 #pragma unroll 1
   for (int it = 0; it < 4; ++it) {
-    const int x = blockIdx.x * 64 + it * 16 + lt;
+    const int tl = it * 16 + lt, x = x0 + tl;
     if (x >= p.N) continue;
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
     if (p.prev[x] != -2) {
-      add(acc, x, 3);
-      for (int a = p.succ_off[x]; a < p.succ_off[x + 1]; ++a) {
-        const int i1 = p.succ[a];
-        add(acc, i1, 2);
-        for (int b = p.succ_off[i1]; b < p.succ_off[i1 + 1]; ++b) {
-          const int i2 = p.succ[b];
-          add(acc, i2, 1);
-          for (int c = p.succ_off[i2]; c < p.succ_off[i2 + 1]; ++c) add(acc, p.succ[c], 0);
+      const bool simple = s_first[tl] == x + 1 && s_first[tl + 1] == x + 2 && s_first[tl + 2] == x + 3;
+      if (simple) {   // the same sums, in the same order, as the walk below
+        float4 r[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4* d = reinterpret_cast<const float4*>(p.dqkv + (size_t)(x + k) * p.C + ch);
+          r[2 * k] = d[0];
+          r[2 * k + 1] = d[1];
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float v[8] = {r[2 * k].x, r[2 * k].y, r[2 * k].z, r[2 * k].w,
+                              r[2 * k + 1].x, r[2 * k + 1].y, r[2 * k + 1].z, r[2 * k + 1].w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float w = k == 0 ? wv[i].w : k == 1 ? wv[i].z : k == 2 ? wv[i].y : wv[i].x;
+            acc[i] = fmaf(w, v[i], acc[i]);
+          }
+        }
+      } else {
+        add(acc, x, 3);
+        for (int a = p.succ_off[x]; a < p.succ_off[x + 1]; ++a) {
+          const int i1 = p.succ[a];
+          add(acc, i1, 2);
+          for (int b = p.succ_off[i1]; b < p.succ_off[i1 + 1]; ++b) {
+            const int i2 = p.succ[b];
+            add(acc, i2, 1);
+            for (int c = p.succ_off[i2]; c < p.succ_off[i2 + 1]; ++c) add(acc, p.succ[c], 0);
+          }
         }
       }
     }
@@ -1209,7 +1327,10 @@ extern "C" stp_status stp_gdn_bwd(const stp_gdn_desc* desc, const void* plan, co
   p.dg = dg;
   p.dbeta = dbeta;
   p.err = reinterpret_cast<uint32_t*>(ws);
-  CUtensorMap mwq, mkt, mpm;
+  CUtensorMap mwq, mkt, mpm, mtx, mty;
+  if (!map_rows(&mtx, p.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, C, kTkRows) ||
+      !map_rows(&mty, p.dqkv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, N, C, 64))
+    return fail(STP_ECUDA, "stp_gdn_bwd: tensor map encoding failed");
   if (n_chunk > 0 &&
       (!map_2d(&mwq, p.wq, (int64_t)n_chunk * H * 128, kD, 128) ||
        !map_2d(&mkt, p.kt, (int64_t)n_chunk * H * kC, kD, kC) ||
@@ -1221,6 +1342,8 @@ extern "C" stp_status stp_gdn_bwd(const stp_gdn_desc* desc, const void* plan, co
     attr_err = cudaFuncSetAttribute(gdn_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWkSmem);
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(gdn_bwd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCkSmem);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(gdn_bwd_token_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTkSmem);
   });
   if (attr_err != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_bwd: %s", cudaGetErrorString(attr_err));
   // pads keep dq^, dk^, dv = 0 (the chunk kernel writes real tokens only)
@@ -1235,7 +1358,19 @@ extern "C" stp_status stp_gdn_bwd(const stp_gdn_desc* desc, const void* plan, co
   }
   if (n_chunk > 0) gdn_bwd_chunk_kernel<<<(unsigned)(n_chunk * H), kCkThreads, kCkSmem, s>>>(p);
   const unsigned n_blocks = (unsigned)((N + 63) / 64);
-  gdn_bwd_token_kernel<<<dim3(n_blocks, (unsigned)(3 * H)), kBT, 0, s>>>(p);
+  {
+    // a CTA per (channel group, one of S token-block strides)
+    static int n_sm = 0;
+    if (n_sm == 0) {
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
+        n_sm = 148;
+    }
+    const int G = 3 * H;
+    const int S = std::max(1, std::min((int)n_blocks, n_sm / G > 0 ? n_sm / G : 1));
+    gdn_bwd_token_kernel<<<(unsigned)(G * S), kBT, kTkSmem, s>>>(mtx, mty, p, S);
+  }
   gdn_bwd_dx_kernel<<<dim3(n_blocks, (unsigned)(3 * H)), kBT, 0, s>>>(p);
   gdn_bwd_dw_kernel<<<(unsigned)((C * 4 + kBT - 1) / kBT), kBT, 0, s>>>(p, (int)n_blocks);
   e = cudaGetLastError();
