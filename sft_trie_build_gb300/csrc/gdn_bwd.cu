@@ -335,18 +335,21 @@ __global__ void __launch_bounds__(kWkThreads, 1)
         }
         fence_after_sync();
       }
-      // E1: dS_n out ([d_v][d_k]), to the bf16 operand, decayed in place
+      // E1: dS_n to the bf16 operand and decayed in place, then (off the
+      // chain: the products of this chunk already run) out to global
+      // memory ([d_v][d_k]) from registers
       float* dse = p.dsend + row * kD * kD;
-#pragma unroll 1
+      uint32_t vv[128];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lrow + cc * 32, vv + cc * 32);
+      tmem_ld_wait();
+#pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        tmem_ld32(tmem + lrow + cc * 32, v);
-        tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 32; ++q) dse[(cc * 32 + q) * kD + r] = __uint_as_float(v[q]);
+        for (int j = 0; j < 4; ++j)
+          st_sw8(dsb, 128, r, cc * 4 + j, pack8(reinterpret_cast<const float*>(vv) + cc * 32 + 8 * j));
 #pragma unroll
-        for (int j = 0; j < 4; ++j) st_sw8(dsb, 128, r, cc * 4 + j, pack8(reinterpret_cast<const float*>(v) + 8 * j));
-#pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * dec);
+        for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(vv[cc * 32 + q]) * dec);
         tmem_st32(tmem + lrow + cc * 32, v);
       }
       tmem_st_wait();
@@ -354,6 +357,8 @@ __global__ void __launch_bounds__(kWkThreads, 1)
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[W_E1]);
+#pragma unroll
+      for (int q = 0; q < 128; ++q) dse[q * kD + r] = __uint_as_float(vv[q]);
       // E2: dV' out ([d_v][64]) and -dV' into rows 64-127 of this chunk's DOV
       uint8_t* dov = sm + kWkOffDov + (n & 1) * 32768;
       if (warp < 2) {
@@ -363,24 +368,23 @@ __global__ void __launch_bounds__(kWkThreads, 1)
         }
         fence_after_sync();
         float* dvo = p.dvp + row * kC * kD;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          tmem_ld32(tmem + 128 + lrow + cc * 32, v);
-          tmem_ld_wait();
 #pragma unroll
-          for (int q = 0; q < 32; ++q) dvo[(cc * 32 + q) * kC + r] = __uint_as_float(v[q]);
+        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + 128 + lrow + cc * 32, vv + cc * 32);
+        tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float f[8];
+        for (int j = 0; j < 16; ++j) {
+          float f[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) f[k] = -__uint_as_float(v[8 * j + k]);
-            st_sw8(dov, 128, kC + r, cc * 4 + j, pack8(f));
-          }
+          for (int k = 0; k < 8; ++k) f[k] = -__uint_as_float(vv[8 * j + k]);
+          st_sw8(dov, 128, kC + r, j, pack8(f));
         }
         fence_proxy_async_smem();
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[W_E2]);
+        // dV' out ([d_v][64]) once the next product may start
+#pragma unroll
+        for (int q = 0; q < 128; ++q) dvo[q * kC + r] = __uint_as_float(vv[q]);
       }
     }
     if (ok && (nck == 0 || __all_sync(0xffffffffu, mbar_wait(&bars[W_M2], (nck - 1) & 1, abort_flag, p.err)))) {
