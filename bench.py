@@ -52,11 +52,11 @@ METRIC = "tree-attn fwd+bwd useful TFLOP/s (% of BF16 peak) and trajectories/s o
 # DRAM bytes (read + write) of one backward call on the workload above, from
 # one ncu capture of every launch of the second call of
 #   python bench.py --profile attn --reps 1
-# (dram__bytes_read.sum + dram__bytes_write.sum, -s 21 -c 21): bwd_delta_kernel
-# 270.6e6 + 22.5e6, the eight bwd_tc_kernel launches 617.7e6 + 3677.4e6, the
-# eight dq_tc_kernel launches 4152.4e6 + 53.9e6.  To be retaken whenever one of
+# (dram__bytes_read.sum + dram__bytes_write.sum, -s 22 -c 22): bwd_delta_kernel
+# 270.6e6 + 22.6e6, the eight bwd_tc_kernel launches 617.5e6 + 3677.4e6, the
+# eight dq_tc_kernel launches 4152.3e6 + 53.1e6.  To be retaken whenever one of
 # the three kernels changes.
-BWD_DRAM_BYTES = 270605568 + 22479360 + 617688576 + 3677362176 + 4152424448 + 53880832
+BWD_DRAM_BYTES = 270577152 + 22558976 + 617461504 + 3677415936 + 4152305920 + 53067264
 
 
 def _peaks():
