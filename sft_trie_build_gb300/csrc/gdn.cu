@@ -13,10 +13,11 @@
 // (the WY form of the delta rule: substituting the recurrence into itself
 // chunk by chunk).  Three kernels (the training forward also writes each
 // chunk's starting state S0 for the backward in gdn_bwd.cu):
-//   gdn_conv_kernel   one block per (64 tokens, q / k / v head): width-4 causal
-//                     convolution along each token's path (prev pointers of
-//                     the plan; the block's rows arrive by one TMA copy),
-//                     SiLU, unit q and k heads; pads get o = 0.
+//   gdn_conv_kernel   persistent, a CTA per (q / k / v head, token-block
+//                     stride), 128-token blocks: width-4 causal convolution
+//                     along each token's path (prev pointers of the plan; a
+//                     block's rows arrive by one TMA copy), SiLU, unit q and k
+//                     heads; pads get o = 0.
 //   gdn_prep_kernel   one block per (chunk, head): [Q K^T; K K^T] on the tensor
 //                     core; T = (I + A)^{-1} of the unit-lower-triangular
 //                     system in float32 (two 32 x 32 diagonal blocks by
@@ -54,6 +55,7 @@ using namespace tc;
 constexpr int kGd = 128;          // head dim
 constexpr int kGc = kGdnChunk;    // tokens per chunk
 constexpr int kConvThreads = 256;
+constexpr int kConvPerSm = 2;   // resident convolution CTAs per SM (~100 registers a thread)
 constexpr int kPrepThreads = 256;
 constexpr int kStThreads = 192;   // warps 0-3 epilogue, 4 loads, 5 MMA
 
@@ -85,7 +87,7 @@ constexpr int kOffBar = kOffOst + 64 * kOstLd;
 constexpr int kStSmem = kOffBar + 256 + 1024;
 
 struct GdnParams {
-  int N, H, C, seg0, chunk0;   // seg0, chunk0: first segment / chunk of a launch
+  int N, T, H, C, seg0, chunk0;   // T: row length; seg0, chunk0: first segment / chunk of a launch
   float scale;
   const int32_t* prev;      // token 1, 2 and 3 back on the path (-2 on prev: a pad)
   const int32_t* prev2;
@@ -186,32 +188,40 @@ __device__ __forceinline__ void unpack8(const uint4 r, float* f) {
 }
 
 // ---------------------------------------------------------------------------
-// Path convolution + SiLU + unit q, k heads.  Unit of work = (64 tokens, one
-// group of 128 channels: a q, k or v head); thread = (token of 16, 8
-// channels), so the 16 lanes of a token hold one head.  A CTA keeps one
-// channel group (its weights stay in registers) and walks token blocks
-// bx0, bx0 + S, ...; one TMA copy per block brings the x rows xb-3 .. xb+63
-// of the group (zero rows outside the tensor) into shared memory, the next
-// block's copy and path pointers in flight while this one is computed.
-// Inside a segment the taps of token x are x-3 .. x, all in the tile; a tap
-// is read from memory only where the path turns (a segment's first tokens,
-// whose taps lie in the parent).
-constexpr int kConvRows = 64 + 3;
+// Path convolution + SiLU + unit q, k heads.  Unit of work = (kConvTok
+// tokens, one group of 128 channels: a q, k or v head); thread = (4
+// consecutive tokens of each 64, 8 channels), so the 16 lanes of a token hold
+// one head.  A CTA keeps one channel group (its weights stay in registers)
+// and walks token blocks bx0, bx0 + S, ...; one TMA copy per block brings the
+// x rows xb-3 .. xb+kConvTok-1 of the group (zero rows outside the tensor)
+// into shared memory, the next block's copy and path pointers in flight
+// while this one is computed.
+// Inside a segment the taps of token x are x-3 .. x, all in the tile: a
+// thread unpacks the 7 rows of its 4 tokens' taps once and slides over them;
+// a tap is read again only where the path turns (a segment's first tokens,
+// whose taps lie in the parent).  The taps are summed in order 0..3 with
+// two-lane float multiply-adds.
+constexpr int kConvTok = 128;                     // tokens per block
+constexpr int kConvRows = kConvTok + 3;
 constexpr int kConvBuf = kConvRows * kGd * 2;   // one block's rows, bf16
+constexpr int kConvSmem = 2 * kConvBuf + 128;   // two blocks, 128-byte aligned
 
-__global__ void __launch_bounds__(kConvThreads, 4) gdn_conv_kernel(const __grid_constant__ CUtensorMap mx,
+__global__ void __launch_bounds__(kConvThreads, kConvPerSm) gdn_conv_kernel(const __grid_constant__ CUtensorMap mx,
                                                                    const GdnParams p, int S) {
-  __shared__ __align__(128) uint8_t xs[2][kConvBuf];   // [67 rows][128 channels] bf16, two blocks
-  __shared__ int taps[2][64][3];   // the 1, 2 and 3 tokens back on each token's path (-2: pad or past the end)
+  extern __shared__ uint8_t conv_dyn[];
+  uint8_t* const xs0 = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(conv_dyn) + 127) & ~uintptr_t(127));
+  auto xs = [&](int b) { return xs0 + b * kConvBuf; };   // [kConvRows rows][128 channels] bf16, two blocks
+  __shared__ int taps[2][kConvTok][3];   // the 1, 2 and 3 tokens back on each token's path (-2: pad or past the end)
+  __shared__ uint32_t plain[2][kConvTok / 32];   // bit t: token t of the block has taps t-3 .. t (no pad, no turn)
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ int abort_flag;
-  const int G = 3 * p.H, nbx = (p.N + 63) / 64;
+  const int G = 3 * p.H, nbx = (p.N + kConvTok - 1) / kConvTok;
   const int grp = blockIdx.x % G, bx0 = blockIdx.x / G;
   const int lt = threadIdx.x >> 4, vec = threadIdx.x & 15;
   const int ch = grp * kGd + vec * 8;
   const bool is_qk = grp < 2 * p.H;
   auto load_taps = [&](int bx, int& t0, int& t1, int& t2) {
-    const int x = bx * 64 + threadIdx.x;
+    const int x = bx * kConvTok + threadIdx.x;
     const bool in = x < p.N;
     t0 = in ? p.prev[x] : -2;
     t1 = in ? p.prev2[x] : -1;
@@ -224,19 +234,41 @@ __global__ void __launch_bounds__(kConvThreads, 4) gdn_conv_kernel(const __grid_
     fence_mbar_init();
     if (bx0 < nbx) {
       mbar_expect_tx(&bars[0], kConvBuf);
-      tma_load_2d_g(xs[0], &mx, &bars[0], grp * kGd, bx0 * 64 - 3);
+      tma_load_2d_g(xs(0), &mx, &bars[0], grp * kGd, bx0 * kConvTok - 3);
     }
   }
-  if (threadIdx.x < 64 && bx0 < nbx) {
+  // whole warps (a token each) store a block's pointers and plain bits
+  auto store_taps = [&](int b, int bx, int t0, int t1, int t2) {
+    const int x = bx * kConvTok + threadIdx.x;
+    taps[b][threadIdx.x][0] = t0;
+    taps[b][threadIdx.x][1] = t1;
+    taps[b][threadIdx.x][2] = t2;
+    const uint32_t m = __ballot_sync(0xffffffffu, x >= 3 && t0 == x - 1 && t1 == x - 2 && t2 == x - 3);
+    if ((threadIdx.x & 31) == 0) plain[b][threadIdx.x >> 5] = m;
+  };
+  if (threadIdx.x < kConvTok && bx0 < nbx) {
     int t0, t1, t2;
     load_taps(bx0, t0, t1, t2);
-    taps[0][threadIdx.x][0] = t0;
-    taps[0][threadIdx.x][1] = t1;
-    taps[0][threadIdx.x][2] = t2;
+    store_taps(0, bx0, t0, t1, t2);
   }
-  float4 wv[8];
+  float2 wt[4][4];   // tap t of channels ch + 2i, ch + 2i + 1
 #pragma unroll
-  for (int i = 0; i < 8; ++i) wv[i] = reinterpret_cast<const float4*>(p.conv_w)[ch + i];
+  for (int i = 0; i < 4; ++i) {
+    const float4 w0 = reinterpret_cast<const float4*>(p.conv_w)[ch + 2 * i];
+    const float4 w1 = reinterpret_cast<const float4*>(p.conv_w)[ch + 2 * i + 1];
+    wt[0][i] = make_float2(w0.x, w1.x);
+    wt[1][i] = make_float2(w0.y, w1.y);
+    wt[2][i] = make_float2(w0.z, w1.z);
+    wt[3][i] = make_float2(w0.w, w1.w);
+  }
+  // A row's pads are its tail, so a block that lies in one row and starts
+  // with a pad is all pads: its rows are not copied (thread 0 reads the
+  // block's first pointer one block ahead).
+  auto all_pads = [&](int b, int first_prev) {
+    const int x0 = b * kConvTok, x1 = min(x0 + kConvTok - 1, p.N - 1);
+    return first_prev == -2 && x0 / p.T == x1 / p.T;
+  };
+  int prev_ahead = (threadIdx.x == 0 && bx0 + S < nbx) ? p.prev[(bx0 + S) * kConvTok] : 0;
   __syncthreads();
   int j = 0;
   for (int bx = bx0; bx < nbx; bx += S, ++j) {
@@ -245,10 +277,15 @@ __global__ void __launch_bounds__(kConvThreads, 4) gdn_conv_kernel(const __grid_
     if (nb < nbx) {   // the next block: its rows by TMA (that buffer was freed by the barrier
                       // that ended the previous block), its path pointers into registers
       if (threadIdx.x == 0) {
-        mbar_expect_tx(&bars[buf ^ 1], kConvBuf);
-        tma_load_2d_g(xs[buf ^ 1], &mx, &bars[buf ^ 1], grp * kGd, nb * 64 - 3);
+        if (all_pads(nb, prev_ahead)) {
+          mbar_arrive(&bars[buf ^ 1]);   // nothing to copy: complete the phase
+        } else {
+          mbar_expect_tx(&bars[buf ^ 1], kConvBuf);
+          tma_load_2d_g(xs(buf ^ 1), &mx, &bars[buf ^ 1], grp * kGd, nb * kConvTok - 3);
+        }
+        prev_ahead = nb + S < nbx ? p.prev[(nb + S) * kConvTok] : 0;
       }
-      if (threadIdx.x < 64) load_taps(nb, n0, n1, n2);
+      if (threadIdx.x < kConvTok) load_taps(nb, n0, n1, n2);
     }
     if (!__syncthreads_and(mbar_wait(&bars[buf], (j >> 1) & 1, &abort_flag, p.err))) {
       // gave up: let the copies in flight land, then leave
@@ -256,66 +293,137 @@ __global__ void __launch_bounds__(kConvThreads, 4) gdn_conv_kernel(const __grid_
       if (nb < nbx) mbar_wait_drain(&bars[buf ^ 1], ((j + 1) >> 1) & 1);
       return;
     }
-    const int xb = bx * 64;
-    const uint8_t* xt = xs[buf];
+    const int xb = bx * kConvTok;
+    const uint8_t* xt = xs(buf) + vec * 16;
+    // This thread's tokens are xb + tb .. xb + tb + 3 for tb = 4 lt, 64 + 4 lt,
+    // ...; tile row r holds token xb - 3 + r, so their in-segment taps are
+    // tile rows tb .. tb + 6, each unpacked once into a ring of four rows
+    // (row tb + j in win[j & 3]).
+#pragma unroll 1
+    for (int h = 0; h < kConvTok / 64; ++h) {
+      const int tb = 64 * h + 4 * lt;
+      const unsigned grpmask = 0xffffu << (threadIdx.x & 16);
+      if (((plain[buf][tb >> 5] >> (tb & 31)) & 0xFu) == 0xFu) {
+        // The common case, four tokens inside one segment: straight-line code,
+        // so the four tokens' chains overlap.  Tile row tb + r is tap r - k of
+        // token k; rows are taken in order, so each token sums taps 0..3 in order.
+        float2 acc[4][4];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int tl = it * 16 + lt, x = xb + tl;
-      const bool in = x < p.N;
-      const int p1 = taps[buf][tl][0];
-      if (p1 == -2) {
-        if (in && grp < p.H) {   // a pad: o = 0 for head grp
-          float4* o4 = reinterpret_cast<float4*>(p.o + ((size_t)x * p.H + grp) * kGd + vec * 8);
-          o4[0] = o4[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[k][i] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < 7; ++r) {
+          float f[8];
+          unpack8(*reinterpret_cast<const uint4*>(xt + (tb + r) * (kGd * 2)), f);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (r - k < 0 || r - k > 3) continue;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              acc[k][i] = __ffma2_rn(wt[r - k][i], make_float2(f[2 * i], f[2 * i + 1]), acc[k][i]);
+          }
         }
-        continue;   // all 16 lanes of a token take the same branch
-      }
-      const int src[4] = {taps[buf][tl][2], taps[buf][tl][1], p1, x};   // taps 0..3
-      float acc[8];
+        float a[4][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        for (int k = 0; k < 4; ++k)
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        if (src[t] < 0) continue;
-        const int r = src[t] - (xb - 3);
-        const uint4 v = (r >= 0 && r < kConvRows)
-                            ? *reinterpret_cast<const uint4*>(xt + r * (kGd * 2) + vec * 16)
-                            : *reinterpret_cast<const uint4*>(p.x + (size_t)src[t] * p.C + ch);
-        float f[8];
-        unpack8(v, f);
+          for (int i = 0; i < 4; ++i) {
+            a[k][2 * i] = __fdividef(acc[k][i].x, 1.f + __expf(-acc[k][i].x));
+            a[k][2 * i + 1] = __fdividef(acc[k][i].y, 1.f + __expf(-acc[k][i].y));
+          }
+        if (is_qk) {
+          float ss[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float w = t == 0 ? wv[i].x : t == 1 ? wv[i].y : t == 2 ? wv[i].z : wv[i].w;
-          acc[i] = fmaf(w, f[i], acc[i]);
+          for (int k = 0; k < 4; ++k) {
+            ss[k] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss[k] = fmaf(a[k][i], a[k][i], ss[k]);
+          }
+#pragma unroll
+          for (int o = 8; o >= 1; o >>= 1)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) ss[k] += __shfl_xor_sync(grpmask, ss[k], o);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float rn = rsqrtf(ss[k] + 1e-6f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[k][i] *= rn;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 out;
+          out.x = pack_bf16x2(a[k][0], a[k][1]);
+          out.y = pack_bf16x2(a[k][2], a[k][3]);
+          out.z = pack_bf16x2(a[k][4], a[k][5]);
+          out.w = pack_bf16x2(a[k][6], a[k][7]);
+          *reinterpret_cast<uint4*>(p.y + (size_t)(xb + tb + k) * p.C + ch) = out;
+        }
+      } else {
+        float win[4][8];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) unpack8(*reinterpret_cast<const uint4*>(xt + (tb + j) * (kGd * 2)), win[j]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int tl = tb + k, x = xb + tl;
+          unpack8(*reinterpret_cast<const uint4*>(xt + (tl + 3) * (kGd * 2)), win[(k + 3) & 3]);
+          const int p1 = taps[buf][tl][0];
+          if (p1 == -2) {
+            if (x < p.N && grp < p.H) {   // a pad: o = 0 for head grp
+              float4* o4 = reinterpret_cast<float4*>(p.o + ((size_t)x * p.H + grp) * kGd + vec * 8);
+              o4[0] = o4[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            continue;   // all 16 lanes of a token take the same branch
+          }
+          const int src[3] = {taps[buf][tl][2], taps[buf][tl][1], p1};   // taps 0..2; tap 3 is x itself
+          float2 acc[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float* f = win[(k + t) & 3];
+            float g[8];
+            if (t < 3 && src[t] != x - 3 + t) {   // the path turns here (or has no such tap)
+              if (src[t] < 0) continue;
+              const int r = src[t] - (xb - 3);
+              const uint4 v = (r >= 0 && r < kConvRows)
+                                  ? *reinterpret_cast<const uint4*>(xt + r * (kGd * 2))
+                                  : *reinterpret_cast<const uint4*>(p.x + (size_t)src[t] * p.C + ch);
+              unpack8(v, g);
+              f = g;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = __ffma2_rn(wt[t][i], make_float2(f[2 * i], f[2 * i + 1]), acc[i]);
+          }
+          float a[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            a[2 * i] = __fdividef(acc[i].x, 1.f + __expf(-acc[i].x));
+            a[2 * i + 1] = __fdividef(acc[i].y, 1.f + __expf(-acc[i].y));
+          }
+          if (is_qk) {
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss = fmaf(a[i], a[i], ss);
+            ss += __shfl_xor_sync(grpmask, ss, 8);
+            ss += __shfl_xor_sync(grpmask, ss, 4);
+            ss += __shfl_xor_sync(grpmask, ss, 2);
+            ss += __shfl_xor_sync(grpmask, ss, 1);
+            const float r = rsqrtf(ss + 1e-6f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] *= r;
+          }
+          uint4 out;
+          out.x = pack_bf16x2(a[0], a[1]);
+          out.y = pack_bf16x2(a[2], a[3]);
+          out.z = pack_bf16x2(a[4], a[5]);
+          out.w = pack_bf16x2(a[6], a[7]);
+          *reinterpret_cast<uint4*>(p.y + (size_t)x * p.C + ch) = out;
         }
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = __fdividef(acc[i], 1.f + __expf(-acc[i]));
-      if (is_qk) {
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ss = fmaf(acc[i], acc[i], ss);
-        const unsigned grpmask = 0xffffu << (threadIdx.x & 16);
-        ss += __shfl_xor_sync(grpmask, ss, 8);
-        ss += __shfl_xor_sync(grpmask, ss, 4);
-        ss += __shfl_xor_sync(grpmask, ss, 2);
-        ss += __shfl_xor_sync(grpmask, ss, 1);
-        const float r = rsqrtf(ss + 1e-6f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] *= r;
-      }
-      uint4 out;
-      out.x = pack_bf16x2(acc[0], acc[1]);
-      out.y = pack_bf16x2(acc[2], acc[3]);
-      out.z = pack_bf16x2(acc[4], acc[5]);
-      out.w = pack_bf16x2(acc[6], acc[7]);
-      *reinterpret_cast<uint4*>(p.y + (size_t)x * p.C + ch) = out;
     }
-    if (threadIdx.x < 64 && nb < nbx) {
-      taps[buf ^ 1][threadIdx.x][0] = n0;
-      taps[buf ^ 1][threadIdx.x][1] = n1;
-      taps[buf ^ 1][threadIdx.x][2] = n2;
-    }
+    if (threadIdx.x < kConvTok && nb < nbx) store_taps(buf ^ 1, nb, n0, n1, n2);
     __syncthreads();   // this block's rows and pointers are read; the next block's pointers are in
   }
 }
@@ -960,6 +1068,7 @@ stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d
   const int32_t* dp = static_cast<const int32_t*>(d_plan);
   GdnParams p;
   p.N = N;
+  p.T = desc->row_len;
   p.H = H;
   p.C = 3 * H * kGd;
   p.seg0 = 0;
@@ -1002,13 +1111,15 @@ stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d
   std::call_once(attr_once, [] {
     attr_err = cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmem);
     if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(gdn_conv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kConvSmem);
+    if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(gdn_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStSmem);
   });
   cudaError_t e = attr_err;
   if (e == cudaSuccess) e = cudaMemsetAsync(p.err, 0, 4, s);
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e));
   if (N > 0) {
-    // a CTA per (channel group, one of S token-block strides): 4 resident per SM
+    // a CTA per (channel group, one of S token-block strides): kConvPerSm resident per SM
     static int n_sm = 0;
     if (n_sm == 0) {
       int dev = 0;
@@ -1016,9 +1127,9 @@ stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d
                                                     cudaSuccess || n_sm <= 0)
         n_sm = 148;
     }
-    const int G = 3 * H, nbx = (N + 63) / 64;
-    const int S = std::max(1, std::min(nbx, 4 * n_sm / G));
-    gdn_conv_kernel<<<(unsigned)(G * S), kConvThreads, 0, s>>>(mx, p, S);
+    const int G = 3 * H, nbx = (N + kConvTok - 1) / kConvTok;
+    const int S = std::max(1, std::min(nbx, kConvPerSm * n_sm / G));
+    gdn_conv_kernel<<<(unsigned)(G * S), kConvThreads, kConvSmem, s>>>(mx, p, S);
   }
   // The chunks of depth 0 are prepared and walked on a high-priority stream
   // (the walk is one CTA per head and root segment: a few SMs), while the

@@ -42,6 +42,26 @@ def test_random_forests(seed):
     _compare(OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared), H=2, seed=seed)
 
 
+@pytest.mark.parametrize("T,seed", [(200, 0), (456, 12)])
+def test_rows_not_multiple_of_block(T, seed):
+    """Rows whose length is not a multiple of the convolution's token block:
+    some blocks start in one row's pads and hold the next row's first tokens
+    (they must be copied), others lie in one row's pads (they need not be).
+    Both kinds occur in these two batches for blocks of 64 and of 128."""
+    b = W.random_forest(seed, n_roots=6, max_depth=2, max_children=3, len_lo=5, len_hi=60, row_len=T,
+                        min_shared=4, vocab=41)
+    po = OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared)
+    N = po.n_rows * T
+    for blk in (64, 128):
+        kinds = set()
+        for x0 in range(0, N, blk):
+            x1 = min(x0 + blk - 1, N - 1)
+            if x0 % T >= po.used[x0 // T]:   # starts with a pad
+                kinds.add("one row" if x0 // T == x1 // T else "straddles")
+        assert kinds == {"one row", "straddles"}
+    _compare(po, H=2, seed=seed)
+
+
 def test_deep_narrow_tree():
     b = W.random_forest(11, n_roots=1, max_depth=6, max_children=2, len_lo=20, len_hi=90, row_len=1024,
                         min_shared=4, vocab=41)
