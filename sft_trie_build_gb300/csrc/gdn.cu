@@ -57,7 +57,7 @@ constexpr int kGc = kGdnChunk;    // tokens per chunk
 constexpr int kConvThreads = 256;
 constexpr int kConvPerSm = 2;   // resident convolution CTAs per SM (~100 registers a thread)
 constexpr int kPrepThreads = 256;
-constexpr int kStThreads = 192;   // warps 0-3 epilogue, 4 loads, 5 MMA
+constexpr int kStThreads = 320;   // warps 0-7 epilogue (a TMEM lane, half its columns), 8 loads, 9 MMA
 
 // gdn_prep_kernel shared memory, from a 1024-byte aligned base: [Q; K] as a
 // 128 x 128 bf16 K-major operand (128-byte swizzle, two 64-column halves);
@@ -757,11 +757,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
   const int par = p.seg_parent[sidx];
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < B_COUNT; ++b) mbar_init(&bars[b], (b == B_SR) ? 4 : (b == B_VR || b == B_UE) ? 2 : 1);
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(&bars[b], (b == B_SR) ? 8 : (b == B_VR || b == B_UE) ? 4 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -771,7 +771,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
   // columns 0-127: the state S; 128 + 128 b (b = chunk parity): [Q~ S0 + P V' ; W S0]
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0) {
       // ------------------------------------------------------------ loads
       tma_prefetch_desc(&mwq);
@@ -800,7 +800,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
       if (lastu >= 0) mbar_wait_drain(&bars[B_UF], lastu);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA
       constexpr uint32_t id_kmn = idesc_bf16(128, 128, 0, 1);
@@ -836,26 +836,28 @@ __global__ void __launch_bounds__(kStThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int r = threadIdx.x;   // TMEM lane: the state's k row; of the accumulator, the chunk row
-    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-    uint32_t v[128];
-    // One padded 528-byte row per thread: a row in shared memory, then one bulk copy to HBM.
+    // thread = (TMEM lane r, column half hc): warps w and w + 4 share lanes 32 (w % 4) ..
+    const int r = threadIdx.x & 127, hc = warp >> 2;   // r: the state's k row; of the accumulator, the chunk row
+    const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16, col0 = (uint32_t)hc * 64;
+    uint32_t v[64];
+    // Half of a padded 528-byte row per thread: into shared memory, then one bulk copy to HBM.
     auto row_out = [&](uint8_t* buf, float* dst) {
-      bulk_wait_read0();   // the previous copy from this row has read it
+      bulk_wait_read0();   // the previous copy from this half row has read it
+      buf += hc * 256;
 #pragma unroll
-      for (int q = 0; q < 32; ++q)
+      for (int q = 0; q < 16; ++q)
         reinterpret_cast<uint4*>(buf)[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       fence_proxy_async_smem();
-      bulk_store(dst, buf, 512);
+      bulk_store(dst + col0, buf, 256);
       bulk_commit();
     };
     {
-      const float* src = par >= 0 ? p.state + (((size_t)par * p.H + h) * kGd + r) * kGd : nullptr;
+      const float* src = par >= 0 ? p.state + (((size_t)par * p.H + h) * kGd + r) * kGd + col0 : nullptr;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
         for (int q = 0; q < 32; ++q) v[q] = src ? __float_as_uint(src[cc * 32 + q]) : 0u;
-        tmem_st32(tmem + lrow + cc * 32, v);
+        tmem_st32(tmem + lrow + col0 + cc * 32, v);
       }
       tmem_st_wait();
     }
@@ -871,22 +873,21 @@ __global__ void __launch_bounds__(kStThreads, 1)
         x0_next = p.chunk_start[c0 + i + 1];
         dec_next = p.decay[(c0 + i + 1) * p.H + h];
       }
-      // E1: S0 -> bf16 operand (k rows, v contiguous in two 64-column halves); S <- e^{gam_L} S0
+      // E1: S0 -> bf16 operand (k rows, v contiguous in two 64-column halves: this
+      // thread's half is one of them); S <- e^{gam_L} S0
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lrow + cc * 32, v + 32 * cc);
+      for (int cc = 0; cc < 2; ++cc) tmem_ld32(tmem + lrow + col0 + cc * 32, v + 32 * cc);
       tmem_ld_wait();
       if (p.s0) {   // training: keep the chunk's starting state for the backward, as [d_v][d_k]
-        float* d = p.s0 + (size_t)((c0 + i) * p.H + h) * kGd * kGd + r;
+        float* d = p.s0 + (size_t)((c0 + i) * p.H + h) * kGd * kGd + (size_t)col0 * kGd + r;
 #pragma unroll
-        for (int q = 0; q < 128; ++q) d[q * kGd] = __uint_as_float(v[q]);
+        for (int q = 0; q < 64; ++q) d[q * kGd] = __uint_as_float(v[q]);
       }
+      {
+        uint8_t* half = sm + kOffSop + hc * 16384 + r * 128;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint8_t* half = sm + kOffSop + (cc >> 1) * 16384 + r * 128;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const uint32_t* e = v + 32 * cc + 8 * jj;
-          const int j = (cc & 1) * 4 + jj;
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t* e = v + 8 * j;
           uint4 w;
           w.x = pack_bf16x2(__uint_as_float(e[0]), __uint_as_float(e[1]));
           w.y = pack_bf16x2(__uint_as_float(e[2]), __uint_as_float(e[3]));
@@ -896,21 +897,21 @@ __global__ void __launch_bounds__(kStThreads, 1)
         }
       }
 #pragma unroll
-      for (int q = 0; q < 128; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * dec);
+      for (int q = 0; q < 64; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * dec);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_st32(tmem + lrow + cc * 32, v + 32 * cc);
+      for (int cc = 0; cc < 2; ++cc) tmem_st32(tmem + lrow + col0 + cc * 32, v + 32 * cc);
       tmem_st_wait();
       fence_proxy_async_smem();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_SR]);
 
-      if (warp < 2) {
+      if ((warp & 3) < 2) {
         // E3 of the previous chunk: its output rows 0-63 of the other accumulator
         if (i > 0) {
           const uint32_t d1p = tmem + 128 + 128 * ((i - 1) & 1);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) tmem_ld32(d1p + lrow + cc * 32, v + 32 * cc);
+          for (int cc = 0; cc < 2; ++cc) tmem_ld32(d1p + lrow + col0 + cc * 32, v + 32 * cc);
           tmem_ld_wait();
           if (r < L_prev) row_out(sm + kOffOst + r * kOstLd, p.o + ((size_t)(x0_prev + r) * p.H + h) * kGd);
         }
@@ -925,27 +926,23 @@ __global__ void __launch_bounds__(kStThreads, 1)
         fence_after_sync();
         const uint32_t d1 = tmem + 128 + 128 * (i & 1);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld32(d1 + lrow + cc * 32, v + 32 * cc);
+        for (int cc = 0; cc < 2; ++cc) tmem_ld32(d1 + lrow + col0 + cc * 32, v + 32 * cc);
         tmem_ld_wait();
+        uint8_t* half = sm + kOffVop + hc * 8192 + t * 128;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint8_t* half = sm + kOffVop + (cc >> 1) * 8192 + t * 128;
+        for (int j = 0; j < 8; ++j) {
+          float f[8];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int col = cc * 32 + 8 * jj + e;
-              f[e] = ut_s[col * kGc + t] - __uint_as_float(v[col]);
-            }
-            const int j = (cc & 1) * 4 + jj;
-            uint4 w;
-            w.x = pack_bf16x2(f[0], f[1]);
-            w.y = pack_bf16x2(f[2], f[3]);
-            w.z = pack_bf16x2(f[4], f[5]);
-            w.w = pack_bf16x2(f[6], f[7]);
-            *reinterpret_cast<uint4*>(half + ((j ^ (t & 7)) << 4)) = w;
+          for (int e = 0; e < 8; ++e) {
+            const int col = 8 * j + e;
+            f[e] = ut_s[(col0 + col) * kGc + t] - __uint_as_float(v[col]);
           }
+          uint4 w;
+          w.x = pack_bf16x2(f[0], f[1]);
+          w.y = pack_bf16x2(f[2], f[3]);
+          w.z = pack_bf16x2(f[4], f[5]);
+          w.w = pack_bf16x2(f[6], f[7]);
+          *reinterpret_cast<uint4*>(half + ((j ^ (t & 7)) << 4)) = w;
         }
         fence_proxy_async_smem();
         fence_before_sync();
@@ -968,17 +965,17 @@ __global__ void __launch_bounds__(kStThreads, 1)
       dec = dec_next;
     }
     if (ok) {
-      if (warp < 2) {   // the last chunk's output rows
+      if ((warp & 3) < 2) {   // the last chunk's output rows
         const uint32_t d1p = tmem + 128 + 128 * ((nck - 1) & 1);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld32(d1p + lrow + cc * 32, v + 32 * cc);
+        for (int cc = 0; cc < 2; ++cc) tmem_ld32(d1p + lrow + col0 + cc * 32, v + 32 * cc);
         tmem_ld_wait();
         if (r < L_prev) row_out(sm + kOffOst + r * kOstLd, p.o + ((size_t)(x0_prev + r) * p.H + h) * kGd);
       }
       // the segment's final state, for its children (rows 64-127 go through the
       // operand buffers, which no MMA reads any more)
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lrow + cc * 32, v + 32 * cc);
+      for (int cc = 0; cc < 2; ++cc) tmem_ld32(tmem + lrow + col0 + cc * 32, v + 32 * cc);
       tmem_ld_wait();
       uint8_t* buf = r < 64 ? sm + kOffOst + r * kOstLd : sm + kOffSop + (r - 64) * kOstLd;
       row_out(buf, p.state + (((size_t)sidx * p.H + h) * kGd + r) * kGd);
@@ -990,7 +987,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace

@@ -162,11 +162,12 @@ __device__ __forceinline__ uint32_t desc_lo_mn8k(uint32_t addr) {
 //   E2  dV' goes out (transposed) and -dV' becomes rows 64-127 of DOV;
 //   M2  dS += [Q~^T | W^T] [dO ; -dV']  (the [Q~; W] tile read MN-major).
 // The segment's start gradient dS0 goes out at the end.
-// Warps 0-3 epilogue (thread = TMEM lane), warp 4 loads ([Q~; W], K~, P of
-// the next chunk into the other of two stages), warp 5 MMA and TMEM owner.
+// Warps 0-7 epilogue (thread = TMEM lane and half of its columns), warp 8
+// loads ([Q~; W], K~, P of the next chunk into the other of two stages), warp
+// 9 MMA and TMEM owner.
 // Global layouts written here (each warp's stores contiguous): dS_n of a
 // chunk and a segment's dS0 as [d_v][d_k], dV' of a chunk as [d_v][64].
-constexpr int kWkThreads = 192;
+constexpr int kWkThreads = 320;   // warps 0-7 epilogue (a TMEM lane, half its columns), 8 loads, 9 MMA
 constexpr int kWkStage = 57344;                  // [Q~; W] 32 KB | K~ 16 KB | P 8 KB
 constexpr int kWkOffKt = 32768, kWkOffP = 49152;
 constexpr int kWkOffDsb = 2 * kWkStage;          // dS_n bf16 [128 d_k][128 d_v], MN-major B
@@ -201,11 +202,11 @@ __global__ void __launch_bounds__(kWkThreads, 1)
   const int c0 = p.seg_chunk0[seg], nck = (p.seg_len[seg] + kC - 1) / kC;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < W_COUNT; ++b) mbar_init(&bars[b], b == W_E1 ? 4 : b == W_E2 ? 2 : 1);
+    for (int b = 0; b < W_COUNT; ++b) mbar_init(&bars[b], b == W_E1 ? 8 : b == W_E2 ? 4 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 256);
     tmem_relinquish();
   }
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
   fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0) {
       // ------------------------------------------------------------ loads
       tma_prefetch_desc(&mwq);
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
         if (last[st] >= 0) mbar_wait_drain(&bars[W_F + st], last[st]);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA
       constexpr uint32_t id_mnmn = idesc_bf16(128, 128, 1, 1);
@@ -276,20 +277,22 @@ __global__ void __launch_bounds__(kWkThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int r = threadIdx.x;   // TMEM lane: d_k row of dS; token row of dV'
-    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    // thread = (TMEM lane r, column half hc): warps w and w + 4 share lanes 32 (w % 4) ..
+    const int r = threadIdx.x & 127, hc = warp >> 2;   // r: d_k row of dS; token row of dV'
+    const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16, col0 = (uint32_t)hc * 64;
     uint8_t* dsb = sm + kWkOffDsb;
     uint32_t v[32];
-    // dO rows of the n-th chunk processed into DOV buffer n % 2 (rows 0-63):
-    // 64 rows x 16 pieces of 8 columns, 8 pieces per thread, all loads in flight at once
-    auto load_do = [&](int n) {
+    // dO rows of the n-th chunk processed into DOV buffer n % 2 (rows 0-63),
+    // by the 128 threads of warps 2, 3, 6, 7 (index u): 64 rows x 16 pieces
+    // of 8 columns, 8 pieces per thread, all loads in flight at once
+    auto load_do = [&](int n, int u) {
       const int c = c0 + nck - 1 - n, L = p.chunk_len[c], x0 = p.chunk_start[c];
       uint8_t* dov = sm + kWkOffDov + (n & 1) * 32768;
       const float* dO = p.d_o + (size_t)x0 * p.H * kD + h * kD;
       float4 a[8], b[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const int e = threadIdx.x + 128 * k, t = e >> 4, c8 = e & 15;
+        const int e = u + 128 * k, t = e >> 4, c8 = e & 15;
         a[k] = b[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (t < L) {
           const float4* src = reinterpret_cast<const float4*>(dO + (size_t)t * p.H * kD + c8 * 8);
@@ -299,7 +302,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const int e = threadIdx.x + 128 * k, t = e >> 4, c8 = e & 15;
+        const int e = u + 128 * k, t = e >> 4, c8 = e & 15;
         const float f[8] = {a[k].x, a[k].y, a[k].z, a[k].w, b[k].x, b[k].y, b[k].z, b[k].w};
         st_sw8(dov, 128, t, c8, pack8(f));
       }
@@ -307,27 +310,30 @@ __global__ void __launch_bounds__(kWkThreads, 1)
     {   // the segment's end gradient: the sum of its children's start gradients
       const int k0 = p.child_off[seg], k1 = p.child_off[seg + 1];
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
           float a = 0.f;
           for (int c = k0; c < k1; ++c)
-            a += p.sgrad[(((size_t)p.child[c] * p.H + h) * kD + cc * 32 + q) * kD + r];
+            a += p.sgrad[(((size_t)p.child[c] * p.H + h) * kD + col0 + cc * 32 + q) * kD + r];
           v[q] = __float_as_uint(a);
         }
-        tmem_st32(tmem + lrow + cc * 32, v);
+        tmem_st32(tmem + lrow + col0 + cc * 32, v);
       }
       tmem_st_wait();
     }
     bool ok = true;
+    // Warps 0, 1, 4, 5 make -dV' (E2: TMEM lanes 0-63); warps 2, 3, 6, 7 load
+    // the dO rows, each chunk's while the chunk before it is finished: the
+    // DOV buffer of chunk n + 1 was last read by the products of chunk n - 1,
+    // complete before E1 of chunk n.
+    const bool e2_warp = (warp & 3) < 2;
+    const int u = (warp & 1) * 32 + hc * 64 + lane;
+    if (nck > 0 && !e2_warp) load_do(0, u);
     for (int n = 0; ok && n < nck; ++n) {
       const int c = c0 + nck - 1 - n, L = p.chunk_len[c], x0 = p.chunk_start[c];
       const size_t row = (size_t)c * p.H + h;
       const float dec = p.decay[row];
-      // this chunk's dO rows: their DOV buffer was last read by the products
-      // of chunk n - 2, complete before E1 of chunk n - 1, so the loads
-      // overlap the products of chunk n - 1
-      load_do(n);
       if (n > 0) {
         if (!__all_sync(0xffffffffu, mbar_wait(&bars[W_M2], (n - 1) & 1, abort_flag, p.err))) {
           ok = false;
@@ -339,18 +345,18 @@ __global__ void __launch_bounds__(kWkThreads, 1)
       // chain: the products of this chunk already run) out to global
       // memory ([d_v][d_k]) from registers
       float* dse = p.dsend + row * kD * kD;
-      uint32_t vv[128];
+      uint32_t vv[64];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + lrow + cc * 32, vv + cc * 32);
+      for (int cc = 0; cc < 2; ++cc) tmem_ld32(tmem + lrow + col0 + cc * 32, vv + cc * 32);
       tmem_ld_wait();
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          st_sw8(dsb, 128, r, cc * 4 + j, pack8(reinterpret_cast<const float*>(vv) + cc * 32 + 8 * j));
+          st_sw8(dsb, 128, r, hc * 8 + cc * 4 + j, pack8(reinterpret_cast<const float*>(vv) + cc * 32 + 8 * j));
 #pragma unroll
         for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(vv[cc * 32 + q]) * dec);
-        tmem_st32(tmem + lrow + cc * 32, v);
+        tmem_st32(tmem + lrow + col0 + cc * 32, v);
       }
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -358,10 +364,11 @@ __global__ void __launch_bounds__(kWkThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[W_E1]);
 #pragma unroll
-      for (int q = 0; q < 128; ++q) dse[q * kD + r] = __uint_as_float(vv[q]);
+      for (int q = 0; q < 64; ++q) dse[(col0 + q) * kD + r] = __uint_as_float(vv[q]);
+      if (!e2_warp && n + 1 < nck) load_do(n + 1, u);
       // E2: dV' out ([d_v][64]) and -dV' into rows 64-127 of this chunk's DOV
       uint8_t* dov = sm + kWkOffDov + (n & 1) * 32768;
-      if (warp < 2) {
+      if (e2_warp) {
         if (!__all_sync(0xffffffffu, mbar_wait(&bars[W_M1], n & 1, abort_flag, p.err))) {
           ok = false;
           break;
@@ -369,14 +376,14 @@ __global__ void __launch_bounds__(kWkThreads, 1)
         fence_after_sync();
         float* dvo = p.dvp + row * kC * kD;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + 128 + lrow + cc * 32, vv + cc * 32);
+        for (int cc = 0; cc < 2; ++cc) tmem_ld32(tmem + 128 + lrow + col0 + cc * 32, vv + cc * 32);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 8; ++j) {
           float f[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) f[k] = -__uint_as_float(vv[8 * j + k]);
-          st_sw8(dov, 128, kC + r, j, pack8(f));
+          st_sw8(dov, 128, kC + r, hc * 8 + j, pack8(f));
         }
         fence_proxy_async_smem();
         fence_before_sync();
@@ -384,7 +391,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
         if (lane == 0) mbar_arrive(&bars[W_E2]);
         // dV' out ([d_v][64]) once the next product may start
 #pragma unroll
-        for (int q = 0; q < 128; ++q) dvo[q * kC + r] = __uint_as_float(vv[q]);
+        for (int q = 0; q < 64; ++q) dvo[(col0 + q) * kC + r] = __uint_as_float(vv[q]);
       }
     }
     if (ok && (nck == 0 || __all_sync(0xffffffffu, mbar_wait(&bars[W_M2], (nck - 1) & 1, abort_flag, p.err)))) {
@@ -392,11 +399,11 @@ __global__ void __launch_bounds__(kWkThreads, 1)
       // the segment's start gradient dS0 ([d_v][d_k])
       float* sg = p.sgrad + ((size_t)seg * p.H + h) * kD * kD;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        tmem_ld32(tmem + lrow + cc * 32, v);
+      for (int cc = 0; cc < 2; ++cc) {
+        tmem_ld32(tmem + lrow + col0 + cc * 32, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 32; ++q) sg[(cc * 32 + q) * kD + r] = __uint_as_float(v[q]);
+        for (int q = 0; q < 32; ++q) sg[(col0 + cc * 32 + q) * kD + r] = __uint_as_float(v[q]);
       }
     }
   }
@@ -405,7 +412,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 5) tmem_dealloc(tmem, 256);
+  if (warp == 9) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
