@@ -878,11 +878,6 @@ __global__ void __launch_bounds__(kStThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) tmem_ld32(tmem + lrow + col0 + cc * 32, v + 32 * cc);
       tmem_ld_wait();
-      if (p.s0) {   // training: keep the chunk's starting state for the backward, as [d_v][d_k]
-        float* d = p.s0 + (size_t)((c0 + i) * p.H + h) * kGd * kGd + (size_t)col0 * kGd + r;
-#pragma unroll
-        for (int q = 0; q < 64; ++q) d[q * kGd] = __uint_as_float(v[q]);
-      }
       {
         uint8_t* half = sm + kOffSop + hc * 16384 + r * 128;
 #pragma unroll
@@ -897,14 +892,23 @@ __global__ void __launch_bounds__(kStThreads, 1)
         }
       }
 #pragma unroll
-      for (int q = 0; q < 64; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * dec);
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t w[32];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) tmem_st32(tmem + lrow + col0 + cc * 32, v + 32 * cc);
+        for (int q = 0; q < 32; ++q) w[q] = __float_as_uint(__uint_as_float(v[32 * cc + q]) * dec);
+        tmem_st32(tmem + lrow + col0 + cc * 32, w);
+      }
       tmem_st_wait();
       fence_proxy_async_smem();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_SR]);
+      if (p.s0) {   // training: keep the chunk's starting state for the backward, as [d_v][d_k]
+                    // (off the chain: the products of this chunk already run)
+        float* d = p.s0 + (size_t)((c0 + i) * p.H + h) * kGd * kGd + (size_t)col0 * kGd + r;
+#pragma unroll
+        for (int q = 0; q < 64; ++q) d[q * kGd] = __uint_as_float(v[q]);
+      }
 
       if ((warp & 3) < 2) {
         // E3 of the previous chunk: its output rows 0-63 of the other accumulator

@@ -162,12 +162,15 @@ __device__ __forceinline__ uint32_t desc_lo_mn8k(uint32_t addr) {
 //   E2  dV' goes out (transposed) and -dV' becomes rows 64-127 of DOV;
 //   M2  dS += [Q~^T | W^T] [dO ; -dV']  (the [Q~; W] tile read MN-major).
 // The segment's start gradient dS0 goes out at the end.
-// Warps 0-7 epilogue (thread = TMEM lane and half of its columns), warp 8
-// loads ([Q~; W], K~, P of the next chunk into the other of two stages), warp
-// 9 MMA and TMEM owner.
+// kWkEpiWarps epilogue warps (thread = TMEM lane and kWkCw of its columns),
+// then a loads warp ([Q~; W], K~, P of the next chunk into the other of two
+// stages) and the MMA warp, which owns TMEM.
 // Global layouts written here (each warp's stores contiguous): dS_n of a
 // chunk and a segment's dS0 as [d_v][d_k], dV' of a chunk as [d_v][64].
-constexpr int kWkThreads = 320;   // warps 0-7 epilogue (a TMEM lane, half its columns), 8 loads, 9 MMA
+constexpr int kWkEpiWarps = 16;                  // epilogue warps: kWkEpiWarps / 4 per TMEM lane group (8 measured slower)
+constexpr int kWkCw = 512 / kWkEpiWarps;         // columns of a TMEM lane per epilogue thread
+constexpr int kWkThreads = 32 * kWkEpiWarps + 64;   // then a loads warp and an MMA warp
+static_assert(kWkCw % 32 == 0 && kWkCw <= 64, "walk kernel column split");
 constexpr int kWkStage = 57344;                  // [Q~; W] 32 KB | K~ 16 KB | P 8 KB
 constexpr int kWkOffKt = 32768, kWkOffP = 49152;
 constexpr int kWkOffDsb = 2 * kWkStage;          // dS_n bf16 [128 d_k][128 d_v], MN-major B
@@ -202,11 +205,11 @@ __global__ void __launch_bounds__(kWkThreads, 1)
   const int c0 = p.seg_chunk0[seg], nck = (p.seg_len[seg] + kC - 1) / kC;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < W_COUNT; ++b) mbar_init(&bars[b], b == W_E1 ? 8 : b == W_E2 ? 4 : 1);
+    for (int b = 0; b < W_COUNT; ++b) mbar_init(&bars[b], b == W_E1 ? kWkEpiWarps : b == W_E2 ? kWkEpiWarps / 2 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kWkEpiWarps + 1) {
     tmem_alloc(tmem_slot, 256);
     tmem_relinquish();
   }
@@ -215,7 +218,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
   fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == kWkEpiWarps) {
     if (lane == 0) {
       // ------------------------------------------------------------ loads
       tma_prefetch_desc(&mwq);
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
         if (last[st] >= 0) mbar_wait_drain(&bars[W_F + st], last[st]);
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == kWkEpiWarps + 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA
       constexpr uint32_t id_mnmn = idesc_bf16(128, 128, 1, 1);
@@ -277,22 +280,25 @@ __global__ void __launch_bounds__(kWkThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // thread = (TMEM lane r, column half hc): warps w and w + 4 share lanes 32 (w % 4) ..
-    const int r = threadIdx.x & 127, hc = warp >> 2;   // r: d_k row of dS; token row of dV'
-    const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16, col0 = (uint32_t)hc * 64;
+    // thread = (TMEM lane r, kWkCw columns from col0): the warps w, w + 4, ...
+    // share lanes 32 (w % 4) ..
+    const int r = threadIdx.x & 127;   // r: d_k row of dS; token row of dV'
+    const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16, col0 = (uint32_t)(warp >> 2) * kWkCw;
+    const int pc0 = (int)col0 >> 3;   // this thread's first 16-byte piece of a bf16 operand row
     uint8_t* dsb = sm + kWkOffDsb;
     uint32_t v[32];
     // dO rows of the n-th chunk processed into DOV buffer n % 2 (rows 0-63),
-    // by the 128 threads of warps 2, 3, 6, 7 (index u): 64 rows x 16 pieces
-    // of 8 columns, 8 pieces per thread, all loads in flight at once
+    // by the threads of the warps w with w % 4 >= 2 (index u): 64 rows x 16
+    // pieces of 8 columns, all loads of a thread in flight at once
+    constexpr int kNu = 16 * kWkEpiWarps, kPer = 1024 / kNu;
     auto load_do = [&](int n, int u) {
       const int c = c0 + nck - 1 - n, L = p.chunk_len[c], x0 = p.chunk_start[c];
       uint8_t* dov = sm + kWkOffDov + (n & 1) * 32768;
       const float* dO = p.d_o + (size_t)x0 * p.H * kD + h * kD;
-      float4 a[8], b[8];
+      float4 a[kPer], b[kPer];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int e = u + 128 * k, t = e >> 4, c8 = e & 15;
+      for (int k = 0; k < kPer; ++k) {
+        const int e = u + kNu * k, t = e >> 4, c8 = e & 15;
         a[k] = b[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (t < L) {
           const float4* src = reinterpret_cast<const float4*>(dO + (size_t)t * p.H * kD + c8 * 8);
@@ -301,8 +307,8 @@ __global__ void __launch_bounds__(kWkThreads, 1)
         }
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int e = u + 128 * k, t = e >> 4, c8 = e & 15;
+      for (int k = 0; k < kPer; ++k) {
+        const int e = u + kNu * k, t = e >> 4, c8 = e & 15;
         const float f[8] = {a[k].x, a[k].y, a[k].z, a[k].w, b[k].x, b[k].y, b[k].z, b[k].w};
         st_sw8(dov, 128, t, c8, pack8(f));
       }
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
     {   // the segment's end gradient: the sum of its children's start gradients
       const int k0 = p.child_off[seg], k1 = p.child_off[seg + 1];
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < kWkCw / 32; ++cc) {
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
           float a = 0.f;
@@ -323,12 +329,12 @@ __global__ void __launch_bounds__(kWkThreads, 1)
       tmem_st_wait();
     }
     bool ok = true;
-    // Warps 0, 1, 4, 5 make -dV' (E2: TMEM lanes 0-63); warps 2, 3, 6, 7 load
-    // the dO rows, each chunk's while the chunk before it is finished: the
-    // DOV buffer of chunk n + 1 was last read by the products of chunk n - 1,
-    // complete before E1 of chunk n.
+    // The warps w with w % 4 < 2 make -dV' (E2: TMEM lanes 0-63); the others
+    // load the dO rows, each chunk's while the chunk before it is finished:
+    // the DOV buffer of chunk n + 1 was last read by the products of chunk
+    // n - 1, complete before E1 of chunk n.
     const bool e2_warp = (warp & 3) < 2;
-    const int u = (warp & 1) * 32 + hc * 64 + lane;
+    const int u = ((warp >> 2) * 2 + (warp & 1)) * 32 + lane;
     if (nck > 0 && !e2_warp) load_do(0, u);
     for (int n = 0; ok && n < nck; ++n) {
       const int c = c0 + nck - 1 - n, L = p.chunk_len[c], x0 = p.chunk_start[c];
@@ -345,15 +351,15 @@ __global__ void __launch_bounds__(kWkThreads, 1)
       // chain: the products of this chunk already run) out to global
       // memory ([d_v][d_k]) from registers
       float* dse = p.dsend + row * kD * kD;
-      uint32_t vv[64];
+      uint32_t vv[kWkCw];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) tmem_ld32(tmem + lrow + col0 + cc * 32, vv + cc * 32);
+      for (int cc = 0; cc < kWkCw / 32; ++cc) tmem_ld32(tmem + lrow + col0 + cc * 32, vv + cc * 32);
       tmem_ld_wait();
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < kWkCw / 32; ++cc) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          st_sw8(dsb, 128, r, hc * 8 + cc * 4 + j, pack8(reinterpret_cast<const float*>(vv) + cc * 32 + 8 * j));
+          st_sw8(dsb, 128, r, pc0 + cc * 4 + j, pack8(reinterpret_cast<const float*>(vv) + cc * 32 + 8 * j));
 #pragma unroll
         for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(vv[cc * 32 + q]) * dec);
         tmem_st32(tmem + lrow + col0 + cc * 32, v);
@@ -364,7 +370,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[W_E1]);
 #pragma unroll
-      for (int q = 0; q < 64; ++q) dse[(col0 + q) * kD + r] = __uint_as_float(vv[q]);
+      for (int q = 0; q < kWkCw; ++q) dse[(col0 + q) * kD + r] = __uint_as_float(vv[q]);
       if (!e2_warp && n + 1 < nck) load_do(n + 1, u);
       // E2: dV' out ([d_v][64]) and -dV' into rows 64-127 of this chunk's DOV
       uint8_t* dov = sm + kWkOffDov + (n & 1) * 32768;
@@ -376,14 +382,14 @@ __global__ void __launch_bounds__(kWkThreads, 1)
         fence_after_sync();
         float* dvo = p.dvp + row * kC * kD;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) tmem_ld32(tmem + 128 + lrow + col0 + cc * 32, vv + cc * 32);
+        for (int cc = 0; cc < kWkCw / 32; ++cc) tmem_ld32(tmem + 128 + lrow + col0 + cc * 32, vv + cc * 32);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < kWkCw / 8; ++j) {
           float f[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k) f[k] = -__uint_as_float(vv[8 * j + k]);
-          st_sw8(dov, 128, kC + r, hc * 8 + j, pack8(f));
+          st_sw8(dov, 128, kC + r, pc0 + j, pack8(f));
         }
         fence_proxy_async_smem();
         fence_before_sync();
@@ -391,7 +397,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
         if (lane == 0) mbar_arrive(&bars[W_E2]);
         // dV' out ([d_v][64]) once the next product may start
 #pragma unroll
-        for (int q = 0; q < 64; ++q) dvo[(col0 + q) * kC + r] = __uint_as_float(vv[q]);
+        for (int q = 0; q < kWkCw; ++q) dvo[(col0 + q) * kC + r] = __uint_as_float(vv[q]);
       }
     }
     if (ok && (nck == 0 || __all_sync(0xffffffffu, mbar_wait(&bars[W_M2], (nck - 1) & 1, abort_flag, p.err)))) {
@@ -399,7 +405,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
       // the segment's start gradient dS0 ([d_v][d_k])
       float* sg = p.sgrad + ((size_t)seg * p.H + h) * kD * kD;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < kWkCw / 32; ++cc) {
         tmem_ld32(tmem + lrow + col0 + cc * 32, v);
         tmem_ld_wait();
 #pragma unroll
@@ -412,7 +418,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 9) tmem_dealloc(tmem, 256);
+  if (warp == kWkEpiWarps + 1) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
