@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(kStThreads, 1)
   const int par = p.seg_parent[sidx];
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < B_COUNT; ++b) mbar_init(&bars[b], (b == B_SR) ? 8 : (b == B_VR || b == B_UE) ? 4 : 1);
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(&bars[b], (b == B_SR || b == B_VR) ? 8 : (b == B_UE) ? 4 : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -891,6 +891,12 @@ __global__ void __launch_bounds__(kStThreads, 1)
           *reinterpret_cast<uint4*>(half + ((j ^ (r & 7)) << 4)) = w;
         }
       }
+      fence_proxy_async_smem();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_SR]);
+      // the decayed state goes back while [Q~; W] S0 runs (that product reads
+      // the bf16 copy); K~^T V' adds to it only after every warp's B_VR arrival
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t w[32];
@@ -899,10 +905,11 @@ __global__ void __launch_bounds__(kStThreads, 1)
         tmem_st32(tmem + lrow + col0 + cc * 32, w);
       }
       tmem_st_wait();
-      fence_proxy_async_smem();
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_SR]);
+      if ((warp & 3) < 2) {   // the E2 warps arrive once V' is in place too
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_VR]);   // this warp's part of the state is stored
+      }
       if (p.s0) {   // training: keep the chunk's starting state for the backward, as [d_v][d_k]
                     // (off the chain: the products of this chunk already run)
         float* d = p.s0 + (size_t)((c0 + i) * p.H + h) * kGd * kGd + (size_t)col0 * kGd + r;

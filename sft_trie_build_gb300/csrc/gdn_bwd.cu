@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
   const int c0 = p.seg_chunk0[seg], nck = (p.seg_len[seg] + kC - 1) / kC;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < W_COUNT; ++b) mbar_init(&bars[b], b == W_E1 ? kWkEpiWarps : b == W_E2 ? kWkEpiWarps / 2 : 1);
+    for (int b = 0; b < W_COUNT; ++b) mbar_init(&bars[b], (b == W_E1 || b == W_E2) ? kWkEpiWarps : 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -360,15 +360,25 @@ __global__ void __launch_bounds__(kWkThreads, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           st_sw8(dsb, 128, r, pc0 + cc * 4 + j, pack8(reinterpret_cast<const float*>(vv) + cc * 32 + 8 * j));
+      }
+      fence_proxy_async_smem();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[W_E1]);
+      // the decayed dS goes back while the first products run (they read the
+      // bf16 copy); the second adds to it only after every warp's W_E2 arrival
+#pragma unroll
+      for (int cc = 0; cc < kWkCw / 32; ++cc) {
 #pragma unroll
         for (int q = 0; q < 32; ++q) v[q] = __float_as_uint(__uint_as_float(vv[cc * 32 + q]) * dec);
         tmem_st32(tmem + lrow + col0 + cc * 32, v);
       }
       tmem_st_wait();
-      fence_proxy_async_smem();
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[W_E1]);
+      if (!e2_warp) {   // the E2 warps arrive once -dV' is in place too
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[W_E2]);   // this warp's part of dS is stored
+      }
 #pragma unroll
       for (int q = 0; q < kWkCw; ++q) dse[(col0 + q) * kD + r] = __uint_as_float(vv[q]);
       if (!e2_warp && n + 1 < nck) load_do(n + 1, u);
