@@ -1195,8 +1195,9 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_token_kernel(const __grid_cons
 
 // dx[j] = w3 dz[j] + sum over successors i of (w2 dz[i] + sum over successors
 // k of i of (w1 dz[k] + sum over successors l of k of w0 dz[l])): every token
-// that reads x[j] through a tap, summed in successor-list order.  Same block
-// and thread shape as the token kernel; pads get 0.
+// that reads x[j] through a tap, summed in successor-list order.  A block per
+// (64 tokens, channel group of 128); thread = (4 consecutive tokens, 8
+// channels); pads get 0.
 __global__ void __launch_bounds__(kBT) gdn_bwd_dx_kernel(const GbParams p) {
   // successor counts and first successors of the block's tokens and the
   // three after them: inside a segment a token's readers are just the next
@@ -1230,43 +1231,65 @@ __global__ void __launch_bounds__(kBT) gdn_bwd_dx_kernel(const GbParams p) {
       acc[i] = fmaf(w, v[i], acc[i]);
     }
   };
+  // thread = (4 consecutive tokens tb .. tb + 3 of the block, 8 channels)
+  const int tb = 4 * lt;
+  bool plain4 = x0 + tb + 3 < p.N;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int tl = tb + k, x = x0 + tl;
+    plain4 = plain4 && p.prev[x] != -2 && s_first[tl] == x + 1 && s_first[tl + 1] == x + 2 &&
+             s_first[tl + 2] == x + 3;
+  }
+  if (plain4) {
+    // Four tokens inside a segment: token k reads rows x + k .. x + k + 3 with
+    // taps 3, 2, 1, 0; the 7 rows are taken once, in order, so every token's
+    // sum has the order of the general path below.
+    const int x = x0 + tb;
+    float acc[4][8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[k][i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 7; ++j) {
+      const float4* d = reinterpret_cast<const float4*>(p.dqkv + (size_t)(x + j) * p.C + ch);
+      const float4 ra = d[0], rb = d[1];
+      const float v[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int q = j - k;   // this row is the token's q-th reader: tap 3 - q
+        if (q < 0 || q > 3) continue;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float w = q == 0 ? wv[i].w : q == 1 ? wv[i].z : q == 2 ? wv[i].y : wv[i].x;
+          acc[k][i] = fmaf(w, v[i], acc[k][i]);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float4* out = reinterpret_cast<float4*>(p.dx + (size_t)(x + k) * p.C + ch);
+      out[0] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+      out[1] = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
+    }
+    return;
+  }
 #pragma unroll 1
-  for (int it = 0; it < 4; ++it) {
-    const int tl = it * 16 + lt, x = x0 + tl;
+  for (int k = 0; k < 4; ++k) {
+    const int tl = tb + k, x = x0 + tl;
     if (x >= p.N) continue;
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
     if (p.prev[x] != -2) {
-      const bool simple = s_first[tl] == x + 1 && s_first[tl + 1] == x + 2 && s_first[tl + 2] == x + 3;
-      if (simple) {   // the same sums, in the same order, as the walk below
-        float4 r[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4* d = reinterpret_cast<const float4*>(p.dqkv + (size_t)(x + k) * p.C + ch);
-          r[2 * k] = d[0];
-          r[2 * k + 1] = d[1];
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float v[8] = {r[2 * k].x, r[2 * k].y, r[2 * k].z, r[2 * k].w,
-                              r[2 * k + 1].x, r[2 * k + 1].y, r[2 * k + 1].z, r[2 * k + 1].w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float w = k == 0 ? wv[i].w : k == 1 ? wv[i].z : k == 2 ? wv[i].y : wv[i].x;
-            acc[i] = fmaf(w, v[i], acc[i]);
-          }
-        }
-      } else {
-        add(acc, x, 3);
-        for (int a = p.succ_off[x]; a < p.succ_off[x + 1]; ++a) {
-          const int i1 = p.succ[a];
-          add(acc, i1, 2);
-          for (int b = p.succ_off[i1]; b < p.succ_off[i1 + 1]; ++b) {
-            const int i2 = p.succ[b];
-            add(acc, i2, 1);
-            for (int c = p.succ_off[i2]; c < p.succ_off[i2 + 1]; ++c) add(acc, p.succ[c], 0);
-          }
+      add(acc, x, 3);
+      for (int a = p.succ_off[x]; a < p.succ_off[x + 1]; ++a) {
+        const int i1 = p.succ[a];
+        add(acc, i1, 2);
+        for (int b = p.succ_off[i1]; b < p.succ_off[i1 + 1]; ++b) {
+          const int i2 = p.succ[b];
+          add(acc, i2, 1);
+          for (int c = p.succ_off[i2]; c < p.succ_off[i2 + 1]; ++c) add(acc, p.succ[c], 0);
         }
       }
     }
