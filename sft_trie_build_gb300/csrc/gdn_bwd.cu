@@ -1199,23 +1199,20 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_token_kernel(const __grid_cons
 // (64 tokens, channel group of 128); thread = (4 consecutive tokens, 8
 // channels); pads get 0.
 __global__ void __launch_bounds__(kBT) gdn_bwd_dx_kernel(const GbParams p) {
-  // successor counts and first successors of the block's tokens and the
-  // three after them: inside a segment a token's readers are just the next
-  // three tokens, read directly; elsewhere (segment ends, branch points) the
-  // successor lists are walked
-  __shared__ int s_off[68], s_first[67];
+  // Successor offsets and path predecessors of the block's tokens and the
+  // three after them, loaded together: a token whose only successor is the
+  // next token (one successor, and the next token's predecessor is it)
+  // passes its gradient straight along; inside a segment a token's readers
+  // are just the next three tokens, read directly; elsewhere (segment ends,
+  // branch points) the successor lists are walked.
+  __shared__ int s_off[68], s_prev[68];
   const int grp = blockIdx.y, lt = threadIdx.x >> 4, vec = threadIdx.x & 15;
   const int ch = grp * kD + vec * 8;
   const int x0 = blockIdx.x * 64;
   if (threadIdx.x < 68) {
     const int t = x0 + (int)threadIdx.x;
     s_off[threadIdx.x] = t <= p.N ? p.succ_off[t] : -1;
-  }
-  __syncthreads();
-  if (threadIdx.x < 67) {
-    const int t = x0 + (int)threadIdx.x;
-    s_first[threadIdx.x] =
-        (t < p.N && s_off[threadIdx.x + 1] - s_off[threadIdx.x] == 1) ? p.succ[s_off[threadIdx.x]] : -1;
+    s_prev[threadIdx.x] = t < p.N ? p.prev[t] : -2;
   }
   float4 wv[8];
 #pragma unroll
@@ -1233,12 +1230,13 @@ __global__ void __launch_bounds__(kBT) gdn_bwd_dx_kernel(const GbParams p) {
   };
   // thread = (4 consecutive tokens tb .. tb + 3 of the block, 8 channels)
   const int tb = 4 * lt;
+  // the only successor of block token i is token i + 1
+  auto next_only = [&](int i) { return s_off[i + 1] - s_off[i] == 1 && s_prev[i + 1] == x0 + i; };
   bool plain4 = x0 + tb + 3 < p.N;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int tl = tb + k, x = x0 + tl;
-    plain4 = plain4 && p.prev[x] != -2 && s_first[tl] == x + 1 && s_first[tl + 1] == x + 2 &&
-             s_first[tl + 2] == x + 3;
+    const int tl = tb + k;
+    plain4 = plain4 && s_prev[tl] != -2 && next_only(tl) && next_only(tl + 1) && next_only(tl + 2);
   }
   if (plain4) {
     // Four tokens inside a segment: token k reads rows x + k .. x + k + 3 with
