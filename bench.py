@@ -168,8 +168,8 @@ def _gdn(meta, dev, heads=16, reps=10) -> dict:
     out = {"heads": heads, "head_dim": 128, "tokens": real, "segments": int(plan[stp.GP_NSEG]),
            "chunks": int(plan[stp.GP_NCHUNK]), "depths": int(plan[stp.GP_NDEPTH]), "ms": ms,
            "tokens_per_s": real / (ms / 1e3), "host_plan_ms": plan_ms,
-           # convolution, the preparation (split in two launches when there are deeper segments), a walk per depth
-           "launches_per_call": 1 + (2 if int(plan[stp.GP_NDEPTH]) > 1 else 1) + int(plan[stp.GP_NDEPTH])}
+           # convolution, the preparation (depth 0, depth 1 and the deeper depths apart), a walk per depth
+           "launches_per_call": 1 + min(int(plan[stp.GP_NDEPTH]), 3) + int(plan[stp.GP_NDEPTH])}
     # training: the forward that keeps the chunk states, then the backward
     try:
         tws = torch.empty(stp.stp_gdn_train_workspace_size(desc, plan), dtype=torch.uint8, device=dev)

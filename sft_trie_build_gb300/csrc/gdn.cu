@@ -1026,7 +1026,7 @@ stp_status ws_size(const stp_gdn_desc* desc, const void* plan, size_t* ws_bytes,
 struct GdnStreams {
   bool ready = false;
   cudaStream_t hi = nullptr, aux = nullptr;
-  cudaEvent_t fork = nullptr, join_hi = nullptr, join_aux = nullptr;
+  cudaEvent_t fork = nullptr, join_hi = nullptr, join_aux = nullptr, dep1 = nullptr;
 };
 std::mutex g_gdn_mu;
 GdnStreams g_gdn_streams[64];
@@ -1046,6 +1046,7 @@ cudaError_t gdn_streams(GdnStreams** out) {
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g.fork, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g.join_hi, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g.join_aux, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&g.dep1, cudaEventDisableTiming);
     if (e != cudaSuccess) return e;
     g.ready = true;
   }
@@ -1139,13 +1140,15 @@ stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d
     const int S = std::max(1, std::min(nbx, kConvPerSm * n_sm / G));
     gdn_conv_kernel<<<(unsigned)(G * S), kConvThreads, kConvSmem, s>>>(mx, p, S);
   }
-  // The chunks of depth 0 are prepared and walked on a high-priority stream
-  // (the walk is one CTA per head and root segment: a few SMs), while the
-  // other depths' chunks are prepared on a second stream; the deeper walks
-  // wait for both.  Chunks are numbered depth by depth.
+  // The chunks of depth 0 are prepared and every depth is walked on a
+  // high-priority stream (a walk is one CTA per head and segment: a few SMs),
+  // while a second stream prepares the depth-1 chunks, then the deeper ones;
+  // the depth-1 walk waits for the first of those, the deeper walks for
+  // both.  Chunks are numbered depth by depth.
   const int32_t* depth_off = w + w[GP_DEPTH_OFF];
   const int32_t* seg_chunk0 = w + w[GP_SEG_CHUNK0];
   const int c1 = n_depth > 1 ? seg_chunk0[depth_off[1]] : n_chunk;   // first chunk below depth 0
+  const int c2 = n_depth > 2 ? seg_chunk0[depth_off[2]] : n_chunk;   // first chunk below depth 1
   auto walk = [&](int d, cudaStream_t st) {
     const int n = depth_off[d + 1] - depth_off[d];
     if (n <= 0) return;
@@ -1165,14 +1168,26 @@ stp_status gdn_forward(const stp_gdn_desc* desc, const void* plan, const void* d
       walk(0, gs->hi);
       GdnParams q = p;
       q.chunk0 = c1;
-      gdn_prep_kernel<<<(unsigned)((n_chunk - c1) * H), kPrepThreads, kPrepSmem, gs->aux>>>(q);
-      e = cudaEventRecord(gs->join_hi, gs->hi);
+      gdn_prep_kernel<<<(unsigned)((c2 - c1) * H), kPrepThreads, kPrepSmem, gs->aux>>>(q);
+      e = cudaEventRecord(gs->dep1, gs->aux);
+    }
+    if (e == cudaSuccess && c2 < n_chunk) {
+      GdnParams q = p;
+      q.chunk0 = c2;
+      gdn_prep_kernel<<<(unsigned)((n_chunk - c2) * H), kPrepThreads, kPrepSmem, gs->aux>>>(q);
     }
     if (e == cudaSuccess) e = cudaEventRecord(gs->join_aux, gs->aux);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(gs->hi, gs->dep1, 0);
+    if (e == cudaSuccess) {
+      walk(1, gs->hi);
+      e = cudaStreamWaitEvent(gs->hi, gs->join_aux, 0);
+    }
+    if (e == cudaSuccess) {
+      for (int d = 2; d < n_depth; ++d) walk(d, gs->hi);
+      e = cudaEventRecord(gs->join_hi, gs->hi);
+    }
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, gs->join_hi, 0);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, gs->join_aux, 0);
     if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_fwd: %s", cudaGetErrorString(e));
-    for (int d = 1; d < n_depth; ++d) walk(d, s);
   } else {
     if (n_chunk > 0) gdn_prep_kernel<<<(unsigned)(n_chunk * H), kPrepThreads, kPrepSmem, s>>>(p);
     for (int d = 0; d < n_depth; ++d) walk(d, s);

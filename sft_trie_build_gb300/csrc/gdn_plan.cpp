@@ -8,8 +8,12 @@
 // segment is a maximal run x, x + 1, ... in which every token continues the
 // previous one and the previous one has no other child; a branch point
 // therefore always ends its segment, and every segment starts from the final
-// state of its parent segment.  Segments are sorted by depth (stable) and cut
-// into chunks of kGdnChunk tokens, the last one ragged.
+// state of its parent segment.  A root segment of at least kGdnSplitChunks
+// chunks is cut after its first kGdnHeadChunks chunks into two segments, the
+// second the only child of the first (chunk for chunk the same work; the
+// forward then walks the first while it prepares the rest).  Segments are
+// sorted by depth (stable) and cut into chunks of kGdnChunk tokens, the last
+// one ragged.
 #include <cstring>
 #include <vector>
 
@@ -78,12 +82,24 @@ extern "C" stp_status stp_gdn_plan(const stp_gdn_desc* desc, const int32_t* subt
     }
   }
 
+  // x continues the run of x - 1 (same row, x - 1's only child)
+  auto continues = [&](int64_t x) { return prev[x] == x - 1 && x % T != 0 && n_child[x - 1] == 1; };
+  // where long root runs are cut: kGdnHeadChunks chunks after their first token
+  std::vector<char> cut(N, 0);
+  for (int64_t x = 0; x < N; ++x) {
+    if (prev[x] != -1) continue;
+    int64_t y = x + 1;
+    while (y < N && continues(y)) ++y;
+    if (y - x >= (int64_t)kGdnSplitChunks * kGdnChunk) cut[x + (int64_t)kGdnHeadChunks * kGdnChunk] = 1;
+    x = y - 1;
+  }
+
   // segments in token (DFS) order: parents come before their children
   std::vector<int64_t> s_start;
   std::vector<int32_t> s_len, s_parent, s_depth, seg_of(N, -1);
   for (int64_t x = 0; x < N; ++x) {
     if (prev[x] == -2) continue;
-    const bool cont = prev[x] == x - 1 && x % T != 0 && n_child[x - 1] == 1;
+    const bool cont = continues(x) && !cut[x];
     if (!cont) {
       const int32_t par = prev[x] >= 0 ? seg_of[prev[x]] : -1;
       s_start.push_back(x);

@@ -73,6 +73,13 @@ constexpr size_t kDsTileBytes = 128 * 128 * 2;  // one bf16 dS^T tile
 // Gated DeltaNet: tokens per chunk of the chunked recurrence, and the layout
 // of the host plan (int32 words; a header of kGdnHeader words, then arrays).
 constexpr int kGdnChunk = 64;
+// A root segment of at least kGdnSplitChunks chunks is planned as two: its
+// first kGdnHeadChunks chunks (depth 0), then the rest as their only child,
+// so that the first walk starts after a short preparation and the rest is
+// prepared beside it.  The cut falls on a chunk boundary: every chunk, and
+// so every result, is the same as without it.
+constexpr int kGdnHeadChunks = 16;
+constexpr int kGdnSplitChunks = 32;
 constexpr int kGdnHeader = 24;
 constexpr int32_t kGdnMagic = 0x31444e47;  // "GDN1"
 enum GdnPlanField {

@@ -1,8 +1,10 @@
 """Host planner of the tree-aware Gated DeltaNet (stp_gdn_plan) against the
 oracle's paths: the path predecessor of every token equals the one read off
 the packer's parent pointers; segments are consecutive runs that break at
-every branch point and start from their parent's last token; depths are
-ordered; chunks of at most 64 tokens tile every segment exactly once."""
+every branch point and start from their parent's last token (and a root run
+of at least 32 chunks is cut once, after its first 16, into two segments);
+depths are ordered; chunks of at most 64 tokens tile every segment exactly
+once, on the same boundaries as without the cut."""
 import numpy as np
 import pytest
 
@@ -41,6 +43,9 @@ def _check(plan_o, H=2):
             ps, pl = a["seg_start"][par], a["seg_len"][par]
             assert prev[s] == ps + pl - 1, "a segment must start from its parent's last token"
             assert d_of[par] == d_of[i] - 1
+            if prev[s] == s - 1 and n_child[s - 1] == 1 and s % T != 0:
+                # no branch point here: the cut of a long root run after 16 chunks
+                assert a["seg_parent"][par] < 0 and pl == 16 * 64 and L + pl >= 32 * 64
         else:
             assert prev[s] == -1 and d_of[i] == 0
         for x in range(s + 1, s + L):
@@ -126,3 +131,24 @@ def test_edge_shapes():
     a = stp.gdn_plan_arrays(plan)
     assert np.array_equal(a["prev"], np.arange(200) - 1)
     assert list(a["seg_len"]) == [200] and list(a["chunk_len"]) == [64, 64, 64, 8]
+
+
+@pytest.mark.parametrize("n", [2047, 2048, 3000])
+def test_long_root_run_is_cut_once(n):
+    """A root run of at least 32 chunks becomes two segments: its first 16
+    chunks at depth 0, the rest their only child at depth 1; the chunks are
+    the same as without the cut."""
+    T = 4096
+    chain = np.full((1, T), n - 1, np.int32)
+    chain[0, n:] = np.arange(n, T)
+    plan = stp.stp_gdn_plan(stp.gdn_desc(1, T, 1), chain, np.array([n], np.int32))
+    a = stp.gdn_plan_arrays(plan)
+    if n < 2048:
+        assert list(a["seg_len"]) == [n] and list(a["seg_parent"]) == [-1]
+        assert list(a["depth_off"]) == [0, 1]
+    else:
+        assert list(a["seg_start"]) == [0, 1024] and list(a["seg_len"]) == [1024, n - 1024]
+        assert list(a["seg_parent"]) == [-1, 0] and list(a["depth_off"]) == [0, 1, 2]
+        assert list(a["child"][a["child_off"][0]: a["child_off"][1]]) == [1]
+    k = np.arange((n + 63) // 64)
+    assert np.array_equal(a["chunk_start"], 64 * k) and np.array_equal(a["chunk_len"], np.minimum(64, n - 64 * k))

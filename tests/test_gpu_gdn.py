@@ -75,6 +75,15 @@ def test_long_chain_many_chunks():
     _compare(po, H=2, seed=5)
 
 
+def test_long_chain_cut_into_two_segments():
+    """A 2200-token chain: the planner cuts it after 16 chunks (1024 + 1176
+    tokens, the second segment the first's only child), so the state crosses
+    one segment boundary through memory; every element against the oracle."""
+    rng = np.random.default_rng(6)
+    seq = rng.integers(1, 1000, 2200).astype(np.int32)
+    _compare(OP.pack([seq], [np.zeros(2200, np.uint8)], 2304, 64), H=1, seed=6)
+
+
 def test_tiny_workload():
     b = W.tiny(0)
     _compare(OP.pack(b.seqs, b.trainable, b.row_len, b.min_shared), H=3, seed=2)
