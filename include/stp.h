@@ -457,7 +457,10 @@ stp_status stp_gdn_plan_bound(const stp_gdn_desc* desc, size_t* plan_bytes);
  * o = 0), writes the plan into `plan` (host, >= stp_gdn_plan_bound bytes):
  * the path predecessor of every token and its successors (the tokens whose
  * predecessor it is), the segments sorted by depth with their parents, and
- * the 64-token chunks.  Its word 5 is the number of int32
+ * the 64-token chunks.  Segments end at branch points; a root run of at least
+ * 32 chunks is also cut once, after its first 16 chunks (the rest is its only
+ * child), which changes no chunk and no result, only how the forward overlaps
+ * the preparation of later chunks with the walk.  Its word 5 is the number of int32
  * words used; copy at least that much to the device for stp_gdn_fwd.
  * Errors: STP_EINVAL (NULL, short buffer, subtree_end outside [x, T) or not
  * nested, row_used outside [0, T]).
