@@ -51,7 +51,7 @@ constexpr int kD = kGdnD, kC = kGdnChunk;
 constexpr int kBT = 256;   // threads of every backward kernel
 
 struct GbParams {
-  int N, H, C, seg0;
+  int N, H, C, seg0, chunk0;   // seg0, chunk0: first segment / chunk of a launch
   float scale;
   const int32_t* prev;
   const int32_t* prev2;
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kWkThreads, 1)
     const int u = ((warp >> 2) * 2 + (warp & 1)) * 32 + lane;
     if (nck > 0 && !e2_warp) load_do(0, u);
     for (int n = 0; ok && n < nck; ++n) {
-      const int c = c0 + nck - 1 - n, L = p.chunk_len[c], x0 = p.chunk_start[c];
+      const int c = c0 + nck - 1 - n;
       const size_t row = (size_t)c * p.H + h;
       const float dec = p.decay[row];
       if (n > 0) {
@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) gdn_bwd_chunk_kernel(const GbPa
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + K_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ch = (int)(blockIdx.x / p.H), h = (int)(blockIdx.x % p.H);
+  const int ch = p.chunk0 + (int)(blockIdx.x / p.H), h = (int)(blockIdx.x % p.H);
   const int x0 = p.chunk_start[ch], L = p.chunk_len[ch];
   const size_t row = (size_t)ch * p.H + h;
   const int Hd = p.H * kD;
@@ -1306,6 +1306,37 @@ __global__ void __launch_bounds__(kBT) gdn_bwd_dw_kernel(const GbParams p, int n
   p.dconv_w[e] = a;
 }
 
+// A high-priority stream for the reverse walks and a second one for the chunk
+// pass of the deeper chunks, with their events; one set per device.
+struct GbStreams {
+  bool ready = false;
+  cudaStream_t hi = nullptr, aux = nullptr;
+  cudaEvent_t fork = nullptr, deep = nullptr, join_hi = nullptr, join_aux = nullptr;
+};
+std::mutex g_gb_mu;
+GbStreams g_gb_streams[64];
+
+cudaError_t gb_streams(GbStreams** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_gb_mu);
+  GbStreams& g = g_gb_streams[dev];
+  if (!g.ready) {
+    int least = 0, greatest = 0;
+    e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&g.hi, cudaStreamNonBlocking, greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&g.aux, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&g.fork, &g.deep, &g.join_hi, &g.join_aux})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+    g.ready = true;
+  }
+  *out = &g;
+  return cudaSuccess;
+}
+
 }  // namespace
 }  // namespace stp
 
@@ -1341,6 +1372,7 @@ extern "C" stp_status stp_gdn_bwd(const stp_gdn_desc* desc, const void* plan, co
   p.H = H;
   p.C = C;
   p.seg0 = 0;
+  p.chunk0 = 0;
   p.scale = desc->scale;
   p.prev = dp + w[GP_PREV];
   p.prev2 = dp + w[GP_PREV2];
@@ -1398,13 +1430,53 @@ extern "C" stp_status stp_gdn_bwd(const stp_gdn_desc* desc, const void* plan, co
   e = cudaMemsetAsync(p.dqkv, 0, (size_t)N * C * 4, s);
   if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_bwd: %s", cudaGetErrorString(e));
   const int32_t* depth_off = w + w[GP_DEPTH_OFF];
-  for (int d = n_depth - 1; d >= 0; --d) {
+  const int32_t* seg_chunk0 = w + w[GP_SEG_CHUNK0];
+  auto walk = [&](int d, cudaStream_t st) {
     const int n = depth_off[d + 1] - depth_off[d];
-    if (n <= 0) continue;
-    p.seg0 = depth_off[d];
-    gdn_bwd_walk_kernel<<<(unsigned)(n * H), kWkThreads, kWkSmem, s>>>(mwq, mkt, mpm, p);
+    if (n <= 0) return;
+    GbParams q = p;
+    q.seg0 = depth_off[d];
+    gdn_bwd_walk_kernel<<<(unsigned)(n * H), kWkThreads, kWkSmem, st>>>(mwq, mkt, mpm, q);
+  };
+  auto chunks = [&](int c_begin, int c_end, cudaStream_t st) {   // the chunk pass over chunks [c_begin, c_end)
+    if (c_end <= c_begin) return;
+    GbParams q = p;
+    q.chunk0 = c_begin;
+    gdn_bwd_chunk_kernel<<<(unsigned)((c_end - c_begin) * H), kCkThreads, kCkSmem, st>>>(q);
+  };
+  // Chunks are numbered depth by depth.  With three depths or more, the chunk
+  // pass over the chunks of depth 2 and below starts on a second stream once
+  // their walks are done, beside the walks of depths 1 and 0 (one CTA per
+  // head and segment: a few SMs), which run on a high-priority stream.
+  const int c2 = n_depth > 2 ? seg_chunk0[depth_off[2]] : n_chunk;   // first chunk below depth 1
+  if (c2 < n_chunk) {
+    GbStreams* gs = nullptr;
+    if ((e = gb_streams(&gs)) != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_bwd: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lock(g_gb_mu);
+    e = cudaEventRecord(gs->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(gs->hi, gs->fork, 0);
+    if (e == cudaSuccess) {
+      for (int d = n_depth - 1; d >= 2; --d) walk(d, gs->hi);
+      e = cudaEventRecord(gs->deep, gs->hi);
+    }
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(gs->aux, gs->deep, 0);
+    if (e == cudaSuccess) {
+      chunks(c2, n_chunk, gs->aux);
+      e = cudaEventRecord(gs->join_aux, gs->aux);
+    }
+    if (e == cudaSuccess) {
+      walk(1, gs->hi);
+      walk(0, gs->hi);
+      chunks(0, c2, gs->hi);
+      e = cudaEventRecord(gs->join_hi, gs->hi);
+    }
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, gs->join_hi, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, gs->join_aux, 0);
+    if (e != cudaSuccess) return fail(STP_ECUDA, "stp_gdn_bwd: %s", cudaGetErrorString(e));
+  } else {
+    for (int d = n_depth - 1; d >= 0; --d) walk(d, s);
+    chunks(0, n_chunk, s);
   }
-  if (n_chunk > 0) gdn_bwd_chunk_kernel<<<(unsigned)(n_chunk * H), kCkThreads, kCkSmem, s>>>(p);
   const unsigned n_blocks = (unsigned)((N + 63) / 64);
   {
     // a CTA per (channel group, one of S token-block strides)
